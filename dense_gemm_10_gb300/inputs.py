@@ -1,0 +1,174 @@
+"""Seeded synthetic GEMM inputs, shared by the tests, the smoke check and the benchmark.
+
+This module only draws random numbers and lays them out; it holds none of the
+GEMM's arithmetic.  Both the oracle side and the GPU side receive exactly the
+tensors built here.
+
+Recipe (one rule for every workload):
+  * a workload has one integer seed s; A is drawn from seed s, B from s + 1,
+    the initial C from s + 2 (numpy PCG64 streams);
+  * samples are drawn in float32 (uniform or normal), then rounded once to the
+    input type with round-to-nearest-even (torch ``.to(bfloat16/float16)``);
+  * a matrix is drawn directly in its stored shape (row-major storage, see
+    ``Problem``), so the "op" flags change the layout, not the distribution;
+  * padding columns beyond a leading dimension hold a NaN bit pattern, so a
+    kernel that reads past the logical width shows up as NaN in its output.
+"""
+from dataclasses import dataclass, field
+import math
+
+import numpy as np
+import torch
+
+_TORCH_DT = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+_NAN_BITS = {"bf16": 0x7FC1, "f16": 0x7E01}
+
+
+def _rng(seed):
+    return np.random.Generator(np.random.PCG64(int(seed)))
+
+
+def draw(shape, dist, seed, dtype):
+    """Draw a CPU tensor of ``dtype`` ("bf16", "f16", "f32") in ``shape``.
+
+    dist: ("uniform", lo, hi) | ("normal", mean, std) | ("ints", lo, hi)
+    (integers uniform in [lo, hi], inclusive) | ("zeros",).
+    """
+    g = _rng(seed)
+    kind = dist[0]
+    if kind == "uniform":
+        x = g.random(size=shape, dtype=np.float32) * np.float32(dist[2] - dist[1]) + np.float32(dist[1])
+    elif kind == "normal":
+        x = g.standard_normal(size=shape, dtype=np.float32) * np.float32(dist[2]) + np.float32(dist[1])
+    elif kind == "ints":
+        x = g.integers(dist[1], dist[2] + 1, size=shape).astype(np.float32)
+    elif kind == "zeros":
+        x = np.zeros(shape, dtype=np.float32)
+    else:
+        raise ValueError("unknown distribution %r" % (dist,))
+    return torch.from_numpy(np.ascontiguousarray(x)).to(_TORCH_DT[dtype])
+
+
+def _pad_columns(t, ld, dtype):
+    """Return a (rows, ld) tensor holding ``t`` in its first columns and NaN bits after."""
+    rows, cols = t.shape
+    if ld == cols:
+        return t.contiguous()
+    out = torch.empty((rows, ld), dtype=t.dtype)
+    if dtype in _NAN_BITS:
+        out.view(torch.int16).fill_(_NAN_BITS[dtype])
+    else:
+        out.fill_(float("nan"))
+    out[:, :cols] = t
+    return out
+
+
+@dataclass
+class Problem:
+    """One GEMM instance: C = alpha * op(A) * op(B) + beta * C0 (row-major storage).
+
+    transA 0: A stored M x K (lda >= K); 1: A stored K x M (lda >= M).
+    transB 0: B stored K x N (ldb >= N); 1: B stored N x K (ldb >= K).
+    C0 is M x N with ldc >= N, in the output type; None when beta == 0.
+    """
+    name: str
+    M: int
+    N: int
+    K: int
+    transA: int
+    transB: int
+    in_dtype: str
+    out_dtype: str
+    alpha: float
+    beta: float
+    A: torch.Tensor
+    lda: int
+    B: torch.Tensor
+    ldb: int
+    C0: object
+    ldc: int
+    seed: int
+    recipe: dict = field(default_factory=dict)
+
+    @property
+    def layout(self):
+        return ("T" if self.transA else "N") + ("T" if self.transB else "N")
+
+
+def make_problem(name, M, N, K, transA=0, transB=0, in_dtype="bf16", out_dtype="f32",
+                 dist_a=("uniform", -1.0, 1.0), dist_b=("uniform", -1.0, 1.0), alpha=1.0,
+                 beta=0.0, dist_c=("normal", 0.0, 1.0), seed=0, lda=None, ldb=None, ldc=None):
+    a_shape = (K, M) if transA else (M, K)
+    b_shape = (N, K) if transB else (K, N)
+    lda = a_shape[1] if lda is None else lda
+    ldb = b_shape[1] if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    if lda < a_shape[1] or ldb < b_shape[1] or ldc < N:
+        raise ValueError("leading dimension smaller than the stored width")
+    A = _pad_columns(draw(a_shape, dist_a, seed, in_dtype), lda, in_dtype)
+    B = _pad_columns(draw(b_shape, dist_b, seed + 1, in_dtype), ldb, in_dtype)
+    C0 = None
+    if beta != 0.0:
+        C0 = _pad_columns(draw((M, N), dist_c, seed + 2, out_dtype), ldc, out_dtype)
+    recipe = {"dist_a": list(dist_a), "dist_b": list(dist_b), "dist_c": list(dist_c) if beta else None,
+              "seeds": [seed, seed + 1, seed + 2]}
+    return Problem(name, M, N, K, transA, transB, in_dtype, out_dtype, float(alpha), float(beta),
+                   A, lda, B, ldb, C0, ldc, seed, recipe)
+
+
+# ---------------------------------------------------------------------------
+# The workloads, named by what they are.
+# ---------------------------------------------------------------------------
+
+def tiny_256():
+    """M = N = K = 256, A and B row-major, bf16 U[-1, 1], alpha 1, beta 0, fp32 C."""
+    return make_problem("tiny_256_bf16_nn", 256, 256, 256, 0, 0, "bf16", "f32")
+
+
+def square_4096_bf16_nt(out_dtype="f32", size=4096):
+    """M = N = K = 4096, A row-major, B column-major (NT), bf16 N(0, 1)/sqrt(K)."""
+    std = 1.0 / math.sqrt(size)
+    return make_problem("square_%d_bf16_nt_%s" % (size, out_dtype), size, size, size, 0, 1, "bf16",
+                        out_dtype, ("normal", 0.0, std), ("normal", 0.0, std))
+
+
+def square_4096_f16_blend(transA, transB, size=4096):
+    """M = N = K = 4096, fp16 U[-1, 1], alpha 1.5, beta 0.5, fp32 C0 ~ N(0, 1)."""
+    lay = ("T" if transA else "N") + ("T" if transB else "N")
+    return make_problem("square_%d_f16_blend_%s" % (size, lay.lower()), size, size, size, transA,
+                        transB, "f16", "f32", alpha=1.5, beta=0.5, dist_c=("normal", 0.0, 1.0))
+
+
+LLM_SHAPES = {
+    # name: (M, K, N) -- M is batch x sequence
+    "qkv_proj": (8192, 4096, 12288),
+    "ffn_up": (8192, 4096, 16384),
+    "ffn_down": (8192, 16384, 4096),
+}
+
+
+def llm_projection(name, transB=0):
+    """LLM projection: activations N(0, 1), weights N(0, 0.02), bf16, beta 0, fp32 C."""
+    M, K, N = LLM_SHAPES[name]
+    return make_problem("%s_%s" % (name, "nt" if transB else "nn"), M, N, K, 0, transB, "bf16", "f32",
+                        ("normal", 0.0, 1.0), ("normal", 0.0, 0.02))
+
+
+def ragged_4095_4097_1000():
+    """Ragged tile edges: M = 4095, N = 4097, K = 1000, NN, bf16 as the LLM shapes."""
+    return make_problem("ragged_4095x4097x1000_nn", 4095, 4097, 1000, 0, 0, "bf16", "f32",
+                        ("normal", 0.0, 1.0), ("normal", 0.0, 0.02))
+
+
+def lm_head_64():
+    """Skinny LM head: M = 64 (decode batch), K = 4096, N = 32000 (vocabulary).
+
+    Weights are stored vocabulary-major (N x K), i.e. the NT layout.
+    """
+    return make_problem("lm_head_64x32000x4096_nt", 64, 32000, 4096, 0, 1, "bf16", "f32",
+                        ("normal", 0.0, 1.0), ("normal", 0.0, 0.02))
+
+
+def bits(t):
+    """Raw 16-bit patterns of a bf16 / fp16 tensor as a numpy uint16 array (no copy of values)."""
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)

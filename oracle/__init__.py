@@ -1,0 +1,147 @@
+"""CPU oracle for C = alpha * op(A) * op(B) + beta * C0 -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The GPU library never calls it and the
+two share no code: the oracle is a plain fp64 triple loop in ``gemm_oracle.c``
+(the definition of "CUDA GEMM 矩阵乘法优化指南", section 2.1, checked in double
+precision as the page at m.lqnn.cn/news/285670 does in its section 1.2).
+
+Inputs are the raw 16-bit patterns (numpy ``uint16``) of the bf16 / fp16
+matrices, in the row-major storage convention described in ``gemm_oracle.c``.
+Every function here is pinned by ``tests/test_oracle.py``.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gemm_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle_gemm.so")
+
+IN_BF16, IN_F16 = 0, 1
+C_F32, C_BF16, C_F16 = 0, 1, 2
+
+_lib = None
+
+
+def build(force=False):
+    """Compile the oracle with gcc (plain C, fp-contraction off so that the
+    same source gives the same roundings on x86-64 and aarch64)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + ".tmp%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", _SRC, "-o", tmp,
+           "-lpthread", "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    # ORACLE_LIB points the pins at another build of the oracle source; the
+    # mutation test uses it to show that a planted mistake fails the pins.
+    path = os.environ.get("ORACLE_LIB") or build()
+    lib = ctypes.CDLL(path)
+    i64, dbl, vp, i32 = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
+    lib.oracle_gemm.restype = i32
+    lib.oracle_gemm.argtypes = [i32, i32, i64, i64, i64, dbl, vp, i64, vp, i64, dbl, vp, i32, i64,
+                                i32, vp, vp, i64, i32]
+    lib.oracle_gemm_at.restype = i32
+    lib.oracle_gemm_at.argtypes = [i32, i32, i64, i64, i64, dbl, vp, i64, vp, i64, dbl, vp, i32,
+                                   i64, i32, i64, vp, vp, vp, vp, i32]
+    lib.oracle_bf16_value.restype = dbl
+    lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
+    lib.oracle_f16_value.restype = dbl
+    lib.oracle_f16_value.argtypes = [ctypes.c_uint16]
+    _lib = lib
+    return lib
+
+
+def bf16_value(bits):
+    """Value of one bfloat16 bit pattern, decoded from the format definition."""
+    return _load().oracle_bf16_value(int(bits) & 0xFFFF)
+
+
+def f16_value(bits):
+    """Value of one IEEE binary16 bit pattern, decoded from the format definition."""
+    return _load().oracle_f16_value(int(bits) & 0xFFFF)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _c0_array(C0, c_type):
+    if C0 is None:
+        return None
+    want = np.float32 if c_type == C_F32 else np.uint16
+    C0 = np.ascontiguousarray(C0)
+    if C0.dtype != want:
+        raise TypeError("C0 must be %s for c_type %d" % (want.__name__, c_type))
+    return C0
+
+
+def gemm(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc, in_type, c_type=C_F32,
+         nthreads=0):
+    """Full oracle.  Returns (R, Mag): fp64 M x N arrays of r_ij and m_ij.
+
+    A, B: uint16 arrays holding the stored matrices (row-major, leading
+    dimensions lda / ldb).  C0: float32 (c_type C_F32) or uint16 bits, M x N
+    with leading dimension ldc; ignored when beta == 0.
+    """
+    lib = _load()
+    A = np.ascontiguousarray(A, dtype=np.uint16)
+    B = np.ascontiguousarray(B, dtype=np.uint16)
+    C0 = _c0_array(C0, c_type) if beta != 0.0 else None
+    R = np.zeros((M, N), dtype=np.float64)
+    Mag = np.zeros((M, N), dtype=np.float64)
+    rc = lib.oracle_gemm(int(transA), int(transB), M, N, K, float(alpha), _ptr(A), lda, _ptr(B),
+                         ldb, float(beta), _ptr(C0), int(c_type), ldc, int(in_type), _ptr(R),
+                         _ptr(Mag), N, int(nthreads))
+    if rc < 0:
+        raise ValueError("oracle_gemm rejected its arguments")
+    return R, Mag
+
+
+def gemm_at(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc, in_type, rows, cols,
+            c_type=C_F32, nthreads=0):
+    """Sampled oracle: r and m at the listed (rows[e], cols[e]) entries."""
+    lib = _load()
+    A = np.ascontiguousarray(A, dtype=np.uint16)
+    B = np.ascontiguousarray(B, dtype=np.uint16)
+    C0 = _c0_array(C0, c_type) if beta != 0.0 else None
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    if rows.shape != cols.shape:
+        raise ValueError("rows and cols differ in length")
+    r = np.zeros(rows.shape, dtype=np.float64)
+    m = np.zeros(rows.shape, dtype=np.float64)
+    rc = lib.oracle_gemm_at(int(transA), int(transB), M, N, K, float(alpha), _ptr(A), lda, _ptr(B),
+                            ldb, float(beta), _ptr(C0), int(c_type), ldc, int(in_type),
+                            rows.size, _ptr(rows), _ptr(cols), _ptr(r), _ptr(m), int(nthreads))
+    if rc < 0:
+        raise ValueError("oracle_gemm_at rejected its arguments")
+    return r, m
+
+
+def within_tolerance(out, r, m, out_is_f32):
+    """Elementwise comparison rule for a GPU result ``out`` against (r, m).
+
+    fp32 output:       |out - r| <= 1e-3 * m + 1e-5
+    bf16 / fp16 output: |out - r| <= 8e-3 * |r| + 1e-3 * m + 1e-5
+    A NaN or Inf in ``out`` where r is finite fails.
+    Returns a boolean array (True = within tolerance).
+    """
+    out = np.asarray(out, dtype=np.float64)
+    err = np.abs(out - r)
+    bound = 1e-3 * m + 1e-5
+    if not out_is_f32:
+        bound = bound + 8e-3 * np.abs(r)
+    ok = err <= bound
+    ok &= np.isfinite(out) | ~np.isfinite(r)
+    return ok

@@ -1,0 +1,232 @@
+/*
+ * gemm_oracle.c -- CPU oracle for the dense GEMM  C = alpha * op(A) * op(B) + beta * C0.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  The GPU library never
+ * links, loads or calls it, and it shares no code, header or table with the
+ * GPU library.
+ *
+ * What it computes (the plain definition, written out):
+ *   "CUDA GEMM 矩阵乘法优化指南", section 2.1 (GEMM): C = alpha*A*B + beta*C with
+ *   A of size M x K, B of size K x N, C of size M x N; every output element
+ *   takes K multiply-adds (2K floating-point operations).
+ *   The page in m.lqnn.cn/news/285670, section 1.2, checks GPU results against
+ *   a double-precision CPU product; this oracle does the same, in fp64, over
+ *   the exact values of the bf16 / fp16 inputs the GPU receives.
+ *
+ *   For every (i, j):
+ *     s_ij = sum_{k = 0 .. K-1} a(i, k) * b(k, j)        (fp64, k ascending)
+ *     r_ij = alpha * s_ij + beta * c0_ij                  (c0 not read if beta == 0)
+ *     m_ij = |alpha| * sum_k |a(i, k) * b(k, j)| + |beta| * |c0_ij|
+ *   m_ij is the magnitude the comparison tolerance scales with.
+ *
+ * Storage convention (row-major, as C and PyTorch store matrices):
+ *   transA == 0: A is stored M x K, a(i, k) = A[i * lda + k]
+ *   transA == 1: A is stored K x M, a(i, k) = A[k * lda + i]
+ *   transB == 0: B is stored K x N, b(k, j) = B[k * ldb + j]
+ *   transB == 1: B is stored N x K, b(k, j) = B[j * ldb + k]
+ *   C0 / R / Mag are M x N row-major with leading dimensions ldc / ldr.
+ *
+ * The 16-bit inputs are decoded from their format definitions (IEEE 754
+ * binary16; bfloat16 = sign, 8-bit exponent with bias 127, 7-bit fraction).
+ * Every bf16/fp16 value is exactly representable in fp64, and so is every
+ * product of two of them (at most 22 significant bits), so the only rounding
+ * in s_ij is that of the fp64 additions.
+ *
+ * Rows of C are split over POSIX threads; the loop body is the definition.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <unistd.h>
+
+enum { ORACLE_IN_BF16 = 0, ORACLE_IN_F16 = 1 };
+enum { ORACLE_C_F32 = 0, ORACLE_C_BF16 = 1, ORACLE_C_F16 = 2 };
+
+/* bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits. */
+double oracle_bf16_value(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 7) & 0xFF;
+  int f = h & 0x7F;
+  double v;
+  if (e == 0xFF) {
+    v = (f == 0) ? INFINITY : NAN;
+  } else if (e == 0) {
+    v = ldexp((double)f / 128.0, -126); /* subnormal: 0.f * 2^(1-127) */
+  } else {
+    v = ldexp(1.0 + (double)f / 128.0, e - 127);
+  }
+  return sign ? -v : v;
+}
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double oracle_f16_value(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 10) & 0x1F;
+  int f = h & 0x3FF;
+  double v;
+  if (e == 0x1F) {
+    v = (f == 0) ? INFINITY : NAN;
+  } else if (e == 0) {
+    v = ldexp((double)f / 1024.0, -14); /* subnormal: 0.f * 2^(1-15) */
+  } else {
+    v = ldexp(1.0 + (double)f / 1024.0, e - 15);
+  }
+  return sign ? -v : v;
+}
+
+static double in_value(int in_type, uint16_t h) {
+  return in_type == ORACLE_IN_F16 ? oracle_f16_value(h) : oracle_bf16_value(h);
+}
+
+static double c0_value(int c_type, const void* C0, int64_t idx) {
+  if (c_type == ORACLE_C_F32) return (double)((const float*)C0)[idx];
+  if (c_type == ORACLE_C_BF16) return oracle_bf16_value(((const uint16_t*)C0)[idx]);
+  return oracle_f16_value(((const uint16_t*)C0)[idx]);
+}
+
+typedef struct {
+  int transA, transB, in_type, c_type;
+  int64_t M, N, K, lda, ldb, ldc, ldr;
+  double alpha, beta;
+  const uint16_t* A;
+  const uint16_t* B;
+  const void* C0;
+  /* full mode: rows [row0, row1) of R / Mag */
+  double* R;
+  double* Mag;
+  int64_t row0, row1;
+  /* sampled mode: entries [e0, e1) of (rows, cols) */
+  const int64_t* rows;
+  const int64_t* cols;
+  int64_t e0, e1;
+} job_t;
+
+/* One output element, straight from the definition. */
+static void element(const job_t* J, int64_t i, int64_t j, double* r, double* m) {
+  double s = 0.0, sa = 0.0;
+  for (int64_t k = 0; k < J->K; ++k) {
+    uint16_t ha = J->transA ? J->A[k * J->lda + i] : J->A[i * J->lda + k];
+    uint16_t hb = J->transB ? J->B[j * J->ldb + k] : J->B[k * J->ldb + j];
+    double p = in_value(J->in_type, ha) * in_value(J->in_type, hb);
+    s += p;
+    sa += fabs(p);
+  }
+  double rv = J->alpha * s;
+  double mv = fabs(J->alpha) * sa;
+  if (J->beta != 0.0) {
+    double c0 = c0_value(J->c_type, J->C0, i * J->ldc + j);
+    rv += J->beta * c0;
+    mv += fabs(J->beta) * fabs(c0);
+  }
+  *r = rv;
+  *m = mv;
+}
+
+static void* run_rows(void* arg) {
+  const job_t* J = (const job_t*)arg;
+  for (int64_t i = J->row0; i < J->row1; ++i)
+    for (int64_t j = 0; j < J->N; ++j)
+      element(J, i, j, &J->R[i * J->ldr + j], &J->Mag[i * J->ldr + j]);
+  return NULL;
+}
+
+static void* run_entries(void* arg) {
+  const job_t* J = (const job_t*)arg;
+  for (int64_t e = J->e0; e < J->e1; ++e) element(J, J->rows[e], J->cols[e], &J->R[e], &J->Mag[e]);
+  return NULL;
+}
+
+static int pick_threads(int nthreads, int64_t work_items) {
+  if (nthreads <= 0) {
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    nthreads = n > 0 ? (int)n : 1;
+  }
+  if (nthreads > 256) nthreads = 256;
+  if (work_items < nthreads) nthreads = work_items > 0 ? (int)work_items : 1;
+  return nthreads;
+}
+
+static int run_jobs(job_t* jobs, int nthreads, void* (*fn)(void*)) {
+  pthread_t tid[256];
+  int started = 0;
+  for (int t = 0; t < nthreads; ++t) {
+    if (pthread_create(&tid[t], NULL, fn, &jobs[t]) != 0) break;
+    ++started;
+  }
+  for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
+  /* any job whose thread could not be started runs on the caller */
+  for (int t = started; t < nthreads; ++t) fn(&jobs[t]);
+  return nthreads;
+}
+
+static int check_args(int transA, int transB, int64_t M, int64_t N, int64_t K, int64_t lda,
+                      int64_t ldb, int in_type, int c_type) {
+  if (M < 0 || N < 0 || K < 0) return -1;
+  if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1)) return -1;
+  if (in_type != ORACLE_IN_BF16 && in_type != ORACLE_IN_F16) return -1;
+  if (c_type != ORACLE_C_F32 && c_type != ORACLE_C_BF16 && c_type != ORACLE_C_F16) return -1;
+  if (lda < (transA ? M : K) || ldb < (transB ? K : N)) return -1;
+  return 0;
+}
+
+/*
+ * Full oracle: R and Mag (M x N, leading dimension ldr) receive r_ij and m_ij.
+ * nthreads <= 0 uses every online core.  Returns the number of threads used,
+ * or -1 on a bad argument.
+ */
+int oracle_gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, double alpha,
+                const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb, double beta,
+                const void* C0, int c_type, int64_t ldc, int in_type, double* R, double* Mag,
+                int64_t ldr, int nthreads) {
+  if (check_args(transA, transB, M, N, K, lda, ldb, in_type, c_type) != 0) return -1;
+  if (ldr < N || (beta != 0.0 && ldc < N)) return -1;
+  if (M == 0 || N == 0) return 0;
+  nthreads = pick_threads(nthreads, M);
+  job_t* jobs = (job_t*)calloc((size_t)nthreads, sizeof(job_t));
+  if (!jobs) return -1;
+  for (int t = 0; t < nthreads; ++t) {
+    job_t* J = &jobs[t];
+    J->transA = transA; J->transB = transB; J->in_type = in_type; J->c_type = c_type;
+    J->M = M; J->N = N; J->K = K; J->lda = lda; J->ldb = ldb; J->ldc = ldc; J->ldr = ldr;
+    J->alpha = alpha; J->beta = beta; J->A = A; J->B = B; J->C0 = C0;
+    J->R = R; J->Mag = Mag;
+    J->row0 = M * t / nthreads;
+    J->row1 = M * (t + 1) / nthreads;
+  }
+  int used = run_jobs(jobs, nthreads, run_rows);
+  free(jobs);
+  return used;
+}
+
+/*
+ * Sampled oracle: for e in [0, count), R[e] / Mag[e] receive r and m at
+ * (rows[e], cols[e]).  Used where the full product would take too long.
+ */
+int oracle_gemm_at(int transA, int transB, int64_t M, int64_t N, int64_t K, double alpha,
+                   const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb, double beta,
+                   const void* C0, int c_type, int64_t ldc, int in_type, int64_t count,
+                   const int64_t* rows, const int64_t* cols, double* R, double* Mag,
+                   int nthreads) {
+  if (check_args(transA, transB, M, N, K, lda, ldb, in_type, c_type) != 0) return -1;
+  if (beta != 0.0 && ldc < N) return -1;
+  for (int64_t e = 0; e < count; ++e)
+    if (rows[e] < 0 || rows[e] >= M || cols[e] < 0 || cols[e] >= N) return -1;
+  if (count == 0) return 0;
+  nthreads = pick_threads(nthreads, count);
+  job_t* jobs = (job_t*)calloc((size_t)nthreads, sizeof(job_t));
+  if (!jobs) return -1;
+  for (int t = 0; t < nthreads; ++t) {
+    job_t* J = &jobs[t];
+    J->transA = transA; J->transB = transB; J->in_type = in_type; J->c_type = c_type;
+    J->M = M; J->N = N; J->K = K; J->lda = lda; J->ldb = ldb; J->ldc = ldc; J->ldr = 0;
+    J->alpha = alpha; J->beta = beta; J->A = A; J->B = B; J->C0 = C0;
+    J->R = R; J->Mag = Mag; J->rows = rows; J->cols = cols;
+    J->e0 = count * t / nthreads;
+    J->e1 = count * (t + 1) / nthreads;
+  }
+  int used = run_jobs(jobs, nthreads, run_entries);
+  free(jobs);
+  return used;
+}

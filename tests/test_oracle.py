@@ -1,0 +1,338 @@
+"""Pins for the CPU oracle (no GPU).
+
+Each test checks the oracle against something other than itself: the value
+definitions of the 16-bit formats and a library decoder over every bit
+pattern, closed forms (identity, permutation, rank-1 products), exact integer
+arithmetic, a brute-force loop written independently in pure Python, the
+degenerate sizes, and invariants of the tolerance magnitude.  Together they
+catch a dropped term, a wrong sign, a wrong index or stride, and a transposed
+operand anywhere in the oracle.
+"""
+import math
+import struct
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dense_gemm_10_gb300 import inputs
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def _stored(transX, rows, cols):
+    """Stored shape of op(X) = rows x cols."""
+    return (cols, rows) if transX else (rows, cols)
+
+
+def _op(stored, trans):
+    return np.ascontiguousarray(stored.T) if trans else stored
+
+
+# ---------------------------------------------------------------------------
+# Decoding the 16-bit formats
+# ---------------------------------------------------------------------------
+
+def test_bf16_decode_known_values():
+    assert oracle.bf16_value(0x3F80) == 1.0
+    assert oracle.bf16_value(0xC040) == -3.0
+    assert oracle.bf16_value(0x4049) == 3.140625
+    assert oracle.bf16_value(0x0001) == 2.0 ** -133           # smallest subnormal
+    assert oracle.bf16_value(0x0080) == 2.0 ** -126           # smallest normal
+    assert oracle.bf16_value(0x7F7F) == (2 - 2 ** -7) * 2.0 ** 127
+    assert oracle.bf16_value(0x8000) == 0.0 and math.copysign(1, oracle.bf16_value(0x8000)) < 0
+    assert oracle.bf16_value(0x7F80) == math.inf
+    assert math.isnan(oracle.bf16_value(0x7FC0))
+
+
+def test_f16_decode_known_values():
+    assert oracle.f16_value(0x3C00) == 1.0
+    assert oracle.f16_value(0xC200) == -3.0
+    assert oracle.f16_value(0x3555) == 0.333251953125
+    assert oracle.f16_value(0x0001) == 2.0 ** -24             # smallest subnormal
+    assert oracle.f16_value(0x0400) == 2.0 ** -14             # smallest normal
+    assert oracle.f16_value(0x7BFF) == 65504.0
+    assert oracle.f16_value(0xFC00) == -math.inf
+    assert math.isnan(oracle.f16_value(0x7E00))
+
+
+def test_bf16_decode_every_pattern_matches_library():
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    mine = np.array([oracle.bf16_value(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan)
+    assert np.array_equal(mine[~nan], ref[~nan])
+
+
+def test_f16_decode_every_pattern_matches_library():
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    mine = np.array([oracle.f16_value(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan)
+    assert np.array_equal(mine[~nan], ref[~nan])
+
+
+# ---------------------------------------------------------------------------
+# Closed forms
+# ---------------------------------------------------------------------------
+
+def _as_dtype_bits(x, dtype):
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(
+        torch.bfloat16 if dtype == "bf16" else torch.float16)
+    return inputs.bits(t), t.to(torch.float64).numpy()
+
+
+@pytest.mark.parametrize("transA", [0, 1])
+@pytest.mark.parametrize("transB", [0, 1])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_identity_left(transA, transB, dtype):
+    """A = I (M = K): r = alpha * B + beta * C0, exactly."""
+    M = K = 23
+    N = 17
+    in_type = oracle.IN_BF16 if dtype == "bf16" else oracle.IN_F16
+    a_bits, _ = _as_dtype_bits(np.eye(M), dtype)
+    b = inputs.draw(_stored(transB, K, N), ("uniform", -2, 2), 5, dtype)
+    b_bits, b_val = inputs.bits(b), b.to(torch.float64).numpy()
+    c0 = inputs.draw((M, N), ("normal", 0, 1), 6, "f32").numpy()
+    alpha, beta = 1.25, -0.75
+    R, Mag = oracle.gemm(transA, transB, M, N, K, alpha, a_bits, M, b_bits, b_bits.shape[1], beta,
+                         c0, N, in_type)
+    opb = _op(b_val, transB)
+    assert np.array_equal(R, alpha * opb + beta * c0.astype(np.float64))
+    assert np.array_equal(Mag, abs(alpha) * np.abs(opb) + abs(beta) * np.abs(c0.astype(np.float64)))
+
+
+@pytest.mark.parametrize("transA", [0, 1])
+@pytest.mark.parametrize("transB", [0, 1])
+def test_identity_right(transA, transB):
+    """B = I (K = N): r = alpha * op(A), exactly."""
+    M, K = 19, 32
+    a = inputs.draw(_stored(transA, M, K), ("uniform", -1, 1), 7, "bf16")
+    a_bits, a_val = inputs.bits(a), a.to(torch.float64).numpy()
+    b_bits, _ = _as_dtype_bits(np.eye(K), "bf16")
+    R, _ = oracle.gemm(transA, transB, M, K, K, -2.0, a_bits, a_bits.shape[1], b_bits, K, 0.0, None,
+                       K, oracle.IN_BF16)
+    assert np.array_equal(R, -2.0 * _op(a_val, transA))
+
+
+@pytest.mark.parametrize("transA", [0, 1])
+def test_permutation(transA):
+    """A = P: the rows of r are the rows of B taken in the order of P."""
+    M = K = 31
+    N = 9
+    perm = np.random.Generator(np.random.PCG64(11)).permutation(M)
+    P = np.zeros((M, K))
+    P[np.arange(M), perm] = 1.0
+    a_bits, _ = _as_dtype_bits(P.T if transA else P, "bf16")
+    b = inputs.draw((K, N), ("uniform", -1, 1), 12, "bf16")
+    b_bits, b_val = inputs.bits(b), b.to(torch.float64).numpy()
+    R, _ = oracle.gemm(transA, 0, M, N, K, 1.0, a_bits, M, b_bits, N, 0.0, None, N, oracle.IN_BF16)
+    assert np.array_equal(R, b_val[perm, :])
+
+
+@pytest.mark.parametrize("transA", [0, 1])
+@pytest.mark.parametrize("transB", [0, 1])
+def test_rank_one_closed_form(transA, transB):
+    """a(i, k) = u_i and b(k, j) = v_j: r_ij = alpha * K * u_i * v_j + beta * c0_ij, exactly."""
+    M, N, K = 12, 10, 40
+    g = np.random.Generator(np.random.PCG64(3))
+    u = 2.0 ** g.integers(-3, 4, size=M) * g.choice([-1, 1], size=M)
+    v = 2.0 ** g.integers(-3, 4, size=N) * g.choice([-1, 1], size=N)
+    opa = np.repeat(u[:, None], K, axis=1)
+    opb = np.repeat(v[None, :], K, axis=0)
+    a_bits, _ = _as_dtype_bits(opa.T if transA else opa, "f16")
+    b_bits, _ = _as_dtype_bits(opb.T if transB else opb, "f16")
+    c0 = g.integers(-8, 9, size=(M, N)).astype(np.float32)
+    alpha, beta = 0.5, 2.0
+    R, Mag = oracle.gemm(transA, transB, M, N, K, alpha, a_bits, a_bits.shape[1], b_bits,
+                         b_bits.shape[1], beta, c0, N, oracle.IN_F16)
+    want = alpha * K * np.outer(u, v) + beta * c0
+    assert np.array_equal(R, want)
+    assert np.array_equal(Mag, abs(alpha) * K * np.abs(np.outer(u, v)) + abs(beta) * np.abs(c0))
+
+
+# ---------------------------------------------------------------------------
+# Exact integer arithmetic
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("transA", [0, 1])
+@pytest.mark.parametrize("transB", [0, 1])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_small_integers_exact(transA, transB, dtype):
+    """Entries in {-4..4}: every partial sum is an integer far below 2^53, so the
+    oracle must equal the exact integer product, whatever the order of the sum.
+    Non-square shapes and padded leading dimensions catch a transposed operand
+    or a wrong stride."""
+    M, N, K = 13, 7, 29
+    pa, pb = 3, 5   # padding columns (filled with NaN bits, which must never be read)
+    in_type = oracle.IN_BF16 if dtype == "bf16" else oracle.IN_F16
+    sa, sb = _stored(transA, M, K), _stored(transB, K, N)
+    p = inputs.make_problem("ints", M, N, K, transA, transB, dtype, "f32", ("ints", -4, 4),
+                            ("ints", -4, 4), alpha=1.5, beta=0.5, dist_c=("ints", -9, 9), seed=21,
+                            lda=sa[1] + pa, ldb=sb[1] + pb, ldc=N + 2)
+    A_int = p.A[:, :sa[1]].to(torch.float64).numpy().astype(np.int64)
+    B_int = p.B[:, :sb[1]].to(torch.float64).numpy().astype(np.int64)
+    C_int = p.C0[:, :N].numpy().astype(np.int64)
+    exact = _op(A_int, transA) @ _op(B_int, transB)
+    R, Mag = oracle.gemm(transA, transB, M, N, K, p.alpha, inputs.bits(p.A), p.lda, inputs.bits(p.B),
+                         p.ldb, p.beta, p.C0.numpy(), p.ldc, in_type)
+    assert np.array_equal(R, 1.5 * exact + 0.5 * C_int)
+    absprod = np.abs(_op(A_int, transA)) @ np.abs(_op(B_int, transB))
+    assert np.array_equal(Mag, 1.5 * absprod + 0.5 * np.abs(C_int))
+
+
+def test_small_integers_exact_at_full_depth():
+    """K = 4096 with entries in {-4..4}: |partial sums| <= 65536, still exact."""
+    M, N, K = 5, 6, 4096
+    p = inputs.make_problem("ints_deep", M, N, K, 0, 1, "bf16", "f32", ("ints", -4, 4), ("ints", -4, 4),
+                            seed=40)
+    A_int = p.A.to(torch.float64).numpy().astype(np.int64)
+    B_int = p.B.to(torch.float64).numpy().astype(np.int64)
+    R, _ = oracle.gemm(0, 1, M, N, K, 1.0, inputs.bits(p.A), K, inputs.bits(p.B), K, 0.0, None, N,
+                       oracle.IN_BF16)
+    assert np.array_equal(R, (A_int @ B_int.T).astype(np.float64))
+
+
+# ---------------------------------------------------------------------------
+# Brute force: an independent loop in pure Python, other loop order, other decoder
+# ---------------------------------------------------------------------------
+
+def _py_value(h, dtype):
+    h = int(h)
+    if dtype == "f16":
+        return struct.unpack("<e", struct.pack("<H", h))[0]
+    return struct.unpack("<f", struct.pack("<I", h << 16))[0]
+
+
+def _brute(transA, transB, M, N, K, alpha, Abits, lda, Bbits, ldb, beta, C0, ldc, dtype):
+    Af, Bf = Abits.reshape(-1), Bbits.reshape(-1)
+    out = [[0.0] * N for _ in range(M)]
+    for j in range(N):
+        for i in range(M):
+            acc = 0.0
+            for k in range(K):
+                ha = Af[k * lda + i] if transA else Af[i * lda + k]
+                hb = Bf[j * ldb + k] if transB else Bf[k * ldb + j]
+                acc += _py_value(ha, dtype) * _py_value(hb, dtype)
+            v = alpha * acc
+            if beta != 0.0:
+                v += beta * float(C0.reshape(-1)[i * ldc + j])
+            out[i][j] = v
+    return np.array(out)
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1), (3, 5, 7), (7, 2, 13), (11, 13, 1), (24, 24, 24), (1, 17, 23)])
+@pytest.mark.parametrize("transA,transB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_brute_force_agreement(shape, transA, transB, dtype):
+    M, N, K = shape
+    seed = 100 + M * 7 + N * 3 + K + 2 * transA + transB
+    g = np.random.Generator(np.random.PCG64(seed))
+    alpha = float(g.uniform(-2, 2))
+    beta = float(g.choice([0.0, float(g.uniform(-2, 2))]))
+    p = inputs.make_problem("brute", M, N, K, transA, transB, dtype, "f32", ("normal", 0, 1),
+                            ("uniform", -3, 3), alpha=alpha, beta=beta, seed=seed,
+                            lda=_stored(transA, M, K)[1] + 1, ldb=_stored(transB, K, N)[1] + 2,
+                            ldc=N + 1)
+    in_type = oracle.IN_BF16 if dtype == "bf16" else oracle.IN_F16
+    c0 = p.C0.numpy() if p.C0 is not None else None
+    R, Mag = oracle.gemm(transA, transB, M, N, K, p.alpha, inputs.bits(p.A), p.lda, inputs.bits(p.B),
+                         p.ldb, p.beta, c0, p.ldc, in_type)
+    want = _brute(transA, transB, M, N, K, p.alpha, inputs.bits(p.A), p.lda, inputs.bits(p.B), p.ldb,
+                  p.beta, c0, p.ldc, dtype)
+    assert np.all(np.abs(R - want) <= 1e-12 * Mag + 1e-300)
+
+
+def test_bf16_output_c0_is_decoded():
+    """beta != 0 with a bf16 C0: the oracle must read C0 as bf16 bits."""
+    M, N, K = 4, 6, 8
+    p = inputs.make_problem("c16", M, N, K, 0, 0, "bf16", "bf16", ("ints", -2, 2), ("ints", -2, 2),
+                            alpha=1.0, beta=-2.0, dist_c=("ints", -5, 5), seed=9)
+    R, _ = oracle.gemm(0, 0, M, N, K, 1.0, inputs.bits(p.A), K, inputs.bits(p.B), N, -2.0,
+                       inputs.bits(p.C0), N, oracle.IN_BF16, c_type=oracle.C_BF16)
+    exact = p.A.double().numpy() @ p.B.double().numpy() - 2.0 * p.C0.double().numpy()
+    assert np.array_equal(R, exact)
+
+
+# ---------------------------------------------------------------------------
+# Degenerate sizes, invariants, the sampled mode
+# ---------------------------------------------------------------------------
+
+def test_k_zero_gives_beta_c0():
+    M, N = 6, 5
+    c0 = inputs.draw((M, N), ("normal", 0, 1), 1, "f32").numpy()
+    a = np.zeros((M, 1), dtype=np.uint16)
+    b = np.zeros((1, N), dtype=np.uint16)
+    R, Mag = oracle.gemm(0, 0, M, N, 0, 3.0, a, 1, b, N, -0.5, c0, N, oracle.IN_BF16)
+    assert np.array_equal(R, -0.5 * c0.astype(np.float64))
+    assert np.array_equal(Mag, 0.5 * np.abs(c0.astype(np.float64)))
+
+
+def test_beta_zero_ignores_nan_c0():
+    M, N, K = 3, 4, 5
+    p = inputs.make_problem("nanc", M, N, K, 0, 0, "bf16", "f32", ("ints", -2, 2), ("ints", -2, 2), seed=2)
+    c0 = np.full((M, N), np.nan, dtype=np.float32)
+    R, _ = oracle.gemm(0, 0, M, N, K, 1.0, inputs.bits(p.A), K, inputs.bits(p.B), N, 0.0, c0, N,
+                       oracle.IN_BF16)
+    assert np.all(np.isfinite(R))
+
+
+def test_empty_sizes():
+    R, Mag = oracle.gemm(0, 0, 0, 5, 3, 1.0, np.zeros((1, 3), np.uint16), 3, np.zeros((3, 5), np.uint16),
+                         5, 0.0, None, 5, oracle.IN_BF16)
+    assert R.shape == (0, 5)
+    R, Mag = oracle.gemm(0, 0, 4, 0, 3, 1.0, np.zeros((4, 3), np.uint16), 3, np.zeros((3, 1), np.uint16),
+                         1, 0.0, None, 1, oracle.IN_BF16)
+    assert R.shape == (4, 0)
+
+
+def test_rejects_bad_arguments():
+    with pytest.raises(ValueError):
+        oracle.gemm(0, 0, 4, 4, 8, 1.0, np.zeros((4, 8), np.uint16), 7, np.zeros((8, 4), np.uint16), 4,
+                    0.0, None, 4, oracle.IN_BF16)   # lda < K
+
+
+def test_magnitude_bounds_result():
+    """|r| <= m always (triangle inequality), with equality when every term is >= 0."""
+    p = inputs.make_problem("mag", 20, 30, 50, 1, 0, "f16", "f32", ("normal", 0, 1), ("normal", 0, 1),
+                            alpha=-1.5, beta=0.25, seed=4)
+    R, Mag = oracle.gemm(1, 0, 20, 30, 50, -1.5, inputs.bits(p.A), 20, inputs.bits(p.B), 30, 0.25,
+                         p.C0.numpy(), 30, oracle.IN_F16)
+    assert np.all(np.abs(R) <= Mag * (1 + 1e-15))
+    q = inputs.make_problem("pos", 9, 8, 70, 0, 0, "bf16", "f32", ("uniform", 0, 1), ("uniform", 0, 1), seed=8)
+    R, Mag = oracle.gemm(0, 0, 9, 8, 70, 2.0, inputs.bits(q.A), 70, inputs.bits(q.B), 8, 0.0, None, 8,
+                         oracle.IN_BF16)
+    assert np.array_equal(R, Mag)
+
+
+def test_sampled_mode_equals_full_mode():
+    p = inputs.make_problem("samp", 37, 41, 64, 0, 1, "bf16", "f32", ("normal", 0, 1), ("normal", 0, 1),
+                            alpha=0.7, beta=1.1, seed=13)
+    R, Mag = oracle.gemm(0, 1, 37, 41, 64, 0.7, inputs.bits(p.A), 64, inputs.bits(p.B), 64, 1.1,
+                         p.C0.numpy(), 41, oracle.IN_BF16, nthreads=3)
+    g = np.random.Generator(np.random.PCG64(0))
+    rows = g.integers(0, 37, 200)
+    cols = g.integers(0, 41, 200)
+    r, m = oracle.gemm_at(0, 1, 37, 41, 64, 0.7, inputs.bits(p.A), 64, inputs.bits(p.B), 64, 1.1,
+                          p.C0.numpy(), 41, oracle.IN_BF16, rows, cols, nthreads=5)
+    assert np.array_equal(r, R[rows, cols]) and np.array_equal(m, Mag[rows, cols])
+
+
+def test_thread_count_does_not_change_results():
+    p = inputs.make_problem("thr", 50, 20, 33, 0, 0, "f16", "f32", ("normal", 0, 1), ("normal", 0, 1), seed=17)
+    args = (0, 0, 50, 20, 33, 1.0, inputs.bits(p.A), 33, inputs.bits(p.B), 20, 0.0, None, 20, oracle.IN_F16)
+    R1, _ = oracle.gemm(*args, nthreads=1)
+    R7, _ = oracle.gemm(*args, nthreads=7)
+    assert np.array_equal(R1, R7)
+
+
+def test_tolerance_rule():
+    r = np.array([1.0, 1.0, 0.0, 1.0])
+    m = np.array([1.0, 1.0, 10.0, 1.0])
+    out = np.array([1.0 + 0.9e-3, 1.0 + 1.2e-3, 9e-3, np.nan])
+    assert list(oracle.within_tolerance(out, r, m, True)) == [True, False, True, False]
+    out16 = np.array([1.0 + 8.5e-3, 1.0 + 1e-2, 0.0, 1.0])
+    assert list(oracle.within_tolerance(out16, r, m, False)) == [True, False, True, True]

@@ -1,0 +1,40 @@
+"""Plant plausible mistakes in copies of the oracle source and check that the
+pins in test_oracle.py catch each one (CPU only; the real oracle is untouched)."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "gemm_oracle.c")
+
+MUTATIONS = {
+    "B read as if never transposed": ("J->B[j * J->ldb + k] : J->B[k * J->ldb + j]",
+                                      "J->B[k * J->ldb + j] : J->B[k * J->ldb + j]"),
+    "A index transposed": ("J->A[k * J->lda + i] : J->A[i * J->lda + k]",
+                           "J->A[i * J->lda + k] : J->A[k * J->lda + i]"),
+    "last k term dropped": ("for (int64_t k = 0; k < J->K; ++k)", "for (int64_t k = 0; k + 1 < J->K; ++k)"),
+    "beta term sign flipped": ("rv += J->beta * c0;", "rv -= J->beta * c0;"),
+    "alpha dropped": ("double rv = J->alpha * s;", "double rv = s;"),
+    "fp16 exponent bias off by one": ("e - 15);", "e - 16);"),
+    "bf16 fraction width wrong": ("1.0 + (double)f / 128.0", "1.0 + (double)f / 256.0"),
+    "C0 leading dimension ignored": ("i * J->ldc + j", "i * J->N + j"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, "mutation site not found: %s" % old
+    mutated = tmp_path / "mut.c"
+    mutated.write_text(src.replace(old, new))
+    lib = tmp_path / "libmut.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", str(mutated),
+                    "-o", str(lib), "-lpthread", "-lm"], check=True)
+    env = dict(os.environ, ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle.py")], cwd=ROOT, env=env,
+                       capture_output=True, text=True)
+    assert r.returncode != 0, "the pins did not catch: %s" % name
