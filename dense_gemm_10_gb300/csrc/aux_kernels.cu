@@ -1,0 +1,67 @@
+// aux_kernels.cu -- the two non-tensor-core kernels of the library:
+//  * repack16: copies a 16-bit operand whose rows are not 16-byte aligned into
+//    an aligned buffer, because the tensor-memory-accelerator copy engine only
+//    reads rows whose pitch is a multiple of 16 bytes;
+//  * scale_c: C = beta * C, the whole GEMM when K == 0 ("CUDA GEMM 矩阵乘法优化指南",
+//    section 2.1, with an empty sum).
+// Both are HBM-bound grid-stride copies over a grid sized to the SM count.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "gemm_internal.h"
+
+namespace g10 {
+
+__global__ void repack16_kernel(const uint16_t* __restrict__ src, int64_t lds,
+                                uint16_t* __restrict__ dst, int64_t ldd, int64_t rows,
+                                int64_t cols) {
+  for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+    const uint16_t* s = src + r * lds;
+    uint16_t* d = dst + r * ldd;
+    for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < cols;
+         c += static_cast<int64_t>(gridDim.x) * blockDim.x)
+      d[c] = s[c];
+  }
+}
+
+__global__ void scale_c_kernel(void* C, int32_t c_type, int64_t M, int64_t N, int64_t ldc,
+                               float beta) {
+  for (int64_t r = blockIdx.y; r < M; r += gridDim.y) {
+    for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < N;
+         c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+      const int64_t off = r * ldc + c;
+      if (c_type == kCF32) {
+        float* p = static_cast<float*>(C) + off;
+        *p = beta == 0.0f ? 0.0f : beta * *p;
+      } else if (c_type == kCBF16) {
+        __nv_bfloat16* p = static_cast<__nv_bfloat16*>(C) + off;
+        *p = __float2bfloat16_rn(beta == 0.0f ? 0.0f : beta * __bfloat162float(*p));
+      } else {
+        __half* p = static_cast<__half*>(C) + off;
+        *p = __float2half_rn(beta == 0.0f ? 0.0f : beta * __half2float(*p));
+      }
+    }
+  }
+}
+
+static dim3 grid_2d(int64_t rows, int64_t cols, int sm_count) {
+  const int64_t bx = (cols + 255) / 256 < 16 ? (cols + 255) / 256 : 16;
+  int64_t by = (static_cast<int64_t>(sm_count) * 8 + bx - 1) / bx;
+  if (by > rows) by = rows;
+  if (by > 65535) by = 65535;
+  return dim3(static_cast<unsigned>(bx > 0 ? bx : 1), static_cast<unsigned>(by > 0 ? by : 1), 1);
+}
+
+cudaError_t repack16_launch(const uint16_t* src, int64_t lds, uint16_t* dst, int64_t ldd,
+                            int64_t rows, int64_t cols, int sm_count, cudaStream_t stream) {
+  repack16_kernel<<<grid_2d(rows, cols, sm_count), 256, 0, stream>>>(src, lds, dst, ldd, rows, cols);
+  return cudaGetLastError();
+}
+
+cudaError_t scale_c_launch(void* C, int32_t c_type, int64_t M, int64_t N, int64_t ldc, float beta,
+                           int sm_count, cudaStream_t stream) {
+  scale_c_kernel<<<grid_2d(M, N, sm_count), 256, 0, stream>>>(C, c_type, M, N, ldc, beta);
+  return cudaGetLastError();
+}
+
+}  // namespace g10

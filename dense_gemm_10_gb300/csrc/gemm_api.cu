@@ -1,0 +1,503 @@
+// gemm_api.cu -- the C ABI of include/gemm_gb300.h: handles, argument checks,
+// the planner, tensor-map encoding and kernel launches.
+//
+// The planner restates, for this GPU, the blocking choices of the pages:
+// output tiles computed by one CTA ("CUDA GEMM 矩阵乘法优化指南", 5.1 and 13.2),
+// a persistent grid of one CTA per SM (12.5), a k-split when there are too few
+// tiles to fill the SMs ("GPU GEMM 优化完全拆解（三）", Split-K 与 Sliced-K), and
+// the transpose identity C^T = B^T A^T that cuBLAS callers use to swap operand
+// roles ("第4章：经典算子实现 —— GEMM", 7.1), here to put a short M on the MMA's
+// N dimension.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gemm_gb300.h"
+#include "gemm_internal.h"
+#include "ptx.cuh"
+
+using namespace g10;
+
+namespace {
+
+constexpr int64_t kMaxExtent = (int64_t{1} << 31) - 4096;  // kernel indexes with int32
+constexpr int64_t kCounterCap = 1 << 16;                    // split-K tiles per call
+constexpr int64_t kDefaultWaitNs = 2000000000;              // 2 s
+
+struct Options {
+  int64_t wait_limit_ns = kDefaultWaitNs;
+  int force_path = 0;
+  int split_k = 0;
+  int raster_group = 0;
+  int force_bn = 0;
+  int drop_load = 0;
+};
+
+// One stored operand, as the tensor-memory-accelerator copy engine will see it.
+struct Operand {
+  const void* ptr = nullptr;  // stored matrix (row-major)
+  int64_t rows = 0, cols = 0; // stored shape
+  int64_t ld = 0;             // leading dimension in elements
+  bool kmajor = false;        // K runs along stored rows (cols == K)
+  bool repack = false;        // copied into the workspace first
+  int64_t packed_ld = 0;
+  size_t ws_offset = 0;
+};
+
+struct Plan {
+  gemm_plan_t pub{};
+  Operand p, q;
+  int64_t I = 0, J = 0, K = 0;
+  int64_t c_si = 0, c_sj = 0;
+  int32_t c_type = kCF32;
+  bool bf16 = true;
+  size_t partial_offset = 0;
+};
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool tma_aligned(const void* p, int64_t ld) {
+  return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((ld * 2) % 16 == 0);
+}
+
+// Heuristic cost of a configuration in "k-block of a 128 x 256 tile" units:
+// waves of units times the k-blocks of one unit, plus a split's extra pass.
+double est_cost(int64_t tiles, int split, int64_t num_kb, int bn, int sm_count) {
+  const int64_t units = tiles * split;
+  const int64_t waves = cdiv(units, sm_count);
+  const double per_kb = bn == 256 ? 1.0 : bn == 128 ? 0.56 : 0.34;  // smem-read bound below 256
+  const double kb = static_cast<double>(cdiv(num_kb, split));
+  const double extra = split > 1 ? 1.5 : 0.0;
+  return static_cast<double>(waves) * (kb + extra) * per_kb + (split > 1 ? 0.5 : 0.0);
+}
+
+gemm_status_t make_plan(const Options& o, int sm_count, gemm_op_t transA, gemm_op_t transB,
+                        int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                        int64_t ldb, float beta, const void* C, int64_t ldc, gemm_dtype_t dtype,
+                        Plan* out) {
+  Plan pl;
+  gemm_plan_t& P = pl.pub;
+  if ((transA != GEMM_OP_N && transA != GEMM_OP_T) || (transB != GEMM_OP_N && transB != GEMM_OP_T))
+    return GEMM_ERR_INVALID_ARG;
+  if (dtype < GEMM_BF16_F32 || dtype > GEMM_F16_F16) return GEMM_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || sm_count <= 0) return GEMM_ERR_INVALID_ARG;
+  pl.bf16 = dtype == GEMM_BF16_F32 || dtype == GEMM_BF16_BF16;
+  pl.c_type = (dtype == GEMM_BF16_F32 || dtype == GEMM_F16_F32) ? kCF32
+              : dtype == GEMM_BF16_BF16                        ? kCBF16
+                                                               : kCF16;
+  const int64_t c_elem = pl.c_type == kCF32 ? 4 : 2;
+  if (M == 0 || N == 0) {
+    P.path = GEMM_PATH_NOOP;
+    *out = pl;
+    return GEMM_OK;
+  }
+  if (C == nullptr || ldc < N) return GEMM_ERR_INVALID_ARG;
+  if (M > kMaxExtent || N > kMaxExtent || K > kMaxExtent) return GEMM_ERR_UNSUPPORTED;
+  if (K == 0) {
+    P.path = GEMM_PATH_SCALE_C;
+    P.launches = 1;
+    *out = pl;
+    return GEMM_OK;
+  }
+  if (A == nullptr || B == nullptr) return GEMM_ERR_INVALID_ARG;
+  if (lda < (transA == GEMM_OP_T ? M : K) || ldb < (transB == GEMM_OP_T ? K : N))
+    return GEMM_ERR_INVALID_ARG;
+
+  // Stored operands.
+  Operand a, b;
+  a.ptr = A; a.ld = lda; a.kmajor = transA == GEMM_OP_N;
+  a.rows = a.kmajor ? M : K; a.cols = a.kmajor ? K : M;
+  b.ptr = B; b.ld = ldb; b.kmajor = transB == GEMM_OP_T;
+  b.rows = b.kmajor ? N : K; b.cols = b.kmajor ? K : N;
+
+  // A short M rides on the MMA's N dimension: compute C^T = op(B)^T op(A)^T.
+  const bool swap = M <= 64 && N > M;
+  P.swap_ab = swap ? 1 : 0;
+  pl.I = swap ? N : M;
+  pl.J = swap ? M : N;
+  pl.K = K;
+  pl.p = swap ? b : a;
+  pl.q = swap ? a : b;
+  pl.c_si = swap ? 1 : ldc;
+  pl.c_sj = swap ? ldc : 1;
+  P.a_kmajor = pl.p.kmajor ? 1 : 0;
+  P.b_kmajor = pl.q.kmajor ? 1 : 0;
+
+  const int64_t num_kb = cdiv(K, kBK);
+  const int64_t tiles_i = cdiv(pl.I, kBM);
+
+  // Tile width and k-split.
+  int bn_choices[3] = {256, 128, 64};
+  int best_bn = 256, best_split = 1;
+  double best_cost = 1e300;
+  for (int bn : bn_choices) {
+    if (o.force_bn && bn != o.force_bn) continue;
+    if (!o.force_bn && bn > 64 && pl.J <= bn / 2) continue;  // too wide for J
+    const int64_t tiles = tiles_i * cdiv(pl.J, bn);
+    int max_split = 1;
+    if (tiles < 2 * static_cast<int64_t>(sm_count) && tiles <= kCounterCap)
+      max_split = static_cast<int>(std::min<int64_t>(16, num_kb / 2));
+    if (max_split < 1) max_split = 1;
+    for (int s = 1; s <= max_split; ++s) {
+      if (o.split_k && s != std::min<int64_t>(o.split_k, num_kb)) continue;
+      const double c = est_cost(tiles, s, num_kb, bn, sm_count);
+      if (c < best_cost - 1e-9) {
+        best_cost = c;
+        best_bn = bn;
+        best_split = s;
+      }
+    }
+  }
+  if (best_cost >= 1e300) {  // forced split beyond what the tile count allows
+    best_bn = o.force_bn ? o.force_bn : 256;
+    const int64_t tiles = tiles_i * cdiv(pl.J, best_bn);
+    best_split = (tiles <= kCounterCap && o.split_k)
+                     ? static_cast<int>(std::min<int64_t>(o.split_k, num_kb))
+                     : 1;
+  }
+  P.path = GEMM_PATH_TC_1CTA;
+  P.bm = kBM;
+  P.bn = best_bn;
+  P.bk = kBK;
+  P.stages = tc_stages(best_bn);
+  P.split_k = best_split;
+  const int64_t tiles_j = cdiv(pl.J, best_bn);
+  P.tiles = tiles_i * tiles_j;
+  P.units = P.tiles * best_split;
+  P.raster_group = o.raster_group ? o.raster_group : 8;
+  if (P.raster_group > tiles_i) P.raster_group = static_cast<int32_t>(tiles_i);
+  P.grid = static_cast<int32_t>(std::min<int64_t>(P.units, sm_count));
+
+  // Workspace: repacked operands, then split-K partials.
+  size_t ws = 0;
+  for (Operand* op : {&pl.p, &pl.q}) {
+    if (!tma_aligned(op->ptr, op->ld)) {
+      op->repack = true;
+      op->packed_ld = static_cast<int64_t>(round_up(static_cast<size_t>(op->cols), 8));
+      op->ws_offset = ws;
+      ws = round_up(ws + static_cast<size_t>(op->rows) * op->packed_ld * 2, 256);
+    }
+  }
+  P.repack_a = (swap ? pl.q.repack : pl.p.repack) ? 1 : 0;
+  P.repack_b = (swap ? pl.p.repack : pl.q.repack) ? 1 : 0;
+  if (best_split > 1) {
+    pl.partial_offset = ws;
+    ws = round_up(ws + static_cast<size_t>(P.units) * best_bn * kBM * 4, 256);
+  }
+  P.workspace_bytes = static_cast<int64_t>(ws);
+  P.vector_store = (!swap && reinterpret_cast<uintptr_t>(C) % 16 == 0 && (ldc * c_elem) % 16 == 0) ? 1 : 0;
+  P.launches = 1 + P.repack_a + P.repack_b;
+  (void)beta;
+  *out = pl;
+  return GEMM_OK;
+}
+
+// ------------------------------------------------------------ tensor maps --
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Describe operand `op` (possibly its repacked copy at `base`/`ld`) for 2-D tiled
+// loads with the 128-byte swizzle: K-major tiles are {64 k} x {box_rows rows};
+// MN-major tiles are {64 rows of M/N} x {64 k}, loaded one 64-wide atom at a time.
+gemm_status_t encode_operand(CUtensorMap* map, const Operand& op, const void* base, int64_t ld,
+                             bool bf16, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return GEMM_ERR_TENSORMAP;
+  cuuint64_t dims[2];
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2];
+  cuuint32_t estr[2] = {1, 1};
+  if (op.kmajor) {
+    dims[0] = static_cast<cuuint64_t>(op.cols);  // K
+    dims[1] = static_cast<cuuint64_t>(op.rows);  // M or N
+    box[0] = kBK;
+    box[1] = static_cast<cuuint32_t>(box_rows);
+  } else {
+    dims[0] = static_cast<cuuint64_t>(op.cols);  // M or N
+    dims[1] = static_cast<cuuint64_t>(op.rows);  // K
+    box[0] = 64;
+    box[1] = kBK;
+  }
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_TENSORMAP;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  bool changed = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) changed = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (changed) cudaSetDevice(prev);
+  }
+};
+
+}  // namespace
+
+struct gemm_handle_s {
+  int device = -1;
+  int sm_count = 0;
+  int32_t* d_status = nullptr;
+  int32_t* d_counters = nullptr;
+  void* d_ws = nullptr;
+  size_t ws_bytes = 0;
+  uint64_t launches = 0;
+  int last_cuda_error = 0;
+  bool prepared[3] = {false, false, false};
+  Options opt;
+};
+
+static gemm_status_t cuda_fail(gemm_handle_t h, cudaError_t e) {
+  if (h) h->last_cuda_error = static_cast<int>(e);
+  return GEMM_ERR_CUDA;
+}
+
+extern "C" {
+
+gemm_status_t gemm_create(gemm_handle_t* out, int device) {
+  if (!out) return GEMM_ERR_INVALID_ARG;
+  *out = nullptr;
+  int count = 0;
+  if (cudaGetDeviceCount(&count) != cudaSuccess || device < 0 || device >= count) {
+    cudaGetLastError();
+    return GEMM_ERR_NO_DEVICE;
+  }
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return GEMM_ERR_NO_DEVICE;
+  if (prop.major != 10 || prop.minor != 3) return GEMM_ERR_NO_DEVICE;  // built for sm_103a only
+  gemm_handle_t h = new (std::nothrow) gemm_handle_s;
+  if (!h) return GEMM_ERR_WORKSPACE;
+  h->device = device;
+  h->sm_count = prop.multiProcessorCount;
+  DeviceGuard g(device);
+  cudaError_t e = cudaMalloc(&h->d_status, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMalloc(&h->d_counters, kCounterCap * sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemset(h->d_counters, 0, kCounterCap * sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(h->d_status);
+    cudaFree(h->d_counters);
+    delete h;
+    return GEMM_ERR_CUDA;
+  }
+  *out = h;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_destroy(gemm_handle_t h) {
+  if (!h) return GEMM_OK;
+  {
+    DeviceGuard g(h->device);
+    cudaDeviceSynchronize();
+    cudaFree(h->d_ws);
+    cudaFree(h->d_counters);
+    cudaFree(h->d_status);
+  }
+  delete h;
+  return GEMM_OK;
+}
+
+const char* gemm_status_string(gemm_status_t s) {
+  switch (s) {
+    case GEMM_OK: return "ok";
+    case GEMM_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM_ERR_UNSUPPORTED: return "unsupported size";
+    case GEMM_ERR_NO_DEVICE: return "no sm_103 device";
+    case GEMM_ERR_CUDA: return "CUDA runtime error";
+    case GEMM_ERR_TENSORMAP: return "tensor map encoding failed";
+    case GEMM_ERR_TIMEOUT: return "kernel barrier wait timed out";
+    case GEMM_ERR_WORKSPACE: return "workspace allocation failed";
+  }
+  return "unknown status";
+}
+
+int gemm_last_cuda_error(gemm_handle_t h) { return h ? h->last_cuda_error : 0; }
+
+gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  switch (opt) {
+    case GEMM_OPT_WAIT_LIMIT_NS:
+      if (value < 1000000) return GEMM_ERR_INVALID_ARG;
+      h->opt.wait_limit_ns = value;
+      return GEMM_OK;
+    case GEMM_OPT_FORCE_PATH:
+      if (value != 0 && value != GEMM_PATH_TC_1CTA) return GEMM_ERR_INVALID_ARG;
+      h->opt.force_path = static_cast<int>(value);
+      return GEMM_OK;
+    case GEMM_OPT_SPLIT_K:
+      if (value < 0 || value > 64) return GEMM_ERR_INVALID_ARG;
+      h->opt.split_k = static_cast<int>(value);
+      return GEMM_OK;
+    case GEMM_OPT_RASTER_GROUP:
+      if (value < 0 || value > 1024) return GEMM_ERR_INVALID_ARG;
+      h->opt.raster_group = static_cast<int>(value);
+      return GEMM_OK;
+    case GEMM_OPT_FORCE_BN:
+      if (value != 0 && value != 64 && value != 128 && value != 256) return GEMM_ERR_INVALID_ARG;
+      h->opt.force_bn = static_cast<int>(value);
+      return GEMM_OK;
+    case GEMM_OPT_TEST_DROP_LOAD:
+      if (value < 0 || value > (int64_t{1} << 30)) return GEMM_ERR_INVALID_ARG;
+      h->opt.drop_load = static_cast<int>(value);
+      return GEMM_OK;
+  }
+  return GEMM_ERR_INVALID_ARG;
+}
+
+gemm_status_t gemm_launch_count(gemm_handle_t h, uint64_t* count) {
+  if (!h || !count) return GEMM_ERR_INVALID_ARG;
+  *count = h->launches;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan(gemm_handle_t h, int sm_count, gemm_op_t transA, gemm_op_t transB,
+                        int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                        const void* B, int64_t ldb, float beta, const void* C, int64_t ldc,
+                        gemm_dtype_t dtype, gemm_plan_t* plan) {
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  Options o = h ? h->opt : Options();
+  Plan pl;
+  gemm_status_t s =
+      make_plan(o, sm_count, transA, transB, M, N, K, A, lda, B, ldb, beta, C, ldc, dtype, &pl);
+  if (s == GEMM_OK) *plan = pl.pub;
+  return s;
+}
+
+gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int64_t M, int64_t N,
+                       int64_t K, float alpha, const void* A, int64_t lda, const void* B,
+                       int64_t ldb, float beta, void* C, int64_t ldc, gemm_dtype_t dtype,
+                       void* stream) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  Plan pl;
+  gemm_status_t s = make_plan(h->opt, h->sm_count, transA, transB, M, N, K, A, lda, B, ldb, beta,
+                              C, ldc, dtype, &pl);
+  if (s != GEMM_OK) return s;
+  const gemm_plan_t& P = pl.pub;
+  if (P.path == GEMM_PATH_NOOP) return GEMM_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DeviceGuard g(h->device);
+  cudaError_t e;
+  if (P.path == GEMM_PATH_SCALE_C) {
+    e = scale_c_launch(C, pl.c_type, M, N, ldc, beta, h->sm_count, st);
+    if (e != cudaSuccess) return cuda_fail(h, e);
+    h->launches += 1;
+    return GEMM_OK;
+  }
+
+  // Grow the workspace (synchronous: cudaFree waits for work that may still use it).
+  if (static_cast<size_t>(P.workspace_bytes) > h->ws_bytes) {
+    const size_t want = round_up(static_cast<size_t>(P.workspace_bytes) + (size_t{1} << 20), 1 << 20);
+    void* nw = nullptr;
+    e = cudaMalloc(&nw, want);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      h->last_cuda_error = static_cast<int>(e);
+      return GEMM_ERR_WORKSPACE;
+    }
+    cudaFree(h->d_ws);
+    h->d_ws = nw;
+    h->ws_bytes = want;
+  }
+  const int bn_slot = P.bn == 256 ? 2 : P.bn == 128 ? 1 : 0;
+  if (!h->prepared[bn_slot]) {
+    e = tc_prepare(P.bn);
+    if (e != cudaSuccess) return cuda_fail(h, e);
+    h->prepared[bn_slot] = true;
+  }
+
+  // Operands that the copy engine cannot read directly are repacked first.
+  const void* pbase = pl.p.ptr;
+  const void* qbase = pl.q.ptr;
+  int64_t pld = pl.p.ld, qld = pl.q.ld;
+  uint8_t* ws = static_cast<uint8_t*>(h->d_ws);
+  for (int w = 0; w < 2; ++w) {
+    const Operand& op = w == 0 ? pl.p : pl.q;
+    if (!op.repack) continue;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(ws + op.ws_offset);
+    e = repack16_launch(static_cast<const uint16_t*>(op.ptr), op.ld, dst, op.packed_ld, op.rows,
+                        op.cols, h->sm_count, st);
+    if (e != cudaSuccess) return cuda_fail(h, e);
+    h->launches += 1;
+    if (w == 0) { pbase = dst; pld = op.packed_ld; } else { qbase = dst; qld = op.packed_ld; }
+  }
+
+  CUtensorMap map_p, map_q;
+  s = encode_operand(&map_p, pl.p, pbase, pld, pl.bf16, kBM);
+  if (s != GEMM_OK) return s;
+  s = encode_operand(&map_q, pl.q, qbase, qld, pl.bf16, P.bn);
+  if (s != GEMM_OK) return s;
+
+  TcArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.I = static_cast<int32_t>(pl.I);
+  a.J = static_cast<int32_t>(pl.J);
+  a.K = static_cast<int32_t>(pl.K);
+  a.tiles_i = static_cast<int32_t>(cdiv(pl.I, kBM));
+  a.tiles_j = static_cast<int32_t>(cdiv(pl.J, P.bn));
+  a.num_kb = static_cast<int32_t>(cdiv(pl.K, kBK));
+  a.split_k = P.split_k;
+  a.units = static_cast<int32_t>(P.units);
+  a.raster_group = P.raster_group;
+  a.p_kmajor = P.a_kmajor;
+  a.q_kmajor = P.b_kmajor;
+  a.idesc = make_idesc_f16(pl.bf16, !pl.p.kmajor, !pl.q.kmajor, kBM, P.bn);
+  a.alpha = alpha;
+  a.beta = beta;
+  a.C = C;
+  a.c_si = pl.c_si;
+  a.c_sj = pl.c_sj;
+  a.c_type = pl.c_type;
+  a.vec_store = P.vector_store;
+  a.partials = P.split_k > 1 ? reinterpret_cast<float*>(ws + pl.partial_offset) : nullptr;
+  a.counters = h->d_counters;
+  a.status = h->d_status;
+  a.wait_limit_ns = static_cast<uint64_t>(h->opt.wait_limit_ns);
+  a.drop_load = h->opt.drop_load;
+  e = tc_launch(P.bn, map_p, map_q, a, P.grid, st);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  h->launches += 1;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_get_status(gemm_handle_t h, void* stream, int32_t* detail) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  DeviceGuard g(h->device);
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  int32_t word = 0;
+  e = cudaMemcpy(&word, h->d_status, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  if (detail) *detail = word;
+  if (word == 0) return GEMM_OK;
+  // A kernel gave up part-way: clear the status and any split-K counters it left behind.
+  e = cudaMemset(h->d_status, 0, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemset(h->d_counters, 0, kCounterCap * sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  return GEMM_ERR_TIMEOUT;
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// gemm_internal.h -- declarations shared by the host planner (gemm_api.cu) and
+// the kernels.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace g10 {
+
+constexpr int kBM = 128;      // MMA M (rows of the output tile held in TMEM lanes)
+constexpr int kBK = 64;       // k-block: 64 16-bit elements = one 128-byte swizzle row
+constexpr int kThreads = 192; // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue
+
+// Element type of C.
+enum CType : int32_t { kCF32 = 0, kCBF16 = 1, kCF16 = 2 };
+
+// Status-word layout written by a kernel that gives up on a barrier:
+//   bits 0-7 = 6 (GEMM_ERR_TIMEOUT), bits 8-11 = role, bits 12-15 = barrier.
+enum : int32_t { kStatusTimeout = 6 };
+enum WaitRole : int32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3 };
+enum WaitBarrier : int32_t {
+  kBarEmpty = 1, kBarFull = 2, kBarAccEmpty = 3, kBarAccFull = 4, kBarDrain = 5
+};
+
+// Arguments of the persistent tcgen05 GEMM kernel, in the kernel's own terms:
+//   D (I x J) = P (I x K) * Q (K x J),  C[i * c_si + j * c_sj] = alpha * D[i][j] + beta * C[...]
+// P is the MMA "A" operand (tile rows on TMEM lanes), Q the MMA "B" operand.
+struct TcArgs {
+  int32_t I, J, K;
+  int32_t tiles_i, tiles_j;
+  int32_t num_kb;        // ceil(K / kBK)
+  int32_t split_k;       // k-splits per tile
+  int32_t units;         // tiles_i * tiles_j * split_k
+  int32_t raster_group;  // tile rows (along I) per raster group
+  int32_t p_kmajor;      // P has K contiguous (else I contiguous)
+  int32_t q_kmajor;      // Q has K contiguous (else J contiguous)
+  uint32_t idesc;        // tcgen05 instruction descriptor
+  float alpha, beta;
+  void* C;
+  int64_t c_si, c_sj;
+  int32_t c_type;        // CType
+  int32_t vec_store;     // c_sj == 1 and every row of C starts 16-byte aligned
+  float* partials;       // split-K partial tiles, [units][BN][kBM] fp32
+  int32_t* counters;     // per-tile arrival counters, zero between calls
+  int32_t* status;       // device status word
+  uint64_t wait_limit_ns;
+  int32_t drop_load;     // tests only: CTA 0 skips its drop_load-th k-block load (1-based)
+};
+
+int tc_stages(int bn);
+size_t tc_smem_bytes(int bn);
+cudaError_t tc_prepare(int bn);  // one-time per device: opt in to the kernel's shared memory
+cudaError_t tc_launch(int bn, const CUtensorMap& map_p, const CUtensorMap& map_q,
+                      const TcArgs& args, int grid, cudaStream_t stream);
+
+// dst[r * ldd + c] = src[r * lds + c] for 16-bit elements, r < rows, c < cols.
+cudaError_t repack16_launch(const uint16_t* src, int64_t lds, uint16_t* dst, int64_t ldd,
+                            int64_t rows, int64_t cols, int sm_count, cudaStream_t stream);
+
+// C = beta * C over an M x N matrix with leading dimension ldc (C = 0 when beta == 0).
+cudaError_t scale_c_launch(void* C, int32_t c_type, int64_t M, int64_t N, int64_t ldc, float beta,
+                           int sm_count, cudaStream_t stream);
+
+}  // namespace g10

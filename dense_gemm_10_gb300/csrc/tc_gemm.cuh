@@ -1,0 +1,443 @@
+// tc_gemm.cuh -- persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+//   D (I x J) = P (I x K) * Q (K x J);   C[i*c_si + j*c_sj] = alpha * D[i][j] + beta * C[...]
+//
+// Design, and the page sections each part restates:
+//  * A persistent grid: one CTA per SM walks a static list of work units in a
+//    grouped (swizzled) raster order so that CTAs running together share rows
+//    of P and columns of Q in L2 ("CUDA GEMM 矩阵乘法优化指南", 12.5 Persistent
+//    Kernel; "GPU GEMM 优化完全拆解（三）", rasterization).
+//  * Warp specialisation: warp 0 issues TMA copies into a multi-stage shared
+//    memory ring guarded by full / empty mbarriers, warp 1 issues tcgen05.mma
+//    from one thread, warps 2-5 run the epilogue ("GPU GEMM 优化完全拆解（三）",
+//    warp specialization; "CUDA GEMM 矩阵乘法优化指南", 12.4 and 13.2).
+//  * Tiles arrive 128-byte swizzled ("[CUDA 优化实战] hgemm sm120", section 4:
+//    the swizzle of 16-bit element (r, c) in a 64-wide row is c ^ ((r & 7) << 3)),
+//    which is the layout the tensor core's shared-memory descriptor expects.
+//  * The fp32 accumulator lives in Tensor Memory, double-buffered so that the
+//    epilogue of one tile overlaps the main loop of the next (the ping-pong idea
+//    of "GPU GEMM 优化完全拆解（三）", Hopper 时代的三种 kernel 设计).
+//  * Split-K: a work unit may cover only a k-range of a tile; its fp32 partial
+//    goes to a workspace and the last unit of the tile to arrive sums all
+//    partials in fixed split order, so the result is deterministic
+//    ("GPU GEMM 优化完全拆解（三）", Split-K 与 Sliced-K).
+//  * Every barrier wait is bounded by a wall-clock limit; a wait that runs out
+//    records the role and barrier in the status word, raises a CTA-wide abort
+//    flag, and every role then leaves its loop.  Before the CTA exits, the
+//    producer waits for each of its copies in flight and the MMA thread for its
+//    last MMAs, and Tensor Memory is always freed.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "gemm_internal.h"
+#include "ptx.cuh"
+
+namespace g10 {
+
+template <int BN>
+struct TcConfig {
+  static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
+  static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int kABytes = kBM * kBK * 2;  // one P tile: 128 rows x 128 bytes
+  static constexpr int kBBytes = BN * kBK * 2;   // one Q tile
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kTmemCols = 2 * BN;       // two fp32 accumulators of BN columns
+  static constexpr int kCtrlBytes = 256;
+  static constexpr size_t kSmemBytes = 1024 + kRingBytes + kCtrlBytes;  // + alignment slack
+};
+
+struct TcCtrl {
+  uint64_t full[8];
+  uint64_t empty[8];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  uint32_t abort;
+  uint32_t last;
+};
+static_assert(sizeof(TcCtrl) <= 256, "control block");
+
+// Swizzle atoms of an MN-major operand: 64 elements along M or N (128 bytes)
+// by 64 k-rows; atoms follow each other along M / N.
+constexpr uint32_t kMnAtomBytes = 64 * 128;
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, TcCtrl* ctrl,
+                                             const TcArgs& a, int role, int which,
+                                             bool honor_abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  volatile uint32_t* abort_flag = &ctrl->abort;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (honor_abort && *abort_flag) return false;
+    if (global_timer_ns() - t0 > a.wait_limit_ns) {
+      *abort_flag = 1u;
+      atomicCAS(a.status, 0, kStatusTimeout | (role << 8) | (which << 12));
+      return false;
+    }
+  }
+}
+
+struct Unit {
+  int ti, tj, tile, kb0, kb1;
+};
+
+// Work unit u -> output tile (grouped raster: raster_group tile rows at a time,
+// walking down the rows of a group before moving to the next column) and k-range.
+__device__ __forceinline__ Unit decode_unit(const TcArgs& a, int u) {
+  Unit w;
+  w.tile = u / a.split_k;
+  const int s = u - w.tile * a.split_k;
+  const int group_tiles = a.raster_group * a.tiles_j;
+  const int g = w.tile / group_tiles;
+  const int first_i = g * a.raster_group;
+  const int rows = min(a.tiles_i - first_i, a.raster_group);
+  const int r = w.tile - g * group_tiles;
+  w.ti = first_i + r % rows;
+  w.tj = r / rows;
+  w.kb0 = static_cast<int>((static_cast<int64_t>(s) * a.num_kb) / a.split_k);
+  w.kb1 = static_cast<int>((static_cast<int64_t>(s + 1) * a.num_kb) / a.split_k);
+  return w;
+}
+
+// ------------------------------------------------------------------ epilogue --
+
+__device__ __forceinline__ float load_c(const TcArgs& a, int64_t off) {
+  if (a.c_type == kCF32) return static_cast<const float*>(a.C)[off];
+  if (a.c_type == kCBF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(a.C)[off]);
+  return __half2float(static_cast<const __half*>(a.C)[off]);
+}
+
+__device__ __forceinline__ void store_c(const TcArgs& a, int64_t off, float v) {
+  if (a.c_type == kCF32)
+    static_cast<float*>(a.C)[off] = v;
+  else if (a.c_type == kCBF16)
+    static_cast<__nv_bfloat16*>(a.C)[off] = __float2bfloat16_rn(v);
+  else
+    static_cast<__half*>(a.C)[off] = __float2half_rn(v);
+}
+
+__device__ __forceinline__ uint32_t pack2(const TcArgs& a, float lo, float hi) {
+  if (a.c_type == kCBF16) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&p);
+  }
+  __half2 p = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+__device__ __forceinline__ float2 unpack2(const TcArgs& a, uint32_t bits) {
+  if (a.c_type == kCBF16) return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&bits));
+  return __half22float2(*reinterpret_cast<__half2*>(&bits));
+}
+
+// Write alpha * v + beta * C for row i, columns j0 .. j0 + 31 of D.
+__device__ __forceinline__ void store_chunk(const TcArgs& a, int i, int j0, float (&v)[32]) {
+  if (i >= a.I) return;
+  const bool blend = a.beta != 0.0f;
+  if (a.vec_store && j0 + 32 <= a.J) {
+    const int64_t base = static_cast<int64_t>(i) * a.c_si + j0;
+    if (a.c_type == kCF32) {
+      float4* p = reinterpret_cast<float4*>(static_cast<float*>(a.C) + base);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float4 o = make_float4(a.alpha * v[4 * q], a.alpha * v[4 * q + 1], a.alpha * v[4 * q + 2],
+                               a.alpha * v[4 * q + 3]);
+        if (blend) {
+          const float4 c = p[q];
+          o.x += a.beta * c.x; o.y += a.beta * c.y; o.z += a.beta * c.z; o.w += a.beta * c.w;
+        }
+        p[q] = o;
+      }
+    } else {
+      uint4* p = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.C) + base);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float o[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) o[t] = a.alpha * v[8 * q + t];
+        if (blend) {
+          const uint4 c = p[q];
+          const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const float2 f = unpack2(a, cw[t]);
+            o[2 * t] += a.beta * f.x;
+            o[2 * t + 1] += a.beta * f.y;
+          }
+        }
+        p[q] = make_uint4(pack2(a, o[0], o[1]), pack2(a, o[2], o[3]), pack2(a, o[4], o[5]),
+                          pack2(a, o[6], o[7]));
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int t = 0; t < 32; ++t) {
+    const int j = j0 + t;
+    if (j < a.J) {
+      const int64_t off = static_cast<int64_t>(i) * a.c_si + static_cast<int64_t>(j) * a.c_sj;
+      float o = a.alpha * v[t];
+      if (blend) o += a.beta * load_c(a, off);
+      store_c(a, off, o);
+    }
+  }
+}
+
+// ----------------------------------------------------------------- the roles --
+
+template <int BN>
+__device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CUtensorMap* map_q,
+                                              const TcArgs& a, uint8_t* ring_a, uint8_t* ring_b,
+                                              TcCtrl* ctrl) {
+  using Cfg = TcConfig<BN>;
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t pending = 0, pending_parity = 0;  // copies in flight, per stage
+  int nload = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
+    const Unit w = decode_unit(a, u);
+    const int i0 = w.ti * kBM;
+    const int j0 = w.tj * BN;
+    for (int kb = w.kb0; kb < w.kb1; ++kb) {
+      if (!wait_bounded(smem_u32(&ctrl->empty[stage]), phase ^ 1u, ctrl, a, kRoleProducer,
+                        kBarEmpty, true)) {
+        ok = false;
+        break;
+      }
+      ++nload;
+      const uint32_t full = smem_u32(&ctrl->full[stage]);
+      if (a.drop_load != 0 && blockIdx.x == 0 && nload == a.drop_load) {
+        pending &= ~(1u << stage);  // test hook: this stage's barrier is never completed
+      } else {
+        mbar_arrive_expect_tx(full, Cfg::kStageBytes);
+        const uint32_t sa = smem_u32(ring_a + stage * Cfg::kABytes);
+        const uint32_t sb = smem_u32(ring_b + stage * Cfg::kBBytes);
+        const int k0 = kb * kBK;
+        if (a.p_kmajor) {
+          tma_load_2d(sa, map_p, full, k0, i0);
+        } else {
+          tma_load_2d(sa, map_p, full, i0, k0);
+          tma_load_2d(sa + kMnAtomBytes, map_p, full, i0 + 64, k0);
+        }
+        if (a.q_kmajor) {
+          tma_load_2d(sb, map_q, full, k0, j0);
+        } else {
+#pragma unroll
+          for (int c = 0; c < BN / 64; ++c)
+            tma_load_2d(sb + c * kMnAtomBytes, map_q, full, j0 + 64 * c, k0);
+        }
+        pending |= 1u << stage;
+        pending_parity = (pending_parity & ~(1u << stage)) | (phase << stage);
+      }
+      if (++stage == Cfg::kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  // No copy may still be writing shared memory when the CTA exits.
+  for (int s = 0; s < Cfg::kStages; ++s)
+    if (pending & (1u << s))
+      wait_bounded(smem_u32(&ctrl->full[s]), (pending_parity >> s) & 1u, ctrl, a, kRoleProducer,
+                   kBarDrain, false);
+}
+
+template <int BN>
+__device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8_t* ring_b,
+                                         TcCtrl* ctrl, uint32_t tmem_base) {
+  using Cfg = TcConfig<BN>;
+  int stage = 0;
+  uint32_t phase = 0;
+  int it = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x, ++it) {
+    const Unit w = decode_unit(a, u);
+    const int buf = it & 1;
+    const uint32_t acc_parity = (it >> 1) & 1;
+    if (!wait_bounded(smem_u32(&ctrl->acc_empty[buf]), acc_parity ^ 1u, ctrl, a, kRoleMma,
+                      kBarAccEmpty, true))
+      break;
+    tc_fence_after_sync();
+    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+    for (int kb = w.kb0; kb < w.kb1; ++kb) {
+      if (!wait_bounded(smem_u32(&ctrl->full[stage]), phase, ctrl, a, kRoleMma, kBarFull, true)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t sa = smem_u32(ring_a + stage * Cfg::kABytes);
+      const uint32_t sb = smem_u32(ring_b + stage * Cfg::kBBytes);
+#pragma unroll
+      for (int k = 0; k < kBK / 16; ++k) {
+        // K-major: the 16-wide k-slice starts 32 bytes further along each swizzled
+        // 128-byte row; 8-row groups are 1024 bytes apart.
+        // MN-major: the k-slice is 16 rows of 128 bytes further on; 8-row groups are
+        // 1024 bytes apart and swizzle atoms along M / N are kMnAtomBytes apart.
+        const uint64_t ad = a.p_kmajor ? smem_desc_sw128(sa + 32 * k, 16, 1024)
+                                       : smem_desc_sw128(sa + 2048 * k, kMnAtomBytes, 1024);
+        const uint64_t bd = a.q_kmajor ? smem_desc_sw128(sb + 32 * k, 16, 1024)
+                                       : smem_desc_sw128(sb + 2048 * k, kMnAtomBytes, 1024);
+        mma_f16_ss(d_tmem, ad, bd, a.idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
+      }
+      mma_commit(smem_u32(&ctrl->empty[stage]));  // frees the stage once these MMAs have read it
+      if (++stage == Cfg::kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok) break;
+    mma_commit(smem_u32(&ctrl->acc_full[buf]));  // accumulator ready for the epilogue
+  }
+  // Tensor Memory is freed only after every MMA issued here has finished.
+  mma_commit(smem_u32(&ctrl->mma_done));
+  wait_bounded(smem_u32(&ctrl->mma_done), 0, ctrl, a, kRoleMma, kBarDrain, false);
+}
+
+template <int BN>
+__device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uint32_t tmem_base,
+                                              int warp, int lane) {
+  const int quarter = warp & 3;  // a warp may only read TMEM lanes 32*(warp%4) .. +31
+  const int row = quarter * 32 + lane;
+  const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+  int it = 0;
+  for (int u = blockIdx.x; u < a.units; u += gridDim.x, ++it) {
+    const Unit w = decode_unit(a, u);
+    const int buf = it & 1;
+    const uint32_t acc_parity = (it >> 1) & 1;
+    const bool ok = wait_bounded(smem_u32(&ctrl->acc_full[buf]), acc_parity, ctrl, a,
+                                 kRoleEpilogue, kBarAccFull, true);
+    if (bar_any(1, 128, !ok)) return;  // all four epilogue warps leave together
+    tc_fence_after_sync();
+    const uint32_t taddr = lane_base + static_cast<uint32_t>(buf * BN);
+    const uint32_t acc_empty = smem_u32(&ctrl->acc_empty[buf]);
+    const int i = w.ti * kBM + row;
+    if (a.split_k == 1) {
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + c, r);
+        tmem_ld_wait(r);
+        if (c + 32 == BN) {  // last read of this accumulator: hand it back to the MMA warp
+          tc_fence_before_sync();
+          mbar_arrive(acc_empty);
+        }
+        float v[32];
+#pragma unroll
+        for (int t = 0; t < 32; ++t) v[t] = __uint_as_float(r[t]);
+        store_chunk(a, i, w.tj * BN + c, v);
+      }
+    } else {
+      // Partial of this k-range: column-major inside the tile so that a warp's
+      // 32 rows are 128 contiguous bytes.
+      float* part = a.partials + static_cast<size_t>(u) * BN * kBM;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + c, r);
+        tmem_ld_wait(r);
+        if (c + 32 == BN) {
+          tc_fence_before_sync();
+          mbar_arrive(acc_empty);
+        }
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          __stcg(part + static_cast<size_t>(c + t) * kBM + row, __uint_as_float(r[t]));
+      }
+      __threadfence();
+      bar_sync(1, 128);
+      if (threadIdx.x == 64) {
+        const int old = atomicAdd(&a.counters[w.tile], 1);
+        const uint32_t last = (old == a.split_k - 1) ? 1u : 0u;
+        if (last) atomicExch(&a.counters[w.tile], 0);  // clean for the next call
+        *reinterpret_cast<volatile uint32_t*>(&ctrl->last) = last;
+      }
+      bar_sync(1, 128);
+      if (*reinterpret_cast<volatile uint32_t*>(&ctrl->last)) {
+        __threadfence();
+        const float* base = a.partials + static_cast<size_t>(w.tile) * a.split_k * BN * kBM;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+#pragma unroll
+          for (int t = 0; t < 32; ++t) v[t] = 0.0f;
+#pragma unroll 1
+          for (int s = 0; s < a.split_k; ++s) {
+            const float* ps = base + static_cast<size_t>(s) * BN * kBM;
+#pragma unroll
+            for (int t = 0; t < 32; ++t) v[t] += __ldcg(ps + static_cast<size_t>(c + t) * kBM + row);
+          }
+          store_chunk(a, i, w.tj * BN + c, v);
+        }
+      }
+    }
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p,
+                   const __grid_constant__ CUtensorMap map_q, const TcArgs a) {
+  using Cfg = TcConfig<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  // 128-byte swizzle atoms need 1024-byte aligned tiles.
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  uint8_t* ring_a = smem;
+  uint8_t* ring_b = smem + Cfg::kStages * Cfg::kABytes;
+  TcCtrl* ctrl = reinterpret_cast<TcCtrl*>(smem + Cfg::kRingBytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::kStages; ++s) {
+      mbar_init(smem_u32(&ctrl->full[s]), 1);
+      mbar_init(smem_u32(&ctrl->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&ctrl->acc_full[b]), 1);
+      mbar_init(smem_u32(&ctrl->acc_empty[b]), 128);
+    }
+    mbar_init(smem_u32(&ctrl->mma_done), 1);
+    ctrl->abort = 0;
+    ctrl->last = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&map_p);
+    prefetch_tensormap(&map_q);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctrl->tmem_base), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = ctrl->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) producer_role<BN>(&map_p, &map_q, a, ring_a, ring_b, ctrl);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) mma_role<BN>(a, ring_a, ring_b, ctrl, tmem_base);
+    __syncwarp();
+  } else {
+    epilogue_role<BN>(a, ctrl, tmem_base, warp, lane);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+}  // namespace g10

@@ -1,0 +1,205 @@
+"""Thin ctypes binding of include/gemm_gb300.h (argument marshalling only).
+
+Every step of the GEMM runs in the CUDA library; this module only turns
+tensors into pointers, sizes and leading dimensions.  There is no fallback: if
+the library has not been built, every call raises.
+"""
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libgemm_gb300.so")
+
+OP_N, OP_T = 0, 1
+BF16_F32, BF16_BF16, F16_F32, F16_F16 = 0, 1, 2, 3
+STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED", 3: "GEMM_ERR_NO_DEVICE",
+          4: "GEMM_ERR_CUDA", 5: "GEMM_ERR_TENSORMAP", 6: "GEMM_ERR_TIMEOUT", 7: "GEMM_ERR_WORKSPACE"}
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NO_DEVICE, ERR_CUDA, ERR_TENSORMAP, ERR_TIMEOUT, ERR_WORKSPACE = range(8)
+PATH_NOOP, PATH_SCALE_C, PATH_TC_1CTA, PATH_TC_2CTA = 0, 1, 2, 3
+OPT_WAIT_LIMIT_NS, OPT_FORCE_PATH, OPT_SPLIT_K, OPT_RASTER_GROUP, OPT_FORCE_BN, OPT_TEST_DROP_LOAD = range(6)
+
+# Exported functions and their (restype, argtypes).
+_i32, _i64, _u64, _f32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [(n, _i32) for n in ("path", "swap_ab", "a_kmajor", "b_kmajor", "bm", "bn", "bk", "stages",
+                                    "split_k", "raster_group", "repack_a", "repack_b", "vector_store",
+                                    "grid", "launches", "reserved")] + \
+               [(n, _i64) for n in ("tiles", "units", "workspace_bytes")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_ if n != "reserved"}
+
+
+SIGNATURES = {
+    "gemm_create": (_i32, [ctypes.POINTER(_vp), ctypes.c_int]),
+    "gemm_run": (_i32, [_vp, _i32, _i32, _i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64,
+                        _i32, _vp]),
+    "gemm_get_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
+    "gemm_status_string": (ctypes.c_char_p, [_i32]),
+    "gemm_last_cuda_error": (ctypes.c_int, [_vp]),
+    "gemm_destroy": (_i32, [_vp]),
+    "gemm_plan": (_i32, [_vp, ctypes.c_int, _i32, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _f32, _vp,
+                         _i64, _i32, ctypes.POINTER(Plan)]),
+    "gemm_set_option": (_i32, [_vp, _i32, _i64]),
+    "gemm_launch_count": (_i32, [_vp, ctypes.POINTER(_u64)]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        super().__init__("%s: %s" % (what or "gemm", STATUS.get(status, str(status))))
+
+
+def lib():
+    """The loaded CUDA library.  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError("the GEMM CUDA library is not built (%s missing); run "
+                                   "dense_gemm_10_gb300.build.build()" % LIB_PATH)
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(L, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = L
+        return _lib
+
+
+def _check(status, what):
+    if status != OK:
+        raise GemmError(status, what)
+
+
+def plan(M, N, K, transA=0, transB=0, dtype=BF16_F32, lda=None, ldb=None, ldc=None, sm_count=152,
+         A=0x1000, B=0x1000, C=0x1000, beta=0.0, handle=None):
+    """Host-only planner query (no GPU needed); pointers matter only for alignment."""
+    lda = lda if lda is not None else (M if transA else K)
+    ldb = ldb if ldb is not None else (K if transB else N)
+    ldc = ldc if ldc is not None else N
+    p = Plan()
+    h = handle.ptr if handle is not None else None
+    st = lib().gemm_plan(h, sm_count, transA, transB, M, N, K, A, lda, B, ldb, beta, C, ldc, dtype,
+                         ctypes.byref(p))
+    _check(st, "gemm_plan")
+    return p
+
+
+class Handle:
+    """A library handle bound to one CUDA device."""
+
+    def __init__(self, device=0):
+        h = _vp()
+        _check(lib().gemm_create(ctypes.byref(h), int(device)), "gemm_create")
+        self.ptr = h.value
+        self.device = int(device)
+
+    def close(self):
+        if self.ptr:
+            lib().gemm_destroy(self.ptr)
+            self.ptr = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set_option(self, opt, value):
+        _check(lib().gemm_set_option(self.ptr, opt, int(value)), "gemm_set_option")
+
+    def launch_count(self):
+        n = _u64()
+        _check(lib().gemm_launch_count(self.ptr, ctypes.byref(n)), "gemm_launch_count")
+        return n.value
+
+    def status(self, stream=None):
+        """Synchronise `stream` and return (status code, raw status word)."""
+        d = _i32()
+        st = lib().gemm_get_status(self.ptr, stream, ctypes.byref(d))
+        return st, d.value
+
+    def run_raw(self, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtype, stream):
+        """gemm_run on raw device pointers; returns the status code (no raise)."""
+        return lib().gemm_run(self.ptr, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                              dtype, stream)
+
+
+_default = {}
+
+
+def default_handle(device=None):
+    import torch
+    dev = torch.cuda.current_device() if device is None else int(device)
+    h = _default.get(dev)
+    if h is None:
+        h = _default[dev] = Handle(dev)
+    return h
+
+
+def dtype_code(in_dtype, out_dtype):
+    import torch
+    table = {(torch.bfloat16, torch.float32): BF16_F32, (torch.bfloat16, torch.bfloat16): BF16_BF16,
+             (torch.float16, torch.float32): F16_F32, (torch.float16, torch.float16): F16_F16}
+    if (in_dtype, out_dtype) not in table:
+        raise TypeError("unsupported dtype pair %s -> %s" % (in_dtype, out_dtype))
+    return table[(in_dtype, out_dtype)]
+
+
+def _ld(t, name):
+    if t.dim() != 2 or (t.stride(1) != 1 and t.shape[1] > 1):
+        raise ValueError("%s must be a 2-D row-major tensor (unit column stride)" % name)
+    return t.stride(0) if t.shape[0] > 1 else max(t.stride(0), t.shape[1], 1)
+
+
+def gemm(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0, handle=None, stream=None, M=None,
+         N=None, K=None):
+    """C = alpha * op(A) * op(B) + beta * C on CUDA tensors, enqueued on `stream`
+    (default: torch's current stream).  A and B are stored row-major as
+    (M, K) / (K, M) and (K, N) / (N, K) per transA / transB; C is (M, N).
+    Sizes default to the logical extents of the tensors."""
+    import torch
+    for t, n in ((A, "A"), (B, "B"), (C, "C")):
+        if not t.is_cuda:
+            raise ValueError("%s must be a CUDA tensor" % n)
+    ta, tb = int(bool(transA)), int(bool(transB))
+    M = M if M is not None else (A.shape[1] if ta else A.shape[0])
+    K = K if K is not None else (A.shape[0] if ta else A.shape[1])
+    N = N if N is not None else (B.shape[0] if tb else B.shape[1])
+    if A.dtype != B.dtype:
+        raise TypeError("A and B must have the same dtype")
+    code = dtype_code(A.dtype, C.dtype)
+    h = handle if handle is not None else default_handle(C.device.index)
+    if stream is None:
+        stream = torch.cuda.current_stream(C.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    st = h.run_raw(ta, tb, M, N, K, float(alpha), A.data_ptr(), _ld(A, "A"), B.data_ptr(), _ld(B, "B"),
+                   float(beta), C.data_ptr(), _ld(C, "C"), code, stream)
+    _check(st, "gemm_run")
+    return C
+
+
+def gemm_host(A_host, B_host, C_host, A_dev, B_dev, C_dev, transA=False, transB=False, alpha=1.0,
+              beta=0.0, handle=None, stream=None):
+    """End-to-end call on host buffers: copy A, B (and C when beta != 0) from
+    pinned host memory to the device, run the GEMM, copy C back, all enqueued
+    on one stream.  The device tensors are caller-provided staging buffers."""
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream(C_dev.device)
+    with torch.cuda.stream(s):
+        A_dev.copy_(A_host, non_blocking=True)
+        B_dev.copy_(B_host, non_blocking=True)
+        if beta != 0.0:
+            C_dev.copy_(C_host, non_blocking=True)
+        gemm(A_dev, B_dev, C_dev, transA, transB, alpha, beta, handle=handle, stream=s.cuda_stream)
+        C_host.copy_(C_dev, non_blocking=True)
+    return C_host

@@ -1,0 +1,195 @@
+/*
+ * gemm_gb300.h -- C ABI of a GB300 (sm_103a) dense GEMM library.
+ *
+ * The operation (all entry points):
+ *   C = alpha * op(A) * op(B) + beta * C
+ * with op(A) of size M x K, op(B) of size K x N and C of size M x N; 2*M*N*K
+ * floating-point operations.  This is the GEMM of "CUDA GEMM 矩阵乘法优化指南"
+ * (blog.zhenwei.site), section 2.1, with the op / alpha / beta calling shape of
+ * the cuBLAS call in "第4章：经典算子实现 —— GEMM" (aiinfra.vidrealm.tech),
+ * section 7.1.  Inputs are bf16 or fp16, products are accumulated in fp32 on
+ * the tensor cores (tcgen05.mma into Tensor Memory), and alpha / beta are
+ * applied in fp32 before the result is rounded (round-to-nearest-even) to the
+ * type of C.
+ *
+ * Storage is row-major (the C / PyTorch convention):
+ *   transA == GEMM_OP_N : A is stored M x K, element (i, k) at A[i * lda + k], lda >= K
+ *   transA == GEMM_OP_T : A is stored K x M, element (i, k) at A[k * lda + i], lda >= M
+ *   transB == GEMM_OP_N : B is stored K x N, element (k, j) at B[k * ldb + j], ldb >= N
+ *   transB == GEMM_OP_T : B is stored N x K, element (k, j) at B[j * ldb + k], ldb >= K
+ *   C is M x N, element (i, j) at C[i * ldc + j], ldc >= N.
+ * So "A row-major, B column-major" is (GEMM_OP_N, GEMM_OP_T), the NT layout.
+ *
+ * Every entry point returns a gemm_status_t and never throws.  No call here
+ * allocates or frees the caller's A, B or C.
+ */
+#ifndef GEMM_GB300_H
+#define GEMM_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque library handle, bound to one CUDA device. */
+typedef struct gemm_handle_s* gemm_handle_t;
+
+typedef enum { GEMM_OP_N = 0, GEMM_OP_T = 1 } gemm_op_t;
+
+/* Input type -> type of C.  Accumulation is fp32 in every case. */
+typedef enum {
+  GEMM_BF16_F32 = 0,  /* A, B bf16; C fp32 */
+  GEMM_BF16_BF16 = 1, /* A, B bf16; C bf16 */
+  GEMM_F16_F32 = 2,   /* A, B fp16; C fp32 */
+  GEMM_F16_F16 = 3    /* A, B fp16; C fp16 */
+} gemm_dtype_t;
+
+typedef enum {
+  GEMM_OK = 0,
+  GEMM_ERR_INVALID_ARG = 1, /* null pointer, negative size, leading dimension too small, bad enum */
+  GEMM_ERR_UNSUPPORTED = 2, /* a size the library cannot index (an extent >= 2^31) */
+  GEMM_ERR_NO_DEVICE = 3,   /* the device is absent or is not sm_103 */
+  GEMM_ERR_CUDA = 4,        /* a CUDA runtime call failed; gemm_last_cuda_error() tells which */
+  GEMM_ERR_TENSORMAP = 5,   /* cuTensorMapEncodeTiled refused an operand description */
+  GEMM_ERR_TIMEOUT = 6,     /* a kernel gave up waiting on one of its barriers (see gemm_get_status) */
+  GEMM_ERR_WORKSPACE = 7    /* the handle could not grow its device workspace */
+} gemm_status_t;
+
+/*
+ * gemm_create: make a handle for CUDA device `device` (the ordinal).
+ * Allocates the handle's device status word and tile counters on that
+ * device.  *out is set to NULL on failure.  Errors: GEMM_ERR_INVALID_ARG (out
+ * is NULL), GEMM_ERR_NO_DEVICE, GEMM_ERR_CUDA.
+ */
+gemm_status_t gemm_create(gemm_handle_t* out, int device);
+
+/*
+ * gemm_run: enqueue C = alpha * op(A) * op(B) + beta * C on `stream`
+ * (a cudaStream_t; NULL is the legacy default stream).  Asynchronous: it
+ * returns once the kernels are launched and never synchronises.
+ *
+ *   transA, transB  GEMM_OP_N / GEMM_OP_T, layouts above.
+ *   M, N, K         sizes, >= 0.  M == 0 or N == 0 is a no-op returning GEMM_OK.
+ *                   K == 0 sets C = beta * C (C = 0 when beta == 0).
+ *   alpha, beta     fp32 scalars, read on the host.  When beta == 0, C is not
+ *                   read, so C may hold anything (NaN included) on entry.
+ *   A, B, C         caller-owned device pointers, bf16 / fp16 / fp32 per `dtype`.
+ *                   A and B are read only; C is read (beta != 0) and written.
+ *                   C must not overlap A or B.
+ *   lda, ldb, ldc   leading dimensions in elements, per the layouts above.
+ *   dtype           gemm_dtype_t.
+ *
+ * Operands whose base address is not 16-byte aligned, or whose row pitch in
+ * bytes is not a multiple of 16, are first copied by a device kernel into an
+ * aligned buffer owned by the handle (the tensor-memory-accelerator copy
+ * engine reads only 16-byte aligned rows); a C with such a pitch is written by
+ * the scalar-store epilogue.  The handle's workspace grows on demand with
+ * cudaMalloc (synchronous), so the first call of a new shape may block.
+ *
+ * The handle's workspace is shared by all calls on it: do not run one handle
+ * on two streams at once.  Errors are returned synchronously for bad
+ * arguments and failed launches; a kernel that times out on a barrier is
+ * reported later by gemm_get_status.
+ */
+gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int64_t M, int64_t N,
+                       int64_t K, float alpha, const void* A, int64_t lda, const void* B,
+                       int64_t ldb, float beta, void* C, int64_t ldc, gemm_dtype_t dtype,
+                       void* stream);
+
+/*
+ * gemm_get_status: synchronise `stream`, then read and clear the handle's
+ * device status word.  Returns GEMM_OK, GEMM_ERR_TIMEOUT (a kernel waited
+ * longer than the wait limit on one of its barriers and returned early; C is
+ * then incomplete) or GEMM_ERR_CUDA (the synchronisation itself failed).
+ * *detail (may be NULL) receives the raw status word: 0, or the role and
+ * barrier that gave up (see gemm_status_string for the code only).
+ */
+gemm_status_t gemm_get_status(gemm_handle_t h, void* stream, int32_t* detail);
+
+/* A static, human-readable string for a status code. */
+const char* gemm_status_string(gemm_status_t s);
+
+/* The last CUDA error code (cudaError_t as int) the handle saw, 0 if none. */
+int gemm_last_cuda_error(gemm_handle_t h);
+
+/*
+ * gemm_destroy: free the handle and its device memory.  Synchronises the
+ * device first.  Passing NULL is a no-op returning GEMM_OK.
+ */
+gemm_status_t gemm_destroy(gemm_handle_t h);
+
+/* ---------------------------------------------------------------------------
+ * Planning and tuning.
+ *
+ * The planner maps a call to one kernel configuration: the operands' major
+ * modes, the output tile, the k-split for shapes with too few tiles to fill
+ * the GPU, and whether the operands must be swapped (C^T = op(B)^T op(A)^T)
+ * so that a short M rides on the MMA's N dimension.  These choices follow the
+ * tiling, split-K and rasterisation designs of "GPU GEMM 优化完全拆解（三）"
+ * (pinghaoyang.com.cn), sections "双缓冲的两个 scope、rasterization 与 Split-K"
+ * and "Hopper 时代的三种 kernel 设计".
+ * ------------------------------------------------------------------------- */
+
+typedef enum {
+  GEMM_PATH_NOOP = 0,      /* M == 0 or N == 0 */
+  GEMM_PATH_SCALE_C = 1,   /* K == 0: C = beta * C */
+  GEMM_PATH_TC_1CTA = 2,   /* persistent tcgen05 kernel, one CTA per output tile (cta_group::1) */
+  GEMM_PATH_TC_2CTA = 3    /* persistent tcgen05 kernel, CTA pairs share a 256-row tile (cta_group::2) */
+} gemm_path_t;
+
+typedef struct {
+  int32_t path;            /* gemm_path_t */
+  int32_t swap_ab;         /* 1: the kernel computes C^T = op(B)^T * op(A)^T */
+  int32_t a_kmajor;        /* MMA A operand (rows of the MMA) has K contiguous */
+  int32_t b_kmajor;        /* MMA B operand (columns of the MMA) has K contiguous */
+  int32_t bm, bn, bk;      /* output tile of one CTA (bm x bn) and k-block depth */
+  int32_t stages;          /* shared-memory ring depth */
+  int32_t split_k;         /* k-splits per output tile (1 = none) */
+  int32_t raster_group;    /* tile rows per raster group */
+  int32_t repack_a;        /* A copied to an aligned workspace first */
+  int32_t repack_b;        /* B copied to an aligned workspace first */
+  int32_t vector_store;    /* epilogue writes C rows with 16-byte stores */
+  int32_t grid;            /* CTAs launched for the main kernel */
+  int32_t launches;        /* kernels launched by one gemm_run */
+  int32_t reserved;
+  int64_t tiles;           /* output tiles */
+  int64_t units;           /* work units = tiles * split_k */
+  int64_t workspace_bytes; /* handle workspace this call needs */
+} gemm_plan_t;
+
+/*
+ * gemm_plan: the configuration gemm_run would use for these arguments on a GPU
+ * with `sm_count` SMs, written to *plan.  Host-only: touches no device, so it
+ * can be called without a GPU.  `h` may be NULL (default options) or a handle
+ * whose options (gemm_set_option) then apply.  Pointers are used only for their
+ * alignment.  Returns the same argument errors as gemm_run.
+ */
+gemm_status_t gemm_plan(gemm_handle_t h, int sm_count, gemm_op_t transA, gemm_op_t transB,
+                        int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                        const void* B, int64_t ldb, float beta, const void* C, int64_t ldc,
+                        gemm_dtype_t dtype, gemm_plan_t* plan);
+
+typedef enum {
+  GEMM_OPT_WAIT_LIMIT_NS = 0, /* barrier wait limit in ns (default 2e9; >= 1e6) */
+  GEMM_OPT_FORCE_PATH = 1,    /* 0 auto, GEMM_PATH_TC_1CTA or GEMM_PATH_TC_2CTA */
+  GEMM_OPT_SPLIT_K = 2,       /* 0 auto, else the k-split to use (clamped to the k-blocks) */
+  GEMM_OPT_RASTER_GROUP = 3,  /* 0 auto, else tile rows per raster group */
+  GEMM_OPT_FORCE_BN = 4,      /* 0 auto, else 64, 128 or 256 */
+  GEMM_OPT_TEST_DROP_LOAD = 5 /* tests only: 0 off; n > 0 makes CTA 0 skip its n-th k-block
+                                 load, so a barrier is never completed and the bounded wait
+                                 must end the kernel with GEMM_ERR_TIMEOUT */
+} gemm_option_t;
+
+/* Set an option on a handle.  Errors: GEMM_ERR_INVALID_ARG for an unknown
+   option or an out-of-range value. */
+gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value);
+
+/* Kernels launched by gemm_run on this handle since it was created. */
+gemm_status_t gemm_launch_count(gemm_handle_t h, uint64_t* count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_GB300_H */

@@ -1,0 +1,156 @@
+"""The C ABI, without a GPU: the library loads, exports every entry point the
+header declares, refuses bad arguments, and plans calls as designed."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from dense_gemm_10_gb300 import build as gbuild
+from dense_gemm_10_gb300 import gemm as G
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gemm_gb300.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    gbuild.build()
+    return G.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(gemm_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("gemm_create", "gemm_run", "gemm_destroy", "gemm_get_status", "gemm_plan"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(G.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    # and the binding's signature table covers the header exactly
+    assert sorted(G.SIGNATURES) == declared_functions()
+
+
+def test_status_strings():
+    for code in range(8):
+        s = G.lib().gemm_status_string(code)
+        assert s and s != b"unknown status"
+    assert G.lib().gemm_status_string(99) == b"unknown status"
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour")
+def test_create_without_gpu_reports_no_device():
+    h = ctypes.c_void_p()
+    assert G.lib().gemm_create(ctypes.byref(h), 0) == G.ERR_NO_DEVICE
+    assert h.value is None
+    assert G.lib().gemm_create(None, 0) == G.ERR_INVALID_ARG
+
+
+def test_null_handle_is_rejected():
+    assert G.lib().gemm_run(None, 0, 0, 4, 4, 4, 1.0, 0x1000, 4, 0x1000, 4, 0.0, 0x1000, 4, 0, None) \
+        == G.ERR_INVALID_ARG
+    assert G.lib().gemm_destroy(None) == G.OK
+    assert G.lib().gemm_set_option(None, 0, 10**9) == G.ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(monkeypatch):
+    monkeypatch.setattr(G, "_lib", None)
+    monkeypatch.setattr(G, "LIB_PATH", "/nonexistent/libgemm_gb300.so")
+    with pytest.raises(RuntimeError, match="not built"):
+        G.lib()
+
+
+def test_product_code_never_touches_the_oracle():
+    pkg = os.path.join(ROOT, "dense_gemm_10_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp", ".c")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b|liboracle|oracle_gemm", text, flags=re.M), \
+                    os.path.join(dirpath, f)
+
+
+# ----------------------------------------------------------------- planner --
+
+def test_plan_square_nt():
+    p = G.plan(4096, 4096, 4096, 0, 1)
+    assert p.path == G.PATH_TC_1CTA and p.swap_ab == 0
+    assert p.a_kmajor == 1 and p.b_kmajor == 1
+    assert p.bm == 128 and p.bk == 64 and p.bn in (128, 256)
+    assert p.split_k == 1 and p.units == p.tiles == (4096 // 128) * (4096 // p.bn)
+    assert p.grid == 152 and p.repack_a == 0 and p.repack_b == 0
+    assert p.vector_store == 1 and p.launches == 1 and p.workspace_bytes == 0
+
+
+@pytest.mark.parametrize("ta,tb,ak,bk", [(0, 0, 1, 0), (0, 1, 1, 1), (1, 0, 0, 0), (1, 1, 0, 1)])
+def test_plan_major_modes(ta, tb, ak, bk):
+    p = G.plan(4096, 4096, 4096, ta, tb, G.F16_F32, beta=0.5)
+    assert (p.a_kmajor, p.b_kmajor) == (ak, bk)
+
+
+def test_plan_lm_head_swaps_and_splits():
+    p = G.plan(64, 32000, 4096, 0, 1)
+    assert p.swap_ab == 1
+    assert p.a_kmajor == 1 and p.b_kmajor == 1   # MMA A = weights (N x K), MMA B = activations (M x K)
+    assert p.bn == 64 and p.tiles == 250
+    assert p.split_k > 1 and p.units == 250 * p.split_k
+    assert p.workspace_bytes >= p.units * 64 * 128 * 4
+    assert p.vector_store == 0 and p.grid == 152
+
+
+def test_plan_ragged_repacks_misaligned_b():
+    p = G.plan(4095, 4097, 1000, 0, 0, lda=1000, ldb=4097, ldc=4097)
+    assert p.repack_a == 0 and p.repack_b == 1
+    assert p.launches == 2
+    assert p.vector_store == 0          # 4097 fp32 = 16388-byte rows
+    assert p.workspace_bytes >= 1000 * 4104 * 2
+
+
+def test_plan_misaligned_pointer_repacks():
+    p = G.plan(512, 512, 512, 0, 1, A=0x1002)
+    assert p.repack_a == 1 and p.repack_b == 0
+
+
+def test_plan_degenerate_sizes():
+    assert G.plan(0, 10, 10).path == G.PATH_NOOP
+    assert G.plan(10, 0, 10).path == G.PATH_NOOP
+    p = G.plan(10, 10, 0, lda=1)
+    assert p.path == G.PATH_SCALE_C and p.launches == 1
+
+
+@pytest.mark.parametrize("kw", [dict(M=-1, N=4, K=4), dict(M=4, N=4, K=8, lda=7), dict(M=4, N=4, K=8, ldb=3),
+                                dict(M=4, N=8, K=4, ldc=7), dict(M=4, N=4, K=4, dtype=9),
+                                dict(M=4, N=4, K=4, transA=2), dict(M=4, N=4, K=4, A=0)])
+def test_plan_rejects_bad_arguments(kw):
+    with pytest.raises(G.GemmError) as e:
+        G.plan(**kw)
+    assert e.value.status == G.ERR_INVALID_ARG
+
+
+def test_plan_rejects_oversized_extent():
+    with pytest.raises(G.GemmError) as e:
+        G.plan(1 << 31, 8, 8)
+    assert e.value.status == G.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("shape", [(256, 256, 256), (1, 1, 1), (300, 520, 200), (8192, 12288, 4096),
+                                   (8192, 4096, 16384), (33, 4000, 70), (4095, 4097, 1000)])
+def test_plan_invariants(shape):
+    M, N, K = shape
+    for sm in (148, 152, 160):
+        p = G.plan(M, N, K, 0, 0, sm_count=sm)
+        I, J = (N, M) if p.swap_ab else (M, N)
+        assert p.tiles == -(-I // p.bm) * -(-J // p.bn)
+        assert p.units == p.tiles * p.split_k
+        assert 1 <= p.split_k <= max(1, -(-K // 64))
+        assert p.grid == min(p.units, sm)
+        assert 1 <= p.raster_group <= max(1, -(-I // 128))

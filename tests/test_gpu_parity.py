@@ -1,0 +1,195 @@
+"""GPU parity against the CPU oracle, element by element, at sizes the oracle
+finishes in seconds: several tiles, ragged tails, every layout, both input
+types, every output type, alpha / beta, the swapped and split-K paths, and the
+degenerate sizes.  Every call goes through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+from dense_gemm_10_gb300 import gemm as G
+from dense_gemm_10_gb300 import inputs
+
+from gpu_util import SENTINEL, assert_close, device_problem, launch, oracle_full, run
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def h():
+    gh = G.Handle(0)
+    yield gh
+    gh.close()
+
+
+def _check(p, h, guard=True):
+    out, full = run(p, h, guard_rows=3 if guard else 0, guard_cols=5 if guard else 0)
+    R, Mag = oracle_full(p)
+    assert_close(out, R, Mag, p.out_dtype == "f32", p.name)
+    if guard:
+        # nothing outside the logical M x N block was written
+        pad = full.clone().to(torch.float64)
+        pad[:p.M, :p.N] = SENTINEL
+        assert torch.all(pad == SENTINEL), "C written outside the M x N block"
+    return out
+
+
+def test_tiny_256(h):
+    """M = N = K = 256, bf16 U[-1, 1], NN, fp32 C."""
+    _check(inputs.tiny_256(), h)
+
+
+@pytest.mark.parametrize("transA,transB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("in_dtype,out_dtype", [("bf16", "f32"), ("f16", "f32"), ("bf16", "bf16"), ("f16", "f16")])
+def test_layouts_and_types(h, transA, transB, in_dtype, out_dtype):
+    """Ragged in every dimension: 3 x 5 tiles with partial last tiles, K not a multiple of 64."""
+    p = inputs.make_problem("lay", 300, 520, 200, transA, transB, in_dtype, out_dtype, ("uniform", -1, 1),
+                            ("uniform", -1, 1), alpha=1.5, beta=0.5, seed=31)
+    _check(p, h)
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1), (1, 1, 70), (127, 129, 63), (128, 256, 64), (129, 257, 65),
+                                   (7, 300, 1000), (1000, 7, 130), (513, 1031, 16)])
+def test_ragged_shapes(h, shape):
+    M, N, K = shape
+    p = inputs.make_problem("rag", M, N, K, 0, 1, "bf16", "f32", ("normal", 0, 1), ("normal", 0, 1), seed=M + N + K)
+    _check(p, h)
+
+
+@pytest.mark.parametrize("transA,transB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_small_integers_bit_exact(h, transA, transB):
+    """Integers in {-4..4}: the fp32 result is exact whatever the order of the
+    sum, so the GPU must equal the oracle bit for bit."""
+    p = inputs.make_problem("ints", 384, 640, 1024, transA, transB, "bf16", "f32", ("ints", -4, 4), ("ints", -4, 4),
+                            alpha=1.5, beta=0.5, dist_c=("ints", -9, 9), seed=5)
+    out, _ = run(p, h)
+    R, _ = oracle_full(p)
+    assert np.array_equal(out, R)
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 2000, 4096), (16, 3000, 512), (64, 640, 130), (40, 1000, 1000)])
+def test_skinny_swapped_split(h, M, N, K):
+    """Short M: the planner swaps operands (C^T = B^T A^T) and splits K."""
+    p = inputs.make_problem("skinny", M, N, K, 0, 1, "bf16", "f32", ("normal", 0, 1), ("normal", 0, 0.02), seed=N)
+    plan = G.plan(M, N, K, 0, 1, sm_count=152)
+    assert plan.swap_ab == 1
+    _check(p, h)
+
+
+@pytest.mark.parametrize("split", [2, 3, 7])
+@pytest.mark.parametrize("bn", [64, 128, 256])
+def test_forced_split_k(h, split, bn):
+    p = inputs.make_problem("split", 256, 512, 960, 0, 0, "f16", "f32", ("uniform", -1, 1), ("uniform", -1, 1),
+                            alpha=-0.75, beta=1.25, seed=split * bn)
+    h.set_option(G.OPT_SPLIT_K, split)
+    h.set_option(G.OPT_FORCE_BN, bn)
+    try:
+        _check(p, h)
+    finally:
+        h.set_option(G.OPT_SPLIT_K, 0)
+        h.set_option(G.OPT_FORCE_BN, 0)
+
+
+@pytest.mark.parametrize("bn", [64, 128, 256])
+@pytest.mark.parametrize("transA,transB", [(0, 0), (1, 1)])
+def test_every_tile_width(h, bn, transA, transB):
+    p = inputs.make_problem("bn", 384, 768, 320, transA, transB, "bf16", "bf16", ("normal", 0, 1), ("normal", 0, 1),
+                            alpha=0.5, beta=-1.0, seed=bn + transA)
+    h.set_option(G.OPT_FORCE_BN, bn)
+    try:
+        _check(p, h)
+    finally:
+        h.set_option(G.OPT_FORCE_BN, 0)
+
+
+def test_misaligned_leading_dimensions(h):
+    """Row pitches that are not multiples of 16 bytes go through the repack and
+    scalar-store paths."""
+    p = inputs.make_problem("mis", 333, 517, 301, 0, 0, "bf16", "f32", ("normal", 0, 1), ("normal", 0, 1),
+                            alpha=1.0, beta=0.5, seed=77, lda=301, ldb=519, ldc=517)
+    plan = G.plan(p.M, p.N, p.K, 0, 0, lda=p.lda, ldb=p.ldb, ldc=p.ldc)
+    assert plan.repack_a == 1 and plan.repack_b == 1 and plan.vector_store == 0
+    _check(p, h)
+
+
+def test_misaligned_base_pointer(h):
+    p = inputs.make_problem("misptr", 200, 264, 136, 0, 1, "f16", "f32", ("normal", 0, 1), ("normal", 0, 1), seed=8)
+    Ad, Bd, Cd, ldc = device_problem(p)
+    # shift A by one element inside a larger buffer: base no longer 16-byte aligned
+    big = torch.empty(Ad.numel() + 8, dtype=Ad.dtype, device="cuda")
+    big[1:1 + Ad.numel()] = Ad.reshape(-1)
+    A_shift = big[1:1 + Ad.numel()]
+    st = h.run_raw(0, 1, p.M, p.N, p.K, 1.0, A_shift.data_ptr(), p.lda, Bd.data_ptr(), p.ldb, 0.0, Cd.data_ptr(),
+                   ldc, G.F16_F32, None)
+    assert st == G.OK
+    assert h.status()[0] == G.OK
+    R, Mag = oracle_full(p)
+    assert_close(Cd[:p.M, :p.N].double().cpu().numpy(), R, Mag, True, "misaligned base")
+
+
+def test_beta_zero_ignores_nan_c(h):
+    p = inputs.make_problem("nanc", 256, 384, 128, 0, 0, "bf16", "f32", seed=3)
+    out, _ = run(p, h)   # C starts as NaN
+    assert np.isfinite(out).all()
+
+
+def test_k_zero_scales_c(h):
+    M, N = 100, 77
+    for beta in (0.0, -2.0):
+        C = torch.randn(M, N, device="cuda")
+        ref = (beta * C).cpu() if beta != 0.0 else torch.zeros(M, N)
+        A = torch.empty(M, 1, dtype=torch.bfloat16, device="cuda")
+        B = torch.empty(1, N, dtype=torch.bfloat16, device="cuda")
+        assert h.run_raw(0, 0, M, N, 0, 1.0, A.data_ptr(), 1, B.data_ptr(), N, beta, C.data_ptr(), N,
+                         G.BF16_F32, None) == G.OK
+        assert h.status()[0] == G.OK
+        assert torch.equal(C.cpu(), ref)
+
+
+def test_empty_m_or_n_is_noop(h):
+    C = torch.full((4, 4), 7.0, device="cuda")
+    A = torch.zeros(4, 4, dtype=torch.bfloat16, device="cuda")
+    before = h.launch_count()
+    assert h.run_raw(0, 0, 0, 4, 4, 1.0, A.data_ptr(), 4, A.data_ptr(), 4, 0.0, C.data_ptr(), 4, G.BF16_F32, None) == G.OK
+    assert h.run_raw(0, 0, 4, 0, 4, 1.0, A.data_ptr(), 4, A.data_ptr(), 4, 0.0, C.data_ptr(), 4, G.BF16_F32, None) == G.OK
+    assert h.launch_count() == before
+    assert torch.all(C == 7.0)
+
+
+def test_bad_arguments_return_errors(h):
+    A = torch.zeros(8, 8, dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros(8, 8, device="cuda")
+    assert h.run_raw(0, 0, 8, 8, 8, 1.0, A.data_ptr(), 7, A.data_ptr(), 8, 0.0, C.data_ptr(), 8, 0, None) \
+        == G.ERR_INVALID_ARG
+    assert h.run_raw(0, 0, 8, 8, 8, 1.0, 0, 8, A.data_ptr(), 8, 0.0, C.data_ptr(), 8, 0, None) == G.ERR_INVALID_ARG
+    assert h.run_raw(0, 0, 8, 8, 8, 1.0, A.data_ptr(), 8, A.data_ptr(), 8, 0.0, C.data_ptr(), 8, 5, None) \
+        == G.ERR_INVALID_ARG
+
+
+def test_run_to_run_determinism(h):
+    """Same inputs, same bits, including the split-K fix-up (fixed summation order)."""
+    for (M, N, K) in [(512, 768, 640), (64, 4000, 4096)]:
+        p = inputs.make_problem("det", M, N, K, 0, 1, "bf16", "f32", ("normal", 0, 1), ("normal", 0, 1), seed=M)
+        a, _ = run(p, h)
+        b, _ = run(p, h)
+        assert np.array_equal(a, b)
+
+
+def test_torch_binding_matches_oracle(h):
+    """The tensor-level binding infers sizes and leading dimensions correctly."""
+    p = inputs.make_problem("bind", 200, 300, 100, 1, 0, "bf16", "bf16", ("normal", 0, 1), ("normal", 0, 1), seed=12)
+    A, B = p.A.cuda(), p.B.cuda()
+    C = torch.empty(200, 300, dtype=torch.bfloat16, device="cuda")
+    G.gemm(A, B, C, transA=True, transB=False, handle=h)
+    torch.cuda.synchronize()
+    R, Mag = oracle_full(p)
+    assert_close(C.double().cpu().numpy(), R, Mag, False, "binding")
+
+
+def test_launch_count_and_plan_agree(h):
+    p = inputs.make_problem("cnt", 333, 517, 301, 0, 0, "bf16", "f32", lda=301, ldb=519, ldc=517, seed=1)
+    plan = G.plan(p.M, p.N, p.K, 0, 0, lda=p.lda, ldb=p.ldb, ldc=p.ldc)
+    Ad, Bd, Cd, ldc = device_problem(p)
+    before = h.launch_count()
+    launch(p, h, Ad, Bd, Cd, ldc)
+    assert h.status()[0] == G.OK
+    assert h.launch_count() - before == plan.launches == 3
