@@ -36,6 +36,7 @@ struct Options {
   int raster_group = 0;
   int force_bn = 0;
   int drop_load = 0;
+  int max_grid = 0;
 };
 
 // One stored operand, as the tensor-memory-accelerator copy engine will see it.
@@ -66,15 +67,21 @@ bool tma_aligned(const void* p, int64_t ld) {
   return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((ld * 2) % 16 == 0);
 }
 
-// Heuristic cost of a configuration in "k-block of a 128 x 256 tile" units:
-// waves of units times the k-blocks of one unit, plus a split's extra pass.
-double est_cost(int64_t tiles, int split, int64_t num_kb, int bn, int sm_count) {
+// Relative time of one k-block of one output tile for each tile configuration
+// (cg, bn), in units of the 2-CTA 256 x 256 tile, measured on GB300 for the
+// 4096^3 bf16 GEMM.  A configuration's cost is waves x k-blocks per unit x
+// this, plus a split's extra pass over its partials.
+double tile_kb_cost(int cg, int bn) {
+  if (cg == 2) return bn == 256 ? 1.0 : 0.62;
+  return bn == 256 ? 1.15 : bn == 128 ? 0.85 : 0.6;
+}
+
+double est_cost(int64_t tiles, int split, int64_t num_kb, int cg, int bn, int slots) {
   const int64_t units = tiles * split;
-  const int64_t waves = cdiv(units, sm_count);
-  const double per_kb = bn == 256 ? 1.0 : bn == 128 ? 0.56 : 0.34;  // smem-read bound below 256
+  const int64_t waves = cdiv(units, slots);
   const double kb = static_cast<double>(cdiv(num_kb, split));
   const double extra = split > 1 ? 1.5 : 0.0;
-  return static_cast<double>(waves) * (kb + extra) * per_kb + (split > 1 ? 0.5 : 0.0);
+  return static_cast<double>(waves) * (kb + extra) * tile_kb_cost(cg, bn);
 }
 
 gemm_status_t make_plan(const Options& o, int sm_count, gemm_op_t transA, gemm_op_t transB,
@@ -130,49 +137,54 @@ gemm_status_t make_plan(const Options& o, int sm_count, gemm_op_t transA, gemm_o
   P.b_kmajor = pl.q.kmajor ? 1 : 0;
 
   const int64_t num_kb = cdiv(K, kBK);
-  const int64_t tiles_i = cdiv(pl.I, kBM);
 
-  // Tile width and k-split.
-  int bn_choices[3] = {256, 128, 64};
-  int best_bn = 256, best_split = 1;
+  // Tile configuration and k-split.
+  static const int kConfigs[5][2] = {{2, 256}, {2, 128}, {1, 256}, {1, 128}, {1, 64}};
+  int best_cg = 1, best_bn = 64, best_split = 1;
   double best_cost = 1e300;
-  for (int bn : bn_choices) {
+  for (const auto& c : kConfigs) {
+    const int cg = c[0], bn = c[1];
+    if (o.force_path == GEMM_PATH_TC_1CTA && cg != 1) continue;
+    if (o.force_path == GEMM_PATH_TC_2CTA && cg != 2) continue;
     if (o.force_bn && bn != o.force_bn) continue;
-    if (!o.force_bn && bn > 64 && pl.J <= bn / 2) continue;  // too wide for J
-    const int64_t tiles = tiles_i * cdiv(pl.J, bn);
+    if (!o.force_bn && bn > 64 && pl.J <= bn / 2) continue;            // too wide for J
+    if (!o.force_path && cg == 2 && pl.I <= kBM) continue;             // one row of tiles
+    const int slots = std::max(1, sm_count / cg);                       // tiles in flight
+    const int64_t tiles = cdiv(pl.I, kBM * cg) * cdiv(pl.J, bn);
     int max_split = 1;
-    if (tiles < 2 * static_cast<int64_t>(sm_count) && tiles <= kCounterCap)
-      max_split = static_cast<int>(std::min<int64_t>(16, num_kb / 2));
-    if (max_split < 1) max_split = 1;
+    if (tiles * cg <= kCounterCap) {
+      if (o.split_k)  // an explicit split is honoured whenever the counters allow
+        max_split = static_cast<int>(std::min<int64_t>(o.split_k, num_kb));
+      else if (tiles * 2 <= slots)  // fewer than half the tiles needed to fill the GPU
+        max_split = static_cast<int>(std::min<int64_t>(16, std::max<int64_t>(1, num_kb / 4)));
+    }
     for (int s = 1; s <= max_split; ++s) {
-      if (o.split_k && s != std::min<int64_t>(o.split_k, num_kb)) continue;
-      const double c = est_cost(tiles, s, num_kb, bn, sm_count);
-      if (c < best_cost - 1e-9) {
-        best_cost = c;
+      if (o.split_k && s != max_split) continue;
+      const double cost = est_cost(tiles, s, num_kb, cg, bn, slots);
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best_cg = cg;
         best_bn = bn;
         best_split = s;
       }
     }
   }
-  if (best_cost >= 1e300) {  // forced split beyond what the tile count allows
-    best_bn = o.force_bn ? o.force_bn : 256;
-    const int64_t tiles = tiles_i * cdiv(pl.J, best_bn);
-    best_split = (tiles <= kCounterCap && o.split_k)
-                     ? static_cast<int>(std::min<int64_t>(o.split_k, num_kb))
-                     : 1;
-  }
-  P.path = GEMM_PATH_TC_1CTA;
-  P.bm = kBM;
+  if (best_cost >= 1e300) return GEMM_ERR_INVALID_ARG;  // forced options admit no configuration
+  P.path = best_cg == 2 ? GEMM_PATH_TC_2CTA : GEMM_PATH_TC_1CTA;
+  P.bm = kBM * best_cg;
   P.bn = best_bn;
   P.bk = kBK;
-  P.stages = tc_stages(best_bn);
+  P.stages = tc_stages(best_bn, best_cg);
   P.split_k = best_split;
+  const int64_t tiles_i = cdiv(pl.I, kBM * best_cg);
   const int64_t tiles_j = cdiv(pl.J, best_bn);
   P.tiles = tiles_i * tiles_j;
   P.units = P.tiles * best_split;
   P.raster_group = o.raster_group ? o.raster_group : 8;
   if (P.raster_group > tiles_i) P.raster_group = static_cast<int32_t>(tiles_i);
-  P.grid = static_cast<int32_t>(std::min<int64_t>(P.units, sm_count));
+  int slots = std::max(1, sm_count / best_cg);
+  if (o.max_grid) slots = std::min(slots, std::max(1, o.max_grid / best_cg));
+  P.grid = static_cast<int32_t>(std::min<int64_t>(P.units, slots) * best_cg);
 
   // Workspace: repacked operands, then split-K partials.
   size_t ws = 0;
@@ -188,7 +200,7 @@ gemm_status_t make_plan(const Options& o, int sm_count, gemm_op_t transA, gemm_o
   P.repack_b = (swap ? pl.p.repack : pl.q.repack) ? 1 : 0;
   if (best_split > 1) {
     pl.partial_offset = ws;
-    ws = round_up(ws + static_cast<size_t>(P.units) * best_bn * kBM * 4, 256);
+    ws = round_up(ws + static_cast<size_t>(P.units) * best_cg * best_bn * kBM * 4, 256);
   }
   P.workspace_bytes = static_cast<int64_t>(ws);
   P.vector_store = (!swap && reinterpret_cast<uintptr_t>(C) % 16 == 0 && (ldc * c_elem) % 16 == 0) ? 1 : 0;
@@ -265,7 +277,8 @@ struct gemm_handle_s {
   size_t ws_bytes = 0;
   uint64_t launches = 0;
   int last_cuda_error = 0;
-  bool prepared[3] = {false, false, false};
+  bool prepared[2][3] = {{false, false, false}, {false, false, false}};  // [cg-1][bn 64/128/256]
+  int max_pairs[3] = {0, 0, 0};                                          // resident CTA pairs per bn
   Options opt;
 };
 
@@ -344,7 +357,8 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
       h->opt.wait_limit_ns = value;
       return GEMM_OK;
     case GEMM_OPT_FORCE_PATH:
-      if (value != 0 && value != GEMM_PATH_TC_1CTA) return GEMM_ERR_INVALID_ARG;
+      if (value != 0 && value != GEMM_PATH_TC_1CTA && value != GEMM_PATH_TC_2CTA)
+        return GEMM_ERR_INVALID_ARG;
       h->opt.force_path = static_cast<int>(value);
       return GEMM_OK;
     case GEMM_OPT_SPLIT_K:
@@ -362,6 +376,10 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
     case GEMM_OPT_TEST_DROP_LOAD:
       if (value < 0 || value > (int64_t{1} << 30)) return GEMM_ERR_INVALID_ARG;
       h->opt.drop_load = static_cast<int>(value);
+      return GEMM_OK;
+    case GEMM_OPT_MAX_GRID:
+      if (value < 0 || value > (int64_t{1} << 20)) return GEMM_ERR_INVALID_ARG;
+      h->opt.max_grid = static_cast<int>(value);
       return GEMM_OK;
   }
   return GEMM_ERR_INVALID_ARG;
@@ -421,12 +439,17 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
     h->d_ws = nw;
     h->ws_bytes = want;
   }
+  const int cg = P.path == GEMM_PATH_TC_2CTA ? 2 : 1;
   const int bn_slot = P.bn == 256 ? 2 : P.bn == 128 ? 1 : 0;
-  if (!h->prepared[bn_slot]) {
-    e = tc_prepare(P.bn);
+  if (!h->prepared[cg - 1][bn_slot]) {
+    int clusters = 0;
+    e = tc_prepare(P.bn, cg, &clusters);
     if (e != cudaSuccess) return cuda_fail(h, e);
-    h->prepared[bn_slot] = true;
+    if (cg == 2) h->max_pairs[bn_slot] = clusters > 0 ? clusters : h->sm_count / 2;
+    h->prepared[cg - 1][bn_slot] = true;
   }
+  int grid = P.grid;
+  if (cg == 2) grid = std::min(grid, h->max_pairs[bn_slot] * 2);
 
   // Operands that the copy engine cannot read directly are repacked first.
   const void* pbase = pl.p.ptr;
@@ -447,7 +470,7 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
   CUtensorMap map_p, map_q;
   s = encode_operand(&map_p, pl.p, pbase, pld, pl.bf16, kBM);
   if (s != GEMM_OK) return s;
-  s = encode_operand(&map_q, pl.q, qbase, qld, pl.bf16, P.bn);
+  s = encode_operand(&map_q, pl.q, qbase, qld, pl.bf16, P.bn / cg);
   if (s != GEMM_OK) return s;
 
   TcArgs a;
@@ -455,7 +478,7 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
   a.I = static_cast<int32_t>(pl.I);
   a.J = static_cast<int32_t>(pl.J);
   a.K = static_cast<int32_t>(pl.K);
-  a.tiles_i = static_cast<int32_t>(cdiv(pl.I, kBM));
+  a.tiles_i = static_cast<int32_t>(cdiv(pl.I, kBM * cg));
   a.tiles_j = static_cast<int32_t>(cdiv(pl.J, P.bn));
   a.num_kb = static_cast<int32_t>(cdiv(pl.K, kBK));
   a.split_k = P.split_k;
@@ -463,7 +486,7 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
   a.raster_group = P.raster_group;
   a.p_kmajor = P.a_kmajor;
   a.q_kmajor = P.b_kmajor;
-  a.idesc = make_idesc_f16(pl.bf16, !pl.p.kmajor, !pl.q.kmajor, kBM, P.bn);
+  a.idesc = make_idesc_f16(pl.bf16, !pl.p.kmajor, !pl.q.kmajor, kBM * cg, P.bn);
   a.alpha = alpha;
   a.beta = beta;
   a.C = C;
@@ -476,7 +499,7 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
   a.status = h->d_status;
   a.wait_limit_ns = static_cast<uint64_t>(h->opt.wait_limit_ns);
   a.drop_load = h->opt.drop_load;
-  e = tc_launch(P.bn, map_p, map_q, a, P.grid, st);
+  e = tc_launch(P.bn, cg, map_p, map_q, a, grid, st);
   if (e != cudaSuccess) return cuda_fail(h, e);
   h->launches += 1;
   return GEMM_OK;

@@ -1,36 +1,45 @@
-// tc_dispatch.cu -- choose the kernel instantiation for a tile width.
+// tc_dispatch.cu -- choose the kernel instantiation for a tile width and CTA group.
 #include "tc_gemm.cuh"
 
 namespace g10 {
 
-cudaError_t tc_prepare_bn64();
-cudaError_t tc_prepare_bn128();
-cudaError_t tc_prepare_bn256();
-cudaError_t tc_launch_bn64(const CUtensorMap&, const CUtensorMap&, const TcArgs&, int, cudaStream_t);
-cudaError_t tc_launch_bn128(const CUtensorMap&, const CUtensorMap&, const TcArgs&, int, cudaStream_t);
-cudaError_t tc_launch_bn256(const CUtensorMap&, const CUtensorMap&, const TcArgs&, int, cudaStream_t);
+#define TC_DECLARE(BN, CG)                                                                  \
+  cudaError_t tc_prepare_bn##BN##_cg##CG(int* max_clusters);                                \
+  cudaError_t tc_launch_bn##BN##_cg##CG(const CUtensorMap&, const CUtensorMap&, const TcArgs&, \
+                                        int, cudaStream_t);
+TC_DECLARE(64, 1)
+TC_DECLARE(128, 1)
+TC_DECLARE(256, 1)
+TC_DECLARE(128, 2)
+TC_DECLARE(256, 2)
 
-int tc_stages(int bn) {
-  return bn == 256 ? TcConfig<256>::kStages : bn == 128 ? TcConfig<128>::kStages : TcConfig<64>::kStages;
+bool tc_supported(int bn, int cg) {
+  return (cg == 1 && (bn == 64 || bn == 128 || bn == 256)) || (cg == 2 && (bn == 128 || bn == 256));
 }
 
-size_t tc_smem_bytes(int bn) {
-  return bn == 256 ? TcConfig<256>::kSmemBytes
-                   : bn == 128 ? TcConfig<128>::kSmemBytes : TcConfig<64>::kSmemBytes;
+int tc_stages(int bn, int cg) {
+  if (cg == 2) return bn == 256 ? TcConfig<256, 2>::kStages : TcConfig<128, 2>::kStages;
+  return bn == 256 ? TcConfig<256, 1>::kStages
+                   : bn == 128 ? TcConfig<128, 1>::kStages : TcConfig<64, 1>::kStages;
 }
 
-cudaError_t tc_prepare(int bn) {
-  if (bn == 256) return tc_prepare_bn256();
-  if (bn == 128) return tc_prepare_bn128();
-  if (bn == 64) return tc_prepare_bn64();
+cudaError_t tc_prepare(int bn, int cg, int* max_clusters) {
+  *max_clusters = 0;
+  if (cg == 1 && bn == 64) return tc_prepare_bn64_cg1(max_clusters);
+  if (cg == 1 && bn == 128) return tc_prepare_bn128_cg1(max_clusters);
+  if (cg == 1 && bn == 256) return tc_prepare_bn256_cg1(max_clusters);
+  if (cg == 2 && bn == 128) return tc_prepare_bn128_cg2(max_clusters);
+  if (cg == 2 && bn == 256) return tc_prepare_bn256_cg2(max_clusters);
   return cudaErrorInvalidValue;
 }
 
-cudaError_t tc_launch(int bn, const CUtensorMap& map_p, const CUtensorMap& map_q,
+cudaError_t tc_launch(int bn, int cg, const CUtensorMap& map_p, const CUtensorMap& map_q,
                       const TcArgs& args, int grid, cudaStream_t stream) {
-  if (bn == 256) return tc_launch_bn256(map_p, map_q, args, grid, stream);
-  if (bn == 128) return tc_launch_bn128(map_p, map_q, args, grid, stream);
-  if (bn == 64) return tc_launch_bn64(map_p, map_q, args, grid, stream);
+  if (cg == 1 && bn == 64) return tc_launch_bn64_cg1(map_p, map_q, args, grid, stream);
+  if (cg == 1 && bn == 128) return tc_launch_bn128_cg1(map_p, map_q, args, grid, stream);
+  if (cg == 1 && bn == 256) return tc_launch_bn256_cg1(map_p, map_q, args, grid, stream);
+  if (cg == 2 && bn == 128) return tc_launch_bn128_cg2(map_p, map_q, args, grid, stream);
+  if (cg == 2 && bn == 256) return tc_launch_bn256_cg2(map_p, map_q, args, grid, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -14,6 +14,11 @@
 //  * Tiles arrive 128-byte swizzled ("[CUDA 优化实战] hgemm sm120", section 4:
 //    the swizzle of 16-bit element (r, c) in a 64-wide row is c ^ ((r & 7) << 3)),
 //    which is the layout the tensor core's shared-memory descriptor expects.
+//  * CG == 2 runs one tile on a CTA pair (a cluster of two CTAs on neighbouring
+//    SMs, "CUDA GEMM 矩阵乘法优化指南" 13.3-13.4): each CTA loads its 128 rows of P
+//    and half of the tile's Q columns, and the leader CTA issues
+//    tcgen05.mma.cta_group::2 with M = 256, which reads both CTAs' shared memory.
+//    Per SM this halves the Q traffic from L2 for the same tile width.
 //  * The fp32 accumulator lives in Tensor Memory, double-buffered so that the
 //    epilogue of one tile overlaps the main loop of the next (the ping-pong idea
 //    of "GPU GEMM 优化完全拆解（三）", Hopper 时代的三种 kernel 设计).
@@ -36,13 +41,17 @@
 
 namespace g10 {
 
-template <int BN>
+template <int BN, int CG>
 struct TcConfig {
   static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
-  static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
-  static constexpr int kABytes = kBM * kBK * 2;  // one P tile: 128 rows x 128 bytes
-  static constexpr int kBBytes = BN * kBK * 2;   // one Q tile
+  static_assert(CG == 1 || CG == 2, "CTA group");
+  static_assert(CG == 1 || BN >= 128, "a CTA pair needs 64-column halves of Q");
+  static constexpr int kTileM = kBM * CG;        // rows of D per tile
+  static constexpr int kQRows = BN / CG;         // rows of Q this CTA loads per k-block
+  static constexpr int kABytes = kBM * kBK * 2;  // this CTA's P tile: 128 rows x 128 bytes
+  static constexpr int kBBytes = kQRows * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = (192 * 1024) / kStageBytes > 8 ? 8 : (192 * 1024) / kStageBytes;
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kTmemCols = 2 * BN;       // two fp32 accumulators of BN columns
   static constexpr int kCtrlBytes = 256;
@@ -190,20 +199,20 @@ __device__ __forceinline__ void store_chunk(const TcArgs& a, int i, int j0, floa
 
 // ----------------------------------------------------------------- the roles --
 
-template <int BN>
+template <int BN, int CG>
 __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CUtensorMap* map_q,
                                               const TcArgs& a, uint8_t* ring_a, uint8_t* ring_b,
-                                              TcCtrl* ctrl) {
-  using Cfg = TcConfig<BN>;
+                                              TcCtrl* ctrl, uint32_t rank, int first, int stride) {
+  using Cfg = TcConfig<BN, CG>;
   int stage = 0;
   uint32_t phase = 0;
   uint32_t pending = 0, pending_parity = 0;  // copies in flight, per stage
   int nload = 0;
   bool ok = true;
-  for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
+  for (int u = first; ok && u < a.units; u += stride) {
     const Unit w = decode_unit(a, u);
-    const int i0 = w.ti * kBM;
-    const int j0 = w.tj * BN;
+    const int i0 = w.ti * Cfg::kTileM + static_cast<int>(rank) * kBM;
+    const int j0 = w.tj * BN + static_cast<int>(rank) * Cfg::kQRows;
     for (int kb = w.kb0; kb < w.kb1; ++kb) {
       if (!wait_bounded(smem_u32(&ctrl->empty[stage]), phase ^ 1u, ctrl, a, kRoleProducer,
                         kBarEmpty, true)) {
@@ -211,26 +220,34 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
         break;
       }
       ++nload;
-      const uint32_t full = smem_u32(&ctrl->full[stage]);
+      const uint32_t full_local = smem_u32(&ctrl->full[stage]);
+      // A pair credits both CTAs' bytes to the leader's barrier, which the MMA waits on.
+      const uint32_t full = CG == 2 ? mapa_shared(full_local, 0) : full_local;
       if (a.drop_load != 0 && blockIdx.x == 0 && nload == a.drop_load) {
         pending &= ~(1u << stage);  // test hook: this stage's barrier is never completed
       } else {
-        mbar_arrive_expect_tx(full, Cfg::kStageBytes);
+        if (rank == 0) mbar_arrive_expect_tx(full_local, CG * Cfg::kStageBytes);
         const uint32_t sa = smem_u32(ring_a + stage * Cfg::kABytes);
         const uint32_t sb = smem_u32(ring_b + stage * Cfg::kBBytes);
         const int k0 = kb * kBK;
+        auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
+          if constexpr (CG == 2)
+            tma_load_2d_pair(dst, map, full, x, y);
+          else
+            tma_load_2d(dst, map, full, x, y);
+        };
         if (a.p_kmajor) {
-          tma_load_2d(sa, map_p, full, k0, i0);
+          load(sa, map_p, k0, i0);
         } else {
-          tma_load_2d(sa, map_p, full, i0, k0);
-          tma_load_2d(sa + kMnAtomBytes, map_p, full, i0 + 64, k0);
+          load(sa, map_p, i0, k0);
+          load(sa + kMnAtomBytes, map_p, i0 + 64, k0);
         }
         if (a.q_kmajor) {
-          tma_load_2d(sb, map_q, full, k0, j0);
+          load(sb, map_q, k0, j0);
         } else {
 #pragma unroll
-          for (int c = 0; c < BN / 64; ++c)
-            tma_load_2d(sb + c * kMnAtomBytes, map_q, full, j0 + 64 * c, k0);
+          for (int c = 0; c < Cfg::kQRows / 64; ++c)
+            load(sb + c * kMnAtomBytes, map_q, j0 + 64 * c, k0);
         }
         pending |= 1u << stage;
         pending_parity = (pending_parity & ~(1u << stage)) | (phase << stage);
@@ -241,22 +258,33 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
       }
     }
   }
-  // No copy may still be writing shared memory when the CTA exits.
-  for (int s = 0; s < Cfg::kStages; ++s)
-    if (pending & (1u << s))
-      wait_bounded(smem_u32(&ctrl->full[s]), (pending_parity >> s) & 1u, ctrl, a, kRoleProducer,
-                   kBarDrain, false);
+  // No copy may still be writing shared memory when the CTA exits.  The leader's
+  // barrier counts both CTAs' bytes, so the leader's wait covers the pair; a
+  // peer CTA is held at the final cluster barrier until the leader has waited.
+  if (rank == 0) {
+    for (int s = 0; s < Cfg::kStages; ++s)
+      if (pending & (1u << s))
+        wait_bounded(smem_u32(&ctrl->full[s]), (pending_parity >> s) & 1u, ctrl, a, kRoleProducer,
+                     kBarDrain, false);
+  }
 }
 
-template <int BN>
+template <int BN, int CG>
 __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8_t* ring_b,
-                                         TcCtrl* ctrl, uint32_t tmem_base) {
-  using Cfg = TcConfig<BN>;
+                                         TcCtrl* ctrl, uint32_t tmem_base, int first, int stride) {
+  using Cfg = TcConfig<BN, CG>;
   int stage = 0;
   uint32_t phase = 0;
   int it = 0;
   bool ok = true;
-  for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x, ++it) {
+  // A pair's commits arrive on the barrier at the same offset in both CTAs.
+  auto commit = [](uint32_t bar) {
+    if constexpr (CG == 2)
+      mma_commit_pair(bar, 0x3);
+    else
+      mma_commit<1>(bar);
+  };
+  for (int u = first; ok && u < a.units; u += stride, ++it) {
     const Unit w = decode_unit(a, u);
     const int buf = it & 1;
     const uint32_t acc_parity = (it >> 1) & 1;
@@ -283,30 +311,32 @@ __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8
                                        : smem_desc_sw128(sa + 2048 * k, kMnAtomBytes, 1024);
         const uint64_t bd = a.q_kmajor ? smem_desc_sw128(sb + 32 * k, 16, 1024)
                                        : smem_desc_sw128(sb + 2048 * k, kMnAtomBytes, 1024);
-        mma_f16_ss(d_tmem, ad, bd, a.idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
+        mma_f16_ss<CG>(d_tmem, ad, bd, a.idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
       }
-      mma_commit(smem_u32(&ctrl->empty[stage]));  // frees the stage once these MMAs have read it
+      commit(smem_u32(&ctrl->empty[stage]));  // frees the stage once these MMAs have read it
       if (++stage == Cfg::kStages) {
         stage = 0;
         phase ^= 1u;
       }
     }
     if (!ok) break;
-    mma_commit(smem_u32(&ctrl->acc_full[buf]));  // accumulator ready for the epilogue
+    commit(smem_u32(&ctrl->acc_full[buf]));  // accumulator ready for the epilogue(s)
   }
   // Tensor Memory is freed only after every MMA issued here has finished.
-  mma_commit(smem_u32(&ctrl->mma_done));
+  mma_commit<CG>(smem_u32(&ctrl->mma_done));
   wait_bounded(smem_u32(&ctrl->mma_done), 0, ctrl, a, kRoleMma, kBarDrain, false);
 }
 
-template <int BN>
+template <int BN, int CG>
 __device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uint32_t tmem_base,
-                                              int warp, int lane) {
+                                              int warp, int lane, uint32_t rank, int first,
+                                              int stride) {
+  using Cfg = TcConfig<BN, CG>;
   const int quarter = warp & 3;  // a warp may only read TMEM lanes 32*(warp%4) .. +31
   const int row = quarter * 32 + lane;
   const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
   int it = 0;
-  for (int u = blockIdx.x; u < a.units; u += gridDim.x, ++it) {
+  for (int u = first; u < a.units; u += stride, ++it) {
     const Unit w = decode_unit(a, u);
     const int buf = it & 1;
     const uint32_t acc_parity = (it >> 1) & 1;
@@ -315,18 +345,24 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uin
     if (bar_any(1, 128, !ok)) return;  // all four epilogue warps leave together
     tc_fence_after_sync();
     const uint32_t taddr = lane_base + static_cast<uint32_t>(buf * BN);
-    const uint32_t acc_empty = smem_u32(&ctrl->acc_empty[buf]);
-    const int i = w.ti * kBM + row;
+    // the MMA (leader CTA) waits until every epilogue thread of the pair has read the buffer
+    const uint32_t acc_empty_local = smem_u32(&ctrl->acc_empty[buf]);
+    const uint32_t acc_empty = CG == 2 ? mapa_shared(acc_empty_local, 0) : acc_empty_local;
+    auto release = [&]() {
+      tc_fence_before_sync();
+      if constexpr (CG == 2)
+        mbar_arrive_cluster(acc_empty);
+      else
+        mbar_arrive(acc_empty);
+    };
+    const int i = w.ti * Cfg::kTileM + static_cast<int>(rank) * kBM + row;
     if (a.split_k == 1) {
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(taddr + c, r);
         tmem_ld_wait(r);
-        if (c + 32 == BN) {  // last read of this accumulator: hand it back to the MMA warp
-          tc_fence_before_sync();
-          mbar_arrive(acc_empty);
-        }
+        if (c + 32 == BN) release();  // last read of this accumulator: hand it back
         float v[32];
 #pragma unroll
         for (int t = 0; t < 32; ++t) v[t] = __uint_as_float(r[t]);
@@ -335,16 +371,15 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uin
     } else {
       // Partial of this k-range: column-major inside the tile so that a warp's
       // 32 rows are 128 contiguous bytes.
-      float* part = a.partials + static_cast<size_t>(u) * BN * kBM;
+      const int slot = u * CG + static_cast<int>(rank);
+      const int ctr = w.tile * CG + static_cast<int>(rank);
+      float* part = a.partials + static_cast<size_t>(slot) * BN * kBM;
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(taddr + c, r);
         tmem_ld_wait(r);
-        if (c + 32 == BN) {
-          tc_fence_before_sync();
-          mbar_arrive(acc_empty);
-        }
+        if (c + 32 == BN) release();
 #pragma unroll
         for (int t = 0; t < 32; ++t)
           __stcg(part + static_cast<size_t>(c + t) * kBM + row, __uint_as_float(r[t]));
@@ -352,15 +387,15 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uin
       __threadfence();
       bar_sync(1, 128);
       if (threadIdx.x == 64) {
-        const int old = atomicAdd(&a.counters[w.tile], 1);
+        const int old = atomicAdd(&a.counters[ctr], 1);
         const uint32_t last = (old == a.split_k - 1) ? 1u : 0u;
-        if (last) atomicExch(&a.counters[w.tile], 0);  // clean for the next call
+        if (last) atomicExch(&a.counters[ctr], 0);  // clean for the next call
         *reinterpret_cast<volatile uint32_t*>(&ctrl->last) = last;
       }
       bar_sync(1, 128);
       if (*reinterpret_cast<volatile uint32_t*>(&ctrl->last)) {
         __threadfence();
-        const float* base = a.partials + static_cast<size_t>(w.tile) * a.split_k * BN * kBM;
+        const int slot0 = w.tile * a.split_k * CG + static_cast<int>(rank);  // split s: slot0 + s*CG
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           float v[32];
@@ -368,7 +403,7 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uin
           for (int t = 0; t < 32; ++t) v[t] = 0.0f;
 #pragma unroll 1
           for (int s = 0; s < a.split_k; ++s) {
-            const float* ps = base + static_cast<size_t>(s) * BN * kBM;
+            const float* ps = a.partials + static_cast<size_t>(slot0 + s * CG) * BN * kBM;
 #pragma unroll
             for (int t = 0; t < 32; ++t) v[t] += __ldcg(ps + static_cast<size_t>(c + t) * kBM + row);
           }
@@ -379,11 +414,11 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uin
   }
 }
 
-template <int BN>
+template <int BN, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p,
                    const __grid_constant__ CUtensorMap map_q, const TcArgs a) {
-  using Cfg = TcConfig<BN>;
+  using Cfg = TcConfig<BN, CG>;
   extern __shared__ uint8_t smem_raw[];
   // 128-byte swizzle atoms need 1024-byte aligned tiles.
   const uint32_t raw = smem_u32(smem_raw);
@@ -394,6 +429,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // A CTA pair (cluster of 2) shares each tile; rank 0 is the leader that issues the MMAs.
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
+  const int first = CG == 2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int stride = CG == 2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::kStages; ++s) {
@@ -402,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctrl->acc_full[b]), 1);
-      mbar_init(smem_u32(&ctrl->acc_empty[b]), 128);
+      mbar_init(smem_u32(&ctrl->acc_empty[b]), 128 * CG);
     }
     mbar_init(smem_u32(&ctrl->mma_done), 1);
     ctrl->abort = 0;
@@ -414,29 +453,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&map_q);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ctrl->tmem_base), Cfg::kTmemCols);
-    tmem_relinquish();
+    tmem_alloc<CG>(smem_u32(&ctrl->tmem_base), Cfg::kTmemCols);
+    tmem_relinquish<CG>();
   }
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // the peer's barriers exist before any remote arrive
   tc_fence_after_sync();
   const uint32_t tmem_base = ctrl->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) producer_role<BN>(&map_p, &map_q, a, ring_a, ring_b, ctrl);
+    if (lane == 0)
+      producer_role<BN, CG>(&map_p, &map_q, a, ring_a, ring_b, ctrl, rank, first, stride);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) mma_role<BN>(a, ring_a, ring_b, ctrl, tmem_base);
+    if (lane == 0 && rank == 0) mma_role<BN, CG>(a, ring_a, ring_b, ctrl, tmem_base, first, stride);
     __syncwarp();
   } else {
-    epilogue_role<BN>(a, ctrl, tmem_base, warp, lane);
+    epilogue_role<BN, CG>(a, ctrl, tmem_base, warp, lane, rank, first, stride);
   }
 
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (CG == 2) {
+    // After an abort, give copies the leader could not account for time to land.
+    if (*reinterpret_cast<volatile uint32_t*>(&ctrl->abort)) {
+      const uint64_t t0 = global_timer_ns();
+      while (global_timer_ns() - t0 < 100000) {
+      }
+    }
+    cluster_sync();  // neither CTA leaves while the pair's MMAs may still touch it
+  }
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    tmem_dealloc<CG>(tmem_base, Cfg::kTmemCols);
   }
 }
 

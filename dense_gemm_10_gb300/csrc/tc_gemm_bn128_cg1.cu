@@ -1,0 +1,4 @@
+// Tile width 128, CTA group 1 of the persistent tcgen05 GEMM kernel.
+#define TC_BN 128
+#define TC_CG 1
+#include "tc_gemm_inst.cuh"

@@ -17,7 +17,7 @@ STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED", 3:
           4: "GEMM_ERR_CUDA", 5: "GEMM_ERR_TENSORMAP", 6: "GEMM_ERR_TIMEOUT", 7: "GEMM_ERR_WORKSPACE"}
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NO_DEVICE, ERR_CUDA, ERR_TENSORMAP, ERR_TIMEOUT, ERR_WORKSPACE = range(8)
 PATH_NOOP, PATH_SCALE_C, PATH_TC_1CTA, PATH_TC_2CTA = 0, 1, 2, 3
-OPT_WAIT_LIMIT_NS, OPT_FORCE_PATH, OPT_SPLIT_K, OPT_RASTER_GROUP, OPT_FORCE_BN, OPT_TEST_DROP_LOAD = range(6)
+OPT_WAIT_LIMIT_NS, OPT_FORCE_PATH, OPT_SPLIT_K, OPT_RASTER_GROUP, OPT_FORCE_BN, OPT_TEST_DROP_LOAD, OPT_MAX_GRID = range(7)
 
 # Exported functions and their (restype, argtypes).
 _i32, _i64, _u64, _f32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p

@@ -176,9 +176,11 @@ typedef enum {
   GEMM_OPT_SPLIT_K = 2,       /* 0 auto, else the k-split to use (clamped to the k-blocks) */
   GEMM_OPT_RASTER_GROUP = 3,  /* 0 auto, else tile rows per raster group */
   GEMM_OPT_FORCE_BN = 4,      /* 0 auto, else 64, 128 or 256 */
-  GEMM_OPT_TEST_DROP_LOAD = 5 /* tests only: 0 off; n > 0 makes CTA 0 skip its n-th k-block
-                                 load, so a barrier is never completed and the bounded wait
-                                 must end the kernel with GEMM_ERR_TIMEOUT */
+  GEMM_OPT_TEST_DROP_LOAD = 5, /* tests only: 0 off; n > 0 makes CTA 0 skip its n-th k-block
+                                  load, so a barrier is never completed and the bounded wait
+                                  must end the kernel with GEMM_ERR_TIMEOUT */
+  GEMM_OPT_MAX_GRID = 6        /* 0 auto, else at most this many CTAs (persistent CTAs then
+                                  walk more tiles each) */
 } gemm_option_t;
 
 /* Set an option on a handle.  Errors: GEMM_ERR_INVALID_ARG for an unknown

@@ -82,11 +82,12 @@ def test_product_code_never_touches_the_oracle():
 # ----------------------------------------------------------------- planner --
 
 def test_plan_square_nt():
+    """4096^3: 256 x 256 tiles on CTA pairs, 76 pairs on 152 SMs."""
     p = G.plan(4096, 4096, 4096, 0, 1)
-    assert p.path == G.PATH_TC_1CTA and p.swap_ab == 0
+    assert p.path == G.PATH_TC_2CTA and p.swap_ab == 0
     assert p.a_kmajor == 1 and p.b_kmajor == 1
-    assert p.bm == 128 and p.bk == 64 and p.bn in (128, 256)
-    assert p.split_k == 1 and p.units == p.tiles == (4096 // 128) * (4096 // p.bn)
+    assert p.bm == 256 and p.bk == 64 and p.bn == 256
+    assert p.split_k == 1 and p.units == p.tiles == 16 * 16
     assert p.grid == 152 and p.repack_a == 0 and p.repack_b == 0
     assert p.vector_store == 1 and p.launches == 1 and p.workspace_bytes == 0
 
@@ -97,14 +98,19 @@ def test_plan_major_modes(ta, tb, ak, bk):
     assert (p.a_kmajor, p.b_kmajor) == (ak, bk)
 
 
-def test_plan_lm_head_swaps_and_splits():
+def test_plan_lm_head_swaps():
     p = G.plan(64, 32000, 4096, 0, 1)
-    assert p.swap_ab == 1
+    assert p.swap_ab == 1 and p.path == G.PATH_TC_1CTA
     assert p.a_kmajor == 1 and p.b_kmajor == 1   # MMA A = weights (N x K), MMA B = activations (M x K)
-    assert p.bn == 64 and p.tiles == 250
-    assert p.split_k > 1 and p.units == 250 * p.split_k
-    assert p.workspace_bytes >= p.units * 64 * 128 * 4
+    assert p.bn == 64 and p.tiles == 250 and p.units == 250 * p.split_k
     assert p.vector_store == 0 and p.grid == 152
+
+
+def test_plan_few_tiles_split_k():
+    """Fewer tiles than half the SMs: the k-dimension is split, partials in the workspace."""
+    p = G.plan(256, 256, 8192, 0, 1)
+    assert p.split_k > 1 and p.units == p.tiles * p.split_k
+    assert p.workspace_bytes >= p.units * (p.bm // 128) * p.bn * 128 * 4
 
 
 def test_plan_ragged_repacks_misaligned_b():
@@ -149,8 +155,10 @@ def test_plan_invariants(shape):
     for sm in (148, 152, 160):
         p = G.plan(M, N, K, 0, 0, sm_count=sm)
         I, J = (N, M) if p.swap_ab else (M, N)
+        cg = 2 if p.path == G.PATH_TC_2CTA else 1
+        assert p.bm == 128 * cg
         assert p.tiles == -(-I // p.bm) * -(-J // p.bn)
         assert p.units == p.tiles * p.split_k
         assert 1 <= p.split_k <= max(1, -(-K // 64))
-        assert p.grid == min(p.units, sm)
-        assert 1 <= p.raster_group <= max(1, -(-I // 128))
+        assert p.grid == min(p.units, sm // cg) * cg
+        assert 1 <= p.raster_group <= max(1, -(-I // p.bm))

@@ -59,7 +59,7 @@ def test_ragged_4095_4097_1000(h):
 def test_lm_head_64(h):
     p = inputs.lm_head_64()
     plan = G.plan(p.M, p.N, p.K, p.transA, p.transB)
-    assert plan.swap_ab == 1 and plan.split_k > 1
+    assert plan.swap_ab == 1
     Cd = _sampled(p, h, count=6000)
     # M = 64 is small enough to check one full row of the vocabulary as well
     from gpu_util import oracle_at as _at

@@ -2,6 +2,8 @@
 finishes in seconds: several tiles, ragged tails, every layout, both input
 types, every output type, alpha / beta, the swapped and split-K paths, and the
 degenerate sizes.  Every call goes through the C ABI."""
+import contextlib
+
 import numpy as np
 import pytest
 import torch
@@ -21,6 +23,24 @@ def h():
     gh.close()
 
 
+CONFIGS = [(1, 64), (1, 128), (1, 256), (2, 128), (2, 256)]   # (CTAs per tile, tile width)
+PATHS = {1: G.PATH_TC_1CTA, 2: G.PATH_TC_2CTA}
+
+
+@contextlib.contextmanager
+def options(h, **kw):
+    """Force planner options on the handle for the duration of a check."""
+    codes = {"path": G.OPT_FORCE_PATH, "bn": G.OPT_FORCE_BN, "split": G.OPT_SPLIT_K, "raster": G.OPT_RASTER_GROUP,
+             "grid": G.OPT_MAX_GRID}
+    try:
+        for k, v in kw.items():
+            h.set_option(codes[k], v)
+        yield
+    finally:
+        for k in kw:
+            h.set_option(codes[k], 0)
+
+
 def _check(p, h, guard=True):
     out, full = run(p, h, guard_rows=3 if guard else 0, guard_cols=5 if guard else 0)
     R, Mag = oracle_full(p)
@@ -38,13 +58,16 @@ def test_tiny_256(h):
     _check(inputs.tiny_256(), h)
 
 
+@pytest.mark.parametrize("cg", [1, 2])
 @pytest.mark.parametrize("transA,transB", [(0, 0), (0, 1), (1, 0), (1, 1)])
 @pytest.mark.parametrize("in_dtype,out_dtype", [("bf16", "f32"), ("f16", "f32"), ("bf16", "bf16"), ("f16", "f16")])
-def test_layouts_and_types(h, transA, transB, in_dtype, out_dtype):
-    """Ragged in every dimension: 3 x 5 tiles with partial last tiles, K not a multiple of 64."""
+def test_layouts_and_types(h, transA, transB, in_dtype, out_dtype, cg):
+    """Ragged in every dimension: partial last tiles, K not a multiple of 64; one
+    CTA per tile and CTA pairs."""
     p = inputs.make_problem("lay", 300, 520, 200, transA, transB, in_dtype, out_dtype, ("uniform", -1, 1),
                             ("uniform", -1, 1), alpha=1.5, beta=0.5, seed=31)
-    _check(p, h)
+    with options(h, path=PATHS[cg]):
+        _check(p, h)
 
 
 @pytest.mark.parametrize("shape", [(1, 1, 1), (1, 1, 70), (127, 129, 63), (128, 256, 64), (129, 257, 65),
@@ -55,13 +78,15 @@ def test_ragged_shapes(h, shape):
     _check(p, h)
 
 
+@pytest.mark.parametrize("cg", [1, 2])
 @pytest.mark.parametrize("transA,transB", [(0, 0), (0, 1), (1, 0), (1, 1)])
-def test_small_integers_bit_exact(h, transA, transB):
+def test_small_integers_bit_exact(h, transA, transB, cg):
     """Integers in {-4..4}: the fp32 result is exact whatever the order of the
     sum, so the GPU must equal the oracle bit for bit."""
     p = inputs.make_problem("ints", 384, 640, 1024, transA, transB, "bf16", "f32", ("ints", -4, 4), ("ints", -4, 4),
                             alpha=1.5, beta=0.5, dist_c=("ints", -9, 9), seed=5)
-    out, _ = run(p, h)
+    with options(h, path=PATHS[cg]):
+        out, _ = run(p, h)
     R, _ = oracle_full(p)
     assert np.array_equal(out, R)
 
@@ -76,29 +101,34 @@ def test_skinny_swapped_split(h, M, N, K):
 
 
 @pytest.mark.parametrize("split", [2, 3, 7])
-@pytest.mark.parametrize("bn", [64, 128, 256])
-def test_forced_split_k(h, split, bn):
-    p = inputs.make_problem("split", 256, 512, 960, 0, 0, "f16", "f32", ("uniform", -1, 1), ("uniform", -1, 1),
-                            alpha=-0.75, beta=1.25, seed=split * bn)
-    h.set_option(G.OPT_SPLIT_K, split)
-    h.set_option(G.OPT_FORCE_BN, bn)
-    try:
+@pytest.mark.parametrize("cg,bn", CONFIGS)
+def test_forced_split_k(h, split, cg, bn):
+    p = inputs.make_problem("split", 300, 520, 960, 0, 0, "f16", "f32", ("uniform", -1, 1), ("uniform", -1, 1),
+                            alpha=-0.75, beta=1.25, seed=split * bn + cg)
+    with options(h, path=PATHS[cg], bn=bn, split=split):
+        plan = G.plan(p.M, p.N, p.K, 0, 0, G.F16_F32, handle=h, beta=p.beta)
+        assert plan.split_k == split and plan.bn == bn and plan.path == PATHS[cg]
         _check(p, h)
-    finally:
-        h.set_option(G.OPT_SPLIT_K, 0)
-        h.set_option(G.OPT_FORCE_BN, 0)
 
 
-@pytest.mark.parametrize("bn", [64, 128, 256])
-@pytest.mark.parametrize("transA,transB", [(0, 0), (1, 1)])
-def test_every_tile_width(h, bn, transA, transB):
-    p = inputs.make_problem("bn", 384, 768, 320, transA, transB, "bf16", "bf16", ("normal", 0, 1), ("normal", 0, 1),
-                            alpha=0.5, beta=-1.0, seed=bn + transA)
-    h.set_option(G.OPT_FORCE_BN, bn)
-    try:
+@pytest.mark.parametrize("cg,bn", CONFIGS)
+@pytest.mark.parametrize("transA,transB", [(0, 0), (1, 1), (0, 1), (1, 0)])
+def test_every_tile_configuration(h, cg, bn, transA, transB):
+    p = inputs.make_problem("cfg", 600, 900, 320, transA, transB, "bf16", "bf16", ("normal", 0, 1), ("normal", 0, 1),
+                            alpha=0.5, beta=-1.0, seed=bn + transA + 2 * transB + 7 * cg)
+    with options(h, path=PATHS[cg], bn=bn):
         _check(p, h)
-    finally:
-        h.set_option(G.OPT_FORCE_BN, 0)
+
+
+@pytest.mark.parametrize("cg,bn", CONFIGS)
+def test_many_tiles_per_cta(h, cg, bn):
+    """More tiles than CTAs: every CTA runs several tiles through both TMEM buffers."""
+    p = inputs.make_problem("persist", 1100, 1500, 192, 0, 1, "bf16", "f32", ("normal", 0, 1), ("normal", 0, 1),
+                            seed=3 * bn + cg)
+    with options(h, path=PATHS[cg], bn=bn, raster=3, grid=6):
+        plan = G.plan(p.M, p.N, p.K, 0, 1, handle=h)
+        assert plan.grid <= 6 and plan.units >= 3 * plan.grid // cg
+        _check(p, h)
 
 
 def test_misaligned_leading_dimensions(h):
