@@ -13,6 +13,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -37,6 +38,7 @@ struct Options {
   int force_bn = 0;
   int drop_load = 0;
   int max_grid = 0;
+  int stream_k = 0;  // 0 auto, 1 off, 2 on
 };
 
 // One stored operand, as the tensor-memory-accelerator copy engine will see it.
@@ -52,6 +54,7 @@ struct Operand {
 
 struct Plan {
   gemm_plan_t pub{};
+  Sched sched{};
   Operand p, q;
   int64_t I = 0, J = 0, K = 0;
   int64_t c_si = 0, c_sj = 0;
@@ -68,23 +71,115 @@ bool tma_aligned(const void* p, int64_t ld) {
 }
 
 // Relative time of one k-block of one output tile for each tile configuration
-// (cg, bn), in units of the 2-CTA 256 x 256 tile, measured on GB300 for the
-// 4096^3 bf16 GEMM.  A configuration's cost is waves x k-blocks per unit x
-// this, plus a split's extra pass over its partials.
+// (cg, bn), in units of the CTA-pair 256 x 256 tile, from GB300 measurements
+// of the 4096^3 and 8192 x 12288 x 4096 bf16 GEMMs.
 double tile_kb_cost(int cg, int bn) {
   if (cg == 2) return bn == 256 ? 1.0 : 0.62;
   return bn == 256 ? 1.15 : bn == 128 ? 0.85 : 0.6;
 }
 
-double est_cost(int64_t tiles, int split, int64_t num_kb, int cg, int bn, int slots) {
-  const int64_t units = tiles * split;
-  const int64_t waves = cdiv(units, slots);
-  const double kb = static_cast<double>(cdiv(num_kb, split));
-  const double extra = split > 1 ? 1.5 : 0.0;
-  return static_cast<double>(waves) * (kb + extra) * tile_kb_cost(cg, bn);
+// Resident slots (CTAs, or CTA pairs when cg == 2) per tile configuration.
+struct SlotTable {
+  int cg1 = 1, cg2[3] = {1, 1, 1};  // cg2 by bn 64 / 128 / 256
+  int of(int cg, int bn) const { return cg == 1 ? cg1 : cg2[bn == 256 ? 2 : bn == 128 ? 1 : 0]; }
+  static SlotTable even(int sm_count) {
+    SlotTable t;
+    t.cg1 = std::max(1, sm_count);
+    for (int& v : t.cg2) v = std::max(1, sm_count / 2);
+    return t;
+  }
+};
+
+struct Choice {
+  bool valid = false;
+  int cg = 1, bn = 64, slots = 1;
+  double cost = 1e300;
+  Sched sched{};
+};
+
+bool needs_partials(const Sched& s) {
+  return (s.mode == kSchedTiles && s.split_k > 1) || s.mode == kSchedStreamK;
 }
 
-gemm_status_t make_plan(const Options& o, int sm_count, gemm_op_t transA, gemm_op_t transB,
+// Work units over all slots (for reporting): whole tiles, split pieces, or
+// stream-K range pieces (one more piece per slot edge that falls inside a tile).
+int64_t count_units(const Sched& s) {
+  const int64_t tiles = static_cast<int64_t>(s.tiles_i) * s.tiles_j;
+  if (s.mode == kSchedTiles) return tiles * s.split_k;
+  int64_t n = s.dp_tiles + (tiles - s.dp_tiles);
+  for (int32_t c = 1; c < s.sk_slots; ++c)
+    if (sk_begin(s, c) % s.num_kb != 0) ++n;
+  return n;
+}
+
+// Estimated time, in k-blocks of one tile, of the stream-K tail: `iters`
+// k-blocks of `tiles` tiles dealt to `g` slots.  Each partial piece costs a
+// store, and the tile's last contribution reads every piece of its tile.
+double sk_tail_cost(int64_t tiles, int64_t num_kb, int64_t g) {
+  const int64_t iters = tiles * num_kb;
+  const double per_slot = static_cast<double>(cdiv(iters, g));
+  if (g <= tiles && tiles % g == 0) return per_slot;  // whole tiles, no partials
+  const double contrib = per_slot >= static_cast<double>(num_kb)
+                             ? 2.0
+                             : std::ceil(static_cast<double>(num_kb) / per_slot) + 1.0;
+  return per_slot + 1.0 + 0.5 * contrib;
+}
+
+Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64_t num_kb, int cg,
+                       int bn, int slots) {
+  Choice ch;
+  ch.cg = cg;
+  ch.bn = bn;
+  ch.slots = slots;
+  const int64_t tiles = tiles_i * tiles_j;
+  Sched& s = ch.sched;
+  s.tiles_i = static_cast<int32_t>(tiles_i);
+  s.tiles_j = static_cast<int32_t>(tiles_j);
+  s.num_kb = static_cast<int32_t>(num_kb);
+  s.raster_group = 8;
+  s.mode = kSchedTiles;
+  s.split_k = 1;
+  if (o.split_k) {  // an explicit split-K request
+    const int64_t split = std::min<int64_t>(o.split_k, num_kb);
+    if (tiles * cg > kCounterCap) return ch;
+    s.split_k = static_cast<int32_t>(split);
+    ch.cost = static_cast<double>(cdiv(tiles * split, slots)) *
+              (static_cast<double>(cdiv(num_kb, split)) + (split > 1 ? 1.5 : 0.0)) *
+              tile_kb_cost(cg, bn);
+    ch.valid = true;
+    return ch;
+  }
+  // Whole tiles: ceil(tiles / slots) waves.
+  double best = static_cast<double>(cdiv(tiles, slots) * num_kb);
+  // Stream-K tail: the tiles of the incomplete last wave shared by g slots.
+  const int64_t full_waves = tiles / slots;
+  const int64_t sk_tiles = tiles - full_waves * slots;
+  if (o.stream_k != 1 && sk_tiles > 0 && sk_tiles * cg <= kCounterCap) {
+    const int64_t iters = sk_tiles * num_kb;
+    int64_t best_g = 0;
+    double best_tail = 1e300;
+    for (int64_t g = 1; g <= std::min<int64_t>(slots, iters); ++g) {
+      const double t = sk_tail_cost(sk_tiles, num_kb, g);
+      if (t < best_tail - 1e-9) {
+        best_tail = t;
+        best_g = g;
+      }
+    }
+    const double sk = static_cast<double>(full_waves * num_kb) + best_tail;
+    if (best_g > 0 && (o.stream_k == 2 || sk < best - 1e-9)) {
+      best = sk;
+      s.mode = kSchedStreamK;
+      s.dp_tiles = static_cast<int32_t>(full_waves * slots);
+      s.sk_slots = static_cast<int32_t>(best_g);
+      s.sk_iters = iters;
+    }
+  }
+  ch.cost = best * tile_kb_cost(cg, bn);
+  ch.valid = true;
+  return ch;
+}
+
+gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t transA, gemm_op_t transB,
                         int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                         int64_t ldb, float beta, const void* C, int64_t ldc, gemm_dtype_t dtype,
                         Plan* out) {
@@ -93,7 +188,7 @@ gemm_status_t make_plan(const Options& o, int sm_count, gemm_op_t transA, gemm_o
   if ((transA != GEMM_OP_N && transA != GEMM_OP_T) || (transB != GEMM_OP_N && transB != GEMM_OP_T))
     return GEMM_ERR_INVALID_ARG;
   if (dtype < GEMM_BF16_F32 || dtype > GEMM_F16_F16) return GEMM_ERR_INVALID_ARG;
-  if (M < 0 || N < 0 || K < 0 || sm_count <= 0) return GEMM_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
   pl.bf16 = dtype == GEMM_BF16_F32 || dtype == GEMM_BF16_BF16;
   pl.c_type = (dtype == GEMM_BF16_F32 || dtype == GEMM_F16_F32) ? kCF32
               : dtype == GEMM_BF16_BF16                        ? kCBF16
@@ -138,55 +233,45 @@ gemm_status_t make_plan(const Options& o, int sm_count, gemm_op_t transA, gemm_o
 
   const int64_t num_kb = cdiv(K, kBK);
 
-  // Tile configuration and k-split.
+  // Tile configuration and schedule: the configuration with the lowest
+  // estimated time, est_time() below.
   static const int kConfigs[5][2] = {{2, 256}, {2, 128}, {1, 256}, {1, 128}, {1, 64}};
-  int best_cg = 1, best_bn = 64, best_split = 1;
-  double best_cost = 1e300;
+  Choice best;
   for (const auto& c : kConfigs) {
     const int cg = c[0], bn = c[1];
     if (o.force_path == GEMM_PATH_TC_1CTA && cg != 1) continue;
     if (o.force_path == GEMM_PATH_TC_2CTA && cg != 2) continue;
     if (o.force_bn && bn != o.force_bn) continue;
-    if (!o.force_bn && bn > 64 && pl.J <= bn / 2) continue;            // too wide for J
-    if (!o.force_path && cg == 2 && pl.I <= kBM) continue;             // one row of tiles
-    const int slots = std::max(1, sm_count / cg);                       // tiles in flight
-    const int64_t tiles = cdiv(pl.I, kBM * cg) * cdiv(pl.J, bn);
-    int max_split = 1;
-    if (tiles * cg <= kCounterCap) {
-      if (o.split_k)  // an explicit split is honoured whenever the counters allow
-        max_split = static_cast<int>(std::min<int64_t>(o.split_k, num_kb));
-      else if (tiles * 2 <= slots)  // fewer than half the tiles needed to fill the GPU
-        max_split = static_cast<int>(std::min<int64_t>(16, std::max<int64_t>(1, num_kb / 4)));
-    }
-    for (int s = 1; s <= max_split; ++s) {
-      if (o.split_k && s != max_split) continue;
-      const double cost = est_cost(tiles, s, num_kb, cg, bn, slots);
-      if (cost < best_cost - 1e-9) {
-        best_cost = cost;
-        best_cg = cg;
-        best_bn = bn;
-        best_split = s;
-      }
-    }
+    if (!o.force_bn && bn > 64 && pl.J <= bn / 2) continue;  // too wide for J
+    if (!o.force_path && cg == 2 && pl.I <= kBM) continue;   // one row of tiles
+    int nslots = slots.of(cg, bn);
+    if (o.max_grid) nslots = std::min(nslots, std::max(1, o.max_grid / cg));
+    Choice ch = choose_schedule(o, cdiv(pl.I, kBM * cg), cdiv(pl.J, bn), num_kb, cg, bn, nslots);
+    if (ch.valid && ch.cost < best.cost - 1e-9) best = ch;
   }
-  if (best_cost >= 1e300) return GEMM_ERR_INVALID_ARG;  // forced options admit no configuration
-  P.path = best_cg == 2 ? GEMM_PATH_TC_2CTA : GEMM_PATH_TC_1CTA;
-  P.bm = kBM * best_cg;
-  P.bn = best_bn;
+  if (!best.valid) return GEMM_ERR_INVALID_ARG;  // forced options admit no configuration
+  const int cg = best.cg;
+  pl.sched = best.sched;
+  pl.sched.raster_group = o.raster_group ? o.raster_group : 8;
+  if (pl.sched.raster_group > pl.sched.tiles_i) pl.sched.raster_group = pl.sched.tiles_i;
+  P.path = cg == 2 ? GEMM_PATH_TC_2CTA : GEMM_PATH_TC_1CTA;
+  P.bm = kBM * cg;
+  P.bn = best.bn;
   P.bk = kBK;
-  P.stages = tc_stages(best_bn, best_cg);
-  P.split_k = best_split;
-  const int64_t tiles_i = cdiv(pl.I, kBM * best_cg);
-  const int64_t tiles_j = cdiv(pl.J, best_bn);
-  P.tiles = tiles_i * tiles_j;
-  P.units = P.tiles * best_split;
-  P.raster_group = o.raster_group ? o.raster_group : 8;
-  if (P.raster_group > tiles_i) P.raster_group = static_cast<int32_t>(tiles_i);
-  int slots = std::max(1, sm_count / best_cg);
-  if (o.max_grid) slots = std::min(slots, std::max(1, o.max_grid / best_cg));
-  P.grid = static_cast<int32_t>(std::min<int64_t>(P.units, slots) * best_cg);
+  P.stages = tc_stages(best.bn, cg);
+  P.schedule = pl.sched.mode;
+  P.split_k = pl.sched.mode == kSchedTiles ? pl.sched.split_k : 1;
+  P.tiles_i = pl.sched.tiles_i;
+  P.tiles_j = pl.sched.tiles_j;
+  P.num_kb = pl.sched.num_kb;
+  P.tiles = static_cast<int64_t>(pl.sched.tiles_i) * pl.sched.tiles_j;
+  P.dp_tiles = pl.sched.mode == kSchedStreamK ? pl.sched.dp_tiles : static_cast<int32_t>(P.tiles);
+  P.sk_slots = pl.sched.mode == kSchedStreamK ? pl.sched.sk_slots : 0;
+  P.units = count_units(pl.sched);
+  P.raster_group = pl.sched.raster_group;
+  P.grid = static_cast<int32_t>(std::min<int64_t>(best.slots, std::max<int64_t>(P.units, 1)) * cg);
 
-  // Workspace: repacked operands, then split-K partials.
+  // Workspace: repacked operands, then partial tiles of split tiles.
   size_t ws = 0;
   for (Operand* op : {&pl.p, &pl.q}) {
     if (!tma_aligned(op->ptr, op->ld)) {
@@ -198,9 +283,9 @@ gemm_status_t make_plan(const Options& o, int sm_count, gemm_op_t transA, gemm_o
   }
   P.repack_a = (swap ? pl.q.repack : pl.p.repack) ? 1 : 0;
   P.repack_b = (swap ? pl.p.repack : pl.q.repack) ? 1 : 0;
-  if (best_split > 1) {
+  if (needs_partials(pl.sched)) {
     pl.partial_offset = ws;
-    ws = round_up(ws + static_cast<size_t>(P.units) * best_cg * best_bn * kBM * 4, 256);
+    ws = round_up(ws + static_cast<size_t>(partial_slots(pl.sched)) * cg * best.bn * kBM * 4, 256);
   }
   P.workspace_bytes = static_cast<int64_t>(ws);
   P.vector_store = (!swap && reinterpret_cast<uintptr_t>(C) % 16 == 0 && (ldc * c_elem) % 16 == 0) ? 1 : 0;
@@ -277,8 +362,7 @@ struct gemm_handle_s {
   size_t ws_bytes = 0;
   uint64_t launches = 0;
   int last_cuda_error = 0;
-  bool prepared[2][3] = {{false, false, false}, {false, false, false}};  // [cg-1][bn 64/128/256]
-  int max_pairs[3] = {0, 0, 0};                                          // resident CTA pairs per bn
+  SlotTable slots;  // resident CTAs / CTA pairs per kernel configuration
   Options opt;
 };
 
@@ -305,7 +389,18 @@ gemm_status_t gemm_create(gemm_handle_t* out, int device) {
   h->device = device;
   h->sm_count = prop.multiProcessorCount;
   DeviceGuard g(device);
-  cudaError_t e = cudaMalloc(&h->d_status, sizeof(int32_t));
+  // Opt every kernel configuration in to its shared memory, and count how many
+  // CTA pairs can be resident at once (a pair must sit inside one GPC).
+  h->slots = SlotTable::even(h->sm_count);
+  static const int kCfg[5][2] = {{1, 64}, {1, 128}, {1, 256}, {2, 128}, {2, 256}};
+  cudaError_t e = cudaSuccess;
+  for (const auto& c : kCfg) {
+    int clusters = 0;
+    e = tc_prepare(c[1], c[0], &clusters);
+    if (e != cudaSuccess) break;
+    if (c[0] == 2 && clusters > 0) h->slots.cg2[c[1] == 256 ? 2 : 1] = std::min(clusters, h->sm_count / 2);
+  }
+  if (e == cudaSuccess) e = cudaMalloc(&h->d_status, sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMalloc(&h->d_counters, kCounterCap * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(h->d_counters, 0, kCounterCap * sizeof(int32_t));
@@ -381,6 +476,10 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
       if (value < 0 || value > (int64_t{1} << 20)) return GEMM_ERR_INVALID_ARG;
       h->opt.max_grid = static_cast<int>(value);
       return GEMM_OK;
+    case GEMM_OPT_STREAM_K:
+      if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+      h->opt.stream_k = static_cast<int>(value);
+      return GEMM_OK;
   }
   return GEMM_ERR_INVALID_ARG;
 }
@@ -396,10 +495,12 @@ gemm_status_t gemm_plan(gemm_handle_t h, int sm_count, gemm_op_t transA, gemm_op
                         const void* B, int64_t ldb, float beta, const void* C, int64_t ldc,
                         gemm_dtype_t dtype, gemm_plan_t* plan) {
   if (!plan) return GEMM_ERR_INVALID_ARG;
+  if (!h && sm_count <= 0) return GEMM_ERR_INVALID_ARG;
   Options o = h ? h->opt : Options();
+  const SlotTable slots = h ? h->slots : SlotTable::even(sm_count);
   Plan pl;
   gemm_status_t s =
-      make_plan(o, sm_count, transA, transB, M, N, K, A, lda, B, ldb, beta, C, ldc, dtype, &pl);
+      make_plan(o, slots, transA, transB, M, N, K, A, lda, B, ldb, beta, C, ldc, dtype, &pl);
   if (s == GEMM_OK) *plan = pl.pub;
   return s;
 }
@@ -410,7 +511,7 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
                        void* stream) {
   if (!h) return GEMM_ERR_INVALID_ARG;
   Plan pl;
-  gemm_status_t s = make_plan(h->opt, h->sm_count, transA, transB, M, N, K, A, lda, B, ldb, beta,
+  gemm_status_t s = make_plan(h->opt, h->slots, transA, transB, M, N, K, A, lda, B, ldb, beta,
                               C, ldc, dtype, &pl);
   if (s != GEMM_OK) return s;
   const gemm_plan_t& P = pl.pub;
@@ -440,16 +541,6 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
     h->ws_bytes = want;
   }
   const int cg = P.path == GEMM_PATH_TC_2CTA ? 2 : 1;
-  const int bn_slot = P.bn == 256 ? 2 : P.bn == 128 ? 1 : 0;
-  if (!h->prepared[cg - 1][bn_slot]) {
-    int clusters = 0;
-    e = tc_prepare(P.bn, cg, &clusters);
-    if (e != cudaSuccess) return cuda_fail(h, e);
-    if (cg == 2) h->max_pairs[bn_slot] = clusters > 0 ? clusters : h->sm_count / 2;
-    h->prepared[cg - 1][bn_slot] = true;
-  }
-  int grid = P.grid;
-  if (cg == 2) grid = std::min(grid, h->max_pairs[bn_slot] * 2);
 
   // Operands that the copy engine cannot read directly are repacked first.
   const void* pbase = pl.p.ptr;
@@ -478,12 +569,7 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
   a.I = static_cast<int32_t>(pl.I);
   a.J = static_cast<int32_t>(pl.J);
   a.K = static_cast<int32_t>(pl.K);
-  a.tiles_i = static_cast<int32_t>(cdiv(pl.I, kBM * cg));
-  a.tiles_j = static_cast<int32_t>(cdiv(pl.J, P.bn));
-  a.num_kb = static_cast<int32_t>(cdiv(pl.K, kBK));
-  a.split_k = P.split_k;
-  a.units = static_cast<int32_t>(P.units);
-  a.raster_group = P.raster_group;
+  a.sched = pl.sched;
   a.p_kmajor = P.a_kmajor;
   a.q_kmajor = P.b_kmajor;
   a.idesc = make_idesc_f16(pl.bf16, !pl.p.kmajor, !pl.q.kmajor, kBM * cg, P.bn);
@@ -494,12 +580,12 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
   a.c_sj = pl.c_sj;
   a.c_type = pl.c_type;
   a.vec_store = P.vector_store;
-  a.partials = P.split_k > 1 ? reinterpret_cast<float*>(ws + pl.partial_offset) : nullptr;
+  a.partials = needs_partials(pl.sched) ? reinterpret_cast<float*>(ws + pl.partial_offset) : nullptr;
   a.counters = h->d_counters;
   a.status = h->d_status;
   a.wait_limit_ns = static_cast<uint64_t>(h->opt.wait_limit_ns);
   a.drop_load = h->opt.drop_load;
-  e = tc_launch(P.bn, cg, map_p, map_q, a, grid, st);
+  e = tc_launch(P.bn, cg, map_p, map_q, a, P.grid, st);
   if (e != cudaSuccess) return cuda_fail(h, e);
   h->launches += 1;
   return GEMM_OK;

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "schedule.h"
+
 namespace g10 {
 
 constexpr int kBM = 128;      // MMA M (rows of the output tile held in TMEM lanes)
@@ -28,11 +30,7 @@ enum WaitBarrier : int32_t {
 // P is the MMA "A" operand (tile rows on TMEM lanes), Q the MMA "B" operand.
 struct TcArgs {
   int32_t I, J, K;
-  int32_t tiles_i, tiles_j;
-  int32_t num_kb;        // ceil(K / kBK)
-  int32_t split_k;       // k-splits per tile
-  int32_t units;         // tiles_i * tiles_j * split_k
-  int32_t raster_group;  // tile rows (along I) per raster group
+  Sched sched;           // work assignment (schedule.h); num_kb = ceil(K / kBK)
   int32_t p_kmajor;      // P has K contiguous (else I contiguous)
   int32_t q_kmajor;      // Q has K contiguous (else J contiguous)
   uint32_t idesc;        // tcgen05 instruction descriptor
@@ -41,8 +39,8 @@ struct TcArgs {
   int64_t c_si, c_sj;
   int32_t c_type;        // CType
   int32_t vec_store;     // c_sj == 1 and every row of C starts 16-byte aligned
-  float* partials;       // split-K partial tiles, [units][BN][kBM] fp32
-  int32_t* counters;     // per-tile arrival counters, zero between calls
+  float* partials;       // partial tiles of split tiles, [partial_slots * CG][BN][kBM] fp32
+  int32_t* counters;     // per split tile (x CG) arrival counters, zero between calls
   int32_t* status;       // device status word
   uint64_t wait_limit_ns;
   int32_t drop_load;     // tests only: CTA 0 skips its drop_load-th k-block load (1-based)

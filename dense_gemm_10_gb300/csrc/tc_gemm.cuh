@@ -22,10 +22,11 @@
 //  * The fp32 accumulator lives in Tensor Memory, double-buffered so that the
 //    epilogue of one tile overlaps the main loop of the next (the ping-pong idea
 //    of "GPU GEMM 优化完全拆解（三）", Hopper 时代的三种 kernel 设计).
-//  * Split-K: a work unit may cover only a k-range of a tile; its fp32 partial
-//    goes to a workspace and the last unit of the tile to arrive sums all
-//    partials in fixed split order, so the result is deterministic
-//    ("GPU GEMM 优化完全拆解（三）", Split-K 与 Sliced-K).
+//  * Split-K and stream-K (schedule.h): a work unit may cover only a k-range
+//    of a tile; its fp32 partial goes to a workspace and the last contribution
+//    of the tile to arrive sums all partials in fixed k order, so the result is
+//    deterministic ("GPU GEMM 优化完全拆解（三）", Split-K 与 Sliced-K;
+//    "CUDA GEMM 矩阵乘法优化指南", 12.5).
 //  * Every barrier wait is bounded by a wall-clock limit; a wait that runs out
 //    records the role and barrier in the status word, raises a CTA-wide abort
 //    flag, and every role then leaves its loop.  Before the CTA exits, the
@@ -89,28 +90,6 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, TcCt
       return false;
     }
   }
-}
-
-struct Unit {
-  int ti, tj, tile, kb0, kb1;
-};
-
-// Work unit u -> output tile (grouped raster: raster_group tile rows at a time,
-// walking down the rows of a group before moving to the next column) and k-range.
-__device__ __forceinline__ Unit decode_unit(const TcArgs& a, int u) {
-  Unit w;
-  w.tile = u / a.split_k;
-  const int s = u - w.tile * a.split_k;
-  const int group_tiles = a.raster_group * a.tiles_j;
-  const int g = w.tile / group_tiles;
-  const int first_i = g * a.raster_group;
-  const int rows = min(a.tiles_i - first_i, a.raster_group);
-  const int r = w.tile - g * group_tiles;
-  w.ti = first_i + r % rows;
-  w.tj = r / rows;
-  w.kb0 = static_cast<int>((static_cast<int64_t>(s) * a.num_kb) / a.split_k);
-  w.kb1 = static_cast<int>((static_cast<int64_t>(s + 1) * a.num_kb) / a.split_k);
-  return w;
 }
 
 // ------------------------------------------------------------------ epilogue --
@@ -209,8 +188,9 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
   uint32_t pending = 0, pending_parity = 0;  // copies in flight, per stage
   int nload = 0;
   bool ok = true;
-  for (int u = first; ok && u < a.units; u += stride) {
-    const Unit w = decode_unit(a, u);
+  WorkIter work(a.sched, first, stride);
+  Unit w;
+  while (ok && work.next(w)) {
     const int i0 = w.ti * Cfg::kTileM + static_cast<int>(rank) * kBM;
     const int j0 = w.tj * BN + static_cast<int>(rank) * Cfg::kQRows;
     for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -284,8 +264,9 @@ __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8
     else
       mma_commit<1>(bar);
   };
-  for (int u = first; ok && u < a.units; u += stride, ++it) {
-    const Unit w = decode_unit(a, u);
+  WorkIter work(a.sched, first, stride);
+  Unit w;
+  for (; ok && work.next(w); ++it) {
     const int buf = it & 1;
     const uint32_t acc_parity = (it >> 1) & 1;
     if (!wait_bounded(smem_u32(&ctrl->acc_empty[buf]), acc_parity ^ 1u, ctrl, a, kRoleMma,
@@ -336,8 +317,9 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uin
   const int row = quarter * 32 + lane;
   const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
   int it = 0;
-  for (int u = first; u < a.units; u += stride, ++it) {
-    const Unit w = decode_unit(a, u);
+  WorkIter work(a.sched, first, stride);
+  Unit w;
+  for (; work.next(w); ++it) {
     const int buf = it & 1;
     const uint32_t acc_parity = (it >> 1) & 1;
     const bool ok = wait_bounded(smem_u32(&ctrl->acc_full[buf]), acc_parity, ctrl, a,
@@ -356,7 +338,7 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uin
         mbar_arrive(acc_empty);
     };
     const int i = w.ti * Cfg::kTileM + static_cast<int>(rank) * kBM + row;
-    if (a.split_k == 1) {
+    if (!w.partial) {
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         uint32_t r[32];
@@ -371,8 +353,8 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uin
     } else {
       // Partial of this k-range: column-major inside the tile so that a warp's
       // 32 rows are 128 contiguous bytes.
-      const int slot = u * CG + static_cast<int>(rank);
-      const int ctr = w.tile * CG + static_cast<int>(rank);
+      const int slot = w.pslot * CG + static_cast<int>(rank);
+      const int ctr = w.ctr * CG + static_cast<int>(rank);
       float* part = a.partials + static_cast<size_t>(slot) * BN * kBM;
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
@@ -388,22 +370,22 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uin
       bar_sync(1, 128);
       if (threadIdx.x == 64) {
         const int old = atomicAdd(&a.counters[ctr], 1);
-        const uint32_t last = (old == a.split_k - 1) ? 1u : 0u;
+        const uint32_t last = (old == w.ncontrib - 1) ? 1u : 0u;
         if (last) atomicExch(&a.counters[ctr], 0);  // clean for the next call
         *reinterpret_cast<volatile uint32_t*>(&ctrl->last) = last;
       }
       bar_sync(1, 128);
       if (*reinterpret_cast<volatile uint32_t*>(&ctrl->last)) {
         __threadfence();
-        const int slot0 = w.tile * a.split_k * CG + static_cast<int>(rank);  // split s: slot0 + s*CG
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           float v[32];
 #pragma unroll
           for (int t = 0; t < 32; ++t) v[t] = 0.0f;
 #pragma unroll 1
-          for (int s = 0; s < a.split_k; ++s) {
-            const float* ps = a.partials + static_cast<size_t>(slot0 + s * CG) * BN * kBM;
+          for (int k = 0; k < w.ncontrib; ++k) {  // fixed k order: the sum does not depend on timing
+            const int ks = contrib_slot(a.sched, w, k) * CG + static_cast<int>(rank);
+            const float* ps = a.partials + static_cast<size_t>(ks) * BN * kBM;
 #pragma unroll
             for (int t = 0; t < 32; ++t) v[t] += __ldcg(ps + static_cast<size_t>(c + t) * kBM + row);
           }

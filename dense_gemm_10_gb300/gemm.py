@@ -17,7 +17,9 @@ STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED", 3:
           4: "GEMM_ERR_CUDA", 5: "GEMM_ERR_TENSORMAP", 6: "GEMM_ERR_TIMEOUT", 7: "GEMM_ERR_WORKSPACE"}
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NO_DEVICE, ERR_CUDA, ERR_TENSORMAP, ERR_TIMEOUT, ERR_WORKSPACE = range(8)
 PATH_NOOP, PATH_SCALE_C, PATH_TC_1CTA, PATH_TC_2CTA = 0, 1, 2, 3
-OPT_WAIT_LIMIT_NS, OPT_FORCE_PATH, OPT_SPLIT_K, OPT_RASTER_GROUP, OPT_FORCE_BN, OPT_TEST_DROP_LOAD, OPT_MAX_GRID = range(7)
+(OPT_WAIT_LIMIT_NS, OPT_FORCE_PATH, OPT_SPLIT_K, OPT_RASTER_GROUP, OPT_FORCE_BN, OPT_TEST_DROP_LOAD, OPT_MAX_GRID,
+ OPT_STREAM_K) = range(8)
+SCHED_TILES, SCHED_STREAM_K = 0, 1
 
 # Exported functions and their (restype, argtypes).
 _i32, _i64, _u64, _f32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p
@@ -26,8 +28,9 @@ _i32, _i64, _u64, _f32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, c
 class Plan(ctypes.Structure):
     _fields_ = [(n, _i32) for n in ("path", "swap_ab", "a_kmajor", "b_kmajor", "bm", "bn", "bk", "stages",
                                     "split_k", "raster_group", "repack_a", "repack_b", "vector_store",
-                                    "grid", "launches", "reserved")] + \
-               [(n, _i64) for n in ("tiles", "units", "workspace_bytes")]
+                                    "grid", "launches", "schedule")] + \
+               [(n, _i64) for n in ("tiles", "units", "workspace_bytes")] + \
+               [(n, _i32) for n in ("tiles_i", "tiles_j", "num_kb", "dp_tiles", "sk_slots", "reserved")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_ if n != "reserved"}

@@ -143,7 +143,7 @@ typedef struct {
   int32_t swap_ab;         /* 1: the kernel computes C^T = op(B)^T * op(A)^T */
   int32_t a_kmajor;        /* MMA A operand (rows of the MMA) has K contiguous */
   int32_t b_kmajor;        /* MMA B operand (columns of the MMA) has K contiguous */
-  int32_t bm, bn, bk;      /* output tile of one CTA (bm x bn) and k-block depth */
+  int32_t bm, bn, bk;      /* output tile (bm x bn; a CTA pair shares bm = 256) and k-block */
   int32_t stages;          /* shared-memory ring depth */
   int32_t split_k;         /* k-splits per output tile (1 = none) */
   int32_t raster_group;    /* tile rows per raster group */
@@ -152,18 +152,26 @@ typedef struct {
   int32_t vector_store;    /* epilogue writes C rows with 16-byte stores */
   int32_t grid;            /* CTAs launched for the main kernel */
   int32_t launches;        /* kernels launched by one gemm_run */
-  int32_t reserved;
+  int32_t schedule;        /* 0: whole (or split-K) tiles; 1: stream-K tail */
   int64_t tiles;           /* output tiles */
-  int64_t units;           /* work units = tiles * split_k */
+  int64_t units;           /* work units over all CTAs (tiles, split pieces or stream-K pieces) */
   int64_t workspace_bytes; /* handle workspace this call needs */
+  int32_t tiles_i;         /* tiles along the MMA rows (M, or N when swapped) */
+  int32_t tiles_j;         /* tiles along the MMA columns */
+  int32_t num_kb;          /* k-blocks per tile */
+  int32_t dp_tiles;        /* tiles run whole (stream-K: the complete waves) */
+  int32_t sk_slots;        /* stream-K: CTAs (or pairs) sharing the remaining tiles' k-blocks */
+  int32_t reserved;
 } gemm_plan_t;
 
 /*
- * gemm_plan: the configuration gemm_run would use for these arguments on a GPU
- * with `sm_count` SMs, written to *plan.  Host-only: touches no device, so it
- * can be called without a GPU.  `h` may be NULL (default options) or a handle
- * whose options (gemm_set_option) then apply.  Pointers are used only for their
- * alignment.  Returns the same argument errors as gemm_run.
+ * gemm_plan: the configuration gemm_run would use for these arguments, written
+ * to *plan.  Host-only: touches no device, so it can be called without a GPU.
+ * With h == NULL the default options and a GPU of `sm_count` SMs (all of them
+ * usable by CTA pairs) are assumed; with a handle, its options
+ * (gemm_set_option) and its device's measured residency apply and sm_count is
+ * ignored.  Pointers are used only for their alignment.  Returns the same
+ * argument errors as gemm_run.
  */
 gemm_status_t gemm_plan(gemm_handle_t h, int sm_count, gemm_op_t transA, gemm_op_t transB,
                         int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
@@ -179,8 +187,9 @@ typedef enum {
   GEMM_OPT_TEST_DROP_LOAD = 5, /* tests only: 0 off; n > 0 makes CTA 0 skip its n-th k-block
                                   load, so a barrier is never completed and the bounded wait
                                   must end the kernel with GEMM_ERR_TIMEOUT */
-  GEMM_OPT_MAX_GRID = 6        /* 0 auto, else at most this many CTAs (persistent CTAs then
+  GEMM_OPT_MAX_GRID = 6,       /* 0 auto, else at most this many CTAs (persistent CTAs then
                                   walk more tiles each) */
+  GEMM_OPT_STREAM_K = 7        /* 0 auto, 1 never, 2 always when the last wave is incomplete */
 } gemm_option_t;
 
 /* Set an option on a handle.  Errors: GEMM_ERR_INVALID_ARG for an unknown

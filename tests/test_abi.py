@@ -82,14 +82,17 @@ def test_product_code_never_touches_the_oracle():
 # ----------------------------------------------------------------- planner --
 
 def test_plan_square_nt():
-    """4096^3: 256 x 256 tiles on CTA pairs, 76 pairs on 152 SMs."""
+    """4096^3: 256 x 256 tiles on CTA pairs, 76 pairs on 152 SMs; the 28 tiles of
+    the incomplete fourth wave are shared out by stream-K."""
     p = G.plan(4096, 4096, 4096, 0, 1)
     assert p.path == G.PATH_TC_2CTA and p.swap_ab == 0
     assert p.a_kmajor == 1 and p.b_kmajor == 1
     assert p.bm == 256 and p.bk == 64 and p.bn == 256
-    assert p.split_k == 1 and p.units == p.tiles == 16 * 16
+    assert p.tiles == 16 * 16 and p.num_kb == 64
+    assert p.schedule == G.SCHED_STREAM_K and p.dp_tiles == 3 * 76 and 0 < p.sk_slots <= 76
     assert p.grid == 152 and p.repack_a == 0 and p.repack_b == 0
-    assert p.vector_store == 1 and p.launches == 1 and p.workspace_bytes == 0
+    assert p.vector_store == 1 and p.launches == 1
+    assert p.workspace_bytes >= p.sk_slots * 2 * 2 * 256 * 128 * 4   # partial slots x CTA pair
 
 
 @pytest.mark.parametrize("ta,tb,ak,bk", [(0, 0, 1, 0), (0, 1, 1, 1), (1, 0, 0, 0), (1, 1, 0, 1)])
@@ -102,15 +105,21 @@ def test_plan_lm_head_swaps():
     p = G.plan(64, 32000, 4096, 0, 1)
     assert p.swap_ab == 1 and p.path == G.PATH_TC_1CTA
     assert p.a_kmajor == 1 and p.b_kmajor == 1   # MMA A = weights (N x K), MMA B = activations (M x K)
-    assert p.bn == 64 and p.tiles == 250 and p.units == 250 * p.split_k
+    assert p.bn == 64 and p.tiles == 250
+    assert p.schedule == G.SCHED_STREAM_K and p.dp_tiles == 152   # one full wave, then 98 tiles shared
     assert p.vector_store == 0 and p.grid == 152
 
 
-def test_plan_few_tiles_split_k():
-    """Fewer tiles than half the SMs: the k-dimension is split, partials in the workspace."""
+def test_plan_few_tiles_stream_k():
+    """Far fewer tiles than SMs with a deep K: every tile's k-blocks are shared out."""
     p = G.plan(256, 256, 8192, 0, 1)
-    assert p.split_k > 1 and p.units == p.tiles * p.split_k
-    assert p.workspace_bytes >= p.units * (p.bm // 128) * p.bn * 128 * 4
+    assert p.schedule == G.SCHED_STREAM_K and p.dp_tiles == 0 and p.sk_slots > p.tiles
+    assert p.units > p.tiles and p.workspace_bytes > 0
+
+
+def test_plan_full_waves_need_no_stream_k():
+    p = G.plan(128 * 152, 64, 512, 0, 1)   # exactly one wave of 128 x 64 tiles
+    assert p.schedule == G.SCHED_TILES and p.units == p.tiles
 
 
 def test_plan_ragged_repacks_misaligned_b():
@@ -157,8 +166,12 @@ def test_plan_invariants(shape):
         I, J = (N, M) if p.swap_ab else (M, N)
         cg = 2 if p.path == G.PATH_TC_2CTA else 1
         assert p.bm == 128 * cg
-        assert p.tiles == -(-I // p.bm) * -(-J // p.bn)
-        assert p.units == p.tiles * p.split_k
+        assert p.tiles == -(-I // p.bm) * -(-J // p.bn) == p.tiles_i * p.tiles_j
+        assert p.num_kb == -(-K // 64)
+        if p.schedule == G.SCHED_TILES:
+            assert p.units == p.tiles * p.split_k and p.dp_tiles == p.tiles
+        else:
+            assert p.split_k == 1 and p.dp_tiles % (p.grid // cg) == 0 and p.units >= p.tiles
         assert 1 <= p.split_k <= max(1, -(-K // 64))
         assert p.grid == min(p.units, sm // cg) * cg
         assert 1 <= p.raster_group <= max(1, -(-I // p.bm))

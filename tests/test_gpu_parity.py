@@ -31,7 +31,7 @@ PATHS = {1: G.PATH_TC_1CTA, 2: G.PATH_TC_2CTA}
 def options(h, **kw):
     """Force planner options on the handle for the duration of a check."""
     codes = {"path": G.OPT_FORCE_PATH, "bn": G.OPT_FORCE_BN, "split": G.OPT_SPLIT_K, "raster": G.OPT_RASTER_GROUP,
-             "grid": G.OPT_MAX_GRID}
+             "grid": G.OPT_MAX_GRID, "stream_k": G.OPT_STREAM_K}
     try:
         for k, v in kw.items():
             h.set_option(codes[k], v)
@@ -120,12 +120,36 @@ def test_every_tile_configuration(h, cg, bn, transA, transB):
         _check(p, h)
 
 
+@pytest.mark.parametrize("grid", [4, 10, 26])
+@pytest.mark.parametrize("cg,bn", CONFIGS)
+def test_stream_k(h, cg, bn, grid):
+    """Stream-K tail forced on small grids: tiles cut into several pieces whose
+    partials are summed by the last piece to finish."""
+    p = inputs.make_problem("sk", 700, 900, 1000, 0, 1, "bf16", "f32", ("normal", 0, 1), ("normal", 0, 1),
+                            alpha=1.25, beta=-0.5, seed=grid + bn + cg)
+    with options(h, path=PATHS[cg], bn=bn, grid=grid, stream_k=2):
+        plan = G.plan(p.M, p.N, p.K, 0, 1, handle=h, beta=p.beta)
+        assert plan.schedule == G.SCHED_STREAM_K and plan.path == PATHS[cg] and plan.grid <= grid
+        _check(p, h)
+
+
+@pytest.mark.parametrize("cg,bn", CONFIGS)
+def test_stream_k_all_tiles_shared(h, cg, bn):
+    """Fewer tiles than CTAs and a deep K: no whole tiles, every tile is shared."""
+    p = inputs.make_problem("skdeep", 250, 250, 4000, 1, 0, "f16", "f16", ("uniform", -1, 1), ("uniform", -1, 1),
+                            seed=bn * cg)
+    with options(h, path=PATHS[cg], bn=bn, stream_k=2):
+        plan = G.plan(p.M, p.N, p.K, 1, 0, G.F16_F16, handle=h)
+        assert plan.schedule == G.SCHED_STREAM_K and plan.dp_tiles == 0
+        _check(p, h)
+
+
 @pytest.mark.parametrize("cg,bn", CONFIGS)
 def test_many_tiles_per_cta(h, cg, bn):
     """More tiles than CTAs: every CTA runs several tiles through both TMEM buffers."""
     p = inputs.make_problem("persist", 1100, 1500, 192, 0, 1, "bf16", "f32", ("normal", 0, 1), ("normal", 0, 1),
                             seed=3 * bn + cg)
-    with options(h, path=PATHS[cg], bn=bn, raster=3, grid=6):
+    with options(h, path=PATHS[cg], bn=bn, raster=3, grid=6, stream_k=1):
         plan = G.plan(p.M, p.N, p.K, 0, 1, handle=h)
         assert plan.grid <= 6 and plan.units >= 3 * plan.grid // cg
         _check(p, h)
