@@ -39,6 +39,7 @@ struct Options {
   int drop_load = 0;
   int max_grid = 0;
   int stream_k = 0;  // 0 auto, 1 off, 2 on
+  int stages = 0;    // 0: the configuration's maximum ring depth
 };
 
 // One stored operand, as the tensor-memory-accelerator copy engine will see it.
@@ -259,6 +260,7 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   P.bn = best.bn;
   P.bk = kBK;
   P.stages = tc_stages(best.bn, cg);
+  if (o.stages > 0 && o.stages < P.stages) P.stages = o.stages;
   P.schedule = pl.sched.mode;
   P.split_k = pl.sched.mode == kSchedTiles ? pl.sched.split_k : 1;
   P.tiles_i = pl.sched.tiles_i;
@@ -480,6 +482,10 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
       if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
       h->opt.stream_k = static_cast<int>(value);
       return GEMM_OK;
+    case GEMM_OPT_STAGES:
+      if (value < 0 || value > 64) return GEMM_ERR_INVALID_ARG;
+      h->opt.stages = static_cast<int>(value);
+      return GEMM_OK;
   }
   return GEMM_ERR_INVALID_ARG;
 }
@@ -572,6 +578,7 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
   a.sched = pl.sched;
   a.p_kmajor = P.a_kmajor;
   a.q_kmajor = P.b_kmajor;
+  a.stages = P.stages;
   a.idesc = make_idesc_f16(pl.bf16, !pl.p.kmajor, !pl.q.kmajor, kBM * cg, P.bn);
   a.alpha = alpha;
   a.beta = beta;

@@ -34,6 +34,7 @@ struct TcArgs {
   int32_t p_kmajor;      // P has K contiguous (else I contiguous)
   int32_t q_kmajor;      // Q has K contiguous (else J contiguous)
   uint32_t idesc;        // tcgen05 instruction descriptor
+  int32_t stages;        // ring stages in use, 1 .. the configuration's maximum
   float alpha, beta;
   void* C;
   int64_t c_si, c_sj;

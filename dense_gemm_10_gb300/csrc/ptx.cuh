@@ -264,6 +264,19 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
                : "memory");
 }
 
+// ------------------------------------------------------------ warp helpers --
+
+// True in exactly one lane of the (converged) warp.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, e;\n\t}"
+      : "=r"(p));
+  return p != 0;
+}
+
 // ---------------------------------------------------------- named barriers --
 
 // Barrier `id` over `count` threads; returns the OR of every participant's `pred`.

@@ -92,6 +92,16 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, TcCt
   }
 }
 
+// Lane 0 of a converged warp waits; the whole warp gets the outcome, so the
+// warp's control flow stays uniform (the issuing roles run as whole warps and
+// elect one lane to issue, which keeps their operands warp-uniform).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, TcCtrl* ctrl,
+                                          const TcArgs& a, int role, int which, bool honor_abort) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, ctrl, a, role, which, honor_abort) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 // ------------------------------------------------------------------ epilogue --
 
 __device__ __forceinline__ float load_c(const TcArgs& a, int64_t off) {
@@ -194,8 +204,8 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
     const int i0 = w.ti * Cfg::kTileM + static_cast<int>(rank) * kBM;
     const int j0 = w.tj * BN + static_cast<int>(rank) * Cfg::kQRows;
     for (int kb = w.kb0; kb < w.kb1; ++kb) {
-      if (!wait_bounded(smem_u32(&ctrl->empty[stage]), phase ^ 1u, ctrl, a, kRoleProducer,
-                        kBarEmpty, true)) {
+      if (!warp_wait(smem_u32(&ctrl->empty[stage]), phase ^ 1u, ctrl, a, kRoleProducer, kBarEmpty,
+                     true)) {
         ok = false;
         break;
       }
@@ -206,33 +216,36 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
       if (a.drop_load != 0 && blockIdx.x == 0 && nload == a.drop_load) {
         pending &= ~(1u << stage);  // test hook: this stage's barrier is never completed
       } else {
-        if (rank == 0) mbar_arrive_expect_tx(full_local, CG * Cfg::kStageBytes);
         const uint32_t sa = smem_u32(ring_a + stage * Cfg::kABytes);
         const uint32_t sb = smem_u32(ring_b + stage * Cfg::kBBytes);
         const int k0 = kb * kBK;
-        auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
-          if constexpr (CG == 2)
-            tma_load_2d_pair(dst, map, full, x, y);
-          else
-            tma_load_2d(dst, map, full, x, y);
-        };
-        if (a.p_kmajor) {
-          load(sa, map_p, k0, i0);
-        } else {
-          load(sa, map_p, i0, k0);
-          load(sa + kMnAtomBytes, map_p, i0 + 64, k0);
-        }
-        if (a.q_kmajor) {
-          load(sb, map_q, k0, j0);
-        } else {
+        if (elect_one()) {
+          if (rank == 0) mbar_arrive_expect_tx(full_local, CG * Cfg::kStageBytes);
+          auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
+            if constexpr (CG == 2)
+              tma_load_2d_pair(dst, map, full, x, y);
+            else
+              tma_load_2d(dst, map, full, x, y);
+          };
+          if (a.p_kmajor) {
+            load(sa, map_p, k0, i0);
+          } else {
+            load(sa, map_p, i0, k0);
+            load(sa + kMnAtomBytes, map_p, i0 + 64, k0);
+          }
+          if (a.q_kmajor) {
+            load(sb, map_q, k0, j0);
+          } else {
 #pragma unroll
-          for (int c = 0; c < Cfg::kQRows / 64; ++c)
-            load(sb + c * kMnAtomBytes, map_q, j0 + 64 * c, k0);
+            for (int c = 0; c < Cfg::kQRows / 64; ++c)
+              load(sb + c * kMnAtomBytes, map_q, j0 + 64 * c, k0);
+          }
         }
+        __syncwarp();
         pending |= 1u << stage;
         pending_parity = (pending_parity & ~(1u << stage)) | (phase << stage);
       }
-      if (++stage == Cfg::kStages) {
+      if (++stage == a.stages) {
         stage = 0;
         phase ^= 1u;
       }
@@ -241,12 +254,13 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
   // No copy may still be writing shared memory when the CTA exits.  The leader's
   // barrier counts both CTAs' bytes, so the leader's wait covers the pair; a
   // peer CTA is held at the final cluster barrier until the leader has waited.
-  if (rank == 0) {
+  if (rank == 0 && (threadIdx.x & 31) == 0) {
     for (int s = 0; s < Cfg::kStages; ++s)
       if (pending & (1u << s))
         wait_bounded(smem_u32(&ctrl->full[s]), (pending_parity >> s) & 1u, ctrl, a, kRoleProducer,
                      kBarDrain, false);
   }
+  __syncwarp();
 }
 
 template <int BN, int CG>
@@ -269,43 +283,51 @@ __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8
   for (; ok && work.next(w); ++it) {
     const int buf = it & 1;
     const uint32_t acc_parity = (it >> 1) & 1;
-    if (!wait_bounded(smem_u32(&ctrl->acc_empty[buf]), acc_parity ^ 1u, ctrl, a, kRoleMma,
-                      kBarAccEmpty, true))
+    if (!warp_wait(smem_u32(&ctrl->acc_empty[buf]), acc_parity ^ 1u, ctrl, a, kRoleMma,
+                   kBarAccEmpty, true))
       break;
     tc_fence_after_sync();
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
     for (int kb = w.kb0; kb < w.kb1; ++kb) {
-      if (!wait_bounded(smem_u32(&ctrl->full[stage]), phase, ctrl, a, kRoleMma, kBarFull, true)) {
+      if (!warp_wait(smem_u32(&ctrl->full[stage]), phase, ctrl, a, kRoleMma, kBarFull, true)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
       const uint32_t sa = smem_u32(ring_a + stage * Cfg::kABytes);
       const uint32_t sb = smem_u32(ring_b + stage * Cfg::kBBytes);
+      // K-major: the 16-wide k-slice starts 32 bytes further along each swizzled
+      // 128-byte row; 8-row groups are 1024 bytes apart.
+      // MN-major: the k-slice is 16 rows of 128 bytes further on; 8-row groups are
+      // 1024 bytes apart and swizzle atoms along M / N are kMnAtomBytes apart.
+      const uint32_t a_step = a.p_kmajor ? 32u : 2048u;
+      const uint32_t b_step = a.q_kmajor ? 32u : 2048u;
+      const uint64_t ad0 = smem_desc_sw128(sa, a.p_kmajor ? 16u : kMnAtomBytes, 1024);
+      const uint64_t bd0 = smem_desc_sw128(sb, a.q_kmajor ? 16u : kMnAtomBytes, 1024);
+      if (elect_one()) {
 #pragma unroll
-      for (int k = 0; k < kBK / 16; ++k) {
-        // K-major: the 16-wide k-slice starts 32 bytes further along each swizzled
-        // 128-byte row; 8-row groups are 1024 bytes apart.
-        // MN-major: the k-slice is 16 rows of 128 bytes further on; 8-row groups are
-        // 1024 bytes apart and swizzle atoms along M / N are kMnAtomBytes apart.
-        const uint64_t ad = a.p_kmajor ? smem_desc_sw128(sa + 32 * k, 16, 1024)
-                                       : smem_desc_sw128(sa + 2048 * k, kMnAtomBytes, 1024);
-        const uint64_t bd = a.q_kmajor ? smem_desc_sw128(sb + 32 * k, 16, 1024)
-                                       : smem_desc_sw128(sb + 2048 * k, kMnAtomBytes, 1024);
-        mma_f16_ss<CG>(d_tmem, ad, bd, a.idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < kBK / 16; ++k)  // the start address sits in the descriptor's low bits
+          mma_f16_ss<CG>(d_tmem, ad0 + ((a_step * k) >> 4), bd0 + ((b_step * k) >> 4), a.idesc,
+                         (kb > w.kb0 || k > 0) ? 1u : 0u);
+        commit(smem_u32(&ctrl->empty[stage]));  // frees the stage once these MMAs have read it
       }
-      commit(smem_u32(&ctrl->empty[stage]));  // frees the stage once these MMAs have read it
-      if (++stage == Cfg::kStages) {
+      __syncwarp();
+      if (++stage == a.stages) {
         stage = 0;
         phase ^= 1u;
       }
     }
     if (!ok) break;
-    commit(smem_u32(&ctrl->acc_full[buf]));  // accumulator ready for the epilogue(s)
+    if (elect_one()) commit(smem_u32(&ctrl->acc_full[buf]));  // accumulator ready for the epilogue(s)
+    __syncwarp();
   }
-  // Tensor Memory is freed only after every MMA issued here has finished.
-  mma_commit<CG>(smem_u32(&ctrl->mma_done));
-  wait_bounded(smem_u32(&ctrl->mma_done), 0, ctrl, a, kRoleMma, kBarDrain, false);
+  // Tensor Memory is freed only after every MMA issued here has finished.  The
+  // elected lane is the one that issued them, so its commit tracks them all.
+  if (elect_one()) {
+    mma_commit<CG>(smem_u32(&ctrl->mma_done));
+    wait_bounded(smem_u32(&ctrl->mma_done), 0, ctrl, a, kRoleMma, kBarDrain, false);
+  }
+  __syncwarp();
 }
 
 template <int BN, int CG>
@@ -445,12 +467,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = ctrl->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0)
-      producer_role<BN, CG>(&map_p, &map_q, a, ring_a, ring_b, ctrl, rank, first, stride);
-    __syncwarp();
+    producer_role<BN, CG>(&map_p, &map_q, a, ring_a, ring_b, ctrl, rank, first, stride);
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) mma_role<BN, CG>(a, ring_a, ring_b, ctrl, tmem_base, first, stride);
-    __syncwarp();
+    if (rank == 0) mma_role<BN, CG>(a, ring_a, ring_b, ctrl, tmem_base, first, stride);
   } else {
     epilogue_role<BN, CG>(a, ctrl, tmem_base, warp, lane, rank, first, stride);
   }

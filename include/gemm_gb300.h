@@ -189,7 +189,8 @@ typedef enum {
                                   must end the kernel with GEMM_ERR_TIMEOUT */
   GEMM_OPT_MAX_GRID = 6,       /* 0 auto, else at most this many CTAs (persistent CTAs then
                                   walk more tiles each) */
-  GEMM_OPT_STREAM_K = 7        /* 0 auto, 1 never, 2 always when the last wave is incomplete */
+  GEMM_OPT_STREAM_K = 7,       /* 0 auto, 1 never, 2 always when the last wave is incomplete */
+  GEMM_OPT_STAGES = 8          /* 0 auto (deepest ring that fits), else at most this many stages */
 } gemm_option_t;
 
 /* Set an option on a handle.  Errors: GEMM_ERR_INVALID_ARG for an unknown
