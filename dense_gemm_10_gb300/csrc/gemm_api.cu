@@ -617,3 +617,161 @@ gemm_status_t gemm_get_status(gemm_handle_t h, void* stream, int32_t* detail) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// gemm_run_noalloc: the same GEMM for callers that must not allocate device
+// memory.  Its scratch (repacked operands, partial tiles of split tiles,
+// arrival counters, the status word) lives in file-scope device arrays that
+// every GPU loading the library holds until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t{16} << 20;  // 16 MiB
+constexpr int kNoAllocCounters = 4096;
+constexpr int kNoAllocMaxDevices = 64;
+
+struct NoAllocDevice {
+  bool ready = false;
+  SlotTable slots;
+  int sm_count = 0;
+  uint8_t* scratch = nullptr;  // device addresses of the arrays below, for this device
+  int32_t* counters = nullptr;
+  int32_t* status = nullptr;
+};
+
+NoAllocDevice g_noalloc_devices[kNoAllocMaxDevices];
+std::mutex g_noalloc_mutex;
+
+}  // namespace
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+static __device__ __align__(256) int32_t g_noalloc_counters[kNoAllocCounters];
+static __device__ __align__(256) int32_t g_noalloc_status[64];
+
+// Once per device, with that device current: look up the arrays' device
+// addresses (in host code their names are only host-side stand-ins) and opt
+// the kernels in to their shared memory.  Allocates nothing.
+static gemm_status_t noalloc_setup(int device, NoAllocDevice** out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (device < 0 || device >= kNoAllocMaxDevices) return GEMM_ERR_NO_DEVICE;
+  NoAllocDevice& d = g_noalloc_devices[device];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_NO_DEVICE;
+    }
+    if (major != 10 || minor != 3) return GEMM_ERR_NO_DEVICE;
+    d.sm_count = sms;
+    d.slots = SlotTable::even(sms);
+    static const int kCfg[5][2] = {{1, 64}, {1, 128}, {1, 256}, {2, 128}, {2, 256}};
+    for (const auto& c : kCfg) {
+      int clusters = 0;
+      if (tc_prepare(c[1], c[0], &clusters) != cudaSuccess) return GEMM_ERR_CUDA;
+      if (c[0] == 2 && clusters > 0) d.slots.cg2[c[1] == 256 ? 2 : 1] = std::min(clusters, sms / 2);
+    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return GEMM_ERR_CUDA;
+    d.scratch = static_cast<uint8_t*>(p);
+    if (cudaGetSymbolAddress(&p, g_noalloc_counters) != cudaSuccess) return GEMM_ERR_CUDA;
+    d.counters = static_cast<int32_t*>(p);
+    if (cudaGetSymbolAddress(&p, g_noalloc_status) != cudaSuccess) return GEMM_ERR_CUDA;
+    d.status = static_cast<int32_t*>(p);
+    d.ready = true;
+  }
+  *out = &d;
+  return GEMM_OK;
+}
+
+static int64_t counters_needed(const Sched& s, int cg) {
+  if (s.mode == kSchedStreamK)
+    return (static_cast<int64_t>(s.tiles_i) * s.tiles_j - s.dp_tiles) * cg;
+  return s.split_k > 1 ? static_cast<int64_t>(s.tiles_i) * s.tiles_j * cg : 0;
+}
+
+extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, int64_t M, int64_t N,
+                                          int64_t K, float alpha, const void* A, int64_t lda,
+                                          const void* B, int64_t ldb, float beta, void* C,
+                                          int64_t ldc, gemm_dtype_t dtype, void* stream) {
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_NO_DEVICE;
+  }
+  NoAllocDevice* d = nullptr;
+  gemm_status_t s = noalloc_setup(device, &d);
+  if (s != GEMM_OK) return s;
+  Options o;
+  Plan pl;
+  s = make_plan(o, d->slots, transA, transB, M, N, K, A, lda, B, ldb, beta, C, ldc, dtype, &pl);
+  if (s != GEMM_OK) return s;
+  int cg = pl.pub.path == GEMM_PATH_TC_2CTA ? 2 : 1;
+  if (pl.pub.path >= GEMM_PATH_TC_1CTA &&
+      (static_cast<size_t>(pl.pub.workspace_bytes) > kNoAllocScratchBytes ||
+       counters_needed(pl.sched, cg) > kNoAllocCounters)) {
+    o.stream_k = 1;  // whole tiles need no partial sums: plan again without the stream-K tail
+    s = make_plan(o, d->slots, transA, transB, M, N, K, A, lda, B, ldb, beta, C, ldc, dtype, &pl);
+    if (s != GEMM_OK) return s;
+    cg = pl.pub.path == GEMM_PATH_TC_2CTA ? 2 : 1;
+    if (static_cast<size_t>(pl.pub.workspace_bytes) > kNoAllocScratchBytes ||
+        counters_needed(pl.sched, cg) > kNoAllocCounters)
+      return GEMM_ERR_WORKSPACE;  // needs more scratch than the fixed 16 MiB array holds
+  }
+  const gemm_plan_t& P = pl.pub;
+  if (P.path == GEMM_PATH_NOOP) return GEMM_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (P.path == GEMM_PATH_SCALE_C) {
+    e = scale_c_launch(C, pl.c_type, M, N, ldc, beta, d->sm_count, st);
+    return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+  }
+  // The arrays keep the previous call's contents: clear what must start at zero.
+  e = cudaMemsetAsync(d->status, 0, sizeof(int32_t), st);
+  const int64_t nctr = counters_needed(pl.sched, cg);
+  if (e == cudaSuccess && nctr > 0) e = cudaMemsetAsync(d->counters, 0, nctr * sizeof(int32_t), st);
+  if (e != cudaSuccess) return GEMM_ERR_CUDA;
+
+  const void* pbase = pl.p.ptr;
+  const void* qbase = pl.q.ptr;
+  int64_t pld = pl.p.ld, qld = pl.q.ld;
+  for (int w = 0; w < 2; ++w) {
+    const Operand& op = w == 0 ? pl.p : pl.q;
+    if (!op.repack) continue;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(d->scratch + op.ws_offset);
+    e = repack16_launch(static_cast<const uint16_t*>(op.ptr), op.ld, dst, op.packed_ld, op.rows,
+                        op.cols, d->sm_count, st);
+    if (e != cudaSuccess) return GEMM_ERR_CUDA;
+    if (w == 0) { pbase = dst; pld = op.packed_ld; } else { qbase = dst; qld = op.packed_ld; }
+  }
+  CUtensorMap map_p, map_q;
+  s = encode_operand(&map_p, pl.p, pbase, pld, pl.bf16, kBM);
+  if (s != GEMM_OK) return s;
+  s = encode_operand(&map_q, pl.q, qbase, qld, pl.bf16, P.bn / cg);
+  if (s != GEMM_OK) return s;
+  TcArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.I = static_cast<int32_t>(pl.I);
+  a.J = static_cast<int32_t>(pl.J);
+  a.K = static_cast<int32_t>(pl.K);
+  a.sched = pl.sched;
+  a.p_kmajor = P.a_kmajor;
+  a.q_kmajor = P.b_kmajor;
+  a.stages = P.stages;
+  a.idesc = make_idesc_f16(pl.bf16, !pl.p.kmajor, !pl.q.kmajor, kBM * cg, P.bn);
+  a.alpha = alpha;
+  a.beta = beta;
+  a.C = C;
+  a.c_si = pl.c_si;
+  a.c_sj = pl.c_sj;
+  a.c_type = pl.c_type;
+  a.vec_store = P.vector_store;
+  a.partials = needs_partials(pl.sched) ? reinterpret_cast<float*>(d->scratch + pl.partial_offset) : nullptr;
+  a.counters = d->counters;
+  a.status = d->status;
+  a.wait_limit_ns = static_cast<uint64_t>(o.wait_limit_ns);
+  a.drop_load = 0;
+  e = tc_launch(P.bn, cg, map_p, map_q, a, P.grid, st);
+  return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}

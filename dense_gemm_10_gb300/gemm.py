@@ -48,6 +48,8 @@ SIGNATURES = {
                          _i64, _i32, ctypes.POINTER(Plan)]),
     "gemm_set_option": (_i32, [_vp, _i32, _i64]),
     "gemm_launch_count": (_i32, [_vp, ctypes.POINTER(_u64)]),
+    "gemm_run_noalloc": (_i32, [_i32, _i32, _i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _i32,
+                                _vp]),
 }
 
 _lib = None

@@ -200,6 +200,39 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
 /* Kernels launched by gemm_run on this handle since it was created. */
 gemm_status_t gemm_launch_count(gemm_handle_t h, uint64_t* count);
 
+/* ---------------------------------------------------------------------------
+ * gemm_run_noalloc: the GEMM of gemm_run for callers that must not allocate
+ * device memory -- for example a caller whose device memory is fully reserved
+ * up front by its own allocator, or one that cannot afford the device-wide
+ * synchronisation that cudaMalloc / cudaFree can imply.  (The source pages
+ * have no counterpart; this is a property of the library's interface.)
+ *
+ * Same arguments and semantics as gemm_run, on the current CUDA device and
+ * without a handle; default options apply.  It calls no cudaMalloc, cudaFree
+ * or other allocating routine.  Its scratch -- repacked copies of operands the
+ * copy engine cannot read directly, partial sums of tiles split by the
+ * stream-K schedule, their arrival counters and a status word -- lives in
+ * fixed file-scope device arrays of the library: 16 MiB of scratch and 4096
+ * counters, which every GPU that loads the library holds until the process
+ * exits.  A call whose plan would need more (a larger repack, or more partial
+ * sums than fit) is first re-planned without the stream-K tail, which needs
+ * no partial sums; if it still does not fit, the call returns
+ * GEMM_ERR_WORKSPACE and launches nothing.
+ *
+ * The first call on a device sets that device up (looks up the arrays'
+ * device addresses, opts the kernels in to their shared memory); make that
+ * first call before any stream capture.  Every call shares the same arrays
+ * and each call clears the counters and status word it uses, so calls that
+ * overlap on the GPU (two streams, or two host threads) race on them: order
+ * them on one stream.  A kernel that gives up on a barrier records it only in
+ * the internal status word, which this entry point does not report.
+ * Returns GEMM_OK, the argument errors of gemm_run, GEMM_ERR_NO_DEVICE,
+ * GEMM_ERR_WORKSPACE or GEMM_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, int64_t M, int64_t N, int64_t K,
+                               float alpha, const void* A, int64_t lda, const void* B, int64_t ldb,
+                               float beta, void* C, int64_t ldc, gemm_dtype_t dtype, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
