@@ -19,8 +19,9 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libgemm_gb300.so")
 HEADER = os.path.join(ROOT, "include", "gemm_gb300.h")
 
-SOURCES = ["gemm_api.cu", "tc_dispatch.cu", "tc_gemm_bn64_cg1.cu", "tc_gemm_bn128_cg1.cu",
-           "tc_gemm_bn256_cg1.cu", "tc_gemm_bn128_cg2.cu", "tc_gemm_bn256_cg2.cu", "aux_kernels.cu"]
+SOURCES = ["gemm_api.cu", "tc_dispatch.cu", "tc_gemm_bn64_cg1_mc1.cu", "tc_gemm_bn128_cg1_mc1.cu",
+           "tc_gemm_bn256_cg1_mc1.cu", "tc_gemm_bn128_cg2_mc1.cu", "tc_gemm_bn256_cg2_mc1.cu",
+           "tc_gemm_bn256_cg2_mc2.cu", "aux_kernels.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-I" + os.path.join(ROOT, "include")]

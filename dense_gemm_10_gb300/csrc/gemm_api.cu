@@ -71,29 +71,45 @@ bool tma_aligned(const void* p, int64_t ld) {
   return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((ld * 2) % 16 == 0);
 }
 
-// Relative time of one k-block of one output tile for each tile configuration
-// (cg, bn), in units of the CTA-pair 256 x 256 tile, from GB300 measurements
-// of the 4096^3 and 8192 x 12288 x 4096 bf16 GEMMs.
-double tile_kb_cost(int cg, int bn) {
-  if (cg == 2) return bn == 256 ? 1.0 : 0.62;
-  return bn == 256 ? 1.15 : bn == 128 ? 0.85 : 0.6;
+// Relative time of one k-block of one schedule tile for each tile
+// configuration, in units of the CTA-pair 256 x 256 tile, from GB300
+// measurements of the 4096^3 and 8192 x 12288 x 4096 bf16 GEMMs.  (A multicast
+// cluster's schedule tile is two 256 x 256 tiles worked side by side.)
+double tile_kb_cost(const TileConfig& c) {
+  if (c.mc == 2) return 0.85;
+  if (c.cg == 2) return c.bn == 256 ? 1.0 : 0.62;
+  return c.bn == 256 ? 1.15 : c.bn == 128 ? 0.85 : 0.6;
 }
 
-// Resident slots (CTAs, or CTA pairs when cg == 2) per tile configuration.
+// Resident schedule slots (CTAs, CTA pairs or clusters) per tile configuration.
 struct SlotTable {
-  int cg1 = 1, cg2[3] = {1, 1, 1};  // cg2 by bn 64 / 128 / 256
-  int of(int cg, int bn) const { return cg == 1 ? cg1 : cg2[bn == 256 ? 2 : bn == 128 ? 1 : 0]; }
+  int n[kNumTileConfigs] = {1, 1, 1, 1, 1, 1};
+  int of(int cfg) const { return n[cfg]; }
   static SlotTable even(int sm_count) {
     SlotTable t;
-    t.cg1 = std::max(1, sm_count);
-    for (int& v : t.cg2) v = std::max(1, sm_count / 2);
+    for (int i = 0; i < kNumTileConfigs; ++i)
+      t.n[i] = std::max(1, sm_count / (kTileConfigs[i].cg * kTileConfigs[i].mc));
     return t;
   }
 };
 
+// Opt every configuration in to its shared memory on the current device and
+// record how many of its clusters can be resident (a cluster sits in one GPC).
+cudaError_t measure_slots(int sm_count, SlotTable* t) {
+  *t = SlotTable::even(sm_count);
+  for (int i = 0; i < kNumTileConfigs; ++i) {
+    const TileConfig& c = kTileConfigs[i];
+    int clusters = 0;
+    cudaError_t e = tc_prepare(c.bn, c.cg, c.mc, &clusters);
+    if (e != cudaSuccess) return e;
+    if (c.cg * c.mc > 1 && clusters > 0) t->n[i] = std::min(clusters, sm_count / (c.cg * c.mc));
+  }
+  return cudaSuccess;
+}
+
 struct Choice {
   bool valid = false;
-  int cg = 1, bn = 64, slots = 1;
+  int cfg = 0, cg = 1, bn = 64, mc = 1, slots = 1;
   double cost = 1e300;
   Sched sched{};
 };
@@ -126,11 +142,15 @@ double sk_tail_cost(int64_t tiles, int64_t num_kb, int64_t g) {
   return per_slot + 1.0 + 0.5 * contrib;
 }
 
-Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64_t num_kb, int cg,
-                       int bn, int slots) {
+Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64_t num_kb, int cfg,
+                       int slots) {
   Choice ch;
-  ch.cg = cg;
-  ch.bn = bn;
+  const TileConfig& tc = kTileConfigs[cfg];
+  const int cl = tc.cg * tc.mc;  // CTAs per slot
+  ch.cfg = cfg;
+  ch.cg = tc.cg;
+  ch.bn = tc.bn;
+  ch.mc = tc.mc;
   ch.slots = slots;
   const int64_t tiles = tiles_i * tiles_j;
   Sched& s = ch.sched;
@@ -142,11 +162,10 @@ Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64
   s.split_k = 1;
   if (o.split_k) {  // an explicit split-K request
     const int64_t split = std::min<int64_t>(o.split_k, num_kb);
-    if (tiles * cg > kCounterCap) return ch;
+    if (tiles * cl > kCounterCap) return ch;
     s.split_k = static_cast<int32_t>(split);
     ch.cost = static_cast<double>(cdiv(tiles * split, slots)) *
-              (static_cast<double>(cdiv(num_kb, split)) + (split > 1 ? 1.5 : 0.0)) *
-              tile_kb_cost(cg, bn);
+              (static_cast<double>(cdiv(num_kb, split)) + (split > 1 ? 1.5 : 0.0)) * tile_kb_cost(tc);
     ch.valid = true;
     return ch;
   }
@@ -155,7 +174,7 @@ Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64
   // Stream-K tail: the tiles of the incomplete last wave shared by g slots.
   const int64_t full_waves = tiles / slots;
   const int64_t sk_tiles = tiles - full_waves * slots;
-  if (o.stream_k != 1 && sk_tiles > 0 && sk_tiles * cg <= kCounterCap) {
+  if (o.stream_k != 1 && sk_tiles > 0 && sk_tiles * cl <= kCounterCap) {
     const int64_t iters = sk_tiles * num_kb;
     int64_t best_g = 0;
     double best_tail = 1e300;
@@ -175,7 +194,7 @@ Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64
       s.sk_iters = iters;
     }
   }
-  ch.cost = best * tile_kb_cost(cg, bn);
+  ch.cost = best * tile_kb_cost(tc);
   ch.valid = true;
   return ch;
 }
@@ -236,30 +255,33 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
 
   // Tile configuration and schedule: the configuration with the lowest
   // estimated time, est_time() below.
-  static const int kConfigs[5][2] = {{2, 256}, {2, 128}, {1, 256}, {1, 128}, {1, 64}};
+  static const int kPreference[kNumTileConfigs] = {5, 4, 3, 2, 1, 0};  // ties go to the first
   Choice best;
-  for (const auto& c : kConfigs) {
-    const int cg = c[0], bn = c[1];
-    if (o.force_path == GEMM_PATH_TC_1CTA && cg != 1) continue;
-    if (o.force_path == GEMM_PATH_TC_2CTA && cg != 2) continue;
-    if (o.force_bn && bn != o.force_bn) continue;
-    if (!o.force_bn && bn > 64 && pl.J <= bn / 2) continue;  // too wide for J
-    if (!o.force_path && cg == 2 && pl.I <= kBM) continue;   // one row of tiles
-    int nslots = slots.of(cg, bn);
-    if (o.max_grid) nslots = std::min(nslots, std::max(1, o.max_grid / cg));
-    Choice ch = choose_schedule(o, cdiv(pl.I, kBM * cg), cdiv(pl.J, bn), num_kb, cg, bn, nslots);
+  for (int cfg : kPreference) {
+    const TileConfig& c = kTileConfigs[cfg];
+    const int path = c.mc == 2 ? GEMM_PATH_TC_2CTA_MULTICAST : c.cg == 2 ? GEMM_PATH_TC_2CTA : GEMM_PATH_TC_1CTA;
+    if (o.force_path && o.force_path != path) continue;
+    if (o.force_bn && c.bn != o.force_bn) continue;
+    if (!o.force_bn && c.bn > 64 && pl.J <= c.bn / 2) continue;       // too wide for J
+    if (!o.force_path && c.cg == 2 && pl.I <= kBM) continue;          // one row of tiles
+    if (!o.force_path && c.mc == 2 && cdiv(pl.J, c.bn) < 2) continue;  // nothing to share
+    int nslots = slots.of(cfg);
+    if (o.max_grid) nslots = std::min(nslots, std::max(1, o.max_grid / (c.cg * c.mc)));
+    Choice ch = choose_schedule(o, cdiv(pl.I, kBM * c.cg), cdiv(cdiv(pl.J, c.bn), c.mc), num_kb, cfg, nslots);
     if (ch.valid && ch.cost < best.cost - 1e-9) best = ch;
   }
   if (!best.valid) return GEMM_ERR_INVALID_ARG;  // forced options admit no configuration
   const int cg = best.cg;
+  const int cl = best.cg * best.mc;
   pl.sched = best.sched;
   pl.sched.raster_group = o.raster_group ? o.raster_group : 8;
   if (pl.sched.raster_group > pl.sched.tiles_i) pl.sched.raster_group = pl.sched.tiles_i;
-  P.path = cg == 2 ? GEMM_PATH_TC_2CTA : GEMM_PATH_TC_1CTA;
+  P.path = best.mc == 2 ? GEMM_PATH_TC_2CTA_MULTICAST : cg == 2 ? GEMM_PATH_TC_2CTA : GEMM_PATH_TC_1CTA;
+  P.cluster = cl;
   P.bm = kBM * cg;
   P.bn = best.bn;
   P.bk = kBK;
-  P.stages = tc_stages(best.bn, cg);
+  P.stages = tc_stages(best.bn, cg, best.mc);
   if (o.stages > 0 && o.stages < P.stages) P.stages = o.stages;
   P.schedule = pl.sched.mode;
   P.split_k = pl.sched.mode == kSchedTiles ? pl.sched.split_k : 1;
@@ -271,7 +293,7 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   P.sk_slots = pl.sched.mode == kSchedStreamK ? pl.sched.sk_slots : 0;
   P.units = count_units(pl.sched);
   P.raster_group = pl.sched.raster_group;
-  P.grid = static_cast<int32_t>(std::min<int64_t>(best.slots, std::max<int64_t>(P.units, 1)) * cg);
+  P.grid = static_cast<int32_t>(std::min<int64_t>(best.slots, std::max<int64_t>(P.units, 1)) * cl);
 
   // Workspace: repacked operands, then partial tiles of split tiles.
   size_t ws = 0;
@@ -287,7 +309,7 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   P.repack_b = (swap ? pl.p.repack : pl.q.repack) ? 1 : 0;
   if (needs_partials(pl.sched)) {
     pl.partial_offset = ws;
-    ws = round_up(ws + static_cast<size_t>(partial_slots(pl.sched)) * cg * best.bn * kBM * 4, 256);
+    ws = round_up(ws + static_cast<size_t>(partial_slots(pl.sched)) * cl * best.bn * kBM * 4, 256);
   }
   P.workspace_bytes = static_cast<int64_t>(ws);
   P.vector_store = (!swap && reinterpret_cast<uintptr_t>(C) % 16 == 0 && (ldc * c_elem) % 16 == 0) ? 1 : 0;
@@ -364,7 +386,7 @@ struct gemm_handle_s {
   size_t ws_bytes = 0;
   uint64_t launches = 0;
   int last_cuda_error = 0;
-  SlotTable slots;  // resident CTAs / CTA pairs per kernel configuration
+  SlotTable slots;  // resident slots (CTAs, pairs, clusters) per kernel configuration
   Options opt;
 };
 
@@ -392,16 +414,8 @@ gemm_status_t gemm_create(gemm_handle_t* out, int device) {
   h->sm_count = prop.multiProcessorCount;
   DeviceGuard g(device);
   // Opt every kernel configuration in to its shared memory, and count how many
-  // CTA pairs can be resident at once (a pair must sit inside one GPC).
-  h->slots = SlotTable::even(h->sm_count);
-  static const int kCfg[5][2] = {{1, 64}, {1, 128}, {1, 256}, {2, 128}, {2, 256}};
-  cudaError_t e = cudaSuccess;
-  for (const auto& c : kCfg) {
-    int clusters = 0;
-    e = tc_prepare(c[1], c[0], &clusters);
-    if (e != cudaSuccess) break;
-    if (c[0] == 2 && clusters > 0) h->slots.cg2[c[1] == 256 ? 2 : 1] = std::min(clusters, h->sm_count / 2);
-  }
+  // of its clusters can be resident at once.
+  cudaError_t e = measure_slots(h->sm_count, &h->slots);
   if (e == cudaSuccess) e = cudaMalloc(&h->d_status, sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMalloc(&h->d_counters, kCounterCap * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(int32_t));
@@ -454,7 +468,8 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
       h->opt.wait_limit_ns = value;
       return GEMM_OK;
     case GEMM_OPT_FORCE_PATH:
-      if (value != 0 && value != GEMM_PATH_TC_1CTA && value != GEMM_PATH_TC_2CTA)
+      if (value != 0 && value != GEMM_PATH_TC_1CTA && value != GEMM_PATH_TC_2CTA &&
+          value != GEMM_PATH_TC_2CTA_MULTICAST)
         return GEMM_ERR_INVALID_ARG;
       h->opt.force_path = static_cast<int>(value);
       return GEMM_OK;
@@ -546,7 +561,8 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
     h->d_ws = nw;
     h->ws_bytes = want;
   }
-  const int cg = P.path == GEMM_PATH_TC_2CTA ? 2 : 1;
+  const int cg = P.bm / kBM;
+  const int mc = P.cluster / cg;
 
   // Operands that the copy engine cannot read directly are repacked first.
   const void* pbase = pl.p.ptr;
@@ -565,7 +581,7 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
   }
 
   CUtensorMap map_p, map_q;
-  s = encode_operand(&map_p, pl.p, pbase, pld, pl.bf16, kBM);
+  s = encode_operand(&map_p, pl.p, pbase, pld, pl.bf16, kBM / mc);
   if (s != GEMM_OK) return s;
   s = encode_operand(&map_q, pl.q, qbase, qld, pl.bf16, P.bn / cg);
   if (s != GEMM_OK) return s;
@@ -592,7 +608,7 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
   a.status = h->d_status;
   a.wait_limit_ns = static_cast<uint64_t>(h->opt.wait_limit_ns);
   a.drop_load = h->opt.drop_load;
-  e = tc_launch(P.bn, cg, map_p, map_q, a, P.grid, st);
+  e = tc_launch(P.bn, cg, mc, map_p, map_q, a, P.grid, st);
   if (e != cudaSuccess) return cuda_fail(h, e);
   h->launches += 1;
   return GEMM_OK;
@@ -665,13 +681,7 @@ static gemm_status_t noalloc_setup(int device, NoAllocDevice** out) {
     }
     if (major != 10 || minor != 3) return GEMM_ERR_NO_DEVICE;
     d.sm_count = sms;
-    d.slots = SlotTable::even(sms);
-    static const int kCfg[5][2] = {{1, 64}, {1, 128}, {1, 256}, {2, 128}, {2, 256}};
-    for (const auto& c : kCfg) {
-      int clusters = 0;
-      if (tc_prepare(c[1], c[0], &clusters) != cudaSuccess) return GEMM_ERR_CUDA;
-      if (c[0] == 2 && clusters > 0) d.slots.cg2[c[1] == 256 ? 2 : 1] = std::min(clusters, sms / 2);
-    }
+    if (measure_slots(sms, &d.slots) != cudaSuccess) return GEMM_ERR_CUDA;
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return GEMM_ERR_CUDA;
     d.scratch = static_cast<uint8_t*>(p);
@@ -685,10 +695,10 @@ static gemm_status_t noalloc_setup(int device, NoAllocDevice** out) {
   return GEMM_OK;
 }
 
-static int64_t counters_needed(const Sched& s, int cg) {
+static int64_t counters_needed(const Sched& s, int cluster) {
   if (s.mode == kSchedStreamK)
-    return (static_cast<int64_t>(s.tiles_i) * s.tiles_j - s.dp_tiles) * cg;
-  return s.split_k > 1 ? static_cast<int64_t>(s.tiles_i) * s.tiles_j * cg : 0;
+    return (static_cast<int64_t>(s.tiles_i) * s.tiles_j - s.dp_tiles) * cluster;
+  return s.split_k > 1 ? static_cast<int64_t>(s.tiles_i) * s.tiles_j * cluster : 0;
 }
 
 extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, int64_t M, int64_t N,
@@ -707,18 +717,18 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   Plan pl;
   s = make_plan(o, d->slots, transA, transB, M, N, K, A, lda, B, ldb, beta, C, ldc, dtype, &pl);
   if (s != GEMM_OK) return s;
-  int cg = pl.pub.path == GEMM_PATH_TC_2CTA ? 2 : 1;
   if (pl.pub.path >= GEMM_PATH_TC_1CTA &&
       (static_cast<size_t>(pl.pub.workspace_bytes) > kNoAllocScratchBytes ||
-       counters_needed(pl.sched, cg) > kNoAllocCounters)) {
+       counters_needed(pl.sched, pl.pub.cluster) > kNoAllocCounters)) {
     o.stream_k = 1;  // whole tiles need no partial sums: plan again without the stream-K tail
     s = make_plan(o, d->slots, transA, transB, M, N, K, A, lda, B, ldb, beta, C, ldc, dtype, &pl);
     if (s != GEMM_OK) return s;
-    cg = pl.pub.path == GEMM_PATH_TC_2CTA ? 2 : 1;
     if (static_cast<size_t>(pl.pub.workspace_bytes) > kNoAllocScratchBytes ||
-        counters_needed(pl.sched, cg) > kNoAllocCounters)
+        counters_needed(pl.sched, pl.pub.cluster) > kNoAllocCounters)
       return GEMM_ERR_WORKSPACE;  // needs more scratch than the fixed 16 MiB array holds
   }
+  const int cg = pl.pub.path >= GEMM_PATH_TC_1CTA ? pl.pub.bm / kBM : 1;
+  const int mc = pl.pub.path >= GEMM_PATH_TC_1CTA ? pl.pub.cluster / cg : 1;
   const gemm_plan_t& P = pl.pub;
   if (P.path == GEMM_PATH_NOOP) return GEMM_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -729,7 +739,7 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   }
   // The arrays keep the previous call's contents: clear what must start at zero.
   e = cudaMemsetAsync(d->status, 0, sizeof(int32_t), st);
-  const int64_t nctr = counters_needed(pl.sched, cg);
+  const int64_t nctr = counters_needed(pl.sched, P.cluster);
   if (e == cudaSuccess && nctr > 0) e = cudaMemsetAsync(d->counters, 0, nctr * sizeof(int32_t), st);
   if (e != cudaSuccess) return GEMM_ERR_CUDA;
 
@@ -746,7 +756,7 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
     if (w == 0) { pbase = dst; pld = op.packed_ld; } else { qbase = dst; qld = op.packed_ld; }
   }
   CUtensorMap map_p, map_q;
-  s = encode_operand(&map_p, pl.p, pbase, pld, pl.bf16, kBM);
+  s = encode_operand(&map_p, pl.p, pbase, pld, pl.bf16, kBM / mc);
   if (s != GEMM_OK) return s;
   s = encode_operand(&map_q, pl.q, qbase, qld, pl.bf16, P.bn / cg);
   if (s != GEMM_OK) return s;
@@ -772,6 +782,6 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   a.status = d->status;
   a.wait_limit_ns = static_cast<uint64_t>(o.wait_limit_ns);
   a.drop_load = 0;
-  e = tc_launch(P.bn, cg, map_p, map_q, a, P.grid, st);
+  e = tc_launch(P.bn, cg, mc, map_p, map_q, a, P.grid, st);
   return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

@@ -47,15 +47,21 @@ struct TcArgs {
   int32_t drop_load;     // tests only: CTA 0 skips its drop_load-th k-block load (1-based)
 };
 
-// Tile configurations: bn in {64, 128, 256} with one CTA per tile (cg == 1), or
-// bn in {128, 256} with a CTA pair per 256-row tile (cg == 2).
-bool tc_supported(int bn, int cg);
-int tc_stages(int bn, int cg);
-// One-time per device: opt in to the kernel's shared memory; for cg == 2 also
-// reports how many CTA pairs can be resident at once.
-cudaError_t tc_prepare(int bn, int cg, int* max_clusters);
-// grid = CTAs (a multiple of cg).
-cudaError_t tc_launch(int bn, int cg, const CUtensorMap& map_p, const CUtensorMap& map_q,
+// Tile configurations: a tile of (128 * cg) x bn per CTA (cg == 1) or CTA
+// pair (cg == 2); mc == 2 clusters two pairs on neighbouring tiles of one tile
+// row, which share the P tile by multicast.
+struct TileConfig {
+  int bn, cg, mc;
+};
+constexpr int kNumTileConfigs = 6;
+extern const TileConfig kTileConfigs[kNumTileConfigs];
+int tc_config_index(int bn, int cg, int mc);  // -1 if not built
+int tc_stages(int bn, int cg, int mc);
+// One-time per device: opt in to the kernel's shared memory; for clusters also
+// report how many can be resident at once.
+cudaError_t tc_prepare(int bn, int cg, int mc, int* max_clusters);
+// grid = CTAs (a multiple of cg * mc).
+cudaError_t tc_launch(int bn, int cg, int mc, const CUtensorMap& map_p, const CUtensorMap& map_q,
                       const TcArgs& args, int grid, cudaStream_t stream);
 
 // dst[r * ldd + c] = src[r * lds + c] for 16-bit elements, r < rows, c < cols.

@@ -1,45 +1,63 @@
-// tc_dispatch.cu -- choose the kernel instantiation for a tile width and CTA group.
+// tc_dispatch.cu -- the kernel instantiation for a tile configuration.
 #include "tc_gemm.cuh"
 
 namespace g10 {
 
-#define TC_DECLARE(BN, CG)                                                                  \
-  cudaError_t tc_prepare_bn##BN##_cg##CG(int* max_clusters);                                \
-  cudaError_t tc_launch_bn##BN##_cg##CG(const CUtensorMap&, const CUtensorMap&, const TcArgs&, \
-                                        int, cudaStream_t);
-TC_DECLARE(64, 1)
-TC_DECLARE(128, 1)
-TC_DECLARE(256, 1)
-TC_DECLARE(128, 2)
-TC_DECLARE(256, 2)
+#define TC_DECLARE(BN, CG, MC)                                                                     \
+  cudaError_t tc_prepare_bn##BN##_cg##CG##_mc##MC(int* max_clusters);                             \
+  cudaError_t tc_launch_bn##BN##_cg##CG##_mc##MC(const CUtensorMap&, const CUtensorMap&,            \
+                                                 const TcArgs&, int, cudaStream_t);
+TC_DECLARE(64, 1, 1)
+TC_DECLARE(128, 1, 1)
+TC_DECLARE(256, 1, 1)
+TC_DECLARE(128, 2, 1)
+TC_DECLARE(256, 2, 1)
+TC_DECLARE(256, 2, 2)
 
-bool tc_supported(int bn, int cg) {
-  return (cg == 1 && (bn == 64 || bn == 128 || bn == 256)) || (cg == 2 && (bn == 128 || bn == 256));
+const TileConfig kTileConfigs[kNumTileConfigs] = {
+    {64, 1, 1}, {128, 1, 1}, {256, 1, 1}, {128, 2, 1}, {256, 2, 1}, {256, 2, 2}};
+
+int tc_config_index(int bn, int cg, int mc) {
+  for (int i = 0; i < kNumTileConfigs; ++i)
+    if (kTileConfigs[i].bn == bn && kTileConfigs[i].cg == cg && kTileConfigs[i].mc == mc) return i;
+  return -1;
 }
 
-int tc_stages(int bn, int cg) {
-  if (cg == 2) return bn == 256 ? TcConfig<256, 2>::kStages : TcConfig<128, 2>::kStages;
-  return bn == 256 ? TcConfig<256, 1>::kStages
-                   : bn == 128 ? TcConfig<128, 1>::kStages : TcConfig<64, 1>::kStages;
+int tc_stages(int bn, int cg, int mc) {
+  switch (tc_config_index(bn, cg, mc)) {
+    case 0: return TcConfig<64, 1, 1>::kStages;
+    case 1: return TcConfig<128, 1, 1>::kStages;
+    case 2: return TcConfig<256, 1, 1>::kStages;
+    case 3: return TcConfig<128, 2, 1>::kStages;
+    case 4: return TcConfig<256, 2, 1>::kStages;
+    case 5: return TcConfig<256, 2, 2>::kStages;
+  }
+  return 0;
 }
 
-cudaError_t tc_prepare(int bn, int cg, int* max_clusters) {
+cudaError_t tc_prepare(int bn, int cg, int mc, int* max_clusters) {
   *max_clusters = 0;
-  if (cg == 1 && bn == 64) return tc_prepare_bn64_cg1(max_clusters);
-  if (cg == 1 && bn == 128) return tc_prepare_bn128_cg1(max_clusters);
-  if (cg == 1 && bn == 256) return tc_prepare_bn256_cg1(max_clusters);
-  if (cg == 2 && bn == 128) return tc_prepare_bn128_cg2(max_clusters);
-  if (cg == 2 && bn == 256) return tc_prepare_bn256_cg2(max_clusters);
+  switch (tc_config_index(bn, cg, mc)) {
+    case 0: return tc_prepare_bn64_cg1_mc1(max_clusters);
+    case 1: return tc_prepare_bn128_cg1_mc1(max_clusters);
+    case 2: return tc_prepare_bn256_cg1_mc1(max_clusters);
+    case 3: return tc_prepare_bn128_cg2_mc1(max_clusters);
+    case 4: return tc_prepare_bn256_cg2_mc1(max_clusters);
+    case 5: return tc_prepare_bn256_cg2_mc2(max_clusters);
+  }
   return cudaErrorInvalidValue;
 }
 
-cudaError_t tc_launch(int bn, int cg, const CUtensorMap& map_p, const CUtensorMap& map_q,
+cudaError_t tc_launch(int bn, int cg, int mc, const CUtensorMap& map_p, const CUtensorMap& map_q,
                       const TcArgs& args, int grid, cudaStream_t stream) {
-  if (cg == 1 && bn == 64) return tc_launch_bn64_cg1(map_p, map_q, args, grid, stream);
-  if (cg == 1 && bn == 128) return tc_launch_bn128_cg1(map_p, map_q, args, grid, stream);
-  if (cg == 1 && bn == 256) return tc_launch_bn256_cg1(map_p, map_q, args, grid, stream);
-  if (cg == 2 && bn == 128) return tc_launch_bn128_cg2(map_p, map_q, args, grid, stream);
-  if (cg == 2 && bn == 256) return tc_launch_bn256_cg2(map_p, map_q, args, grid, stream);
+  switch (tc_config_index(bn, cg, mc)) {
+    case 0: return tc_launch_bn64_cg1_mc1(map_p, map_q, args, grid, stream);
+    case 1: return tc_launch_bn128_cg1_mc1(map_p, map_q, args, grid, stream);
+    case 2: return tc_launch_bn256_cg1_mc1(map_p, map_q, args, grid, stream);
+    case 3: return tc_launch_bn128_cg2_mc1(map_p, map_q, args, grid, stream);
+    case 4: return tc_launch_bn256_cg2_mc1(map_p, map_q, args, grid, stream);
+    case 5: return tc_launch_bn256_cg2_mc2(map_p, map_q, args, grid, stream);
+  }
   return cudaErrorInvalidValue;
 }
 

@@ -19,6 +19,12 @@
 //    and half of the tile's Q columns, and the leader CTA issues
 //    tcgen05.mma.cta_group::2 with M = 256, which reads both CTAs' shared memory.
 //    Per SM this halves the Q traffic from L2 for the same tile width.
+//  * MC == 2 puts two CTA pairs in one cluster of four on neighbouring tiles of
+//    the same tile row: they need the same P rows, so each pair loads half of
+//    them and the tensor-memory-accelerator multicast writes that half into
+//    both pairs ("CUDA GEMM 矩阵乘法优化指南" 13.3: one read, several CTAs).  A
+//    stage is reused only after both pairs' MMAs have released it.  L2 reads
+//    per k-block fall from 128 KB to 96 KB per four SMs.
 //  * The fp32 accumulator lives in Tensor Memory, double-buffered so that the
 //    epilogue of one tile overlaps the main loop of the next (the ping-pong idea
 //    of "GPU GEMM 优化完全拆解（三）", Hopper 时代的三种 kernel 设计).
@@ -42,11 +48,13 @@
 
 namespace g10 {
 
-template <int BN, int CG>
+template <int BN, int CG, int MC>
 struct TcConfig {
   static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
   static_assert(CG == 1 || CG == 2, "CTA group");
   static_assert(CG == 1 || BN >= 128, "a CTA pair needs 64-column halves of Q");
+  static_assert(MC == 1 || (MC == 2 && CG == 2), "multicast runs on CTA pairs");
+  static constexpr int kCluster = CG * MC;       // CTAs per cluster
   static constexpr int kTileM = kBM * CG;        // rows of D per tile
   static constexpr int kQRows = BN / CG;         // rows of Q this CTA loads per k-block
   static constexpr int kABytes = kBM * kBK * 2;  // this CTA's P tile: 128 rows x 128 bytes
@@ -188,11 +196,16 @@ __device__ __forceinline__ void store_chunk(const TcArgs& a, int i, int j0, floa
 
 // ----------------------------------------------------------------- the roles --
 
-template <int BN, int CG>
+template <int BN, int CG, int MC>
 __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CUtensorMap* map_q,
                                               const TcArgs& a, uint8_t* ring_a, uint8_t* ring_b,
                                               TcCtrl* ctrl, uint32_t rank, int first, int stride) {
-  using Cfg = TcConfig<BN, CG>;
+  using Cfg = TcConfig<BN, CG, MC>;
+  const int q = static_cast<int>(rank) % CG;      // rank inside the CTA pair
+  const int pair = static_cast<int>(rank) / CG;   // which pair of the cluster
+  const uint32_t leader = static_cast<uint32_t>(pair * CG);
+  // multicast of P: this CTA and the CTA of the other pair with the same rank inside its pair
+  const uint16_t p_mask = static_cast<uint16_t>((1u << q) | (1u << (q + CG)));
   int stage = 0;
   uint32_t phase = 0;
   uint32_t pending = 0, pending_parity = 0;  // copies in flight, per stage
@@ -201,8 +214,8 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
   WorkIter work(a.sched, first, stride);
   Unit w;
   while (ok && work.next(w)) {
-    const int i0 = w.ti * Cfg::kTileM + static_cast<int>(rank) * kBM;
-    const int j0 = w.tj * BN + static_cast<int>(rank) * Cfg::kQRows;
+    const int i0 = w.ti * Cfg::kTileM + q * kBM;
+    const int j0 = (w.tj * MC + pair) * BN + q * Cfg::kQRows;
     for (int kb = w.kb0; kb < w.kb1; ++kb) {
       if (!warp_wait(smem_u32(&ctrl->empty[stage]), phase ^ 1u, ctrl, a, kRoleProducer, kBarEmpty,
                      true)) {
@@ -212,7 +225,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
       ++nload;
       const uint32_t full_local = smem_u32(&ctrl->full[stage]);
       // A pair credits both CTAs' bytes to the leader's barrier, which the MMA waits on.
-      const uint32_t full = CG == 2 ? mapa_shared(full_local, 0) : full_local;
+      const uint32_t full = CG == 2 ? mapa_shared(full_local, leader) : full_local;
       if (a.drop_load != 0 && blockIdx.x == 0 && nload == a.drop_load) {
         pending &= ~(1u << stage);  // test hook: this stage's barrier is never completed
       } else {
@@ -220,14 +233,20 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
         const uint32_t sb = smem_u32(ring_b + stage * Cfg::kBBytes);
         const int k0 = kb * kBK;
         if (elect_one()) {
-          if (rank == 0) mbar_arrive_expect_tx(full_local, CG * Cfg::kStageBytes);
+          if (q == 0) mbar_arrive_expect_tx(full_local, CG * Cfg::kStageBytes);
           auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
             if constexpr (CG == 2)
               tma_load_2d_pair(dst, map, full, x, y);
             else
               tma_load_2d(dst, map, full, x, y);
           };
-          if (a.p_kmajor) {
+          if constexpr (MC == 2) {
+            // this pair's half of the P tile: 64 rows (K-major) or one 64-wide atom (M-major)
+            if (a.p_kmajor)
+              tma_load_2d_pair_multicast(sa + pair * 64 * 128, map_p, full, k0, i0 + 64 * pair, p_mask);
+            else
+              tma_load_2d_pair_multicast(sa + pair * kMnAtomBytes, map_p, full, i0 + 64 * pair, k0, p_mask);
+          } else if (a.p_kmajor) {
             load(sa, map_p, k0, i0);
           } else {
             load(sa, map_p, i0, k0);
@@ -254,7 +273,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
   // No copy may still be writing shared memory when the CTA exits.  The leader's
   // barrier counts both CTAs' bytes, so the leader's wait covers the pair; a
   // peer CTA is held at the final cluster barrier until the leader has waited.
-  if (rank == 0 && (threadIdx.x & 31) == 0) {
+  if (q == 0 && (threadIdx.x & 31) == 0) {
     for (int s = 0; s < Cfg::kStages; ++s)
       if (pending & (1u << s))
         wait_bounded(smem_u32(&ctrl->full[s]), (pending_parity >> s) & 1u, ctrl, a, kRoleProducer,
@@ -263,18 +282,28 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
   __syncwarp();
 }
 
-template <int BN, int CG>
+template <int BN, int CG, int MC>
 __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8_t* ring_b,
-                                         TcCtrl* ctrl, uint32_t tmem_base, int first, int stride) {
-  using Cfg = TcConfig<BN, CG>;
+                                         TcCtrl* ctrl, uint32_t tmem_base, uint32_t rank, int first,
+                                         int stride) {
+  using Cfg = TcConfig<BN, CG, MC>;
   int stage = 0;
   uint32_t phase = 0;
   int it = 0;
   bool ok = true;
-  // A pair's commits arrive on the barrier at the same offset in both CTAs.
-  auto commit = [](uint32_t bar) {
+  // A stage is freed in every CTA of the cluster (with multicast the other pair
+  // writes into it too); the accumulator is handed to the pair's two epilogues.
+  const uint16_t all_mask = static_cast<uint16_t>((1u << Cfg::kCluster) - 1u);
+  const uint16_t pair_mask = static_cast<uint16_t>(((1u << CG) - 1u) << rank);
+  auto commit_stage = [&](uint32_t bar) {
     if constexpr (CG == 2)
-      mma_commit_pair(bar, 0x3);
+      mma_commit_pair(bar, all_mask);
+    else
+      mma_commit<1>(bar);
+  };
+  auto commit_acc = [&](uint32_t bar) {
+    if constexpr (CG == 2)
+      mma_commit_pair(bar, pair_mask);
     else
       mma_commit<1>(bar);
   };
@@ -309,7 +338,7 @@ __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8
         for (int k = 0; k < kBK / 16; ++k)  // the start address sits in the descriptor's low bits
           mma_f16_ss<CG>(d_tmem, ad0 + ((a_step * k) >> 4), bd0 + ((b_step * k) >> 4), a.idesc,
                          (kb > w.kb0 || k > 0) ? 1u : 0u);
-        commit(smem_u32(&ctrl->empty[stage]));  // frees the stage once these MMAs have read it
+        commit_stage(smem_u32(&ctrl->empty[stage]));  // frees the stage once these MMAs have read it
       }
       __syncwarp();
       if (++stage == a.stages) {
@@ -318,7 +347,7 @@ __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8
       }
     }
     if (!ok) break;
-    if (elect_one()) commit(smem_u32(&ctrl->acc_full[buf]));  // accumulator ready for the epilogue(s)
+    if (elect_one()) commit_acc(smem_u32(&ctrl->acc_full[buf]));  // accumulator ready for the epilogues
     __syncwarp();
   }
   // Tensor Memory is freed only after every MMA issued here has finished.  The
@@ -330,11 +359,14 @@ __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8
   __syncwarp();
 }
 
-template <int BN, int CG>
+template <int BN, int CG, int MC>
 __device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uint32_t tmem_base,
                                               int warp, int lane, uint32_t rank, int first,
                                               int stride) {
-  using Cfg = TcConfig<BN, CG>;
+  using Cfg = TcConfig<BN, CG, MC>;
+  const int q = static_cast<int>(rank) % CG;
+  const int pair = static_cast<int>(rank) / CG;
+  const uint32_t leader = static_cast<uint32_t>(pair * CG);
   const int quarter = warp & 3;  // a warp may only read TMEM lanes 32*(warp%4) .. +31
   const int row = quarter * 32 + lane;
   const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -351,7 +383,7 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uin
     const uint32_t taddr = lane_base + static_cast<uint32_t>(buf * BN);
     // the MMA (leader CTA) waits until every epilogue thread of the pair has read the buffer
     const uint32_t acc_empty_local = smem_u32(&ctrl->acc_empty[buf]);
-    const uint32_t acc_empty = CG == 2 ? mapa_shared(acc_empty_local, 0) : acc_empty_local;
+    const uint32_t acc_empty = CG == 2 ? mapa_shared(acc_empty_local, leader) : acc_empty_local;
     auto release = [&]() {
       tc_fence_before_sync();
       if constexpr (CG == 2)
@@ -359,7 +391,8 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uin
       else
         mbar_arrive(acc_empty);
     };
-    const int i = w.ti * Cfg::kTileM + static_cast<int>(rank) * kBM + row;
+    const int i = w.ti * Cfg::kTileM + q * kBM + row;
+    const int jt = (w.tj * MC + pair) * BN;  // first column of this pair's tile
     if (!w.partial) {
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
@@ -370,13 +403,13 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uin
         float v[32];
 #pragma unroll
         for (int t = 0; t < 32; ++t) v[t] = __uint_as_float(r[t]);
-        store_chunk(a, i, w.tj * BN + c, v);
+        store_chunk(a, i, jt + c, v);
       }
     } else {
       // Partial of this k-range: column-major inside the tile so that a warp's
       // 32 rows are 128 contiguous bytes.
-      const int slot = w.pslot * CG + static_cast<int>(rank);
-      const int ctr = w.ctr * CG + static_cast<int>(rank);
+      const int slot = w.pslot * Cfg::kCluster + static_cast<int>(rank);
+      const int ctr = w.ctr * Cfg::kCluster + static_cast<int>(rank);
       float* part = a.partials + static_cast<size_t>(slot) * BN * kBM;
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
@@ -406,23 +439,23 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uin
           for (int t = 0; t < 32; ++t) v[t] = 0.0f;
 #pragma unroll 1
           for (int k = 0; k < w.ncontrib; ++k) {  // fixed k order: the sum does not depend on timing
-            const int ks = contrib_slot(a.sched, w, k) * CG + static_cast<int>(rank);
+            const int ks = contrib_slot(a.sched, w, k) * Cfg::kCluster + static_cast<int>(rank);
             const float* ps = a.partials + static_cast<size_t>(ks) * BN * kBM;
 #pragma unroll
             for (int t = 0; t < 32; ++t) v[t] += __ldcg(ps + static_cast<size_t>(c + t) * kBM + row);
           }
-          store_chunk(a, i, w.tj * BN + c, v);
+          store_chunk(a, i, jt + c, v);
         }
       }
     }
   }
 }
 
-template <int BN, int CG>
+template <int BN, int CG, int MC>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p,
                    const __grid_constant__ CUtensorMap map_q, const TcArgs a) {
-  using Cfg = TcConfig<BN, CG>;
+  using Cfg = TcConfig<BN, CG, MC>;
   extern __shared__ uint8_t smem_raw[];
   // 128-byte swizzle atoms need 1024-byte aligned tiles.
   const uint32_t raw = smem_u32(smem_raw);
@@ -433,15 +466,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // A CTA pair (cluster of 2) shares each tile; rank 0 is the leader that issues the MMAs.
-  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
-  const int first = CG == 2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int stride = CG == 2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  // A CTA pair shares each tile; its even rank is the leader that issues the MMAs.
+  // A cluster (one or two pairs, or one CTA) walks the schedule as one slot.
+  constexpr int kCl = Cfg::kCluster;
+  const uint32_t rank = kCl > 1 ? cluster_ctarank() : 0u;
+  const int first = static_cast<int>(blockIdx.x) / kCl;
+  const int stride = static_cast<int>(gridDim.x) / kCl;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::kStages; ++s) {
       mbar_init(smem_u32(&ctrl->full[s]), 1);
-      mbar_init(smem_u32(&ctrl->empty[s]), 1);
+      mbar_init(smem_u32(&ctrl->empty[s]), MC);  // one release per pair using the stage
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctrl->acc_full[b]), 1);
@@ -462,21 +497,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
-  if constexpr (CG == 2) cluster_sync();  // the peer's barriers exist before any remote arrive
+  if constexpr (kCl > 1) cluster_sync();  // every CTA's barriers exist before any remote arrive
   tc_fence_after_sync();
   const uint32_t tmem_base = ctrl->tmem_base;
 
   if (warp == 0) {
-    producer_role<BN, CG>(&map_p, &map_q, a, ring_a, ring_b, ctrl, rank, first, stride);
+    producer_role<BN, CG, MC>(&map_p, &map_q, a, ring_a, ring_b, ctrl, rank, first, stride);
   } else if (warp == 1) {
-    if (rank == 0) mma_role<BN, CG>(a, ring_a, ring_b, ctrl, tmem_base, first, stride);
+    if (rank % CG == 0) mma_role<BN, CG, MC>(a, ring_a, ring_b, ctrl, tmem_base, rank, first, stride);
   } else {
-    epilogue_role<BN, CG>(a, ctrl, tmem_base, warp, lane, rank, first, stride);
+    epilogue_role<BN, CG, MC>(a, ctrl, tmem_base, warp, lane, rank, first, stride);
   }
 
   tc_fence_before_sync();
   __syncthreads();
-  if constexpr (CG == 2) {
+  if constexpr (kCl > 1) {
     // After an abort, give copies the leader could not account for time to land.
     if (*reinterpret_cast<volatile uint32_t*>(&ctrl->abort)) {
       const uint64_t t0 = global_timer_ns();

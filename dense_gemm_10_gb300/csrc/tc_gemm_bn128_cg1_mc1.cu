@@ -1,0 +1,5 @@
+// Tile width 128, CTA group 1, 1 CTA pair(s) sharing P by multicast.
+#define TC_BN 128
+#define TC_CG 1
+#define TC_MC 1
+#include "tc_gemm_inst.cuh"

@@ -16,7 +16,7 @@ BF16_F32, BF16_BF16, F16_F32, F16_F16 = 0, 1, 2, 3
 STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED", 3: "GEMM_ERR_NO_DEVICE",
           4: "GEMM_ERR_CUDA", 5: "GEMM_ERR_TENSORMAP", 6: "GEMM_ERR_TIMEOUT", 7: "GEMM_ERR_WORKSPACE"}
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NO_DEVICE, ERR_CUDA, ERR_TENSORMAP, ERR_TIMEOUT, ERR_WORKSPACE = range(8)
-PATH_NOOP, PATH_SCALE_C, PATH_TC_1CTA, PATH_TC_2CTA = 0, 1, 2, 3
+PATH_NOOP, PATH_SCALE_C, PATH_TC_1CTA, PATH_TC_2CTA, PATH_TC_2CTA_MULTICAST = 0, 1, 2, 3, 4
 (OPT_WAIT_LIMIT_NS, OPT_FORCE_PATH, OPT_SPLIT_K, OPT_RASTER_GROUP, OPT_FORCE_BN, OPT_TEST_DROP_LOAD, OPT_MAX_GRID,
  OPT_STREAM_K, OPT_STAGES) = range(9)
 SCHED_TILES, SCHED_STREAM_K = 0, 1
@@ -30,10 +30,10 @@ class Plan(ctypes.Structure):
                                     "split_k", "raster_group", "repack_a", "repack_b", "vector_store",
                                     "grid", "launches", "schedule")] + \
                [(n, _i64) for n in ("tiles", "units", "workspace_bytes")] + \
-               [(n, _i32) for n in ("tiles_i", "tiles_j", "num_kb", "dp_tiles", "sk_slots", "reserved")]
+               [(n, _i32) for n in ("tiles_i", "tiles_j", "num_kb", "dp_tiles", "sk_slots", "cluster")]
 
     def as_dict(self):
-        return {n: getattr(self, n) for n, _ in self._fields_ if n != "reserved"}
+        return {n: getattr(self, n) for n, _ in self._fields_}
 
 
 SIGNATURES = {

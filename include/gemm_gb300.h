@@ -135,7 +135,9 @@ typedef enum {
   GEMM_PATH_NOOP = 0,      /* M == 0 or N == 0 */
   GEMM_PATH_SCALE_C = 1,   /* K == 0: C = beta * C */
   GEMM_PATH_TC_1CTA = 2,   /* persistent tcgen05 kernel, one CTA per output tile (cta_group::1) */
-  GEMM_PATH_TC_2CTA = 3    /* persistent tcgen05 kernel, CTA pairs share a 256-row tile (cta_group::2) */
+  GEMM_PATH_TC_2CTA = 3,   /* persistent tcgen05 kernel, CTA pairs share a 256-row tile (cta_group::2) */
+  GEMM_PATH_TC_2CTA_MULTICAST = 4 /* as GEMM_PATH_TC_2CTA, two pairs per cluster of four on
+                                     neighbouring tiles sharing the A-side tile by TMA multicast */
 } gemm_path_t;
 
 typedef struct {
@@ -153,15 +155,16 @@ typedef struct {
   int32_t grid;            /* CTAs launched for the main kernel */
   int32_t launches;        /* kernels launched by one gemm_run */
   int32_t schedule;        /* 0: whole (or split-K) tiles; 1: stream-K tail */
-  int64_t tiles;           /* output tiles */
+  int64_t tiles;           /* schedule tiles = tiles_i * tiles_j */
   int64_t units;           /* work units over all CTAs (tiles, split pieces or stream-K pieces) */
   int64_t workspace_bytes; /* handle workspace this call needs */
-  int32_t tiles_i;         /* tiles along the MMA rows (M, or N when swapped) */
-  int32_t tiles_j;         /* tiles along the MMA columns */
+  int32_t tiles_i;         /* schedule tiles along the MMA rows (M, or N when swapped) */
+  int32_t tiles_j;         /* schedule tiles along the MMA columns (with multicast a schedule
+                              tile is two neighbouring output tiles) */
   int32_t num_kb;          /* k-blocks per tile */
   int32_t dp_tiles;        /* tiles run whole (stream-K: the complete waves) */
-  int32_t sk_slots;        /* stream-K: CTAs (or pairs) sharing the remaining tiles' k-blocks */
-  int32_t reserved;
+  int32_t sk_slots;        /* stream-K: clusters sharing the remaining tiles' k-blocks */
+  int32_t cluster;         /* CTAs per schedule slot: 1, 2 (a pair) or 4 (two pairs, multicast) */
 } gemm_plan_t;
 
 /*
@@ -180,7 +183,7 @@ gemm_status_t gemm_plan(gemm_handle_t h, int sm_count, gemm_op_t transA, gemm_op
 
 typedef enum {
   GEMM_OPT_WAIT_LIMIT_NS = 0, /* barrier wait limit in ns (default 2e9; >= 1e6) */
-  GEMM_OPT_FORCE_PATH = 1,    /* 0 auto, GEMM_PATH_TC_1CTA or GEMM_PATH_TC_2CTA */
+  GEMM_OPT_FORCE_PATH = 1,    /* 0 auto, or GEMM_PATH_TC_1CTA / _2CTA / _2CTA_MULTICAST */
   GEMM_OPT_SPLIT_K = 2,       /* 0 auto, else the k-split to use (clamped to the k-blocks) */
   GEMM_OPT_RASTER_GROUP = 3,  /* 0 auto, else tile rows per raster group */
   GEMM_OPT_FORCE_BN = 4,      /* 0 auto, else 64, 128 or 256 */

@@ -82,17 +82,19 @@ def test_product_code_never_touches_the_oracle():
 # ----------------------------------------------------------------- planner --
 
 def test_plan_square_nt():
-    """4096^3: 256 x 256 tiles on CTA pairs, 76 pairs on 152 SMs; the 28 tiles of
-    the incomplete fourth wave are shared out by stream-K."""
+    """4096^3: 256 x 256 tiles on CTA pairs (two pairs per cluster when the A tile
+    is multicast); the tiles of an incomplete last wave are shared by stream-K."""
     p = G.plan(4096, 4096, 4096, 0, 1)
-    assert p.path == G.PATH_TC_2CTA and p.swap_ab == 0
+    assert p.path in (G.PATH_TC_2CTA, G.PATH_TC_2CTA_MULTICAST) and p.swap_ab == 0
+    assert p.cluster == (4 if p.path == G.PATH_TC_2CTA_MULTICAST else 2)
     assert p.a_kmajor == 1 and p.b_kmajor == 1
-    assert p.bm == 256 and p.bk == 64 and p.bn == 256
-    assert p.tiles == 16 * 16 and p.num_kb == 64
-    assert p.schedule == G.SCHED_STREAM_K and p.dp_tiles == 3 * 76 and 0 < p.sk_slots <= 76
+    assert p.bm == 256 and p.bk == 64 and p.bn == 256 and p.num_kb == 64
+    assert p.tiles_i == 16 and p.tiles_j == 16 // (p.cluster // 2) and p.tiles == p.tiles_i * p.tiles_j
+    slots = 152 // p.cluster
+    assert p.schedule == G.SCHED_STREAM_K and p.dp_tiles == (p.tiles // slots) * slots and 0 < p.sk_slots <= slots
     assert p.grid == 152 and p.repack_a == 0 and p.repack_b == 0
     assert p.vector_store == 1 and p.launches == 1
-    assert p.workspace_bytes >= p.sk_slots * 2 * 2 * 256 * 128 * 4   # partial slots x CTA pair
+    assert p.workspace_bytes >= p.sk_slots * 2 * p.cluster * 256 * 128 * 4   # partial slots x CTAs
 
 
 @pytest.mark.parametrize("ta,tb,ak,bk", [(0, 0, 1, 0), (0, 1, 1, 1), (1, 0, 0, 0), (1, 1, 0, 1)])
@@ -164,14 +166,15 @@ def test_plan_invariants(shape):
     for sm in (148, 152, 160):
         p = G.plan(M, N, K, 0, 0, sm_count=sm)
         I, J = (N, M) if p.swap_ab else (M, N)
-        cg = 2 if p.path == G.PATH_TC_2CTA else 1
-        assert p.bm == 128 * cg
-        assert p.tiles == -(-I // p.bm) * -(-J // p.bn) == p.tiles_i * p.tiles_j
+        cg = p.bm // 128
+        mc = p.cluster // cg
+        assert (cg, mc) == {G.PATH_TC_1CTA: (1, 1), G.PATH_TC_2CTA: (2, 1), G.PATH_TC_2CTA_MULTICAST: (2, 2)}[p.path]
+        assert p.tiles == -(-I // p.bm) * -(-(-(-J // p.bn)) // mc) == p.tiles_i * p.tiles_j
         assert p.num_kb == -(-K // 64)
         if p.schedule == G.SCHED_TILES:
             assert p.units == p.tiles * p.split_k and p.dp_tiles == p.tiles
         else:
-            assert p.split_k == 1 and p.dp_tiles % (p.grid // cg) == 0 and p.units >= p.tiles
+            assert p.split_k == 1 and p.dp_tiles % (p.grid // p.cluster) == 0 and p.units >= p.tiles
         assert 1 <= p.split_k <= max(1, -(-K // 64))
-        assert p.grid == min(p.units, sm // cg) * cg
+        assert p.grid == min(p.units, sm // p.cluster) * p.cluster
         assert 1 <= p.raster_group <= max(1, -(-I // p.bm))

@@ -23,8 +23,9 @@ def h():
     gh.close()
 
 
-CONFIGS = [(1, 64), (1, 128), (1, 256), (2, 128), (2, 256)]   # (CTAs per tile, tile width)
-PATHS = {1: G.PATH_TC_1CTA, 2: G.PATH_TC_2CTA}
+# (CTAs per schedule slot, tile width): one CTA, a CTA pair, or two pairs sharing A by multicast
+CONFIGS = [(1, 64), (1, 128), (1, 256), (2, 128), (2, 256), (4, 256)]
+PATHS = {1: G.PATH_TC_1CTA, 2: G.PATH_TC_2CTA, 4: G.PATH_TC_2CTA_MULTICAST}
 
 
 @contextlib.contextmanager
@@ -58,7 +59,7 @@ def test_tiny_256(h):
     _check(inputs.tiny_256(), h)
 
 
-@pytest.mark.parametrize("cg", [1, 2])
+@pytest.mark.parametrize("cg", [1, 2, 4])
 @pytest.mark.parametrize("transA,transB", [(0, 0), (0, 1), (1, 0), (1, 1)])
 @pytest.mark.parametrize("in_dtype,out_dtype", [("bf16", "f32"), ("f16", "f32"), ("bf16", "bf16"), ("f16", "f16")])
 def test_layouts_and_types(h, transA, transB, in_dtype, out_dtype, cg):
@@ -78,7 +79,7 @@ def test_ragged_shapes(h, shape):
     _check(p, h)
 
 
-@pytest.mark.parametrize("cg", [1, 2])
+@pytest.mark.parametrize("cg", [1, 2, 4])
 @pytest.mark.parametrize("transA,transB", [(0, 0), (0, 1), (1, 0), (1, 1)])
 def test_small_integers_bit_exact(h, transA, transB, cg):
     """Integers in {-4..4}: the fp32 result is exact whatever the order of the
@@ -125,8 +126,8 @@ def test_every_tile_configuration(h, cg, bn, transA, transB):
 def test_stream_k(h, cg, bn, gi):
     """Stream-K tail forced on small grids: tiles cut into several pieces whose
     partials are summed by the last piece to finish.  The grids leave an
-    incomplete last wave for every configuration (90, 48, 24, 24, 12 tiles)."""
-    grid = (7, 13, 29)[gi] if cg == 1 else (10, 14, 30)[gi]
+    incomplete last wave for every configuration (90, 48, 24, 24, 12 and 6 schedule tiles)."""
+    grid = {1: (7, 13, 29), 2: (10, 14, 30), 4: (16, 20, 28)}[cg][gi]
     p = inputs.make_problem("sk", 700, 900, 1000, 0, 1, "bf16", "f32", ("normal", 0, 1), ("normal", 0, 1),
                             alpha=1.25, beta=-0.5, seed=grid + bn + cg)
     with options(h, path=PATHS[cg], bn=bn, grid=grid, stream_k=2):

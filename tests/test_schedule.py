@@ -108,8 +108,7 @@ def test_planned_schedules(shim, shape, sm):
     gbuild.build()
     M, N, K, ta, tb = shape
     p = G.plan(M, N, K, ta, tb, sm_count=sm)
-    cg = 2 if p.path == G.PATH_TC_2CTA else 1
-    check_schedule(shim, params(p), p.grid // cg)
+    check_schedule(shim, params(p), p.grid // p.cluster)
 
 
 @pytest.mark.parametrize("tiles_i,tiles_j,num_kb,slots,dp_tiles,sk_slots", [
