@@ -40,6 +40,8 @@ struct Options {
   int max_grid = 0;
   int stream_k = 0;  // 0 auto, 1 off, 2 on
   int stages = 0;    // 0: the configuration's maximum ring depth
+  int l2_hints = 0;  // GEMM_OPT_L2_HINTS
+  int tma_store = 0; // GEMM_OPT_EPILOGUE: 0 auto, 1 bulk stores when possible, 2 direct stores
 };
 
 // One stored operand, as the tensor-memory-accelerator copy engine will see it.
@@ -55,6 +57,7 @@ struct Operand {
 
 struct Plan {
   gemm_plan_t pub{};
+  bool tma_store = false;  // C leaves through staged bulk tensor stores
   Sched sched{};
   Operand p, q;
   int64_t I = 0, J = 0, K = 0;
@@ -313,8 +316,10 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   }
   P.workspace_bytes = static_cast<int64_t>(ws);
   P.vector_store = (!swap && reinterpret_cast<uintptr_t>(C) % 16 == 0 && (ldc * c_elem) % 16 == 0) ? 1 : 0;
+  // Bulk tensor stores need 16-byte aligned rows; the blend with the old C
+  // (beta != 0) keeps the direct path, which reads C as it writes it.
+  pl.tma_store = P.vector_store && beta == 0.0f && o.tma_store != 2;
   P.launches = 1 + P.repack_a + P.repack_b;
-  (void)beta;
   *out = pl;
   return GEMM_OK;
 }
@@ -360,6 +365,26 @@ gemm_status_t encode_operand(CUtensorMap* map, const Operand& op, const void* ba
   CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_TENSORMAP;
+}
+
+// Describe C (I x J in the kernel's terms, row pitch ldc) for bulk stores of
+// 32-row x 128-byte tiles with the 128-byte swizzle.
+gemm_status_t encode_c(CUtensorMap* map, void* C, int64_t rows, int64_t cols, int64_t ldc,
+                       int32_t c_type) {
+  auto fn = encode_fn();
+  if (!fn) return GEMM_ERR_TENSORMAP;
+  const int64_t esize = c_type == kCF32 ? 4 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc * esize)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUtensorMapDataType dt = c_type == kCF32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                           : c_type == kCBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = fn(map, dt, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_TENSORMAP;
 }
@@ -501,6 +526,14 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
       if (value < 0 || value > 64) return GEMM_ERR_INVALID_ARG;
       h->opt.stages = static_cast<int>(value);
       return GEMM_OK;
+    case GEMM_OPT_L2_HINTS:
+      if (value < 0 || value > 3) return GEMM_ERR_INVALID_ARG;
+      h->opt.l2_hints = static_cast<int>(value);
+      return GEMM_OK;
+    case GEMM_OPT_EPILOGUE:
+      if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+      h->opt.tma_store = static_cast<int>(value);
+      return GEMM_OK;
   }
   return GEMM_ERR_INVALID_ARG;
 }
@@ -585,6 +618,12 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
   if (s != GEMM_OK) return s;
   s = encode_operand(&map_q, pl.q, qbase, qld, pl.bf16, P.bn / cg);
   if (s != GEMM_OK) return s;
+  CUtensorMap map_c;
+  std::memset(&map_c, 0, sizeof(map_c));
+  if (pl.tma_store) {
+    s = encode_c(&map_c, C, pl.I, pl.J, ldc, pl.c_type);
+    if (s != GEMM_OK) return s;
+  }
 
   TcArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -595,6 +634,7 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
   a.p_kmajor = P.a_kmajor;
   a.q_kmajor = P.b_kmajor;
   a.stages = P.stages;
+  a.l2_hints = h->opt.l2_hints;
   a.idesc = make_idesc_f16(pl.bf16, !pl.p.kmajor, !pl.q.kmajor, kBM * cg, P.bn);
   a.alpha = alpha;
   a.beta = beta;
@@ -603,12 +643,13 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
   a.c_sj = pl.c_sj;
   a.c_type = pl.c_type;
   a.vec_store = P.vector_store;
+  a.tma_store = pl.tma_store ? 1 : 0;
   a.partials = needs_partials(pl.sched) ? reinterpret_cast<float*>(ws + pl.partial_offset) : nullptr;
   a.counters = h->d_counters;
   a.status = h->d_status;
   a.wait_limit_ns = static_cast<uint64_t>(h->opt.wait_limit_ns);
   a.drop_load = h->opt.drop_load;
-  e = tc_launch(P.bn, cg, mc, map_p, map_q, a, P.grid, st);
+  e = tc_launch(P.bn, cg, mc, map_p, map_q, map_c, a, P.grid, st);
   if (e != cudaSuccess) return cuda_fail(h, e);
   h->launches += 1;
   return GEMM_OK;
@@ -760,6 +801,12 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   if (s != GEMM_OK) return s;
   s = encode_operand(&map_q, pl.q, qbase, qld, pl.bf16, P.bn / cg);
   if (s != GEMM_OK) return s;
+  CUtensorMap map_c;
+  std::memset(&map_c, 0, sizeof(map_c));
+  if (pl.tma_store) {
+    s = encode_c(&map_c, C, pl.I, pl.J, ldc, pl.c_type);
+    if (s != GEMM_OK) return s;
+  }
   TcArgs a;
   std::memset(&a, 0, sizeof(a));
   a.I = static_cast<int32_t>(pl.I);
@@ -777,11 +824,12 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   a.c_sj = pl.c_sj;
   a.c_type = pl.c_type;
   a.vec_store = P.vector_store;
+  a.tma_store = pl.tma_store ? 1 : 0;
   a.partials = needs_partials(pl.sched) ? reinterpret_cast<float*>(d->scratch + pl.partial_offset) : nullptr;
   a.counters = d->counters;
   a.status = d->status;
   a.wait_limit_ns = static_cast<uint64_t>(o.wait_limit_ns);
   a.drop_load = 0;
-  e = tc_launch(P.bn, cg, mc, map_p, map_q, a, P.grid, st);
+  e = tc_launch(P.bn, cg, mc, map_p, map_q, map_c, a, P.grid, st);
   return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

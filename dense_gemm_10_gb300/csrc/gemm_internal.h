@@ -35,11 +35,13 @@ struct TcArgs {
   int32_t q_kmajor;      // Q has K contiguous (else J contiguous)
   uint32_t idesc;        // tcgen05 instruction descriptor
   int32_t stages;        // ring stages in use, 1 .. the configuration's maximum
+  int32_t l2_hints;      // bit 0: A/B loads evict-last in L2; bit 1: C stores streaming (evict-first)
   float alpha, beta;
   void* C;
   int64_t c_si, c_sj;
   int32_t c_type;        // CType
   int32_t vec_store;     // c_sj == 1 and every row of C starts 16-byte aligned
+  int32_t tma_store;     // C tiles leave through shared-memory staging and bulk tensor stores
   float* partials;       // partial tiles of split tiles, [partial_slots * CG][BN][kBM] fp32
   int32_t* counters;     // per split tile (x CG) arrival counters, zero between calls
   int32_t* status;       // device status word
@@ -61,8 +63,9 @@ int tc_stages(int bn, int cg, int mc);
 // report how many can be resident at once.
 cudaError_t tc_prepare(int bn, int cg, int mc, int* max_clusters);
 // grid = CTAs (a multiple of cg * mc).
+// map_c describes C for the bulk-store epilogue (ignored unless args.tma_store).
 cudaError_t tc_launch(int bn, int cg, int mc, const CUtensorMap& map_p, const CUtensorMap& map_q,
-                      const TcArgs& args, int grid, cudaStream_t stream);
+                      const CUtensorMap& map_c, const TcArgs& args, int grid, cudaStream_t stream);
 
 // dst[r * ldd + c] = src[r * lds + c] for 16-bit elements, r < rows, c < cols.
 cudaError_t repack16_launch(const uint16_t* src, int64_t lds, uint16_t* dst, int64_t ldd,

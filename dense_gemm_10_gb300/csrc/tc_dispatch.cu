@@ -6,7 +6,8 @@ namespace g10 {
 #define TC_DECLARE(BN, CG, MC)                                                                     \
   cudaError_t tc_prepare_bn##BN##_cg##CG##_mc##MC(int* max_clusters);                             \
   cudaError_t tc_launch_bn##BN##_cg##CG##_mc##MC(const CUtensorMap&, const CUtensorMap&,            \
-                                                 const TcArgs&, int, cudaStream_t);
+                                                 const CUtensorMap&, const TcArgs&, int,            \
+                                                 cudaStream_t);
 TC_DECLARE(64, 1, 1)
 TC_DECLARE(128, 1, 1)
 TC_DECLARE(256, 1, 1)
@@ -49,14 +50,14 @@ cudaError_t tc_prepare(int bn, int cg, int mc, int* max_clusters) {
 }
 
 cudaError_t tc_launch(int bn, int cg, int mc, const CUtensorMap& map_p, const CUtensorMap& map_q,
-                      const TcArgs& args, int grid, cudaStream_t stream) {
+                      const CUtensorMap& map_c, const TcArgs& args, int grid, cudaStream_t stream) {
   switch (tc_config_index(bn, cg, mc)) {
-    case 0: return tc_launch_bn64_cg1_mc1(map_p, map_q, args, grid, stream);
-    case 1: return tc_launch_bn128_cg1_mc1(map_p, map_q, args, grid, stream);
-    case 2: return tc_launch_bn256_cg1_mc1(map_p, map_q, args, grid, stream);
-    case 3: return tc_launch_bn128_cg2_mc1(map_p, map_q, args, grid, stream);
-    case 4: return tc_launch_bn256_cg2_mc1(map_p, map_q, args, grid, stream);
-    case 5: return tc_launch_bn256_cg2_mc2(map_p, map_q, args, grid, stream);
+    case 0: return tc_launch_bn64_cg1_mc1(map_p, map_q, map_c, args, grid, stream);
+    case 1: return tc_launch_bn128_cg1_mc1(map_p, map_q, map_c, args, grid, stream);
+    case 2: return tc_launch_bn256_cg1_mc1(map_p, map_q, map_c, args, grid, stream);
+    case 3: return tc_launch_bn128_cg2_mc1(map_p, map_q, map_c, args, grid, stream);
+    case 4: return tc_launch_bn256_cg2_mc1(map_p, map_q, map_c, args, grid, stream);
+    case 5: return tc_launch_bn256_cg2_mc2(map_p, map_q, map_c, args, grid, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -60,11 +60,15 @@ struct TcConfig {
   static constexpr int kABytes = kBM * kBK * 2;  // this CTA's P tile: 128 rows x 128 bytes
   static constexpr int kBBytes = kQRows * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = (192 * 1024) / kStageBytes > 8 ? 8 : (192 * 1024) / kStageBytes;
+  // as many stages as fit in 227 KB beside the control block and alignment slack (at most 8)
+  // epilogue staging: per epilogue warp two 32-row x 128-byte buffers for bulk stores of C
+  static constexpr int kStagingBytes = 4 * 2 * 32 * 128;
+  static constexpr int kCtrlBytes = 256;
+  static constexpr int kRingMax = 232448 - 1024 - kStagingBytes - kCtrlBytes;  // 227 KB less the rest
+  static constexpr int kStages = kRingMax / kStageBytes > 8 ? 8 : kRingMax / kStageBytes;
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kTmemCols = 2 * BN;       // two fp32 accumulators of BN columns
-  static constexpr int kCtrlBytes = 256;
-  static constexpr size_t kSmemBytes = 1024 + kRingBytes + kCtrlBytes;  // + alignment slack
+  static constexpr size_t kSmemBytes = 1024 + kRingBytes + kStagingBytes + kCtrlBytes;  // + alignment slack
 };
 
 struct TcCtrl {
@@ -141,7 +145,7 @@ __device__ __forceinline__ float2 unpack2(const TcArgs& a, uint32_t bits) {
   return __half22float2(*reinterpret_cast<__half2*>(&bits));
 }
 
-// Write alpha * v + beta * C for row i, columns j0 .. j0 + 31 of D.
+// Write v + beta * C for row i, columns j0 .. j0 + 31 of D (v already holds alpha * D).
 __device__ __forceinline__ void store_chunk(const TcArgs& a, int i, int j0, float (&v)[32]) {
   if (i >= a.I) return;
   const bool blend = a.beta != 0.0f;
@@ -151,13 +155,15 @@ __device__ __forceinline__ void store_chunk(const TcArgs& a, int i, int j0, floa
       float4* p = reinterpret_cast<float4*>(static_cast<float*>(a.C) + base);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        float4 o = make_float4(a.alpha * v[4 * q], a.alpha * v[4 * q + 1], a.alpha * v[4 * q + 2],
-                               a.alpha * v[4 * q + 3]);
+        float4 o = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         if (blend) {
           const float4 c = p[q];
           o.x += a.beta * c.x; o.y += a.beta * c.y; o.z += a.beta * c.z; o.w += a.beta * c.w;
         }
-        p[q] = o;
+        if (a.l2_hints & 2)
+          __stcs(p + q, o);  // written once, not re-read here: evict first
+        else
+          p[q] = o;
       }
     } else {
       uint4* p = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.C) + base);
@@ -165,7 +171,7 @@ __device__ __forceinline__ void store_chunk(const TcArgs& a, int i, int j0, floa
       for (int q = 0; q < 4; ++q) {
         float o[8];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) o[t] = a.alpha * v[8 * q + t];
+        for (int t = 0; t < 8; ++t) o[t] = v[8 * q + t];
         if (blend) {
           const uint4 c = p[q];
           const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
@@ -176,8 +182,12 @@ __device__ __forceinline__ void store_chunk(const TcArgs& a, int i, int j0, floa
             o[2 * t + 1] += a.beta * f.y;
           }
         }
-        p[q] = make_uint4(pack2(a, o[0], o[1]), pack2(a, o[2], o[3]), pack2(a, o[4], o[5]),
-                          pack2(a, o[6], o[7]));
+        const uint4 packed = make_uint4(pack2(a, o[0], o[1]), pack2(a, o[2], o[3]), pack2(a, o[4], o[5]),
+                                        pack2(a, o[6], o[7]));
+        if (a.l2_hints & 2)
+          __stcs(p + q, packed);
+        else
+          p[q] = packed;
       }
     }
     return;
@@ -187,12 +197,76 @@ __device__ __forceinline__ void store_chunk(const TcArgs& a, int i, int j0, floa
     const int j = j0 + t;
     if (j < a.J) {
       const int64_t off = static_cast<int64_t>(i) * a.c_si + static_cast<int64_t>(j) * a.c_sj;
-      float o = a.alpha * v[t];
+      float o = v[t];
       if (blend) o += a.beta * load_c(a, off);
       store_c(a, off, o);
     }
   }
 }
+
+// One epilogue warp's output path.  The warp owns 32 rows of the tile and
+// produces them 32 columns at a time.  With tma_store the rows go through a
+// 128-byte-swizzled 32 x 128-byte staging buffer (two per warp, alternating)
+// and leave as one bulk tensor store per 128 bytes of row: whole lines in a few
+// large transfers, instead of each thread writing its own row with 16-byte
+// stores.  Otherwise store_chunk writes them directly.
+struct EpiOut {
+  const TcArgs* a;
+  const CUtensorMap* map_c;
+  uint32_t staging;  // this warp's two buffers (shared address, 1024-byte aligned)
+  int lane;
+  int y0;            // first row of the warp's 32 rows
+  int nstore;        // bulk stores issued so far
+
+  __device__ __forceinline__ void put(int i, int j, const float (&v)[32], int half) {
+    const TcArgs& A = *a;
+    if (!A.tma_store) {
+      float w[32];
+#pragma unroll
+      for (int t = 0; t < 32; ++t) w[t] = v[t];
+      store_chunk(A, i, j, w);
+      return;
+    }
+    // 16-bit C: two 32-column pieces fill one 128-byte row (half 0, then half 1)
+    const bool wide = A.c_type == kCF32;
+    const uint32_t buf = staging + static_cast<uint32_t>((nstore & 1) * 32 * 128);
+    if (wide || half == 0) {
+      if (lane == 0) bulk_wait_group_read<1>();  // the store that last read this buffer is done
+      __syncwarp();
+    }
+    const uint32_t row = buf + static_cast<uint32_t>(lane * 128);
+    const uint32_t sw = static_cast<uint32_t>(lane & 7);  // 128-byte swizzle of 16-byte pieces
+    if (wide) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        st_shared_v4(row + ((k ^ sw) << 4), __float_as_uint(v[4 * k]), __float_as_uint(v[4 * k + 1]),
+                     __float_as_uint(v[4 * k + 2]), __float_as_uint(v[4 * k + 3]));
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        st_shared_v4(row + (((4 * half + k) ^ sw) << 4), pack2(A, v[8 * k], v[8 * k + 1]),
+                     pack2(A, v[8 * k + 2], v[8 * k + 3]), pack2(A, v[8 * k + 4], v[8 * k + 5]),
+                     pack2(A, v[8 * k + 6], v[8 * k + 7]));
+    }
+    if (wide || half == 1) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(map_c, buf, wide ? j : j - 32, y0);
+        bulk_commit_group();
+      }
+      __syncwarp();
+      ++nstore;
+    }
+  }
+
+  __device__ __forceinline__ void finish() {
+    if (a->tma_store) {
+      if (lane == 0) bulk_wait_group_all();
+      __syncwarp();
+    }
+  }
+};
 
 // ----------------------------------------------------------------- the roles --
 
@@ -206,6 +280,9 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
   const uint32_t leader = static_cast<uint32_t>(pair * CG);
   // multicast of P: this CTA and the CTA of the other pair with the same rank inside its pair
   const uint16_t p_mask = static_cast<uint16_t>((1u << q) | (1u << (q + CG)));
+  // Operand tiles are re-read by other tiles: ask L2 to keep them over the output stream.
+  const bool hint = (a.l2_hints & 1) != 0;
+  const uint64_t policy = hint ? l2_policy_evict_last() : 0;
   int stage = 0;
   uint32_t phase = 0;
   uint32_t pending = 0, pending_parity = 0;  // copies in flight, per stage
@@ -235,17 +312,30 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
         if (elect_one()) {
           if (q == 0) mbar_arrive_expect_tx(full_local, CG * Cfg::kStageBytes);
           auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
-            if constexpr (CG == 2)
-              tma_load_2d_pair(dst, map, full, x, y);
+            if constexpr (CG == 2) {
+              if (hint)
+                tma_load_2d_pair_hint(dst, map, full, x, y, policy);
+              else
+                tma_load_2d_pair(dst, map, full, x, y);
+            } else {
+              if (hint)
+                tma_load_2d_hint(dst, map, full, x, y, policy);
+              else
+                tma_load_2d(dst, map, full, x, y);
+            }
+          };
+          auto load_mc = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
+            if (hint)
+              tma_load_2d_pair_multicast_hint(dst, map, full, x, y, p_mask, policy);
             else
-              tma_load_2d(dst, map, full, x, y);
+              tma_load_2d_pair_multicast(dst, map, full, x, y, p_mask);
           };
           if constexpr (MC == 2) {
             // this pair's half of the P tile: 64 rows (K-major) or one 64-wide atom (M-major)
             if (a.p_kmajor)
-              tma_load_2d_pair_multicast(sa + pair * 64 * 128, map_p, full, k0, i0 + 64 * pair, p_mask);
+              load_mc(sa + pair * 64 * 128, map_p, k0, i0 + 64 * pair);
             else
-              tma_load_2d_pair_multicast(sa + pair * kMnAtomBytes, map_p, full, i0 + 64 * pair, k0, p_mask);
+              load_mc(sa + pair * kMnAtomBytes, map_p, i0 + 64 * pair, k0);
           } else if (a.p_kmajor) {
             load(sa, map_p, k0, i0);
           } else {
@@ -360,7 +450,8 @@ __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8
 }
 
 template <int BN, int CG, int MC>
-__device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uint32_t tmem_base,
+__device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap* map_c,
+                                              uint8_t* staging, TcCtrl* ctrl, uint32_t tmem_base,
                                               int warp, int lane, uint32_t rank, int first,
                                               int stride) {
   using Cfg = TcConfig<BN, CG, MC>;
@@ -370,6 +461,12 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uin
   const int quarter = warp & 3;  // a warp may only read TMEM lanes 32*(warp%4) .. +31
   const int row = quarter * 32 + lane;
   const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+  EpiOut out;
+  out.a = &a;
+  out.map_c = map_c;
+  out.staging = smem_u32(staging + (warp - 2) * 2 * 32 * 128);
+  out.lane = lane;
+  out.nstore = 0;
   int it = 0;
   WorkIter work(a.sched, first, stride);
   Unit w;
@@ -378,7 +475,7 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uin
     const uint32_t acc_parity = (it >> 1) & 1;
     const bool ok = wait_bounded(smem_u32(&ctrl->acc_full[buf]), acc_parity, ctrl, a,
                                  kRoleEpilogue, kBarAccFull, true);
-    if (bar_any(1, 128, !ok)) return;  // all four epilogue warps leave together
+    if (bar_any(1, 128, !ok)) break;  // all four epilogue warps leave together
     tc_fence_after_sync();
     const uint32_t taddr = lane_base + static_cast<uint32_t>(buf * BN);
     // the MMA (leader CTA) waits until every epilogue thread of the pair has read the buffer
@@ -393,6 +490,7 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uin
     };
     const int i = w.ti * Cfg::kTileM + q * kBM + row;
     const int jt = (w.tj * MC + pair) * BN;  // first column of this pair's tile
+    out.y0 = w.ti * Cfg::kTileM + q * kBM + quarter * 32;
     if (!w.partial) {
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
@@ -402,8 +500,8 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uin
         if (c + 32 == BN) release();  // last read of this accumulator: hand it back
         float v[32];
 #pragma unroll
-        for (int t = 0; t < 32; ++t) v[t] = __uint_as_float(r[t]);
-        store_chunk(a, i, jt + c, v);
+        for (int t = 0; t < 32; ++t) v[t] = a.alpha * __uint_as_float(r[t]);
+        out.put(i, jt + c, v, (c >> 5) & 1);
       }
     } else {
       // Partial of this k-range: column-major inside the tile so that a warp's
@@ -444,17 +542,21 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, TcCtrl* ctrl, uin
 #pragma unroll
             for (int t = 0; t < 32; ++t) v[t] += __ldcg(ps + static_cast<size_t>(c + t) * kBM + row);
           }
-          store_chunk(a, i, jt + c, v);
+#pragma unroll
+          for (int t = 0; t < 32; ++t) v[t] *= a.alpha;
+          out.put(i, jt + c, v, (c >> 5) & 1);
         }
       }
     }
   }
+  out.finish();  // every bulk store of C has completed before the CTA can exit
 }
 
 template <int BN, int CG, int MC>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p,
-                   const __grid_constant__ CUtensorMap map_q, const TcArgs a) {
+                   const __grid_constant__ CUtensorMap map_q,
+                   const __grid_constant__ CUtensorMap map_c, const TcArgs a) {
   using Cfg = TcConfig<BN, CG, MC>;
   extern __shared__ uint8_t smem_raw[];
   // 128-byte swizzle atoms need 1024-byte aligned tiles.
@@ -462,7 +564,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   uint8_t* ring_a = smem;
   uint8_t* ring_b = smem + Cfg::kStages * Cfg::kABytes;
-  TcCtrl* ctrl = reinterpret_cast<TcCtrl*>(smem + Cfg::kRingBytes);
+  uint8_t* staging = smem + Cfg::kRingBytes;  // 1024-byte aligned: whole stages precede it
+  TcCtrl* ctrl = reinterpret_cast<TcCtrl*>(smem + Cfg::kRingBytes + Cfg::kStagingBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -506,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (rank % CG == 0) mma_role<BN, CG, MC>(a, ring_a, ring_b, ctrl, tmem_base, rank, first, stride);
   } else {
-    epilogue_role<BN, CG, MC>(a, ctrl, tmem_base, warp, lane, rank, first, stride);
+    epilogue_role<BN, CG, MC>(a, &map_c, staging, ctrl, tmem_base, warp, lane, rank, first, stride);
   }
 
   tc_fence_before_sync();

@@ -30,11 +30,12 @@ cudaError_t TC_NAME(tc_prepare_bn, TC_BN, _cg, TC_CG, _mc, TC_MC)(int* max_clust
 }
 
 cudaError_t TC_NAME(tc_launch_bn, TC_BN, _cg, TC_CG, _mc, TC_MC)(const CUtensorMap& map_p,
-                                                     const CUtensorMap& map_q, const TcArgs& args,
+                                                     const CUtensorMap& map_q,
+                                                     const CUtensorMap& map_c, const TcArgs& args,
                                                      int grid, cudaStream_t stream) {
   using Cfg = TcConfig<TC_BN, TC_CG, TC_MC>;
   if (TC_CG * TC_MC == 1) {
-    tc_gemm_kernel<TC_BN, TC_CG, TC_MC><<<grid, kThreads, Cfg::kSmemBytes, stream>>>(map_p, map_q, args);
+    tc_gemm_kernel<TC_BN, TC_CG, TC_MC><<<grid, kThreads, Cfg::kSmemBytes, stream>>>(map_p, map_q, map_c, args);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -49,7 +50,7 @@ cudaError_t TC_NAME(tc_launch_bn, TC_BN, _cg, TC_CG, _mc, TC_MC)(const CUtensorM
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<TC_BN, TC_CG, TC_MC>, map_p, map_q, args);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<TC_BN, TC_CG, TC_MC>, map_p, map_q, map_c, args);
 }
 
 }  // namespace g10

@@ -151,7 +151,7 @@ typedef struct {
   int32_t raster_group;    /* tile rows per raster group */
   int32_t repack_a;        /* A copied to an aligned workspace first */
   int32_t repack_b;        /* B copied to an aligned workspace first */
-  int32_t vector_store;    /* epilogue writes C rows with 16-byte stores */
+  int32_t vector_store;    /* epilogue writes C rows with 16-byte (or bulk tensor) stores */
   int32_t grid;            /* CTAs launched for the main kernel */
   int32_t launches;        /* kernels launched by one gemm_run */
   int32_t schedule;        /* 0: whole (or split-K) tiles; 1: stream-K tail */
@@ -193,7 +193,12 @@ typedef enum {
   GEMM_OPT_MAX_GRID = 6,       /* 0 auto, else at most this many CTAs (persistent CTAs then
                                   walk more tiles each) */
   GEMM_OPT_STREAM_K = 7,       /* 0 auto, 1 never, 2 always when the last wave is incomplete */
-  GEMM_OPT_STAGES = 8          /* 0 auto (deepest ring that fits), else at most this many stages */
+  GEMM_OPT_STAGES = 8,         /* 0 auto (deepest ring that fits), else at most this many stages */
+  GEMM_OPT_L2_HINTS = 9,       /* bit 0: A/B tile loads marked evict-last in L2; bit 1: C written
+                                  with streaming (evict-first) stores */
+  GEMM_OPT_EPILOGUE = 10       /* 0 auto: C tiles leave through shared-memory staging and bulk
+                                  tensor stores when rows are 16-byte aligned and beta == 0;
+                                  2: always direct stores from registers */
 } gemm_option_t;
 
 /* Set an option on a handle.  Errors: GEMM_ERR_INVALID_ARG for an unknown
