@@ -316,9 +316,11 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   }
   P.workspace_bytes = static_cast<int64_t>(ws);
   P.vector_store = (!swap && reinterpret_cast<uintptr_t>(C) % 16 == 0 && (ldc * c_elem) % 16 == 0) ? 1 : 0;
-  // Bulk tensor stores need 16-byte aligned rows; the blend with the old C
-  // (beta != 0) keeps the direct path, which reads C as it writes it.
-  pl.tma_store = P.vector_store && beta == 0.0f && o.tma_store != 2;
+  // Bulk tensor stores need 16-byte aligned rows and a row width that is a
+  // whole number of 16-byte pieces (a partial piece at the right edge would be
+  // written whole, past column N); the blend with the old C (beta != 0) keeps
+  // the direct path, which reads C as it writes it.
+  pl.tma_store = P.vector_store && (N * c_elem) % 16 == 0 && beta == 0.0f && o.tma_store != 2;
   P.launches = 1 + P.repack_a + P.repack_b;
   *out = pl;
   return GEMM_OK;

@@ -64,11 +64,15 @@ struct TcConfig {
   // epilogue staging: per epilogue warp two 32-row x 128-byte buffers for bulk stores of C
   static constexpr int kStagingBytes = 4 * 2 * 32 * 128;
   static constexpr int kCtrlBytes = 256;
-  static constexpr int kRingMax = 232448 - 1024 - kStagingBytes - kCtrlBytes;  // 227 KB less the rest
+  static constexpr int kRingMax = 232448 - 1024 - kStagingBytes - 1024;  // 227 KB less the rest
   static constexpr int kStages = kRingMax / kStageBytes > 8 ? 8 : kRingMax / kStageBytes;
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kTmemCols = 2 * BN;       // two fp32 accumulators of BN columns
-  static constexpr size_t kSmemBytes = 1024 + kRingBytes + kStagingBytes + kCtrlBytes;  // + alignment slack
+  // layout: [alignment slack][ring][control block, padded to 1 KB][staging]; a
+  // launch without the bulk-store epilogue requests shared memory only up to the
+  // control block, leaving the rest to L1.
+  static constexpr size_t kSmemNoStaging = 1024 + kRingBytes + 1024;
+  static constexpr size_t kSmemBytes = kSmemNoStaging + kStagingBytes;
 };
 
 struct TcCtrl {
@@ -564,8 +568,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   uint8_t* ring_a = smem;
   uint8_t* ring_b = smem + Cfg::kStages * Cfg::kABytes;
-  uint8_t* staging = smem + Cfg::kRingBytes;  // 1024-byte aligned: whole stages precede it
-  TcCtrl* ctrl = reinterpret_cast<TcCtrl*>(smem + Cfg::kRingBytes + Cfg::kStagingBytes);
+  TcCtrl* ctrl = reinterpret_cast<TcCtrl*>(smem + Cfg::kRingBytes);
+  uint8_t* staging = smem + Cfg::kRingBytes + 1024;  // 1024-byte aligned; requested only with tma_store
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;

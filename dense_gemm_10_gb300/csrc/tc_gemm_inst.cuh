@@ -34,8 +34,9 @@ cudaError_t TC_NAME(tc_launch_bn, TC_BN, _cg, TC_CG, _mc, TC_MC)(const CUtensorM
                                                      const CUtensorMap& map_c, const TcArgs& args,
                                                      int grid, cudaStream_t stream) {
   using Cfg = TcConfig<TC_BN, TC_CG, TC_MC>;
+  const size_t smem = args.tma_store ? Cfg::kSmemBytes : Cfg::kSmemNoStaging;
   if (TC_CG * TC_MC == 1) {
-    tc_gemm_kernel<TC_BN, TC_CG, TC_MC><<<grid, kThreads, Cfg::kSmemBytes, stream>>>(map_p, map_q, map_c, args);
+    tc_gemm_kernel<TC_BN, TC_CG, TC_MC><<<grid, kThreads, smem, stream>>>(map_p, map_q, map_c, args);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -46,7 +47,7 @@ cudaError_t TC_NAME(tc_launch_bn, TC_BN, _cg, TC_CG, _mc, TC_MC)(const CUtensorM
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;

@@ -197,7 +197,8 @@ typedef enum {
   GEMM_OPT_L2_HINTS = 9,       /* bit 0: A/B tile loads marked evict-last in L2; bit 1: C written
                                   with streaming (evict-first) stores */
   GEMM_OPT_EPILOGUE = 10       /* 0 auto: C tiles leave through shared-memory staging and bulk
-                                  tensor stores when rows are 16-byte aligned and beta == 0;
+                                  tensor stores when rows start 16-byte aligned, N is a whole
+                                  number of 16-byte pieces and beta == 0;
                                   2: always direct stores from registers */
 } gemm_option_t;
 
