@@ -40,7 +40,6 @@ struct Options {
   int max_grid = 0;
   int stream_k = 0;  // 0 auto, 1 off, 2 on
   int stages = 0;    // 0: the configuration's maximum ring depth
-  int l2_hints = 0;  // GEMM_OPT_L2_HINTS
   int tma_store = 0; // GEMM_OPT_EPILOGUE: 0 auto, 1 bulk stores when possible, 2 direct stores
 };
 
@@ -79,7 +78,7 @@ bool tma_aligned(const void* p, int64_t ld) {
 // measurements of the 4096^3 and 8192 x 12288 x 4096 bf16 GEMMs.  (A multicast
 // cluster's schedule tile is two 256 x 256 tiles worked side by side.)
 double tile_kb_cost(const TileConfig& c) {
-  if (c.mc == 2) return 0.85;
+  if (c.mc == 2) return 1.05;  // measured slightly slower than a lone pair: used only on request
   if (c.cg == 2) return c.bn == 256 ? 1.0 : 0.62;
   return c.bn == 256 ? 1.15 : c.bn == 128 ? 0.85 : 0.6;
 }
@@ -528,10 +527,6 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
       if (value < 0 || value > 64) return GEMM_ERR_INVALID_ARG;
       h->opt.stages = static_cast<int>(value);
       return GEMM_OK;
-    case GEMM_OPT_L2_HINTS:
-      if (value < 0 || value > 3) return GEMM_ERR_INVALID_ARG;
-      h->opt.l2_hints = static_cast<int>(value);
-      return GEMM_OK;
     case GEMM_OPT_EPILOGUE:
       if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
       h->opt.tma_store = static_cast<int>(value);
@@ -636,7 +631,6 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
   a.p_kmajor = P.a_kmajor;
   a.q_kmajor = P.b_kmajor;
   a.stages = P.stages;
-  a.l2_hints = h->opt.l2_hints;
   a.idesc = make_idesc_f16(pl.bf16, !pl.p.kmajor, !pl.q.kmajor, kBM * cg, P.bn);
   a.alpha = alpha;
   a.beta = beta;

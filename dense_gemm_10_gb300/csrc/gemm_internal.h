@@ -35,7 +35,6 @@ struct TcArgs {
   int32_t q_kmajor;      // Q has K contiguous (else J contiguous)
   uint32_t idesc;        // tcgen05 instruction descriptor
   int32_t stages;        // ring stages in use, 1 .. the configuration's maximum
-  int32_t l2_hints;      // bit 0: A/B loads evict-last in L2; bit 1: C stores streaming (evict-first)
   float alpha, beta;
   void* C;
   int64_t c_si, c_sj;

@@ -164,10 +164,7 @@ __device__ __forceinline__ void store_chunk(const TcArgs& a, int i, int j0, floa
           const float4 c = p[q];
           o.x += a.beta * c.x; o.y += a.beta * c.y; o.z += a.beta * c.z; o.w += a.beta * c.w;
         }
-        if (a.l2_hints & 2)
-          __stcs(p + q, o);  // written once, not re-read here: evict first
-        else
-          p[q] = o;
+        p[q] = o;
       }
     } else {
       uint4* p = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.C) + base);
@@ -186,12 +183,8 @@ __device__ __forceinline__ void store_chunk(const TcArgs& a, int i, int j0, floa
             o[2 * t + 1] += a.beta * f.y;
           }
         }
-        const uint4 packed = make_uint4(pack2(a, o[0], o[1]), pack2(a, o[2], o[3]), pack2(a, o[4], o[5]),
-                                        pack2(a, o[6], o[7]));
-        if (a.l2_hints & 2)
-          __stcs(p + q, packed);
-        else
-          p[q] = packed;
+        p[q] = make_uint4(pack2(a, o[0], o[1]), pack2(a, o[2], o[3]), pack2(a, o[4], o[5]),
+                          pack2(a, o[6], o[7]));
       }
     }
     return;
@@ -284,9 +277,6 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
   const uint32_t leader = static_cast<uint32_t>(pair * CG);
   // multicast of P: this CTA and the CTA of the other pair with the same rank inside its pair
   const uint16_t p_mask = static_cast<uint16_t>((1u << q) | (1u << (q + CG)));
-  // Operand tiles are re-read by other tiles: ask L2 to keep them over the output stream.
-  const bool hint = (a.l2_hints & 1) != 0;
-  const uint64_t policy = hint ? l2_policy_evict_last() : 0;
   int stage = 0;
   uint32_t phase = 0;
   uint32_t pending = 0, pending_parity = 0;  // copies in flight, per stage
@@ -316,23 +306,13 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
         if (elect_one()) {
           if (q == 0) mbar_arrive_expect_tx(full_local, CG * Cfg::kStageBytes);
           auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
-            if constexpr (CG == 2) {
-              if (hint)
-                tma_load_2d_pair_hint(dst, map, full, x, y, policy);
-              else
-                tma_load_2d_pair(dst, map, full, x, y);
-            } else {
-              if (hint)
-                tma_load_2d_hint(dst, map, full, x, y, policy);
-              else
-                tma_load_2d(dst, map, full, x, y);
-            }
+            if constexpr (CG == 2)
+              tma_load_2d_pair(dst, map, full, x, y);
+            else
+              tma_load_2d(dst, map, full, x, y);
           };
           auto load_mc = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
-            if (hint)
-              tma_load_2d_pair_multicast_hint(dst, map, full, x, y, p_mask, policy);
-            else
-              tma_load_2d_pair_multicast(dst, map, full, x, y, p_mask);
+            tma_load_2d_pair_multicast(dst, map, full, x, y, p_mask);
           };
           if constexpr (MC == 2) {
             // this pair's half of the P tile: 64 rows (K-major) or one 64-wide atom (M-major)

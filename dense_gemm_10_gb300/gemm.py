@@ -18,7 +18,8 @@ STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED", 3:
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NO_DEVICE, ERR_CUDA, ERR_TENSORMAP, ERR_TIMEOUT, ERR_WORKSPACE = range(8)
 PATH_NOOP, PATH_SCALE_C, PATH_TC_1CTA, PATH_TC_2CTA, PATH_TC_2CTA_MULTICAST = 0, 1, 2, 3, 4
 (OPT_WAIT_LIMIT_NS, OPT_FORCE_PATH, OPT_SPLIT_K, OPT_RASTER_GROUP, OPT_FORCE_BN, OPT_TEST_DROP_LOAD, OPT_MAX_GRID,
- OPT_STREAM_K, OPT_STAGES, OPT_L2_HINTS, OPT_EPILOGUE) = range(11)
+ OPT_STREAM_K, OPT_STAGES) = range(9)
+OPT_EPILOGUE = 10
 SCHED_TILES, SCHED_STREAM_K = 0, 1
 
 # Exported functions and their (restype, argtypes).

@@ -194,8 +194,6 @@ typedef enum {
                                   walk more tiles each) */
   GEMM_OPT_STREAM_K = 7,       /* 0 auto, 1 never, 2 always when the last wave is incomplete */
   GEMM_OPT_STAGES = 8,         /* 0 auto (deepest ring that fits), else at most this many stages */
-  GEMM_OPT_L2_HINTS = 9,       /* bit 0: A/B tile loads marked evict-last in L2; bit 1: C written
-                                  with streaming (evict-first) stores */
   GEMM_OPT_EPILOGUE = 10       /* 0 auto: C tiles leave through shared-memory staging and bulk
                                   tensor stores when rows start 16-byte aligned, N is a whole
                                   number of 16-byte pieces and beta == 0;
