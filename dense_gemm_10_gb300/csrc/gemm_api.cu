@@ -79,13 +79,13 @@ bool tma_aligned(const void* p, int64_t ld) {
 // cluster's schedule tile is two 256 x 256 tiles worked side by side.)
 double tile_kb_cost(const TileConfig& c) {
   if (c.mc == 2) return 1.05;  // measured slightly slower than a lone pair: used only on request
-  if (c.cg == 2) return c.bn == 256 ? 1.0 : 0.62;
+  if (c.cg == 2) return c.bn == 256 ? 1.0 : c.bn == 128 ? 0.62 : 0.55;
   return c.bn == 256 ? 1.15 : c.bn == 128 ? 0.85 : 0.6;
 }
 
 // Resident schedule slots (CTAs, CTA pairs or clusters) per tile configuration.
 struct SlotTable {
-  int n[kNumTileConfigs] = {1, 1, 1, 1, 1, 1};
+  int n[kNumTileConfigs] = {1, 1, 1, 1, 1, 1, 1};
   int of(int cfg) const { return n[cfg]; }
   static SlotTable even(int sm_count) {
     SlotTable t;
@@ -257,7 +257,7 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
 
   // Tile configuration and schedule: the configuration with the lowest
   // estimated time, est_time() below.
-  static const int kPreference[kNumTileConfigs] = {5, 4, 3, 2, 1, 0};  // ties go to the first
+  static const int kPreference[kNumTileConfigs] = {5, 4, 3, 2, 1, 6, 0};  // ties go to the first
   Choice best;
   for (int cfg : kPreference) {
     const TileConfig& c = kTileConfigs[cfg];
@@ -267,6 +267,7 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
     if (!o.force_bn && c.bn > 64 && pl.J <= c.bn / 2) continue;       // too wide for J
     if (!o.force_path && c.cg == 2 && pl.I <= kBM) continue;          // one row of tiles
     if (!o.force_path && c.mc == 2 && cdiv(pl.J, c.bn) < 2) continue;  // nothing to share
+    if (c.bn / c.cg < 64 && !pl.q.kmajor) continue;  // half-atom Q halves: K-major only
     int nslots = slots.of(cfg);
     if (o.max_grid) nslots = std::min(nslots, std::max(1, o.max_grid / (c.cg * c.mc)));
     Choice ch = choose_schedule(o, cdiv(pl.I, kBM * c.cg), cdiv(cdiv(pl.J, c.bn), c.mc), num_kb, cfg, nslots);

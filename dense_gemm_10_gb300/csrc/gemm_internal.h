@@ -54,7 +54,7 @@ struct TcArgs {
 struct TileConfig {
   int bn, cg, mc;
 };
-constexpr int kNumTileConfigs = 6;
+constexpr int kNumTileConfigs = 7;
 extern const TileConfig kTileConfigs[kNumTileConfigs];
 int tc_config_index(int bn, int cg, int mc);  // -1 if not built
 int tc_stages(int bn, int cg, int mc);

@@ -14,9 +14,10 @@ TC_DECLARE(256, 1, 1)
 TC_DECLARE(128, 2, 1)
 TC_DECLARE(256, 2, 1)
 TC_DECLARE(256, 2, 2)
+TC_DECLARE(64, 2, 1)
 
 const TileConfig kTileConfigs[kNumTileConfigs] = {
-    {64, 1, 1}, {128, 1, 1}, {256, 1, 1}, {128, 2, 1}, {256, 2, 1}, {256, 2, 2}};
+    {64, 1, 1}, {128, 1, 1}, {256, 1, 1}, {128, 2, 1}, {256, 2, 1}, {256, 2, 2}, {64, 2, 1}};
 
 int tc_config_index(int bn, int cg, int mc) {
   for (int i = 0; i < kNumTileConfigs; ++i)
@@ -32,6 +33,7 @@ int tc_stages(int bn, int cg, int mc) {
     case 3: return TcConfig<128, 2, 1>::kStages;
     case 4: return TcConfig<256, 2, 1>::kStages;
     case 5: return TcConfig<256, 2, 2>::kStages;
+    case 6: return TcConfig<64, 2, 1>::kStages;
   }
   return 0;
 }
@@ -45,6 +47,7 @@ cudaError_t tc_prepare(int bn, int cg, int mc, int* max_clusters) {
     case 3: return tc_prepare_bn128_cg2_mc1(max_clusters);
     case 4: return tc_prepare_bn256_cg2_mc1(max_clusters);
     case 5: return tc_prepare_bn256_cg2_mc2(max_clusters);
+    case 6: return tc_prepare_bn64_cg2_mc1(max_clusters);
   }
   return cudaErrorInvalidValue;
 }
@@ -58,6 +61,7 @@ cudaError_t tc_launch(int bn, int cg, int mc, const CUtensorMap& map_p, const CU
     case 3: return tc_launch_bn128_cg2_mc1(map_p, map_q, map_c, args, grid, stream);
     case 4: return tc_launch_bn256_cg2_mc1(map_p, map_q, map_c, args, grid, stream);
     case 5: return tc_launch_bn256_cg2_mc2(map_p, map_q, map_c, args, grid, stream);
+    case 6: return tc_launch_bn64_cg2_mc1(map_p, map_q, map_c, args, grid, stream);
   }
   return cudaErrorInvalidValue;
 }

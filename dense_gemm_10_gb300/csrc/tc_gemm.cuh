@@ -52,7 +52,9 @@ template <int BN, int CG, int MC>
 struct TcConfig {
   static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
   static_assert(CG == 1 || CG == 2, "CTA group");
-  static_assert(CG == 1 || BN >= 128, "a CTA pair needs 64-column halves of Q");
+  // a CTA pair with BN == 64 loads 32-row halves of Q: K-major Q only (an
+  // M/N-major swizzle atom is 64 elements wide); the planner enforces it
+  static_assert(CG == 1 || BN >= 64, "a CTA pair needs at least 32-row halves of Q");
   static_assert(MC == 1 || (MC == 2 && CG == 2), "multicast runs on CTA pairs");
   static constexpr int kCluster = CG * MC;       // CTAs per cluster
   static constexpr int kTileM = kBM * CG;        // rows of D per tile

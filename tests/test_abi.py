@@ -104,11 +104,20 @@ def test_plan_major_modes(ta, tb, ak, bk):
 
 
 def test_plan_lm_head_swaps():
+    """M = 64: the vocabulary rides on the MMA's M (swap-AB); a CTA pair covers 256
+    vocabulary rows and each CTA loads half of the 64 activation rows."""
     p = G.plan(64, 32000, 4096, 0, 1)
-    assert p.swap_ab == 1 and p.path == G.PATH_TC_1CTA
+    assert p.swap_ab == 1 and p.path == G.PATH_TC_2CTA and p.cluster == 2
     assert p.a_kmajor == 1 and p.b_kmajor == 1   # MMA A = weights (N x K), MMA B = activations (M x K)
-    assert p.bn == 64 and p.tiles == 250
-    assert p.schedule == G.SCHED_STREAM_K and p.dp_tiles == 152   # one full wave, then 98 tiles shared
+    assert p.bm == 256 and p.bn == 64 and p.tiles == 125
+    assert p.schedule == G.SCHED_STREAM_K and p.dp_tiles == 76   # one full wave of pairs, then 49 tiles shared
+
+
+def test_plan_half_atom_pairs_need_k_major_q():
+    """A CTA pair with 64-wide tiles loads 32-row halves of the MMA's B operand,
+    which only the K-major layout allows."""
+    p = G.plan(64, 32000, 4096, 1, 1)     # A stored K x M: the activations are M-major
+    assert not (p.cluster == 2 and p.bn == 64)
     assert p.vector_store == 0 and p.grid == 152
 
 
