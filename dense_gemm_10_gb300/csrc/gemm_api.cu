@@ -79,7 +79,7 @@ bool tma_aligned(const void* p, int64_t ld) {
 // cluster's schedule tile is two 256 x 256 tiles worked side by side.)
 double tile_kb_cost(const TileConfig& c) {
   if (c.mc == 2) return 1.05;  // measured slightly slower than a lone pair: used only on request
-  if (c.cg == 2) return c.bn == 256 ? 1.0 : c.bn == 128 ? 0.62 : 0.55;
+  if (c.cg == 2) return c.bn == 256 ? 1.0 : c.bn == 128 ? 0.62 : 0.65;
   return c.bn == 256 ? 1.15 : c.bn == 128 ? 0.85 : 0.6;
 }
 
@@ -145,7 +145,7 @@ double sk_tail_cost(int64_t tiles, int64_t num_kb, int64_t g) {
 }
 
 Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64_t num_kb, int cfg,
-                       int slots) {
+                       int slots, bool hbm_bound) {
   Choice ch;
   const TileConfig& tc = kTileConfigs[cfg];
   const int cl = tc.cg * tc.mc;  // CTAs per slot
@@ -171,12 +171,19 @@ Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64
     ch.valid = true;
     return ch;
   }
-  // Whole tiles: ceil(tiles / slots) waves.
-  double best = static_cast<double>(cdiv(tiles, slots) * num_kb);
+  // Whole tiles: ceil(tiles / slots) waves, on a grid that gives every slot the
+  // same number of tiles (for an HBM-bound GEMM the slots of a last, partly
+  // filled wave only compete for bandwidth).
+  const int64_t waves = cdiv(tiles, slots);
+  double best = static_cast<double>(waves * num_kb);
+  ch.slots = static_cast<int>(cdiv(tiles, waves));
   // Stream-K tail: the tiles of the incomplete last wave shared by g slots.
   const int64_t full_waves = tiles / slots;
   const int64_t sk_tiles = tiles - full_waves * slots;
-  if (o.stream_k != 1 && sk_tiles > 0 && sk_tiles * cl <= kCounterCap) {
+  // An HBM-bound GEMM with at least one full wave already streams from every
+  // SM: evening out the waves only adds the partial-sum traffic.
+  const bool sk_allowed = o.stream_k == 2 || (o.stream_k == 0 && !(hbm_bound && tiles >= slots));
+  if (sk_allowed && sk_tiles > 0 && sk_tiles * cl <= kCounterCap) {
     const int64_t iters = sk_tiles * num_kb;
     int64_t best_g = 0;
     double best_tail = 1e300;
@@ -190,6 +197,7 @@ Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64
     const double sk = static_cast<double>(full_waves * num_kb) + best_tail;
     if (best_g > 0 && (o.stream_k == 2 || sk < best - 1e-9)) {
       best = sk;
+      ch.slots = slots;
       s.mode = kSchedStreamK;
       s.dp_tiles = static_cast<int32_t>(full_waves * slots);
       s.sk_slots = static_cast<int32_t>(best_g);
@@ -254,6 +262,11 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   P.b_kmajor = pl.q.kmajor ? 1 : 0;
 
   const int64_t num_kb = cdiv(K, kBK);
+  // Below the machine balance (≈ 2.2 PFLOP/s over ≈ 7 TB/s ≈ 300 FLOP per byte)
+  // the GEMM is bound by HBM, not by the tensor cores.
+  const double alg_bytes = 2.0 * (static_cast<double>(M) * K + static_cast<double>(K) * N) +
+                           static_cast<double>(M) * N * c_elem * (beta != 0.0f ? 2 : 1);
+  const bool hbm_bound = 2.0 * static_cast<double>(M) * N * K / alg_bytes < 256.0;
 
   // Tile configuration and schedule: the configuration with the lowest
   // estimated time, est_time() below.
@@ -270,7 +283,8 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
     if (c.bn / c.cg < 64 && !pl.q.kmajor) continue;  // half-atom Q halves: K-major only
     int nslots = slots.of(cfg);
     if (o.max_grid) nslots = std::min(nslots, std::max(1, o.max_grid / (c.cg * c.mc)));
-    Choice ch = choose_schedule(o, cdiv(pl.I, kBM * c.cg), cdiv(cdiv(pl.J, c.bn), c.mc), num_kb, cfg, nslots);
+    Choice ch = choose_schedule(o, cdiv(pl.I, kBM * c.cg), cdiv(cdiv(pl.J, c.bn), c.mc), num_kb, cfg, nslots,
+                                hbm_bound);
     if (ch.valid && ch.cost < best.cost - 1e-9) best = ch;
   }
   if (!best.valid) return GEMM_ERR_INVALID_ARG;  // forced options admit no configuration

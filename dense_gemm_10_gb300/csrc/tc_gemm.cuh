@@ -505,17 +505,23 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
         for (int t = 0; t < 32; ++t)
           __stcg(part + static_cast<size_t>(c + t) * kBM + row, __uint_as_float(r[t]));
       }
-      __threadfence();
+      // One GPU-scope fence by the arriving thread, after the barrier that orders
+      // every epilogue thread's partial stores before it, publishes the whole
+      // partial (fences are cumulative); a fence in each of the 128 threads
+      // would stall every one of them on its own stores.
       bar_sync(1, 128);
       if (threadIdx.x == 64) {
+        __threadfence();
         const int old = atomicAdd(&a.counters[ctr], 1);
         const uint32_t last = (old == w.ncontrib - 1) ? 1u : 0u;
-        if (last) atomicExch(&a.counters[ctr], 0);  // clean for the next call
+        if (last) {
+          atomicExch(&a.counters[ctr], 0);  // clean for the next call
+          __threadfence();                  // the other contributions, before anyone reads them
+        }
         *reinterpret_cast<volatile uint32_t*>(&ctrl->last) = last;
       }
       bar_sync(1, 128);
       if (*reinterpret_cast<volatile uint32_t*>(&ctrl->last)) {
-        __threadfence();
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           float v[32];

@@ -104,13 +104,22 @@ def test_plan_major_modes(ta, tb, ak, bk):
 
 
 def test_plan_lm_head_swaps():
-    """M = 64: the vocabulary rides on the MMA's M (swap-AB); a CTA pair covers 256
-    vocabulary rows and each CTA loads half of the 64 activation rows."""
+    """M = 64: the vocabulary rides on the MMA's M (swap-AB), 128 vocabulary rows
+    against the 64 activation rows per tile.  The GEMM is bound by HBM, so there
+    is no stream-K tail (more than a full wave of tiles already streams from
+    every SM), and the 250 tiles go out as two equal waves of 125 CTAs
+    rather than 152 + 98."""
     p = G.plan(64, 32000, 4096, 0, 1)
-    assert p.swap_ab == 1 and p.path == G.PATH_TC_2CTA and p.cluster == 2
+    assert p.swap_ab == 1 and p.path == G.PATH_TC_1CTA and p.cluster == 1
     assert p.a_kmajor == 1 and p.b_kmajor == 1   # MMA A = weights (N x K), MMA B = activations (M x K)
-    assert p.bm == 256 and p.bn == 64 and p.tiles == 125
-    assert p.schedule == G.SCHED_STREAM_K and p.dp_tiles == 76   # one full wave of pairs, then 49 tiles shared
+    assert p.bm == 128 and p.bn == 64 and p.tiles == 250
+    assert p.schedule == G.SCHED_TILES and p.grid == 125
+
+
+def test_plan_compute_bound_keeps_stream_k():
+    """Above the machine balance the last partial wave is shared out (stream-K)."""
+    p = G.plan(4096, 4096, 4096, 0, 1)
+    assert p.schedule == G.SCHED_STREAM_K and p.path == G.PATH_TC_2CTA and p.grid == 152
 
 
 def test_plan_half_atom_pairs_need_k_major_q():
@@ -118,7 +127,7 @@ def test_plan_half_atom_pairs_need_k_major_q():
     which only the K-major layout allows."""
     p = G.plan(64, 32000, 4096, 1, 1)     # A stored K x M: the activations are M-major
     assert not (p.cluster == 2 and p.bn == 64)
-    assert p.vector_store == 0 and p.grid == 152
+    assert p.vector_store == 0 and p.grid == 125   # two equal waves of 250 whole tiles
 
 
 def test_plan_few_tiles_stream_k():
