@@ -41,6 +41,7 @@ struct Options {
   int stream_k = 0;  // 0 auto, 1 off, 2 on
   int stages = 0;    // 0: the configuration's maximum ring depth
   int tma_store = 0; // GEMM_OPT_EPILOGUE: 0 auto, 1 bulk stores when possible, 2 direct stores
+  int kdepth = 0;    // GEMM_OPT_KDEPTH: 0 auto, else 64-wide k-slices per ring stage
 };
 
 // One stored operand, as the tensor-memory-accelerator copy engine will see it.
@@ -56,7 +57,7 @@ struct Operand {
 
 struct Plan {
   gemm_plan_t pub{};
-  bool tma_store = false;  // C leaves through staged bulk tensor stores
+  int32_t tma_store = kBulkNone;  // BulkStore: how C leaves the epilogue
   Sched sched{};
   Operand p, q;
   int64_t I = 0, J = 0, K = 0;
@@ -73,7 +74,13 @@ bool tma_aligned(const void* p, int64_t ld) {
   return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((ld * 2) % 16 == 0);
 }
 
-// Relative time of one k-block of one schedule tile for each tile
+// 64-wide k-slices per ring stage unless GEMM_OPT_KDEPTH says otherwise.  The
+// 64-wide tiles have small stages (20-24 KB per k-slice); two slices per stage
+// halve the barrier round trips per byte, which measured 5-8% faster on the
+// HBM-bound 64 x 32000 x 4096 GEMM.  The wider tiles measured no gain.
+int default_kdepth(const TileConfig& c) { return c.bn == 64 ? 2 : 1; }
+
+// Relative time of one 64-wide k-slice of one schedule tile for each tile
 // configuration, in units of the CTA-pair 256 x 256 tile, from GB300
 // measurements of the 4096^3 and 8192 x 12288 x 4096 bf16 GEMMs.  (A multicast
 // cluster's schedule tile is two 256 x 256 tiles worked side by side.)
@@ -111,7 +118,7 @@ cudaError_t measure_slots(int sm_count, SlotTable* t) {
 
 struct Choice {
   bool valid = false;
-  int cfg = 0, cg = 1, bn = 64, mc = 1, slots = 1;
+  int cfg = 0, cg = 1, bn = 64, mc = 1, slots = 1, kdepth = 1;
   double cost = 1e300;
   Sched sched{};
 };
@@ -144,9 +151,11 @@ double sk_tail_cost(int64_t tiles, int64_t num_kb, int64_t g) {
   return per_slot + 1.0 + 0.5 * contrib;
 }
 
-Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64_t num_kb, int cfg,
-                       int slots, bool hbm_bound) {
+// num_kb counts stages of kdepth 64-wide k-slices each.
+Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64_t num_kb, int kdepth,
+                       int cfg, int slots, bool hbm_bound) {
   Choice ch;
+  ch.kdepth = kdepth;
   const TileConfig& tc = kTileConfigs[cfg];
   const int cl = tc.cg * tc.mc;  // CTAs per slot
   ch.cfg = cfg;
@@ -167,7 +176,7 @@ Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64
     if (tiles * cl > kCounterCap) return ch;
     s.split_k = static_cast<int32_t>(split);
     ch.cost = static_cast<double>(cdiv(tiles * split, slots)) *
-              (static_cast<double>(cdiv(num_kb, split)) + (split > 1 ? 1.5 : 0.0)) * tile_kb_cost(tc);
+              (static_cast<double>(cdiv(num_kb, split)) + (split > 1 ? 1.5 : 0.0)) * kdepth * tile_kb_cost(tc);
     ch.valid = true;
     return ch;
   }
@@ -204,7 +213,7 @@ Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64
       s.sk_iters = iters;
     }
   }
-  ch.cost = best * tile_kb_cost(tc);
+  ch.cost = best * kdepth * tile_kb_cost(tc);
   ch.valid = true;
   return ch;
 }
@@ -261,7 +270,7 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   P.a_kmajor = pl.p.kmajor ? 1 : 0;
   P.b_kmajor = pl.q.kmajor ? 1 : 0;
 
-  const int64_t num_kb = cdiv(K, kBK);
+  const int64_t num_kslices = cdiv(K, kBK);  // 64-wide k-slices
   // Below the machine balance (≈ 2.2 PFLOP/s over ≈ 7 TB/s ≈ 300 FLOP per byte)
   // the GEMM is bound by HBM, not by the tensor cores.
   const double alg_bytes = 2.0 * (static_cast<double>(M) * K + static_cast<double>(K) * N) +
@@ -283,8 +292,11 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
     if (c.bn / c.cg < 64 && !pl.q.kmajor) continue;  // half-atom Q halves: K-major only
     int nslots = slots.of(cfg);
     if (o.max_grid) nslots = std::min(nslots, std::max(1, o.max_grid / (c.cg * c.mc)));
-    Choice ch = choose_schedule(o, cdiv(pl.I, kBM * c.cg), cdiv(cdiv(pl.J, c.bn), c.mc), num_kb, cfg, nslots,
-                                hbm_bound);
+    // Two k-slices per stage where the ring still holds at least two such stages.
+    int kdepth = o.kdepth ? o.kdepth : default_kdepth(c);
+    if (kdepth > 1 && tc_stages(c.bn, c.cg, c.mc) / kdepth < 2) kdepth = 1;
+    Choice ch = choose_schedule(o, cdiv(pl.I, kBM * c.cg), cdiv(cdiv(pl.J, c.bn), c.mc),
+                                cdiv(num_kslices, kdepth), kdepth, cfg, nslots, hbm_bound);
     if (ch.valid && ch.cost < best.cost - 1e-9) best = ch;
   }
   if (!best.valid) return GEMM_ERR_INVALID_ARG;  // forced options admit no configuration
@@ -297,8 +309,9 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   P.cluster = cl;
   P.bm = kBM * cg;
   P.bn = best.bn;
-  P.bk = kBK;
-  P.stages = tc_stages(best.bn, cg, best.mc);
+  P.kdepth = best.kdepth;
+  P.bk = kBK * best.kdepth;
+  P.stages = tc_stages(best.bn, cg, best.mc) / best.kdepth;
   if (o.stages > 0 && o.stages < P.stages) P.stages = o.stages;
   P.schedule = pl.sched.mode;
   P.split_k = pl.sched.mode == kSchedTiles ? pl.sched.split_k : 1;
@@ -329,12 +342,16 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
     ws = round_up(ws + static_cast<size_t>(partial_slots(pl.sched)) * cl * best.bn * kBM * 4, 256);
   }
   P.workspace_bytes = static_cast<int64_t>(ws);
-  P.vector_store = (!swap && reinterpret_cast<uintptr_t>(C) % 16 == 0 && (ldc * c_elem) % 16 == 0) ? 1 : 0;
+  const bool c_rows_aligned = reinterpret_cast<uintptr_t>(C) % 16 == 0 && (ldc * c_elem) % 16 == 0;
+  P.vector_store = (!swap && c_rows_aligned) ? 1 : 0;
   // Bulk tensor stores need 16-byte aligned rows and a row width that is a
   // whole number of 16-byte pieces (a partial piece at the right edge would be
   // written whole, past column N); the blend with the old C (beta != 0) keeps
-  // the direct path, which reads C as it writes it.
-  pl.tma_store = P.vector_store && (N * c_elem) % 16 == 0 && beta == 0.0f && o.tma_store != 2;
+  // the direct path, which reads C as it writes it.  A swapped problem stores
+  // transposed blocks (C's rows run along the kernel's J).
+  const bool bulk = c_rows_aligned && (N * c_elem) % 16 == 0 && beta == 0.0f && o.tma_store != 2;
+  pl.tma_store = !bulk ? kBulkNone : swap ? kBulkTransposed : kBulkRows;
+  P.bulk_store = pl.tma_store;
   P.launches = 1 + P.repack_a + P.repack_b;
   *out = pl;
   return GEMM_OK;
@@ -385,23 +402,25 @@ gemm_status_t encode_operand(CUtensorMap* map, const Operand& op, const void* ba
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_TENSORMAP;
 }
 
-// Describe C (I x J in the kernel's terms, row pitch ldc) for bulk stores of
-// 32-row x 128-byte tiles with the 128-byte swizzle.
+// Describe C as stored (rows x cols, row pitch ldc) for bulk stores.  Rows:
+// boxes of 32 rows x 128 bytes with the 128-byte swizzle.  Transposed: boxes
+// of 32 rows x 32 elements, 128-byte swizzled for fp32, plain for 16 bits.
 gemm_status_t encode_c(CUtensorMap* map, void* C, int64_t rows, int64_t cols, int64_t ldc,
-                       int32_t c_type) {
+                       int32_t c_type, bool transposed) {
   auto fn = encode_fn();
   if (!fn) return GEMM_ERR_TENSORMAP;
   const int64_t esize = c_type == kCF32 ? 4 : 2;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc * esize)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), 32};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(transposed ? 32 : 128 / esize), 32};
+  const CUtensorMapSwizzle swz =
+      transposed && esize == 2 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
   cuuint32_t estr[2] = {1, 1};
   CUtensorMapDataType dt = c_type == kCF32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                            : c_type == kCBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUresult r = fn(map, dt, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(map, dt, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_TENSORMAP;
 }
 
@@ -546,6 +565,10 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
       if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
       h->opt.tma_store = static_cast<int>(value);
       return GEMM_OK;
+    case GEMM_OPT_KDEPTH:
+      if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+      h->opt.kdepth = static_cast<int>(value);
+      return GEMM_OK;
   }
   return GEMM_ERR_INVALID_ARG;
 }
@@ -632,8 +655,10 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
   if (s != GEMM_OK) return s;
   CUtensorMap map_c;
   std::memset(&map_c, 0, sizeof(map_c));
-  if (pl.tma_store) {
-    s = encode_c(&map_c, C, pl.I, pl.J, ldc, pl.c_type);
+  if (pl.tma_store != kBulkNone) {
+    // C as stored: I x J, or J x I for a swapped problem
+    s = pl.tma_store == kBulkRows ? encode_c(&map_c, C, pl.I, pl.J, ldc, pl.c_type, false)
+                                  : encode_c(&map_c, C, pl.J, pl.I, ldc, pl.c_type, true);
     if (s != GEMM_OK) return s;
   }
 
@@ -646,6 +671,7 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
   a.p_kmajor = P.a_kmajor;
   a.q_kmajor = P.b_kmajor;
   a.stages = P.stages;
+  a.kdepth = P.kdepth;
   a.idesc = make_idesc_f16(pl.bf16, !pl.p.kmajor, !pl.q.kmajor, kBM * cg, P.bn);
   a.alpha = alpha;
   a.beta = beta;
@@ -654,7 +680,7 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
   a.c_sj = pl.c_sj;
   a.c_type = pl.c_type;
   a.vec_store = P.vector_store;
-  a.tma_store = pl.tma_store ? 1 : 0;
+  a.tma_store = pl.tma_store;
   a.partials = needs_partials(pl.sched) ? reinterpret_cast<float*>(ws + pl.partial_offset) : nullptr;
   a.counters = h->d_counters;
   a.status = h->d_status;
@@ -814,8 +840,10 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   if (s != GEMM_OK) return s;
   CUtensorMap map_c;
   std::memset(&map_c, 0, sizeof(map_c));
-  if (pl.tma_store) {
-    s = encode_c(&map_c, C, pl.I, pl.J, ldc, pl.c_type);
+  if (pl.tma_store != kBulkNone) {
+    // C as stored: I x J, or J x I for a swapped problem
+    s = pl.tma_store == kBulkRows ? encode_c(&map_c, C, pl.I, pl.J, ldc, pl.c_type, false)
+                                  : encode_c(&map_c, C, pl.J, pl.I, ldc, pl.c_type, true);
     if (s != GEMM_OK) return s;
   }
   TcArgs a;
@@ -827,6 +855,7 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   a.p_kmajor = P.a_kmajor;
   a.q_kmajor = P.b_kmajor;
   a.stages = P.stages;
+  a.kdepth = P.kdepth;
   a.idesc = make_idesc_f16(pl.bf16, !pl.p.kmajor, !pl.q.kmajor, kBM * cg, P.bn);
   a.alpha = alpha;
   a.beta = beta;
@@ -835,7 +864,7 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   a.c_sj = pl.c_sj;
   a.c_type = pl.c_type;
   a.vec_store = P.vector_store;
-  a.tma_store = pl.tma_store ? 1 : 0;
+  a.tma_store = pl.tma_store;
   a.partials = needs_partials(pl.sched) ? reinterpret_cast<float*>(d->scratch + pl.partial_offset) : nullptr;
   a.counters = d->counters;
   a.status = d->status;

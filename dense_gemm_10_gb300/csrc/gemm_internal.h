@@ -30,23 +30,28 @@ enum WaitBarrier : int32_t {
 // P is the MMA "A" operand (tile rows on TMEM lanes), Q the MMA "B" operand.
 struct TcArgs {
   int32_t I, J, K;
-  Sched sched;           // work assignment (schedule.h); num_kb = ceil(K / kBK)
+  Sched sched;           // work assignment (schedule.h); num_kb = ceil(K / (kBK * kdepth))
   int32_t p_kmajor;      // P has K contiguous (else I contiguous)
   int32_t q_kmajor;      // Q has K contiguous (else J contiguous)
   uint32_t idesc;        // tcgen05 instruction descriptor
-  int32_t stages;        // ring stages in use, 1 .. the configuration's maximum
+  int32_t stages;        // ring stages in use, 1 .. the configuration's maximum / kdepth
+  int32_t kdepth;        // kBK-wide k-slices per stage (1 or 2); one barrier per stage
   float alpha, beta;
   void* C;
   int64_t c_si, c_sj;
   int32_t c_type;        // CType
   int32_t vec_store;     // c_sj == 1 and every row of C starts 16-byte aligned
-  int32_t tma_store;     // C tiles leave through shared-memory staging and bulk tensor stores
+  int32_t tma_store;     // BulkStore: how C tiles leave through shared-memory staging
   float* partials;       // partial tiles of split tiles, [partial_slots * CG][BN][kBM] fp32
   int32_t* counters;     // per split tile (x CG) arrival counters, zero between calls
   int32_t* status;       // device status word
   uint64_t wait_limit_ns;
   int32_t drop_load;     // tests only: CTA 0 skips its drop_load-th k-block load (1-based)
 };
+
+// Epilogue store paths: direct stores, or staged bulk tensor stores of rows of
+// C, or (for swapped problems, whose C is stored J x I) of transposed blocks.
+enum BulkStore : int32_t { kBulkNone = 0, kBulkRows = 1, kBulkTransposed = 2 };
 
 // Tile configurations: a tile of (128 * cg) x bn per CTA (cg == 1) or CTA
 // pair (cg == 2); mc == 2 clusters two pairs on neighbouring tiles of one tile

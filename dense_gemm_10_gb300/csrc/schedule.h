@@ -91,7 +91,7 @@ G10_HD int32_t contrib_slot(const Sched& s, const Unit& w, int32_t k) {
 }
 
 struct WorkIter {
-  const Sched* s;
+  Sched s;            // a copy: on the device it stays in registers
   int32_t slot, slots;
   int32_t phase;      // stream-K: 0 = this slot's k-range share, 1 = whole tiles
   int64_t x, x_end;   // stream-K iteration cursor
@@ -99,7 +99,7 @@ struct WorkIter {
   int32_t nseg;       // stream-K segments produced so far
 
   G10_HD WorkIter(const Sched& sc, int32_t slot_, int32_t slots_)
-      : s(&sc), slot(slot_), slots(slots_), phase(0), x(0), x_end(0), u(slot_), nseg(0) {
+      : s(sc), slot(slot_), slots(slots_), phase(0), x(0), x_end(0), u(slot_), nseg(0) {
     if (sc.mode == kSchedStreamK && slot_ < sc.sk_slots) {
       x = sk_begin(sc, slot_);
       x_end = sk_begin(sc, slot_ + 1);
@@ -107,7 +107,7 @@ struct WorkIter {
   }
 
   G10_HD bool next(Unit& w) {
-    const Sched& S = *s;
+    const Sched& S = s;
     if (S.mode == kSchedTiles) {
       const int32_t units = S.tiles_i * S.tiles_j * S.split_k;
       if (u >= units) return false;

@@ -69,6 +69,8 @@ struct TcConfig {
   static constexpr int kRingMax = 232448 - 1024 - kStagingBytes - 1024;  // 227 KB less the rest
   static constexpr int kStages = kRingMax / kStageBytes > 8 ? 8 : kRingMax / kStageBytes;
   static constexpr int kRingBytes = kStages * kStageBytes;
+  // the last tile's epilogue stages C in the idle ring: eight 4 KB buffers per epilogue warp
+  static_assert(kRingBytes >= 4 * 8 * 32 * 128, "ring too small to stage a tile of C");
   static constexpr int kTmemCols = 2 * BN;       // two fp32 accumulators of BN columns
   // layout: [alignment slack][ring][control block, padded to 1 KB][staging]; a
   // launch without the bulk-store epilogue requests shared memory only up to the
@@ -122,23 +124,51 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, TcCtrl*
 
 // ------------------------------------------------------------------ epilogue --
 
-__device__ __forceinline__ float load_c(const TcArgs& a, int64_t off) {
-  if (a.c_type == kCF32) return static_cast<const float*>(a.C)[off];
-  if (a.c_type == kCBF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(a.C)[off]);
-  return __half2float(static_cast<const __half*>(a.C)[off]);
+// The epilogue's view of C, copied out of the kernel parameters into registers
+// once per CTA.  (Reached through a pointer to the parameters instead, every
+// field would be reloaded after each global store, which the compiler must
+// assume may alias it: that made a warp's scalar store cost ~150 cycles.)
+struct COut {
+  void* C;
+  int64_t si, sj;    // element strides of C along I and J
+  int32_t I, J;
+  int32_t type;      // CType
+  float beta;
+  bool vec;          // c_sj == 1 and rows 16-byte aligned: 16-byte stores
+  int32_t tma;       // kBulkNone, kBulkRows or kBulkTransposed
+};
+
+__device__ __forceinline__ COut make_cout(const TcArgs& a) {
+  COut o;
+  o.C = a.C;
+  o.si = a.c_si;
+  o.sj = a.c_sj;
+  o.I = a.I;
+  o.J = a.J;
+  o.type = a.c_type;
+  o.beta = a.beta;
+  o.vec = a.vec_store != 0;
+  o.tma = a.tma_store;
+  return o;
 }
 
-__device__ __forceinline__ void store_c(const TcArgs& a, int64_t off, float v) {
-  if (a.c_type == kCF32)
-    static_cast<float*>(a.C)[off] = v;
-  else if (a.c_type == kCBF16)
-    static_cast<__nv_bfloat16*>(a.C)[off] = __float2bfloat16_rn(v);
+__device__ __forceinline__ float load_c(const COut& c, int64_t off) {
+  if (c.type == kCF32) return static_cast<const float*>(c.C)[off];
+  if (c.type == kCBF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(c.C)[off]);
+  return __half2float(static_cast<const __half*>(c.C)[off]);
+}
+
+__device__ __forceinline__ void store_c(const COut& c, int64_t off, float v) {
+  if (c.type == kCF32)
+    static_cast<float*>(c.C)[off] = v;
+  else if (c.type == kCBF16)
+    static_cast<__nv_bfloat16*>(c.C)[off] = __float2bfloat16_rn(v);
   else
-    static_cast<__half*>(a.C)[off] = __float2half_rn(v);
+    static_cast<__half*>(c.C)[off] = __float2half_rn(v);
 }
 
-__device__ __forceinline__ uint32_t pack2(const TcArgs& a, float lo, float hi) {
-  if (a.c_type == kCBF16) {
+__device__ __forceinline__ uint32_t pack2(int32_t type, float lo, float hi) {
+  if (type == kCBF16) {
     __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&p);
   }
@@ -146,47 +176,47 @@ __device__ __forceinline__ uint32_t pack2(const TcArgs& a, float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&p);
 }
 
-__device__ __forceinline__ float2 unpack2(const TcArgs& a, uint32_t bits) {
-  if (a.c_type == kCBF16) return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&bits));
+__device__ __forceinline__ float2 unpack2(int32_t type, uint32_t bits) {
+  if (type == kCBF16) return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&bits));
   return __half22float2(*reinterpret_cast<__half2*>(&bits));
 }
 
 // Write v + beta * C for row i, columns j0 .. j0 + 31 of D (v already holds alpha * D).
-__device__ __forceinline__ void store_chunk(const TcArgs& a, int i, int j0, float (&v)[32]) {
-  if (i >= a.I) return;
-  const bool blend = a.beta != 0.0f;
-  if (a.vec_store && j0 + 32 <= a.J) {
-    const int64_t base = static_cast<int64_t>(i) * a.c_si + j0;
-    if (a.c_type == kCF32) {
-      float4* p = reinterpret_cast<float4*>(static_cast<float*>(a.C) + base);
+__device__ __forceinline__ void store_chunk(const COut& c, int i, int j0, const float (&v)[32]) {
+  if (i >= c.I) return;
+  const bool blend = c.beta != 0.0f;
+  if (c.vec && j0 + 32 <= c.J) {
+    const int64_t base = static_cast<int64_t>(i) * c.si + j0;
+    if (c.type == kCF32) {
+      float4* p = reinterpret_cast<float4*>(static_cast<float*>(c.C) + base);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         float4 o = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         if (blend) {
-          const float4 c = p[q];
-          o.x += a.beta * c.x; o.y += a.beta * c.y; o.z += a.beta * c.z; o.w += a.beta * c.w;
+          const float4 x = p[q];
+          o.x += c.beta * x.x; o.y += c.beta * x.y; o.z += c.beta * x.z; o.w += c.beta * x.w;
         }
         p[q] = o;
       }
     } else {
-      uint4* p = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.C) + base);
+      uint4* p = reinterpret_cast<uint4*>(static_cast<uint16_t*>(c.C) + base);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         float o[8];
 #pragma unroll
         for (int t = 0; t < 8; ++t) o[t] = v[8 * q + t];
         if (blend) {
-          const uint4 c = p[q];
-          const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+          const uint4 x = p[q];
+          const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
-            const float2 f = unpack2(a, cw[t]);
-            o[2 * t] += a.beta * f.x;
-            o[2 * t + 1] += a.beta * f.y;
+            const float2 f = unpack2(c.type, xw[t]);
+            o[2 * t] += c.beta * f.x;
+            o[2 * t + 1] += c.beta * f.y;
           }
         }
-        p[q] = make_uint4(pack2(a, o[0], o[1]), pack2(a, o[2], o[3]), pack2(a, o[4], o[5]),
-                          pack2(a, o[6], o[7]));
+        p[q] = make_uint4(pack2(c.type, o[0], o[1]), pack2(c.type, o[2], o[3]), pack2(c.type, o[4], o[5]),
+                          pack2(c.type, o[6], o[7]));
       }
     }
     return;
@@ -194,45 +224,90 @@ __device__ __forceinline__ void store_chunk(const TcArgs& a, int i, int j0, floa
 #pragma unroll
   for (int t = 0; t < 32; ++t) {
     const int j = j0 + t;
-    if (j < a.J) {
-      const int64_t off = static_cast<int64_t>(i) * a.c_si + static_cast<int64_t>(j) * a.c_sj;
+    if (j < c.J) {
+      const int64_t off = static_cast<int64_t>(i) * c.si + static_cast<int64_t>(j) * c.sj;
       float o = v[t];
-      if (blend) o += a.beta * load_c(a, off);
-      store_c(a, off, o);
+      if (blend) o += c.beta * load_c(c, off);
+      store_c(c, off, o);
     }
   }
 }
 
-// One epilogue warp's output path.  The warp owns 32 rows of the tile and
-// produces them 32 columns at a time.  With tma_store the rows go through a
-// 128-byte-swizzled 32 x 128-byte staging buffer (two per warp, alternating)
-// and leave as one bulk tensor store per 128 bytes of row: whole lines in a few
-// large transfers, instead of each thread writing its own row with 16-byte
-// stores.  Otherwise store_chunk writes them directly.
-struct EpiOut {
-  const TcArgs* a;
-  const CUtensorMap* map_c;
-  uint32_t staging;  // this warp's two buffers (shared address, 1024-byte aligned)
-  int lane;
-  int y0;            // first row of the warp's 32 rows
-  int nstore;        // bulk stores issued so far
+// One epilogue warp's output path.  The warp owns 32 rows of the tile (I) and
+// produces them 32 columns (J) at a time.
+//  * kBulkRows: each thread's 32 values go into its row of a 128-byte-swizzled
+//    32 x 128-byte staging buffer, which leaves as one bulk tensor store.
+//  * kBulkTransposed (swapped problems, where C is J x I in memory): the warp's
+//    32 x 32 block is written transposed, one value per thread per memory row,
+//    so that the store's box is 32 rows of C by 32 contiguous elements.
+//  * kBulkNone: store_chunk writes the values directly.
+// Staging buffers are 4 KB.  A warp normally alternates between two, waiting
+// before reuse until the store that last read a buffer has read it; for a
+// CTA's last tile (use_ring) the idle operand ring provides eight per warp, so
+// every store of the tile is in flight at once.
+constexpr uint32_t kStagingBuf = 32 * 128;
 
-  __device__ __forceinline__ void put(int i, int j, const float (&v)[32], int half) {
-    const TcArgs& A = *a;
-    if (!A.tma_store) {
-      float w[32];
-#pragma unroll
-      for (int t = 0; t < 32; ++t) w[t] = v[t];
-      store_chunk(A, i, j, w);
-      return;
-    }
-    // 16-bit C: two 32-column pieces fill one 128-byte row (half 0, then half 1)
-    const bool wide = A.c_type == kCF32;
-    const uint32_t buf = staging + static_cast<uint32_t>((nstore & 1) * 32 * 128);
-    if (wide || half == 0) {
+struct EpiOut {
+  COut c;
+  const CUtensorMap* map_c;
+  uint32_t staging;  // this warp's buffers (shared address, 1024-byte aligned)
+  int lane;
+  int y0;            // first row of the warp's 32 rows (I)
+  int nstore;        // bulk stores issued from the current buffers
+  bool ring;         // buffers in the operand ring: no reuse, no waits
+
+  __device__ __forceinline__ void use_ring(uint32_t base) {
+    staging = base;
+    nstore = 0;
+    ring = true;
+  }
+
+  __device__ __forceinline__ uint32_t buffer(bool fresh) {
+    const uint32_t buf = staging + static_cast<uint32_t>((ring ? nstore : (nstore & 1)) * kStagingBuf);
+    if (fresh && !ring) {
       if (lane == 0) bulk_wait_group_read<1>();  // the store that last read this buffer is done
       __syncwarp();
     }
+    return buf;
+  }
+
+  __device__ __forceinline__ void issue(uint32_t buf, int x, int y) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(map_c, buf, x, y);
+      bulk_commit_group();
+    }
+    __syncwarp();
+    ++nstore;
+  }
+
+  __device__ __forceinline__ void put(int i, int j, const float (&v)[32], int half) {
+    if (c.tma == kBulkNone) {
+      store_chunk(c, i, j, v);
+      return;
+    }
+    if (c.tma == kBulkTransposed) {
+      const uint32_t buf = buffer(true);
+      if (c.type == kCF32) {
+        // memory row t holds 32 fp32 of I: 16-byte piece (lane / 4) sits at (lane / 4) ^ (t & 7)
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          st_shared_b32(buf + static_cast<uint32_t>(t * 128 + ((((lane >> 2) ^ (t & 7)) << 4) | ((lane & 3) << 2))),
+                        __float_as_uint(v[t]));
+      } else {
+        // 16-bit: unswizzled 64-byte rows
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          st_shared_b16(buf + static_cast<uint32_t>(t * 64 + lane * 2),
+                        static_cast<uint16_t>(pack2(c.type, v[t], 0.0f) & 0xFFFFu));
+      }
+      issue(buf, y0, j);
+      return;
+    }
+    // 16-bit C: two 32-column pieces fill one 128-byte row (half 0, then half 1)
+    const bool wide = c.type == kCF32;
+    const uint32_t buf = buffer(wide || half == 0);
     const uint32_t row = buf + static_cast<uint32_t>(lane * 128);
     const uint32_t sw = static_cast<uint32_t>(lane & 7);  // 128-byte swizzle of 16-byte pieces
     if (wide) {
@@ -243,24 +318,15 @@ struct EpiOut {
     } else {
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        st_shared_v4(row + (((4 * half + k) ^ sw) << 4), pack2(A, v[8 * k], v[8 * k + 1]),
-                     pack2(A, v[8 * k + 2], v[8 * k + 3]), pack2(A, v[8 * k + 4], v[8 * k + 5]),
-                     pack2(A, v[8 * k + 6], v[8 * k + 7]));
+        st_shared_v4(row + (((4 * half + k) ^ sw) << 4), pack2(c.type, v[8 * k], v[8 * k + 1]),
+                     pack2(c.type, v[8 * k + 2], v[8 * k + 3]), pack2(c.type, v[8 * k + 4], v[8 * k + 5]),
+                     pack2(c.type, v[8 * k + 6], v[8 * k + 7]));
     }
-    if (wide || half == 1) {
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_2d(map_c, buf, wide ? j : j - 32, y0);
-        bulk_commit_group();
-      }
-      __syncwarp();
-      ++nstore;
-    }
+    if (wide || half == 1) issue(buf, wide ? j : j - 32, y0);
   }
 
   __device__ __forceinline__ void finish() {
-    if (a->tma_store) {
+    if (c.tma != kBulkNone) {
       if (lane == 0) bulk_wait_group_all();
       __syncwarp();
     }
@@ -289,7 +355,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
   while (ok && work.next(w)) {
     const int i0 = w.ti * Cfg::kTileM + q * kBM;
     const int j0 = (w.tj * MC + pair) * BN + q * Cfg::kQRows;
-    for (int kb = w.kb0; kb < w.kb1; ++kb) {
+    for (int kb = w.kb0; kb < w.kb1; ++kb) {  // one stage: k-slices kb * kdepth .. + kdepth - 1
       if (!warp_wait(smem_u32(&ctrl->empty[stage]), phase ^ 1u, ctrl, a, kRoleProducer, kBarEmpty,
                      true)) {
         ok = false;
@@ -302,11 +368,11 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
       if (a.drop_load != 0 && blockIdx.x == 0 && nload == a.drop_load) {
         pending &= ~(1u << stage);  // test hook: this stage's barrier is never completed
       } else {
-        const uint32_t sa = smem_u32(ring_a + stage * Cfg::kABytes);
-        const uint32_t sb = smem_u32(ring_b + stage * Cfg::kBBytes);
-        const int k0 = kb * kBK;
+        // k-slices of this stage inside K (a ragged K leaves fewer in the last stage)
+        const int ks0 = kb * a.kdepth;
+        const int nks = min(a.kdepth, (a.K + kBK - 1) / kBK - ks0);
         if (elect_one()) {
-          if (q == 0) mbar_arrive_expect_tx(full_local, CG * Cfg::kStageBytes);
+          if (q == 0) mbar_arrive_expect_tx(full_local, CG * nks * Cfg::kStageBytes);
           auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
             if constexpr (CG == 2)
               tma_load_2d_pair(dst, map, full, x, y);
@@ -316,24 +382,30 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
           auto load_mc = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
             tma_load_2d_pair_multicast(dst, map, full, x, y, p_mask);
           };
-          if constexpr (MC == 2) {
-            // this pair's half of the P tile: 64 rows (K-major) or one 64-wide atom (M-major)
-            if (a.p_kmajor)
-              load_mc(sa + pair * 64 * 128, map_p, k0, i0 + 64 * pair);
-            else
-              load_mc(sa + pair * kMnAtomBytes, map_p, i0 + 64 * pair, k0);
-          } else if (a.p_kmajor) {
-            load(sa, map_p, k0, i0);
-          } else {
-            load(sa, map_p, i0, k0);
-            load(sa + kMnAtomBytes, map_p, i0 + 64, k0);
-          }
-          if (a.q_kmajor) {
-            load(sb, map_q, k0, j0);
-          } else {
+          for (int t = 0; t < nks; ++t) {
+            const int slot = stage * a.kdepth + t;  // ring slot of one k-slice
+            const uint32_t sa = smem_u32(ring_a + slot * Cfg::kABytes);
+            const uint32_t sb = smem_u32(ring_b + slot * Cfg::kBBytes);
+            const int k0 = (ks0 + t) * kBK;
+            if constexpr (MC == 2) {
+              // this pair's half of the P tile: 64 rows (K-major) or one 64-wide atom (M-major)
+              if (a.p_kmajor)
+                load_mc(sa + pair * 64 * 128, map_p, k0, i0 + 64 * pair);
+              else
+                load_mc(sa + pair * kMnAtomBytes, map_p, i0 + 64 * pair, k0);
+            } else if (a.p_kmajor) {
+              load(sa, map_p, k0, i0);
+            } else {
+              load(sa, map_p, i0, k0);
+              load(sa + kMnAtomBytes, map_p, i0 + 64, k0);
+            }
+            if (a.q_kmajor) {
+              load(sb, map_q, k0, j0);
+            } else {
 #pragma unroll
-            for (int c = 0; c < Cfg::kQRows / 64; ++c)
-              load(sb + c * kMnAtomBytes, map_q, j0 + 64 * c, k0);
+              for (int c = 0; c < Cfg::kQRows / 64; ++c)
+                load(sb + c * kMnAtomBytes, map_q, j0 + 64 * c, k0);
+            }
           }
         }
         __syncwarp();
@@ -399,21 +471,26 @@ __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8
         break;
       }
       tc_fence_after_sync();
-      const uint32_t sa = smem_u32(ring_a + stage * Cfg::kABytes);
-      const uint32_t sb = smem_u32(ring_b + stage * Cfg::kBBytes);
+      const int ks0 = kb * a.kdepth;
+      const int nks = min(a.kdepth, (a.K + kBK - 1) / kBK - ks0);
       // K-major: the 16-wide k-slice starts 32 bytes further along each swizzled
       // 128-byte row; 8-row groups are 1024 bytes apart.
       // MN-major: the k-slice is 16 rows of 128 bytes further on; 8-row groups are
       // 1024 bytes apart and swizzle atoms along M / N are kMnAtomBytes apart.
       const uint32_t a_step = a.p_kmajor ? 32u : 2048u;
       const uint32_t b_step = a.q_kmajor ? 32u : 2048u;
-      const uint64_t ad0 = smem_desc_sw128(sa, a.p_kmajor ? 16u : kMnAtomBytes, 1024);
-      const uint64_t bd0 = smem_desc_sw128(sb, a.q_kmajor ? 16u : kMnAtomBytes, 1024);
       if (elect_one()) {
+        for (int t = 0; t < nks; ++t) {
+          const int slot = stage * a.kdepth + t;
+          const uint64_t ad0 =
+              smem_desc_sw128(smem_u32(ring_a + slot * Cfg::kABytes), a.p_kmajor ? 16u : kMnAtomBytes, 1024);
+          const uint64_t bd0 =
+              smem_desc_sw128(smem_u32(ring_b + slot * Cfg::kBBytes), a.q_kmajor ? 16u : kMnAtomBytes, 1024);
 #pragma unroll
-        for (int k = 0; k < kBK / 16; ++k)  // the start address sits in the descriptor's low bits
-          mma_f16_ss<CG>(d_tmem, ad0 + ((a_step * k) >> 4), bd0 + ((b_step * k) >> 4), a.idesc,
-                         (kb > w.kb0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < kBK / 16; ++k)  // the start address sits in the descriptor's low bits
+            mma_f16_ss<CG>(d_tmem, ad0 + ((a_step * k) >> 4), bd0 + ((b_step * k) >> 4), a.idesc,
+                           (kb > w.kb0 || t > 0 || k > 0) ? 1u : 0u);
+        }
         commit_stage(smem_u32(&ctrl->empty[stage]));  // frees the stage once these MMAs have read it
       }
       __syncwarp();
@@ -437,7 +514,8 @@ __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8
 
 template <int BN, int CG, int MC>
 __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap* map_c,
-                                              uint8_t* staging, TcCtrl* ctrl, uint32_t tmem_base,
+                                              uint8_t* staging, uint8_t* ring, TcCtrl* ctrl,
+                                              uint32_t tmem_base,
                                               int warp, int lane, uint32_t rank, int first,
                                               int stride) {
   using Cfg = TcConfig<BN, CG, MC>;
@@ -448,11 +526,12 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
   const int row = quarter * 32 + lane;
   const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
   EpiOut out;
-  out.a = &a;
+  out.c = make_cout(a);
   out.map_c = map_c;
-  out.staging = smem_u32(staging + (warp - 2) * 2 * 32 * 128);
+  out.staging = smem_u32(staging + (warp - 2) * 2 * kStagingBuf);
   out.lane = lane;
   out.nstore = 0;
+  out.ring = false;
   int it = 0;
   WorkIter work(a.sched, first, stride);
   Unit w;
@@ -463,6 +542,13 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
                                  kRoleEpilogue, kBarAccFull, true);
     if (bar_any(1, 128, !ok)) break;  // all four epilogue warps leave together
     tc_fence_after_sync();
+    if (out.c.tma != kBulkNone && !out.ring) {
+      WorkIter peek = work;
+      Unit next_unit;
+      // This CTA's last unit: its copies have landed and its MMAs (the pair's)
+      // have read the ring for the last time, so the ring can stage C.
+      if (!peek.next(next_unit)) out.use_ring(smem_u32(ring + (warp - 2) * 8 * kStagingBuf));
+    }
     const uint32_t taddr = lane_base + static_cast<uint32_t>(buf * BN);
     // the MMA (leader CTA) waits until every epilogue thread of the pair has read the buffer
     const uint32_t acc_empty_local = smem_u32(&ctrl->acc_empty[buf]);
@@ -548,8 +634,13 @@ template <int BN, int CG, int MC>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p,
                    const __grid_constant__ CUtensorMap map_q,
-                   const __grid_constant__ CUtensorMap map_c, const TcArgs a) {
+                   const __grid_constant__ CUtensorMap map_c, const TcArgs args) {
   using Cfg = TcConfig<BN, CG, MC>;
+  // The roles take the arguments by reference; a local copy whose address never
+  // leaves this kernel lets the compiler keep the fields in registers across
+  // the global stores and "memory"-clobbering asm of the loops, instead of
+  // reloading them from the parameter space after each one.
+  const TcArgs a = args;
   extern __shared__ uint8_t smem_raw[];
   // 128-byte swizzle atoms need 1024-byte aligned tiles.
   const uint32_t raw = smem_u32(smem_raw);
@@ -601,7 +692,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (rank % CG == 0) mma_role<BN, CG, MC>(a, ring_a, ring_b, ctrl, tmem_base, rank, first, stride);
   } else {
-    epilogue_role<BN, CG, MC>(a, &map_c, staging, ctrl, tmem_base, warp, lane, rank, first, stride);
+    epilogue_role<BN, CG, MC>(a, &map_c, staging, ring_a, ctrl, tmem_base, warp, lane, rank, first,
+                              stride);
   }
 
   tc_fence_before_sync();

@@ -20,6 +20,8 @@ PATH_NOOP, PATH_SCALE_C, PATH_TC_1CTA, PATH_TC_2CTA, PATH_TC_2CTA_MULTICAST = 0,
 (OPT_WAIT_LIMIT_NS, OPT_FORCE_PATH, OPT_SPLIT_K, OPT_RASTER_GROUP, OPT_FORCE_BN, OPT_TEST_DROP_LOAD, OPT_MAX_GRID,
  OPT_STREAM_K, OPT_STAGES) = range(9)
 OPT_EPILOGUE = 10
+OPT_KDEPTH = 11
+BULK_NONE, BULK_ROWS, BULK_TRANSPOSED = 0, 1, 2   # gemm_plan_t.bulk_store
 SCHED_TILES, SCHED_STREAM_K = 0, 1
 
 # Exported functions and their (restype, argtypes).
@@ -31,7 +33,8 @@ class Plan(ctypes.Structure):
                                     "split_k", "raster_group", "repack_a", "repack_b", "vector_store",
                                     "grid", "launches", "schedule")] + \
                [(n, _i64) for n in ("tiles", "units", "workspace_bytes")] + \
-               [(n, _i32) for n in ("tiles_i", "tiles_j", "num_kb", "dp_tiles", "sk_slots", "cluster")]
+               [(n, _i32) for n in ("tiles_i", "tiles_j", "num_kb", "dp_tiles", "sk_slots", "cluster", "kdepth",
+                                    "bulk_store")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

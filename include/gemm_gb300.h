@@ -145,8 +145,9 @@ typedef struct {
   int32_t swap_ab;         /* 1: the kernel computes C^T = op(B)^T * op(A)^T */
   int32_t a_kmajor;        /* MMA A operand (rows of the MMA) has K contiguous */
   int32_t b_kmajor;        /* MMA B operand (columns of the MMA) has K contiguous */
-  int32_t bm, bn, bk;      /* output tile (bm x bn; a CTA pair shares bm = 256) and k-block */
-  int32_t stages;          /* shared-memory ring depth */
+  int32_t bm, bn, bk;      /* output tile (bm x bn; a CTA pair shares bm = 256) and the k-block
+                              of one stage: 64 x kdepth */
+  int32_t stages;          /* shared-memory ring depth, in stages of bk */
   int32_t split_k;         /* k-splits per output tile (1 = none) */
   int32_t raster_group;    /* tile rows per raster group */
   int32_t repack_a;        /* A copied to an aligned workspace first */
@@ -161,10 +162,14 @@ typedef struct {
   int32_t tiles_i;         /* schedule tiles along the MMA rows (M, or N when swapped) */
   int32_t tiles_j;         /* schedule tiles along the MMA columns (with multicast a schedule
                               tile is two neighbouring output tiles) */
-  int32_t num_kb;          /* k-blocks per tile */
+  int32_t num_kb;          /* k-blocks of bk per tile */
   int32_t dp_tiles;        /* tiles run whole (stream-K: the complete waves) */
   int32_t sk_slots;        /* stream-K: clusters sharing the remaining tiles' k-blocks */
   int32_t cluster;         /* CTAs per schedule slot: 1, 2 (a pair) or 4 (two pairs, multicast) */
+  int32_t kdepth;          /* 64-wide k-slices per ring stage (1 or 2): each stage's copies
+                              complete one barrier */
+  int32_t bulk_store;      /* how C leaves: 0 direct stores, 1 bulk tensor stores of rows,
+                              2 bulk tensor stores of transposed blocks (swapped problems) */
 } gemm_plan_t;
 
 /*
@@ -194,10 +199,13 @@ typedef enum {
                                   walk more tiles each) */
   GEMM_OPT_STREAM_K = 7,       /* 0 auto, 1 never, 2 always when the last wave is incomplete */
   GEMM_OPT_STAGES = 8,         /* 0 auto (deepest ring that fits), else at most this many stages */
-  GEMM_OPT_EPILOGUE = 10       /* 0 auto: C tiles leave through shared-memory staging and bulk
+  GEMM_OPT_EPILOGUE = 10,      /* 0 auto: C tiles leave through shared-memory staging and bulk
                                   tensor stores when rows start 16-byte aligned, N is a whole
                                   number of 16-byte pieces and beta == 0;
                                   2: always direct stores from registers */
+  GEMM_OPT_KDEPTH = 11         /* 0 auto, else 1 or 2 64-wide k-slices per ring stage (2 halves
+                                  the barrier round trips per byte; falls back to 1 where the
+                                  ring would hold fewer than two stages) */
 } gemm_option_t;
 
 /* Set an option on a handle.  Errors: GEMM_ERR_INVALID_ARG for an unknown

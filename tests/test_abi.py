@@ -122,6 +122,21 @@ def test_plan_compute_bound_keeps_stream_k():
     assert p.schedule == G.SCHED_STREAM_K and p.path == G.PATH_TC_2CTA and p.grid == 152
 
 
+def test_plan_bulk_store_paths():
+    """C leaves through bulk tensor stores of rows, of transposed blocks for a
+    swapped problem, or directly (misaligned rows, a partial 16-byte piece at
+    the right edge, or beta != 0, which reads C)."""
+    assert G.plan(4096, 4096, 4096, 0, 1).bulk_store == G.BULK_ROWS
+    assert G.plan(64, 32000, 4096, 0, 1).bulk_store == G.BULK_TRANSPOSED
+    assert G.plan(64, 32000, 4096, 0, 1, G.BF16_BF16).bulk_store == G.BULK_TRANSPOSED
+    assert G.plan(4096, 4096, 4096, 0, 1, beta=0.5).bulk_store == G.BULK_NONE
+    assert G.plan(64, 32000, 4096, 0, 1, beta=1.0).bulk_store == G.BULK_NONE
+    assert G.plan(512, 1002, 256, 0, 1).bulk_store == G.BULK_NONE          # 4008-byte rows
+    assert G.plan(512, 1004, 256, 0, 1, ldc=1008).bulk_store == G.BULK_ROWS
+    assert G.plan(512, 1004, 256, 0, 1, C=0x1004, ldc=1008).bulk_store == G.BULK_NONE
+    assert G.plan(40, 1001, 256, 0, 1, G.BF16_BF16, ldc=1008).bulk_store == G.BULK_NONE
+
+
 def test_plan_half_atom_pairs_need_k_major_q():
     """A CTA pair with 64-wide tiles loads 32-row halves of the MMA's B operand,
     which only the K-major layout allows."""
@@ -188,11 +203,15 @@ def test_plan_invariants(shape):
         mc = p.cluster // cg
         assert (cg, mc) == {G.PATH_TC_1CTA: (1, 1), G.PATH_TC_2CTA: (2, 1), G.PATH_TC_2CTA_MULTICAST: (2, 2)}[p.path]
         assert p.tiles == -(-I // p.bm) * -(-(-(-J // p.bn)) // mc) == p.tiles_i * p.tiles_j
-        assert p.num_kb == -(-K // 64)
+        assert p.kdepth in (1, 2) and p.bk == 64 * p.kdepth and 2 <= p.stages and p.stages * p.kdepth <= 8
+        assert p.num_kb == -(-K // p.bk)
+        slots = sm // p.cluster
         if p.schedule == G.SCHED_TILES:
             assert p.units == p.tiles * p.split_k and p.dp_tiles == p.tiles
+            waves = -(-p.units // slots)           # the units spread evenly over the waves
+            assert p.grid == -(-p.units // waves) * p.cluster
         else:
             assert p.split_k == 1 and p.dp_tiles % (p.grid // p.cluster) == 0 and p.units >= p.tiles
-        assert 1 <= p.split_k <= max(1, -(-K // 64))
-        assert p.grid == min(p.units, sm // p.cluster) * p.cluster
+            assert p.grid == min(p.units, slots) * p.cluster
+        assert 1 <= p.split_k <= max(1, p.num_kb)
         assert 1 <= p.raster_group <= max(1, -(-I // p.bm))

@@ -11,7 +11,7 @@ import torch
 from dense_gemm_10_gb300 import gemm as G
 from dense_gemm_10_gb300 import inputs
 
-from gpu_util import SENTINEL, assert_close, device_problem, launch, oracle_full, run
+from gpu_util import SENTINEL, assert_close, device_problem, dtype_code, launch, oracle_full, run
 
 pytestmark = pytest.mark.gpu
 
@@ -38,7 +38,7 @@ def skip_half_atom(cg, bn, q_kmajor):
 def options(h, **kw):
     """Force planner options on the handle for the duration of a check."""
     codes = {"path": G.OPT_FORCE_PATH, "bn": G.OPT_FORCE_BN, "split": G.OPT_SPLIT_K, "raster": G.OPT_RASTER_GROUP,
-             "grid": G.OPT_MAX_GRID, "stream_k": G.OPT_STREAM_K}
+             "grid": G.OPT_MAX_GRID, "stream_k": G.OPT_STREAM_K, "kdepth": G.OPT_KDEPTH}
     try:
         for k, v in kw.items():
             h.set_option(codes[k], v)
@@ -87,12 +87,13 @@ def test_ragged_shapes(h, shape):
 
 @pytest.mark.parametrize("cg", [1, 2, 4])
 @pytest.mark.parametrize("transA,transB", [(0, 0), (0, 1), (1, 0), (1, 1)])
-def test_small_integers_bit_exact(h, transA, transB, cg):
+@pytest.mark.parametrize("kdepth", [1, 2])
+def test_small_integers_bit_exact(h, transA, transB, cg, kdepth):
     """Integers in {-4..4}: the fp32 result is exact whatever the order of the
     sum, so the GPU must equal the oracle bit for bit."""
     p = inputs.make_problem("ints", 384, 640, 1024, transA, transB, "bf16", "f32", ("ints", -4, 4), ("ints", -4, 4),
                             alpha=1.5, beta=0.5, dist_c=("ints", -9, 9), seed=5)
-    with options(h, path=PATHS[cg]):
+    with options(h, path=PATHS[cg], kdepth=kdepth):
         out, _ = run(p, h)
     R, _ = oracle_full(p)
     assert np.array_equal(out, R)
@@ -107,30 +108,38 @@ def test_skinny_swapped_split(h, M, N, K):
     _check(p, h)
 
 
+@pytest.mark.parametrize("kdepth", [1, 2])
 @pytest.mark.parametrize("split", [2, 3, 7])
 @pytest.mark.parametrize("cg,bn", CONFIGS)
-def test_forced_split_k(h, split, cg, bn):
+def test_forced_split_k(h, split, cg, bn, kdepth):
+    """K = 960: 15 k-slices of 64, or 8 stages of two (the last holding one)."""
     p = inputs.make_problem("split", 300, 520, 960, 0, 1, "f16", "f32", ("uniform", -1, 1), ("uniform", -1, 1),
                             alpha=-0.75, beta=1.25, seed=split * bn + cg)
-    with options(h, path=PATHS[cg], bn=bn, split=split):
+    with options(h, path=PATHS[cg], bn=bn, split=split, kdepth=kdepth):
         plan = G.plan(p.M, p.N, p.K, 0, 1, G.F16_F32, handle=h, beta=p.beta)
         assert plan.split_k == split and plan.bn == bn and plan.path == PATHS[cg]
+        assert plan.kdepth == kdepth and plan.num_kb == -(-15 // kdepth)
         _check(p, h)
 
 
+@pytest.mark.parametrize("kdepth", [1, 2])
 @pytest.mark.parametrize("cg,bn", CONFIGS)
 @pytest.mark.parametrize("transA,transB", [(0, 0), (1, 1), (0, 1), (1, 0)])
-def test_every_tile_configuration(h, cg, bn, transA, transB):
+def test_every_tile_configuration(h, cg, bn, transA, transB, kdepth):
+    """K = 300: five k-slices, the last one partial; with two slices per stage the
+    last stage holds that partial slice alone."""
     skip_half_atom(cg, bn, transB == 1)
-    p = inputs.make_problem("cfg", 600, 900, 320, transA, transB, "bf16", "bf16", ("normal", 0, 1), ("normal", 0, 1),
+    p = inputs.make_problem("cfg", 600, 900, 300, transA, transB, "bf16", "bf16", ("normal", 0, 1), ("normal", 0, 1),
                             alpha=0.5, beta=-1.0, seed=bn + transA + 2 * transB + 7 * cg)
-    with options(h, path=PATHS[cg], bn=bn):
+    with options(h, path=PATHS[cg], bn=bn, kdepth=kdepth):
+        assert G.plan(p.M, p.N, p.K, transA, transB, G.BF16_BF16, handle=h, beta=p.beta).kdepth == kdepth
         _check(p, h)
 
 
+@pytest.mark.parametrize("kdepth", [1, 2])
 @pytest.mark.parametrize("gi", [0, 1, 2])
 @pytest.mark.parametrize("cg,bn", CONFIGS)
-def test_stream_k(h, cg, bn, gi):
+def test_stream_k(h, cg, bn, gi, kdepth):
     """Stream-K tail forced on small grids: tiles cut into several pieces whose
     partials are summed by the last piece to finish.  The grids leave an
     incomplete last wave for every configuration (90, 48, 24, 24, 12 and 6 schedule tiles)."""
@@ -139,19 +148,22 @@ def test_stream_k(h, cg, bn, gi):
         grid = (8, 12, 16)[gi]   # 3 x 15 = 45 tiles: 45 % 4, 45 % 6, 45 % 8 all non-zero
     p = inputs.make_problem("sk", 700, 900, 1000, 0, 1, "bf16", "f32", ("normal", 0, 1), ("normal", 0, 1),
                             alpha=1.25, beta=-0.5, seed=grid + bn + cg)
-    with options(h, path=PATHS[cg], bn=bn, grid=grid, stream_k=2):
+    with options(h, path=PATHS[cg], bn=bn, grid=grid, stream_k=2, kdepth=kdepth):
         plan = G.plan(p.M, p.N, p.K, 0, 1, handle=h, beta=p.beta)
         assert plan.schedule == G.SCHED_STREAM_K and plan.path == PATHS[cg] and plan.grid <= grid
+        assert plan.kdepth == kdepth
         _check(p, h)
 
 
+@pytest.mark.parametrize("kdepth", [1, 2])
 @pytest.mark.parametrize("cg,bn", CONFIGS)
-def test_stream_k_all_tiles_shared(h, cg, bn):
+def test_stream_k_all_tiles_shared(h, cg, bn, kdepth):
+    """Fewer tiles than CTAs and a deep K (63 k-slices, the last partial): no
+    whole tiles, every tile is shared."""
     skip_half_atom(cg, bn, False)
-    """Fewer tiles than CTAs and a deep K: no whole tiles, every tile is shared."""
     p = inputs.make_problem("skdeep", 250, 250, 4000, 1, 0, "f16", "f16", ("uniform", -1, 1), ("uniform", -1, 1),
                             seed=bn * cg)
-    with options(h, path=PATHS[cg], bn=bn, stream_k=2):
+    with options(h, path=PATHS[cg], bn=bn, stream_k=2, kdepth=kdepth):
         plan = G.plan(p.M, p.N, p.K, 1, 0, G.F16_F16, handle=h)
         assert plan.schedule == G.SCHED_STREAM_K and plan.dp_tiles == 0
         _check(p, h)
@@ -166,6 +178,68 @@ def test_many_tiles_per_cta(h, cg, bn):
         plan = G.plan(p.M, p.N, p.K, 0, 1, handle=h)
         assert plan.grid <= 6 and plan.units >= 3 * plan.grid // cg
         _check(p, h)
+
+
+def _check_bulk(p, h, expect_bulk):
+    """Like _check, with 8 guard columns, which keep C's rows 16-byte aligned so
+    that the epilogue can use bulk tensor stores; the guard region must survive
+    the clipped edge boxes."""
+    plan = G.plan(p.M, p.N, p.K, p.transA, p.transB, dtype_code(p), handle=h, ldc=p.ldc + 8, beta=p.beta)
+    assert plan.bulk_store == expect_bulk, plan.as_dict()
+    out, full = run(p, h, guard_rows=3, guard_cols=8)
+    R, Mag = oracle_full(p)
+    assert_close(out, R, Mag, p.out_dtype == "f32", p.name)
+    pad = full.clone().to(torch.float64)
+    pad[:p.M, :p.N] = SENTINEL
+    assert torch.all(pad == SENTINEL), "C written outside the M x N block"
+
+
+OUT_TYPES = [("bf16", "f32"), ("bf16", "bf16"), ("f16", "f16")]
+
+
+@pytest.mark.parametrize("in_dtype,out_dtype", OUT_TYPES)
+@pytest.mark.parametrize("grid", [0, 6])
+@pytest.mark.parametrize("cg,bn", CONFIGS)
+def test_bulk_store_rows(h, cg, bn, grid, in_dtype, out_dtype):
+    """Staged bulk tensor stores of C rows, ragged in M and N (N = 904 keeps
+    whole 16-byte pieces).  grid = 6: each CTA stores several tiles through its
+    two staging buffers and its last one through the idle operand ring."""
+    p = inputs.make_problem("bulk", 600, 904, 300, 0, 1, in_dtype, out_dtype, ("normal", 0, 1), ("normal", 0, 1),
+                            alpha=0.75, seed=bn + cg + grid)
+    with options(h, path=PATHS[cg], bn=bn, grid=grid, stream_k=1):
+        _check_bulk(p, h, G.BULK_ROWS)
+
+
+@pytest.mark.parametrize("in_dtype,out_dtype", OUT_TYPES)
+@pytest.mark.parametrize("M,N,K", [(64, 2000, 1000), (40, 1000, 700), (1, 1032, 256), (64, 904, 130)])
+def test_bulk_store_transposed(h, M, N, K, in_dtype, out_dtype):
+    """Swapped problems (short M): C is stored J x I from the kernel's point of
+    view, and each warp writes its 32 x 32 block transposed into staging."""
+    p = inputs.make_problem("bulkT", M, N, K, 0, 1, in_dtype, out_dtype, ("normal", 0, 1), ("normal", 0, 0.5),
+                            alpha=1.5, seed=M + N)
+    _check_bulk(p, h, G.BULK_TRANSPOSED)
+
+
+@pytest.mark.parametrize("grid", [0, 7])
+@pytest.mark.parametrize("cg,bn", [(1, 64), (1, 128), (1, 256), (2, 64), (2, 128), (2, 256)])
+def test_bulk_store_transposed_configs(h, cg, bn, grid):
+    """Every configuration a swapped problem can take, forced, on full and small grids."""
+    p = inputs.make_problem("bulkTc", 48, 3000, 520, 0, 1, "bf16", "f32", ("normal", 0, 1), ("normal", 0, 1),
+                            seed=bn * cg + grid)
+    with options(h, path=PATHS[cg], bn=bn, grid=grid, stream_k=1):
+        _check_bulk(p, h, G.BULK_TRANSPOSED)
+
+
+@pytest.mark.parametrize("kdepth", [1, 2])
+@pytest.mark.parametrize("cg,bn", CONFIGS)
+def test_bulk_store_after_stream_k(h, cg, bn, kdepth):
+    """Stream-K fix-ups leave through bulk stores as well (the last arriving
+    piece sums the partials and stores the tile)."""
+    grid = {1: 13, 2: 14, 4: 20}[cg] if (cg, bn) != (2, 64) else 12
+    p = inputs.make_problem("bulksk", 700, 904, 1000, 0, 1, "bf16", "f32", ("normal", 0, 1), ("normal", 0, 1),
+                            seed=grid + bn + cg)
+    with options(h, path=PATHS[cg], bn=bn, grid=grid, stream_k=2, kdepth=kdepth):
+        _check_bulk(p, h, G.BULK_ROWS)
 
 
 def test_misaligned_leading_dimensions(h):
