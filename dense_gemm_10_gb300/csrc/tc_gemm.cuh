@@ -325,9 +325,11 @@ struct EpiOut {
     if (wide || half == 1) issue(buf, wide ? j : j - 32, y0);
   }
 
+  // Before the CTA exits, every bulk store must have read its staging buffer;
+  // the global writes complete with the grid, like any other store.
   __device__ __forceinline__ void finish() {
     if (c.tma != kBulkNone) {
-      if (lane == 0) bulk_wait_group_all();
+      if (lane == 0) bulk_wait_group_read<0>();
       __syncwarp();
     }
   }
@@ -627,7 +629,7 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
       }
     }
   }
-  out.finish();  // every bulk store of C has completed before the CTA can exit
+  out.finish();  // every bulk store has read its staging buffer before the CTA can exit
 }
 
 template <int BN, int CG, int MC>
