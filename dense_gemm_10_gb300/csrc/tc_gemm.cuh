@@ -337,7 +337,7 @@ struct EpiOut {
 
 // ----------------------------------------------------------------- the roles --
 
-template <int BN, int CG, int MC>
+template <int BN, int CG, int MC, int KD>
 __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CUtensorMap* map_q,
                                               const TcArgs& a, uint8_t* ring_a, uint8_t* ring_b,
                                               TcCtrl* ctrl, uint32_t rank, int first, int stride) {
@@ -347,6 +347,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
   const uint32_t leader = static_cast<uint32_t>(pair * CG);
   // multicast of P: this CTA and the CTA of the other pair with the same rank inside its pair
   const uint16_t p_mask = static_cast<uint16_t>((1u << q) | (1u << (q + CG)));
+  const int kslices = (a.K + kBK - 1) / kBK;
   int stage = 0;
   uint32_t phase = 0;
   uint32_t pending = 0, pending_parity = 0;  // copies in flight, per stage
@@ -371,8 +372,8 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
         pending &= ~(1u << stage);  // test hook: this stage's barrier is never completed
       } else {
         // k-slices of this stage inside K (a ragged K leaves fewer in the last stage)
-        const int ks0 = kb * a.kdepth;
-        const int nks = min(a.kdepth, (a.K + kBK - 1) / kBK - ks0);
+        const int ks0 = kb * KD;
+        const int nks = KD == 1 ? 1 : min(KD, kslices - ks0);
         if (elect_one()) {
           if (q == 0) mbar_arrive_expect_tx(full_local, CG * nks * Cfg::kStageBytes);
           auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
@@ -384,8 +385,10 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
           auto load_mc = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
             tma_load_2d_pair_multicast(dst, map, full, x, y, p_mask);
           };
-          for (int t = 0; t < nks; ++t) {
-            const int slot = stage * a.kdepth + t;  // ring slot of one k-slice
+#pragma unroll
+          for (int t = 0; t < KD; ++t) {
+            if (t == nks) break;
+            const int slot = stage * KD + t;  // ring slot of one k-slice
             const uint32_t sa = smem_u32(ring_a + slot * Cfg::kABytes);
             const uint32_t sb = smem_u32(ring_b + slot * Cfg::kBBytes);
             const int k0 = (ks0 + t) * kBK;
@@ -432,11 +435,12 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
   __syncwarp();
 }
 
-template <int BN, int CG, int MC>
+template <int BN, int CG, int MC, int KD>
 __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8_t* ring_b,
                                          TcCtrl* ctrl, uint32_t tmem_base, uint32_t rank, int first,
                                          int stride) {
   using Cfg = TcConfig<BN, CG, MC>;
+  const int kslices = (a.K + kBK - 1) / kBK;
   int stage = 0;
   uint32_t phase = 0;
   int it = 0;
@@ -473,8 +477,8 @@ __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8
         break;
       }
       tc_fence_after_sync();
-      const int ks0 = kb * a.kdepth;
-      const int nks = min(a.kdepth, (a.K + kBK - 1) / kBK - ks0);
+      const int ks0 = kb * KD;
+      const int nks = KD == 1 ? 1 : min(KD, kslices - ks0);
       // K-major: the 16-wide k-slice starts 32 bytes further along each swizzled
       // 128-byte row; 8-row groups are 1024 bytes apart.
       // MN-major: the k-slice is 16 rows of 128 bytes further on; 8-row groups are
@@ -482,8 +486,10 @@ __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8
       const uint32_t a_step = a.p_kmajor ? 32u : 2048u;
       const uint32_t b_step = a.q_kmajor ? 32u : 2048u;
       if (elect_one()) {
-        for (int t = 0; t < nks; ++t) {
-          const int slot = stage * a.kdepth + t;
+#pragma unroll
+        for (int t = 0; t < KD; ++t) {
+          if (t == nks) break;
+          const int slot = stage * KD + t;
           const uint64_t ad0 =
               smem_desc_sw128(smem_u32(ring_a + slot * Cfg::kABytes), a.p_kmajor ? 16u : kMnAtomBytes, 1024);
           const uint64_t bd0 =
@@ -690,9 +696,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = ctrl->tmem_base;
 
   if (warp == 0) {
-    producer_role<BN, CG, MC>(&map_p, &map_q, a, ring_a, ring_b, ctrl, rank, first, stride);
+    // k-slices per stage are a template argument of the issuing roles, so that
+    // the one-slice loop compiles to the same straight-line issue code as
+    // before two-slice stages existed (a runtime trip count cost ~12% at 4096^3)
+    if (a.kdepth == 2)
+      producer_role<BN, CG, MC, 2>(&map_p, &map_q, a, ring_a, ring_b, ctrl, rank, first, stride);
+    else
+      producer_role<BN, CG, MC, 1>(&map_p, &map_q, a, ring_a, ring_b, ctrl, rank, first, stride);
   } else if (warp == 1) {
-    if (rank % CG == 0) mma_role<BN, CG, MC>(a, ring_a, ring_b, ctrl, tmem_base, rank, first, stride);
+    if (rank % CG == 0) {
+      if (a.kdepth == 2)
+        mma_role<BN, CG, MC, 2>(a, ring_a, ring_b, ctrl, tmem_base, rank, first, stride);
+      else
+        mma_role<BN, CG, MC, 1>(a, ring_a, ring_b, ctrl, tmem_base, rank, first, stride);
+    }
   } else {
     epilogue_role<BN, CG, MC>(a, &map_c, staging, ring_a, ctrl, tmem_base, warp, lane, rank, first,
                               stride);
