@@ -400,7 +400,9 @@ def run_skinny(args, G, h, inputs, metrics, dev, stream, pk, pk_src):
             "tflops": metrics.flops(p.M, p.N, p.K) / (ms / 1e3) / 1e12,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                          "frac_of_8000": gbs / 8000.0, "peak_source": "%s hbm_gbs (copy)" % pk_src,
-                         "algorithmic_bytes_per_launch": nbytes},
+                         "algorithmic_bytes_per_launch": nbytes,
+                         "traffic": recorded_traffic("tc_gemm_kernel<%d,%d>:lm_head_64x32000x4096_nt_f32"
+                                                     % (plan.bn, plan.bm // 128))},
             "plan": plan.as_dict(), "l2": "2 weight copies of 262 MB alternate"}
 
 
