@@ -8,7 +8,9 @@ Recipe (one rule for every workload):
   * a workload has one integer seed s; A is drawn from seed s, B from s + 1,
     the initial C from s + 2 (numpy PCG64 streams);
   * samples are drawn in float32 (uniform or normal), then rounded once to the
-    input type with round-to-nearest-even (torch ``.to(bfloat16/float16)``);
+    input type with round-to-nearest-even (torch ``.to(...)``: bfloat16,
+    float16, or the 8-bit float8_e4m3fn / float8_e5m2; the distributions used
+    stay inside the 8-bit formats' ranges);
   * a matrix is drawn directly in its stored shape (row-major storage, see
     ``Problem``), so the "op" flags change the layout, not the distribution;
   * padding columns beyond a leading dimension hold a NaN bit pattern, so a
@@ -20,8 +22,11 @@ import math
 import numpy as np
 import torch
 
-_TORCH_DT = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+_TORCH_DT = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32,
+             "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
 _NAN_BITS = {"bf16": 0x7FC1, "f16": 0x7E01}
+_NAN_BITS8 = {"e4m3": 0x7F, "e5m2": 0x7F}
+FP8 = ("e4m3", "e5m2")
 
 
 def _rng(seed):
@@ -29,7 +34,7 @@ def _rng(seed):
 
 
 def draw(shape, dist, seed, dtype):
-    """Draw a CPU tensor of ``dtype`` ("bf16", "f16", "f32") in ``shape``.
+    """Draw a CPU tensor of ``dtype`` ("bf16", "f16", "f32", "e4m3", "e5m2") in ``shape``.
 
     dist: ("uniform", lo, hi) | ("normal", mean, std) | ("ints", lo, hi)
     (integers uniform in [lo, hi], inclusive) | ("zeros",).
@@ -57,6 +62,8 @@ def _pad_columns(t, ld, dtype):
     out = torch.empty((rows, ld), dtype=t.dtype)
     if dtype in _NAN_BITS:
         out.view(torch.int16).fill_(_NAN_BITS[dtype])
+    elif dtype in _NAN_BITS8:
+        out.view(torch.uint8).fill_(_NAN_BITS8[dtype])
     else:
         out.fill_(float("nan"))
     out[:, :cols] = t
@@ -70,6 +77,7 @@ class Problem:
     transA 0: A stored M x K (lda >= K); 1: A stored K x M (lda >= M).
     transB 0: B stored K x N (ldb >= N); 1: B stored N x K (ldb >= K).
     C0 is M x N with ldc >= N, in the output type; None when beta == 0.
+    A has type in_dtype, B has b_dtype (the same unless a mixed 8-bit pair).
     """
     name: str
     M: int
@@ -89,6 +97,11 @@ class Problem:
     ldc: int
     seed: int
     recipe: dict = field(default_factory=dict)
+    b_dtype: str = None
+
+    def __post_init__(self):
+        if self.b_dtype is None:
+            self.b_dtype = self.in_dtype
 
     @property
     def layout(self):
@@ -97,7 +110,8 @@ class Problem:
 
 def make_problem(name, M, N, K, transA=0, transB=0, in_dtype="bf16", out_dtype="f32",
                  dist_a=("uniform", -1.0, 1.0), dist_b=("uniform", -1.0, 1.0), alpha=1.0,
-                 beta=0.0, dist_c=("normal", 0.0, 1.0), seed=0, lda=None, ldb=None, ldc=None):
+                 beta=0.0, dist_c=("normal", 0.0, 1.0), seed=0, lda=None, ldb=None, ldc=None, b_dtype=None):
+    b_dtype = in_dtype if b_dtype is None else b_dtype
     a_shape = (K, M) if transA else (M, K)
     b_shape = (N, K) if transB else (K, N)
     lda = a_shape[1] if lda is None else lda
@@ -106,14 +120,14 @@ def make_problem(name, M, N, K, transA=0, transB=0, in_dtype="bf16", out_dtype="
     if lda < a_shape[1] or ldb < b_shape[1] or ldc < N:
         raise ValueError("leading dimension smaller than the stored width")
     A = _pad_columns(draw(a_shape, dist_a, seed, in_dtype), lda, in_dtype)
-    B = _pad_columns(draw(b_shape, dist_b, seed + 1, in_dtype), ldb, in_dtype)
+    B = _pad_columns(draw(b_shape, dist_b, seed + 1, b_dtype), ldb, b_dtype)
     C0 = None
     if beta != 0.0:
         C0 = _pad_columns(draw((M, N), dist_c, seed + 2, out_dtype), ldc, out_dtype)
     recipe = {"dist_a": list(dist_a), "dist_b": list(dist_b), "dist_c": list(dist_c) if beta else None,
               "seeds": [seed, seed + 1, seed + 2]}
     return Problem(name, M, N, K, transA, transB, in_dtype, out_dtype, float(alpha), float(beta),
-                   A, lda, B, ldb, C0, ldc, seed, recipe)
+                   A, lda, B, ldb, C0, ldc, seed, recipe, b_dtype)
 
 
 # ---------------------------------------------------------------------------
@@ -169,6 +183,16 @@ def lm_head_64():
                         ("normal", 0.0, 1.0), ("normal", 0.0, 0.02))
 
 
+def square_4096_fp8_nt(fmt="e4m3", out_dtype="f32", size=4096):
+    """M = N = K = 4096, A row-major, B column-major (NT), 8-bit float inputs
+    N(0, 1) (inside both formats' ranges), alpha 1 / K so that C is O(1)."""
+    return make_problem("square_%d_%s_nt_%s" % (size, fmt, out_dtype), size, size, size, 0, 1, fmt,
+                        out_dtype, ("normal", 0.0, 1.0), ("normal", 0.0, 1.0), alpha=1.0 / size)
+
+
 def bits(t):
-    """Raw 16-bit patterns of a bf16 / fp16 tensor as a numpy uint16 array (no copy of values)."""
+    """Raw bit patterns of an input tensor, without copying values: numpy
+    uint16 for bf16 / fp16, uint8 for the 8-bit formats."""
+    if t.element_size() == 1:
+        return t.contiguous().view(torch.uint8).numpy()
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)

@@ -6,8 +6,9 @@ two share no code: the oracle is a plain fp64 triple loop in ``gemm_oracle.c``
 (the definition of "CUDA GEMM 矩阵乘法优化指南", section 2.1, checked in double
 precision as the page at m.lqnn.cn/news/285670 does in its section 1.2).
 
-Inputs are the raw 16-bit patterns (numpy ``uint16``) of the bf16 / fp16
-matrices, in the row-major storage convention described in ``gemm_oracle.c``.
+Inputs are the raw bit patterns of the matrices, in the row-major storage
+convention described in ``gemm_oracle.c``: numpy ``uint16`` for bf16 / fp16,
+``uint8`` for the 8-bit E4M3 / E5M2 formats.
 Every function here is pinned by ``tests/test_oracle.py``.
 """
 import ctypes
@@ -20,7 +21,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gemm_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle_gemm.so")
 
-IN_BF16, IN_F16 = 0, 1
+IN_BF16, IN_F16, IN_E4M3, IN_E5M2 = 0, 1, 2, 3
 C_F32, C_BF16, C_F16 = 0, 1, 2
 
 _lib = None
@@ -48,16 +49,20 @@ def _load():
     path = os.environ.get("ORACLE_LIB") or build()
     lib = ctypes.CDLL(path)
     i64, dbl, vp, i32 = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
-    lib.oracle_gemm.restype = i32
-    lib.oracle_gemm.argtypes = [i32, i32, i64, i64, i64, dbl, vp, i64, vp, i64, dbl, vp, i32, i64,
-                                i32, vp, vp, i64, i32]
-    lib.oracle_gemm_at.restype = i32
-    lib.oracle_gemm_at.argtypes = [i32, i32, i64, i64, i64, dbl, vp, i64, vp, i64, dbl, vp, i32,
-                                   i64, i32, i64, vp, vp, vp, vp, i32]
+    lib.oracle_gemm_ab.restype = i32
+    lib.oracle_gemm_ab.argtypes = [i32, i32, i64, i64, i64, dbl, vp, i64, vp, i64, dbl, vp, i32, i64,
+                                   i32, i32, vp, vp, i64, i32]
+    lib.oracle_gemm_at_ab.restype = i32
+    lib.oracle_gemm_at_ab.argtypes = [i32, i32, i64, i64, i64, dbl, vp, i64, vp, i64, dbl, vp, i32,
+                                      i64, i32, i32, i64, vp, vp, vp, vp, i32]
     lib.oracle_bf16_value.restype = dbl
     lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
     lib.oracle_f16_value.restype = dbl
     lib.oracle_f16_value.argtypes = [ctypes.c_uint16]
+    lib.oracle_e4m3_value.restype = dbl
+    lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+    lib.oracle_e5m2_value.restype = dbl
+    lib.oracle_e5m2_value.argtypes = [ctypes.c_uint8]
     _lib = lib
     return lib
 
@@ -70,6 +75,25 @@ def bf16_value(bits):
 def f16_value(bits):
     """Value of one IEEE binary16 bit pattern, decoded from the format definition."""
     return _load().oracle_f16_value(int(bits) & 0xFFFF)
+
+
+def e4m3_value(bits):
+    """Value of one FP8 E4M3 bit pattern, decoded from the format definition."""
+    return _load().oracle_e4m3_value(int(bits) & 0xFF)
+
+
+def e5m2_value(bits):
+    """Value of one FP8 E5M2 bit pattern, decoded from the format definition."""
+    return _load().oracle_e5m2_value(int(bits) & 0xFF)
+
+
+def _codes(X, in_type):
+    """The stored matrix as an array of codes of the type's width."""
+    want = np.uint8 if in_type in (IN_E4M3, IN_E5M2) else np.uint16
+    X = np.ascontiguousarray(X)
+    if X.dtype != want:
+        raise TypeError("input of type %d must be %s codes" % (in_type, want.__name__))
+    return X
 
 
 def _ptr(a):
@@ -87,33 +111,36 @@ def _c0_array(C0, c_type):
 
 
 def gemm(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc, in_type, c_type=C_F32,
-         nthreads=0):
+         nthreads=0, b_type=None):
     """Full oracle.  Returns (R, Mag): fp64 M x N arrays of r_ij and m_ij.
 
-    A, B: uint16 arrays holding the stored matrices (row-major, leading
-    dimensions lda / ldb).  C0: float32 (c_type C_F32) or uint16 bits, M x N
-    with leading dimension ldc; ignored when beta == 0.
+    A, B: code arrays holding the stored matrices (row-major, leading
+    dimensions lda / ldb); A has type in_type, B has b_type (default: the
+    same).  C0: float32 (c_type C_F32) or uint16 bits, M x N with leading
+    dimension ldc; ignored when beta == 0.
     """
     lib = _load()
-    A = np.ascontiguousarray(A, dtype=np.uint16)
-    B = np.ascontiguousarray(B, dtype=np.uint16)
+    b_type = in_type if b_type is None else b_type
+    A = _codes(A, in_type)
+    B = _codes(B, b_type)
     C0 = _c0_array(C0, c_type) if beta != 0.0 else None
     R = np.zeros((M, N), dtype=np.float64)
     Mag = np.zeros((M, N), dtype=np.float64)
-    rc = lib.oracle_gemm(int(transA), int(transB), M, N, K, float(alpha), _ptr(A), lda, _ptr(B),
-                         ldb, float(beta), _ptr(C0), int(c_type), ldc, int(in_type), _ptr(R),
-                         _ptr(Mag), N, int(nthreads))
+    rc = lib.oracle_gemm_ab(int(transA), int(transB), M, N, K, float(alpha), _ptr(A), lda, _ptr(B),
+                            ldb, float(beta), _ptr(C0), int(c_type), ldc, int(in_type), int(b_type),
+                            _ptr(R), _ptr(Mag), N, int(nthreads))
     if rc < 0:
         raise ValueError("oracle_gemm rejected its arguments")
     return R, Mag
 
 
 def gemm_at(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc, in_type, rows, cols,
-            c_type=C_F32, nthreads=0):
+            c_type=C_F32, nthreads=0, b_type=None):
     """Sampled oracle: r and m at the listed (rows[e], cols[e]) entries."""
     lib = _load()
-    A = np.ascontiguousarray(A, dtype=np.uint16)
-    B = np.ascontiguousarray(B, dtype=np.uint16)
+    b_type = in_type if b_type is None else b_type
+    A = _codes(A, in_type)
+    B = _codes(B, b_type)
     C0 = _c0_array(C0, c_type) if beta != 0.0 else None
     rows = np.ascontiguousarray(rows, dtype=np.int64)
     cols = np.ascontiguousarray(cols, dtype=np.int64)
@@ -121,9 +148,9 @@ def gemm_at(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc, in_ty
         raise ValueError("rows and cols differ in length")
     r = np.zeros(rows.shape, dtype=np.float64)
     m = np.zeros(rows.shape, dtype=np.float64)
-    rc = lib.oracle_gemm_at(int(transA), int(transB), M, N, K, float(alpha), _ptr(A), lda, _ptr(B),
-                            ldb, float(beta), _ptr(C0), int(c_type), ldc, int(in_type),
-                            rows.size, _ptr(rows), _ptr(cols), _ptr(r), _ptr(m), int(nthreads))
+    rc = lib.oracle_gemm_at_ab(int(transA), int(transB), M, N, K, float(alpha), _ptr(A), lda, _ptr(B),
+                               ldb, float(beta), _ptr(C0), int(c_type), ldc, int(in_type), int(b_type),
+                               rows.size, _ptr(rows), _ptr(cols), _ptr(r), _ptr(m), int(nthreads))
     if rc < 0:
         raise ValueError("oracle_gemm_at rejected its arguments")
     return r, m

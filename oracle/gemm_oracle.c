@@ -27,9 +27,16 @@
  *   transB == 1: B is stored N x K, b(k, j) = B[j * ldb + k]
  *   C0 / R / Mag are M x N row-major with leading dimensions ldc / ldr.
  *
- * The 16-bit inputs are decoded from their format definitions (IEEE 754
- * binary16; bfloat16 = sign, 8-bit exponent with bias 127, 7-bit fraction).
- * Every bf16/fp16 value is exactly representable in fp64, and so is every
+ * The inputs are decoded from their format definitions: IEEE 754 binary16;
+ * bfloat16 = sign, 8-bit exponent with bias 127, 7-bit fraction; and the two
+ * 8-bit formats the tensor core takes ("CUDA GEMM 矩阵乘法优化指南", 13.2:
+ * FP8 E4M3 / E5M2; their bit layouts are the usual OCP 8-bit ones):
+ *   E4M3: sign, 4-bit exponent with bias 7, 3-bit fraction; no infinities,
+ *         exponent 1111 with fraction 111 is NaN, so the largest value is 448;
+ *   E5M2: sign, 5-bit exponent with bias 15, 2-bit fraction, with IEEE-style
+ *         infinities and NaNs.
+ * A and B may have different types (an E4M3 x E5M2 product is allowed).
+ * Every such value is exactly representable in fp64, and so is every
  * product of two of them (at most 22 significant bits), so the only rounding
  * in s_ij is that of the fp64 additions.
  *
@@ -41,7 +48,7 @@
 #include <stdlib.h>
 #include <unistd.h>
 
-enum { ORACLE_IN_BF16 = 0, ORACLE_IN_F16 = 1 };
+enum { ORACLE_IN_BF16 = 0, ORACLE_IN_F16 = 1, ORACLE_IN_E4M3 = 2, ORACLE_IN_E5M2 = 3 };
 enum { ORACLE_C_F32 = 0, ORACLE_C_BF16 = 1, ORACLE_C_F16 = 2 };
 
 /* bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits. */
@@ -76,8 +83,46 @@ double oracle_f16_value(uint16_t h) {
   return sign ? -v : v;
 }
 
-static double in_value(int in_type, uint16_t h) {
-  return in_type == ORACLE_IN_F16 ? oracle_f16_value(h) : oracle_bf16_value(h);
+/* FP8 E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits; S.1111.111 is NaN. */
+double oracle_e4m3_value(uint8_t b) {
+  int sign = (b >> 7) & 1;
+  int e = (b >> 3) & 0xF;
+  int f = b & 0x7;
+  double v;
+  if (e == 0xF && f == 0x7) {
+    v = NAN;
+  } else if (e == 0) {
+    v = ldexp((double)f / 8.0, -6); /* subnormal: 0.f * 2^(1-7) */
+  } else {
+    v = ldexp(1.0 + (double)f / 8.0, e - 7);
+  }
+  return sign ? -v : v;
+}
+
+/* FP8 E5M2: 1 sign bit, 5 exponent bits (bias 15), 2 fraction bits, IEEE-style specials. */
+double oracle_e5m2_value(uint8_t b) {
+  int sign = (b >> 7) & 1;
+  int e = (b >> 2) & 0x1F;
+  int f = b & 0x3;
+  double v;
+  if (e == 0x1F) {
+    v = (f == 0) ? INFINITY : NAN;
+  } else if (e == 0) {
+    v = ldexp((double)f / 4.0, -14); /* subnormal: 0.f * 2^(1-15) */
+  } else {
+    v = ldexp(1.0 + (double)f / 4.0, e - 15);
+  }
+  return sign ? -v : v;
+}
+
+/* Element idx of a stored matrix of the given input type. */
+static double in_value(int in_type, const void* base, int64_t idx) {
+  switch (in_type) {
+    case ORACLE_IN_F16: return oracle_f16_value(((const uint16_t*)base)[idx]);
+    case ORACLE_IN_E4M3: return oracle_e4m3_value(((const uint8_t*)base)[idx]);
+    case ORACLE_IN_E5M2: return oracle_e5m2_value(((const uint8_t*)base)[idx]);
+    default: return oracle_bf16_value(((const uint16_t*)base)[idx]);
+  }
 }
 
 static double c0_value(int c_type, const void* C0, int64_t idx) {
@@ -87,11 +132,11 @@ static double c0_value(int c_type, const void* C0, int64_t idx) {
 }
 
 typedef struct {
-  int transA, transB, in_type, c_type;
+  int transA, transB, a_type, b_type, c_type;
   int64_t M, N, K, lda, ldb, ldc, ldr;
   double alpha, beta;
-  const uint16_t* A;
-  const uint16_t* B;
+  const void* A;
+  const void* B;
   const void* C0;
   /* full mode: rows [row0, row1) of R / Mag */
   double* R;
@@ -107,9 +152,9 @@ typedef struct {
 static void element(const job_t* J, int64_t i, int64_t j, double* r, double* m) {
   double s = 0.0, sa = 0.0;
   for (int64_t k = 0; k < J->K; ++k) {
-    uint16_t ha = J->transA ? J->A[k * J->lda + i] : J->A[i * J->lda + k];
-    uint16_t hb = J->transB ? J->B[j * J->ldb + k] : J->B[k * J->ldb + j];
-    double p = in_value(J->in_type, ha) * in_value(J->in_type, hb);
+    double a = in_value(J->a_type, J->A, J->transA ? k * J->lda + i : i * J->lda + k);
+    double b = in_value(J->b_type, J->B, J->transB ? j * J->ldb + k : k * J->ldb + j);
+    double p = a * b;
     s += p;
     sa += fabs(p);
   }
@@ -162,10 +207,11 @@ static int run_jobs(job_t* jobs, int nthreads, void* (*fn)(void*)) {
 }
 
 static int check_args(int transA, int transB, int64_t M, int64_t N, int64_t K, int64_t lda,
-                      int64_t ldb, int in_type, int c_type) {
+                      int64_t ldb, int a_type, int b_type, int c_type) {
   if (M < 0 || N < 0 || K < 0) return -1;
   if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1)) return -1;
-  if (in_type != ORACLE_IN_BF16 && in_type != ORACLE_IN_F16) return -1;
+  if (a_type < ORACLE_IN_BF16 || a_type > ORACLE_IN_E5M2) return -1;
+  if (b_type < ORACLE_IN_BF16 || b_type > ORACLE_IN_E5M2) return -1;
   if (c_type != ORACLE_C_F32 && c_type != ORACLE_C_BF16 && c_type != ORACLE_C_F16) return -1;
   if (lda < (transA ? M : K) || ldb < (transB ? K : N)) return -1;
   return 0;
@@ -173,14 +219,15 @@ static int check_args(int transA, int transB, int64_t M, int64_t N, int64_t K, i
 
 /*
  * Full oracle: R and Mag (M x N, leading dimension ldr) receive r_ij and m_ij.
- * nthreads <= 0 uses every online core.  Returns the number of threads used,
- * or -1 on a bad argument.
+ * A holds elements of a_type, B of b_type (2-byte codes for bf16 / fp16,
+ * 1-byte codes for E4M3 / E5M2).  nthreads <= 0 uses every online core.
+ * Returns the number of threads used, or -1 on a bad argument.
  */
-int oracle_gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, double alpha,
-                const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb, double beta,
-                const void* C0, int c_type, int64_t ldc, int in_type, double* R, double* Mag,
-                int64_t ldr, int nthreads) {
-  if (check_args(transA, transB, M, N, K, lda, ldb, in_type, c_type) != 0) return -1;
+int oracle_gemm_ab(int transA, int transB, int64_t M, int64_t N, int64_t K, double alpha,
+                   const void* A, int64_t lda, const void* B, int64_t ldb, double beta,
+                   const void* C0, int c_type, int64_t ldc, int a_type, int b_type, double* R,
+                   double* Mag, int64_t ldr, int nthreads) {
+  if (check_args(transA, transB, M, N, K, lda, ldb, a_type, b_type, c_type) != 0) return -1;
   if (ldr < N || (beta != 0.0 && ldc < N)) return -1;
   if (M == 0 || N == 0) return 0;
   nthreads = pick_threads(nthreads, M);
@@ -188,7 +235,8 @@ int oracle_gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, double 
   if (!jobs) return -1;
   for (int t = 0; t < nthreads; ++t) {
     job_t* J = &jobs[t];
-    J->transA = transA; J->transB = transB; J->in_type = in_type; J->c_type = c_type;
+    J->transA = transA; J->transB = transB; J->a_type = a_type; J->b_type = b_type;
+    J->c_type = c_type;
     J->M = M; J->N = N; J->K = K; J->lda = lda; J->ldb = ldb; J->ldc = ldc; J->ldr = ldr;
     J->alpha = alpha; J->beta = beta; J->A = A; J->B = B; J->C0 = C0;
     J->R = R; J->Mag = Mag;
@@ -200,16 +248,25 @@ int oracle_gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, double 
   return used;
 }
 
+/* Both operands of one type. */
+int oracle_gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, double alpha,
+                const void* A, int64_t lda, const void* B, int64_t ldb, double beta,
+                const void* C0, int c_type, int64_t ldc, int in_type, double* R, double* Mag,
+                int64_t ldr, int nthreads) {
+  return oracle_gemm_ab(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C0, c_type, ldc,
+                        in_type, in_type, R, Mag, ldr, nthreads);
+}
+
 /*
  * Sampled oracle: for e in [0, count), R[e] / Mag[e] receive r and m at
  * (rows[e], cols[e]).  Used where the full product would take too long.
  */
-int oracle_gemm_at(int transA, int transB, int64_t M, int64_t N, int64_t K, double alpha,
-                   const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb, double beta,
-                   const void* C0, int c_type, int64_t ldc, int in_type, int64_t count,
-                   const int64_t* rows, const int64_t* cols, double* R, double* Mag,
-                   int nthreads) {
-  if (check_args(transA, transB, M, N, K, lda, ldb, in_type, c_type) != 0) return -1;
+int oracle_gemm_at_ab(int transA, int transB, int64_t M, int64_t N, int64_t K, double alpha,
+                      const void* A, int64_t lda, const void* B, int64_t ldb, double beta,
+                      const void* C0, int c_type, int64_t ldc, int a_type, int b_type,
+                      int64_t count, const int64_t* rows, const int64_t* cols, double* R,
+                      double* Mag, int nthreads) {
+  if (check_args(transA, transB, M, N, K, lda, ldb, a_type, b_type, c_type) != 0) return -1;
   if (beta != 0.0 && ldc < N) return -1;
   for (int64_t e = 0; e < count; ++e)
     if (rows[e] < 0 || rows[e] >= M || cols[e] < 0 || cols[e] >= N) return -1;
@@ -219,7 +276,8 @@ int oracle_gemm_at(int transA, int transB, int64_t M, int64_t N, int64_t K, doub
   if (!jobs) return -1;
   for (int t = 0; t < nthreads; ++t) {
     job_t* J = &jobs[t];
-    J->transA = transA; J->transB = transB; J->in_type = in_type; J->c_type = c_type;
+    J->transA = transA; J->transB = transB; J->a_type = a_type; J->b_type = b_type;
+    J->c_type = c_type;
     J->M = M; J->N = N; J->K = K; J->lda = lda; J->ldb = ldb; J->ldc = ldc; J->ldr = 0;
     J->alpha = alpha; J->beta = beta; J->A = A; J->B = B; J->C0 = C0;
     J->R = R; J->Mag = Mag; J->rows = rows; J->cols = cols;
@@ -229,4 +287,13 @@ int oracle_gemm_at(int transA, int transB, int64_t M, int64_t N, int64_t K, doub
   int used = run_jobs(jobs, nthreads, run_entries);
   free(jobs);
   return used;
+}
+
+int oracle_gemm_at(int transA, int transB, int64_t M, int64_t N, int64_t K, double alpha,
+                   const void* A, int64_t lda, const void* B, int64_t ldb, double beta,
+                   const void* C0, int c_type, int64_t ldc, int in_type, int64_t count,
+                   const int64_t* rows, const int64_t* cols, double* R, double* Mag,
+                   int nthreads) {
+  return oracle_gemm_at_ab(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C0, c_type, ldc,
+                           in_type, in_type, count, rows, cols, R, Mag, nthreads);
 }

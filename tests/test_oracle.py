@@ -1,8 +1,8 @@
 """Pins for the CPU oracle (no GPU).
 
 Each test checks the oracle against something other than itself: the value
-definitions of the 16-bit formats and a library decoder over every bit
-pattern, closed forms (identity, permutation, rank-1 products), exact integer
+definitions of the 16-bit and 8-bit formats and a library decoder over every
+bit pattern, closed forms (identity, permutation, rank-1 products), exact integer
 arithmetic, a brute-force loop written independently in pure Python, the
 degenerate sizes, and invariants of the tolerance magnitude.  Together they
 catch a dropped term, a wrong sign, a wrong index or stride, and a transposed
@@ -73,6 +73,83 @@ def test_f16_decode_every_pattern_matches_library():
     nan = np.isnan(ref)
     assert np.array_equal(np.isnan(mine), nan)
     assert np.array_equal(mine[~nan], ref[~nan])
+
+
+# ---------------------------------------------------------------------------
+# Decoding the 8-bit formats (E4M3 / E5M2: OCP 8-bit float layouts)
+# ---------------------------------------------------------------------------
+
+def test_fp8_decode_known_values():
+    """Values fixed by the format definitions."""
+    e4, e5 = oracle.e4m3_value, oracle.e5m2_value
+    assert e4(0x38) == 1.0 and e4(0xB8) == -1.0
+    assert e4(0x7E) == 448.0                      # largest finite E4M3
+    assert e4(0x08) == 2.0 ** -6                  # smallest normal
+    assert e4(0x01) == 2.0 ** -9                  # smallest subnormal
+    assert e4(0x07) == 7.0 / 8.0 * 2.0 ** -6      # largest subnormal
+    assert e4(0x78) == 256.0 and e4(0x3C) == 1.5
+    assert math.isnan(e4(0x7F)) and math.isnan(e4(0xFF))   # the only NaNs; no infinities
+    assert math.copysign(1.0, e4(0x80)) == -1.0 and e4(0x80) == 0.0
+    assert e5(0x3C) == 1.0 and e5(0xBC) == -1.0
+    assert e5(0x7B) == 57344.0                    # largest finite E5M2
+    assert e5(0x04) == 2.0 ** -14 and e5(0x01) == 2.0 ** -16
+    assert e5(0x7C) == math.inf and e5(0xFC) == -math.inf
+    assert all(math.isnan(e5(b)) for b in (0x7D, 0x7E, 0x7F, 0xFD))
+    assert e5(0x3E) == 1.5
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_fp8_decode_every_pattern_matches_library(fmt):
+    codes = np.arange(256, dtype=np.uint8)
+    dt = torch.float8_e4m3fn if fmt == "e4m3" else torch.float8_e5m2
+    ref = torch.from_numpy(codes.copy()).view(dt).to(torch.float64).numpy()
+    dec = oracle.e4m3_value if fmt == "e4m3" else oracle.e5m2_value
+    mine = np.array([dec(int(b)) for b in codes])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan)
+    assert np.array_equal(mine[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(mine[~nan]), np.signbit(ref[~nan]))
+
+
+def _decoded(t):
+    return t.to(torch.float64).numpy()
+
+
+@pytest.mark.parametrize("transA,transB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("fa,fb", [("e4m3", "e4m3"), ("e5m2", "e5m2"), ("e4m3", "e5m2"), ("e5m2", "e4m3")])
+def test_fp8_product_matches_library_matmul(transA, transB, fa, fb):
+    """8-bit inputs, each operand with its own format, against numpy's matmul
+    of the library-decoded values (fp64, exact products, order-only rounding)."""
+    M, N, K = 13, 11, 150
+    p = inputs.make_problem("f8", M, N, K, transA, transB, fa, "f32", ("normal", 0, 2), ("normal", 0, 2),
+                            alpha=0.75, beta=-0.5, seed=41, b_dtype=fb)
+    codes = {"e4m3": oracle.IN_E4M3, "e5m2": oracle.IN_E5M2}
+    R, Mag = oracle.gemm(transA, transB, M, N, K, p.alpha, inputs.bits(p.A), p.lda, inputs.bits(p.B), p.ldb,
+                         p.beta, p.C0.numpy(), p.ldc, codes[fa], b_type=codes[fb])
+    a = _op(_decoded(p.A[:, :(M if transA else K)]), transA)
+    b = _op(_decoded(p.B[:, :(K if transB else N)]), transB)
+    ref = p.alpha * (a @ b) + p.beta * p.C0[:, :N].double().numpy()
+    assert np.allclose(R, ref, rtol=1e-12, atol=1e-12)
+    assert np.allclose(Mag, abs(p.alpha) * (np.abs(a) @ np.abs(b)) + abs(p.beta) * np.abs(p.C0[:, :N].double().numpy()),
+                       rtol=1e-12, atol=1e-12)
+
+
+def test_fp8_small_integers_exact():
+    """Integers in {-8..8} are exact in both formats; the integer product is exact."""
+    M, N, K = 20, 24, 300
+    p = inputs.make_problem("f8i", M, N, K, 0, 1, "e4m3", "f32", ("ints", -8, 8), ("ints", -8, 8), seed=3,
+                            b_dtype="e5m2")
+    R, _ = oracle.gemm(0, 1, M, N, K, 1.0, inputs.bits(p.A), K, inputs.bits(p.B), K, 0.0, None, N,
+                       oracle.IN_E4M3, b_type=oracle.IN_E5M2)
+    a = p.A.to(torch.float32).numpy().astype(np.int64)
+    b = p.B.to(torch.float32).numpy().astype(np.int64)
+    assert np.array_equal(R, (a @ b.T).astype(np.float64))
+
+
+def test_fp8_code_width_is_checked():
+    with pytest.raises(TypeError):
+        oracle.gemm(0, 0, 2, 2, 2, 1.0, np.zeros((2, 2), np.uint16), 2, np.zeros((2, 2), np.uint8), 2, 0.0,
+                    None, 2, oracle.IN_E4M3)
 
 
 # ---------------------------------------------------------------------------

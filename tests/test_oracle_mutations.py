@@ -10,16 +10,21 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "gemm_oracle.c")
 
 MUTATIONS = {
-    "B read as if never transposed": ("J->B[j * J->ldb + k] : J->B[k * J->ldb + j]",
-                                      "J->B[k * J->ldb + j] : J->B[k * J->ldb + j]"),
-    "A index transposed": ("J->A[k * J->lda + i] : J->A[i * J->lda + k]",
-                           "J->A[i * J->lda + k] : J->A[k * J->lda + i]"),
+    "B read as if never transposed": ("J->transB ? j * J->ldb + k : k * J->ldb + j",
+                                      "J->transB ? k * J->ldb + j : k * J->ldb + j"),
+    "A index transposed": ("J->transA ? k * J->lda + i : i * J->lda + k",
+                           "J->transA ? i * J->lda + k : k * J->lda + i"),
     "last k term dropped": ("for (int64_t k = 0; k < J->K; ++k)", "for (int64_t k = 0; k + 1 < J->K; ++k)"),
     "beta term sign flipped": ("rv += J->beta * c0;", "rv -= J->beta * c0;"),
     "alpha dropped": ("double rv = J->alpha * s;", "double rv = s;"),
     "fp16 exponent bias off by one": ("e - 15);", "e - 16);"),
     "bf16 fraction width wrong": ("1.0 + (double)f / 128.0", "1.0 + (double)f / 256.0"),
     "C0 leading dimension ignored": ("i * J->ldc + j", "i * J->N + j"),
+    "E4M3 exponent bias off by one": ("e - 7);", "e - 8);"),
+    "E4M3 NaN rule too wide": ("e == 0xF && f == 0x7", "e == 0xF"),
+    "E5M2 fraction width wrong": ("1.0 + (double)f / 4.0", "1.0 + (double)f / 8.0"),
+    "E5M2 subnormal scale wrong": ("(double)f / 4.0, -14)", "(double)f / 4.0, -15)"),
+    "B decoded with A's type": ("in_value(J->b_type, J->B", "in_value(J->a_type, J->B"),
 }
 
 
