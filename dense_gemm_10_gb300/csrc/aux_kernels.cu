@@ -1,5 +1,5 @@
 // aux_kernels.cu -- the two non-tensor-core kernels of the library:
-//  * repack16: copies a 16-bit operand whose rows are not 16-byte aligned into
+//  * repack: copies an operand whose rows are not 16-byte aligned into
 //    an aligned buffer, because the tensor-memory-accelerator copy engine only
 //    reads rows whose pitch is a multiple of 16 bytes;
 //  * scale_c: C = beta * C, the whole GEMM when K == 0 ("CUDA GEMM 矩阵乘法优化指南",
@@ -12,12 +12,12 @@
 
 namespace g10 {
 
-__global__ void repack16_kernel(const uint16_t* __restrict__ src, int64_t lds,
-                                uint16_t* __restrict__ dst, int64_t ldd, int64_t rows,
-                                int64_t cols) {
+template <typename T>
+__global__ void repack_kernel(const T* __restrict__ src, int64_t lds, T* __restrict__ dst, int64_t ldd,
+                              int64_t rows, int64_t cols) {
   for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
-    const uint16_t* s = src + r * lds;
-    uint16_t* d = dst + r * ldd;
+    const T* s = src + r * lds;
+    T* d = dst + r * ldd;
     for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < cols;
          c += static_cast<int64_t>(gridDim.x) * blockDim.x)
       d[c] = s[c];
@@ -52,9 +52,14 @@ static dim3 grid_2d(int64_t rows, int64_t cols, int sm_count) {
   return dim3(static_cast<unsigned>(bx > 0 ? bx : 1), static_cast<unsigned>(by > 0 ? by : 1), 1);
 }
 
-cudaError_t repack16_launch(const uint16_t* src, int64_t lds, uint16_t* dst, int64_t ldd,
-                            int64_t rows, int64_t cols, int sm_count, cudaStream_t stream) {
-  repack16_kernel<<<grid_2d(rows, cols, sm_count), 256, 0, stream>>>(src, lds, dst, ldd, rows, cols);
+cudaError_t repack_launch(const void* src, int64_t lds, void* dst, int64_t ldd, int64_t rows,
+                          int64_t cols, int esize, int sm_count, cudaStream_t stream) {
+  if (esize == 1)
+    repack_kernel<uint8_t><<<grid_2d(rows, cols, sm_count), 256, 0, stream>>>(
+        static_cast<const uint8_t*>(src), lds, static_cast<uint8_t*>(dst), ldd, rows, cols);
+  else
+    repack_kernel<uint16_t><<<grid_2d(rows, cols, sm_count), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(src), lds, static_cast<uint16_t*>(dst), ldd, rows, cols);
   return cudaGetLastError();
 }
 

@@ -63,15 +63,48 @@ struct Plan {
   int64_t I = 0, J = 0, K = 0;
   int64_t c_si = 0, c_sj = 0;
   int32_t c_type = kCF32;
-  bool bf16 = true;
+  int32_t eb = 2;                  // input element bytes (2: bf16 / fp16, 1: FP8)
+  uint32_t a_fmt = 1, b_fmt = 1;   // instruction-descriptor formats of the stored A and B
+  int32_t in_dtype = 0;            // CU_TENSOR_MAP data type of A and B
+  int cfg = 0;                     // index into kTileConfigs
   size_t partial_offset = 0;
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-bool tma_aligned(const void* p, int64_t ld) {
-  return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((ld * 2) % 16 == 0);
+bool tma_aligned(const void* p, int64_t ld, int eb) {
+  return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((ld * eb) % 16 == 0);
+}
+
+// The input and output types a gemm_dtype_t names.
+struct DtypeInfo {
+  bool valid = false;
+  int32_t eb = 2;
+  uint32_t a_fmt = 0, b_fmt = 0;  // kind::f16: 0 f16, 1 bf16; kind::f8f6f4: 0 E4M3, 1 E5M2
+  int32_t c_type = kCF32;
+  CUtensorMapDataType map_type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+};
+
+DtypeInfo dtype_info(int dtype) {
+  DtypeInfo d;
+  if (dtype >= GEMM_BF16_F32 && dtype <= GEMM_F16_F16) {
+    const bool bf16 = dtype == GEMM_BF16_F32 || dtype == GEMM_BF16_BF16;
+    d.valid = true;
+    d.a_fmt = d.b_fmt = bf16 ? 1u : 0u;
+    d.c_type = (dtype == GEMM_BF16_F32 || dtype == GEMM_F16_F32) ? kCF32 : bf16 ? kCBF16 : kCF16;
+    d.map_type = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  } else if (dtype >= GEMM_E4M3_F32 && dtype <= GEMM_E5M2_F16) {
+    // 16 + (A is E5M2) + 2 * (B is E5M2) + 4 * (C: 0 fp32, 1 bf16, 2 fp16)
+    const int x = dtype - GEMM_E4M3_F32;
+    d.valid = true;
+    d.eb = 1;
+    d.a_fmt = x & 1;
+    d.b_fmt = (x >> 1) & 1;
+    d.c_type = x >> 2 == 0 ? kCF32 : x >> 2 == 1 ? kCBF16 : kCF16;
+    d.map_type = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  }
+  return d;
 }
 
 // 64-wide k-slices per ring stage unless GEMM_OPT_KDEPTH says otherwise.  The
@@ -92,7 +125,10 @@ double tile_kb_cost(const TileConfig& c) {
 
 // Resident schedule slots (CTAs, CTA pairs or clusters) per tile configuration.
 struct SlotTable {
-  int n[kNumTileConfigs] = {1, 1, 1, 1, 1, 1, 1};
+  int n[kNumTileConfigs];
+  SlotTable() {
+    for (int& x : n) x = 1;
+  }
   int of(int cfg) const { return n[cfg]; }
   static SlotTable even(int sm_count) {
     SlotTable t;
@@ -109,7 +145,7 @@ cudaError_t measure_slots(int sm_count, SlotTable* t) {
   for (int i = 0; i < kNumTileConfigs; ++i) {
     const TileConfig& c = kTileConfigs[i];
     int clusters = 0;
-    cudaError_t e = tc_prepare(c.bn, c.cg, c.mc, &clusters);
+    cudaError_t e = tc_prepare(i, &clusters);
     if (e != cudaSuccess) return e;
     if (c.cg * c.mc > 1 && clusters > 0) t->n[i] = std::min(clusters, sm_count / (c.cg * c.mc));
   }
@@ -226,12 +262,12 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   gemm_plan_t& P = pl.pub;
   if ((transA != GEMM_OP_N && transA != GEMM_OP_T) || (transB != GEMM_OP_N && transB != GEMM_OP_T))
     return GEMM_ERR_INVALID_ARG;
-  if (dtype < GEMM_BF16_F32 || dtype > GEMM_F16_F16) return GEMM_ERR_INVALID_ARG;
+  const DtypeInfo dt = dtype_info(dtype);
+  if (!dt.valid) return GEMM_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
-  pl.bf16 = dtype == GEMM_BF16_F32 || dtype == GEMM_BF16_BF16;
-  pl.c_type = (dtype == GEMM_BF16_F32 || dtype == GEMM_F16_F32) ? kCF32
-              : dtype == GEMM_BF16_BF16                        ? kCBF16
-                                                               : kCF16;
+  pl.eb = dt.eb;
+  pl.in_dtype = static_cast<int32_t>(dt.map_type);
+  pl.c_type = dt.c_type;
   const int64_t c_elem = pl.c_type == kCF32 ? 4 : 2;
   if (M == 0 || N == 0) {
     P.path = GEMM_PATH_NOOP;
@@ -249,6 +285,8 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   if (A == nullptr || B == nullptr) return GEMM_ERR_INVALID_ARG;
   if (lda < (transA == GEMM_OP_T ? M : K) || ldb < (transB == GEMM_OP_T ? K : N))
     return GEMM_ERR_INVALID_ARG;
+  // 8-bit operands: K-major only (A stored M x K, B stored N x K).
+  if (dt.eb == 1 && (transA != GEMM_OP_N || transB != GEMM_OP_T)) return GEMM_ERR_UNSUPPORTED;
 
   // Stored operands.
   Operand a, b;
@@ -265,24 +303,28 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   pl.K = K;
   pl.p = swap ? b : a;
   pl.q = swap ? a : b;
+  pl.a_fmt = swap ? dt.b_fmt : dt.a_fmt;  // formats of the MMA's A (P) and B (Q) operands
+  pl.b_fmt = swap ? dt.a_fmt : dt.b_fmt;
   pl.c_si = swap ? 1 : ldc;
   pl.c_sj = swap ? ldc : 1;
   P.a_kmajor = pl.p.kmajor ? 1 : 0;
   P.b_kmajor = pl.q.kmajor ? 1 : 0;
 
-  const int64_t num_kslices = cdiv(K, kBK);  // 64-wide k-slices
-  // Below the machine balance (≈ 2.2 PFLOP/s over ≈ 7 TB/s ≈ 300 FLOP per byte)
-  // the GEMM is bound by HBM, not by the tensor cores.
-  const double alg_bytes = 2.0 * (static_cast<double>(M) * K + static_cast<double>(K) * N) +
+  const int64_t num_kslices = cdiv(K, slice_k(dt.eb));  // 128-byte k-slices
+  // Below the machine balance (≈ 2.2 PFLOP/s over ≈ 7 TB/s ≈ 300 FLOP per byte
+  // for 16-bit inputs, twice that for the 8-bit ones at twice the rate) the
+  // GEMM is bound by HBM, not by the tensor cores.
+  const double alg_bytes = dt.eb * (static_cast<double>(M) * K + static_cast<double>(K) * N) +
                            static_cast<double>(M) * N * c_elem * (beta != 0.0f ? 2 : 1);
-  const bool hbm_bound = 2.0 * static_cast<double>(M) * N * K / alg_bytes < 256.0;
+  const bool hbm_bound = 2.0 * static_cast<double>(M) * N * K / alg_bytes < 256.0 * (3 - dt.eb);
 
   // Tile configuration and schedule: the configuration with the lowest
   // estimated time, est_time() below.
-  static const int kPreference[kNumTileConfigs] = {5, 4, 3, 2, 1, 6, 0};  // ties go to the first
+  static const int kPreference[kNumTileConfigs] = {5, 4, 3, 2, 1, 6, 0, 10, 9, 8, 7};  // ties go first
   Choice best;
   for (int cfg : kPreference) {
     const TileConfig& c = kTileConfigs[cfg];
+    if (c.eb != dt.eb) continue;
     const int path = c.mc == 2 ? GEMM_PATH_TC_2CTA_MULTICAST : c.cg == 2 ? GEMM_PATH_TC_2CTA : GEMM_PATH_TC_1CTA;
     if (o.force_path && o.force_path != path) continue;
     if (o.force_bn && c.bn != o.force_bn) continue;
@@ -294,7 +336,7 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
     if (o.max_grid) nslots = std::min(nslots, std::max(1, o.max_grid / (c.cg * c.mc)));
     // Two k-slices per stage where the ring still holds at least two such stages.
     int kdepth = o.kdepth ? o.kdepth : default_kdepth(c);
-    if (kdepth > 1 && tc_stages(c.bn, c.cg, c.mc) / kdepth < 2) kdepth = 1;
+    if (kdepth > 1 && tc_stages(cfg) / kdepth < 2) kdepth = 1;
     Choice ch = choose_schedule(o, cdiv(pl.I, kBM * c.cg), cdiv(cdiv(pl.J, c.bn), c.mc),
                                 cdiv(num_kslices, kdepth), kdepth, cfg, nslots, hbm_bound);
     if (ch.valid && ch.cost < best.cost - 1e-9) best = ch;
@@ -303,6 +345,7 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   const int cg = best.cg;
   const int cl = best.cg * best.mc;
   pl.sched = best.sched;
+  pl.cfg = best.cfg;
   pl.sched.raster_group = o.raster_group ? o.raster_group : 8;
   if (pl.sched.raster_group > pl.sched.tiles_i) pl.sched.raster_group = pl.sched.tiles_i;
   P.path = best.mc == 2 ? GEMM_PATH_TC_2CTA_MULTICAST : cg == 2 ? GEMM_PATH_TC_2CTA : GEMM_PATH_TC_1CTA;
@@ -310,8 +353,8 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   P.bm = kBM * cg;
   P.bn = best.bn;
   P.kdepth = best.kdepth;
-  P.bk = kBK * best.kdepth;
-  P.stages = tc_stages(best.bn, cg, best.mc) / best.kdepth;
+  P.bk = slice_k(dt.eb) * best.kdepth;
+  P.stages = tc_stages(best.cfg) / best.kdepth;
   if (o.stages > 0 && o.stages < P.stages) P.stages = o.stages;
   P.schedule = pl.sched.mode;
   P.split_k = pl.sched.mode == kSchedTiles ? pl.sched.split_k : 1;
@@ -328,11 +371,11 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   // Workspace: repacked operands, then partial tiles of split tiles.
   size_t ws = 0;
   for (Operand* op : {&pl.p, &pl.q}) {
-    if (!tma_aligned(op->ptr, op->ld)) {
-      op->repack = true;
-      op->packed_ld = static_cast<int64_t>(round_up(static_cast<size_t>(op->cols), 8));
+    if (!tma_aligned(op->ptr, op->ld, dt.eb)) {
+      op->repack = true;  // rows padded to whole 16-byte pieces
+      op->packed_ld = static_cast<int64_t>(round_up(static_cast<size_t>(op->cols), 16 / dt.eb));
       op->ws_offset = ws;
-      ws = round_up(ws + static_cast<size_t>(op->rows) * op->packed_ld * 2, 256);
+      ws = round_up(ws + static_cast<size_t>(op->rows) * op->packed_ld * dt.eb, 256);
     }
   }
   P.repack_a = (swap ? pl.q.repack : pl.p.repack) ? 1 : 0;
@@ -374,20 +417,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Describe operand `op` (possibly its repacked copy at `base`/`ld`) for 2-D tiled
-// loads with the 128-byte swizzle: K-major tiles are {64 k} x {box_rows rows};
-// MN-major tiles are {64 rows of M/N} x {64 k}, loaded one 64-wide atom at a time.
+// loads with the 128-byte swizzle: K-major tiles are {one 128-byte k-slice} x
+// {box_rows rows} (64 16-bit or 128 8-bit elements of k); MN-major tiles
+// (16-bit only) are {64 rows of M/N} x {64 k}, loaded one 64-wide atom at a time.
 gemm_status_t encode_operand(CUtensorMap* map, const Operand& op, const void* base, int64_t ld,
-                             bool bf16, int box_rows) {
+                             int eb, int32_t map_type, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return GEMM_ERR_TENSORMAP;
   cuuint64_t dims[2];
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * eb};
   cuuint32_t box[2];
   cuuint32_t estr[2] = {1, 1};
   if (op.kmajor) {
     dims[0] = static_cast<cuuint64_t>(op.cols);  // K
     dims[1] = static_cast<cuuint64_t>(op.rows);  // M or N
-    box[0] = kBK;
+    box[0] = static_cast<cuuint32_t>(slice_k(eb));
     box[1] = static_cast<cuuint32_t>(box_rows);
   } else {
     dims[0] = static_cast<cuuint64_t>(op.cols);  // M or N
@@ -395,8 +439,7 @@ gemm_status_t encode_operand(CUtensorMap* map, const Operand& op, const void* ba
     box[0] = 64;
     box[1] = kBK;
   }
-  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  CUresult r = fn(map, static_cast<CUtensorMapDataType>(map_type), 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_TENSORMAP;
@@ -640,18 +683,17 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
   for (int w = 0; w < 2; ++w) {
     const Operand& op = w == 0 ? pl.p : pl.q;
     if (!op.repack) continue;
-    uint16_t* dst = reinterpret_cast<uint16_t*>(ws + op.ws_offset);
-    e = repack16_launch(static_cast<const uint16_t*>(op.ptr), op.ld, dst, op.packed_ld, op.rows,
-                        op.cols, h->sm_count, st);
+    void* dst = ws + op.ws_offset;
+    e = repack_launch(op.ptr, op.ld, dst, op.packed_ld, op.rows, op.cols, pl.eb, h->sm_count, st);
     if (e != cudaSuccess) return cuda_fail(h, e);
     h->launches += 1;
     if (w == 0) { pbase = dst; pld = op.packed_ld; } else { qbase = dst; qld = op.packed_ld; }
   }
 
   CUtensorMap map_p, map_q;
-  s = encode_operand(&map_p, pl.p, pbase, pld, pl.bf16, kBM / mc);
+  s = encode_operand(&map_p, pl.p, pbase, pld, pl.eb, pl.in_dtype, kBM / mc);
   if (s != GEMM_OK) return s;
-  s = encode_operand(&map_q, pl.q, qbase, qld, pl.bf16, P.bn / cg);
+  s = encode_operand(&map_q, pl.q, qbase, qld, pl.eb, pl.in_dtype, P.bn / cg);
   if (s != GEMM_OK) return s;
   CUtensorMap map_c;
   std::memset(&map_c, 0, sizeof(map_c));
@@ -672,7 +714,7 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
   a.q_kmajor = P.b_kmajor;
   a.stages = P.stages;
   a.kdepth = P.kdepth;
-  a.idesc = make_idesc_f16(pl.bf16, !pl.p.kmajor, !pl.q.kmajor, kBM * cg, P.bn);
+  a.idesc = make_idesc(pl.a_fmt, pl.b_fmt, !pl.p.kmajor, !pl.q.kmajor, kBM * cg, P.bn);
   a.alpha = alpha;
   a.beta = beta;
   a.C = C;
@@ -686,7 +728,7 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
   a.status = h->d_status;
   a.wait_limit_ns = static_cast<uint64_t>(h->opt.wait_limit_ns);
   a.drop_load = h->opt.drop_load;
-  e = tc_launch(P.bn, cg, mc, map_p, map_q, map_c, a, P.grid, st);
+  e = tc_launch(pl.cfg, map_p, map_q, map_c, a, P.grid, st);
   if (e != cudaSuccess) return cuda_fail(h, e);
   h->launches += 1;
   return GEMM_OK;
@@ -827,16 +869,15 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   for (int w = 0; w < 2; ++w) {
     const Operand& op = w == 0 ? pl.p : pl.q;
     if (!op.repack) continue;
-    uint16_t* dst = reinterpret_cast<uint16_t*>(d->scratch + op.ws_offset);
-    e = repack16_launch(static_cast<const uint16_t*>(op.ptr), op.ld, dst, op.packed_ld, op.rows,
-                        op.cols, d->sm_count, st);
+    void* dst = d->scratch + op.ws_offset;
+    e = repack_launch(op.ptr, op.ld, dst, op.packed_ld, op.rows, op.cols, pl.eb, d->sm_count, st);
     if (e != cudaSuccess) return GEMM_ERR_CUDA;
     if (w == 0) { pbase = dst; pld = op.packed_ld; } else { qbase = dst; qld = op.packed_ld; }
   }
   CUtensorMap map_p, map_q;
-  s = encode_operand(&map_p, pl.p, pbase, pld, pl.bf16, kBM / mc);
+  s = encode_operand(&map_p, pl.p, pbase, pld, pl.eb, pl.in_dtype, kBM / mc);
   if (s != GEMM_OK) return s;
-  s = encode_operand(&map_q, pl.q, qbase, qld, pl.bf16, P.bn / cg);
+  s = encode_operand(&map_q, pl.q, qbase, qld, pl.eb, pl.in_dtype, P.bn / cg);
   if (s != GEMM_OK) return s;
   CUtensorMap map_c;
   std::memset(&map_c, 0, sizeof(map_c));
@@ -856,7 +897,7 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   a.q_kmajor = P.b_kmajor;
   a.stages = P.stages;
   a.kdepth = P.kdepth;
-  a.idesc = make_idesc_f16(pl.bf16, !pl.p.kmajor, !pl.q.kmajor, kBM * cg, P.bn);
+  a.idesc = make_idesc(pl.a_fmt, pl.b_fmt, !pl.p.kmajor, !pl.q.kmajor, kBM * cg, P.bn);
   a.alpha = alpha;
   a.beta = beta;
   a.C = C;
@@ -870,6 +911,6 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   a.status = d->status;
   a.wait_limit_ns = static_cast<uint64_t>(o.wait_limit_ns);
   a.drop_load = 0;
-  e = tc_launch(P.bn, cg, mc, map_p, map_q, map_c, a, P.grid, st);
+  e = tc_launch(pl.cfg, map_p, map_q, map_c, a, P.grid, st);
   return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

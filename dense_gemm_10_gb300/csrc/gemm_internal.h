@@ -10,9 +10,13 @@
 
 namespace g10 {
 
-constexpr int kBM = 128;      // MMA M (rows of the output tile held in TMEM lanes)
-constexpr int kBK = 64;       // k-block: 64 16-bit elements = one 128-byte swizzle row
-constexpr int kThreads = 192; // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue
+constexpr int kBM = 128;          // MMA M (rows of the output tile held in TMEM lanes)
+constexpr int kSliceBytes = 128;  // a k-slice: one 128-byte swizzle row of every tile row
+constexpr int kBK = 64;           // k-slice of 16-bit elements (64 x 2 bytes)
+constexpr int kThreads = 192;     // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue
+
+// k elements of one k-slice for an element of eb bytes (2: bf16 / fp16, 1: FP8).
+__host__ __device__ constexpr int slice_k(int eb) { return kSliceBytes / eb; }
 
 // Element type of C.
 enum CType : int32_t { kCF32 = 0, kCBF16 = 1, kCF16 = 2 };
@@ -30,12 +34,12 @@ enum WaitBarrier : int32_t {
 // P is the MMA "A" operand (tile rows on TMEM lanes), Q the MMA "B" operand.
 struct TcArgs {
   int32_t I, J, K;
-  Sched sched;           // work assignment (schedule.h); num_kb = ceil(K / (kBK * kdepth))
+  Sched sched;           // work assignment (schedule.h); num_kb = ceil(K / (slice_k * kdepth))
   int32_t p_kmajor;      // P has K contiguous (else I contiguous)
   int32_t q_kmajor;      // Q has K contiguous (else J contiguous)
   uint32_t idesc;        // tcgen05 instruction descriptor
   int32_t stages;        // ring stages in use, 1 .. the configuration's maximum / kdepth
-  int32_t kdepth;        // kBK-wide k-slices per stage (1 or 2); one barrier per stage
+  int32_t kdepth;        // k-slices per stage (1 or 2); one barrier per stage
   float alpha, beta;
   void* C;
   int64_t c_si, c_sj;
@@ -55,25 +59,27 @@ enum BulkStore : int32_t { kBulkNone = 0, kBulkRows = 1, kBulkTransposed = 2 };
 
 // Tile configurations: a tile of (128 * cg) x bn per CTA (cg == 1) or CTA
 // pair (cg == 2); mc == 2 clusters two pairs on neighbouring tiles of one tile
-// row, which share the P tile by multicast.
+// row, which share the P tile by multicast.  eb is the input element size in
+// bytes: 2 for bf16 / fp16 (tcgen05.mma kind::f16), 1 for the 8-bit formats
+// (kind::f8f6f4).
 struct TileConfig {
-  int bn, cg, mc;
+  int bn, cg, mc, eb;
 };
-constexpr int kNumTileConfigs = 7;
+constexpr int kNumTileConfigs = 11;
 extern const TileConfig kTileConfigs[kNumTileConfigs];
-int tc_config_index(int bn, int cg, int mc);  // -1 if not built
-int tc_stages(int bn, int cg, int mc);
+int tc_stages(int cfg);  // ring depth in k-slices
 // One-time per device: opt in to the kernel's shared memory; for clusters also
 // report how many can be resident at once.
-cudaError_t tc_prepare(int bn, int cg, int mc, int* max_clusters);
+cudaError_t tc_prepare(int cfg, int* max_clusters);
 // grid = CTAs (a multiple of cg * mc).
 // map_c describes C for the bulk-store epilogue (ignored unless args.tma_store).
-cudaError_t tc_launch(int bn, int cg, int mc, const CUtensorMap& map_p, const CUtensorMap& map_q,
+cudaError_t tc_launch(int cfg, const CUtensorMap& map_p, const CUtensorMap& map_q,
                       const CUtensorMap& map_c, const TcArgs& args, int grid, cudaStream_t stream);
 
-// dst[r * ldd + c] = src[r * lds + c] for 16-bit elements, r < rows, c < cols.
-cudaError_t repack16_launch(const uint16_t* src, int64_t lds, uint16_t* dst, int64_t ldd,
-                            int64_t rows, int64_t cols, int sm_count, cudaStream_t stream);
+// dst[r * ldd + c] = src[r * lds + c] for elements of esize (1 or 2) bytes,
+// r < rows, c < cols; leading dimensions in elements.
+cudaError_t repack_launch(const void* src, int64_t lds, void* dst, int64_t ldd, int64_t rows,
+                          int64_t cols, int esize, int sm_count, cudaStream_t stream);
 
 // C = beta * C over an M x N matrix with leading dimension ldc (C = 0 when beta == 0).
 cudaError_t scale_c_launch(void* C, int32_t c_type, int64_t M, int64_t N, int64_t ldc, float beta,

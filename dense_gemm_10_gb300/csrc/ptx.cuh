@@ -230,39 +230,57 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor of tcgen05.mma.kind::f16 with an fp32 accumulator.
+// Instruction descriptor of tcgen05.mma (kind::f16 or kind::f8f6f4) with an
+// fp32 accumulator.
 //   bits  4-5   D format (1 = f32)
-//   bits  7-9   A format (0 = f16, 1 = bf16)
-//   bits 10-12  B format
+//   bits  7-9   A format: kind::f16 0 = f16, 1 = bf16; kind::f8f6f4 0 = E4M3, 1 = E5M2
+//   bits 10-12  B format, the same codes
 //   bit  15     A major (0 = K-major, 1 = M-major)
 //   bit  16     B major (0 = K-major, 1 = N-major)
 //   bits 17-22  N >> 3
 //   bits 24-28  M >> 4
-__host__ __device__ constexpr uint32_t make_idesc_f16(bool bf16, bool a_mn_major, bool b_mn_major,
-                                                      int m, int n) {
-  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
-         ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
-         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+__host__ __device__ constexpr uint32_t make_idesc(uint32_t a_fmt, uint32_t b_fmt, bool a_mn_major,
+                                                  bool b_mn_major, int m, int n) {
+  return (1u << 4) | ((a_fmt & 7u) << 7) | ((b_fmt & 7u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]; issued by a single thread.  With CG == 2 the
 // leader CTA issues it for the pair: A rows and B rows come half from each
 // CTA's shared memory (same offsets), and each CTA's TMEM receives its rows of D.
-template <int CG>
-__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                           uint32_t idesc, uint32_t accumulate) {
-  if constexpr (CG == 1)
+// EB = input element bytes: 2 -> kind::f16 (K = 16), 1 -> kind::f8f6f4 (K = 32);
+// either way one instruction consumes 32 bytes of every operand row.
+template <int CG, int EB>
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  static_assert(EB == 1 || EB == 2, "element bytes");
+  if constexpr (CG == 1 && EB == 2)
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
-  else
+  else if constexpr (CG == 2 && EB == 2)
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else if constexpr (CG == 1)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }

@@ -59,8 +59,8 @@ struct TcConfig {
   static constexpr int kCluster = CG * MC;       // CTAs per cluster
   static constexpr int kTileM = kBM * CG;        // rows of D per tile
   static constexpr int kQRows = BN / CG;         // rows of Q this CTA loads per k-block
-  static constexpr int kABytes = kBM * kBK * 2;  // this CTA's P tile: 128 rows x 128 bytes
-  static constexpr int kBBytes = kQRows * kBK * 2;
+  static constexpr int kABytes = kBM * kSliceBytes;  // this CTA's P tile: 128 rows x 128 bytes
+  static constexpr int kBBytes = kQRows * kSliceBytes;
   static constexpr int kStageBytes = kABytes + kBBytes;
   // as many stages as fit in 227 KB beside the control block and alignment slack (at most 8)
   // epilogue staging: per epilogue warp two 32-row x 128-byte buffers for bulk stores of C
@@ -337,7 +337,7 @@ struct EpiOut {
 
 // ----------------------------------------------------------------- the roles --
 
-template <int BN, int CG, int MC, int KD>
+template <int BN, int CG, int MC, int EB, int KD>
 __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CUtensorMap* map_q,
                                               const TcArgs& a, uint8_t* ring_a, uint8_t* ring_b,
                                               TcCtrl* ctrl, uint32_t rank, int first, int stride) {
@@ -347,7 +347,11 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
   const uint32_t leader = static_cast<uint32_t>(pair * CG);
   // multicast of P: this CTA and the CTA of the other pair with the same rank inside its pair
   const uint16_t p_mask = static_cast<uint16_t>((1u << q) | (1u << (q + CG)));
-  const int kslices = (a.K + kBK - 1) / kBK;
+  constexpr int kSliceK = slice_k(EB);  // k elements of one 128-byte slice
+  // 8-bit operands are always K-major (the planner admits no other layout)
+  const bool p_kmajor = EB == 1 || a.p_kmajor != 0;
+  const bool q_kmajor = EB == 1 || a.q_kmajor != 0;
+  const int kslices = (a.K + kSliceK - 1) / kSliceK;
   int stage = 0;
   uint32_t phase = 0;
   uint32_t pending = 0, pending_parity = 0;  // copies in flight, per stage
@@ -391,20 +395,20 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
             const int slot = stage * KD + t;  // ring slot of one k-slice
             const uint32_t sa = smem_u32(ring_a + slot * Cfg::kABytes);
             const uint32_t sb = smem_u32(ring_b + slot * Cfg::kBBytes);
-            const int k0 = (ks0 + t) * kBK;
+            const int k0 = (ks0 + t) * kSliceK;
             if constexpr (MC == 2) {
               // this pair's half of the P tile: 64 rows (K-major) or one 64-wide atom (M-major)
-              if (a.p_kmajor)
+              if (p_kmajor)
                 load_mc(sa + pair * 64 * 128, map_p, k0, i0 + 64 * pair);
               else
                 load_mc(sa + pair * kMnAtomBytes, map_p, i0 + 64 * pair, k0);
-            } else if (a.p_kmajor) {
+            } else if (p_kmajor) {
               load(sa, map_p, k0, i0);
             } else {
               load(sa, map_p, i0, k0);
               load(sa + kMnAtomBytes, map_p, i0 + 64, k0);
             }
-            if (a.q_kmajor) {
+            if (q_kmajor) {
               load(sb, map_q, k0, j0);
             } else {
 #pragma unroll
@@ -435,12 +439,16 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
   __syncwarp();
 }
 
-template <int BN, int CG, int MC, int KD>
+template <int BN, int CG, int MC, int EB, int KD>
 __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8_t* ring_b,
                                          TcCtrl* ctrl, uint32_t tmem_base, uint32_t rank, int first,
                                          int stride) {
   using Cfg = TcConfig<BN, CG, MC>;
-  const int kslices = (a.K + kBK - 1) / kBK;
+  constexpr int kSliceK = slice_k(EB);  // k elements of one 128-byte slice
+  // 8-bit operands are always K-major (the planner admits no other layout)
+  const bool p_kmajor = EB == 1 || a.p_kmajor != 0;
+  const bool q_kmajor = EB == 1 || a.q_kmajor != 0;
+  const int kslices = (a.K + kSliceK - 1) / kSliceK;
   int stage = 0;
   uint32_t phase = 0;
   int it = 0;
@@ -483,20 +491,20 @@ __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8
       // 128-byte row; 8-row groups are 1024 bytes apart.
       // MN-major: the k-slice is 16 rows of 128 bytes further on; 8-row groups are
       // 1024 bytes apart and swizzle atoms along M / N are kMnAtomBytes apart.
-      const uint32_t a_step = a.p_kmajor ? 32u : 2048u;
-      const uint32_t b_step = a.q_kmajor ? 32u : 2048u;
+      const uint32_t a_step = p_kmajor ? 32u : 2048u;
+      const uint32_t b_step = q_kmajor ? 32u : 2048u;
       if (elect_one()) {
 #pragma unroll
         for (int t = 0; t < KD; ++t) {
           if (t == nks) break;
           const int slot = stage * KD + t;
           const uint64_t ad0 =
-              smem_desc_sw128(smem_u32(ring_a + slot * Cfg::kABytes), a.p_kmajor ? 16u : kMnAtomBytes, 1024);
+              smem_desc_sw128(smem_u32(ring_a + slot * Cfg::kABytes), p_kmajor ? 16u : kMnAtomBytes, 1024);
           const uint64_t bd0 =
-              smem_desc_sw128(smem_u32(ring_b + slot * Cfg::kBBytes), a.q_kmajor ? 16u : kMnAtomBytes, 1024);
+              smem_desc_sw128(smem_u32(ring_b + slot * Cfg::kBBytes), q_kmajor ? 16u : kMnAtomBytes, 1024);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)  // the start address sits in the descriptor's low bits
-            mma_f16_ss<CG>(d_tmem, ad0 + ((a_step * k) >> 4), bd0 + ((b_step * k) >> 4), a.idesc,
+          for (int k = 0; k < kSliceBytes / 32; ++k)  // the start address sits in the descriptor's low bits
+            mma_ss<CG, EB>(d_tmem, ad0 + ((a_step * k) >> 4), bd0 + ((b_step * k) >> 4), a.idesc,
                            (kb > w.kb0 || t > 0 || k > 0) ? 1u : 0u);
         }
         commit_stage(smem_u32(&ctrl->empty[stage]));  // frees the stage once these MMAs have read it
@@ -638,7 +646,7 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
   out.finish();  // every bulk store has read its staging buffer before the CTA can exit
 }
 
-template <int BN, int CG, int MC>
+template <int BN, int CG, int MC, int EB>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p,
                    const __grid_constant__ CUtensorMap map_q,
@@ -700,15 +708,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the one-slice loop compiles to the same straight-line issue code as
     // before two-slice stages existed (a runtime trip count cost ~12% at 4096^3)
     if (a.kdepth == 2)
-      producer_role<BN, CG, MC, 2>(&map_p, &map_q, a, ring_a, ring_b, ctrl, rank, first, stride);
+      producer_role<BN, CG, MC, EB, 2>(&map_p, &map_q, a, ring_a, ring_b, ctrl, rank, first, stride);
     else
-      producer_role<BN, CG, MC, 1>(&map_p, &map_q, a, ring_a, ring_b, ctrl, rank, first, stride);
+      producer_role<BN, CG, MC, EB, 1>(&map_p, &map_q, a, ring_a, ring_b, ctrl, rank, first, stride);
   } else if (warp == 1) {
     if (rank % CG == 0) {
       if (a.kdepth == 2)
-        mma_role<BN, CG, MC, 2>(a, ring_a, ring_b, ctrl, tmem_base, rank, first, stride);
+        mma_role<BN, CG, MC, EB, 2>(a, ring_a, ring_b, ctrl, tmem_base, rank, first, stride);
       else
-        mma_role<BN, CG, MC, 1>(a, ring_a, ring_b, ctrl, tmem_base, rank, first, stride);
+        mma_role<BN, CG, MC, EB, 1>(a, ring_a, ring_b, ctrl, tmem_base, rank, first, stride);
     }
   } else {
     epilogue_role<BN, CG, MC>(a, &map_c, staging, ring_a, ctrl, tmem_base, warp, lane, rank, first,

@@ -1,5 +1,7 @@
-// Tile width 128, CTA group 1, 1 CTA pair(s) sharing P by multicast.
+// Tile width 128, CTA group 1, one CTA per tile;
+// 16-bit inputs (tcgen05.mma kind::f16).
 #define TC_BN 128
 #define TC_CG 1
 #define TC_MC 1
+#define TC_EB 2
 #include "tc_gemm_inst.cuh"

@@ -1,16 +1,17 @@
 // tc_gemm_inst.cuh -- one instantiation of the tcgen05 GEMM kernel per
-// translation unit (TC_BN, TC_CG and TC_MC set by the including file), so the
-// tile configurations compile in parallel.
+// translation unit (TC_BN, TC_CG, TC_MC and TC_EB set by the including file),
+// so the tile configurations compile in parallel.
 #include "tc_gemm.cuh"
 
-#define TC_CAT6(a, b, c, d, e, f) a##b##c##d##e##f
-#define TC_NAME(a, b, c, d, e, f) TC_CAT6(a, b, c, d, e, f)
+#define TC_CAT8(a, b, c, d, e, f, g, h) a##b##c##d##e##f##g##h
+#define TC_NAME(a, b, c, d, e, f, g, h) TC_CAT8(a, b, c, d, e, f, g, h)
+#define TC_KERNEL tc_gemm_kernel<TC_BN, TC_CG, TC_MC, TC_EB>
 
 namespace g10 {
 
-cudaError_t TC_NAME(tc_prepare_bn, TC_BN, _cg, TC_CG, _mc, TC_MC)(int* max_clusters) {
+cudaError_t TC_NAME(tc_prepare_bn, TC_BN, _cg, TC_CG, _mc, TC_MC, _eb, TC_EB)(int* max_clusters) {
   using Cfg = TcConfig<TC_BN, TC_CG, TC_MC>;
-  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<TC_BN, TC_CG, TC_MC>,
+  cudaError_t e = cudaFuncSetAttribute(TC_KERNEL,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(Cfg::kSmemBytes));
   if (e != cudaSuccess || TC_CG * TC_MC == 1) return e;
@@ -26,17 +27,16 @@ cudaError_t TC_NAME(tc_prepare_bn, TC_BN, _cg, TC_CG, _mc, TC_MC)(int* max_clust
   cfg.dynamicSmemBytes = Cfg::kSmemBytes;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(max_clusters, tc_gemm_kernel<TC_BN, TC_CG, TC_MC>, &cfg);
+  return cudaOccupancyMaxActiveClusters(max_clusters, TC_KERNEL, &cfg);
 }
 
-cudaError_t TC_NAME(tc_launch_bn, TC_BN, _cg, TC_CG, _mc, TC_MC)(const CUtensorMap& map_p,
-                                                     const CUtensorMap& map_q,
-                                                     const CUtensorMap& map_c, const TcArgs& args,
-                                                     int grid, cudaStream_t stream) {
+cudaError_t TC_NAME(tc_launch_bn, TC_BN, _cg, TC_CG, _mc, TC_MC, _eb, TC_EB)(
+    const CUtensorMap& map_p, const CUtensorMap& map_q, const CUtensorMap& map_c, const TcArgs& args,
+    int grid, cudaStream_t stream) {
   using Cfg = TcConfig<TC_BN, TC_CG, TC_MC>;
   const size_t smem = args.tma_store ? Cfg::kSmemBytes : Cfg::kSmemNoStaging;
   if (TC_CG * TC_MC == 1) {
-    tc_gemm_kernel<TC_BN, TC_CG, TC_MC><<<grid, kThreads, smem, stream>>>(map_p, map_q, map_c, args);
+    TC_KERNEL<<<grid, kThreads, smem, stream>>>(map_p, map_q, map_c, args);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -51,7 +51,7 @@ cudaError_t TC_NAME(tc_launch_bn, TC_BN, _cg, TC_CG, _mc, TC_MC)(const CUtensorM
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<TC_BN, TC_CG, TC_MC>, map_p, map_q, map_c, args);
+  return cudaLaunchKernelEx(&cfg, TC_KERNEL, map_p, map_q, map_c, args);
 }
 
 }  // namespace g10

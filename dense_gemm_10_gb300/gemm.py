@@ -13,6 +13,17 @@ LIB_PATH = os.path.join(HERE, "libgemm_gb300.so")
 
 OP_N, OP_T = 0, 1
 BF16_F32, BF16_BF16, F16_F32, F16_F16 = 0, 1, 2, 3
+_FP8_FORMATS = ("e4m3", "e5m2")
+_C_TYPES = ("f32", "bf16", "f16")
+
+
+def fp8_dtype(a="e4m3", b="e4m3", c="f32"):
+    """gemm_dtype_t code for 8-bit inputs: 16 + (A E5M2) + 2 (B E5M2) + 4 (C type)."""
+    return 16 + _FP8_FORMATS.index(a) + 2 * _FP8_FORMATS.index(b) + 4 * _C_TYPES.index(c)
+
+
+E4M3_F32, E5M2_F32, E4M3_BF16, E5M2_BF16 = fp8_dtype(), fp8_dtype("e5m2", "e5m2"), fp8_dtype(c="bf16"), \
+    fp8_dtype("e5m2", "e5m2", "bf16")
 STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED", 3: "GEMM_ERR_NO_DEVICE",
           4: "GEMM_ERR_CUDA", 5: "GEMM_ERR_TENSORMAP", 6: "GEMM_ERR_TIMEOUT", 7: "GEMM_ERR_WORKSPACE"}
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NO_DEVICE, ERR_CUDA, ERR_TENSORMAP, ERR_TIMEOUT, ERR_WORKSPACE = range(8)
@@ -154,13 +165,19 @@ def default_handle(device=None):
     return h
 
 
-def dtype_code(in_dtype, out_dtype):
+def dtype_code(in_dtype, out_dtype, b_dtype=None):
+    """gemm_dtype_t code for torch dtypes of A (and B, default the same) and C."""
     import torch
+    b_dtype = in_dtype if b_dtype is None else b_dtype
     table = {(torch.bfloat16, torch.float32): BF16_F32, (torch.bfloat16, torch.bfloat16): BF16_BF16,
              (torch.float16, torch.float32): F16_F32, (torch.float16, torch.float16): F16_F16}
-    if (in_dtype, out_dtype) not in table:
-        raise TypeError("unsupported dtype pair %s -> %s" % (in_dtype, out_dtype))
-    return table[(in_dtype, out_dtype)]
+    if b_dtype == in_dtype and (in_dtype, out_dtype) in table:
+        return table[(in_dtype, out_dtype)]
+    f8 = {torch.float8_e4m3fn: "e4m3", torch.float8_e5m2: "e5m2"}
+    cty = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}
+    if in_dtype in f8 and b_dtype in f8 and out_dtype in cty:
+        return fp8_dtype(f8[in_dtype], f8[b_dtype], cty[out_dtype])
+    raise TypeError("unsupported dtypes %s x %s -> %s" % (in_dtype, b_dtype, out_dtype))
 
 
 def _ld(t, name):
@@ -183,9 +200,7 @@ def gemm(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0, handle=None, 
     M = M if M is not None else (A.shape[1] if ta else A.shape[0])
     K = K if K is not None else (A.shape[0] if ta else A.shape[1])
     N = N if N is not None else (B.shape[0] if tb else B.shape[1])
-    if A.dtype != B.dtype:
-        raise TypeError("A and B must have the same dtype")
-    code = dtype_code(A.dtype, C.dtype)
+    code = dtype_code(A.dtype, C.dtype, B.dtype)
     h = handle if handle is not None else default_handle(C.device.index)
     if stream is None:
         stream = torch.cuda.current_stream(C.device).cuda_stream

@@ -8,7 +8,7 @@ when beta != 0 (the blend needs its old value).  The arithmetic intensity is
 their ratio.
 """
 
-ELEM_BYTES = {"bf16": 2, "f16": 2, "f32": 4}
+ELEM_BYTES = {"bf16": 2, "f16": 2, "f32": 4, "e4m3": 1, "e5m2": 1}
 
 
 def flops(M, N, K):

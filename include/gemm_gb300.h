@@ -7,7 +7,8 @@
  * floating-point operations.  This is the GEMM of "CUDA GEMM 矩阵乘法优化指南"
  * (blog.zhenwei.site), section 2.1, with the op / alpha / beta calling shape of
  * the cuBLAS call in "第4章：经典算子实现 —— GEMM" (aiinfra.vidrealm.tech),
- * section 7.1.  Inputs are bf16 or fp16, products are accumulated in fp32 on
+ * section 7.1.  Inputs are bf16, fp16 or 8-bit floats (E4M3 / E5M2; see
+ * gemm_dtype_t), products are accumulated in fp32 on
  * the tensor cores (tcgen05.mma into Tensor Memory), and alpha / beta are
  * applied in fp32 before the result is rounded (round-to-nearest-even) to the
  * type of C.
@@ -37,18 +38,46 @@ typedef struct gemm_handle_s* gemm_handle_t;
 
 typedef enum { GEMM_OP_N = 0, GEMM_OP_T = 1 } gemm_op_t;
 
-/* Input type -> type of C.  Accumulation is fp32 in every case. */
+/*
+ * Input types -> type of C.  Accumulation is fp32 in every case.
+ *
+ * The 8-bit float inputs are the tensor core's FP8 formats ("CUDA GEMM
+ * 矩阵乘法优化指南", section 13.2: E4M3 / E5M2, issued as tcgen05.mma
+ * kind::f8f6f4 with 32 products of k per instruction), in the OCP 8-bit
+ * layouts: E4M3 = sign, 4-bit exponent (bias 7), 3-bit fraction, no
+ * infinities, largest value 448; E5M2 = sign, 5-bit exponent (bias 15),
+ * 2-bit fraction, IEEE-style infinities and NaNs.  A and B may differ.  With
+ * 8-bit inputs both operands must be K-major (transA == GEMM_OP_N and
+ * transB == GEMM_OP_T: A stored M x K, B stored N x K, the usual layout of
+ * FP8 weights); other layouts return GEMM_ERR_UNSUPPORTED.  Leading dimensions
+ * are in elements (= bytes); the code is 16 + (A is E5M2) + 2 * (B is E5M2) +
+ * 4 * (0 for fp32 C, 1 for bf16 C, 2 for fp16 C).  Per-tensor scale factors of
+ * FP8 data fold into alpha.
+ */
 typedef enum {
   GEMM_BF16_F32 = 0,  /* A, B bf16; C fp32 */
   GEMM_BF16_BF16 = 1, /* A, B bf16; C bf16 */
   GEMM_F16_F32 = 2,   /* A, B fp16; C fp32 */
-  GEMM_F16_F16 = 3    /* A, B fp16; C fp16 */
+  GEMM_F16_F16 = 3,   /* A, B fp16; C fp16 */
+  GEMM_E4M3_F32 = 16,        /* A, B E4M3; C fp32 */
+  GEMM_E5M2_E4M3_F32 = 17,   /* A E5M2, B E4M3; C fp32 */
+  GEMM_E4M3_E5M2_F32 = 18,   /* A E4M3, B E5M2; C fp32 */
+  GEMM_E5M2_F32 = 19,        /* A, B E5M2; C fp32 */
+  GEMM_E4M3_BF16 = 20,       /* ... the same pairs with bf16 C */
+  GEMM_E5M2_E4M3_BF16 = 21,
+  GEMM_E4M3_E5M2_BF16 = 22,
+  GEMM_E5M2_BF16 = 23,
+  GEMM_E4M3_F16 = 24,        /* ... and with fp16 C */
+  GEMM_E5M2_E4M3_F16 = 25,
+  GEMM_E4M3_E5M2_F16 = 26,
+  GEMM_E5M2_F16 = 27
 } gemm_dtype_t;
 
 typedef enum {
   GEMM_OK = 0,
   GEMM_ERR_INVALID_ARG = 1, /* null pointer, negative size, leading dimension too small, bad enum */
-  GEMM_ERR_UNSUPPORTED = 2, /* a size the library cannot index (an extent >= 2^31) */
+  GEMM_ERR_UNSUPPORTED = 2, /* a size the library cannot index (an extent >= 2^31), or an
+                               8-bit input layout other than A M x K, B N x K */
   GEMM_ERR_NO_DEVICE = 3,   /* the device is absent or is not sm_103 */
   GEMM_ERR_CUDA = 4,        /* a CUDA runtime call failed; gemm_last_cuda_error() tells which */
   GEMM_ERR_TENSORMAP = 5,   /* cuTensorMapEncodeTiled refused an operand description */
@@ -74,7 +103,7 @@ gemm_status_t gemm_create(gemm_handle_t* out, int device);
  *                   K == 0 sets C = beta * C (C = 0 when beta == 0).
  *   alpha, beta     fp32 scalars, read on the host.  When beta == 0, C is not
  *                   read, so C may hold anything (NaN included) on entry.
- *   A, B, C         caller-owned device pointers, bf16 / fp16 / fp32 per `dtype`.
+ *   A, B, C         caller-owned device pointers, of the types `dtype` names.
  *                   A and B are read only; C is read (beta != 0) and written.
  *                   C must not overlap A or B.
  *   lda, ldb, ldc   leading dimensions in elements, per the layouts above.

@@ -8,10 +8,13 @@ from dense_gemm_10_gb300 import gemm as G
 from dense_gemm_10_gb300 import inputs
 
 _TORCH = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+_ORACLE_IN = {"bf16": oracle.IN_BF16, "f16": oracle.IN_F16, "e4m3": oracle.IN_E4M3, "e5m2": oracle.IN_E5M2}
 SENTINEL = 1536.0   # exact in fp32, bf16 and fp16
 
 
 def dtype_code(p):
+    if p.in_dtype in inputs.FP8:
+        return G.fp8_dtype(p.in_dtype, p.b_dtype, p.out_dtype)
     return {("bf16", "f32"): G.BF16_F32, ("bf16", "bf16"): G.BF16_BF16, ("f16", "f32"): G.F16_F32,
             ("f16", "f16"): G.F16_F16}[(p.in_dtype, p.out_dtype)]
 
@@ -58,17 +61,16 @@ def _c0_for_oracle(p):
 
 def oracle_full(p, nthreads=0):
     c0, ct = _c0_for_oracle(p)
-    in_type = oracle.IN_BF16 if p.in_dtype == "bf16" else oracle.IN_F16
     return oracle.gemm(p.transA, p.transB, p.M, p.N, p.K, p.alpha, inputs.bits(p.A), p.lda, inputs.bits(p.B),
-                       p.ldb, p.beta, c0, p.ldc, in_type, c_type=ct, nthreads=nthreads)
+                       p.ldb, p.beta, c0, p.ldc, _ORACLE_IN[p.in_dtype], c_type=ct, nthreads=nthreads,
+                       b_type=_ORACLE_IN[p.b_dtype])
 
 
 def oracle_at(p, rows, cols, nthreads=0):
     c0, ct = _c0_for_oracle(p)
-    in_type = oracle.IN_BF16 if p.in_dtype == "bf16" else oracle.IN_F16
     return oracle.gemm_at(p.transA, p.transB, p.M, p.N, p.K, p.alpha, inputs.bits(p.A), p.lda,
-                          inputs.bits(p.B), p.ldb, p.beta, c0, p.ldc, in_type, rows, cols, c_type=ct,
-                          nthreads=nthreads)
+                          inputs.bits(p.B), p.ldb, p.beta, c0, p.ldc, _ORACLE_IN[p.in_dtype], rows, cols,
+                          c_type=ct, nthreads=nthreads, b_type=_ORACLE_IN[p.b_dtype])
 
 
 def assert_close(out, r, m, out_is_f32, what=""):

@@ -137,6 +137,28 @@ def test_plan_bulk_store_paths():
     assert G.plan(40, 1001, 256, 0, 1, G.BF16_BF16, ldc=1008).bulk_store == G.BULK_NONE
 
 
+def test_plan_fp8():
+    """8-bit inputs: 128-element k-slices (one 128-byte swizzle row), the 8-bit
+    tile configurations, rows aligned to 16 elements, and K-major operands only."""
+    p = G.plan(4096, 4096, 4096, 0, 1, G.E4M3_F32)
+    assert p.path == G.PATH_TC_2CTA and p.bn == 256 and p.bk == 128 and p.num_kb == 32
+    s = G.plan(64, 32000, 4096, 0, 1, G.fp8_dtype("e4m3", "e5m2", "bf16"))
+    assert s.swap_ab == 1 and s.bn == 64 and s.kdepth == 2 and s.bk == 256 and s.bulk_store == G.BULK_TRANSPOSED
+    assert G.plan(300, 520, 301, 0, 1, G.E5M2_F32, lda=304, ldb=320).repack_a == 0
+    r = G.plan(300, 520, 301, 0, 1, G.E5M2_F32, lda=305, ldb=320)
+    assert r.repack_a == 1 and r.repack_b == 0 and r.workspace_bytes >= 300 * 304   # rows padded to 16 bytes
+    for ta, tb in [(0, 0), (1, 0), (1, 1)]:
+        with pytest.raises(G.GemmError) as e:
+            G.plan(256, 256, 256, ta, tb, G.E4M3_F32)
+        assert e.value.status == G.ERR_UNSUPPORTED
+    for bad in (4, 15, 28):
+        with pytest.raises(G.GemmError) as e:
+            G.plan(256, 256, 256, 0, 1, bad)
+        assert e.value.status == G.ERR_INVALID_ARG
+    assert [G.fp8_dtype(a, b, c) for c in ("f32", "bf16", "f16") for b in ("e4m3", "e5m2")
+            for a in ("e4m3", "e5m2")] == list(range(16, 28))
+
+
 def test_plan_half_atom_pairs_need_k_major_q():
     """A CTA pair with 64-wide tiles loads 32-row halves of the MMA's B operand,
     which only the K-major layout allows."""
