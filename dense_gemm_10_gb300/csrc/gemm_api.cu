@@ -177,14 +177,20 @@ int64_t count_units(const Sched& s) {
 // Estimated time, in k-blocks of one tile, of the stream-K tail: `iters`
 // k-blocks of `tiles` tiles dealt to `g` slots.  Each partial piece costs a
 // store, and the tile's last contribution reads every piece of its tile.
-double sk_tail_cost(int64_t tiles, int64_t num_kb, int64_t g) {
+// Time of a stream-K tail in k-blocks (one k-block = one ring stage of operand
+// bytes per CTA).  Besides its share of the k-blocks, the slot that finishes a
+// tile writes its fp32 partial and then reads every contribution back, and
+// those bytes travel the same per-SM path as its operand loads: r k-blocks for
+// the write and, measured on GB300 (4096^3 bf16 and 8-bit), ~1.5 r per
+// contribution read.  r = a CTA's fp32 partial tile in stages of operand bytes.
+double sk_tail_cost(int64_t tiles, int64_t num_kb, int64_t g, double r) {
   const int64_t iters = tiles * num_kb;
   const double per_slot = static_cast<double>(cdiv(iters, g));
   if (g <= tiles && tiles % g == 0) return per_slot;  // whole tiles, no partials
   const double contrib = per_slot >= static_cast<double>(num_kb)
                              ? 2.0
                              : std::ceil(static_cast<double>(num_kb) / per_slot) + 1.0;
-  return per_slot + 1.0 + 0.5 * contrib;
+  return per_slot + r * (1.0 + 1.5 * contrib);
 }
 
 // num_kb counts stages of kdepth 64-wide k-slices each.
@@ -200,6 +206,9 @@ Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64
   ch.mc = tc.mc;
   ch.slots = slots;
   const int64_t tiles = tiles_i * tiles_j;
+  // a CTA's fp32 partial tile (bn x 128) in stages of its operand bytes
+  const double stage_bytes = static_cast<double>(kdepth) * (kBM + tc.bn / tc.cg) * kSliceBytes;
+  const double r = 4.0 * tc.bn * kBM / stage_bytes;
   Sched& s = ch.sched;
   s.tiles_i = static_cast<int32_t>(tiles_i);
   s.tiles_j = static_cast<int32_t>(tiles_j);
@@ -212,7 +221,8 @@ Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64
     if (tiles * cl > kCounterCap) return ch;
     s.split_k = static_cast<int32_t>(split);
     ch.cost = static_cast<double>(cdiv(tiles * split, slots)) *
-              (static_cast<double>(cdiv(num_kb, split)) + (split > 1 ? 1.5 : 0.0)) * kdepth * tile_kb_cost(tc);
+              (static_cast<double>(cdiv(num_kb, split)) + (split > 1 ? r * (1.0 + 1.5) : 0.0)) * kdepth *
+              tile_kb_cost(tc);
     ch.valid = true;
     return ch;
   }
@@ -233,7 +243,12 @@ Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64
     int64_t best_g = 0;
     double best_tail = 1e300;
     for (int64_t g = 1; g <= std::min<int64_t>(slots, iters); ++g) {
-      const double t = sk_tail_cost(sk_tiles, num_kb, g);
+      // After full waves, a tail whose share per slot exceeds half a tile is
+      // mostly whole-tile work already; its partial sums and the tail tiles'
+      // out-of-raster operand reads cost more than the quantisation saves
+      // (measured at 8192 x 4096 x 16384).
+      if (full_waves > 0 && 2 * cdiv(iters, g) > num_kb) continue;
+      const double t = sk_tail_cost(sk_tiles, num_kb, g, r);
       if (t < best_tail - 1e-9) {
         best_tail = t;
         best_g = g;

@@ -541,6 +541,7 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
   const int quarter = warp & 3;  // a warp may only read TMEM lanes 32*(warp%4) .. +31
   const int row = quarter * 32 + lane;
   const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+  const float alpha = a.alpha;
   EpiOut out;
   out.c = make_cout(a);
   out.map_c = map_c;
@@ -588,15 +589,16 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
         if (c + 32 == BN) release();  // last read of this accumulator: hand it back
         float v[32];
 #pragma unroll
-        for (int t = 0; t < 32; ++t) v[t] = a.alpha * __uint_as_float(r[t]);
+        for (int t = 0; t < 32; ++t) v[t] = alpha * __uint_as_float(r[t]);
         out.put(i, jt + c, v, (c >> 5) & 1);
       }
     } else {
-      // Partial of this k-range: column-major inside the tile so that a warp's
-      // 32 rows are 128 contiguous bytes.
+      // Partial of this k-range, in groups of four columns: the float4 of row r,
+      // columns 4g .. 4g + 3 sits at index g * kBM + r, so that a warp's 32 rows
+      // are 512 contiguous bytes and every access moves 16 bytes per lane.
       const int slot = w.pslot * Cfg::kCluster + static_cast<int>(rank);
       const int ctr = w.ctr * Cfg::kCluster + static_cast<int>(rank);
-      float* part = a.partials + static_cast<size_t>(slot) * BN * kBM;
+      float4* part = reinterpret_cast<float4*>(a.partials + static_cast<size_t>(slot) * BN * kBM);
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         uint32_t r[32];
@@ -604,8 +606,10 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
         tmem_ld_wait(r);
         if (c + 32 == BN) release();
 #pragma unroll
-        for (int t = 0; t < 32; ++t)
-          __stcg(part + static_cast<size_t>(c + t) * kBM + row, __uint_as_float(r[t]));
+        for (int g = 0; g < 8; ++g)
+          __stcg(part + static_cast<size_t>((c >> 2) + g) * kBM + row,
+                 make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                             __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3])));
       }
       // One GPU-scope fence by the arriving thread, after the barrier that orders
       // every epilogue thread's partial stores before it, publishes the whole
@@ -624,21 +628,40 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
       }
       bar_sync(1, 128);
       if (*reinterpret_cast<volatile uint32_t*>(&ctrl->last)) {
+        // 64 columns per round: 16 independent 16-byte loads per contribution in
+        // flight (the sum is latency-bound, one L2 round trip per round).
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          float v[32];
+        for (int c = 0; c < BN; c += 64) {
+          float4 acc[16];
 #pragma unroll
-          for (int t = 0; t < 32; ++t) v[t] = 0.0f;
+          for (int g = 0; g < 16; ++g) acc[g] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll 1
           for (int k = 0; k < w.ncontrib; ++k) {  // fixed k order: the sum does not depend on timing
             const int ks = contrib_slot(a.sched, w, k) * Cfg::kCluster + static_cast<int>(rank);
-            const float* ps = a.partials + static_cast<size_t>(ks) * BN * kBM;
+            const float4* ps = reinterpret_cast<const float4*>(a.partials + static_cast<size_t>(ks) * BN * kBM);
+            float4 x[16];
 #pragma unroll
-            for (int t = 0; t < 32; ++t) v[t] += __ldcg(ps + static_cast<size_t>(c + t) * kBM + row);
+            for (int g = 0; g < 16; ++g) x[g] = __ldcg(ps + static_cast<size_t>((c >> 2) + g) * kBM + row);
+#pragma unroll
+            for (int g = 0; g < 16; ++g) {
+              acc[g].x += x[g].x;
+              acc[g].y += x[g].y;
+              acc[g].z += x[g].z;
+              acc[g].w += x[g].w;
+            }
           }
 #pragma unroll
-          for (int t = 0; t < 32; ++t) v[t] *= a.alpha;
-          out.put(i, jt + c, v, (c >> 5) & 1);
+          for (int h = 0; h < 2; ++h) {
+            float v[32];
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              v[4 * g] = alpha * acc[8 * h + g].x;
+              v[4 * g + 1] = alpha * acc[8 * h + g].y;
+              v[4 * g + 2] = alpha * acc[8 * h + g].z;
+              v[4 * g + 3] = alpha * acc[8 * h + g].w;
+            }
+            out.put(i, jt + c + 32 * h, v, h);
+          }
         }
       }
     }
