@@ -12,6 +12,7 @@ Also reported, in the same line:
                 host<->device copies inside the timed region
   cpu_baseline  the CPU oracle (plain fp64 triple loop) on a bounded sample
   skinny        the LM-head GEMM (M = 64, K = 4096, N = 32000) in GB/s
+  fp8           the 4096^3 GEMM with 8-bit E4M3 inputs in TFLOP/s
   clocks        SM clocks and throttle reasons sampled during the timed region
 
 `--impl reference` times the CPU oracle instead (the reference arm).
@@ -48,6 +49,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-skinny", action="store_true")
+    ap.add_argument("--fp8-steps", type=int, default=4000)
+    ap.add_argument("--no-fp8", action="store_true")
     return ap.parse_args()
 
 
@@ -334,6 +337,9 @@ def run_ours(args):
     skinny = None
     if not args.no_skinny:
         skinny = run_skinny(args, G, h, inputs, metrics, dev, stream, pk, pk_src)
+    fp8 = None
+    if not args.no_fp8:
+        fp8 = run_fp8(args, G, h, inputs, metrics, dev, stream, pk, pk_src)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -353,13 +359,60 @@ def run_ours(args):
                        "plan": plan.as_dict(), "parallelism": "replicas" if ws > 1 else "single GPU",
                        "wall_s_timed_region": wall},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clk, "skinny": skinny,
+            "clocks": clk, "skinny": skinny, "fp8": fp8,
         }
         print(json.dumps(line), flush=True)
     h.close()
     if ws > 1:
         dist.destroy_process_group()
     return 0
+
+
+def run_fp8(args, G, h, inputs, metrics, dev, stream, pk, pk_src):
+    """4096^3 with 8-bit E4M3 inputs (A M x K, B N x K), fp32 C: TFLOP/s against
+    the measured bf16 burst peak scaled by the nominal FP8 / bf16 ratio (2)."""
+    import torch
+    p = inputs.square_4096_fp8_nt("e4m3", "f32", SIZE)
+    code = G.fp8_dtype("e4m3", "e4m3", "f32")
+    set_bytes = p.A.numel() + p.B.numel() + p.M * p.N * 4
+    n_sets = max(2, math.ceil(2 * L2_BYTES / set_bytes) + 1)
+    sets = [(p.A.to(dev), p.B.to(dev), torch.empty(p.M, p.N, dtype=torch.float32, device=dev))
+            for _ in range(n_sets)]
+    plan = G.plan(p.M, p.N, p.K, p.transA, p.transB, code)
+    sptr = stream.cuda_stream
+
+    def step(i):
+        A, B, C = sets[i % n_sets]
+        st = h.run_raw(p.transA, p.transB, p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb,
+                       0.0, C.data_ptr(), p.N, code, sptr)
+        if st != G.OK:
+            raise G.GemmError(st, "gemm_run")
+
+    with torch.cuda.stream(stream):
+        for i in range(20):
+            step(i)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.fp8_steps):
+            step(i)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    st, word = h.status(sptr)
+    if st != G.OK:
+        raise RuntimeError("fp8 kernel status %s (0x%x)" % (G.STATUS.get(st), word))
+    ms = e0.elapsed_time(e1) / args.fp8_steps
+    tflops = metrics.flops(p.M, p.N, p.K) / (ms / 1e3) / 1e12
+    peak = 2.0 * float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    cg = plan.bm // 128
+    return {"workload": "square_4096_e4m3_nt_f32", "value": tflops, "unit": "TFLOP/s", "us_per_call": ms * 1e3,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tflops / peak, "frac_of_nominal_4500": tflops / 4500.0,
+                         "peak_source": "%s bf16_tflops x 2 (nominal FP8 / bf16 dense ratio 4.5 / 2.25)" % pk_src,
+                         "traffic": recorded_traffic("tc_gemm_kernel<%d,%d,e4m3>:square_4096_e4m3_nt_f32"
+                                                     % (plan.bn, cg))},
+            "plan": plan.as_dict(), "l2": "%d rotating input sets (%.0f MB total)" % (
+                n_sets, n_sets * set_bytes / 2 ** 20)}
 
 
 def run_skinny(args, G, h, inputs, metrics, dev, stream, pk, pk_src):
