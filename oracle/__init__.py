@@ -59,6 +59,8 @@ def _load():
     lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
     lib.oracle_f16_value.restype = dbl
     lib.oracle_f16_value.argtypes = [ctypes.c_uint16]
+    lib.oracle_epilogue.restype = i32
+    lib.oracle_epilogue.argtypes = [i64, i64, vp, vp, i64, vp, i32, dbl]
     lib.oracle_e4m3_value.restype = dbl
     lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
     lib.oracle_e5m2_value.restype = dbl
@@ -156,15 +158,44 @@ def gemm_at(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc, in_ty
     return r, m
 
 
-def within_tolerance(out, r, m, out_is_f32):
+ACT_NONE, ACT_RELU, ACT_GELU = 0, 1, 2
+E4M3_MAX = 448.0
+
+
+def epilogue(R, Mag, bias=None, act=ACT_NONE, scale=1.0):
+    """The fused epilogue applied to a full oracle result (see oracle_epilogue in
+    gemm_oracle.c): out = scale * act(r + bias_j), with the magnitude carried
+    through the same steps.  Returns new arrays."""
+    R = np.array(R, dtype=np.float64, order="C", copy=True)
+    Mag = np.array(Mag, dtype=np.float64, order="C", copy=True)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    if b is not None and b.shape != (R.shape[1],):
+        raise ValueError("bias must hold one value per column")
+    rc = _load().oracle_epilogue(R.shape[0], R.shape[1], _ptr(R), _ptr(Mag), R.shape[1], _ptr(b), int(act),
+                                 float(scale))
+    if rc != 0:
+        raise ValueError("oracle_epilogue rejected its arguments")
+    return R, Mag
+
+
+def within_tolerance(out, r, m, out_is_f32, e4m3=False):
     """Elementwise comparison rule for a GPU result ``out`` against (r, m).
 
     fp32 output:       |out - r| <= 1e-3 * m + 1e-5
     bf16 / fp16 output: |out - r| <= 8e-3 * |r| + 1e-3 * m + 1e-5
+    E4M3 output (e4m3=True): r saturates at +-448 first (the format's largest
+    value), then |out - r| <= 2^-4 * |r| + 1e-3 * m + 2^-10 (half a unit in the
+    last of E4M3's 3 fraction bits, and half its smallest subnormal).
     A NaN or Inf in ``out`` where r is finite fails.
     Returns a boolean array (True = within tolerance).
     """
     out = np.asarray(out, dtype=np.float64)
+    if e4m3:
+        r = np.clip(r, -E4M3_MAX, E4M3_MAX)
+        bound = 2.0 ** -4 * np.abs(r) + 1e-3 * m + 2.0 ** -10
+        ok = np.abs(out - r) <= bound
+        ok &= np.isfinite(out) | ~np.isfinite(r)
+        return ok
     err = np.abs(out - r)
     bound = 1e-3 * m + 1e-5
     if not out_is_f32:

@@ -297,3 +297,40 @@ int oracle_gemm_at(int transA, int transB, int64_t M, int64_t N, int64_t K, doub
   return oracle_gemm_at_ab(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C0, c_type, ldc,
                            in_type, in_type, count, rows, cols, R, Mag, nthreads);
 }
+
+/*
+ * Fused epilogue, applied in place to R / Mag produced by oracle_gemm (M x N,
+ * leading dimension ldr).  The pages name the operations fused into a GEMM's
+ * write-back: "第4章：经典算子实现 —— GEMM", section 7.2 (GEMM + bias +
+ * activation) and "GPU GEMM 优化完全拆解（三）", mainloop 与 epilogue (elementwise
+ * ReLU and quantisation scaling before the store).  Written out:
+ *   z_ij   = r_ij + bias_j                    (bias: N fp32 values, or NULL)
+ *   d_ij   = act(z_ij)                        act 0: z;  1 (ReLU): max(z, 0);
+ *                                             2 (GELU): z * Phi(z) = z * (1 + erf(z / sqrt 2)) / 2
+ *   out_ij = scale * d_ij
+ * and the tolerance magnitude follows the same steps:
+ *   m'_ij  = |scale| * L * (m_ij + |bias_j|),  L = 1 (identity, ReLU) or 1.13 (GELU, whose
+ *                                             slope lies in [-0.129, 1.129]).
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_epilogue(int64_t M, int64_t N, double* R, double* Mag, int64_t ldr, const float* bias,
+                    int act, double scale) {
+  if (M < 0 || N < 0 || ldr < N || act < 0 || act > 2) return -1;
+  const double lip = act == 2 ? 1.13 : 1.0;
+  for (int64_t i = 0; i < M; ++i) {
+    for (int64_t j = 0; j < N; ++j) {
+      double z = R[i * ldr + j];
+      double m = Mag[i * ldr + j];
+      if (bias) {
+        z += (double)bias[j];
+        m += fabs((double)bias[j]);
+      }
+      double d = z;
+      if (act == 1) d = z > 0.0 ? z : 0.0;
+      if (act == 2) d = 0.5 * z * (1.0 + erf(z / sqrt(2.0)));
+      R[i * ldr + j] = scale * d;
+      Mag[i * ldr + j] = fabs(scale) * lip * m;
+    }
+  }
+  return 0;
+}

@@ -406,6 +406,52 @@ def test_thread_count_does_not_change_results():
     assert np.array_equal(R1, R7)
 
 
+# ---------------------------------------------------------------------------
+# Fused epilogue: bias, activation, output scale
+# ---------------------------------------------------------------------------
+
+def _grid(M=7, N=9, seed=1):
+    g = np.random.default_rng(seed)
+    return g.normal(0, 3, (M, N)), g.uniform(0.5, 2.0, (M, N)), g.normal(0, 1, N).astype(np.float32)
+
+
+def test_epilogue_identity_and_bias():
+    R, Mag, b = _grid()
+    R0, M0 = oracle.epilogue(R, Mag)
+    assert np.array_equal(R0, R) and np.array_equal(M0, Mag)
+    R1, M1 = oracle.epilogue(R, Mag, bias=b)
+    assert np.array_equal(R1, R + b.astype(np.float64)[None, :])       # one value per column
+    assert np.array_equal(M1, Mag + np.abs(b.astype(np.float64))[None, :])
+
+
+def test_epilogue_relu_and_scale():
+    R, Mag, b = _grid(seed=2)
+    out, m = oracle.epilogue(R, Mag, bias=b, act=oracle.ACT_RELU, scale=-0.5)
+    z = R + b.astype(np.float64)[None, :]
+    assert np.array_equal(out, -0.5 * np.where(z > 0, z, 0.0))
+    assert np.allclose(m, 0.5 * (Mag + np.abs(b)[None, :]), rtol=0, atol=1e-15)
+
+
+def test_epilogue_gelu_matches_library_and_closed_forms():
+    x = np.linspace(-8, 8, 1601)
+    R = x[None, :]
+    out, m = oracle.epilogue(R, np.ones_like(R), act=oracle.ACT_GELU)
+    ref = torch.nn.functional.gelu(torch.from_numpy(x), approximate="none").numpy()
+    assert np.allclose(out[0], ref, rtol=1e-14, atol=1e-15)
+    neg, _ = oracle.epilogue(-R, np.ones_like(R), act=oracle.ACT_GELU)
+    assert np.allclose(out[0] - neg[0], x, rtol=0, atol=1e-13)         # GELU(x) - GELU(-x) = x
+    one, _ = oracle.epilogue(np.array([[1.0, 0.0]]), np.ones((1, 2)), act=oracle.ACT_GELU)
+    assert abs(one[0, 0] - 0.8413447460685429) < 1e-15 and one[0, 1] == 0.0   # Phi(1); GELU(0) = 0
+    assert np.all(m == 1.13)                                           # the largest slope bounds the error
+
+
+def test_e4m3_output_tolerance():
+    r = np.array([1.0, 1.0, 500.0, 0.0, 0.0, 3.0])
+    m = np.zeros(6)
+    out = np.array([1.0625, 1.07, 448.0, 2 ** -10, 2 ** -9, np.nan])
+    assert list(oracle.within_tolerance(out, r, m, True, e4m3=True)) == [True, False, True, True, False, False]
+
+
 def test_tolerance_rule():
     r = np.array([1.0, 1.0, 0.0, 1.0])
     m = np.array([1.0, 1.0, 10.0, 1.0])

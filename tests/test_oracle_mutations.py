@@ -25,6 +25,10 @@ MUTATIONS = {
     "E5M2 fraction width wrong": ("1.0 + (double)f / 4.0", "1.0 + (double)f / 8.0"),
     "E5M2 subnormal scale wrong": ("(double)f / 4.0, -14)", "(double)f / 4.0, -15)"),
     "B decoded with A's type": ("in_value(J->b_type, J->B", "in_value(J->a_type, J->B"),
+    "GELU argument not divided by sqrt 2": ("erf(z / sqrt(2.0))", "erf(z)"),
+    "ReLU passes negatives": ("d = z > 0.0 ? z : 0.0;", "d = z > 0.0 ? z : -z;"),
+    "bias indexed by row": ("z += (double)bias[j];", "z += (double)bias[i % N];"),
+    "output scale dropped": ("R[i * ldr + j] = scale * d;", "R[i * ldr + j] = d;"),
 }
 
 
