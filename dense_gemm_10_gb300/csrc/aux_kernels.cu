@@ -2,13 +2,14 @@
 //  * repack: copies an operand whose rows are not 16-byte aligned into
 //    an aligned buffer, because the tensor-memory-accelerator copy engine only
 //    reads rows whose pitch is a multiple of 16 bytes;
-//  * scale_c: C = beta * C, the whole GEMM when K == 0 ("CUDA GEMM 矩阵乘法优化指南",
-//    section 2.1, with an empty sum).
+//  * scale_c: C = ops(beta * C), the whole GEMM when K == 0 ("CUDA GEMM
+//    矩阵乘法优化指南", section 2.1, with an empty sum), with the fused epilogue
+//    operations of epi_ops.cuh.
 // Both are HBM-bound grid-stride copies over a grid sized to the SM count.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#include "gemm_internal.h"
+#include "epi_ops.cuh"
 
 namespace g10 {
 
@@ -25,20 +26,26 @@ __global__ void repack_kernel(const T* __restrict__ src, int64_t lds, T* __restr
 }
 
 __global__ void scale_c_kernel(void* C, int32_t c_type, int64_t M, int64_t N, int64_t ldc,
-                               float beta) {
+                               float beta, EpiOps ops) {
+  const bool any = ops.any();
   for (int64_t r = blockIdx.y; r < M; r += gridDim.y) {
     for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < N;
          c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
       const int64_t off = r * ldc + c;
       if (c_type == kCF32) {
         float* p = static_cast<float*>(C) + off;
-        *p = beta == 0.0f ? 0.0f : beta * *p;
+        float z = beta == 0.0f ? 0.0f : beta * *p;
+        *p = any ? apply_ops(ops, z, r, c) : z;
       } else if (c_type == kCBF16) {
         __nv_bfloat16* p = static_cast<__nv_bfloat16*>(C) + off;
-        *p = __float2bfloat16_rn(beta == 0.0f ? 0.0f : beta * __bfloat162float(*p));
-      } else {
+        float z = beta == 0.0f ? 0.0f : beta * __bfloat162float(*p);
+        *p = __float2bfloat16_rn(any ? apply_ops(ops, z, r, c) : z);
+      } else if (c_type == kCF16) {
         __half* p = static_cast<__half*>(C) + off;
-        *p = __float2half_rn(beta == 0.0f ? 0.0f : beta * __half2float(*p));
+        float z = beta == 0.0f ? 0.0f : beta * __half2float(*p);
+        *p = __float2half_rn(any ? apply_ops(ops, z, r, c) : z);
+      } else {  // E4M3 output is written only (beta == 0)
+        static_cast<uint8_t*>(C)[off] = to_e4m3(any ? apply_ops(ops, 0.0f, r, c) : 0.0f);
       }
     }
   }
@@ -64,8 +71,8 @@ cudaError_t repack_launch(const void* src, int64_t lds, void* dst, int64_t ldd, 
 }
 
 cudaError_t scale_c_launch(void* C, int32_t c_type, int64_t M, int64_t N, int64_t ldc, float beta,
-                           int sm_count, cudaStream_t stream) {
-  scale_c_kernel<<<grid_2d(M, N, sm_count), 256, 0, stream>>>(C, c_type, M, N, ldc, beta);
+                           const EpiOps& ops, int sm_count, cudaStream_t stream) {
+  scale_c_kernel<<<grid_2d(M, N, sm_count), 256, 0, stream>>>(C, c_type, M, N, ldc, beta, ops);
   return cudaGetLastError();
 }
 

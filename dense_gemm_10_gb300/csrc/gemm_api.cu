@@ -88,20 +88,24 @@ struct DtypeInfo {
 
 DtypeInfo dtype_info(int dtype) {
   DtypeInfo d;
-  if (dtype >= GEMM_BF16_F32 && dtype <= GEMM_F16_F16) {
-    const bool bf16 = dtype == GEMM_BF16_F32 || dtype == GEMM_BF16_BF16;
+  if (dtype >= GEMM_BF16_F32 && dtype <= GEMM_F16_E4M3) {
+    const bool bf16 = dtype == GEMM_BF16_F32 || dtype == GEMM_BF16_BF16 || dtype == GEMM_BF16_E4M3;
     d.valid = true;
     d.a_fmt = d.b_fmt = bf16 ? 1u : 0u;
-    d.c_type = (dtype == GEMM_BF16_F32 || dtype == GEMM_F16_F32) ? kCF32 : bf16 ? kCBF16 : kCF16;
+    d.c_type = (dtype == GEMM_BF16_F32 || dtype == GEMM_F16_F32)    ? kCF32
+               : (dtype == GEMM_BF16_E4M3 || dtype == GEMM_F16_E4M3) ? kCE4M3
+               : bf16                                              ? kCBF16
+                                                                   : kCF16;
     d.map_type = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  } else if (dtype >= GEMM_E4M3_F32 && dtype <= GEMM_E5M2_F16) {
-    // 16 + (A is E5M2) + 2 * (B is E5M2) + 4 * (C: 0 fp32, 1 bf16, 2 fp16)
+  } else if (dtype >= GEMM_E4M3_F32 && dtype <= GEMM_E5M2_E4M3OUT) {
+    // 16 + (A is E5M2) + 2 * (B is E5M2) + 4 * (C: 0 fp32, 1 bf16, 2 fp16, 3 E4M3)
     const int x = dtype - GEMM_E4M3_F32;
+    static const int32_t kC[4] = {kCF32, kCBF16, kCF16, kCE4M3};
     d.valid = true;
     d.eb = 1;
     d.a_fmt = x & 1;
     d.b_fmt = (x >> 1) & 1;
-    d.c_type = x >> 2 == 0 ? kCF32 : x >> 2 == 1 ? kCBF16 : kCF16;
+    d.c_type = kC[x >> 2];
     d.map_type = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   }
   return d;
@@ -247,7 +251,7 @@ Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64
       // mostly whole-tile work already; its partial sums and the tail tiles'
       // out-of-raster operand reads cost more than the quantisation saves
       // (measured at 8192 x 4096 x 16384).
-      if (full_waves > 0 && 2 * cdiv(iters, g) > num_kb) continue;
+      if (o.stream_k != 2 && full_waves > 0 && 2 * cdiv(iters, g) > num_kb) continue;
       const double t = sk_tail_cost(sk_tiles, num_kb, g, r);
       if (t < best_tail - 1e-9) {
         best_tail = t;
@@ -283,7 +287,9 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   pl.eb = dt.eb;
   pl.in_dtype = static_cast<int32_t>(dt.map_type);
   pl.c_type = dt.c_type;
-  const int64_t c_elem = pl.c_type == kCF32 ? 4 : 2;
+  // E4M3 output is a quantised result, written only.
+  if (dt.c_type == kCE4M3 && beta != 0.0f) return GEMM_ERR_UNSUPPORTED;
+  const int64_t c_elem = pl.c_type == kCF32 ? 4 : pl.c_type == kCE4M3 ? 1 : 2;
   if (M == 0 || N == 0) {
     P.path = GEMM_PATH_NOOP;
     *out = pl;
@@ -407,7 +413,8 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   // written whole, past column N); the blend with the old C (beta != 0) keeps
   // the direct path, which reads C as it writes it.  A swapped problem stores
   // transposed blocks (C's rows run along the kernel's J).
-  const bool bulk = c_rows_aligned && (N * c_elem) % 16 == 0 && beta == 0.0f && o.tma_store != 2;
+  const bool bulk = c_rows_aligned && (N * c_elem) % 16 == 0 && beta == 0.0f && o.tma_store != 2 &&
+                    pl.c_type != kCE4M3;  // 8-bit C leaves through direct stores
   pl.tma_store = !bulk ? kBulkNone : swap ? kBulkTransposed : kBulkRows;
   P.bulk_store = pl.tma_store;
   P.launches = 1 + P.repack_a + P.repack_b;
@@ -652,10 +659,10 @@ gemm_status_t gemm_plan(gemm_handle_t h, int sm_count, gemm_op_t transA, gemm_op
   return s;
 }
 
-gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int64_t M, int64_t N,
-                       int64_t K, float alpha, const void* A, int64_t lda, const void* B,
-                       int64_t ldb, float beta, void* C, int64_t ldc, gemm_dtype_t dtype,
-                       void* stream) {
+static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int64_t M,
+                              int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
+                              const void* B, int64_t ldb, float beta, void* C, int64_t ldc,
+                              gemm_dtype_t dtype, EpiOps ops, void* stream) {
   if (!h) return GEMM_ERR_INVALID_ARG;
   Plan pl;
   gemm_status_t s = make_plan(h->opt, h->slots, transA, transB, M, N, K, A, lda, B, ldb, beta,
@@ -667,7 +674,8 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
   DeviceGuard g(h->device);
   cudaError_t e;
   if (P.path == GEMM_PATH_SCALE_C) {
-    e = scale_c_launch(C, pl.c_type, M, N, ldc, beta, h->sm_count, st);
+    ops.bias_on_i = 0;  // C as stored: the bias runs along its columns
+    e = scale_c_launch(C, pl.c_type, M, N, ldc, beta, ops, h->sm_count, st);
     if (e != cudaSuccess) return cuda_fail(h, e);
     h->launches += 1;
     return GEMM_OK;
@@ -743,10 +751,36 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
   a.status = h->d_status;
   a.wait_limit_ns = static_cast<uint64_t>(h->opt.wait_limit_ns);
   a.drop_load = h->opt.drop_load;
+  ops.bias_on_i = P.swap_ab;  // a swapped problem computes C^T: C's columns are the kernel's rows
+  a.ops = ops;
   e = tc_launch(pl.cfg, map_p, map_q, map_c, a, P.grid, st);
   if (e != cudaSuccess) return cuda_fail(h, e);
   h->launches += 1;
   return GEMM_OK;
+}
+
+gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int64_t M, int64_t N,
+                       int64_t K, float alpha, const void* A, int64_t lda, const void* B,
+                       int64_t ldb, float beta, void* C, int64_t ldc, gemm_dtype_t dtype,
+                       void* stream) {
+  return run_gemm(h, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtype, EpiOps(),
+                  stream);
+}
+
+gemm_status_t gemm_run_ex(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int64_t M, int64_t N,
+                          int64_t K, float alpha, const void* A, int64_t lda, const void* B,
+                          int64_t ldb, float beta, void* C, int64_t ldc, gemm_dtype_t dtype,
+                          const gemm_epilogue_t* epi, void* stream) {
+  EpiOps ops;
+  if (epi) {
+    if (epi->activation < GEMM_ACT_NONE || epi->activation > GEMM_ACT_GELU) return GEMM_ERR_INVALID_ARG;
+    if (!std::isfinite(epi->out_scale)) return GEMM_ERR_INVALID_ARG;
+    if (epi->bias && reinterpret_cast<uintptr_t>(epi->bias) % sizeof(float) != 0) return GEMM_ERR_INVALID_ARG;
+    ops.bias = epi->bias;
+    ops.act = epi->activation;
+    ops.out_scale = epi->out_scale;
+  }
+  return run_gemm(h, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtype, ops, stream);
 }
 
 gemm_status_t gemm_get_status(gemm_handle_t h, void* stream, int32_t* detail) {
@@ -869,7 +903,7 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (P.path == GEMM_PATH_SCALE_C) {
-    e = scale_c_launch(C, pl.c_type, M, N, ldc, beta, d->sm_count, st);
+    e = scale_c_launch(C, pl.c_type, M, N, ldc, beta, EpiOps(), d->sm_count, st);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
   }
   // The arrays keep the previous call's contents: clear what must start at zero.
@@ -926,6 +960,7 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   a.status = d->status;
   a.wait_limit_ns = static_cast<uint64_t>(o.wait_limit_ns);
   a.drop_load = 0;
+  a.ops = EpiOps();  // no fused operations (the memset above zeroed out_scale)
   e = tc_launch(pl.cfg, map_p, map_q, map_c, a, P.grid, st);
   return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

@@ -19,7 +19,18 @@ constexpr int kThreads = 192;     // warp 0 TMA producer, warp 1 MMA issuer, war
 __host__ __device__ constexpr int slice_k(int eb) { return kSliceBytes / eb; }
 
 // Element type of C.
-enum CType : int32_t { kCF32 = 0, kCBF16 = 1, kCF16 = 2 };
+enum CType : int32_t { kCF32 = 0, kCBF16 = 1, kCF16 = 2, kCE4M3 = 3 };
+
+// Elementwise operations fused into the store of C (after the alpha / beta
+// blend): z += bias, z = act(z), z *= out_scale, then the conversion to C's type.
+enum Activation : int32_t { kActNone = 0, kActRelu = 1, kActGelu = 2 };
+struct EpiOps {
+  const float* bias = nullptr;  // one fp32 value per column of the caller's C, or null
+  int32_t bias_on_i = 0;        // the bias runs along the kernel's I (a swapped problem)
+  int32_t act = kActNone;
+  float out_scale = 1.0f;
+  __host__ __device__ bool any() const { return bias != nullptr || act != kActNone || out_scale != 1.0f; }
+};
 
 // Status-word layout written by a kernel that gives up on a barrier:
 //   bits 0-7 = 6 (GEMM_ERR_TIMEOUT), bits 8-11 = role, bits 12-15 = barrier.
@@ -51,6 +62,7 @@ struct TcArgs {
   int32_t* status;       // device status word
   uint64_t wait_limit_ns;
   int32_t drop_load;     // tests only: CTA 0 skips its drop_load-th k-block load (1-based)
+  EpiOps ops;            // fused elementwise operations of the epilogue
 };
 
 // Epilogue store paths: direct stores, or staged bulk tensor stores of rows of
@@ -81,8 +93,9 @@ cudaError_t tc_launch(int cfg, const CUtensorMap& map_p, const CUtensorMap& map_
 cudaError_t repack_launch(const void* src, int64_t lds, void* dst, int64_t ldd, int64_t rows,
                           int64_t cols, int esize, int sm_count, cudaStream_t stream);
 
-// C = beta * C over an M x N matrix with leading dimension ldc (C = 0 when beta == 0).
+// The whole GEMM when K == 0: C = ops(beta * C) over an M x N matrix with
+// leading dimension ldc (beta * C = 0 when beta == 0; C is then not read).
 cudaError_t scale_c_launch(void* C, int32_t c_type, int64_t M, int64_t N, int64_t ldc, float beta,
-                           int sm_count, cudaStream_t stream);
+                           const EpiOps& ops, int sm_count, cudaStream_t stream);
 
 }  // namespace g10

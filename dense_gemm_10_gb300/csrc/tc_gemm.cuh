@@ -43,6 +43,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "epi_ops.cuh"
 #include "gemm_internal.h"
 #include "ptx.cuh"
 
@@ -136,6 +137,8 @@ struct COut {
   float beta;
   bool vec;          // c_sj == 1 and rows 16-byte aligned: 16-byte stores
   int32_t tma;       // kBulkNone, kBulkRows or kBulkTransposed
+  bool has_ops;      // any fused bias / activation / output scale
+  EpiOps ops;
 };
 
 __device__ __forceinline__ COut make_cout(const TcArgs& a) {
@@ -149,12 +152,15 @@ __device__ __forceinline__ COut make_cout(const TcArgs& a) {
   o.beta = a.beta;
   o.vec = a.vec_store != 0;
   o.tma = a.tma_store;
+  o.ops = a.ops;
+  o.has_ops = a.ops.any();
   return o;
 }
 
 __device__ __forceinline__ float load_c(const COut& c, int64_t off) {
   if (c.type == kCF32) return static_cast<const float*>(c.C)[off];
   if (c.type == kCBF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(c.C)[off]);
+  if (c.type == kCE4M3) return from_e4m3(static_cast<const uint8_t*>(c.C)[off]);
   return __half2float(static_cast<const __half*>(c.C)[off]);
 }
 
@@ -163,6 +169,8 @@ __device__ __forceinline__ void store_c(const COut& c, int64_t off, float v) {
     static_cast<float*>(c.C)[off] = v;
   else if (c.type == kCBF16)
     static_cast<__nv_bfloat16*>(c.C)[off] = __float2bfloat16_rn(v);
+  else if (c.type == kCE4M3)
+    static_cast<uint8_t*>(c.C)[off] = to_e4m3(v);
   else
     static_cast<__half*>(c.C)[off] = __float2half_rn(v);
 }
@@ -181,12 +189,30 @@ __device__ __forceinline__ float2 unpack2(int32_t type, uint32_t bits) {
   return __half22float2(*reinterpret_cast<__half2*>(&bits));
 }
 
-// Write v + beta * C for row i, columns j0 .. j0 + 31 of D (v already holds alpha * D).
+// Write ops(v + beta * C) for row i, columns j0 .. j0 + 31 of D (v already
+// holds alpha * D).
 __device__ __forceinline__ void store_chunk(const COut& c, int i, int j0, const float (&v)[32]) {
   if (i >= c.I) return;
   const bool blend = c.beta != 0.0f;
   if (c.vec && j0 + 32 <= c.J) {
     const int64_t base = static_cast<int64_t>(i) * c.si + j0;
+    if (c.type == kCE4M3) {  // written only (beta == 0): 32 bytes as two 16-byte stores
+      uint32_t w[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        uint32_t b = 0;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float z = c.has_ops ? apply_ops(c.ops, v[4 * q + t], i, j0 + 4 * q + t) : v[4 * q + t];
+          b |= static_cast<uint32_t>(to_e4m3(z)) << (8 * t);
+        }
+        w[q] = b;
+      }
+      uint4* p = reinterpret_cast<uint4*>(static_cast<uint8_t*>(c.C) + base);
+      p[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      p[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      return;
+    }
     if (c.type == kCF32) {
       float4* p = reinterpret_cast<float4*>(static_cast<float*>(c.C) + base);
 #pragma unroll
@@ -195,6 +221,13 @@ __device__ __forceinline__ void store_chunk(const COut& c, int i, int j0, const 
         if (blend) {
           const float4 x = p[q];
           o.x += c.beta * x.x; o.y += c.beta * x.y; o.z += c.beta * x.z; o.w += c.beta * x.w;
+        }
+        if (c.has_ops) {
+          const int j = j0 + 4 * q;
+          o.x = apply_ops(c.ops, o.x, i, j);
+          o.y = apply_ops(c.ops, o.y, i, j + 1);
+          o.z = apply_ops(c.ops, o.z, i, j + 2);
+          o.w = apply_ops(c.ops, o.w, i, j + 3);
         }
         p[q] = o;
       }
@@ -215,6 +248,10 @@ __device__ __forceinline__ void store_chunk(const COut& c, int i, int j0, const 
             o[2 * t + 1] += c.beta * f.y;
           }
         }
+        if (c.has_ops) {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) o[t] = apply_ops(c.ops, o[t], i, j0 + 8 * q + t);
+        }
         p[q] = make_uint4(pack2(c.type, o[0], o[1]), pack2(c.type, o[2], o[3]), pack2(c.type, o[4], o[5]),
                           pack2(c.type, o[6], o[7]));
       }
@@ -228,6 +265,7 @@ __device__ __forceinline__ void store_chunk(const COut& c, int i, int j0, const 
       const int64_t off = static_cast<int64_t>(i) * c.si + static_cast<int64_t>(j) * c.sj;
       float o = v[t];
       if (blend) o += c.beta * load_c(c, off);
+      if (c.has_ops) o = apply_ops(c.ops, o, i, j);
       store_c(c, off, o);
     }
   }
@@ -282,11 +320,18 @@ struct EpiOut {
     ++nstore;
   }
 
-  __device__ __forceinline__ void put(int i, int j, const float (&v)[32], int half) {
+  __device__ __forceinline__ void put(int i, int j, const float (&vin)[32], int half) {
     if (c.tma == kBulkNone) {
-      store_chunk(c, i, j, v);
+      store_chunk(c, i, j, vin);
       return;
     }
+    // bulk paths run with beta == 0: the fused operations apply to alpha * D,
+    // inside C only (the bias holds no value for the clipped edge of a tile)
+    float v[32];
+    const bool row_in = i < c.I;
+#pragma unroll
+    for (int t = 0; t < 32; ++t)
+      v[t] = (c.has_ops && row_in && j + t < c.J) ? apply_ops(c.ops, vin[t], i, j + t) : vin[t];
     if (c.tma == kBulkTransposed) {
       const uint32_t buf = buffer(true);
       if (c.type == kCF32) {

@@ -12,9 +12,10 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libgemm_gb300.so")
 
 OP_N, OP_T = 0, 1
-BF16_F32, BF16_BF16, F16_F32, F16_F16 = 0, 1, 2, 3
+BF16_F32, BF16_BF16, F16_F32, F16_F16, BF16_E4M3, F16_E4M3 = 0, 1, 2, 3, 4, 5
 _FP8_FORMATS = ("e4m3", "e5m2")
-_C_TYPES = ("f32", "bf16", "f16")
+_C_TYPES = ("f32", "bf16", "f16", "e4m3")
+ACT_NONE, ACT_RELU, ACT_GELU = 0, 1, 2
 
 
 def fp8_dtype(a="e4m3", b="e4m3", c="f32"):
@@ -37,6 +38,11 @@ SCHED_TILES, SCHED_STREAM_K = 0, 1
 
 # Exported functions and their (restype, argtypes).
 _i32, _i64, _u64, _f32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p
+
+
+class Epilogue(ctypes.Structure):
+    """gemm_epilogue_t: C = convert(out_scale * act(alpha A B + beta C + bias[j]))."""
+    _fields_ = [("bias", _vp), ("activation", _i32), ("out_scale", _f32)]
 
 
 class Plan(ctypes.Structure):
@@ -65,6 +71,8 @@ SIGNATURES = {
     "gemm_launch_count": (_i32, [_vp, ctypes.POINTER(_u64)]),
     "gemm_run_noalloc": (_i32, [_i32, _i32, _i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _i32,
                                 _vp]),
+    "gemm_run_ex": (_i32, [_vp, _i32, _i32, _i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64,
+                           _i32, ctypes.POINTER(Epilogue), _vp]),
 }
 
 _lib = None
@@ -152,6 +160,13 @@ class Handle:
         return lib().gemm_run(self.ptr, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
                               dtype, stream)
 
+    def run_ex_raw(self, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtype, stream,
+                   bias=0, act=ACT_NONE, out_scale=1.0):
+        """gemm_run_ex on raw device pointers (bias: device pointer or 0); returns the status code."""
+        epi = Epilogue(bias or None, int(act), float(out_scale))
+        return lib().gemm_run_ex(self.ptr, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                                 dtype, ctypes.byref(epi), stream)
+
 
 _default = {}
 
@@ -173,8 +188,10 @@ def dtype_code(in_dtype, out_dtype, b_dtype=None):
              (torch.float16, torch.float32): F16_F32, (torch.float16, torch.float16): F16_F16}
     if b_dtype == in_dtype and (in_dtype, out_dtype) in table:
         return table[(in_dtype, out_dtype)]
+    if b_dtype == in_dtype and out_dtype == torch.float8_e4m3fn and in_dtype in (torch.bfloat16, torch.float16):
+        return BF16_E4M3 if in_dtype == torch.bfloat16 else F16_E4M3
     f8 = {torch.float8_e4m3fn: "e4m3", torch.float8_e5m2: "e5m2"}
-    cty = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}
+    cty = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16", torch.float8_e4m3fn: "e4m3"}
     if in_dtype in f8 and b_dtype in f8 and out_dtype in cty:
         return fp8_dtype(f8[in_dtype], f8[b_dtype], cty[out_dtype])
     raise TypeError("unsupported dtypes %s x %s -> %s" % (in_dtype, b_dtype, out_dtype))
@@ -187,10 +204,11 @@ def _ld(t, name):
 
 
 def gemm(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0, handle=None, stream=None, M=None,
-         N=None, K=None):
-    """C = alpha * op(A) * op(B) + beta * C on CUDA tensors, enqueued on `stream`
-    (default: torch's current stream).  A and B are stored row-major as
-    (M, K) / (K, M) and (K, N) / (N, K) per transA / transB; C is (M, N).
+         N=None, K=None, bias=None, act=ACT_NONE, out_scale=1.0):
+    """C = convert(out_scale * act(alpha * op(A) * op(B) + beta * C + bias)) on
+    CUDA tensors, enqueued on `stream` (default: torch's current stream).  A and
+    B are stored row-major as (M, K) / (K, M) and (K, N) / (N, K) per transA /
+    transB; C is (M, N); bias (optional) is a CUDA fp32 tensor of N values.
     Sizes default to the logical extents of the tensors."""
     import torch
     for t, n in ((A, "A"), (B, "B"), (C, "C")):
@@ -206,8 +224,12 @@ def gemm(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0, handle=None, 
         stream = torch.cuda.current_stream(C.device).cuda_stream
     elif hasattr(stream, "cuda_stream"):
         stream = stream.cuda_stream
-    st = h.run_raw(ta, tb, M, N, K, float(alpha), A.data_ptr(), _ld(A, "A"), B.data_ptr(), _ld(B, "B"),
-                   float(beta), C.data_ptr(), _ld(C, "C"), code, stream)
+    if bias is not None and (not bias.is_cuda or bias.dtype != torch.float32 or bias.numel() < N
+                             or not bias.is_contiguous()):
+        raise ValueError("bias must be a contiguous CUDA float32 tensor of N values")
+    st = h.run_ex_raw(ta, tb, M, N, K, float(alpha), A.data_ptr(), _ld(A, "A"), B.data_ptr(), _ld(B, "B"),
+                      float(beta), C.data_ptr(), _ld(C, "C"), code, stream,
+                      bias=bias.data_ptr() if bias is not None else 0, act=act, out_scale=out_scale)
     _check(st, "gemm_run")
     return C
 

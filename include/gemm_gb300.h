@@ -51,14 +51,21 @@ typedef enum { GEMM_OP_N = 0, GEMM_OP_T = 1 } gemm_op_t;
  * transB == GEMM_OP_T: A stored M x K, B stored N x K, the usual layout of
  * FP8 weights); other layouts return GEMM_ERR_UNSUPPORTED.  Leading dimensions
  * are in elements (= bytes); the code is 16 + (A is E5M2) + 2 * (B is E5M2) +
- * 4 * (0 for fp32 C, 1 for bf16 C, 2 for fp16 C).  Per-tensor scale factors of
- * FP8 data fold into alpha.
+ * 4 * (0 for fp32 C, 1 for bf16 C, 2 for fp16 C, 3 for E4M3 C).  Per-tensor
+ * scale factors of FP8 data fold into alpha.
+ *
+ * E4M3 C is a quantised output: the fp32 result (after the fused epilogue of
+ * gemm_run_ex, whose out_scale is the quantisation scale) is rounded to
+ * nearest even and saturated to +-448.  It is written only: beta must be 0
+ * (else GEMM_ERR_UNSUPPORTED).
  */
 typedef enum {
   GEMM_BF16_F32 = 0,  /* A, B bf16; C fp32 */
   GEMM_BF16_BF16 = 1, /* A, B bf16; C bf16 */
   GEMM_F16_F32 = 2,   /* A, B fp16; C fp32 */
   GEMM_F16_F16 = 3,   /* A, B fp16; C fp16 */
+  GEMM_BF16_E4M3 = 4, /* A, B bf16; C E4M3 (quantised output) */
+  GEMM_F16_E4M3 = 5,  /* A, B fp16; C E4M3 (quantised output) */
   GEMM_E4M3_F32 = 16,        /* A, B E4M3; C fp32 */
   GEMM_E5M2_E4M3_F32 = 17,   /* A E5M2, B E4M3; C fp32 */
   GEMM_E4M3_E5M2_F32 = 18,   /* A E4M3, B E5M2; C fp32 */
@@ -70,7 +77,11 @@ typedef enum {
   GEMM_E4M3_F16 = 24,        /* ... and with fp16 C */
   GEMM_E5M2_E4M3_F16 = 25,
   GEMM_E4M3_E5M2_F16 = 26,
-  GEMM_E5M2_F16 = 27
+  GEMM_E5M2_F16 = 27,
+  GEMM_E4M3_E4M3OUT = 28,      /* ... and with E4M3 C (quantised output) */
+  GEMM_E5M2_E4M3_E4M3OUT = 29,
+  GEMM_E4M3_E5M2_E4M3OUT = 30,
+  GEMM_E5M2_E4M3OUT = 31
 } gemm_dtype_t;
 
 typedef enum {
@@ -125,6 +136,39 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
                        int64_t K, float alpha, const void* A, int64_t lda, const void* B,
                        int64_t ldb, float beta, void* C, int64_t ldc, gemm_dtype_t dtype,
                        void* stream);
+
+/*
+ * Fused epilogue: elementwise operations applied to each element of the
+ * result before it is stored, in this order ("第4章：经典算子实现 —— GEMM",
+ * section 7.2: GEMM + bias + activation; "GPU GEMM 优化完全拆解（三）",
+ * mainloop 与 epilogue: ReLU and quantisation scaling before write-back):
+ *   z = alpha * op(A) * op(B) + beta * C + bias[j]
+ *   C = convert(out_scale * act(z))
+ * act: GEMM_ACT_NONE (identity), GEMM_ACT_RELU max(z, 0), GEMM_ACT_GELU
+ * z * Phi(z) = z * (1 + erf(z / sqrt 2)) / 2 (the exact form, evaluated in
+ * fp32 with the device erff).
+ */
+typedef enum { GEMM_ACT_NONE = 0, GEMM_ACT_RELU = 1, GEMM_ACT_GELU = 2 } gemm_activation_t;
+
+typedef struct {
+  const float* bias;   /* device pointer to N fp32 values, one per column j of C, read only;
+                          NULL for none.  Must be 4-byte aligned. */
+  int32_t activation;  /* gemm_activation_t */
+  float out_scale;     /* finite; multiplies act(z) before the conversion to C's type (the
+                          quantisation scale for E4M3 C); 1 for none */
+} gemm_epilogue_t;
+
+/*
+ * gemm_run_ex: gemm_run with the fused epilogue `epi` (NULL = none, the same as
+ * gemm_run).  The operations cost no extra pass over C: they are applied in the
+ * kernel's epilogue (and by the K == 0 kernel, where z = beta * C + bias).
+ * Errors: those of gemm_run, and GEMM_ERR_INVALID_ARG for an unknown
+ * activation, a non-finite out_scale or a misaligned bias.
+ */
+gemm_status_t gemm_run_ex(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int64_t M, int64_t N,
+                          int64_t K, float alpha, const void* A, int64_t lda, const void* B,
+                          int64_t ldb, float beta, void* C, int64_t ldc, gemm_dtype_t dtype,
+                          const gemm_epilogue_t* epi, void* stream);
 
 /*
  * gemm_get_status: synchronise `stream`, then read and clear the handle's

@@ -16,7 +16,8 @@ def dtype_code(p):
     if p.in_dtype in inputs.FP8:
         return G.fp8_dtype(p.in_dtype, p.b_dtype, p.out_dtype)
     return {("bf16", "f32"): G.BF16_F32, ("bf16", "bf16"): G.BF16_BF16, ("f16", "f32"): G.F16_F32,
-            ("f16", "f16"): G.F16_F16}[(p.in_dtype, p.out_dtype)]
+            ("f16", "f16"): G.F16_F16, ("bf16", "e4m3"): G.BF16_E4M3,
+            ("f16", "e4m3"): G.F16_E4M3}[(p.in_dtype, p.out_dtype)]
 
 
 def device_problem(p, guard_rows=0, guard_cols=0):

@@ -151,12 +151,23 @@ def test_plan_fp8():
         with pytest.raises(G.GemmError) as e:
             G.plan(256, 256, 256, ta, tb, G.E4M3_F32)
         assert e.value.status == G.ERR_UNSUPPORTED
-    for bad in (4, 15, 28):
+    for bad in (6, 15, 32):
         with pytest.raises(G.GemmError) as e:
             G.plan(256, 256, 256, 0, 1, bad)
         assert e.value.status == G.ERR_INVALID_ARG
-    assert [G.fp8_dtype(a, b, c) for c in ("f32", "bf16", "f16") for b in ("e4m3", "e5m2")
-            for a in ("e4m3", "e5m2")] == list(range(16, 28))
+    assert [G.fp8_dtype(a, b, c) for c in ("f32", "bf16", "f16", "e4m3") for b in ("e4m3", "e5m2")
+            for a in ("e4m3", "e5m2")] == list(range(16, 32))
+
+
+def test_plan_e4m3_output():
+    """E4M3 C (quantised output): written only, by the direct-store epilogue."""
+    for dt in (G.BF16_E4M3, G.F16_E4M3, G.fp8_dtype("e4m3", "e4m3", "e4m3")):
+        p = G.plan(4096, 4096, 4096, 0, 1, dt)
+        assert p.bulk_store == G.BULK_NONE and p.vector_store == 1
+        with pytest.raises(G.GemmError) as e:
+            G.plan(256, 256, 256, 0, 1, dt, beta=0.5)
+        assert e.value.status == G.ERR_UNSUPPORTED
+    assert G.plan(256, 256, 256, 0, 1, G.BF16_E4M3, ldc=260).vector_store == 0   # 260-byte rows
 
 
 def test_plan_half_atom_pairs_need_k_major_q():
