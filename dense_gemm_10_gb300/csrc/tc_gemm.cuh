@@ -271,6 +271,38 @@ __device__ __forceinline__ void store_chunk(const COut& c, int i, int j0, const 
   }
 }
 
+// The fused operations on a row piece v[0..31] = columns j0 .. j0 + 31 of row i
+// (nvalid of them inside C).  Each operation is its own loop behind a branch
+// that is uniform across the warp, and everything stays in registers: local
+// memory or extra L1 traffic would compete with the shared-memory port that
+// feeds the tensor core.  The bias along J comes in as one coalesced load per
+// warp (lane t holds bias[j0 + t]) and is broadcast by shuffles.
+__device__ __forceinline__ void apply_ops32(const EpiOps& ops, float (&v)[32], int lane, int64_t i, int64_t j0,
+                                            int nvalid) {
+  if (ops.bias) {
+    if (ops.bias_on_i) {
+      const float b = __ldg(ops.bias + i);
+#pragma unroll
+      for (int t = 0; t < 32; ++t) v[t] += b;
+    } else {
+      const float mine = lane < nvalid ? __ldg(ops.bias + j0 + lane) : 0.0f;
+#pragma unroll
+      for (int t = 0; t < 32; ++t) v[t] += __shfl_sync(0xffffffffu, mine, t);
+    }
+  }
+  if (ops.act == kActRelu) {
+#pragma unroll
+    for (int t = 0; t < 32; ++t) v[t] = v[t] > 0.0f ? v[t] : 0.0f;
+  } else if (ops.act == kActGelu) {
+#pragma unroll
+    for (int t = 0; t < 32; ++t) v[t] = 0.5f * v[t] * (1.0f + erff(v[t] * 0.70710678118654752f));
+  }
+  if (ops.out_scale != 1.0f) {
+#pragma unroll
+    for (int t = 0; t < 32; ++t) v[t] *= ops.out_scale;
+  }
+}
+
 // One epilogue warp's output path.  The warp owns 32 rows of the tile (I) and
 // produces them 32 columns (J) at a time.
 //  * kBulkRows: each thread's 32 values go into its row of a 128-byte-swizzled
@@ -328,10 +360,11 @@ struct EpiOut {
     // bulk paths run with beta == 0: the fused operations apply to alpha * D,
     // inside C only (the bias holds no value for the clipped edge of a tile)
     float v[32];
-    const bool row_in = i < c.I;
 #pragma unroll
-    for (int t = 0; t < 32; ++t)
-      v[t] = (c.has_ops && row_in && j + t < c.J) ? apply_ops(c.ops, vin[t], i, j + t) : vin[t];
+    for (int t = 0; t < 32; ++t) v[t] = vin[t];
+    // (the whole warp enters: the bias shuffle needs every lane; rows past I
+    // compute values the clipped store drops)
+    if (c.has_ops) apply_ops32(c.ops, v, lane, i < c.I ? i : c.I - 1, j, c.J - j < 32 ? c.J - j : 32);
     if (c.tma == kBulkTransposed) {
       const uint32_t buf = buffer(true);
       if (c.type == kCF32) {
