@@ -130,6 +130,88 @@ def make_problem(name, M, N, K, transA=0, transB=0, in_dtype="bf16", out_dtype="
                    A, lda, B, ldb, C0, ldc, seed, recipe, b_dtype)
 
 
+@dataclass
+class BatchedProblem:
+    """A strided batch of GEMMs C_b = alpha * op(A_b) * op(B_b) + beta * C0_b,
+    b < batch, with A_b = A[b * strideA :] etc. (row-major storage as in
+    Problem; a stride of 0 reuses one matrix for every batch).  A, B, C0 are
+    flat tensors of the input / output types."""
+    name: str
+    batch: int
+    M: int
+    N: int
+    K: int
+    transA: int
+    transB: int
+    in_dtype: str
+    out_dtype: str
+    alpha: float
+    beta: float
+    A: torch.Tensor
+    lda: int
+    strideA: int
+    B: torch.Tensor
+    ldb: int
+    strideB: int
+    C0: object
+    ldc: int
+    strideC: int
+    seed: int
+    b_dtype: str = None
+
+    def __post_init__(self):
+        if self.b_dtype is None:
+            self.b_dtype = self.in_dtype
+
+
+def _stack(mats, stride, dtype):
+    """Lay the matrices out flat at `stride` elements apart (NaN bits between)."""
+    rows, ld = mats[0].shape
+    if stride == 0:
+        return mats[0].reshape(-1).clone()
+    if stride < rows * ld:
+        raise ValueError("batch stride smaller than one matrix")
+    flat = torch.empty(stride * (len(mats) - 1) + rows * ld, dtype=mats[0].dtype)
+    if dtype in _NAN_BITS:
+        flat.view(torch.int16).fill_(_NAN_BITS[dtype])
+    elif dtype in _NAN_BITS8:
+        flat.view(torch.uint8).fill_(_NAN_BITS8[dtype])
+    else:
+        flat.fill_(float("nan"))
+    for b, m in enumerate(mats):
+        flat[b * stride:b * stride + rows * ld] = m.reshape(-1)
+    return flat
+
+
+def make_batched_problem(name, batch, M, N, K, transA=0, transB=0, in_dtype="bf16", out_dtype="f32",
+                         dist_a=("uniform", -1.0, 1.0), dist_b=("uniform", -1.0, 1.0), alpha=1.0, beta=0.0,
+                         dist_c=("normal", 0.0, 1.0), seed=0, lda=None, ldb=None, ldc=None, strideA=None,
+                         strideB=None, strideC=None, b_dtype=None):
+    """Batch b draws A from seed + 3b, B from seed + 3b + 1, C0 from seed + 3b + 2
+    (one draw when that operand's stride is 0); strides default to packed."""
+    b_dtype = in_dtype if b_dtype is None else b_dtype
+    a_shape = (K, M) if transA else (M, K)
+    b_shape = (N, K) if transB else (K, N)
+    lda = a_shape[1] if lda is None else lda
+    ldb = b_shape[1] if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    strideA = a_shape[0] * lda if strideA is None else strideA
+    strideB = b_shape[0] * ldb if strideB is None else strideB
+    strideC = M * ldc if strideC is None else strideC
+    nA = 1 if strideA == 0 else batch
+    nB = 1 if strideB == 0 else batch
+    A = _stack([_pad_columns(draw(a_shape, dist_a, seed + 3 * b, in_dtype), lda, in_dtype) for b in range(nA)],
+               strideA, in_dtype)
+    B = _stack([_pad_columns(draw(b_shape, dist_b, seed + 3 * b + 1, b_dtype), ldb, b_dtype) for b in range(nB)],
+               strideB, b_dtype)
+    C0 = None
+    if beta != 0.0:
+        C0 = _stack([_pad_columns(draw((M, N), dist_c, seed + 3 * b + 2, out_dtype), ldc, out_dtype)
+                     for b in range(batch)], strideC, out_dtype)
+    return BatchedProblem(name, batch, M, N, K, transA, transB, in_dtype, out_dtype, float(alpha), float(beta),
+                          A, lda, strideA, B, ldb, strideB, C0, ldc, strideC, seed, b_dtype)
+
+
 # ---------------------------------------------------------------------------
 # The workloads, named by what they are.
 # ---------------------------------------------------------------------------
@@ -172,6 +254,14 @@ def ragged_4095_4097_1000():
     """Ragged tile edges: M = 4095, N = 4097, K = 1000, NN, bf16 as the LLM shapes."""
     return make_problem("ragged_4095x4097x1000_nn", 4095, 4097, 1000, 0, 0, "bf16", "f32",
                         ("normal", 0.0, 1.0), ("normal", 0.0, 0.02))
+
+
+def attention_scores(batch_heads=32, seq=2048, head_dim=128):
+    """Attention scores Q K^T for batch x heads pairs: Q (S x d) and K (S x d)
+    row-major, so the product is NT; bf16 N(0, 1), alpha 1/sqrt(d), bf16 out."""
+    return make_batched_problem("attn_qk_%dx%dx%d" % (batch_heads, seq, head_dim), batch_heads, seq, seq,
+                                head_dim, 0, 1, "bf16", "bf16", ("normal", 0.0, 1.0), ("normal", 0.0, 1.0),
+                                alpha=1.0 / math.sqrt(head_dim))
 
 
 def lm_head_64():

@@ -59,6 +59,9 @@ def _load():
     lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
     lib.oracle_f16_value.restype = dbl
     lib.oracle_f16_value.argtypes = [ctypes.c_uint16]
+    lib.oracle_gemm_batched.restype = i32
+    lib.oracle_gemm_batched.argtypes = [i32, i32, i64, i64, i64, dbl, vp, i64, i64, vp, i64, i64, dbl, vp, i32,
+                                        i64, i64, i32, i32, i64, vp, vp, i64, i32]
     lib.oracle_epilogue.restype = i32
     lib.oracle_epilogue.argtypes = [i64, i64, vp, vp, i64, vp, i32, dbl]
     lib.oracle_e4m3_value.restype = dbl
@@ -133,6 +136,26 @@ def gemm(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc, in_type,
                             _ptr(R), _ptr(Mag), N, int(nthreads))
     if rc < 0:
         raise ValueError("oracle_gemm rejected its arguments")
+    return R, Mag
+
+
+def gemm_batched(transA, transB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C0, ldc, strideC,
+                 in_type, batch, c_type=C_F32, nthreads=0, b_type=None):
+    """Strided batched oracle.  Returns (R, Mag): fp64 arrays of shape (batch, M, N).
+    A, B, C0: flat code / value arrays holding every batch at the given element
+    strides (0 = the same matrix for every batch)."""
+    lib = _load()
+    b_type = in_type if b_type is None else b_type
+    A = _codes(A, in_type).reshape(-1)
+    B = _codes(B, b_type).reshape(-1)
+    C0 = _c0_array(C0, c_type).reshape(-1) if beta != 0.0 else None
+    R = np.zeros((batch, M, N), dtype=np.float64)
+    Mag = np.zeros((batch, M, N), dtype=np.float64)
+    rc = lib.oracle_gemm_batched(int(transA), int(transB), M, N, K, float(alpha), _ptr(A), lda, strideA,
+                                 _ptr(B), ldb, strideB, float(beta), _ptr(C0), int(c_type), ldc, strideC,
+                                 int(in_type), int(b_type), batch, _ptr(R), _ptr(Mag), N, int(nthreads))
+    if rc < 0:
+        raise ValueError("oracle_gemm_batched rejected its arguments")
     return R, Mag
 
 

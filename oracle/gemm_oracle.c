@@ -334,3 +334,33 @@ int oracle_epilogue(int64_t M, int64_t N, double* R, double* Mag, int64_t ldr, c
   }
   return 0;
 }
+
+/*
+ * Strided batched oracle: for b in [0, batch), the GEMM above on
+ *   A_b = A + b * strideA,  B_b = B + b * strideB,  C0_b / R_b / Mag_b = ... + b * stride
+ * (strides in elements; a stride of 0 reuses one operand for every batch).
+ * This is the product a batched attention score or value GEMM computes per
+ * (batch, head) pair ("第4章：经典算子实现 —— GEMM", section 1: Q (B*H, S, d) x K^T).
+ * R / Mag hold batch x M x N, leading dimension ldr, batch stride M * ldr.
+ * Returns the threads used by the last batch, or -1 on a bad argument.
+ */
+int oracle_gemm_batched(int transA, int transB, int64_t M, int64_t N, int64_t K, double alpha,
+                        const void* A, int64_t lda, int64_t strideA, const void* B, int64_t ldb,
+                        int64_t strideB, double beta, const void* C0, int c_type, int64_t ldc,
+                        int64_t strideC, int a_type, int b_type, int64_t batch, double* R,
+                        double* Mag, int64_t ldr, int nthreads) {
+  if (batch < 0 || strideA < 0 || strideB < 0 || strideC < 0) return -1;
+  const int64_t ea = (a_type == ORACLE_IN_E4M3 || a_type == ORACLE_IN_E5M2) ? 1 : 2;
+  const int64_t eb = (b_type == ORACLE_IN_E4M3 || b_type == ORACLE_IN_E5M2) ? 1 : 2;
+  const int64_t ec = c_type == ORACLE_C_F32 ? 4 : 2;
+  int used = 0;
+  for (int64_t b = 0; b < batch; ++b) {
+    const char* Ab = (const char*)A + b * strideA * ea;
+    const char* Bb = (const char*)B + b * strideB * eb;
+    const char* Cb = C0 ? (const char*)C0 + b * strideC * ec : NULL;
+    used = oracle_gemm_ab(transA, transB, M, N, K, alpha, Ab, lda, Bb, ldb, beta, Cb, c_type, ldc,
+                          a_type, b_type, R + b * M * ldr, Mag + b * M * ldr, ldr, nthreads);
+    if (used < 0) return -1;
+  }
+  return used;
+}

@@ -407,6 +407,59 @@ def test_thread_count_does_not_change_results():
 
 
 # ---------------------------------------------------------------------------
+# Strided batched GEMM
+# ---------------------------------------------------------------------------
+
+def _batch_mats(flat, count, stride, rows, ld, cols):
+    """Decoded fp64 matrices of a flat batch (stride 0: the same one each time)."""
+    x = flat.to(torch.float64).numpy()
+    return [x[b * stride:b * stride + rows * ld].reshape(rows, ld)[:, :cols] for b in range(count)]
+
+
+@pytest.mark.parametrize("transA,transB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("bcast", ["none", "A", "B"])
+def test_batched_matches_per_batch_library_matmul(transA, transB, bcast):
+    """Each batch against numpy's matmul of the library-decoded matrices, with
+    padded leading dimensions, gaps between batches and broadcast operands."""
+    batch, M, N, K = 4, 9, 11, 37
+    a_rows = K if transA else M
+    b_rows = N if transB else K
+    lda = (M if transA else K) + 3
+    ldb = (K if transB else N) + 2
+    p = inputs.make_batched_problem("ob", batch, M, N, K, transA, transB, "bf16", "f32", ("normal", 0, 1),
+                                    ("normal", 0, 1), alpha=-0.5, beta=1.25, seed=3, lda=lda, ldb=ldb,
+                                    ldc=N + 1, strideA=0 if bcast == "A" else a_rows * lda + 5,
+                                    strideB=0 if bcast == "B" else b_rows * ldb + 7, strideC=M * (N + 1) + 4)
+    R, Mag = oracle.gemm_batched(transA, transB, M, N, K, p.alpha, inputs.bits(p.A), p.lda, p.strideA,
+                                 inputs.bits(p.B), p.ldb, p.strideB, p.beta, p.C0.numpy(), p.ldc, p.strideC,
+                                 oracle.IN_BF16, batch)
+    As = _batch_mats(p.A, batch, p.strideA, a_rows, lda, M if transA else K)
+    Bs = _batch_mats(p.B, batch, p.strideB, b_rows, ldb, K if transB else N)
+    Cs = _batch_mats(p.C0, batch, p.strideC, M, N + 1, N)
+    for b in range(batch):
+        a = As[b].T if transA else As[b]
+        bb = Bs[b].T if transB else Bs[b]
+        ref = p.alpha * (a @ bb) + p.beta * Cs[b]
+        assert np.allclose(R[b], ref, rtol=1e-12, atol=1e-12), b
+        assert np.allclose(Mag[b], abs(p.alpha) * (np.abs(a) @ np.abs(bb)) + abs(p.beta) * np.abs(Cs[b]),
+                           rtol=1e-12, atol=1e-12)
+
+
+def test_batched_fp8_and_empty_batch():
+    p = inputs.make_batched_problem("ob8", 3, 5, 6, 70, 0, 1, "e4m3", "f32", ("normal", 0, 1), ("normal", 0, 1),
+                                    seed=9, b_dtype="e5m2")
+    R, _ = oracle.gemm_batched(0, 1, 5, 6, 70, 1.0, inputs.bits(p.A), 70, p.strideA, inputs.bits(p.B), 70,
+                               p.strideB, 0.0, None, 6, p.strideC, oracle.IN_E4M3, 3, b_type=oracle.IN_E5M2)
+    for b in range(3):
+        a = p.A[b * 350:(b + 1) * 350].to(torch.float64).numpy().reshape(5, 70)
+        bb = p.B[b * 420:(b + 1) * 420].to(torch.float64).numpy().reshape(6, 70)
+        assert np.allclose(R[b], a @ bb.T, rtol=1e-12, atol=1e-12)
+    R0, M0 = oracle.gemm_batched(0, 0, 4, 4, 4, 1.0, np.zeros(16, np.uint16), 4, 16, np.zeros(16, np.uint16), 4,
+                                 16, 0.0, None, 4, 16, oracle.IN_BF16, 0)
+    assert R0.shape == (0, 4, 4)
+
+
+# ---------------------------------------------------------------------------
 # Fused epilogue: bias, activation, output scale
 # ---------------------------------------------------------------------------
 

@@ -29,6 +29,8 @@ MUTATIONS = {
     "ReLU passes negatives": ("d = z > 0.0 ? z : 0.0;", "d = z > 0.0 ? z : -z;"),
     "bias indexed by row": ("z += (double)bias[j];", "z += (double)bias[i % N];"),
     "output scale dropped": ("R[i * ldr + j] = scale * d;", "R[i * ldr + j] = d;"),
+    "B batch stride ignored": ("(const char*)B + b * strideB * eb", "(const char*)B"),
+    "C0 batch offset ignored": ("(const char*)C0 + b * strideC * ec", "(const char*)C0"),
 }
 
 
