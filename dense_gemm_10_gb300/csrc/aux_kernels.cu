@@ -14,11 +14,12 @@
 namespace g10 {
 
 template <typename T>
-__global__ void repack_kernel(const T* __restrict__ src, int64_t lds, T* __restrict__ dst, int64_t ldd,
-                              int64_t rows, int64_t cols) {
+__global__ void repack_kernel(const T* __restrict__ src, int64_t lds, int64_t sbs, T* __restrict__ dst,
+                              int64_t ldd, int64_t dbs, int64_t rows, int64_t cols, int64_t nb) {
+  for (int64_t b = blockIdx.z; b < nb; b += gridDim.z)
   for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
-    const T* s = src + r * lds;
-    T* d = dst + r * ldd;
+    const T* s = src + b * sbs + r * lds;
+    T* d = dst + b * dbs + r * ldd;
     for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < cols;
          c += static_cast<int64_t>(gridDim.x) * blockDim.x)
       d[c] = s[c];
@@ -26,12 +27,13 @@ __global__ void repack_kernel(const T* __restrict__ src, int64_t lds, T* __restr
 }
 
 __global__ void scale_c_kernel(void* C, int32_t c_type, int64_t M, int64_t N, int64_t ldc,
-                               float beta, EpiOps ops) {
+                               float beta, EpiOps ops, int64_t batch, int64_t sbc) {
   const bool any = ops.any();
+  for (int64_t b = blockIdx.z; b < batch; b += gridDim.z)
   for (int64_t r = blockIdx.y; r < M; r += gridDim.y) {
     for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < N;
          c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-      const int64_t off = r * ldc + c;
+      const int64_t off = b * sbc + r * ldc + c;
       if (c_type == kCF32) {
         float* p = static_cast<float*>(C) + off;
         float z = beta == 0.0f ? 0.0f : beta * *p;
@@ -51,28 +53,35 @@ __global__ void scale_c_kernel(void* C, int32_t c_type, int64_t M, int64_t N, in
   }
 }
 
-static dim3 grid_2d(int64_t rows, int64_t cols, int sm_count) {
+static dim3 grid_3d(int64_t rows, int64_t cols, int64_t nb, int sm_count) {
   const int64_t bx = (cols + 255) / 256 < 16 ? (cols + 255) / 256 : 16;
   int64_t by = (static_cast<int64_t>(sm_count) * 8 + bx - 1) / bx;
   if (by > rows) by = rows;
   if (by > 65535) by = 65535;
-  return dim3(static_cast<unsigned>(bx > 0 ? bx : 1), static_cast<unsigned>(by > 0 ? by : 1), 1);
+  int64_t bz = nb < 65535 ? nb : 65535;
+  if (bz * by > 4 * 65535) bz = (4 * 65535) / (by > 0 ? by : 1);
+  return dim3(static_cast<unsigned>(bx > 0 ? bx : 1), static_cast<unsigned>(by > 0 ? by : 1),
+              static_cast<unsigned>(bz > 0 ? bz : 1));
 }
 
-cudaError_t repack_launch(const void* src, int64_t lds, void* dst, int64_t ldd, int64_t rows,
-                          int64_t cols, int esize, int sm_count, cudaStream_t stream) {
+cudaError_t repack_launch(const void* src, int64_t lds, int64_t sbs, void* dst, int64_t ldd, int64_t dbs,
+                          int64_t rows, int64_t cols, int64_t nb, int esize, int sm_count,
+                          cudaStream_t stream) {
+  const dim3 g = grid_3d(rows, cols, nb, sm_count);
   if (esize == 1)
-    repack_kernel<uint8_t><<<grid_2d(rows, cols, sm_count), 256, 0, stream>>>(
-        static_cast<const uint8_t*>(src), lds, static_cast<uint8_t*>(dst), ldd, rows, cols);
+    repack_kernel<uint8_t><<<g, 256, 0, stream>>>(static_cast<const uint8_t*>(src), lds, sbs,
+                                                  static_cast<uint8_t*>(dst), ldd, dbs, rows, cols, nb);
   else
-    repack_kernel<uint16_t><<<grid_2d(rows, cols, sm_count), 256, 0, stream>>>(
-        static_cast<const uint16_t*>(src), lds, static_cast<uint16_t*>(dst), ldd, rows, cols);
+    repack_kernel<uint16_t><<<g, 256, 0, stream>>>(static_cast<const uint16_t*>(src), lds, sbs,
+                                                   static_cast<uint16_t*>(dst), ldd, dbs, rows, cols, nb);
   return cudaGetLastError();
 }
 
 cudaError_t scale_c_launch(void* C, int32_t c_type, int64_t M, int64_t N, int64_t ldc, float beta,
-                           const EpiOps& ops, int sm_count, cudaStream_t stream) {
-  scale_c_kernel<<<grid_2d(M, N, sm_count), 256, 0, stream>>>(C, c_type, M, N, ldc, beta, ops);
+                           const EpiOps& ops, int64_t batch, int64_t sbc, int sm_count,
+                           cudaStream_t stream) {
+  scale_c_kernel<<<grid_3d(M, N, batch, sm_count), 256, 0, stream>>>(C, c_type, M, N, ldc, beta, ops, batch,
+                                                                       sbc);
   return cudaGetLastError();
 }
 

@@ -53,6 +53,8 @@ struct Operand {
   bool repack = false;        // copied into the workspace first
   int64_t packed_ld = 0;
   size_t ws_offset = 0;
+  int64_t bstride = 0;        // elements between batches' matrices (strided batches)
+  int64_t nb = 1;             // distinct matrices: 1 when shared by every batch
 };
 
 struct Plan {
@@ -62,6 +64,7 @@ struct Plan {
   Operand p, q;
   int64_t I = 0, J = 0, K = 0;
   int64_t c_si = 0, c_sj = 0;
+  int64_t batch = 1, c_sb = 0;  // strided batch: count, C's batch stride in elements
   int32_t c_type = kCF32;
   int32_t eb = 2;                  // input element bytes (2: bf16 / fp16, 1: FP8)
   uint32_t a_fmt = 1, b_fmt = 1;   // instruction-descriptor formats of the stored A and B
@@ -73,8 +76,9 @@ struct Plan {
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-bool tma_aligned(const void* p, int64_t ld, int eb) {
-  return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((ld * eb) % 16 == 0);
+bool tma_aligned(const void* p, int64_t ld, int eb, int64_t bstride, int64_t nb) {
+  return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((ld * eb) % 16 == 0) &&
+         (nb == 1 || (bstride * eb) % 16 == 0);
 }
 
 // The input and output types a gemm_dtype_t names.
@@ -170,7 +174,7 @@ bool needs_partials(const Sched& s) {
 // Work units over all slots (for reporting): whole tiles, split pieces, or
 // stream-K range pieces (one more piece per slot edge that falls inside a tile).
 int64_t count_units(const Sched& s) {
-  const int64_t tiles = static_cast<int64_t>(s.tiles_i) * s.tiles_j;
+  const int64_t tiles = sched_tiles(s);
   if (s.mode == kSchedTiles) return tiles * s.split_k;
   int64_t n = s.dp_tiles + (tiles - s.dp_tiles);
   for (int32_t c = 1; c < s.sk_slots; ++c)
@@ -198,8 +202,8 @@ double sk_tail_cost(int64_t tiles, int64_t num_kb, int64_t g, double r) {
 }
 
 // num_kb counts stages of kdepth 64-wide k-slices each.
-Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64_t num_kb, int kdepth,
-                       int cfg, int slots, bool hbm_bound) {
+Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64_t batch, int64_t num_kb,
+                       int kdepth, int cfg, int slots, bool hbm_bound) {
   Choice ch;
   ch.kdepth = kdepth;
   const TileConfig& tc = kTileConfigs[cfg];
@@ -209,13 +213,14 @@ Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64
   ch.bn = tc.bn;
   ch.mc = tc.mc;
   ch.slots = slots;
-  const int64_t tiles = tiles_i * tiles_j;
+  const int64_t tiles = tiles_i * tiles_j * batch;
   // a CTA's fp32 partial tile (bn x 128) in stages of its operand bytes
   const double stage_bytes = static_cast<double>(kdepth) * (kBM + tc.bn / tc.cg) * kSliceBytes;
   const double r = 4.0 * tc.bn * kBM / stage_bytes;
   Sched& s = ch.sched;
   s.tiles_i = static_cast<int32_t>(tiles_i);
   s.tiles_j = static_cast<int32_t>(tiles_j);
+  s.batch = static_cast<int32_t>(batch);
   s.num_kb = static_cast<int32_t>(num_kb);
   s.raster_group = 8;
   s.mode = kSchedTiles;
@@ -276,7 +281,8 @@ Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64
 gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t transA, gemm_op_t transB,
                         int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                         int64_t ldb, float beta, const void* C, int64_t ldc, gemm_dtype_t dtype,
-                        Plan* out) {
+                        Plan* out, int64_t batch = 1, int64_t strideA = 0, int64_t strideB = 0,
+                        int64_t strideC = 0) {
   Plan pl;
   gemm_plan_t& P = pl.pub;
   if ((transA != GEMM_OP_N && transA != GEMM_OP_T) || (transB != GEMM_OP_N && transB != GEMM_OP_T))
@@ -290,13 +296,19 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   // E4M3 output is a quantised result, written only.
   if (dt.c_type == kCE4M3 && beta != 0.0f) return GEMM_ERR_UNSUPPORTED;
   const int64_t c_elem = pl.c_type == kCF32 ? 4 : pl.c_type == kCE4M3 ? 1 : 2;
-  if (M == 0 || N == 0) {
+  if (batch < 0 || strideA < 0 || strideB < 0 || strideC < 0) return GEMM_ERR_INVALID_ARG;
+  P.batch = static_cast<int32_t>(batch > 1 ? batch : 1);
+  if (M == 0 || N == 0 || batch == 0) {
     P.path = GEMM_PATH_NOOP;
     *out = pl;
     return GEMM_OK;
   }
   if (C == nullptr || ldc < N) return GEMM_ERR_INVALID_ARG;
-  if (M > kMaxExtent || N > kMaxExtent || K > kMaxExtent) return GEMM_ERR_UNSUPPORTED;
+  if (M > kMaxExtent || N > kMaxExtent || K > kMaxExtent || batch > kMaxExtent) return GEMM_ERR_UNSUPPORTED;
+  // every batch writes its own C
+  if (batch > 1 && strideC < (M - 1) * ldc + N) return GEMM_ERR_INVALID_ARG;
+  pl.batch = batch;
+  pl.c_sb = batch > 1 ? strideC : 0;
   if (K == 0) {
     P.path = GEMM_PATH_SCALE_C;
     P.launches = 1;
@@ -315,6 +327,10 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   a.rows = a.kmajor ? M : K; a.cols = a.kmajor ? K : M;
   b.ptr = B; b.ld = ldb; b.kmajor = transB == GEMM_OP_T;
   b.rows = b.kmajor ? N : K; b.cols = b.kmajor ? K : N;
+  a.nb = (batch > 1 && strideA > 0) ? batch : 1;  // a stride of 0 shares one matrix
+  b.nb = (batch > 1 && strideB > 0) ? batch : 1;
+  a.bstride = a.nb > 1 ? strideA : 0;
+  b.bstride = b.nb > 1 ? strideB : 0;
 
   // A short M rides on the MMA's N dimension: compute C^T = op(B)^T op(A)^T.
   const bool swap = M <= 64 && N > M;
@@ -324,6 +340,8 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   pl.K = K;
   pl.p = swap ? b : a;
   pl.q = swap ? a : b;
+  // the schedule indexes tiles (and split-K partial slots) with 32-bit integers
+  if (cdiv(pl.I, kBM) * cdiv(pl.J, 64) * batch > (int64_t{1} << 30)) return GEMM_ERR_UNSUPPORTED;
   pl.a_fmt = swap ? dt.b_fmt : dt.a_fmt;  // formats of the MMA's A (P) and B (Q) operands
   pl.b_fmt = swap ? dt.a_fmt : dt.b_fmt;
   pl.c_si = swap ? 1 : ldc;
@@ -335,9 +353,9 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   // Below the machine balance (≈ 2.2 PFLOP/s over ≈ 7 TB/s ≈ 300 FLOP per byte
   // for 16-bit inputs, twice that for the 8-bit ones at twice the rate) the
   // GEMM is bound by HBM, not by the tensor cores.
-  const double alg_bytes = dt.eb * (static_cast<double>(M) * K + static_cast<double>(K) * N) +
-                           static_cast<double>(M) * N * c_elem * (beta != 0.0f ? 2 : 1);
-  const bool hbm_bound = 2.0 * static_cast<double>(M) * N * K / alg_bytes < 256.0 * (3 - dt.eb);
+  const double alg_bytes = dt.eb * (static_cast<double>(M) * K * a.nb + static_cast<double>(K) * N * b.nb) +
+                           static_cast<double>(M) * N * batch * c_elem * (beta != 0.0f ? 2 : 1);
+  const bool hbm_bound = 2.0 * static_cast<double>(M) * N * K * batch / alg_bytes < 256.0 * (3 - dt.eb);
 
   // Tile configuration and schedule: the configuration with the lowest
   // estimated time, est_time() below.
@@ -358,7 +376,7 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
     // Two k-slices per stage where the ring still holds at least two such stages.
     int kdepth = o.kdepth ? o.kdepth : default_kdepth(c);
     if (kdepth > 1 && tc_stages(cfg) / kdepth < 2) kdepth = 1;
-    Choice ch = choose_schedule(o, cdiv(pl.I, kBM * c.cg), cdiv(cdiv(pl.J, c.bn), c.mc),
+    Choice ch = choose_schedule(o, cdiv(pl.I, kBM * c.cg), cdiv(cdiv(pl.J, c.bn), c.mc), batch,
                                 cdiv(num_kslices, kdepth), kdepth, cfg, nslots, hbm_bound);
     if (ch.valid && ch.cost < best.cost - 1e-9) best = ch;
   }
@@ -382,7 +400,7 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   P.tiles_i = pl.sched.tiles_i;
   P.tiles_j = pl.sched.tiles_j;
   P.num_kb = pl.sched.num_kb;
-  P.tiles = static_cast<int64_t>(pl.sched.tiles_i) * pl.sched.tiles_j;
+  P.tiles = sched_tiles(pl.sched);
   P.dp_tiles = pl.sched.mode == kSchedStreamK ? pl.sched.dp_tiles : static_cast<int32_t>(P.tiles);
   P.sk_slots = pl.sched.mode == kSchedStreamK ? pl.sched.sk_slots : 0;
   P.units = count_units(pl.sched);
@@ -392,11 +410,11 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   // Workspace: repacked operands, then partial tiles of split tiles.
   size_t ws = 0;
   for (Operand* op : {&pl.p, &pl.q}) {
-    if (!tma_aligned(op->ptr, op->ld, dt.eb)) {
-      op->repack = true;  // rows padded to whole 16-byte pieces
+    if (!tma_aligned(op->ptr, op->ld, dt.eb, op->bstride, op->nb)) {
+      op->repack = true;  // rows padded to whole 16-byte pieces, batches packed
       op->packed_ld = static_cast<int64_t>(round_up(static_cast<size_t>(op->cols), 16 / dt.eb));
       op->ws_offset = ws;
-      ws = round_up(ws + static_cast<size_t>(op->rows) * op->packed_ld * dt.eb, 256);
+      ws = round_up(ws + static_cast<size_t>(op->rows) * op->packed_ld * dt.eb * op->nb, 256);
     }
   }
   P.repack_a = (swap ? pl.q.repack : pl.p.repack) ? 1 : 0;
@@ -406,7 +424,8 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
     ws = round_up(ws + static_cast<size_t>(partial_slots(pl.sched)) * cl * best.bn * kBM * 4, 256);
   }
   P.workspace_bytes = static_cast<int64_t>(ws);
-  const bool c_rows_aligned = reinterpret_cast<uintptr_t>(C) % 16 == 0 && (ldc * c_elem) % 16 == 0;
+  const bool c_rows_aligned = reinterpret_cast<uintptr_t>(C) % 16 == 0 && (ldc * c_elem) % 16 == 0 &&
+                              (pl.c_sb * c_elem) % 16 == 0;
   P.vector_store = (!swap && c_rows_aligned) ? 1 : 0;
   // Bulk tensor stores need 16-byte aligned rows and a row width that is a
   // whole number of 16-byte pieces (a partial piece at the right edge would be
@@ -443,13 +462,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // {box_rows rows} (64 16-bit or 128 8-bit elements of k); MN-major tiles
 // (16-bit only) are {64 rows of M/N} x {64 k}, loaded one 64-wide atom at a time.
 gemm_status_t encode_operand(CUtensorMap* map, const Operand& op, const void* base, int64_t ld,
-                             int eb, int32_t map_type, int box_rows) {
+                             int64_t bstride, int eb, int32_t map_type, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return GEMM_ERR_TENSORMAP;
-  cuuint64_t dims[2];
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * eb};
-  cuuint32_t box[2];
-  cuuint32_t estr[2] = {1, 1};
+  // third dimension: the batch (one matrix when shared; its stride is then any valid value)
+  cuuint64_t dims[3];
+  dims[2] = static_cast<cuuint64_t>(op.nb);
+  const int64_t one = round_up(static_cast<size_t>(op.rows * ld * eb), 16);
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * eb,
+                           static_cast<cuuint64_t>(op.nb > 1 ? bstride * eb : one)};
+  cuuint32_t box[3];
+  box[2] = 1;
+  cuuint32_t estr[3] = {1, 1, 1};
   if (op.kmajor) {
     dims[0] = static_cast<cuuint64_t>(op.cols);  // K
     dims[1] = static_cast<cuuint64_t>(op.rows);  // M or N
@@ -461,7 +485,7 @@ gemm_status_t encode_operand(CUtensorMap* map, const Operand& op, const void* ba
     box[0] = 64;
     box[1] = kBK;
   }
-  CUresult r = fn(map, static_cast<CUtensorMapDataType>(map_type), 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  CUresult r = fn(map, static_cast<CUtensorMapDataType>(map_type), 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_TENSORMAP;
@@ -471,20 +495,23 @@ gemm_status_t encode_operand(CUtensorMap* map, const Operand& op, const void* ba
 // boxes of 32 rows x 128 bytes with the 128-byte swizzle.  Transposed: boxes
 // of 32 rows x 32 elements, 128-byte swizzled for fp32, plain for 16 bits.
 gemm_status_t encode_c(CUtensorMap* map, void* C, int64_t rows, int64_t cols, int64_t ldc,
-                       int32_t c_type, bool transposed) {
+                       int32_t c_type, bool transposed, int64_t batch, int64_t strideC) {
   auto fn = encode_fn();
   if (!fn) return GEMM_ERR_TENSORMAP;
   const int64_t esize = c_type == kCF32 ? 4 : 2;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc * esize)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(transposed ? 32 : 128 / esize), 32};
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(batch)};
+  const int64_t one = round_up(static_cast<size_t>(rows * ldc * esize), 16);
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ldc * esize),
+                           static_cast<cuuint64_t>(batch > 1 ? strideC * esize : one)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(transposed ? 32 : 128 / esize), 32, 1};
   const CUtensorMapSwizzle swz =
       transposed && esize == 2 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
-  cuuint32_t estr[2] = {1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
   CUtensorMapDataType dt = c_type == kCF32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                            : c_type == kCBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUresult r = fn(map, dt, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+  CUresult r = fn(map, dt, 3, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_TENSORMAP;
 }
@@ -644,29 +671,39 @@ gemm_status_t gemm_launch_count(gemm_handle_t h, uint64_t* count) {
   return GEMM_OK;
 }
 
-gemm_status_t gemm_plan(gemm_handle_t h, int sm_count, gemm_op_t transA, gemm_op_t transB,
-                        int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
-                        const void* B, int64_t ldb, float beta, const void* C, int64_t ldc,
-                        gemm_dtype_t dtype, gemm_plan_t* plan) {
+gemm_status_t gemm_plan_strided_batched(gemm_handle_t h, int sm_count, gemm_op_t transA, gemm_op_t transB,
+                                        int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                                        int64_t strideA, const void* B, int64_t ldb, int64_t strideB,
+                                        float beta, const void* C, int64_t ldc, int64_t strideC,
+                                        int64_t batch, gemm_dtype_t dtype, gemm_plan_t* plan) {
   if (!plan) return GEMM_ERR_INVALID_ARG;
   if (!h && sm_count <= 0) return GEMM_ERR_INVALID_ARG;
   Options o = h ? h->opt : Options();
   const SlotTable slots = h ? h->slots : SlotTable::even(sm_count);
   Plan pl;
-  gemm_status_t s =
-      make_plan(o, slots, transA, transB, M, N, K, A, lda, B, ldb, beta, C, ldc, dtype, &pl);
+  gemm_status_t s = make_plan(o, slots, transA, transB, M, N, K, A, lda, B, ldb, beta, C, ldc, dtype, &pl,
+                              batch, strideA, strideB, strideC);
   if (s == GEMM_OK) *plan = pl.pub;
   return s;
+}
+
+gemm_status_t gemm_plan(gemm_handle_t h, int sm_count, gemm_op_t transA, gemm_op_t transB,
+                        int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                        const void* B, int64_t ldb, float beta, const void* C, int64_t ldc,
+                        gemm_dtype_t dtype, gemm_plan_t* plan) {
+  return gemm_plan_strided_batched(h, sm_count, transA, transB, M, N, K, A, lda, 0, B, ldb, 0, beta, C, ldc,
+                                   0, 1, dtype, plan);
 }
 
 static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int64_t M,
                               int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
                               const void* B, int64_t ldb, float beta, void* C, int64_t ldc,
-                              gemm_dtype_t dtype, EpiOps ops, void* stream) {
+                              gemm_dtype_t dtype, EpiOps ops, void* stream, int64_t batch = 1,
+                              int64_t strideA = 0, int64_t strideB = 0, int64_t strideC = 0) {
   if (!h) return GEMM_ERR_INVALID_ARG;
   Plan pl;
   gemm_status_t s = make_plan(h->opt, h->slots, transA, transB, M, N, K, A, lda, B, ldb, beta,
-                              C, ldc, dtype, &pl);
+                              C, ldc, dtype, &pl, batch, strideA, strideB, strideC);
   if (s != GEMM_OK) return s;
   const gemm_plan_t& P = pl.pub;
   if (P.path == GEMM_PATH_NOOP) return GEMM_OK;
@@ -675,7 +712,7 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
   cudaError_t e;
   if (P.path == GEMM_PATH_SCALE_C) {
     ops.bias_on_i = 0;  // C as stored: the bias runs along its columns
-    e = scale_c_launch(C, pl.c_type, M, N, ldc, beta, ops, h->sm_count, st);
+    e = scale_c_launch(C, pl.c_type, M, N, ldc, beta, ops, pl.batch, pl.c_sb, h->sm_count, st);
     if (e != cudaSuccess) return cuda_fail(h, e);
     h->launches += 1;
     return GEMM_OK;
@@ -707,23 +744,26 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
     const Operand& op = w == 0 ? pl.p : pl.q;
     if (!op.repack) continue;
     void* dst = ws + op.ws_offset;
-    e = repack_launch(op.ptr, op.ld, dst, op.packed_ld, op.rows, op.cols, pl.eb, h->sm_count, st);
+    e = repack_launch(op.ptr, op.ld, op.bstride, dst, op.packed_ld, op.rows * op.packed_ld, op.rows, op.cols,
+                      op.nb, pl.eb, h->sm_count, st);
     if (e != cudaSuccess) return cuda_fail(h, e);
     h->launches += 1;
     if (w == 0) { pbase = dst; pld = op.packed_ld; } else { qbase = dst; qld = op.packed_ld; }
   }
 
   CUtensorMap map_p, map_q;
-  s = encode_operand(&map_p, pl.p, pbase, pld, pl.eb, pl.in_dtype, kBM / mc);
+  s = encode_operand(&map_p, pl.p, pbase, pld, pl.p.repack ? pl.p.rows * pld : pl.p.bstride, pl.eb,
+                     pl.in_dtype, kBM / mc);
   if (s != GEMM_OK) return s;
-  s = encode_operand(&map_q, pl.q, qbase, qld, pl.eb, pl.in_dtype, P.bn / cg);
+  s = encode_operand(&map_q, pl.q, qbase, qld, pl.q.repack ? pl.q.rows * qld : pl.q.bstride, pl.eb,
+                     pl.in_dtype, P.bn / cg);
   if (s != GEMM_OK) return s;
   CUtensorMap map_c;
   std::memset(&map_c, 0, sizeof(map_c));
   if (pl.tma_store != kBulkNone) {
     // C as stored: I x J, or J x I for a swapped problem
-    s = pl.tma_store == kBulkRows ? encode_c(&map_c, C, pl.I, pl.J, ldc, pl.c_type, false)
-                                  : encode_c(&map_c, C, pl.J, pl.I, ldc, pl.c_type, true);
+    s = pl.tma_store == kBulkRows ? encode_c(&map_c, C, pl.I, pl.J, ldc, pl.c_type, false, pl.batch, pl.c_sb)
+                                  : encode_c(&map_c, C, pl.J, pl.I, ldc, pl.c_type, true, pl.batch, pl.c_sb);
     if (s != GEMM_OK) return s;
   }
 
@@ -743,6 +783,9 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
   a.C = C;
   a.c_si = pl.c_si;
   a.c_sj = pl.c_sj;
+  a.c_sb = pl.c_sb;
+  a.p_bcast = pl.p.nb == 1 ? 1 : 0;
+  a.q_bcast = pl.q.nb == 1 ? 1 : 0;
   a.c_type = pl.c_type;
   a.vec_store = P.vector_store;
   a.tma_store = pl.tma_store;
@@ -767,10 +810,7 @@ gemm_status_t gemm_run(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int6
                   stream);
 }
 
-gemm_status_t gemm_run_ex(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int64_t M, int64_t N,
-                          int64_t K, float alpha, const void* A, int64_t lda, const void* B,
-                          int64_t ldb, float beta, void* C, int64_t ldc, gemm_dtype_t dtype,
-                          const gemm_epilogue_t* epi, void* stream) {
+static gemm_status_t epi_ops(const gemm_epilogue_t* epi, EpiOps* out) {
   EpiOps ops;
   if (epi) {
     if (epi->activation < GEMM_ACT_NONE || epi->activation > GEMM_ACT_GELU) return GEMM_ERR_INVALID_ARG;
@@ -780,7 +820,30 @@ gemm_status_t gemm_run_ex(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, i
     ops.act = epi->activation;
     ops.out_scale = epi->out_scale;
   }
+  *out = ops;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_run_ex(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int64_t M, int64_t N,
+                          int64_t K, float alpha, const void* A, int64_t lda, const void* B,
+                          int64_t ldb, float beta, void* C, int64_t ldc, gemm_dtype_t dtype,
+                          const gemm_epilogue_t* epi, void* stream) {
+  EpiOps ops;
+  gemm_status_t s = epi_ops(epi, &ops);
+  if (s != GEMM_OK) return s;
   return run_gemm(h, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtype, ops, stream);
+}
+
+gemm_status_t gemm_run_strided_batched(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int64_t M,
+                                       int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
+                                       int64_t strideA, const void* B, int64_t ldb, int64_t strideB,
+                                       float beta, void* C, int64_t ldc, int64_t strideC, int64_t batch,
+                                       gemm_dtype_t dtype, const gemm_epilogue_t* epi, void* stream) {
+  EpiOps ops;
+  gemm_status_t s = epi_ops(epi, &ops);
+  if (s != GEMM_OK) return s;
+  return run_gemm(h, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtype, ops, stream, batch,
+                  strideA, strideB, strideC);
 }
 
 gemm_status_t gemm_get_status(gemm_handle_t h, void* stream, int32_t* detail) {
@@ -903,7 +966,7 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (P.path == GEMM_PATH_SCALE_C) {
-    e = scale_c_launch(C, pl.c_type, M, N, ldc, beta, EpiOps(), d->sm_count, st);
+    e = scale_c_launch(C, pl.c_type, M, N, ldc, beta, EpiOps(), pl.batch, pl.c_sb, d->sm_count, st);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
   }
   // The arrays keep the previous call's contents: clear what must start at zero.
@@ -919,21 +982,24 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
     const Operand& op = w == 0 ? pl.p : pl.q;
     if (!op.repack) continue;
     void* dst = d->scratch + op.ws_offset;
-    e = repack_launch(op.ptr, op.ld, dst, op.packed_ld, op.rows, op.cols, pl.eb, d->sm_count, st);
+    e = repack_launch(op.ptr, op.ld, op.bstride, dst, op.packed_ld, op.rows * op.packed_ld, op.rows, op.cols,
+                      op.nb, pl.eb, d->sm_count, st);
     if (e != cudaSuccess) return GEMM_ERR_CUDA;
     if (w == 0) { pbase = dst; pld = op.packed_ld; } else { qbase = dst; qld = op.packed_ld; }
   }
   CUtensorMap map_p, map_q;
-  s = encode_operand(&map_p, pl.p, pbase, pld, pl.eb, pl.in_dtype, kBM / mc);
+  s = encode_operand(&map_p, pl.p, pbase, pld, pl.p.repack ? pl.p.rows * pld : pl.p.bstride, pl.eb,
+                     pl.in_dtype, kBM / mc);
   if (s != GEMM_OK) return s;
-  s = encode_operand(&map_q, pl.q, qbase, qld, pl.eb, pl.in_dtype, P.bn / cg);
+  s = encode_operand(&map_q, pl.q, qbase, qld, pl.q.repack ? pl.q.rows * qld : pl.q.bstride, pl.eb,
+                     pl.in_dtype, P.bn / cg);
   if (s != GEMM_OK) return s;
   CUtensorMap map_c;
   std::memset(&map_c, 0, sizeof(map_c));
   if (pl.tma_store != kBulkNone) {
     // C as stored: I x J, or J x I for a swapped problem
-    s = pl.tma_store == kBulkRows ? encode_c(&map_c, C, pl.I, pl.J, ldc, pl.c_type, false)
-                                  : encode_c(&map_c, C, pl.J, pl.I, ldc, pl.c_type, true);
+    s = pl.tma_store == kBulkRows ? encode_c(&map_c, C, pl.I, pl.J, ldc, pl.c_type, false, pl.batch, pl.c_sb)
+                                  : encode_c(&map_c, C, pl.J, pl.I, ldc, pl.c_type, true, pl.batch, pl.c_sb);
     if (s != GEMM_OK) return s;
   }
   TcArgs a;
@@ -952,6 +1018,9 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   a.C = C;
   a.c_si = pl.c_si;
   a.c_sj = pl.c_sj;
+  a.c_sb = pl.c_sb;
+  a.p_bcast = pl.p.nb == 1 ? 1 : 0;
+  a.q_bcast = pl.q.nb == 1 ? 1 : 0;
   a.c_type = pl.c_type;
   a.vec_store = P.vector_store;
   a.tma_store = pl.tma_store;

@@ -63,6 +63,9 @@ struct TcArgs {
   uint64_t wait_limit_ns;
   int32_t drop_load;     // tests only: CTA 0 skips its drop_load-th k-block load (1-based)
   EpiOps ops;            // fused elementwise operations of the epilogue
+  int64_t c_sb;          // batch stride of C in elements (strided batches; tile batch in Unit::tb)
+  int32_t p_bcast;       // P is one matrix shared by every batch (its tensor map has one batch)
+  int32_t q_bcast;
 };
 
 // Epilogue store paths: direct stores, or staged bulk tensor stores of rows of
@@ -88,14 +91,17 @@ cudaError_t tc_prepare(int cfg, int* max_clusters);
 cudaError_t tc_launch(int cfg, const CUtensorMap& map_p, const CUtensorMap& map_q,
                       const CUtensorMap& map_c, const TcArgs& args, int grid, cudaStream_t stream);
 
-// dst[r * ldd + c] = src[r * lds + c] for elements of esize (1 or 2) bytes,
-// r < rows, c < cols; leading dimensions in elements.
-cudaError_t repack_launch(const void* src, int64_t lds, void* dst, int64_t ldd, int64_t rows,
-                          int64_t cols, int esize, int sm_count, cudaStream_t stream);
+// dst[b * dbs + r * ldd + c] = src[b * sbs + r * lds + c] for elements of
+// esize (1 or 2) bytes, b < nb, r < rows, c < cols; strides in elements.
+cudaError_t repack_launch(const void* src, int64_t lds, int64_t sbs, void* dst, int64_t ldd, int64_t dbs,
+                          int64_t rows, int64_t cols, int64_t nb, int esize, int sm_count,
+                          cudaStream_t stream);
 
-// The whole GEMM when K == 0: C = ops(beta * C) over an M x N matrix with
-// leading dimension ldc (beta * C = 0 when beta == 0; C is then not read).
+// The whole GEMM when K == 0: C = ops(beta * C) over `batch` M x N matrices
+// with leading dimension ldc, sbc elements apart (beta * C = 0 when beta == 0;
+// C is then not read).
 cudaError_t scale_c_launch(void* C, int32_t c_type, int64_t M, int64_t N, int64_t ldc, float beta,
-                           const EpiOps& ops, int sm_count, cudaStream_t stream);
+                           const EpiOps& ops, int64_t batch, int64_t sbc, int sm_count,
+                           cudaStream_t stream);
 
 }  // namespace g10

@@ -15,6 +15,9 @@
 //    slot, slot + slots, ... of the first dp_tiles.  This removes the tail
 //    effect of a last, partly filled wave ("CUDA GEMM 矩阵乘法优化指南", 12.5,
 //    which names Stream-K as the cure for it).
+// A strided batch of GEMMs shares one schedule: the tiles of batch b follow
+// those of batch b - 1 (tile index = b * tiles_i * tiles_j + raster position),
+// so whole tiles, split-K and stream-K treat the batch as one larger grid.
 // A tile split over several units is finished by whichever contribution
 // arrives last: every contribution stores an fp32 partial, and the last one
 // sums all partials in k order, so results do not depend on timing.
@@ -33,7 +36,8 @@ namespace g10 {
 enum : int32_t { kSchedTiles = 0, kSchedStreamK = 1 };
 
 struct Sched {
-  int32_t tiles_i, tiles_j;  // output tiles along I and J
+  int32_t tiles_i, tiles_j;  // output tiles along I and J (of one batch)
+  int32_t batch;             // independent GEMMs sharing the schedule (>= 1)
   int32_t num_kb;            // k-blocks per tile
   int32_t raster_group;      // tile rows per raster group
   int32_t mode;              // kSchedTiles or kSchedStreamK
@@ -45,6 +49,7 @@ struct Sched {
 
 struct Unit {
   int32_t ti, tj, tile;  // output tile (raster position and linear index)
+  int32_t tb;            // batch of the tile
   int32_t kb0, kb1;      // k-blocks [kb0, kb1) of the tile
   int32_t partial;       // 1: store an fp32 partial; the last contribution sums them
   int32_t pslot;         // partial slot of this contribution
@@ -54,11 +59,19 @@ struct Unit {
   int32_t first_j;       // stream-K: which of that slot's two partial slots it used
 };
 
-// Tile index -> (ti, tj) in grouped raster order: raster_group tile rows at a
-// time, walking down the rows of a group before moving one column right, so
-// that tiles running together share rows of P and columns of Q in L2
-// ("GPU GEMM 优化完全拆解（三）", rasterization).
-G10_HD void raster_tile(const Sched& s, int32_t tile, int32_t& ti, int32_t& tj) {
+// Output tiles of the whole schedule (every batch).
+G10_HD int64_t sched_tiles(const Sched& s) {
+  return static_cast<int64_t>(s.tiles_i) * s.tiles_j * s.batch;
+}
+
+// Tile index -> (batch, ti, tj): within a batch, grouped raster order:
+// raster_group tile rows at a time, walking down the rows of a group before
+// moving one column right, so that tiles running together share rows of P and
+// columns of Q in L2 ("GPU GEMM 优化完全拆解（三）", rasterization).
+G10_HD void raster_tile(const Sched& s, int32_t tile, int32_t& ti, int32_t& tj, int32_t& tb) {
+  const int32_t per_batch = s.tiles_i * s.tiles_j;
+  tb = tile / per_batch;
+  tile -= tb * per_batch;
   const int32_t group_tiles = s.raster_group * s.tiles_j;
   const int32_t g = tile / group_tiles;
   const int32_t first_i = g * s.raster_group;
@@ -80,8 +93,7 @@ G10_HD int32_t sk_owner(const Sched& s, int64_t x) {
 
 // Number of partial slots the schedule needs.
 G10_HD int64_t partial_slots(const Sched& s) {
-  return s.mode == kSchedTiles ? static_cast<int64_t>(s.tiles_i) * s.tiles_j * s.split_k
-                               : static_cast<int64_t>(s.sk_slots) * 2;
+  return s.mode == kSchedTiles ? sched_tiles(s) * s.split_k : static_cast<int64_t>(s.sk_slots) * 2;
 }
 
 // Partial slot of contribution k (k = 0 holds the lowest k-blocks) to w's tile.
@@ -109,7 +121,7 @@ struct WorkIter {
   G10_HD bool next(Unit& w) {
     const Sched& S = s;
     if (S.mode == kSchedTiles) {
-      const int32_t units = S.tiles_i * S.tiles_j * S.split_k;
+      const int32_t units = static_cast<int32_t>(sched_tiles(S)) * S.split_k;
       if (u >= units) return false;
       w.tile = u / S.split_k;
       const int32_t k = u - w.tile * S.split_k;
@@ -121,7 +133,7 @@ struct WorkIter {
       w.ncontrib = S.split_k;
       w.first_c = 0;
       w.first_j = 0;
-      raster_tile(S, w.tile, w.ti, w.tj);
+      raster_tile(S, w.tile, w.ti, w.tj, w.tb);
       u += slots;
       return true;
     }
@@ -141,7 +153,7 @@ struct WorkIter {
         w.ncontrib = c_last - c_first + 1;
         w.first_c = c_first;
         w.first_j = sk_begin(S, c_first) < t0 ? 1 : 0;
-        raster_tile(S, w.tile, w.ti, w.tj);
+        raster_tile(S, w.tile, w.ti, w.tj, w.tb);
         ++nseg;
         x = end;
         return true;
@@ -158,7 +170,7 @@ struct WorkIter {
     w.ncontrib = 1;
     w.first_c = 0;
     w.first_j = 0;
-    raster_tile(S, w.tile, w.ti, w.tj);
+    raster_tile(S, w.tile, w.ti, w.tj, w.tb);
     u += slots;
     return true;
   }

@@ -323,6 +323,8 @@ struct EpiOut {
   uint32_t staging;  // this warp's buffers (shared address, 1024-byte aligned)
   int lane;
   int y0;            // first row of the warp's 32 rows (I)
+  int z;             // batch of the current tile (bulk stores)
+  void* c0;          // C of batch 0; c.C points at the current tile's batch
   int nstore;        // bulk stores issued from the current buffers
   bool ring;         // buffers in the operand ring: no reuse, no waits
 
@@ -341,11 +343,11 @@ struct EpiOut {
     return buf;
   }
 
-  __device__ __forceinline__ void issue(uint32_t buf, int x, int y) {
+  __device__ __forceinline__ void issue(uint32_t buf, int x, int y) {  // at batch z
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      tma_store_2d(map_c, buf, x, y);
+      tma_store_3d(map_c, buf, x, y, z);
       bulk_commit_group();
     }
     __syncwarp();
@@ -440,6 +442,8 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
   while (ok && work.next(w)) {
     const int i0 = w.ti * Cfg::kTileM + q * kBM;
     const int j0 = (w.tj * MC + pair) * BN + q * Cfg::kQRows;
+    const int zp = a.p_bcast ? 0 : w.tb;  // batch coordinate (0 for an operand shared by all batches)
+    const int zq = a.q_bcast ? 0 : w.tb;
     for (int kb = w.kb0; kb < w.kb1; ++kb) {  // one stage: k-slices kb * kdepth .. + kdepth - 1
       if (!warp_wait(smem_u32(&ctrl->empty[stage]), phase ^ 1u, ctrl, a, kRoleProducer, kBarEmpty,
                      true)) {
@@ -458,14 +462,14 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
         const int nks = KD == 1 ? 1 : min(KD, kslices - ks0);
         if (elect_one()) {
           if (q == 0) mbar_arrive_expect_tx(full_local, CG * nks * Cfg::kStageBytes);
-          auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
+          auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z) {
             if constexpr (CG == 2)
-              tma_load_2d_pair(dst, map, full, x, y);
+              tma_load_3d_pair(dst, map, full, x, y, z);
             else
-              tma_load_2d(dst, map, full, x, y);
+              tma_load_3d(dst, map, full, x, y, z);
           };
-          auto load_mc = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
-            tma_load_2d_pair_multicast(dst, map, full, x, y, p_mask);
+          auto load_mc = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z) {
+            tma_load_3d_pair_multicast(dst, map, full, x, y, z, p_mask);
           };
 #pragma unroll
           for (int t = 0; t < KD; ++t) {
@@ -477,21 +481,21 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
             if constexpr (MC == 2) {
               // this pair's half of the P tile: 64 rows (K-major) or one 64-wide atom (M-major)
               if (p_kmajor)
-                load_mc(sa + pair * 64 * 128, map_p, k0, i0 + 64 * pair);
+                load_mc(sa + pair * 64 * 128, map_p, k0, i0 + 64 * pair, zp);
               else
-                load_mc(sa + pair * kMnAtomBytes, map_p, i0 + 64 * pair, k0);
+                load_mc(sa + pair * kMnAtomBytes, map_p, i0 + 64 * pair, k0, zp);
             } else if (p_kmajor) {
-              load(sa, map_p, k0, i0);
+              load(sa, map_p, k0, i0, zp);
             } else {
-              load(sa, map_p, i0, k0);
-              load(sa + kMnAtomBytes, map_p, i0 + 64, k0);
+              load(sa, map_p, i0, k0, zp);
+              load(sa + kMnAtomBytes, map_p, i0 + 64, k0, zp);
             }
             if (q_kmajor) {
-              load(sb, map_q, k0, j0);
+              load(sb, map_q, k0, j0, zq);
             } else {
 #pragma unroll
               for (int c = 0; c < Cfg::kQRows / 64; ++c)
-                load(sb + c * kMnAtomBytes, map_q, j0 + 64 * c, k0);
+                load(sb + c * kMnAtomBytes, map_q, j0 + 64 * c, k0, zq);
             }
           }
         }
@@ -622,6 +626,8 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
   const float alpha = a.alpha;
   EpiOut out;
   out.c = make_cout(a);
+  out.c0 = a.C;
+  out.z = 0;
   out.map_c = map_c;
   out.staging = smem_u32(staging + (warp - 2) * 2 * kStagingBuf);
   out.lane = lane;
@@ -658,6 +664,9 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
     const int i = w.ti * Cfg::kTileM + q * kBM + row;
     const int jt = (w.tj * MC + pair) * BN;  // first column of this pair's tile
     out.y0 = w.ti * Cfg::kTileM + q * kBM + quarter * 32;
+    out.z = w.tb;
+    out.c.C = static_cast<char*>(out.c0) +
+              static_cast<int64_t>(w.tb) * a.c_sb * (a.c_type == kCF32 ? 4 : a.c_type == kCE4M3 ? 1 : 2);
     if (!w.partial) {
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {

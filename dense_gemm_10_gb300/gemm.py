@@ -51,7 +51,7 @@ class Plan(ctypes.Structure):
                                     "grid", "launches", "schedule")] + \
                [(n, _i64) for n in ("tiles", "units", "workspace_bytes")] + \
                [(n, _i32) for n in ("tiles_i", "tiles_j", "num_kb", "dp_tiles", "sk_slots", "cluster", "kdepth",
-                                    "bulk_store")]
+                                    "bulk_store", "batch")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -73,6 +73,10 @@ SIGNATURES = {
                                 _vp]),
     "gemm_run_ex": (_i32, [_vp, _i32, _i32, _i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64,
                            _i32, ctypes.POINTER(Epilogue), _vp]),
+    "gemm_run_strided_batched": (_i32, [_vp, _i32, _i32, _i64, _i64, _i64, _f32, _vp, _i64, _i64, _vp, _i64,
+                                        _i64, _f32, _vp, _i64, _i64, _i64, _i32, ctypes.POINTER(Epilogue), _vp]),
+    "gemm_plan_strided_batched": (_i32, [_vp, ctypes.c_int, _i32, _i32, _i64, _i64, _i64, _vp, _i64, _i64, _vp,
+                                         _i64, _i64, _f32, _vp, _i64, _i64, _i64, _i32, ctypes.POINTER(Plan)]),
 }
 
 _lib = None
@@ -160,6 +164,14 @@ class Handle:
         return lib().gemm_run(self.ptr, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
                               dtype, stream)
 
+    def run_batched_raw(self, transA, transB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc,
+                        strideC, batch, dtype, stream, bias=0, act=ACT_NONE, out_scale=1.0):
+        """gemm_run_strided_batched on raw device pointers; returns the status code."""
+        epi = Epilogue(bias or None, int(act), float(out_scale))
+        return lib().gemm_run_strided_batched(self.ptr, transA, transB, M, N, K, alpha, A, lda, strideA, B, ldb,
+                                              strideB, beta, C, ldc, strideC, batch, dtype, ctypes.byref(epi),
+                                              stream)
+
     def run_ex_raw(self, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtype, stream,
                    bias=0, act=ACT_NONE, out_scale=1.0):
         """gemm_run_ex on raw device pointers (bias: device pointer or 0); returns the status code."""
@@ -178,6 +190,24 @@ def default_handle(device=None):
     if h is None:
         h = _default[dev] = Handle(dev)
     return h
+
+
+def plan_batched(M, N, K, batch, transA=0, transB=0, dtype=BF16_F32, lda=None, ldb=None, ldc=None,
+                 strideA=None, strideB=None, strideC=None, sm_count=152, A=0x1000, B=0x1000, C=0x1000, beta=0.0,
+                 handle=None):
+    """Host-only planner query for a strided batched call (strides default to packed)."""
+    lda = lda if lda is not None else (M if transA else K)
+    ldb = ldb if ldb is not None else (K if transB else N)
+    ldc = ldc if ldc is not None else N
+    strideA = strideA if strideA is not None else (K if transA else M) * lda
+    strideB = strideB if strideB is not None else (N if transB else K) * ldb
+    strideC = strideC if strideC is not None else M * ldc
+    p = Plan()
+    h = handle.ptr if handle is not None else None
+    st = lib().gemm_plan_strided_batched(h, sm_count, transA, transB, M, N, K, A, lda, strideA, B, ldb, strideB,
+                                         beta, C, ldc, strideC, batch, dtype, ctypes.byref(p))
+    _check(st, "gemm_plan_strided_batched")
+    return p
 
 
 def dtype_code(in_dtype, out_dtype, b_dtype=None):

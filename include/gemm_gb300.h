@@ -171,6 +171,30 @@ gemm_status_t gemm_run_ex(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, i
                           const gemm_epilogue_t* epi, void* stream);
 
 /*
+ * gemm_run_strided_batched: `batch` independent GEMMs in one launch,
+ *   C_b = alpha * op(A_b) * op(B_b) + beta * C_b   (with the fused epilogue epi, may be NULL)
+ * where A_b = A + b * strideA, B_b = B + b * strideB and C_b = C + b * strideC
+ * (strides in elements of each matrix's type), b = 0 .. batch - 1.  This is
+ * the shape of attention's per-(batch, head) products, Q (B*H, S, d) x K^T
+ * ("第4章：经典算子实现 —— GEMM", section 1), with the batch taken as a third
+ * dimension of the tensor-memory-accelerator copies ("CUDA GEMM 矩阵乘法优化
+ * 指南", 12.2: 3-D copies for attention heads).  All batches share one
+ * persistent schedule (their tiles follow one another), so a batch of small
+ * GEMMs still fills the GPU.
+ *   strideA / strideB  >= 0; 0 reuses one A (or B) for every batch.
+ *   strideC            >= (M - 1) * ldc + N when batch > 1 (no two C_b overlap).
+ *   bias (epi)         one value per column, the same for every batch.
+ * batch == 0 is a no-op.  Other arguments, layouts and errors as in gemm_run
+ * and gemm_run_ex; GEMM_ERR_UNSUPPORTED when the tiles of all batches exceed
+ * 2^30.
+ */
+gemm_status_t gemm_run_strided_batched(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int64_t M,
+                                       int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
+                                       int64_t strideA, const void* B, int64_t ldb, int64_t strideB,
+                                       float beta, void* C, int64_t ldc, int64_t strideC, int64_t batch,
+                                       gemm_dtype_t dtype, const gemm_epilogue_t* epi, void* stream);
+
+/*
  * gemm_get_status: synchronise `stream`, then read and clear the handle's
  * device status word.  Returns GEMM_OK, GEMM_ERR_TIMEOUT (a kernel waited
  * longer than the wait limit on one of its barriers and returned early; C is
@@ -229,7 +253,7 @@ typedef struct {
   int32_t grid;            /* CTAs launched for the main kernel */
   int32_t launches;        /* kernels launched by one gemm_run */
   int32_t schedule;        /* 0: whole (or split-K) tiles; 1: stream-K tail */
-  int64_t tiles;           /* schedule tiles = tiles_i * tiles_j */
+  int64_t tiles;           /* schedule tiles = tiles_i * tiles_j * batch */
   int64_t units;           /* work units over all CTAs (tiles, split pieces or stream-K pieces) */
   int64_t workspace_bytes; /* handle workspace this call needs */
   int32_t tiles_i;         /* schedule tiles along the MMA rows (M, or N when swapped) */
@@ -243,6 +267,7 @@ typedef struct {
                               complete one barrier */
   int32_t bulk_store;      /* how C leaves: 0 direct stores, 1 bulk tensor stores of rows,
                               2 bulk tensor stores of transposed blocks (swapped problems) */
+  int32_t batch;           /* GEMMs in the call (1 unless strided batched); tiles counts all */
 } gemm_plan_t;
 
 /*
@@ -258,6 +283,13 @@ gemm_status_t gemm_plan(gemm_handle_t h, int sm_count, gemm_op_t transA, gemm_op
                         int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                         const void* B, int64_t ldb, float beta, const void* C, int64_t ldc,
                         gemm_dtype_t dtype, gemm_plan_t* plan);
+
+/* gemm_plan for a strided batched call (arguments as gemm_run_strided_batched). */
+gemm_status_t gemm_plan_strided_batched(gemm_handle_t h, int sm_count, gemm_op_t transA, gemm_op_t transB,
+                                        int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                                        int64_t strideA, const void* B, int64_t ldb, int64_t strideB,
+                                        float beta, const void* C, int64_t ldc, int64_t strideC,
+                                        int64_t batch, gemm_dtype_t dtype, gemm_plan_t* plan);
 
 typedef enum {
   GEMM_OPT_WAIT_LIMIT_NS = 0, /* barrier wait limit in ns (default 2e9; >= 1e6) */

@@ -170,6 +170,28 @@ def test_plan_e4m3_output():
     assert G.plan(256, 256, 256, 0, 1, G.BF16_E4M3, ldc=260).vector_store == 0   # 260-byte rows
 
 
+def test_plan_strided_batched():
+    """A batch extends the tile grid; a stride of 0 shares one operand; C
+    batches may not overlap; misaligned batch strides repack every batch."""
+    p = G.plan_batched(2048, 2048, 128, 32, 0, 1, G.BF16_BF16)      # attention scores, 32 heads
+    assert p.batch == 32 and p.tiles == p.tiles_i * p.tiles_j * 32 and p.num_kb == 2
+    one = G.plan(2048, 2048, 128, 0, 1, G.BF16_BF16)
+    assert one.batch == 1 and one.tiles == one.tiles_i * one.tiles_j
+    s = G.plan_batched(64, 4096, 1024, 8, 0, 1, strideB=0)           # B shared, skinny M
+    assert s.swap_ab == 1 and s.batch == 8 and s.repack_a == 0 and s.repack_b == 0
+    r = G.plan_batched(100, 96, 64, 3, 0, 1, strideA=100 * 64 + 4)   # 8-byte gap: not 16-byte aligned
+    assert r.repack_a == 1 and r.workspace_bytes >= 3 * 100 * 64 * 2
+    assert G.plan_batched(100, 96, 64, 3, 0, 1, strideC=100 * 96 + 2).vector_store == 0   # 8-byte gap (fp32)
+    assert G.plan_batched(4, 4, 4, 0).path == G.PATH_NOOP
+    for bad in (dict(strideC=4 * 4 - 1), dict(strideA=-1)):
+        with pytest.raises(G.GemmError) as e:
+            G.plan_batched(4, 4, 4, 2, **bad)
+        assert e.value.status == G.ERR_INVALID_ARG
+    with pytest.raises(G.GemmError) as e:
+        G.plan_batched(65536, 65536, 64, 4096)        # 2^31 tiles in all
+    assert e.value.status == G.ERR_UNSUPPORTED
+
+
 def test_plan_half_atom_pairs_need_k_major_q():
     """A CTA pair with 64-wide tiles loads 32-row halves of the MMA's B operand,
     which only the K-major layout allows."""

@@ -34,36 +34,40 @@ def shim(tmp_path_factory):
 
 
 def params(plan_or_tuple):
+    """tiles_i tiles_j num_kb raster_group mode split_k dp_tiles sk_slots sk_iters batch."""
     p = plan_or_tuple
     if isinstance(p, tuple):
-        return np.array(p, dtype=np.int64)
+        return np.array(p + (1,) if len(p) == 9 else p, dtype=np.int64)
     sk_iters = (p.tiles - p.dp_tiles) * p.num_kb if p.schedule == 1 else 0
     return np.array([p.tiles_i, p.tiles_j, p.num_kb, p.raster_group, p.schedule, p.split_k, p.dp_tiles,
-                     p.sk_slots, sk_iters], dtype=np.int64)
+                     p.sk_slots, sk_iters, p.batch], dtype=np.int64)
 
 
 def enumerate_units(lib, prm, slots):
     units = []
     cap = 1 << 16
-    buf = np.zeros(11 * cap, dtype=np.int32)
+    buf = np.zeros(12 * cap, dtype=np.int32)
     for s in range(slots):
         n = lib.sched_units(prm.ctypes.data, s, slots, buf.ctypes.data, cap)
         assert n <= cap
         for k in range(n):
-            units.append((s, tuple(int(x) for x in buf[11 * k:11 * k + 11])))
+            units.append((s, tuple(int(x) for x in buf[12 * k:12 * k + 12])))
     return units
 
 
 def check_schedule(lib, prm, slots):
     tiles_i, tiles_j, num_kb, _, mode = (int(x) for x in prm[:5])
-    tiles = tiles_i * tiles_j
+    batch = int(prm[9])
+    tiles = tiles_i * tiles_j * batch
     units = enumerate_units(lib, prm, slots)
     by_tile = {}
     for s, u in units:
         by_tile.setdefault(u[2], []).append((s, u))
     assert sorted(by_tile) == list(range(tiles)), "every tile exactly once in the schedule"
-    pos = {(u[0], u[1]) for _, u in units}
-    assert len(pos) == tiles and all(0 <= a < tiles_i and 0 <= b < tiles_j for a, b in pos)
+    pos = {(u[11], u[0], u[1]) for _, u in units}
+    assert len(pos) == tiles and all(0 <= c < batch and 0 <= a < tiles_i and 0 <= b < tiles_j for c, a, b in pos)
+    for _, u in units:   # the tile index is batch-major
+        assert u[11] == u[2] // (tiles_i * tiles_j)
     n_pslots = lib.sched_partial_slots(prm.ctypes.data)
     used_pslots = set()
     counters = set()
@@ -123,3 +127,20 @@ def test_stream_k_edge_cases(shim, tiles_i, tiles_j, num_kb, slots, dp_tiles, sk
 @pytest.mark.parametrize("split", [1, 2, 3, 7, 64])
 def test_split_k_schedule(shim, split):
     check_schedule(shim, params((4, 6, 64, 5, 0, split, 0, 0, 0)), 9)
+
+
+@pytest.mark.parametrize("batch", [2, 7, 32])
+@pytest.mark.parametrize("mode", ["tiles", "split", "stream_k"])
+def test_batched_schedules(shim, batch, mode):
+    """A batch extends the tile grid: every (batch, tile, k-block) exactly once."""
+    ti, tj, kb, slots = 3, 5, 9, 13
+    tiles = ti * tj * batch
+    if mode == "tiles":
+        prm = (ti, tj, kb, 2, 0, 1, 0, 0, 0, batch)
+    elif mode == "split":
+        prm = (ti, tj, kb, 2, 0, 3, 0, 0, 0, batch)
+    else:
+        dp = (tiles // slots) * slots
+        iters = (tiles - dp) * kb
+        prm = (ti, tj, kb, 2, 1, 1, dp, min(slots, iters), iters, batch)
+    check_schedule(shim, params(prm), slots)
