@@ -212,6 +212,69 @@ def make_batched_problem(name, batch, M, N, K, transA=0, transB=0, in_dtype="bf1
                           A, lda, strideA, B, ldb, strideB, C0, ldc, strideC, seed, b_dtype)
 
 
+@dataclass
+class GroupedProblem:
+    """Grouped GEMMs with stacked rows (mixture-of-experts routing): group g owns
+    rows [off_g, off_g + m_sizes[g]) of A (sum(m) x K) and C (sum(m) x N) and
+    multiplies them by B_g = B[g * strideB:] (N x K when transB, else K x N)."""
+    name: str
+    m_sizes: list
+    N: int
+    K: int
+    transB: int
+    in_dtype: str
+    out_dtype: str
+    alpha: float
+    beta: float
+    A: torch.Tensor
+    lda: int
+    B: torch.Tensor
+    ldb: int
+    strideB: int
+    C0: object
+    ldc: int
+    seed: int
+    b_dtype: str = None
+
+    def __post_init__(self):
+        if self.b_dtype is None:
+            self.b_dtype = self.in_dtype
+
+    @property
+    def M(self):
+        return int(sum(self.m_sizes))
+
+
+def make_grouped_problem(name, m_sizes, N, K, transB=1, in_dtype="bf16", out_dtype="f32",
+                         dist_a=("normal", 0.0, 1.0), dist_b=("normal", 0.0, 0.02), alpha=1.0, beta=0.0,
+                         dist_c=("normal", 0.0, 1.0), seed=0, lda=None, ldb=None, strideB=None, ldc=None,
+                         b_dtype=None):
+    """A from seed, C0 from seed + 2, expert g's weights from seed + 3 + g."""
+    b_dtype = in_dtype if b_dtype is None else b_dtype
+    M = int(sum(m_sizes))
+    b_shape = (N, K) if transB else (K, N)
+    lda = K if lda is None else lda
+    ldb = b_shape[1] if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    strideB = b_shape[0] * ldb if strideB is None else strideB
+    A = _pad_columns(draw((M, K), dist_a, seed, in_dtype), lda, in_dtype)
+    B = _stack([_pad_columns(draw(b_shape, dist_b, seed + 3 + g, b_dtype), ldb, b_dtype)
+                for g in range(len(m_sizes))], strideB, b_dtype)
+    C0 = None
+    if beta != 0.0:
+        C0 = _pad_columns(draw((M, N), dist_c, seed + 2, out_dtype), ldc, out_dtype)
+    return GroupedProblem(name, [int(m) for m in m_sizes], N, K, transB, in_dtype, out_dtype, float(alpha),
+                          float(beta), A, lda, B, ldb, strideB, C0, ldc, seed, b_dtype)
+
+
+def moe_routing(tokens=8192, experts=64, seed=0):
+    """Uneven tokens per expert for a mixture-of-experts layer: a seeded
+    multinomial draw of `tokens` routed tokens over `experts` experts."""
+    g = _rng(seed)
+    w = g.gamma(2.0, 1.0, experts)
+    return [int(x) for x in g.multinomial(tokens, w / w.sum())]
+
+
 # ---------------------------------------------------------------------------
 # The workloads, named by what they are.
 # ---------------------------------------------------------------------------

@@ -62,6 +62,9 @@ def _load():
     lib.oracle_gemm_batched.restype = i32
     lib.oracle_gemm_batched.argtypes = [i32, i32, i64, i64, i64, dbl, vp, i64, i64, vp, i64, i64, dbl, vp, i32,
                                         i64, i64, i32, i32, i64, vp, vp, i64, i32]
+    lib.oracle_gemm_grouped.restype = i32
+    lib.oracle_gemm_grouped.argtypes = [i32, i64, vp, i64, i64, dbl, vp, i64, vp, i64, i64, dbl, vp, i32, i64, i32,
+                                        i32, vp, vp, i64, i32]
     lib.oracle_epilogue.restype = i32
     lib.oracle_epilogue.argtypes = [i64, i64, vp, vp, i64, vp, i32, dbl]
     lib.oracle_e4m3_value.restype = dbl
@@ -156,6 +159,26 @@ def gemm_batched(transA, transB, M, N, K, alpha, A, lda, strideA, B, ldb, stride
                                  int(in_type), int(b_type), batch, _ptr(R), _ptr(Mag), N, int(nthreads))
     if rc < 0:
         raise ValueError("oracle_gemm_batched rejected its arguments")
+    return R, Mag
+
+
+def gemm_grouped(transB, m_sizes, N, K, alpha, A, lda, B, ldb, strideB, beta, C0, ldc, in_type, c_type=C_F32,
+                 nthreads=0, b_type=None):
+    """Grouped oracle.  Returns (R, Mag): fp64 arrays of shape (sum(m_sizes), N)."""
+    lib = _load()
+    b_type = in_type if b_type is None else b_type
+    sizes = np.ascontiguousarray(m_sizes, dtype=np.int64)
+    A = _codes(A, in_type).reshape(-1)
+    B = _codes(B, b_type).reshape(-1)
+    C0 = _c0_array(C0, c_type).reshape(-1) if beta != 0.0 else None
+    rows = int(sizes.sum())
+    R = np.zeros((rows, N), dtype=np.float64)
+    Mag = np.zeros((rows, N), dtype=np.float64)
+    rc = lib.oracle_gemm_grouped(int(transB), sizes.size, _ptr(sizes), N, K, float(alpha), _ptr(A), lda, _ptr(B),
+                                 ldb, strideB, float(beta), _ptr(C0), int(c_type), ldc, int(in_type), int(b_type),
+                                 _ptr(R), _ptr(Mag), N, int(nthreads))
+    if rc < 0:
+        raise ValueError("oracle_gemm_grouped rejected its arguments")
     return R, Mag
 
 

@@ -364,3 +364,36 @@ int oracle_gemm_batched(int transA, int transB, int64_t M, int64_t N, int64_t K,
   }
   return used;
 }
+
+/*
+ * Grouped oracle (mixture-of-experts routing, the grouped GEMM of DeepGEMM that
+ * "第4章：经典算子实现 —— GEMM" points to for MoE): `groups` GEMMs whose
+ * rows are stacked.  Group g owns rows [off_g, off_g + m_sizes[g]) of A (stored
+ * sum(m) x K, row-major, lda) and of C / R / Mag (sum(m) x N), off_g being the
+ * sum of the sizes before it, and multiplies them by its own B_g = B + g * strideB
+ * (transB as in oracle_gemm):
+ *   R[off_g + i][j] = alpha * sum_k A[off_g + i][k] * b_g(k, j) + beta * C0[off_g + i][j].
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_gemm_grouped(int transB, int64_t groups, const int64_t* m_sizes, int64_t N, int64_t K,
+                        double alpha, const void* A, int64_t lda, const void* B, int64_t ldb,
+                        int64_t strideB, double beta, const void* C0, int c_type, int64_t ldc,
+                        int a_type, int b_type, double* R, double* Mag, int64_t ldr, int nthreads) {
+  if (groups < 0 || strideB < 0) return -1;
+  const int64_t ea = (a_type == ORACLE_IN_E4M3 || a_type == ORACLE_IN_E5M2) ? 1 : 2;
+  const int64_t eb = (b_type == ORACLE_IN_E4M3 || b_type == ORACLE_IN_E5M2) ? 1 : 2;
+  const int64_t ec = c_type == ORACLE_C_F32 ? 4 : 2;
+  int64_t off = 0;
+  for (int64_t g = 0; g < groups; ++g) {
+    const int64_t m = m_sizes[g];
+    if (m < 0) return -1;
+    const char* Ag = (const char*)A + off * lda * ea;
+    const char* Bg = (const char*)B + g * strideB * eb;
+    const char* Cg = C0 ? (const char*)C0 + off * ldc * ec : NULL;
+    if (m > 0 && oracle_gemm_ab(0, transB, m, N, K, alpha, Ag, lda, Bg, ldb, beta, Cg, c_type, ldc,
+                                a_type, b_type, R + off * ldr, Mag + off * ldr, ldr, nthreads) < 0)
+      return -1;
+    off += m;
+  }
+  return 0;
+}

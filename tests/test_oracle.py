@@ -460,6 +460,46 @@ def test_batched_fp8_and_empty_batch():
 
 
 # ---------------------------------------------------------------------------
+# Grouped GEMM (stacked rows, one weight matrix per group)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("transB", [0, 1])
+def test_grouped_matches_per_group_library_matmul(transB):
+    sizes = [5, 0, 17, 1, 9]
+    N, K = 13, 40
+    p = inputs.make_grouped_problem("og", sizes, N, K, transB, "bf16", "f32", alpha=1.5, beta=-0.5, seed=4,
+                                    lda=K + 3, ldb=(K if transB else N) + 2, ldc=N + 1)
+    b_rows = N if transB else K
+    ldb = (K if transB else N) + 2
+    R, Mag = oracle.gemm_grouped(transB, sizes, N, K, p.alpha, inputs.bits(p.A), p.lda, inputs.bits(p.B), p.ldb,
+                                 p.strideB, p.beta, p.C0.numpy(), p.ldc, oracle.IN_BF16)
+    a = p.A.to(torch.float64).numpy()[:, :K]
+    c0 = p.C0.to(torch.float64).numpy()[:, :N]
+    Bs = _batch_mats(p.B, len(sizes), p.strideB, b_rows, ldb, K if transB else N)
+    off = 0
+    for g, m in enumerate(sizes):
+        bg = Bs[g].T if transB else Bs[g]
+        ref = p.alpha * (a[off:off + m] @ bg) + p.beta * c0[off:off + m]
+        assert np.allclose(R[off:off + m], ref, rtol=1e-12, atol=1e-12), g
+        off += m
+    assert R.shape == (sum(sizes), N)
+
+
+def test_grouped_single_group_is_the_plain_gemm():
+    p = inputs.make_grouped_problem("og1", [37], 21, 50, 1, "f16", "f32", seed=5)
+    R, Mag = oracle.gemm_grouped(1, [37], 21, 50, 1.0, inputs.bits(p.A), 50, inputs.bits(p.B), 50, p.strideB, 0.0,
+                                 None, 21, oracle.IN_F16)
+    R1, M1 = oracle.gemm(0, 1, 37, 21, 50, 1.0, inputs.bits(p.A), 50, inputs.bits(p.B), 50, 0.0, None, 21,
+                         oracle.IN_F16)
+    assert np.array_equal(R, R1) and np.array_equal(Mag, M1)
+
+
+def test_moe_routing_sizes():
+    s = inputs.moe_routing(8192, 64, seed=0)
+    assert len(s) == 64 and sum(s) == 8192 and min(s) >= 0 and max(s) > 2 * 8192 // 64   # uneven
+
+
+# ---------------------------------------------------------------------------
 # Fused epilogue: bias, activation, output scale
 # ---------------------------------------------------------------------------
 

@@ -31,6 +31,8 @@ MUTATIONS = {
     "output scale dropped": ("R[i * ldr + j] = scale * d;", "R[i * ldr + j] = d;"),
     "B batch stride ignored": ("(const char*)B + b * strideB * eb", "(const char*)B"),
     "C0 batch offset ignored": ("(const char*)C0 + b * strideC * ec", "(const char*)C0"),
+    "group weights not advanced": ("(const char*)B + g * strideB * eb", "(const char*)B"),
+    "group rows not offset": ("(const char*)A + off * lda * ea", "(const char*)A"),
 }
 
 
