@@ -17,6 +17,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/gemm_gb300.h"
 #include "gemm_internal.h"
@@ -65,6 +66,10 @@ struct Plan {
   int64_t I = 0, J = 0, K = 0;
   int64_t c_si = 0, c_sj = 0;
   int64_t batch = 1, c_sb = 0;  // strided batch: count, C's batch stride in elements
+  // grouped GEMMs: per-group tile prefix, first row and row count (host copies)
+  std::vector<int32_t> group_tiles, group_m;
+  std::vector<int64_t> group_row;
+  size_t group_offset = 0;      // their place in the workspace
   int32_t c_type = kCF32;
   int32_t eb = 2;                  // input element bytes (2: bf16 / fp16, 1: FP8)
   uint32_t a_fmt = 1, b_fmt = 1;   // instruction-descriptor formats of the stored A and B
@@ -282,7 +287,7 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
                         int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                         int64_t ldb, float beta, const void* C, int64_t ldc, gemm_dtype_t dtype,
                         Plan* out, int64_t batch = 1, int64_t strideA = 0, int64_t strideB = 0,
-                        int64_t strideC = 0) {
+                        int64_t strideC = 0, int64_t groups = 0, const int64_t* m_sizes = nullptr) {
   Plan pl;
   gemm_plan_t& P = pl.pub;
   if ((transA != GEMM_OP_N && transA != GEMM_OP_T) || (transB != GEMM_OP_N && transB != GEMM_OP_T))
@@ -296,7 +301,16 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   // E4M3 output is a quantised result, written only.
   if (dt.c_type == kCE4M3 && beta != 0.0f) return GEMM_ERR_UNSUPPORTED;
   const int64_t c_elem = pl.c_type == kCF32 ? 4 : pl.c_type == kCE4M3 ? 1 : 2;
-  if (batch < 0 || strideA < 0 || strideB < 0 || strideC < 0) return GEMM_ERR_INVALID_ARG;
+  if (batch < 0 || strideA < 0 || strideB < 0 || strideC < 0 || groups < 0) return GEMM_ERR_INVALID_ARG;
+  if (groups > 0) {  // stacked rows: A (sum m) x K row-major, one B per group
+    if (!m_sizes || transA != GEMM_OP_N || batch != 1) return GEMM_ERR_INVALID_ARG;
+    M = 0;
+    for (int64_t g = 0; g < groups; ++g) {
+      if (m_sizes[g] < 0) return GEMM_ERR_INVALID_ARG;
+      M += m_sizes[g];
+    }
+    pl.I = M;  // the stacked rows (also what the K == 0 path scales)
+  }
   P.batch = static_cast<int32_t>(batch > 1 ? batch : 1);
   if (M == 0 || N == 0 || batch == 0) {
     P.path = GEMM_PATH_NOOP;
@@ -329,11 +343,12 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   b.rows = b.kmajor ? N : K; b.cols = b.kmajor ? K : N;
   a.nb = (batch > 1 && strideA > 0) ? batch : 1;  // a stride of 0 shares one matrix
   b.nb = (batch > 1 && strideB > 0) ? batch : 1;
+  if (groups > 1 && strideB > 0) b.nb = groups;  // one weight matrix per group
   a.bstride = a.nb > 1 ? strideA : 0;
   b.bstride = b.nb > 1 ? strideB : 0;
 
   // A short M rides on the MMA's N dimension: compute C^T = op(B)^T op(A)^T.
-  const bool swap = M <= 64 && N > M;
+  const bool swap = groups == 0 && M <= 64 && N > M;
   P.swap_ab = swap ? 1 : 0;
   pl.I = swap ? N : M;
   pl.J = swap ? M : N;
@@ -364,6 +379,7 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   for (int cfg : kPreference) {
     const TileConfig& c = kTileConfigs[cfg];
     if (c.eb != dt.eb) continue;
+    if (groups > 0 && c.mc == 2) continue;  // groups share no A tile between neighbouring tiles
     const int path = c.mc == 2 ? GEMM_PATH_TC_2CTA_MULTICAST : c.cg == 2 ? GEMM_PATH_TC_2CTA : GEMM_PATH_TC_1CTA;
     if (o.force_path && o.force_path != path) continue;
     if (o.force_bn && c.bn != o.force_bn) continue;
@@ -376,7 +392,14 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
     // Two k-slices per stage where the ring still holds at least two such stages.
     int kdepth = o.kdepth ? o.kdepth : default_kdepth(c);
     if (kdepth > 1 && tc_stages(cfg) / kdepth < 2) kdepth = 1;
-    Choice ch = choose_schedule(o, cdiv(pl.I, kBM * c.cg), cdiv(cdiv(pl.J, c.bn), c.mc), batch,
+    // grouped: each group's rows padded to whole tiles
+    int64_t tile_rows = cdiv(pl.I, kBM * c.cg);
+    if (groups > 0) {
+      tile_rows = 0;
+      for (int64_t g = 0; g < groups; ++g) tile_rows += cdiv(m_sizes[g], kBM * c.cg);
+      if (tile_rows == 0) tile_rows = 1;
+    }
+    Choice ch = choose_schedule(o, tile_rows, cdiv(cdiv(pl.J, c.bn), c.mc), batch,
                                 cdiv(num_kslices, kdepth), kdepth, cfg, nslots, hbm_bound);
     if (ch.valid && ch.cost < best.cost - 1e-9) best = ch;
   }
@@ -385,6 +408,20 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   const int cl = best.cg * best.mc;
   pl.sched = best.sched;
   pl.cfg = best.cfg;
+  if (groups > 0) {
+    const int64_t tile_m = kBM * best.cg;
+    pl.group_tiles.assign(1, 0);
+    int64_t row = 0;
+    for (int64_t g = 0; g < groups; ++g) {
+      pl.group_tiles.push_back(pl.group_tiles.back() +
+                               static_cast<int32_t>(cdiv(m_sizes[g], tile_m) * pl.sched.tiles_j));
+      pl.group_row.push_back(row);
+      pl.group_m.push_back(static_cast<int32_t>(m_sizes[g]));
+      row += m_sizes[g];
+    }
+    pl.sched.groups = static_cast<int32_t>(groups);
+    pl.sched.group_tile_start = pl.group_tiles.data();  // the host copy, for planning
+  }
   pl.sched.raster_group = o.raster_group ? o.raster_group : 8;
   if (pl.sched.raster_group > pl.sched.tiles_i) pl.sched.raster_group = pl.sched.tiles_i;
   P.path = best.mc == 2 ? GEMM_PATH_TC_2CTA_MULTICAST : cg == 2 ? GEMM_PATH_TC_2CTA : GEMM_PATH_TC_1CTA;
@@ -419,6 +456,11 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   }
   P.repack_a = (swap ? pl.q.repack : pl.p.repack) ? 1 : 0;
   P.repack_b = (swap ? pl.p.repack : pl.q.repack) ? 1 : 0;
+  if (groups > 0) {
+    pl.group_offset = ws;
+    ws = round_up(ws + (groups + 1) * 4 + groups * 4, 8);
+    ws = round_up(ws + groups * 8, 256);
+  }
   if (needs_partials(pl.sched)) {
     pl.partial_offset = ws;
     ws = round_up(ws + static_cast<size_t>(partial_slots(pl.sched)) * cl * best.bn * kBM * 4, 256);
@@ -432,12 +474,14 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   // written whole, past column N); the blend with the old C (beta != 0) keeps
   // the direct path, which reads C as it writes it.  A swapped problem stores
   // transposed blocks (C's rows run along the kernel's J).
+  // (a group's rows end inside C: a bulk store could not stop at the group's edge)
   const bool bulk = c_rows_aligned && (N * c_elem) % 16 == 0 && beta == 0.0f && o.tma_store != 2 &&
-                    pl.c_type != kCE4M3;  // 8-bit C leaves through direct stores
+                    pl.c_type != kCE4M3 && groups == 0;  // 8-bit C leaves through direct stores
   pl.tma_store = !bulk ? kBulkNone : swap ? kBulkTransposed : kBulkRows;
   P.bulk_store = pl.tma_store;
   P.launches = 1 + P.repack_a + P.repack_b;
   *out = pl;
+  if (out->sched.groups > 0) out->sched.group_tile_start = out->group_tiles.data();  // the copy's own table
   return GEMM_OK;
 }
 
@@ -699,11 +743,13 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
                               int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
                               const void* B, int64_t ldb, float beta, void* C, int64_t ldc,
                               gemm_dtype_t dtype, EpiOps ops, void* stream, int64_t batch = 1,
-                              int64_t strideA = 0, int64_t strideB = 0, int64_t strideC = 0) {
+                              int64_t strideA = 0, int64_t strideB = 0, int64_t strideC = 0,
+                              int64_t groups = 0, const int64_t* m_sizes = nullptr) {
   if (!h) return GEMM_ERR_INVALID_ARG;
   Plan pl;
   gemm_status_t s = make_plan(h->opt, h->slots, transA, transB, M, N, K, A, lda, B, ldb, beta,
-                              C, ldc, dtype, &pl, batch, strideA, strideB, strideC);
+                              C, ldc, dtype, &pl, batch, strideA, strideB, strideC, groups, m_sizes);
+  if (s == GEMM_OK && groups > 0) M = pl.I;  // the stacked rows
   if (s != GEMM_OK) return s;
   const gemm_plan_t& P = pl.pub;
   if (P.path == GEMM_PATH_NOOP) return GEMM_OK;
@@ -793,6 +839,20 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
   a.counters = h->d_counters;
   a.status = h->d_status;
   a.wait_limit_ns = static_cast<uint64_t>(h->opt.wait_limit_ns);
+  if (pl.sched.groups > 0) {  // the group tables go to the workspace with the launch's stream
+    const int64_t G = pl.sched.groups;
+    uint8_t* base = ws + pl.group_offset;
+    int32_t* d_tiles = reinterpret_cast<int32_t*>(base);
+    int32_t* d_m = d_tiles + (G + 1);
+    int64_t* d_row = reinterpret_cast<int64_t*>(base + round_up((G + 1) * 4 + G * 4, 8));
+    e = cudaMemcpyAsync(d_tiles, pl.group_tiles.data(), (G + 1) * 4, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(d_m, pl.group_m.data(), G * 4, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(d_row, pl.group_row.data(), G * 8, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(h, e);
+    a.sched.group_tile_start = d_tiles;
+    a.group_m = d_m;
+    a.group_row = d_row;
+  }
   a.drop_load = h->opt.drop_load;
   ops.bias_on_i = P.swap_ab;  // a swapped problem computes C^T: C's columns are the kernel's rows
   a.ops = ops;
@@ -832,6 +892,39 @@ gemm_status_t gemm_run_ex(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, i
   gemm_status_t s = epi_ops(epi, &ops);
   if (s != GEMM_OK) return s;
   return run_gemm(h, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtype, ops, stream);
+}
+
+gemm_status_t gemm_run_grouped(gemm_handle_t h, gemm_op_t transB, int64_t groups, const int64_t* m_sizes,
+                               int64_t N, int64_t K, float alpha, const void* A, int64_t lda, const void* B,
+                               int64_t ldb, int64_t strideB, float beta, void* C, int64_t ldc,
+                               gemm_dtype_t dtype, const gemm_epilogue_t* epi, void* stream) {
+  EpiOps ops;
+  gemm_status_t s = epi_ops(epi, &ops);
+  if (s != GEMM_OK) return s;
+  if (!h || groups < 0 || (groups > 0 && !m_sizes)) return GEMM_ERR_INVALID_ARG;
+  if (groups == 0) return GEMM_OK;
+  return run_gemm(h, GEMM_OP_N, transB, 0, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtype, ops, stream, 1, 0,
+                  strideB, 0, groups, m_sizes);
+}
+
+gemm_status_t gemm_plan_grouped(gemm_handle_t h, int sm_count, gemm_op_t transB, int64_t groups,
+                                const int64_t* m_sizes, int64_t N, int64_t K, const void* A, int64_t lda,
+                                const void* B, int64_t ldb, int64_t strideB, float beta, const void* C,
+                                int64_t ldc, gemm_dtype_t dtype, gemm_plan_t* plan) {
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  if (!h && sm_count <= 0) return GEMM_ERR_INVALID_ARG;
+  if (groups < 0 || (groups > 0 && !m_sizes)) return GEMM_ERR_INVALID_ARG;
+  Options o = h ? h->opt : Options();
+  const SlotTable slots = h ? h->slots : SlotTable::even(sm_count);
+  Plan pl;
+  gemm_status_t s = GEMM_OK;
+  if (groups == 0)
+    pl.pub.path = GEMM_PATH_NOOP;
+  else
+    s = make_plan(o, slots, GEMM_OP_N, transB, 0, N, K, A, lda, B, ldb, beta, C, ldc, dtype, &pl, 1, 0, strideB,
+                  0, groups, m_sizes);
+  if (s == GEMM_OK) *plan = pl.pub;
+  return s;
 }
 
 gemm_status_t gemm_run_strided_batched(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int64_t M,

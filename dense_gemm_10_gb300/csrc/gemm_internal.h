@@ -66,6 +66,10 @@ struct TcArgs {
   int64_t c_sb;          // batch stride of C in elements (strided batches; tile batch in Unit::tb)
   int32_t p_bcast;       // P is one matrix shared by every batch (its tensor map has one batch)
   int32_t q_bcast;
+  // grouped GEMMs (sched.groups > 0): group g's rows of P and C start at row
+  // group_row[g] and number group_m[g]; the tile's group is Unit::tb
+  const int64_t* group_row;
+  const int32_t* group_m;
 };
 
 // Epilogue store paths: direct stores, or staged bulk tensor stores of rows of

@@ -18,6 +18,8 @@
 // A strided batch of GEMMs shares one schedule: the tiles of batch b follow
 // those of batch b - 1 (tile index = b * tiles_i * tiles_j + raster position),
 // so whole tiles, split-K and stream-K treat the batch as one larger grid.
+// Grouped GEMMs (groups > 0) do the same with a different row count per group:
+// group g owns tiles [group_tile_start[g], group_tile_start[g + 1]).
 // A tile split over several units is finished by whichever contribution
 // arrives last: every contribution stores an fp32 partial, and the last one
 // sums all partials in k order, so results do not depend on timing.
@@ -38,6 +40,8 @@ enum : int32_t { kSchedTiles = 0, kSchedStreamK = 1 };
 struct Sched {
   int32_t tiles_i, tiles_j;  // output tiles along I and J (of one batch)
   int32_t batch;             // independent GEMMs sharing the schedule (>= 1)
+  int32_t groups;            // > 0: grouped GEMMs, tile ranges in group_tile_start
+  const int32_t* group_tile_start;  // groups + 1 prefix sums of tile_rows_g * tiles_j
   int32_t num_kb;            // k-blocks per tile
   int32_t raster_group;      // tile rows per raster group
   int32_t mode;              // kSchedTiles or kSchedStreamK
@@ -49,7 +53,7 @@ struct Sched {
 
 struct Unit {
   int32_t ti, tj, tile;  // output tile (raster position and linear index)
-  int32_t tb;            // batch of the tile
+  int32_t tb;            // batch (or group) of the tile
   int32_t kb0, kb1;      // k-blocks [kb0, kb1) of the tile
   int32_t partial;       // 1: store an fp32 partial; the last contribution sums them
   int32_t pslot;         // partial slot of this contribution
@@ -61,6 +65,7 @@ struct Unit {
 
 // Output tiles of the whole schedule (every batch).
 G10_HD int64_t sched_tiles(const Sched& s) {
+  if (s.groups > 0) return s.group_tile_start[s.groups];
   return static_cast<int64_t>(s.tiles_i) * s.tiles_j * s.batch;
 }
 
@@ -69,13 +74,26 @@ G10_HD int64_t sched_tiles(const Sched& s) {
 // moving one column right, so that tiles running together share rows of P and
 // columns of Q in L2 ("GPU GEMM 优化完全拆解（三）", rasterization).
 G10_HD void raster_tile(const Sched& s, int32_t tile, int32_t& ti, int32_t& tj, int32_t& tb) {
-  const int32_t per_batch = s.tiles_i * s.tiles_j;
-  tb = tile / per_batch;
-  tile -= tb * per_batch;
+  int32_t tiles_i = s.tiles_i;
+  if (s.groups > 0) {  // the group holding the tile: the last start <= tile
+    int32_t lo = 0, hi = s.groups - 1;
+    while (lo < hi) {
+      const int32_t mid = (lo + hi + 1) / 2;
+      if (s.group_tile_start[mid] <= tile) lo = mid;
+      else hi = mid - 1;
+    }
+    tb = lo;
+    tiles_i = (s.group_tile_start[lo + 1] - s.group_tile_start[lo]) / s.tiles_j;
+    tile -= s.group_tile_start[lo];
+  } else {
+    const int32_t per_batch = s.tiles_i * s.tiles_j;
+    tb = tile / per_batch;
+    tile -= tb * per_batch;
+  }
   const int32_t group_tiles = s.raster_group * s.tiles_j;
   const int32_t g = tile / group_tiles;
   const int32_t first_i = g * s.raster_group;
-  const int32_t rows = (s.tiles_i - first_i) < s.raster_group ? (s.tiles_i - first_i) : s.raster_group;
+  const int32_t rows = (tiles_i - first_i) < s.raster_group ? (tiles_i - first_i) : s.raster_group;
   const int32_t r = tile - g * group_tiles;
   ti = first_i + r % rows;
   tj = r / rows;

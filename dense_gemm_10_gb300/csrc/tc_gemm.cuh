@@ -440,7 +440,8 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
   WorkIter work(a.sched, first, stride);
   Unit w;
   while (ok && work.next(w)) {
-    const int i0 = w.ti * Cfg::kTileM + q * kBM;
+    // (grouped GEMMs: the group's rows start further down P)
+    const int i0 = (a.sched.groups > 0 ? static_cast<int>(a.group_row[w.tb]) : 0) + w.ti * Cfg::kTileM + q * kBM;
     const int j0 = (w.tj * MC + pair) * BN + q * Cfg::kQRows;
     const int zp = a.p_bcast ? 0 : w.tb;  // batch coordinate (0 for an operand shared by all batches)
     const int zq = a.q_bcast ? 0 : w.tb;
@@ -665,8 +666,15 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
     const int jt = (w.tj * MC + pair) * BN;  // first column of this pair's tile
     out.y0 = w.ti * Cfg::kTileM + q * kBM + quarter * 32;
     out.z = w.tb;
-    out.c.C = static_cast<char*>(out.c0) +
-              static_cast<int64_t>(w.tb) * a.c_sb * (a.c_type == kCF32 ? 4 : a.c_type == kCE4M3 ? 1 : 2);
+    {
+      const int64_t esize = a.c_type == kCF32 ? 4 : a.c_type == kCE4M3 ? 1 : 2;
+      if (a.sched.groups > 0) {  // the group's rows of C; rows past its count are not stored
+        out.c.C = static_cast<char*>(out.c0) + a.group_row[w.tb] * a.c_si * esize;
+        out.c.I = a.group_m[w.tb];
+      } else {
+        out.c.C = static_cast<char*>(out.c0) + static_cast<int64_t>(w.tb) * a.c_sb * esize;
+      }
+    }
     if (!w.partial) {
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {

@@ -77,6 +77,10 @@ SIGNATURES = {
                                         _i64, _f32, _vp, _i64, _i64, _i64, _i32, ctypes.POINTER(Epilogue), _vp]),
     "gemm_plan_strided_batched": (_i32, [_vp, ctypes.c_int, _i32, _i32, _i64, _i64, _i64, _vp, _i64, _i64, _vp,
                                          _i64, _i64, _f32, _vp, _i64, _i64, _i64, _i32, ctypes.POINTER(Plan)]),
+    "gemm_run_grouped": (_i32, [_vp, _i32, _i64, _vp, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _i64, _f32, _vp, _i64,
+                                _i32, ctypes.POINTER(Epilogue), _vp]),
+    "gemm_plan_grouped": (_i32, [_vp, ctypes.c_int, _i32, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _f32, _vp,
+                                 _i64, _i32, ctypes.POINTER(Plan)]),
 }
 
 _lib = None
@@ -172,6 +176,14 @@ class Handle:
                                               strideB, beta, C, ldc, strideC, batch, dtype, ctypes.byref(epi),
                                               stream)
 
+    def run_grouped_raw(self, transB, m_sizes, N, K, alpha, A, lda, B, ldb, strideB, beta, C, ldc, dtype, stream,
+                        bias=0, act=ACT_NONE, out_scale=1.0):
+        """gemm_run_grouped on raw device pointers, group sizes from a Python list; returns the status."""
+        sizes = (ctypes.c_int64 * max(1, len(m_sizes)))(*m_sizes)
+        epi = Epilogue(bias or None, int(act), float(out_scale))
+        return lib().gemm_run_grouped(self.ptr, transB, len(m_sizes), ctypes.cast(sizes, _vp), N, K, alpha, A, lda, B,
+                                      ldb, strideB, beta, C, ldc, dtype, ctypes.byref(epi), stream)
+
     def run_ex_raw(self, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtype, stream,
                    bias=0, act=ACT_NONE, out_scale=1.0):
         """gemm_run_ex on raw device pointers (bias: device pointer or 0); returns the status code."""
@@ -207,6 +219,22 @@ def plan_batched(M, N, K, batch, transA=0, transB=0, dtype=BF16_F32, lda=None, l
     st = lib().gemm_plan_strided_batched(h, sm_count, transA, transB, M, N, K, A, lda, strideA, B, ldb, strideB,
                                          beta, C, ldc, strideC, batch, dtype, ctypes.byref(p))
     _check(st, "gemm_plan_strided_batched")
+    return p
+
+
+def plan_grouped(m_sizes, N, K, transB=1, dtype=BF16_F32, lda=None, ldb=None, strideB=None, ldc=None, sm_count=152,
+                 A=0x1000, B=0x1000, C=0x1000, beta=0.0, handle=None):
+    """Host-only planner query for a grouped call."""
+    lda = K if lda is None else lda
+    ldb = ldb if ldb is not None else (K if transB else N)
+    ldc = N if ldc is None else ldc
+    strideB = strideB if strideB is not None else (N if transB else K) * ldb
+    sizes = (ctypes.c_int64 * max(1, len(m_sizes)))(*m_sizes)
+    p = Plan()
+    h = handle.ptr if handle is not None else None
+    st = lib().gemm_plan_grouped(h, sm_count, transB, len(m_sizes), ctypes.cast(sizes, _vp), N, K, A, lda, B, ldb,
+                                 strideB, beta, C, ldc, dtype, ctypes.byref(p))
+    _check(st, "gemm_plan_grouped")
     return p
 
 

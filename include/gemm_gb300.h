@@ -284,6 +284,34 @@ gemm_status_t gemm_plan(gemm_handle_t h, int sm_count, gemm_op_t transA, gemm_op
                         const void* B, int64_t ldb, float beta, const void* C, int64_t ldc,
                         gemm_dtype_t dtype, gemm_plan_t* plan);
 
+/*
+ * gemm_run_grouped: `groups` GEMMs with stacked rows, the grouped GEMM of
+ * mixture-of-experts layers (DeepGEMM's, which "第4章：经典算子实现 —— GEMM"
+ * cites for MoE routing): tokens sorted by expert, expert g owning
+ * m_sizes[g] consecutive rows (m_sizes: a host array; 0 is allowed):
+ *   C[off_g + i, :] = alpha * A[off_g + i, :] * op(B_g) + beta * C[off_g + i, :],  i < m_sizes[g]
+ * with off_g the sum of the sizes before g.  A is stored sum(m) x K row-major
+ * (lda >= K); B_g = B + g * strideB (elements) is N x K when transB ==
+ * GEMM_OP_T, else K x N; C is sum(m) x N (ldc).  strideB == 0 gives every group
+ * the same B.  One launch covers every group: the groups' tiles share one
+ * persistent schedule, a group's last tile rows are masked at its edge, and C
+ * leaves through direct stores.  8-bit inputs need transB == GEMM_OP_T.
+ * groups == 0 is a no-op.  The fused epilogue `epi` (may be NULL) applies as
+ * in gemm_run_ex.  Errors as gemm_run_ex; GEMM_ERR_INVALID_ARG for a negative
+ * size or a missing m_sizes.
+ */
+gemm_status_t gemm_run_grouped(gemm_handle_t h, gemm_op_t transB, int64_t groups, const int64_t* m_sizes,
+                               int64_t N, int64_t K, float alpha, const void* A, int64_t lda, const void* B,
+                               int64_t ldb, int64_t strideB, float beta, void* C, int64_t ldc,
+                               gemm_dtype_t dtype, const gemm_epilogue_t* epi, void* stream);
+
+/* gemm_plan for a grouped call (arguments as gemm_run_grouped; tiles_i counts
+   every group's tile rows). */
+gemm_status_t gemm_plan_grouped(gemm_handle_t h, int sm_count, gemm_op_t transB, int64_t groups,
+                                const int64_t* m_sizes, int64_t N, int64_t K, const void* A, int64_t lda,
+                                const void* B, int64_t ldb, int64_t strideB, float beta, const void* C,
+                                int64_t ldc, gemm_dtype_t dtype, gemm_plan_t* plan);
+
 /* gemm_plan for a strided batched call (arguments as gemm_run_strided_batched). */
 gemm_status_t gemm_plan_strided_batched(gemm_handle_t h, int sm_count, gemm_op_t transA, gemm_op_t transB,
                                         int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,

@@ -192,6 +192,25 @@ def test_plan_strided_batched():
     assert e.value.status == G.ERR_UNSUPPORTED
 
 
+def test_plan_grouped():
+    """Grouped calls: tiles counted per group (padded to whole tiles), no
+    multicast, direct stores; sizes must be non-negative."""
+    sizes = [5, 0, 130, 1, 257, 64]
+    p = G.plan_grouped(sizes, 300, 200, 1)
+    cg = p.bm // 128
+    rows = sum(-(-m // (128 * cg)) for m in sizes)
+    assert p.tiles == rows * p.tiles_j and p.path != G.PATH_TC_2CTA_MULTICAST and p.bulk_store == G.BULK_NONE
+    assert p.swap_ab == 0 and p.workspace_bytes >= (len(sizes) + 1) * 4
+    assert G.plan_grouped([], 8, 8).path == G.PATH_NOOP
+    assert G.plan_grouped([4, 0], 8, 0).path == G.PATH_SCALE_C
+    with pytest.raises(G.GemmError) as e:
+        G.plan_grouped([3, -1], 8, 8)
+    assert e.value.status == G.ERR_INVALID_ARG
+    with pytest.raises(G.GemmError) as e:
+        G.plan_grouped([3, 4], 8, 32, 0, G.E4M3_F32)       # 8-bit weights must be N x K
+    assert e.value.status == G.ERR_UNSUPPORTED
+
+
 def test_plan_half_atom_pairs_need_k_major_q():
     """A CTA pair with 64-wide tiles loads 32-row halves of the MMA's B operand,
     which only the K-major layout allows."""

@@ -30,6 +30,8 @@ def shim(tmp_path_factory):
     lib.sched_contrib_slot.argtypes = [vp, vp, i32]
     lib.sched_partial_slots.restype = ctypes.c_int64
     lib.sched_partial_slots.argtypes = [vp]
+    lib.sched_set_groups.restype = None
+    lib.sched_set_groups.argtypes = [vp, i32]
     return lib
 
 
@@ -55,19 +57,26 @@ def enumerate_units(lib, prm, slots):
     return units
 
 
-def check_schedule(lib, prm, slots):
+def check_schedule(lib, prm, slots, group_rows=None):
+    """group_rows: tile rows of each group of a grouped schedule (else None)."""
     tiles_i, tiles_j, num_kb, _, mode = (int(x) for x in prm[:5])
     batch = int(prm[9])
-    tiles = tiles_i * tiles_j * batch
+    tiles = tiles_i * tiles_j * batch if group_rows is None else sum(group_rows) * tiles_j
     units = enumerate_units(lib, prm, slots)
     by_tile = {}
     for s, u in units:
         by_tile.setdefault(u[2], []).append((s, u))
     assert sorted(by_tile) == list(range(tiles)), "every tile exactly once in the schedule"
     pos = {(u[11], u[0], u[1]) for _, u in units}
-    assert len(pos) == tiles and all(0 <= c < batch and 0 <= a < tiles_i and 0 <= b < tiles_j for c, a, b in pos)
-    for _, u in units:   # the tile index is batch-major
-        assert u[11] == u[2] // (tiles_i * tiles_j)
+    if group_rows is None:
+        assert len(pos) == tiles and all(0 <= c < batch and 0 <= a < tiles_i and 0 <= b < tiles_j for c, a, b in pos)
+        for _, u in units:   # the tile index is batch-major
+            assert u[11] == u[2] // (tiles_i * tiles_j)
+    else:
+        assert len(pos) == tiles and all(0 <= a < group_rows[c] and 0 <= b < tiles_j for c, a, b in pos)
+        start = np.concatenate([[0], np.cumsum(group_rows) * tiles_j])
+        for _, u in units:   # group-major, every group's tiles in its own range
+            assert start[u[11]] <= u[2] < start[u[11] + 1]
     n_pslots = lib.sched_partial_slots(prm.ctypes.data)
     used_pslots = set()
     counters = set()
@@ -127,6 +136,28 @@ def test_stream_k_edge_cases(shim, tiles_i, tiles_j, num_kb, slots, dp_tiles, sk
 @pytest.mark.parametrize("split", [1, 2, 3, 7, 64])
 def test_split_k_schedule(shim, split):
     check_schedule(shim, params((4, 6, 64, 5, 0, split, 0, 0, 0)), 9)
+
+
+@pytest.mark.parametrize("mode", ["tiles", "split", "stream_k"])
+def test_grouped_schedules(shim, mode):
+    """Groups with different tile-row counts (one empty): every (group, tile,
+    k-block) exactly once, found by the group search."""
+    rows = [3, 0, 1, 5, 2, 1]
+    tj, kb, slots = 4, 7, 9
+    table = np.concatenate([[0], np.cumsum(rows) * tj]).astype(np.int32)
+    tiles = int(table[-1])
+    if mode == "tiles":
+        prm = (sum(rows), tj, kb, 2, 0, 1, 0, 0, 0, 1)
+    elif mode == "split":
+        prm = (sum(rows), tj, kb, 2, 0, 2, 0, 0, 0, 1)
+    else:
+        dp = (tiles // slots) * slots
+        prm = (sum(rows), tj, kb, 2, 1, 1, dp, slots, (tiles - dp) * kb, 1)
+    shim.sched_set_groups(table.ctypes.data, len(rows))
+    try:
+        check_schedule(shim, params(prm), slots, group_rows=rows)
+    finally:
+        shim.sched_set_groups(None, 0)
 
 
 @pytest.mark.parametrize("batch", [2, 7, 32])
