@@ -345,7 +345,9 @@ def square_4096_fp8_nt(fmt="e4m3", out_dtype="f32", size=4096):
 
 def bits(t):
     """Raw bit patterns of an input tensor, without copying values: numpy
-    uint16 for bf16 / fp16, uint8 for the 8-bit formats."""
+    uint16 for bf16 / fp16, uint8 for the 8-bit formats, float32 as it is."""
     if t.element_size() == 1:
         return t.contiguous().view(torch.uint8).numpy()
+    if t.dtype == torch.float32:
+        return t.contiguous().numpy()
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)

@@ -21,7 +21,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gemm_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle_gemm.so")
 
-IN_BF16, IN_F16, IN_E4M3, IN_E5M2 = 0, 1, 2, 3
+IN_BF16, IN_F16, IN_E4M3, IN_E5M2, IN_F32 = 0, 1, 2, 3, 4
 C_F32, C_BF16, C_F16 = 0, 1, 2
 
 _lib = None
@@ -97,7 +97,7 @@ def e5m2_value(bits):
 
 def _codes(X, in_type):
     """The stored matrix as an array of codes of the type's width."""
-    want = np.uint8 if in_type in (IN_E4M3, IN_E5M2) else np.uint16
+    want = np.uint8 if in_type in (IN_E4M3, IN_E5M2) else np.float32 if in_type == IN_F32 else np.uint16
     X = np.ascontiguousarray(X)
     if X.dtype != want:
         raise TypeError("input of type %d must be %s codes" % (in_type, want.__name__))
@@ -224,7 +224,7 @@ def epilogue(R, Mag, bias=None, act=ACT_NONE, scale=1.0):
     return R, Mag
 
 
-def within_tolerance(out, r, m, out_is_f32, e4m3=False):
+def within_tolerance(out, r, m, out_is_f32, e4m3=False, tf32=False):
     """Elementwise comparison rule for a GPU result ``out`` against (r, m).
 
     fp32 output:       |out - r| <= 1e-3 * m + 1e-5
@@ -232,10 +232,17 @@ def within_tolerance(out, r, m, out_is_f32, e4m3=False):
     E4M3 output (e4m3=True): r saturates at +-448 first (the format's largest
     value), then |out - r| <= 2^-4 * |r| + 1e-3 * m + 2^-10 (half a unit in the
     last of E4M3's 3 fraction bits, and half its smallest subnormal).
+    Products of TF32-rounded inputs (tf32=True, one pass; each input keeps
+    10 fraction bits, so a product is off by up to ~2^-10 relative):
+    |out - r| <= 2^-8 * m + 1e-5.
     A NaN or Inf in ``out`` where r is finite fails.
     Returns a boolean array (True = within tolerance).
     """
     out = np.asarray(out, dtype=np.float64)
+    if tf32:
+        ok = np.abs(out - r) <= 2.0 ** -8 * m + 1e-5
+        ok &= np.isfinite(out) | ~np.isfinite(r)
+        return ok
     if e4m3:
         r = np.clip(r, -E4M3_MAX, E4M3_MAX)
         bound = 2.0 ** -4 * np.abs(r) + 1e-3 * m + 2.0 ** -10

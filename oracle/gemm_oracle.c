@@ -36,6 +36,9 @@
  *   E5M2: sign, 5-bit exponent with bias 15, 2-bit fraction, with IEEE-style
  *         infinities and NaNs.
  * A and B may have different types (an E4M3 x E5M2 product is allowed).
+ * fp32 inputs (the FP32 GEMM that "GPU GEMM 优化完全拆解（三）", 数值精度,
+ * emulates with three TF32 products) are exact in fp64 as they are; the
+ * product of two has at most 48 significant bits, so it is exact too.
  * Every such value is exactly representable in fp64, and so is every
  * product of two of them (at most 22 significant bits), so the only rounding
  * in s_ij is that of the fp64 additions.
@@ -48,7 +51,7 @@
 #include <stdlib.h>
 #include <unistd.h>
 
-enum { ORACLE_IN_BF16 = 0, ORACLE_IN_F16 = 1, ORACLE_IN_E4M3 = 2, ORACLE_IN_E5M2 = 3 };
+enum { ORACLE_IN_BF16 = 0, ORACLE_IN_F16 = 1, ORACLE_IN_E4M3 = 2, ORACLE_IN_E5M2 = 3, ORACLE_IN_F32 = 4 };
 enum { ORACLE_C_F32 = 0, ORACLE_C_BF16 = 1, ORACLE_C_F16 = 2 };
 
 /* bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits. */
@@ -121,8 +124,13 @@ static double in_value(int in_type, const void* base, int64_t idx) {
     case ORACLE_IN_F16: return oracle_f16_value(((const uint16_t*)base)[idx]);
     case ORACLE_IN_E4M3: return oracle_e4m3_value(((const uint8_t*)base)[idx]);
     case ORACLE_IN_E5M2: return oracle_e5m2_value(((const uint8_t*)base)[idx]);
+    case ORACLE_IN_F32: return (double)((const float*)base)[idx]; /* exact in fp64 */
     default: return oracle_bf16_value(((const uint16_t*)base)[idx]);
   }
+}
+
+static int64_t elem_bytes(int in_type) {
+  return (in_type == ORACLE_IN_E4M3 || in_type == ORACLE_IN_E5M2) ? 1 : in_type == ORACLE_IN_F32 ? 4 : 2;
 }
 
 static double c0_value(int c_type, const void* C0, int64_t idx) {
@@ -210,8 +218,8 @@ static int check_args(int transA, int transB, int64_t M, int64_t N, int64_t K, i
                       int64_t ldb, int a_type, int b_type, int c_type) {
   if (M < 0 || N < 0 || K < 0) return -1;
   if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1)) return -1;
-  if (a_type < ORACLE_IN_BF16 || a_type > ORACLE_IN_E5M2) return -1;
-  if (b_type < ORACLE_IN_BF16 || b_type > ORACLE_IN_E5M2) return -1;
+  if (a_type < ORACLE_IN_BF16 || a_type > ORACLE_IN_F32) return -1;
+  if (b_type < ORACLE_IN_BF16 || b_type > ORACLE_IN_F32) return -1;
   if (c_type != ORACLE_C_F32 && c_type != ORACLE_C_BF16 && c_type != ORACLE_C_F16) return -1;
   if (lda < (transA ? M : K) || ldb < (transB ? K : N)) return -1;
   return 0;
@@ -350,8 +358,8 @@ int oracle_gemm_batched(int transA, int transB, int64_t M, int64_t N, int64_t K,
                         int64_t strideC, int a_type, int b_type, int64_t batch, double* R,
                         double* Mag, int64_t ldr, int nthreads) {
   if (batch < 0 || strideA < 0 || strideB < 0 || strideC < 0) return -1;
-  const int64_t ea = (a_type == ORACLE_IN_E4M3 || a_type == ORACLE_IN_E5M2) ? 1 : 2;
-  const int64_t eb = (b_type == ORACLE_IN_E4M3 || b_type == ORACLE_IN_E5M2) ? 1 : 2;
+  const int64_t ea = elem_bytes(a_type);
+  const int64_t eb = elem_bytes(b_type);
   const int64_t ec = c_type == ORACLE_C_F32 ? 4 : 2;
   int used = 0;
   for (int64_t b = 0; b < batch; ++b) {
@@ -380,8 +388,8 @@ int oracle_gemm_grouped(int transB, int64_t groups, const int64_t* m_sizes, int6
                         int64_t strideB, double beta, const void* C0, int c_type, int64_t ldc,
                         int a_type, int b_type, double* R, double* Mag, int64_t ldr, int nthreads) {
   if (groups < 0 || strideB < 0) return -1;
-  const int64_t ea = (a_type == ORACLE_IN_E4M3 || a_type == ORACLE_IN_E5M2) ? 1 : 2;
-  const int64_t eb = (b_type == ORACLE_IN_E4M3 || b_type == ORACLE_IN_E5M2) ? 1 : 2;
+  const int64_t ea = elem_bytes(a_type);
+  const int64_t eb = elem_bytes(b_type);
   const int64_t ec = c_type == ORACLE_C_F32 ? 4 : 2;
   int64_t off = 0;
   for (int64_t g = 0; g < groups; ++g) {

@@ -407,6 +407,56 @@ def test_thread_count_does_not_change_results():
 
 
 # ---------------------------------------------------------------------------
+# fp32 inputs (the FP32 GEMM emulated with three TF32 products)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("transA,transB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_fp32_inputs_match_library_matmul(transA, transB):
+    M, N, K = 17, 23, 90
+    p = inputs.make_problem("of32", M, N, K, transA, transB, "f32", "f32", ("normal", 0, 1), ("normal", 0, 1),
+                            alpha=0.5, beta=2.0, seed=6)
+    R, Mag = oracle.gemm(transA, transB, M, N, K, p.alpha, inputs.bits(p.A), p.lda, inputs.bits(p.B), p.ldb, p.beta,
+                         p.C0.numpy(), p.ldc, oracle.IN_F32)
+    a = _op(p.A.double().numpy(), transA)
+    b = _op(p.B.double().numpy(), transB)
+    ref = p.alpha * (a @ b) + p.beta * p.C0.double().numpy()
+    assert np.allclose(R, ref, rtol=1e-13, atol=1e-13)
+
+
+def test_fp32_inputs_exact_integers_and_types():
+    p = inputs.make_problem("of32i", 30, 40, 500, 0, 0, "f32", "f32", ("ints", -50, 50), ("ints", -50, 50), seed=7)
+    R, _ = oracle.gemm(0, 0, 30, 40, 500, 1.0, inputs.bits(p.A), 500, inputs.bits(p.B), 40, 0.0, None, 40,
+                       oracle.IN_F32)
+    assert np.array_equal(R, (p.A.numpy().astype(np.int64) @ p.B.numpy().astype(np.int64)).astype(np.float64))
+    with pytest.raises(TypeError):   # fp32 inputs are float32 arrays, not codes
+        oracle.gemm(0, 0, 2, 2, 2, 1.0, np.zeros((2, 2), np.uint16), 2, np.zeros((2, 2), np.uint16), 2, 0.0, None,
+                    2, oracle.IN_F32)
+
+
+def test_fp32_batched_and_grouped_offsets():
+    """fp32 operands advance by 4 bytes per element in batches and groups."""
+    p = inputs.make_batched_problem("ob32", 3, 6, 5, 40, 0, 1, "f32", "f32", ("normal", 0, 1), ("normal", 0, 1), seed=8)
+    R, _ = oracle.gemm_batched(0, 1, 6, 5, 40, 1.0, inputs.bits(p.A), 40, p.strideA, inputs.bits(p.B), 40, p.strideB,
+                               0.0, None, 5, p.strideC, oracle.IN_F32, 3)
+    a = p.A.double().numpy().reshape(3, 6, 40)
+    b = p.B.double().numpy().reshape(3, 5, 40)
+    assert np.allclose(R, np.einsum("bik,bjk->bij", a, b), rtol=1e-13, atol=1e-13)
+    q = inputs.make_grouped_problem("og32", [2, 0, 4], 5, 40, 1, "f32", "f32", seed=9)
+    Rg, _ = oracle.gemm_grouped(1, [2, 0, 4], 5, 40, 1.0, inputs.bits(q.A), 40, inputs.bits(q.B), 40, q.strideB,
+                                0.0, None, 5, oracle.IN_F32)
+    w = q.B.double().numpy().reshape(3, 5, 40)
+    aa = q.A.double().numpy()
+    assert np.allclose(Rg[:2], aa[:2] @ w[0].T, rtol=1e-13) and np.allclose(Rg[2:], aa[2:] @ w[2].T, rtol=1e-13)
+
+
+def test_tf32_tolerance_rule():
+    r = np.array([1.0, 1.0, 0.0])
+    m = np.array([1.0, 1.0, 1.0])
+    assert list(oracle.within_tolerance(np.array([1.0 + 3.8e-3, 1.0 + 4.1e-3, np.inf]), r, m, True, tf32=True)) \
+        == [True, False, False]
+
+
+# ---------------------------------------------------------------------------
 # Strided batched GEMM
 # ---------------------------------------------------------------------------
 

@@ -33,6 +33,7 @@ MUTATIONS = {
     "C0 batch offset ignored": ("(const char*)C0 + b * strideC * ec", "(const char*)C0"),
     "group weights not advanced": ("(const char*)B + g * strideB * eb", "(const char*)B"),
     "group rows not offset": ("(const char*)A + off * lda * ea", "(const char*)A"),
+    "fp32 read at the 16-bit width": ("in_type == ORACLE_IN_F32 ? 4 : 2", "in_type == ORACLE_IN_F32 ? 2 : 2"),
 }
 
 
