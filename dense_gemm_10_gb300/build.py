@@ -21,7 +21,8 @@ HEADER = os.path.join(ROOT, "include", "gemm_gb300.h")
 
 SOURCES = ["gemm_api.cu", "tc_dispatch.cu", "tc_gemm_bn64_cg1_mc1.cu", "tc_gemm_bn128_cg1_mc1.cu",
            "tc_gemm_bn64_cg1_mc1_f8.cu", "tc_gemm_bn128_cg1_mc1_f8.cu", "tc_gemm_bn128_cg2_mc1_f8.cu",
-           "tc_gemm_bn256_cg2_mc1_f8.cu",
+           "tc_gemm_bn256_cg2_mc1_f8.cu", "tc_gemm_bn64_cg1_mc1_tf32.cu", "tc_gemm_bn128_cg1_mc1_tf32.cu",
+           "tc_gemm_bn256_cg2_mc1_tf32.cu",
            "tc_gemm_bn256_cg1_mc1.cu", "tc_gemm_bn128_cg2_mc1.cu", "tc_gemm_bn256_cg2_mc1.cu",
            "tc_gemm_bn256_cg2_mc2.cu", "tc_gemm_bn64_cg2_mc1.cu", "aux_kernels.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -2,6 +2,13 @@
 //  * repack: copies an operand whose rows are not 16-byte aligned into
 //    an aligned buffer, because the tensor-memory-accelerator copy engine only
 //    reads rows whose pitch is a multiple of 16 bytes;
+//  * split_tf32: writes an fp32 operand K-major as TF32 values for the TF32
+//    tensor-core kind ("GPU GEMM 优化完全拆解（三）", 数值精度).  One part: the
+//    value cut to TF32 (sign, 8-bit exponent, top 10 fraction bits), as the
+//    tensor core reads an fp32 operand.  Several parts (the fp32 GEMM from
+//    three TF32 products): hi = TF32(x) and lo = TF32(x - hi), both rounded to
+//    nearest, laid out in segments of K chosen by a bit pattern, so that one
+//    TF32 GEMM over parts x K sums the chosen products;
 //  * scale_c: C = ops(beta * C), the whole GEMM when K == 0 ("CUDA GEMM
 //    矩阵乘法优化指南", section 2.1, with an empty sum), with the fused epilogue
 //    operations of epi_ops.cuh.
@@ -53,6 +60,64 @@ __global__ void scale_c_kernel(void* C, int32_t c_type, int64_t M, int64_t N, in
   }
 }
 
+// fp32 -> TF32 (10 fraction bits), round to nearest, ties away from zero.
+__device__ __forceinline__ float to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
+// fp32 -> TF32 by dropping the 13 low fraction bits (NaN stays NaN).
+__device__ __forceinline__ float cut_tf32(float x) {
+  return x != x ? x : __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+}
+
+// Element (r, k) of one source matrix: src[k * lds + r] (kTrans) or src[r * lds + k].
+// Output row r: parts * K values at dst[r * ldd]; parts == 1: the cut value;
+// else segment s holds the low part when bit s of pattern is set, the high part
+// otherwise.  Transposed sources go through a 32 x 32 shared-memory tile so
+// that reads and writes are both coalesced.
+template <bool kTrans>
+__global__ void split_tf32_kernel(const float* __restrict__ src, int64_t lds, int64_t sbs, float* __restrict__ dst,
+                                  int64_t ldd, int64_t dbs, int64_t rows, int64_t K, int64_t nb, int parts,
+                                  int pattern) {
+  __shared__ float tile[32][33];
+  const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8 threads
+  const int64_t tiles_r = (rows + 31) / 32, tiles_k = (K + 31) / 32;
+  for (int64_t b = blockIdx.z; b < nb; b += gridDim.z) {
+    const float* S = src + b * sbs;
+    float* D = dst + b * dbs;
+    for (int64_t t = blockIdx.x; t < tiles_r * tiles_k; t += gridDim.x) {
+      const int64_t r0 = (t / tiles_k) * 32, k0 = (t % tiles_k) * 32;
+      __syncthreads();
+      for (int i = ty; i < 32; i += 8) {  // tile[k - k0][r - r0]
+        if (kTrans) {
+          const int64_t k = k0 + i, r = r0 + tx;
+          tile[i][tx] = (k < K && r < rows) ? S[k * lds + r] : 0.0f;
+        } else {
+          const int64_t r = r0 + i, k = k0 + tx;
+          tile[tx][i] = (k < K && r < rows) ? S[r * lds + k] : 0.0f;
+        }
+      }
+      __syncthreads();
+      for (int i = ty; i < 32; i += 8) {
+        const int64_t r = r0 + i, k = k0 + tx;
+        if (r >= rows || k >= K) continue;
+        const float x = tile[tx][i];
+        float* row = D + r * ldd;
+        if (parts == 1) {
+          row[k] = cut_tf32(x);
+          continue;
+        }
+        float hi = to_tf32(x);
+        if (isinf(hi) && !isinf(x)) hi = cut_tf32(x);  // rounded past the largest value
+        const float lo = isfinite(x) ? to_tf32(x - hi) : 0.0f;
+        for (int s = 0; s < parts; ++s) row[s * K + k] = ((pattern >> s) & 1) ? lo : hi;
+      }
+    }
+  }
+}
+
 static dim3 grid_3d(int64_t rows, int64_t cols, int64_t nb, int sm_count) {
   const int64_t bx = (cols + 255) / 256 < 16 ? (cols + 255) / 256 : 16;
   int64_t by = (static_cast<int64_t>(sm_count) * 8 + bx - 1) / bx;
@@ -74,6 +139,23 @@ cudaError_t repack_launch(const void* src, int64_t lds, int64_t sbs, void* dst, 
   else
     repack_kernel<uint16_t><<<g, 256, 0, stream>>>(static_cast<const uint16_t*>(src), lds, sbs,
                                                    static_cast<uint16_t*>(dst), ldd, dbs, rows, cols, nb);
+  return cudaGetLastError();
+}
+
+cudaError_t split_tf32_launch(const float* src, int64_t lds, int64_t sbs, bool transposed, float* dst,
+                              int64_t ldd, int64_t dbs, int64_t rows, int64_t K, int64_t nb, int parts,
+                              int pattern, int sm_count, cudaStream_t stream) {
+  const int64_t tiles = ((rows + 31) / 32) * ((K + 31) / 32);
+  int64_t gx = static_cast<int64_t>(sm_count) * 8;
+  if (gx > tiles) gx = tiles;
+  int64_t gz = nb < 65535 ? nb : 65535;
+  const dim3 grid(static_cast<unsigned>(gx > 0 ? gx : 1), 1, static_cast<unsigned>(gz > 0 ? gz : 1));
+  if (transposed)
+    split_tf32_kernel<true><<<grid, dim3(32, 8), 0, stream>>>(src, lds, sbs, dst, ldd, dbs, rows, K, nb, parts,
+                                                              pattern);
+  else
+    split_tf32_kernel<false><<<grid, dim3(32, 8), 0, stream>>>(src, lds, sbs, dst, ldd, dbs, rows, K, nb, parts,
+                                                               pattern);
   return cudaGetLastError();
 }
 

@@ -56,6 +56,13 @@ struct Operand {
   size_t ws_offset = 0;
   int64_t bstride = 0;        // elements between batches' matrices (strided batches)
   int64_t nb = 1;             // distinct matrices: 1 when shared by every batch
+  // fp32 operands written as TF32 parts (split_tf32_launch) instead of repacked:
+  // the source is ptr/ld/bstride, `src_k` values of k per row, read transposed
+  // when `split_trans`; the copy is rows x cols (= parts * src_k) K-major.
+  int split_parts = 0;
+  int split_pattern = 0;
+  bool split_trans = false;
+  int64_t src_k = 0;
 };
 
 struct Plan {
@@ -93,6 +100,7 @@ struct DtypeInfo {
   uint32_t a_fmt = 0, b_fmt = 0;  // kind::f16: 0 f16, 1 bf16; kind::f8f6f4: 0 E4M3, 1 E5M2
   int32_t c_type = kCF32;
   CUtensorMapDataType map_type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  int parts = 0;  // fp32 inputs: TF32 products per product (1 or 3)
 };
 
 DtypeInfo dtype_info(int dtype) {
@@ -106,6 +114,13 @@ DtypeInfo dtype_info(int dtype) {
                : bf16                                              ? kCBF16
                                                                    : kCF16;
     d.map_type = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  } else if (dtype == GEMM_F32_F32 || dtype == GEMM_TF32_F32) {
+    d.valid = true;
+    d.eb = 4;
+    d.a_fmt = d.b_fmt = 2;  // kind::tf32
+    d.c_type = kCF32;
+    d.map_type = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    d.parts = dtype == GEMM_F32_F32 ? 3 : 1;
   } else if (dtype >= GEMM_E4M3_F32 && dtype <= GEMM_E5M2_E4M3OUT) {
     // 16 + (A is E5M2) + 2 * (B is E5M2) + 4 * (C: 0 fp32, 1 bf16, 2 fp16, 3 E4M3)
     const int x = dtype - GEMM_E4M3_F32;
@@ -346,13 +361,35 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   if (groups > 1 && strideB > 0) b.nb = groups;  // one weight matrix per group
   a.bstride = a.nb > 1 ? strideA : 0;
   b.bstride = b.nb > 1 ? strideB : 0;
+  // fp32 inputs run on the TF32 tensor-core kind, K-major.  One TF32 product
+  // per product (GEMM_TF32_F32): an fp32 operand the copy engine can load
+  // K-major goes in as it is (the tensor core keeps its top 19 bits); any
+  // other is written K-major with its values cut to TF32 the same way.  The
+  // fp32 GEMM (GEMM_F32_F32) splits every value x into hi = TF32(x) and lo =
+  // TF32(x - hi) and sums lo_a hi_b + hi_a lo_b + hi_a hi_b (the small
+  // products first) as one GEMM over 3K: A's rows become [lo | hi | hi] and
+  // B's [hi | lo | hi].
+  int64_t Kg = K;  // k extent of the GEMM the kernel runs
+  if (dt.parts > 0) {
+    Kg = K * dt.parts;
+    for (Operand* op : {&a, &b}) {
+      if (dt.parts == 1 && op->kmajor && tma_aligned(op->ptr, op->ld, dt.eb, op->bstride, op->nb)) continue;
+      op->split_parts = dt.parts;
+      op->split_pattern = dt.parts == 1 ? 0 : op == &a ? 0x1 : 0x2;
+      op->split_trans = !op->kmajor;
+      op->src_k = K;
+      op->rows = op->kmajor ? op->rows : op->cols;
+      op->cols = Kg;
+      op->kmajor = true;
+    }
+  }
 
   // A short M rides on the MMA's N dimension: compute C^T = op(B)^T op(A)^T.
   const bool swap = groups == 0 && M <= 64 && N > M;
   P.swap_ab = swap ? 1 : 0;
   pl.I = swap ? N : M;
   pl.J = swap ? M : N;
-  pl.K = K;
+  pl.K = Kg;
   pl.p = swap ? b : a;
   pl.q = swap ? a : b;
   // the schedule indexes tiles (and split-K partial slots) with 32-bit integers
@@ -364,17 +401,18 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   P.a_kmajor = pl.p.kmajor ? 1 : 0;
   P.b_kmajor = pl.q.kmajor ? 1 : 0;
 
-  const int64_t num_kslices = cdiv(K, slice_k(dt.eb));  // 128-byte k-slices
+  const int64_t num_kslices = cdiv(Kg, slice_k(dt.eb));  // 128-byte k-slices
   // Below the machine balance (≈ 2.2 PFLOP/s over ≈ 7 TB/s ≈ 300 FLOP per byte
-  // for 16-bit inputs, twice that for the 8-bit ones at twice the rate) the
+  // for 16-bit inputs; twice the rate for 8-bit inputs, half for TF32) the
   // GEMM is bound by HBM, not by the tensor cores.
-  const double alg_bytes = dt.eb * (static_cast<double>(M) * K * a.nb + static_cast<double>(K) * N * b.nb) +
+  const double alg_bytes = dt.eb * (static_cast<double>(M) * Kg * a.nb + static_cast<double>(Kg) * N * b.nb) +
                            static_cast<double>(M) * N * batch * c_elem * (beta != 0.0f ? 2 : 1);
-  const bool hbm_bound = 2.0 * static_cast<double>(M) * N * K * batch / alg_bytes < 256.0 * (3 - dt.eb);
+  const double rate = dt.eb == 1 ? 2.0 : dt.eb == 4 ? 0.5 : 1.0;
+  const bool hbm_bound = 2.0 * static_cast<double>(M) * N * Kg * batch / alg_bytes < 256.0 * rate;
 
   // Tile configuration and schedule: the configuration with the lowest
   // estimated time, est_time() below.
-  static const int kPreference[kNumTileConfigs] = {5, 4, 3, 2, 1, 6, 0, 10, 9, 8, 7};  // ties go first
+  static const int kPreference[kNumTileConfigs] = {5, 4, 3, 2, 1, 6, 0, 10, 9, 8, 7, 13, 12, 11};  // ties go first
   Choice best;
   for (int cfg : kPreference) {
     const TileConfig& c = kTileConfigs[cfg];
@@ -447,7 +485,7 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   // Workspace: repacked operands, then partial tiles of split tiles.
   size_t ws = 0;
   for (Operand* op : {&pl.p, &pl.q}) {
-    if (!tma_aligned(op->ptr, op->ld, dt.eb, op->bstride, op->nb)) {
+    if (op->split_parts > 0 || !tma_aligned(op->ptr, op->ld, dt.eb, op->bstride, op->nb)) {
       op->repack = true;  // rows padded to whole 16-byte pieces, batches packed
       op->packed_ld = static_cast<int64_t>(round_up(static_cast<size_t>(op->cols), 16 / dt.eb));
       op->ws_offset = ws;
@@ -739,6 +777,35 @@ gemm_status_t gemm_plan(gemm_handle_t h, int sm_count, gemm_op_t transA, gemm_op
                                    0, 1, dtype, plan);
 }
 
+// Write the operands the copy engine cannot read as they are (repacked or
+// split into TF32 parts) into the workspace at `ws`; *pbase / *qbase and their
+// leading dimensions then describe what the kernel loads.  Counts launches.
+static cudaError_t prepare_operands(const Plan& pl, uint8_t* ws, int sm_count, cudaStream_t st,
+                                    const void** pbase, int64_t* pld, const void** qbase, int64_t* qld,
+                                    uint64_t* launches) {
+  *pbase = pl.p.ptr;
+  *qbase = pl.q.ptr;
+  *pld = pl.p.ld;
+  *qld = pl.q.ld;
+  for (int w = 0; w < 2; ++w) {
+    const Operand& op = w == 0 ? pl.p : pl.q;
+    if (!op.repack) continue;
+    void* dst = ws + op.ws_offset;
+    cudaError_t e;
+    if (op.split_parts > 0)
+      e = split_tf32_launch(static_cast<const float*>(op.ptr), op.ld, op.bstride, op.split_trans,
+                            static_cast<float*>(dst), op.packed_ld, op.rows * op.packed_ld, op.rows, op.src_k,
+                            op.nb, op.split_parts, op.split_pattern, sm_count, st);
+    else
+      e = repack_launch(op.ptr, op.ld, op.bstride, dst, op.packed_ld, op.rows * op.packed_ld, op.rows, op.cols,
+                        op.nb, pl.eb, sm_count, st);
+    if (e != cudaSuccess) return e;
+    if (launches) *launches += 1;
+    if (w == 0) { *pbase = dst; *pld = op.packed_ld; } else { *qbase = dst; *qld = op.packed_ld; }
+  }
+  return cudaSuccess;
+}
+
 static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int64_t M,
                               int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
                               const void* B, int64_t ldb, float beta, void* C, int64_t ldc,
@@ -781,21 +848,13 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
   const int cg = P.bm / kBM;
   const int mc = P.cluster / cg;
 
-  // Operands that the copy engine cannot read directly are repacked first.
-  const void* pbase = pl.p.ptr;
-  const void* qbase = pl.q.ptr;
-  int64_t pld = pl.p.ld, qld = pl.q.ld;
+  // Operands that the copy engine cannot read directly are repacked (or split) first.
+  const void* pbase;
+  const void* qbase;
+  int64_t pld, qld;
   uint8_t* ws = static_cast<uint8_t*>(h->d_ws);
-  for (int w = 0; w < 2; ++w) {
-    const Operand& op = w == 0 ? pl.p : pl.q;
-    if (!op.repack) continue;
-    void* dst = ws + op.ws_offset;
-    e = repack_launch(op.ptr, op.ld, op.bstride, dst, op.packed_ld, op.rows * op.packed_ld, op.rows, op.cols,
-                      op.nb, pl.eb, h->sm_count, st);
-    if (e != cudaSuccess) return cuda_fail(h, e);
-    h->launches += 1;
-    if (w == 0) { pbase = dst; pld = op.packed_ld; } else { qbase = dst; qld = op.packed_ld; }
-  }
+  e = prepare_operands(pl, ws, h->sm_count, st, &pbase, &pld, &qbase, &qld, &h->launches);
+  if (e != cudaSuccess) return cuda_fail(h, e);
 
   CUtensorMap map_p, map_q;
   s = encode_operand(&map_p, pl.p, pbase, pld, pl.p.repack ? pl.p.rows * pld : pl.p.bstride, pl.eb,
@@ -1068,18 +1127,11 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   if (e == cudaSuccess && nctr > 0) e = cudaMemsetAsync(d->counters, 0, nctr * sizeof(int32_t), st);
   if (e != cudaSuccess) return GEMM_ERR_CUDA;
 
-  const void* pbase = pl.p.ptr;
-  const void* qbase = pl.q.ptr;
-  int64_t pld = pl.p.ld, qld = pl.q.ld;
-  for (int w = 0; w < 2; ++w) {
-    const Operand& op = w == 0 ? pl.p : pl.q;
-    if (!op.repack) continue;
-    void* dst = d->scratch + op.ws_offset;
-    e = repack_launch(op.ptr, op.ld, op.bstride, dst, op.packed_ld, op.rows * op.packed_ld, op.rows, op.cols,
-                      op.nb, pl.eb, d->sm_count, st);
-    if (e != cudaSuccess) return GEMM_ERR_CUDA;
-    if (w == 0) { pbase = dst; pld = op.packed_ld; } else { qbase = dst; qld = op.packed_ld; }
-  }
+  const void* pbase;
+  const void* qbase;
+  int64_t pld, qld;
+  e = prepare_operands(pl, d->scratch, d->sm_count, st, &pbase, &pld, &qbase, &qld, nullptr);
+  if (e != cudaSuccess) return GEMM_ERR_CUDA;
   CUtensorMap map_p, map_q;
   s = encode_operand(&map_p, pl.p, pbase, pld, pl.p.repack ? pl.p.rows * pld : pl.p.bstride, pl.eb,
                      pl.in_dtype, kBM / mc);

@@ -80,11 +80,11 @@ enum BulkStore : int32_t { kBulkNone = 0, kBulkRows = 1, kBulkTransposed = 2 };
 // pair (cg == 2); mc == 2 clusters two pairs on neighbouring tiles of one tile
 // row, which share the P tile by multicast.  eb is the input element size in
 // bytes: 2 for bf16 / fp16 (tcgen05.mma kind::f16), 1 for the 8-bit formats
-// (kind::f8f6f4).
+// (kind::f8f6f4), 4 for TF32 (kind::tf32).
 struct TileConfig {
   int bn, cg, mc, eb;
 };
-constexpr int kNumTileConfigs = 11;
+constexpr int kNumTileConfigs = 14;
 extern const TileConfig kTileConfigs[kNumTileConfigs];
 int tc_stages(int cfg);  // ring depth in k-slices
 // One-time per device: opt in to the kernel's shared memory; for clusters also
@@ -100,6 +100,16 @@ cudaError_t tc_launch(int cfg, const CUtensorMap& map_p, const CUtensorMap& map_
 cudaError_t repack_launch(const void* src, int64_t lds, int64_t sbs, void* dst, int64_t ldd, int64_t dbs,
                           int64_t rows, int64_t cols, int64_t nb, int esize, int sm_count,
                           cudaStream_t stream);
+
+// TF32 values of fp32 operands, written K-major: row r of dst (b-th matrix at
+// dbs elements) receives parts x K values.  parts == 1: each value with its 13
+// low fraction bits dropped.  parts > 1: segment s holds lo = TF32(x - hi)
+// when bit s of pattern is set, else hi = TF32(x) (both rounded to nearest).
+// Source element (r, k) is src[k * lds + r] when transposed, else
+// src[r * lds + k].
+cudaError_t split_tf32_launch(const float* src, int64_t lds, int64_t sbs, bool transposed, float* dst,
+                              int64_t ldd, int64_t dbs, int64_t rows, int64_t K, int64_t nb, int parts,
+                              int pattern, int sm_count, cudaStream_t stream);
 
 // The whole GEMM when K == 0: C = ops(beta * C) over `batch` M x N matrices
 // with leading dimension ldc, sbc elements apart (beta * C = 0 when beta == 0;

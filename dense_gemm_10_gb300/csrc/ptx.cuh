@@ -233,7 +233,8 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 // Instruction descriptor of tcgen05.mma (kind::f16 or kind::f8f6f4) with an
 // fp32 accumulator.
 //   bits  4-5   D format (1 = f32)
-//   bits  7-9   A format: kind::f16 0 = f16, 1 = bf16; kind::f8f6f4 0 = E4M3, 1 = E5M2
+//   bits  7-9   A format: kind::f16 0 = f16, 1 = bf16; kind::tf32 2 = TF32;
+//               kind::f8f6f4 0 = E4M3, 1 = E5M2
 //   bits 10-12  B format, the same codes
 //   bit  15     A major (0 = K-major, 1 = M-major)
 //   bit  16     B major (0 = K-major, 1 = N-major)
@@ -249,12 +250,29 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t a_fmt, uint32_t b_fmt
 // D[tmem] (+)= A[smem] * B[smem]; issued by a single thread.  With CG == 2 the
 // leader CTA issues it for the pair: A rows and B rows come half from each
 // CTA's shared memory (same offsets), and each CTA's TMEM receives its rows of D.
-// EB = input element bytes: 2 -> kind::f16 (K = 16), 1 -> kind::f8f6f4 (K = 32);
-// either way one instruction consumes 32 bytes of every operand row.
+// EB = input element bytes: 2 -> kind::f16 (K = 16), 1 -> kind::f8f6f4 (K = 32),
+// 4 -> kind::tf32 (K = 8); every kind consumes 32 bytes of each operand row.
 template <int CG, int EB>
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                        uint32_t idesc, uint32_t accumulate) {
-  static_assert(EB == 1 || EB == 2, "element bytes");
+  static_assert(EB == 1 || EB == 2 || EB == 4, "element bytes");
+  if constexpr (EB == 4) {
+    if constexpr (CG == 1)
+      asm volatile(
+          "{\n\t.reg .pred p;\n\t"
+          "setp.ne.b32 p, %4, 0;\n\t"
+          "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+          "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+          : "memory");
+    else
+      asm volatile(
+          "{\n\t.reg .pred p;\n\t"
+          "setp.ne.b32 p, %4, 0;\n\t"
+          "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+          "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+          : "memory");
+    return;
+  }
   if constexpr (CG == 1 && EB == 2)
     asm volatile(
         "{\n\t.reg .pred p;\n\t"

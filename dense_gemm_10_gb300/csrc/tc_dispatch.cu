@@ -28,6 +28,9 @@ TC_DECLARE(64, 1, 1, 1)
 TC_DECLARE(128, 1, 1, 1)
 TC_DECLARE(128, 2, 1, 1)
 TC_DECLARE(256, 2, 1, 1)
+TC_DECLARE(64, 1, 1, 4)
+TC_DECLARE(128, 1, 1, 4)
+TC_DECLARE(256, 2, 1, 4)
 
 namespace {
 struct Entry {
@@ -39,12 +42,14 @@ struct Entry {
 const Entry kEntries[kNumTileConfigs] = {
     TC_ENTRY(64, 1, 1, 2),  TC_ENTRY(128, 1, 1, 2), TC_ENTRY(256, 1, 1, 2), TC_ENTRY(128, 2, 1, 2),
     TC_ENTRY(256, 2, 1, 2), TC_ENTRY(256, 2, 2, 2), TC_ENTRY(64, 2, 1, 2),  TC_ENTRY(64, 1, 1, 1),
-    TC_ENTRY(128, 1, 1, 1), TC_ENTRY(128, 2, 1, 1), TC_ENTRY(256, 2, 1, 1)};
+    TC_ENTRY(128, 1, 1, 1), TC_ENTRY(128, 2, 1, 1), TC_ENTRY(256, 2, 1, 1), TC_ENTRY(64, 1, 1, 4),
+    TC_ENTRY(128, 1, 1, 4), TC_ENTRY(256, 2, 1, 4)};
 }  // namespace
 
 const TileConfig kTileConfigs[kNumTileConfigs] = {
     {64, 1, 1, 2},  {128, 1, 1, 2}, {256, 1, 1, 2}, {128, 2, 1, 2}, {256, 2, 1, 2}, {256, 2, 2, 2},
-    {64, 2, 1, 2},  {64, 1, 1, 1},  {128, 1, 1, 1}, {128, 2, 1, 1}, {256, 2, 1, 1}};
+    {64, 2, 1, 2},  {64, 1, 1, 1},  {128, 1, 1, 1}, {128, 2, 1, 1}, {256, 2, 1, 1}, {64, 1, 1, 4},
+    {128, 1, 1, 4}, {256, 2, 1, 4}};
 
 int tc_stages(int cfg) { return cfg >= 0 && cfg < kNumTileConfigs ? kEntries[cfg].stages : 0; }
 

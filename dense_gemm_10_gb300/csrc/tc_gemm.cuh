@@ -428,9 +428,9 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
   // multicast of P: this CTA and the CTA of the other pair with the same rank inside its pair
   const uint16_t p_mask = static_cast<uint16_t>((1u << q) | (1u << (q + CG)));
   constexpr int kSliceK = slice_k(EB);  // k elements of one 128-byte slice
-  // 8-bit operands are always K-major (the planner admits no other layout)
-  const bool p_kmajor = EB == 1 || a.p_kmajor != 0;
-  const bool q_kmajor = EB == 1 || a.q_kmajor != 0;
+  // 8- and 32-bit operands are always K-major (the planner admits no other layout)
+  const bool p_kmajor = EB != 2 || a.p_kmajor != 0;
+  const bool q_kmajor = EB != 2 || a.q_kmajor != 0;
   const int kslices = (a.K + kSliceK - 1) / kSliceK;
   int stage = 0;
   uint32_t phase = 0;
@@ -528,9 +528,9 @@ __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8
                                          int stride) {
   using Cfg = TcConfig<BN, CG, MC>;
   constexpr int kSliceK = slice_k(EB);  // k elements of one 128-byte slice
-  // 8-bit operands are always K-major (the planner admits no other layout)
-  const bool p_kmajor = EB == 1 || a.p_kmajor != 0;
-  const bool q_kmajor = EB == 1 || a.q_kmajor != 0;
+  // 8- and 32-bit operands are always K-major (the planner admits no other layout)
+  const bool p_kmajor = EB != 2 || a.p_kmajor != 0;
+  const bool q_kmajor = EB != 2 || a.q_kmajor != 0;
   const int kslices = (a.K + kSliceK - 1) / kSliceK;
   int stage = 0;
   uint32_t phase = 0;

@@ -13,6 +13,7 @@ LIB_PATH = os.path.join(HERE, "libgemm_gb300.so")
 
 OP_N, OP_T = 0, 1
 BF16_F32, BF16_BF16, F16_F32, F16_F16, BF16_E4M3, F16_E4M3 = 0, 1, 2, 3, 4, 5
+F32_F32, TF32_F32 = 6, 7   # fp32 inputs: three TF32 products per product, or one
 _FP8_FORMATS = ("e4m3", "e5m2")
 _C_TYPES = ("f32", "bf16", "f16", "e4m3")
 ACT_NONE, ACT_RELU, ACT_GELU = 0, 1, 2
@@ -238,10 +239,14 @@ def plan_grouped(m_sizes, N, K, transB=1, dtype=BF16_F32, lda=None, ldb=None, st
     return p
 
 
-def dtype_code(in_dtype, out_dtype, b_dtype=None):
-    """gemm_dtype_t code for torch dtypes of A (and B, default the same) and C."""
+def dtype_code(in_dtype, out_dtype, b_dtype=None, tf32=False):
+    """gemm_dtype_t code for torch dtypes of A (and B, default the same) and C.
+    fp32 inputs: the fp32 GEMM from three TF32 products, or one TF32 product
+    per product with tf32=True."""
     import torch
     b_dtype = in_dtype if b_dtype is None else b_dtype
+    if in_dtype == torch.float32 and b_dtype == torch.float32 and out_dtype == torch.float32:
+        return TF32_F32 if tf32 else F32_F32
     table = {(torch.bfloat16, torch.float32): BF16_F32, (torch.bfloat16, torch.bfloat16): BF16_BF16,
              (torch.float16, torch.float32): F16_F32, (torch.float16, torch.float16): F16_F16}
     if b_dtype == in_dtype and (in_dtype, out_dtype) in table:
@@ -262,12 +267,14 @@ def _ld(t, name):
 
 
 def gemm(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0, handle=None, stream=None, M=None,
-         N=None, K=None, bias=None, act=ACT_NONE, out_scale=1.0):
+         N=None, K=None, bias=None, act=ACT_NONE, out_scale=1.0, tf32=False):
     """C = convert(out_scale * act(alpha * op(A) * op(B) + beta * C + bias)) on
     CUDA tensors, enqueued on `stream` (default: torch's current stream).  A and
     B are stored row-major as (M, K) / (K, M) and (K, N) / (N, K) per transA /
     transB; C is (M, N); bias (optional) is a CUDA fp32 tensor of N values.
-    Sizes default to the logical extents of the tensors."""
+    fp32 A, B and C: the fp32 GEMM from three TF32 products, or one TF32
+    product per product with tf32=True.  Sizes default to the logical extents
+    of the tensors."""
     import torch
     for t, n in ((A, "A"), (B, "B"), (C, "C")):
         if not t.is_cuda:
@@ -276,7 +283,7 @@ def gemm(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0, handle=None, 
     M = M if M is not None else (A.shape[1] if ta else A.shape[0])
     K = K if K is not None else (A.shape[0] if ta else A.shape[1])
     N = N if N is not None else (B.shape[0] if tb else B.shape[1])
-    code = dtype_code(A.dtype, C.dtype, B.dtype)
+    code = dtype_code(A.dtype, C.dtype, B.dtype, tf32)
     h = handle if handle is not None else default_handle(C.device.index)
     if stream is None:
         stream = torch.cuda.current_stream(C.device).cuda_stream

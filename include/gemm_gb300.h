@@ -54,6 +54,25 @@ typedef enum { GEMM_OP_N = 0, GEMM_OP_T = 1 } gemm_op_t;
  * 4 * (0 for fp32 C, 1 for bf16 C, 2 for fp16 C, 3 for E4M3 C).  Per-tensor
  * scale factors of FP8 data fold into alpha.
  *
+ * fp32 inputs ("GPU GEMM 优化完全拆解（三）", section 数值精度: the tensor cores
+ * take no fp32 operands; TF32 keeps the sign, the 8-bit exponent and 10
+ * fraction bits; three TF32 products emulate one fp32 product) run on the
+ * tensor core's TF32 kind (tcgen05.mma kind::tf32, 8 products of k per
+ * instruction) and write fp32 C:
+ *   GEMM_F32_F32   the fp32 GEMM: each value x is split into hi = TF32(x) and
+ *                  lo = TF32(x - hi) (rounded to nearest) and every product is
+ *                  lo_a hi_b + hi_a lo_b + hi_a hi_b, which misses a * b by
+ *                  about 2^-21 of |a b|.  Both operands are first written
+ *                  K-major as TF32 parts into the workspace (3 x K values a
+ *                  row: two more launches, 3x the operand bytes), then one
+ *                  TF32 GEMM over 3K sums the three products.
+ *   GEMM_TF32_F32  one TF32 product per product: the 13 low fraction bits of
+ *                  every input are dropped (about 2^-10 of each value).  A
+ *                  K-major operand (A with transA == GEMM_OP_N, B with transB
+ *                  == GEMM_OP_T) that the copy engine can load is read as it
+ *                  is; any other is first written K-major, cut the same way.
+ * Leading dimensions and strides are in elements (4 bytes).
+ *
  * E4M3 C is a quantised output: the fp32 result (after the fused epilogue of
  * gemm_run_ex, whose out_scale is the quantisation scale) is rounded to
  * nearest even and saturated to +-448.  It is written only: beta must be 0
@@ -66,6 +85,8 @@ typedef enum {
   GEMM_F16_F16 = 3,   /* A, B fp16; C fp16 */
   GEMM_BF16_E4M3 = 4, /* A, B bf16; C E4M3 (quantised output) */
   GEMM_F16_E4M3 = 5,  /* A, B fp16; C E4M3 (quantised output) */
+  GEMM_F32_F32 = 6,   /* A, B fp32; C fp32: three TF32 products per product */
+  GEMM_TF32_F32 = 7,  /* A, B fp32 read as TF32; C fp32: one TF32 product */
   GEMM_E4M3_F32 = 16,        /* A, B E4M3; C fp32 */
   GEMM_E5M2_E4M3_F32 = 17,   /* A E5M2, B E4M3; C fp32 */
   GEMM_E4M3_E5M2_F32 = 18,   /* A E4M3, B E5M2; C fp32 */
@@ -243,12 +264,13 @@ typedef struct {
   int32_t a_kmajor;        /* MMA A operand (rows of the MMA) has K contiguous */
   int32_t b_kmajor;        /* MMA B operand (columns of the MMA) has K contiguous */
   int32_t bm, bn, bk;      /* output tile (bm x bn; a CTA pair shares bm = 256) and the k-block
-                              of one stage: 64 x kdepth */
+                              of one stage: kdepth 128-byte k-slices (64 k for 16-bit
+                              inputs, 128 for 8-bit, 32 for fp32/TF32) */
   int32_t stages;          /* shared-memory ring depth, in stages of bk */
   int32_t split_k;         /* k-splits per output tile (1 = none) */
   int32_t raster_group;    /* tile rows per raster group */
-  int32_t repack_a;        /* A copied to an aligned workspace first */
-  int32_t repack_b;        /* B copied to an aligned workspace first */
+  int32_t repack_a;        /* A copied to an aligned workspace first (fp32: written as TF32 parts) */
+  int32_t repack_b;        /* B copied to an aligned workspace first (fp32: written as TF32 parts) */
   int32_t vector_store;    /* epilogue writes C rows with 16-byte (or bulk tensor) stores */
   int32_t grid;            /* CTAs launched for the main kernel */
   int32_t launches;        /* kernels launched by one gemm_run */
@@ -259,11 +281,11 @@ typedef struct {
   int32_t tiles_i;         /* schedule tiles along the MMA rows (M, or N when swapped) */
   int32_t tiles_j;         /* schedule tiles along the MMA columns (with multicast a schedule
                               tile is two neighbouring output tiles) */
-  int32_t num_kb;          /* k-blocks of bk per tile */
+  int32_t num_kb;          /* k-blocks of bk per tile (GEMM_F32_F32: over 3K) */
   int32_t dp_tiles;        /* tiles run whole (stream-K: the complete waves) */
   int32_t sk_slots;        /* stream-K: clusters sharing the remaining tiles' k-blocks */
   int32_t cluster;         /* CTAs per schedule slot: 1, 2 (a pair) or 4 (two pairs, multicast) */
-  int32_t kdepth;          /* 64-wide k-slices per ring stage (1 or 2): each stage's copies
+  int32_t kdepth;          /* 128-byte k-slices per ring stage (1 or 2): each stage's copies
                               complete one barrier */
   int32_t bulk_store;      /* how C leaves: 0 direct stores, 1 bulk tensor stores of rows,
                               2 bulk tensor stores of transposed blocks (swapped problems) */

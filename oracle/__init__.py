@@ -224,7 +224,7 @@ def epilogue(R, Mag, bias=None, act=ACT_NONE, scale=1.0):
     return R, Mag
 
 
-def within_tolerance(out, r, m, out_is_f32, e4m3=False, tf32=False):
+def within_tolerance(out, r, m, out_is_f32, e4m3=False, tf32=False, tf32x3_k=None):
     """Elementwise comparison rule for a GPU result ``out`` against (r, m).
 
     fp32 output:       |out - r| <= 1e-3 * m + 1e-5
@@ -235,10 +235,20 @@ def within_tolerance(out, r, m, out_is_f32, e4m3=False, tf32=False):
     Products of TF32-rounded inputs (tf32=True, one pass; each input keeps
     10 fraction bits, so a product is off by up to ~2^-10 relative):
     |out - r| <= 2^-8 * m + 1e-5.
+    fp32 products from three TF32 products (tf32x3_k = K): each x = hi + lo +
+    e with hi, lo TF32 values and |e| <= 2^-22 |x|; dropping lo_a lo_b and
+    the two e terms costs at most 2^-20 |a b| per product; the fp32 sum of 3K
+    terms (each partial sum at most m, each addition off by at most 2^-23 of
+    it, truncation included) adds at most 3K * 2^-23 * m:
+    |out - r| <= (3K * 2^-23 + 2^-20) * m + 2^-126.
     A NaN or Inf in ``out`` where r is finite fails.
     Returns a boolean array (True = within tolerance).
     """
     out = np.asarray(out, dtype=np.float64)
+    if tf32x3_k is not None:
+        ok = np.abs(out - r) <= (3 * int(tf32x3_k) * 2.0 ** -23 + 2.0 ** -20) * m + 2.0 ** -126
+        ok &= np.isfinite(out) | ~np.isfinite(r)
+        return ok
     if tf32:
         ok = np.abs(out - r) <= 2.0 ** -8 * m + 1e-5
         ok &= np.isfinite(out) | ~np.isfinite(r)

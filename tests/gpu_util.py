@@ -8,7 +8,8 @@ from dense_gemm_10_gb300 import gemm as G
 from dense_gemm_10_gb300 import inputs
 
 _TORCH = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
-_ORACLE_IN = {"bf16": oracle.IN_BF16, "f16": oracle.IN_F16, "e4m3": oracle.IN_E4M3, "e5m2": oracle.IN_E5M2}
+_ORACLE_IN = {"bf16": oracle.IN_BF16, "f16": oracle.IN_F16, "e4m3": oracle.IN_E4M3, "e5m2": oracle.IN_E5M2,
+              "f32": oracle.IN_F32}
 SENTINEL = 1536.0   # exact in fp32, bf16 and fp16
 
 
@@ -17,7 +18,7 @@ def dtype_code(p):
         return G.fp8_dtype(p.in_dtype, p.b_dtype, p.out_dtype)
     return {("bf16", "f32"): G.BF16_F32, ("bf16", "bf16"): G.BF16_BF16, ("f16", "f32"): G.F16_F32,
             ("f16", "f16"): G.F16_F16, ("bf16", "e4m3"): G.BF16_E4M3,
-            ("f16", "e4m3"): G.F16_E4M3}[(p.in_dtype, p.out_dtype)]
+            ("f16", "e4m3"): G.F16_E4M3, ("f32", "f32"): G.F32_F32}[(p.in_dtype, p.out_dtype)]
 
 
 def device_problem(p, guard_rows=0, guard_cols=0):
@@ -35,17 +36,18 @@ def device_problem(p, guard_rows=0, guard_cols=0):
     return Ad, Bd, Cd, ldc
 
 
-def launch(p, h, Ad, Bd, Cd, ldc, stream=None):
+def launch(p, h, Ad, Bd, Cd, ldc, stream=None, code=None):
     st = h.run_raw(p.transA, p.transB, p.M, p.N, p.K, p.alpha, Ad.data_ptr(), p.lda, Bd.data_ptr(), p.ldb,
-                   p.beta, Cd.data_ptr(), ldc, dtype_code(p), stream)
+                   p.beta, Cd.data_ptr(), ldc, dtype_code(p) if code is None else code, stream)
     if st != G.OK:
         raise G.GemmError(st, "gemm_run")
 
 
-def run(p, h, guard_rows=0, guard_cols=0):
-    """Run p on the GPU; returns (C as fp64 numpy M x N, whole C buffer on the CPU)."""
+def run(p, h, guard_rows=0, guard_cols=0, code=None):
+    """Run p on the GPU (dtype code `code`, default the problem's own); returns
+    (C as fp64 numpy M x N, whole C buffer on the CPU)."""
     Ad, Bd, Cd, ldc = device_problem(p, guard_rows, guard_cols)
-    launch(p, h, Ad, Bd, Cd, ldc)
+    launch(p, h, Ad, Bd, Cd, ldc, code=code)
     st, detail = h.status()
     assert st == G.OK, "kernel status %s (word 0x%x)" % (G.STATUS.get(st), detail)
     full = Cd.cpu()

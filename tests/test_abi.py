@@ -151,12 +151,37 @@ def test_plan_fp8():
         with pytest.raises(G.GemmError) as e:
             G.plan(256, 256, 256, ta, tb, G.E4M3_F32)
         assert e.value.status == G.ERR_UNSUPPORTED
-    for bad in (6, 15, 32):
+    for bad in (8, 15, 32):
         with pytest.raises(G.GemmError) as e:
             G.plan(256, 256, 256, 0, 1, bad)
         assert e.value.status == G.ERR_INVALID_ARG
     assert [G.fp8_dtype(a, b, c) for c in ("f32", "bf16", "f16", "e4m3") for b in ("e4m3", "e5m2")
             for a in ("e4m3", "e5m2")] == list(range(16, 32))
+
+
+def test_plan_fp32():
+    """fp32 inputs: 32-element (128-byte) k-slices of the TF32 kind, K-major only.
+    The fp32 GEMM writes both operands as TF32 parts (3K values a row, padded to
+    16 bytes) and runs one GEMM over 3K; one-pass TF32 reads aligned K-major
+    operands as they are and writes only the others."""
+    p = G.plan(4096, 4096, 4096, 0, 1, G.F32_F32)
+    assert p.path == G.PATH_TC_2CTA and p.bn == 256 and p.bk == 32 and p.num_kb == 3 * 4096 // 32
+    assert p.repack_a == 1 and p.repack_b == 1 and p.launches == 3 and p.a_kmajor == 1 and p.b_kmajor == 1
+    assert p.workspace_bytes >= 2 * 4096 * 3 * 4096 * 4
+    t = G.plan(4096, 4096, 4096, 0, 1, G.TF32_F32)
+    assert t.bk == 32 and t.num_kb == 128 and t.repack_a == 0 and t.repack_b == 0 and t.launches == 1
+    for ta, tb in [(0, 0), (1, 0), (1, 1)]:   # MN-major operands are written K-major first
+        u = G.plan(256, 264, 300, ta, tb, G.TF32_F32)
+        assert (u.repack_a, u.repack_b) == (ta, 1 - tb) and u.a_kmajor == 1 and u.b_kmajor == 1
+        assert u.launches == 1 + ta + (1 - tb)
+    r = G.plan(300, 520, 301, 0, 1, G.F32_F32, lda=301, ldb=301)
+    assert r.bk == 32 * r.kdepth and r.num_kb == -(-3 * 301 // r.bk)
+    assert r.workspace_bytes >= (300 + 520) * 904 * 4          # 903 values a row, padded to 904
+    v = G.plan(300, 520, 301, 0, 1, G.TF32_F32, lda=301, ldb=304)
+    assert v.repack_a == 1 and v.repack_b == 0                 # 1204-byte rows: not 16-byte aligned
+    s = G.plan(16, 4096, 4096, 0, 1, G.F32_F32)
+    assert s.swap_ab == 1 and s.bn == 64
+
 
 
 def test_plan_e4m3_output():

@@ -302,7 +302,7 @@ def test_bad_arguments_return_errors(h):
     assert h.run_raw(0, 0, 8, 8, 8, 1.0, A.data_ptr(), 7, A.data_ptr(), 8, 0.0, C.data_ptr(), 8, 0, None) \
         == G.ERR_INVALID_ARG
     assert h.run_raw(0, 0, 8, 8, 8, 1.0, 0, 8, A.data_ptr(), 8, 0.0, C.data_ptr(), 8, 0, None) == G.ERR_INVALID_ARG
-    assert h.run_raw(0, 0, 8, 8, 8, 1.0, A.data_ptr(), 8, A.data_ptr(), 8, 0.0, C.data_ptr(), 8, 6, None) \
+    assert h.run_raw(0, 0, 8, 8, 8, 1.0, A.data_ptr(), 8, A.data_ptr(), 8, 0.0, C.data_ptr(), 8, 8, None) \
         == G.ERR_INVALID_ARG
 
 

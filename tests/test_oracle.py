@@ -456,6 +456,26 @@ def test_tf32_tolerance_rule():
         == [True, False, False]
 
 
+def test_tf32x3_tolerance_rule():
+    """K = 64: (192 * 2^-23 + 2^-20) = 2^-15.32...; a 1-ulp fp32 error passes, 2^-14 does not."""
+    r = np.array([1.0, 1.0, 1.0, 0.0, 5.0])
+    m = np.array([1.0, 1.0, 1.0, 0.0, 5.0])
+    bound = 192 * 2.0 ** -23 + 2.0 ** -20
+    out = np.array([1.0 + 2.0 ** -23, 1.0 + 0.99 * bound, 1.0 + 2.0 ** -14, 0.0, np.nan])
+    assert list(oracle.within_tolerance(out, r, m, True, tf32x3_k=64)) == [True, True, False, True, False]
+    # the error bound of the split itself: x - hi - lo for hi, lo rounded to TF32
+    g = np.random.default_rng(1)
+    x = g.standard_normal(10000).astype(np.float32).astype(np.float64)
+    def tf32(v):   # round to nearest on 10 fraction bits (ties away from zero)
+        e = np.floor(np.log2(np.abs(v)))
+        q = 2.0 ** (e - 10)
+        return np.sign(v) * np.floor(np.abs(v) / q + 0.5) * q
+    hi = tf32(x)
+    lo = np.where(x != hi, tf32(np.where(x != hi, x - hi, 1.0)), 0.0)
+    assert np.all(np.abs(x - hi) <= 2.0 ** -11 * np.abs(x))
+    assert np.all(np.abs(x - hi - lo) <= 2.0 ** -22 * np.abs(x))
+
+
 # ---------------------------------------------------------------------------
 # Strided batched GEMM
 # ---------------------------------------------------------------------------
