@@ -13,6 +13,8 @@ Also reported, in the same line:
   cpu_baseline  the CPU oracle (plain fp64 triple loop) on a bounded sample
   skinny        the LM-head GEMM (M = 64, K = 4096, N = 32000) in GB/s
   fp8           the 4096^3 GEMM with 8-bit E4M3 inputs in TFLOP/s
+  fp32          the 4096^3 fp32 GEMM from three TF32 products (and with one
+                TF32 product) in TFLOP/s of fp32 work
   clocks        SM clocks and throttle reasons sampled during the timed region
 
 `--impl reference` times the CPU oracle instead (the reference arm).
@@ -51,6 +53,8 @@ def parse():
     ap.add_argument("--no-skinny", action="store_true")
     ap.add_argument("--fp8-steps", type=int, default=4000)
     ap.add_argument("--no-fp8", action="store_true")
+    ap.add_argument("--fp32-steps", type=int, default=300)
+    ap.add_argument("--no-fp32", action="store_true")
     return ap.parse_args()
 
 
@@ -340,6 +344,9 @@ def run_ours(args):
     fp8 = None
     if not args.no_fp8:
         fp8 = run_fp8(args, G, h, inputs, metrics, dev, stream, pk, pk_src)
+    fp32 = None
+    if not args.no_fp32:
+        fp32 = run_fp32(args, G, h, inputs, metrics, dev, stream, pk, pk_src)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -359,7 +366,7 @@ def run_ours(args):
                        "plan": plan.as_dict(), "parallelism": "replicas" if ws > 1 else "single GPU",
                        "wall_s_timed_region": wall},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clk, "skinny": skinny, "fp8": fp8,
+            "clocks": clk, "skinny": skinny, "fp8": fp8, "fp32": fp32,
         }
         print(json.dumps(line), flush=True)
     h.close()
@@ -413,6 +420,59 @@ def run_fp8(args, G, h, inputs, metrics, dev, stream, pk, pk_src):
                                                      % (plan.bn, cg))},
             "plan": plan.as_dict(), "l2": "%d rotating input sets (%.0f MB total)" % (
                 n_sets, n_sets * set_bytes / 2 ** 20)}
+
+
+def run_fp32(args, G, h, inputs, metrics, dev, stream, pk, pk_src):
+    """4096^3 with fp32 inputs and C (A M x K, B N x K): the fp32 GEMM from
+    three TF32 products per product (two split launches and one GEMM over 3K)
+    and, for comparison, one TF32 product per product (one launch).  Values are
+    TFLOP/s of fp32 work (2 M N K per call); the roofline counts the TF32
+    products the tensor cores execute against the measured bf16 burst peak
+    scaled by the nominal TF32 / bf16 dense ratio (1.1 / 2.25)."""
+    import torch
+    p = inputs.square_4096_f32_nt(SIZE)
+    set_bytes = (p.A.numel() + p.B.numel() + p.M * p.N) * 4
+    n_sets = max(2, math.ceil(2 * L2_BYTES / set_bytes) + 1)
+    sets = [(p.A.to(dev), p.B.to(dev), torch.empty(p.M, p.N, dtype=torch.float32, device=dev))
+            for _ in range(n_sets)]
+    sptr = stream.cuda_stream
+    peak = 1.1 / 2.25 * float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    out = {"workload": "square_4096_f32_nt_f32", "unit": "TFLOP/s",
+           "l2": "%d rotating input sets (%.0f MB total)" % (n_sets, n_sets * set_bytes / 2 ** 20)}
+    for name, code, parts in (("f32_3xtf32", G.F32_F32, 3), ("tf32", G.TF32_F32, 1)):
+        def step(i):
+            A, B, C = sets[i % n_sets]
+            st = h.run_raw(0, 1, p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, 0.0,
+                           C.data_ptr(), p.N, code, sptr)
+            if st != G.OK:
+                raise G.GemmError(st, "gemm_run")
+
+        steps = args.fp32_steps * (3 if parts == 1 else 1)
+        with torch.cuda.stream(stream):
+            for i in range(5):
+                step(i)
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(steps):
+                step(i)
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        st, word = h.status(sptr)
+        if st != G.OK:
+            raise RuntimeError("fp32 kernel status %s (0x%x)" % (G.STATUS.get(st), word))
+        ms = e0.elapsed_time(e1) / steps
+        tflops = metrics.flops(p.M, p.N, p.K) / (ms / 1e3) / 1e12
+        plan = G.plan(p.M, p.N, p.K, 0, 1, code)
+        out[name] = {"value": tflops, "us_per_call": ms * 1e3, "launches_per_call": plan.launches,
+                     "roofline": {"bound": "tensor", "achieved": parts * tflops, "peak": peak, "unit": "TFLOP/s",
+                                  "frac": parts * tflops / peak,
+                                  "peak_source": "%s bf16_tflops x 1.1 / 2.25 (nominal TF32 / bf16 dense ratio)"
+                                                 % pk_src,
+                                  "achieved_counts": "%d TF32 products per product, whole call" % parts},
+                     "plan": plan.as_dict()}
+    out["value"] = out["f32_3xtf32"]["value"]
+    return out
 
 
 def run_skinny(args, G, h, inputs, metrics, dev, stream, pk, pk_src):

@@ -343,6 +343,13 @@ def square_4096_fp8_nt(fmt="e4m3", out_dtype="f32", size=4096):
                         out_dtype, ("normal", 0.0, 1.0), ("normal", 0.0, 1.0), alpha=1.0 / size)
 
 
+def square_4096_f32_nt(size=4096):
+    """M = N = K = 4096 fp32, A row-major, B column-major (NT), entries N(0, 1),
+    alpha 1 / K so that C is O(1): the fp32 GEMM emulated with TF32 products."""
+    return make_problem("square_%d_f32_nt_f32" % size, size, size, size, 0, 1, "f32", "f32",
+                        ("normal", 0.0, 1.0), ("normal", 0.0, 1.0), alpha=1.0 / size)
+
+
 def bits(t):
     """Raw bit patterns of an input tensor, without copying values: numpy
     uint16 for bf16 / fp16, uint8 for the 8-bit formats, float32 as it is."""
