@@ -164,7 +164,9 @@ class ClockSampler:
     def start(self):
         try:
             import tempfile
-            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            scratch = os.path.join(ROOT, ".scratch")   # inside the repository, git-ignored
+            os.makedirs(scratch, exist_ok=True)
+            fd, self.path = tempfile.mkstemp(suffix=".csv", dir=scratch)
             os.close(fd)
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
                                           "--format=csv,noheader,nounits", "-lms", "200"],

@@ -350,6 +350,130 @@ def square_4096_f32_nt(size=4096):
                         ("normal", 0.0, 1.0), ("normal", 0.0, 1.0), alpha=1.0 / size)
 
 
+# ----------------------------------------------------------------------------
+# Block-scaled inputs: MXFP8 (E4M3 / E5M2 codes, one E8M0 scale per 32 values
+# of k) and NVFP4 (E2M1 codes packed two to a byte, one unsigned E4M3 scale per
+# 16).  Values are drawn in float32 as N(0, 1) times a per-block power of two
+# 2^t, t uniform in [-6, 6], so that the scales differ from block to block;
+# each block is then quantised the usual way for its format:
+#   MXFP8: shared exponent e = floor(log2(max |x|)) - emax (emax 8 for E4M3,
+#          15 for E5M2), scale code e + 127, codes = RNE(x / 2^e) saturated;
+#   NVFP4: scale = RNE_E4M3(max |x| / 6), codes = the nearest E2M1 value of
+#          x / scale (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6).
+# This prepares data; the GEMM arithmetic on it lives in the oracle and the
+# kernels.  Scale rows are padded to 16 bytes with the code 0xFF (NaN as
+# E8M0), matrix rows past K with 0xFF bytes: neither may be read.
+
+BLOCK_FORMATS = {"mxfp8": ("e8m0", 32), "nvfp4": ("ue4m3", 16)}
+_E2M1_MAGS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float32)
+
+
+def _block_values(rows, K, block, seed, seed_t):
+    g, gt = _rng(seed), _rng(seed_t)
+    nblk = -(-K // block)
+    t = gt.integers(-6, 7, size=(rows, nblk)).astype(np.float32)
+    x = g.standard_normal(size=(rows, nblk * block), dtype=np.float32)
+    x = x.reshape(rows, nblk, block) * np.exp2(t)[..., None]
+    if nblk * block > K:   # the last block's tail lies past K: no values there
+        flat = x.reshape(rows, nblk * block)
+        flat[:, K:] = 0.0
+    return x
+
+
+def _quantise(x, fmt, elem):
+    """x: rows x nblk x block float32 -> (codes rows x nblk*block uint8, scale codes rows x nblk uint8)."""
+    rows, nblk, block = x.shape
+    amax = np.abs(x).max(axis=2)
+    if fmt == "mxfp8":
+        emax, vmax = (8, 448.0) if elem == "e4m3" else (15, 57344.0)
+        e = np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - emax
+        e = np.clip(e, -127, 127)
+        sf = (e + 127).astype(np.uint8)
+        q = np.clip(x / np.exp2(e)[..., None], -vmax, vmax).astype(np.float32)
+        codes = torch.from_numpy(np.ascontiguousarray(q.reshape(rows, -1))).to(_TORCH_DT[elem])
+        return codes.view(torch.uint8).numpy(), sf
+    sf_t = torch.from_numpy(np.ascontiguousarray((amax / 6.0).astype(np.float32))).to(torch.float8_e4m3fn)
+    sf = sf_t.view(torch.uint8).numpy().copy()
+    scale = sf_t.to(torch.float32).numpy()
+    q = x / np.where(scale > 0, scale, 1.0)[..., None]
+    idx = np.abs(np.abs(q)[..., None] - _E2M1_MAGS).argmin(axis=-1).astype(np.uint8)
+    codes = idx | ((q < 0).astype(np.uint8) << 3)
+    return codes.reshape(rows, -1), sf
+
+
+def _store_codes(codes, K, ld, elem):
+    """rows x >= K codes -> rows x bytes-per-row uint8 tensor (E2M1: two per byte, even one low)."""
+    rows = codes.shape[0]
+    if elem == "e2m1":
+        c = np.zeros((rows, ld), dtype=np.uint8)
+        c[:, :K] = codes[:, :K]
+        packed = c[:, 0::2] | (c[:, 1::2] << 4)
+        packed[:, -(-K // 2):] = 0xFF
+        return torch.from_numpy(np.ascontiguousarray(packed))
+    out = np.full((rows, ld), 0xFF, dtype=np.uint8)
+    out[:, :K] = codes[:, :K]
+    return torch.from_numpy(out)
+
+
+@dataclass
+class BlockScaledProblem:
+    """C = alpha * A' * B'^T + beta * C0 with A' (M x K) and B' (N x K) given as
+    block-scaled codes: A, B uint8 tensors of the stored rows (lda / ldb in
+    elements; E2M1 packs two elements a byte), SFA (M x ld_sfa) and SFB (N x
+    ld_sfb) the scale codes, one per `block` values of k."""
+    name: str
+    M: int
+    N: int
+    K: int
+    fmt: str          # "mxfp8" | "nvfp4"
+    a_elem: str       # "e4m3" | "e5m2" | "e2m1"
+    b_elem: str
+    out_dtype: str
+    alpha: float
+    beta: float
+    A: torch.Tensor
+    lda: int
+    SFA: torch.Tensor
+    ld_sfa: int
+    B: torch.Tensor
+    ldb: int
+    SFB: torch.Tensor
+    ld_sfb: int
+    C0: object
+    ldc: int
+    block: int
+    seed: int
+
+
+def make_block_scaled_problem(name, M, N, K, fmt="mxfp8", out_dtype="f32", a_elem=None, b_elem=None, alpha=1.0,
+                              beta=0.0, seed=0, lda=None, ldb=None, ldc=None, ld_sf=None):
+    """A from seeds (s, s + 3), B from (s + 1, s + 4), C0 from s + 2.  Default
+    leading dimensions: K rounded up to 16 bytes of codes; scale rows padded
+    to 16 bytes."""
+    _, block = BLOCK_FORMATS[fmt]
+    a_elem = a_elem or ("e4m3" if fmt == "mxfp8" else "e2m1")
+    b_elem = b_elem or a_elem
+    per16 = 32 if fmt == "nvfp4" else 16          # elements in 16 bytes
+    up = lambda v, m: -(-v // m) * m
+    lda = up(K, per16) if lda is None else lda
+    ldb = up(K, per16) if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    nblk = -(-K // block)
+    ld_sf = up(max(nblk, 1), 16) if ld_sf is None else ld_sf
+    mats = []
+    for rows, elem, sv, st, ld in ((M, a_elem, seed, seed + 3, lda), (N, b_elem, seed + 1, seed + 4, ldb)):
+        codes, sf = _quantise(_block_values(rows, K, block, sv, st), fmt, elem)
+        sfs = np.full((rows, ld_sf), 0xFF, dtype=np.uint8)
+        sfs[:, :nblk] = sf
+        mats.append((_store_codes(codes, K, ld, elem), torch.from_numpy(sfs)))
+    C0 = None
+    if beta != 0.0:
+        C0 = _pad_columns(draw((M, N), ("normal", 0.0, 1.0), seed + 2, out_dtype), ldc, out_dtype)
+    return BlockScaledProblem(name, M, N, K, fmt, a_elem, b_elem, out_dtype, float(alpha), float(beta),
+                              mats[0][0], lda, mats[0][1], ld_sf, mats[1][0], ldb, mats[1][1], ld_sf, C0, ldc,
+                              block, seed)
+
+
 def bits(t):
     """Raw bit patterns of an input tensor, without copying values: numpy
     uint16 for bf16 / fp16, uint8 for the 8-bit formats, float32 as it is."""

@@ -8,7 +8,8 @@ precision as the page at m.lqnn.cn/news/285670 does in its section 1.2).
 
 Inputs are the raw bit patterns of the matrices, in the row-major storage
 convention described in ``gemm_oracle.c``: numpy ``uint16`` for bf16 / fp16,
-``uint8`` for the 8-bit E4M3 / E5M2 formats.
+``uint8`` for the 8-bit E4M3 / E5M2 formats and for packed FP4 E2M1 (two
+elements a byte, the even one in the low four bits), ``float32`` for fp32.
 Every function here is pinned by ``tests/test_oracle.py``.
 """
 import ctypes
@@ -21,7 +22,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gemm_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle_gemm.so")
 
-IN_BF16, IN_F16, IN_E4M3, IN_E5M2, IN_F32 = 0, 1, 2, 3, 4
+IN_BF16, IN_F16, IN_E4M3, IN_E5M2, IN_F32, IN_E2M1 = 0, 1, 2, 3, 4, 5
+SF_E8M0, SF_UE4M3 = 0, 1
 C_F32, C_BF16, C_F16 = 0, 1, 2
 
 _lib = None
@@ -71,6 +73,12 @@ def _load():
     lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
     lib.oracle_e5m2_value.restype = dbl
     lib.oracle_e5m2_value.argtypes = [ctypes.c_uint8]
+    for name in ("oracle_e2m1_value", "oracle_e8m0_value", "oracle_ue4m3_value"):
+        getattr(lib, name).restype = dbl
+        getattr(lib, name).argtypes = [ctypes.c_uint8]
+    lib.oracle_gemm_block_scaled.restype = i32
+    lib.oracle_gemm_block_scaled.argtypes = [i64, i64, i64, dbl, vp, i64, vp, i64, vp, i64, vp, i64, dbl, vp, i32,
+                                             i64, i32, i32, i32, i64, i64, vp, vp, vp, vp, i64, i32]
     _lib = lib
     return lib
 
@@ -95,9 +103,24 @@ def e5m2_value(bits):
     return _load().oracle_e5m2_value(int(bits) & 0xFF)
 
 
+def e2m1_value(bits):
+    """Value of one FP4 E2M1 code (low four bits), decoded from the format definition."""
+    return _load().oracle_e2m1_value(int(bits) & 0xF)
+
+
+def e8m0_value(bits):
+    """Value of one E8M0 scale-factor code: 2^(bits - 127), NaN for 255."""
+    return _load().oracle_e8m0_value(int(bits) & 0xFF)
+
+
+def ue4m3_value(bits):
+    """Value of one unsigned E4M3 scale-factor code (sign bit ignored)."""
+    return _load().oracle_ue4m3_value(int(bits) & 0xFF)
+
+
 def _codes(X, in_type):
     """The stored matrix as an array of codes of the type's width."""
-    want = np.uint8 if in_type in (IN_E4M3, IN_E5M2) else np.float32 if in_type == IN_F32 else np.uint16
+    want = np.uint8 if in_type in (IN_E4M3, IN_E5M2, IN_E2M1) else np.float32 if in_type == IN_F32 else np.uint16
     X = np.ascontiguousarray(X)
     if X.dtype != want:
         raise TypeError("input of type %d must be %s codes" % (in_type, want.__name__))
@@ -202,6 +225,41 @@ def gemm_at(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc, in_ty
     if rc < 0:
         raise ValueError("oracle_gemm_at rejected its arguments")
     return r, m
+
+
+def gemm_block_scaled(M, N, K, alpha, A, lda, SFA, ld_sfa, B, ldb, SFB, ld_sfb, beta, C0, ldc, a_type, b_type,
+                      sf_type, block, rows=None, cols=None, c_type=C_F32, nthreads=0):
+    """Block-scaled oracle (MXFP8: E4M3 / E5M2 with an E8M0 scale per 32 values
+    of k; NVFP4: packed E2M1 with an unsigned E4M3 scale per 16).  A is stored
+    M x K, B N x K (K contiguous, lda / ldb in elements); SFA / SFB are uint8
+    scale codes, one per block of k, rows of ld_sfa / ld_sfb codes.  Returns
+    (R, Mag): M x N arrays, or arrays of the sampled entries when rows / cols
+    are given."""
+    lib = _load()
+    A = _codes(A, a_type)
+    B = _codes(B, b_type)
+    SFA = np.ascontiguousarray(SFA, dtype=np.uint8)
+    SFB = np.ascontiguousarray(SFB, dtype=np.uint8)
+    C0 = _c0_array(C0, c_type) if beta != 0.0 else None
+    if rows is None:
+        R = np.zeros((M, N), dtype=np.float64)
+        Mag = np.zeros((M, N), dtype=np.float64)
+        count, rp, cp = 0, None, None
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        cols = np.ascontiguousarray(cols, dtype=np.int64)
+        if rows.shape != cols.shape:
+            raise ValueError("rows and cols differ in length")
+        R = np.zeros(rows.shape, dtype=np.float64)
+        Mag = np.zeros(rows.shape, dtype=np.float64)
+        count, rp, cp = rows.size, _ptr(rows), _ptr(cols)
+    rc = lib.oracle_gemm_block_scaled(M, N, K, float(alpha), _ptr(A), lda, _ptr(SFA), ld_sfa, _ptr(B), ldb,
+                                      _ptr(SFB), ld_sfb, float(beta), _ptr(C0), int(c_type), ldc, int(a_type),
+                                      int(b_type), int(sf_type), int(block), count, rp, cp, _ptr(R), _ptr(Mag), N,
+                                      int(nthreads))
+    if rc < 0:
+        raise ValueError("oracle_gemm_block_scaled rejected its arguments")
+    return R, Mag
 
 
 ACT_NONE, ACT_RELU, ACT_GELU = 0, 1, 2

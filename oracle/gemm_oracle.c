@@ -43,6 +43,20 @@
  * product of two of them (at most 22 significant bits), so the only rounding
  * in s_ij is that of the fp64 additions.
  *
+ * Block-scaled inputs ("CUDA GEMM 矩阵乘法优化指南", 13.2: block scaling with
+ * the FP4 / FP8 formats; MXFP8: every 32 consecutive elements share one E8M0
+ * scale factor; NVFP4: every 16 share one E4M3 scale factor):
+ *   a(i, k) = elem(A, i, k) * sf(SFA[i * ld_sfa + k / block])
+ *   b(k, j) = elem(B, j, k) * sf(SFB[j * ld_sfb + k / block])
+ * with A stored M x K and B stored N x K (K contiguous in both) and
+ *   E8M0:  2^(x - 127), 255 is NaN (an exponent-only scale);
+ *   UE4M3: the E4M3 value of the code with its sign bit ignored;
+ *   E2M1 elements (FP4): sign, 2-bit exponent with bias 1, 1-bit fraction
+ *          (values 0, 0.5, 1, 1.5, 2, 3, 4, 6), two per byte, the even
+ *          element of a pair in the low four bits.
+ * Each a(i, k) * b(k, j) is a product of values with at most 4 significant
+ * bits times powers of two, exact in fp64.
+ *
  * Rows of C are split over POSIX threads; the loop body is the definition.
  */
 #include <math.h>
@@ -51,7 +65,9 @@
 #include <stdlib.h>
 #include <unistd.h>
 
-enum { ORACLE_IN_BF16 = 0, ORACLE_IN_F16 = 1, ORACLE_IN_E4M3 = 2, ORACLE_IN_E5M2 = 3, ORACLE_IN_F32 = 4 };
+enum { ORACLE_IN_BF16 = 0, ORACLE_IN_F16 = 1, ORACLE_IN_E4M3 = 2, ORACLE_IN_E5M2 = 3, ORACLE_IN_F32 = 4,
+       ORACLE_IN_E2M1 = 5 };
+enum { ORACLE_SF_E8M0 = 0, ORACLE_SF_UE4M3 = 1 };
 enum { ORACLE_C_F32 = 0, ORACLE_C_BF16 = 1, ORACLE_C_F16 = 2 };
 
 /* bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits. */
@@ -118,9 +134,28 @@ double oracle_e5m2_value(uint8_t b) {
   return sign ? -v : v;
 }
 
+/* FP4 E2M1 (low four bits of x): 1 sign bit, 2 exponent bits (bias 1), 1 fraction bit. */
+double oracle_e2m1_value(uint8_t x) {
+  int sign = (x >> 3) & 1;
+  int e = (x >> 1) & 0x3;
+  int f = x & 0x1;
+  double v = e == 0 ? (double)f / 2.0 /* subnormal: 0.f * 2^(1-1) */ : ldexp(1.0 + (double)f / 2.0, e - 1);
+  return sign ? -v : v;
+}
+
+/* E8M0 scale factor: 2^(x - 127); 255 is NaN. */
+double oracle_e8m0_value(uint8_t x) { return x == 255 ? NAN : ldexp(1.0, (int)x - 127); }
+
+/* Unsigned E4M3 scale factor: the E4M3 value with the sign bit ignored. */
+double oracle_ue4m3_value(uint8_t x) { return oracle_e4m3_value((uint8_t)(x & 0x7F)); }
+
 /* Element idx of a stored matrix of the given input type. */
 static double in_value(int in_type, const void* base, int64_t idx) {
   switch (in_type) {
+    case ORACLE_IN_E2M1: {
+      const uint8_t byte = ((const uint8_t*)base)[idx >> 1];
+      return oracle_e2m1_value((idx & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF));
+    }
     case ORACLE_IN_F16: return oracle_f16_value(((const uint16_t*)base)[idx]);
     case ORACLE_IN_E4M3: return oracle_e4m3_value(((const uint8_t*)base)[idx]);
     case ORACLE_IN_E5M2: return oracle_e5m2_value(((const uint8_t*)base)[idx]);
@@ -129,7 +164,9 @@ static double in_value(int in_type, const void* base, int64_t idx) {
   }
 }
 
+/* Bytes per element (0 for E2M1, which packs two to a byte). */
 static int64_t elem_bytes(int in_type) {
+  if (in_type == ORACLE_IN_E2M1) return 0;
   return (in_type == ORACLE_IN_E4M3 || in_type == ORACLE_IN_E5M2) ? 1 : in_type == ORACLE_IN_F32 ? 4 : 2;
 }
 
@@ -146,6 +183,11 @@ typedef struct {
   const void* A;
   const void* B;
   const void* C0;
+  /* block scaling (block > 0): scale factors of A's and B's blocks of k */
+  int64_t block, ld_sfa, ld_sfb;
+  int sf_type;
+  const uint8_t* SFA;
+  const uint8_t* SFB;
   /* full mode: rows [row0, row1) of R / Mag */
   double* R;
   double* Mag;
@@ -156,12 +198,20 @@ typedef struct {
   int64_t e0, e1;
 } job_t;
 
+static double sf_value(int sf_type, uint8_t x) {
+  return sf_type == ORACLE_SF_UE4M3 ? oracle_ue4m3_value(x) : oracle_e8m0_value(x);
+}
+
 /* One output element, straight from the definition. */
 static void element(const job_t* J, int64_t i, int64_t j, double* r, double* m) {
   double s = 0.0, sa = 0.0;
   for (int64_t k = 0; k < J->K; ++k) {
     double a = in_value(J->a_type, J->A, J->transA ? k * J->lda + i : i * J->lda + k);
     double b = in_value(J->b_type, J->B, J->transB ? j * J->ldb + k : k * J->ldb + j);
+    if (J->block > 0) {
+      a *= sf_value(J->sf_type, J->SFA[i * J->ld_sfa + k / J->block]);
+      b *= sf_value(J->sf_type, J->SFB[j * J->ld_sfb + k / J->block]);
+    }
     double p = a * b;
     s += p;
     sa += fabs(p);
@@ -218,8 +268,8 @@ static int check_args(int transA, int transB, int64_t M, int64_t N, int64_t K, i
                       int64_t ldb, int a_type, int b_type, int c_type) {
   if (M < 0 || N < 0 || K < 0) return -1;
   if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1)) return -1;
-  if (a_type < ORACLE_IN_BF16 || a_type > ORACLE_IN_F32) return -1;
-  if (b_type < ORACLE_IN_BF16 || b_type > ORACLE_IN_F32) return -1;
+  if (a_type < ORACLE_IN_BF16 || a_type > ORACLE_IN_E2M1) return -1;
+  if (b_type < ORACLE_IN_BF16 || b_type > ORACLE_IN_E2M1) return -1;
   if (c_type != ORACLE_C_F32 && c_type != ORACLE_C_BF16 && c_type != ORACLE_C_F16) return -1;
   if (lda < (transA ? M : K) || ldb < (transB ? K : N)) return -1;
   return 0;
@@ -360,6 +410,7 @@ int oracle_gemm_batched(int transA, int transB, int64_t M, int64_t N, int64_t K,
   if (batch < 0 || strideA < 0 || strideB < 0 || strideC < 0) return -1;
   const int64_t ea = elem_bytes(a_type);
   const int64_t eb = elem_bytes(b_type);
+  if (ea == 0 || eb == 0) return -1;  /* packed FP4: block-scaled entry point only */
   const int64_t ec = c_type == ORACLE_C_F32 ? 4 : 2;
   int used = 0;
   for (int64_t b = 0; b < batch; ++b) {
@@ -390,6 +441,7 @@ int oracle_gemm_grouped(int transB, int64_t groups, const int64_t* m_sizes, int6
   if (groups < 0 || strideB < 0) return -1;
   const int64_t ea = elem_bytes(a_type);
   const int64_t eb = elem_bytes(b_type);
+  if (ea == 0 || eb == 0) return -1;  /* packed FP4: block-scaled entry point only */
   const int64_t ec = c_type == ORACLE_C_F32 ? 4 : 2;
   int64_t off = 0;
   for (int64_t g = 0; g < groups; ++g) {
@@ -404,4 +456,53 @@ int oracle_gemm_grouped(int transB, int64_t groups, const int64_t* m_sizes, int6
     off += m;
   }
   return 0;
+}
+
+/*
+ * Block-scaled oracle (see the header): A stored M x K, B stored N x K, both
+ * with K contiguous (lda, ldb in elements; even for E2M1), a_type / b_type
+ * E4M3, E5M2 or E2M1; SFA M x ceil(K / block) and SFB N x ceil(K / block)
+ * scale codes of sf_type, row pitches ld_sfa / ld_sfb.  Full mode when rows ==
+ * NULL (R, Mag M x N with leading dimension ldr), else the `count` entries
+ * (rows[e], cols[e]).  Returns the number of threads used, or -1.
+ */
+int oracle_gemm_block_scaled(int64_t M, int64_t N, int64_t K, double alpha, const void* A, int64_t lda,
+                             const uint8_t* SFA, int64_t ld_sfa, const void* B, int64_t ldb,
+                             const uint8_t* SFB, int64_t ld_sfb, double beta, const void* C0,
+                             int c_type, int64_t ldc, int a_type, int b_type, int sf_type, int64_t block,
+                             int64_t count, const int64_t* rows, const int64_t* cols, double* R,
+                             double* Mag, int64_t ldr, int nthreads) {
+  if (check_args(0, 1, M, N, K, lda, ldb, a_type, b_type, c_type) != 0) return -1;
+  if (block <= 0 || (sf_type != ORACLE_SF_E8M0 && sf_type != ORACLE_SF_UE4M3)) return -1;
+  const int64_t nblk = (K + block - 1) / block;
+  if (ld_sfa < nblk || ld_sfb < nblk || (K > 0 && (!SFA || !SFB))) return -1;
+  if (beta != 0.0 && ldc < N) return -1;
+  if (!rows && ldr < N) return -1;
+  if (rows)
+    for (int64_t e = 0; e < count; ++e)
+      if (rows[e] < 0 || rows[e] >= M || cols[e] < 0 || cols[e] >= N) return -1;
+  const int64_t items = rows ? count : M;
+  if (items == 0 || (!rows && N == 0)) return 0;
+  nthreads = pick_threads(nthreads, items);
+  job_t* jobs = (job_t*)calloc((size_t)nthreads, sizeof(job_t));
+  if (!jobs) return -1;
+  for (int t = 0; t < nthreads; ++t) {
+    job_t* J = &jobs[t];
+    J->transA = 0; J->transB = 1; J->a_type = a_type; J->b_type = b_type; J->c_type = c_type;
+    J->M = M; J->N = N; J->K = K; J->lda = lda; J->ldb = ldb; J->ldc = ldc; J->ldr = ldr;
+    J->alpha = alpha; J->beta = beta; J->A = A; J->B = B; J->C0 = C0;
+    J->block = block; J->ld_sfa = ld_sfa; J->ld_sfb = ld_sfb; J->sf_type = sf_type;
+    J->SFA = SFA; J->SFB = SFB;
+    J->R = R; J->Mag = Mag; J->rows = rows; J->cols = cols;
+    if (rows) {
+      J->e0 = count * t / nthreads;
+      J->e1 = count * (t + 1) / nthreads;
+    } else {
+      J->row0 = M * t / nthreads;
+      J->row1 = M * (t + 1) / nthreads;
+    }
+  }
+  int used = run_jobs(jobs, nthreads, rows ? run_entries : run_rows);
+  free(jobs);
+  return used;
 }

@@ -622,3 +622,114 @@ def test_tolerance_rule():
     assert list(oracle.within_tolerance(out, r, m, True)) == [True, False, True, False]
     out16 = np.array([1.0 + 8.5e-3, 1.0 + 1e-2, 0.0, 1.0])
     assert list(oracle.within_tolerance(out16, r, m, False)) == [True, False, True, True]
+
+
+# ---------------------------------------------------------------------------
+# Block-scaled inputs (MXFP8, NVFP4)
+# ---------------------------------------------------------------------------
+
+def test_e2m1_codes():
+    """FP4 E2M1: sign bit 3, exponent bits 2..1 (bias 1), fraction bit 0."""
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for c in range(16):
+        v = oracle.e2m1_value(c)
+        assert v == (-1.0 if c & 8 else 1.0) * mags[c & 7]
+        assert math.copysign(1.0, v) == (-1.0 if c & 8 else 1.0)
+
+
+def test_scale_factor_codes():
+    for c in range(255):
+        assert oracle.e8m0_value(c) == math.ldexp(1.0, c - 127)
+    assert math.isnan(oracle.e8m0_value(255))
+    e4 = torch.arange(128, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    for c in range(256):
+        v = oracle.ue4m3_value(c)
+        if (c & 0x7F) == 0x7F:
+            assert math.isnan(v)
+        else:
+            assert v == e4[c & 0x7F]
+
+
+def _decode_block_scaled(p, which):
+    """Independent decode with torch / numpy: the fp64 matrix (rows x K) of values x scales."""
+    X, SF, ld, elem, rows = (p.A, p.SFA, p.lda, p.a_elem, p.M) if which == "A" else \
+        (p.B, p.SFB, p.ldb, p.b_elem, p.N)
+    raw = X.numpy()
+    if elem == "e2m1":
+        codes = np.empty((rows, raw.shape[1] * 2), dtype=np.uint8)
+        codes[:, 0::2] = raw & 0xF
+        codes[:, 1::2] = raw >> 4
+        table = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+        vals = np.where(codes & 8, -1.0, 1.0) * table[codes & 7]
+    else:
+        dt = torch.float8_e4m3fn if elem == "e4m3" else torch.float8_e5m2
+        vals = torch.from_numpy(raw.copy()).view(dt).double().numpy()
+    vals = vals[:, :p.K]
+    sf = SF.numpy()[:, :-(-p.K // p.block)].astype(np.int64)
+    if p.fmt == "mxfp8":
+        scale = np.ldexp(1.0, sf - 127)
+    else:
+        scale = torch.from_numpy((sf & 0x7F).astype(np.uint8)).view(torch.float8_e4m3fn).double().numpy()
+    return vals * np.repeat(scale, p.block, axis=1)[:, :p.K]
+
+
+def _oracle_block_scaled(p, rows=None, cols=None):
+    et = {"e4m3": oracle.IN_E4M3, "e5m2": oracle.IN_E5M2, "e2m1": oracle.IN_E2M1}
+    sft = oracle.SF_E8M0 if p.fmt == "mxfp8" else oracle.SF_UE4M3
+    c0 = None if p.beta == 0.0 else p.C0.numpy()
+    return oracle.gemm_block_scaled(p.M, p.N, p.K, p.alpha, p.A.numpy(), p.lda, p.SFA.numpy(), p.ld_sfa,
+                                    p.B.numpy(), p.ldb, p.SFB.numpy(), p.ld_sfb, p.beta, c0, p.ldc,
+                                    et[p.a_elem], et[p.b_elem], sft, p.block, rows=rows, cols=cols)
+
+
+@pytest.mark.parametrize("fmt,a,b,K", [("mxfp8", "e4m3", "e4m3", 96), ("mxfp8", "e4m3", "e5m2", 70),
+                                       ("mxfp8", "e5m2", "e5m2", 33), ("nvfp4", "e2m1", "e2m1", 64),
+                                       ("nvfp4", "e2m1", "e2m1", 37)])
+def test_block_scaled_against_numpy(fmt, a, b, K):
+    """Decoded with torch's FP8 and a table for FP4, scaled and multiplied by numpy."""
+    p = inputs.make_block_scaled_problem("bs", 9, 11, K, fmt, a_elem=a, b_elem=b, alpha=0.75, beta=-0.5, seed=K)
+    R, Mag = _oracle_block_scaled(p)
+    Ad, Bd = _decode_block_scaled(p, "A"), _decode_block_scaled(p, "B")
+    c0 = p.C0.numpy()[:, :p.N].astype(np.float64)
+    assert np.allclose(R, 0.75 * Ad @ Bd.T - 0.5 * c0, rtol=1e-12, atol=1e-12)
+    assert np.allclose(Mag, 0.75 * np.abs(Ad) @ np.abs(Bd).T + 0.5 * np.abs(c0), rtol=1e-12)
+    rows, cols = np.array([0, 8, 3]), np.array([10, 0, 5])
+    r, m = _oracle_block_scaled(p, rows, cols)
+    assert np.array_equal(r, R[rows, cols]) and np.array_equal(m, Mag[rows, cols])
+
+
+def test_block_scale_placement_closed_form():
+    """K = 64, two MXFP8 blocks: A all 1.0 with block scales 2^1 and 2^-2 in row 0,
+    B all 1.0 with scale 1: C = 32 * 2 + 32 * 0.25 = 72 exactly."""
+    A = np.full((1, 64), 0x38, dtype=np.uint8)     # E4M3 1.0
+    B = np.full((2, 64), 0x38, dtype=np.uint8)
+    SFA = np.zeros((1, 16), dtype=np.uint8)
+    SFA[0, :2] = [128, 125]
+    SFB = np.full((2, 16), 127, dtype=np.uint8)
+    SFB[1, 1] = 130                                 # column 1: second block times 8
+    R, _ = oracle.gemm_block_scaled(1, 2, 64, 1.0, A, 64, SFA, 16, B, 64, SFB, 16, 0.0, None, 2,
+                                    oracle.IN_E4M3, oracle.IN_E4M3, oracle.SF_E8M0, 32)
+    assert R.tolist() == [[72.0, 32 * 2 + 32 * 0.25 * 8]]
+
+
+def test_fp4_nibble_order():
+    """The even element of a pair is the low four bits: byte 0x21 is (0.5, 1.0)."""
+    A = np.array([[0x21]], dtype=np.uint8)
+    B = np.array([[0x42], [0x24]], dtype=np.uint8)  # (1.0, 2.0) and (2.0, 1.0)
+    SF = np.full((2, 16), 0x38, dtype=np.uint8)     # UE4M3 1.0
+    R, _ = oracle.gemm_block_scaled(1, 2, 2, 1.0, A, 2, SF[:1], 16, B, 2, SF, 16, 0.0, None, 2,
+                                    oracle.IN_E2M1, oracle.IN_E2M1, oracle.SF_UE4M3, 16)
+    assert R.tolist() == [[0.5 * 1.0 + 1.0 * 2.0, 0.5 * 2.0 + 1.0 * 1.0]]
+
+
+def test_block_scaled_generator_reconstructs():
+    """The quantised blocks stay close to the drawn values: MXFP8 E4M3 within
+    2^-3 of the block maximum, NVFP4 within half its coarsest step, 1/3 of the
+    maximum (plus the E4M3 rounding of the scale)."""
+    for fmt, tol in (("mxfp8", 2.0 ** -3), ("nvfp4", 0.36)):
+        p = inputs.make_block_scaled_problem("rq", 4, 4, 96, fmt, seed=3)
+        x = inputs._block_values(4, 96, p.block, 3, 6).reshape(4, -1)[:, :96]
+        d = _decode_block_scaled(p, "A")
+        amax = np.repeat(np.abs(x.reshape(4, -1, p.block)).max(axis=2), p.block, axis=1)
+        assert np.all(np.abs(d - x) <= tol * amax + 1e-30)
+        assert np.all(p.SFA.numpy()[:, -(-96 // p.block):] == 0xFF)     # scale padding never read

@@ -34,17 +34,24 @@ MUTATIONS = {
     "group weights not advanced": ("(const char*)B + g * strideB * eb", "(const char*)B"),
     "group rows not offset": ("(const char*)A + off * lda * ea", "(const char*)A"),
     "fp32 read at the 16-bit width": ("in_type == ORACLE_IN_F32 ? 4 : 2", "in_type == ORACLE_IN_F32 ? 2 : 2"),
+    "scale block size doubled": ("k / J->block]", "k / (2 * J->block)]"),
+    "FP4 nibble order swapped": ("(idx & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF)",
+                                 "(idx & 1) ? (uint8_t)(byte & 0xF) : (uint8_t)(byte >> 4)"),
+    "E8M0 bias off by one": ("ldexp(1.0, (int)x - 127)", "ldexp(1.0, (int)x - 128)"),
+    "E2M1 exponent bias dropped": ("ldexp(1.0 + (double)f / 2.0, e - 1)", "ldexp(1.0 + (double)f / 2.0, e)"),
+    "UE4M3 sign bit kept": ("oracle_e4m3_value((uint8_t)(x & 0x7F))", "oracle_e4m3_value(x)"),
+    "B scaled by A's factors": ("J->SFB[j * J->ld_sfb", "J->SFA[i * J->ld_sfa"),
 }
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
-def test_pins_catch_planted_mistake(name, tmp_path):
+def test_pins_catch_planted_mistake(name, repo_tmp):
     old, new = MUTATIONS[name]
     src = open(SRC).read()
     assert src.count(old) >= 1, "mutation site not found: %s" % old
-    mutated = tmp_path / "mut.c"
+    mutated = repo_tmp / "mut.c"
     mutated.write_text(src.replace(old, new))
-    lib = tmp_path / "libmut.so"
+    lib = repo_tmp / "libmut.so"
     subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", str(mutated),
                     "-o", str(lib), "-lpthread", "-lm"], check=True)
     env = dict(os.environ, ORACLE_LIB=str(lib))

@@ -17,8 +17,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 @pytest.fixture(scope="module")
-def shim(tmp_path_factory):
-    out = tmp_path_factory.mktemp("sched") / "libsched.so"
+def shim(repo_tmp_module):
+    out = repo_tmp_module / "libsched.so"
     subprocess.run(["g++", "-O1", "-std=c++17", "-fPIC", "-shared",
                     "-I" + os.path.join(ROOT, "dense_gemm_10_gb300", "csrc"),
                     os.path.join(ROOT, "tests", "sched_shim.cpp"), "-o", str(out)], check=True)
