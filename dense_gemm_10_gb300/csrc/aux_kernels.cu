@@ -1,4 +1,4 @@
-// aux_kernels.cu -- the two non-tensor-core kernels of the library:
+// aux_kernels.cu -- the non-tensor-core kernels of the library:
 //  * repack: copies an operand whose rows are not 16-byte aligned into
 //    an aligned buffer, because the tensor-memory-accelerator copy engine only
 //    reads rows whose pitch is a multiple of 16 bytes;
@@ -9,12 +9,18 @@
 //    three TF32 products): hi = TF32(x) and lo = TF32(x - hi), both rounded to
 //    nearest, laid out in segments of K chosen by a bit pattern, so that one
 //    TF32 GEMM over parts x K sums the chosen products;
+//  * dequant_block_scaled: writes a block-scaled operand (MXFP8 or NVFP4 codes
+//    with one scale code per block of k, "CUDA GEMM 矩阵乘法优化指南", 13.2) as
+//    bf16 values code x scale, K-major, for the bf16 tensor-core GEMM.  Each
+//    such value has at most 6 significant bits (E2M1 x E4M3, E4M3 x 2^e,
+//    E5M2 x 2^e), so bf16 holds it exactly inside its exponent range;
 //  * scale_c: C = ops(beta * C), the whole GEMM when K == 0 ("CUDA GEMM
 //    矩阵乘法优化指南", section 2.1, with an empty sum), with the fused epilogue
 //    operations of epi_ops.cuh.
 // Both are HBM-bound grid-stride copies over a grid sized to the SM count.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "epi_ops.cuh"
 
@@ -118,6 +124,69 @@ __global__ void split_tf32_kernel(const float* __restrict__ src, int64_t lds, in
   }
 }
 
+// Code values.  E4M3 / E5M2 through CUDA's FP8 conversions; E2M1 (sign, two
+// exponent bits with bias 1, one fraction bit) from its eight magnitudes.
+__device__ __forceinline__ float fp8_value(uint8_t c, bool e5m2) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(c), e5m2 ? __NV_E5M2 : __NV_E4M3);
+  return __half2float(__half(h));
+}
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+  const float mag = (c & 6u) == 0 ? 0.5f * static_cast<float>(c & 1u)
+                                  : static_cast<float>(2u + (c & 1u)) * __int_as_float((125 + ((c >> 1) & 3)) << 23);  // (2 + m) 2^(e - 2)
+  return (c & 8u) ? -mag : mag;
+}
+// Scale codes: E8M0 = 2^(s - 127) (255 is NaN); unsigned E4M3 = E4M3 without its sign.
+__device__ __forceinline__ float scale_value(uint8_t s, bool e8m0) {
+  if (!e8m0) return fp8_value(static_cast<uint8_t>(s & 0x7F), false);
+  if (s == 255) return __int_as_float(0x7FC00000);
+  return s == 0 ? __int_as_float(0x00400000) /* 2^-127, a subnormal */ : __int_as_float(static_cast<int>(s) << 23);
+}
+
+// One thread per 8 consecutive values of a row: dst[r * ldd + k] for k0 <= k < k0 + 8
+// (values past K written as 0).  fmt: 0 E4M3, 1 E5M2, 2 E2M1 (two a byte, even k
+// in the low four bits); lds in values.  8 divides the block, so one scale code
+// covers the 8 values.
+__global__ void dequant_kernel(const uint8_t* __restrict__ src, int64_t lds, const uint8_t* __restrict__ sf,
+                               int64_t ld_sf, int fmt, int e8m0, int block, __nv_bfloat16* __restrict__ dst,
+                               int64_t ldd, int64_t rows, int64_t K) {
+  const int64_t vecs = ldd / 8;
+  const int64_t total = rows * vecs;
+  for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < total;
+       v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = v / vecs;
+    const int64_t k0 = (v - r * vecs) * 8;
+    uint32_t packed[4] = {0u, 0u, 0u, 0u};
+    if (k0 < K) {
+      const float scale = scale_value(sf[r * ld_sf + k0 / block], e8m0 != 0);
+      float x[8];
+      if (fmt == 2) {
+        const uint8_t* row = src + r * (lds / 2);
+#pragma unroll
+        for (int t = 0; t < 8; t += 2) {
+          const uint32_t byte = (k0 + t < K) ? row[(k0 + t) / 2] : 0u;
+          x[t] = e2m1_value(byte & 0xFu);
+          x[t + 1] = e2m1_value(byte >> 4);
+        }
+      } else {
+        const uint8_t* row = src + r * lds;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) x[t] = (k0 + t < K) ? fp8_value(row[k0 + t], fmt == 1) : 0.0f;
+      }
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        if (k0 + t >= K) x[t] = 0.0f;  // (the high half of a last, half-used FP4 byte too)
+      }
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const uint16_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(x[2 * t] * scale));
+        const uint16_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(x[2 * t + 1] * scale));
+        packed[t] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+      }
+    }
+    *reinterpret_cast<uint4*>(dst + r * ldd + k0) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  }
+}
+
 static dim3 grid_3d(int64_t rows, int64_t cols, int64_t nb, int sm_count) {
   const int64_t bx = (cols + 255) / 256 < 16 ? (cols + 255) / 256 : 16;
   int64_t by = (static_cast<int64_t>(sm_count) * 8 + bx - 1) / bx;
@@ -156,6 +225,20 @@ cudaError_t split_tf32_launch(const float* src, int64_t lds, int64_t sbs, bool t
   else
     split_tf32_kernel<false><<<grid, dim3(32, 8), 0, stream>>>(src, lds, sbs, dst, ldd, dbs, rows, K, nb, parts,
                                                                pattern);
+  return cudaGetLastError();
+}
+
+cudaError_t dequant_launch(const void* src, int64_t lds, const void* sf, int64_t ld_sf, int fmt, bool e8m0,
+                           int block, void* dst, int64_t ldd, int64_t rows, int64_t K, int sm_count,
+                           cudaStream_t stream) {
+  const int64_t total = rows * (ldd / 8);
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  dequant_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      static_cast<const uint8_t*>(src), lds, static_cast<const uint8_t*>(sf), ld_sf, fmt, e8m0 ? 1 : 0, block,
+      static_cast<__nv_bfloat16*>(dst), ldd, rows, K);
   return cudaGetLastError();
 }
 

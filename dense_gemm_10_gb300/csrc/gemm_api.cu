@@ -63,6 +63,11 @@ struct Operand {
   int split_pattern = 0;
   bool split_trans = false;
   int64_t src_k = 0;
+  // block-scaled operands written as bf16 (dequant_launch) instead: source
+  // codes of format dq - 1 at ptr (ld values a row), scale codes sf (ld_sf a row)
+  int dq = 0;
+  const void* sf = nullptr;
+  int64_t ld_sf = 0;
 };
 
 struct Plan {
@@ -101,6 +106,20 @@ struct DtypeInfo {
   int32_t c_type = kCF32;
   CUtensorMapDataType map_type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   int parts = 0;  // fp32 inputs: TF32 products per product (1 or 3)
+  // block-scaled inputs (gemm_run_block_scaled): 1 MXFP8 (E8M0 scales), 2 NVFP4
+  // (unsigned E4M3 scales); values of k per scale; code formats of A and B
+  // (0 E4M3, 1 E5M2, 2 E2M1).  The GEMM itself then runs on bf16 values.
+  int sc = 0;
+  int block = 0;
+  int src_a = 0, src_b = 0;
+};
+
+// Scale codes of a block-scaled GEMM (rows of ld codes, one per block of k).
+struct BlockScale {
+  const void* sfa = nullptr;
+  int64_t ld_sfa = 0;
+  const void* sfb = nullptr;
+  int64_t ld_sfb = 0;
 };
 
 DtypeInfo dtype_info(int dtype) {
@@ -114,6 +133,20 @@ DtypeInfo dtype_info(int dtype) {
                : bf16                                              ? kCBF16
                                                                    : kCF16;
     d.map_type = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  } else if ((dtype >= GEMM_MXFP8_F32 && dtype <= GEMM_MXFP8_E5M2_F16) ||
+             (dtype >= GEMM_NVFP4_F32 && dtype <= GEMM_NVFP4_F16)) {
+    // MXFP8: 32 + (A is E5M2) + 2 * (B is E5M2) + 4 * (C: 0 fp32, 1 bf16, 2 fp16); NVFP4: 48 + C
+    static const int32_t kC[3] = {kCF32, kCBF16, kCF16};
+    const bool mx = dtype <= GEMM_MXFP8_E5M2_F16;
+    const int x = mx ? dtype - GEMM_MXFP8_F32 : dtype - GEMM_NVFP4_F32;
+    d.valid = true;
+    d.a_fmt = d.b_fmt = 1;  // the GEMM's operands: bf16
+    d.c_type = kC[mx ? x >> 2 : x];
+    d.map_type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    d.sc = mx ? 1 : 2;
+    d.block = mx ? 32 : 16;
+    d.src_a = mx ? (x & 1) : 2;
+    d.src_b = mx ? ((x >> 1) & 1) : 2;
   } else if (dtype == GEMM_F32_F32 || dtype == GEMM_TF32_F32) {
     d.valid = true;
     d.eb = 4;
@@ -302,7 +335,8 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
                         int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                         int64_t ldb, float beta, const void* C, int64_t ldc, gemm_dtype_t dtype,
                         Plan* out, int64_t batch = 1, int64_t strideA = 0, int64_t strideB = 0,
-                        int64_t strideC = 0, int64_t groups = 0, const int64_t* m_sizes = nullptr) {
+                        int64_t strideC = 0, int64_t groups = 0, const int64_t* m_sizes = nullptr,
+                        const BlockScale* bs = nullptr) {
   Plan pl;
   gemm_plan_t& P = pl.pub;
   if ((transA != GEMM_OP_N && transA != GEMM_OP_T) || (transB != GEMM_OP_N && transB != GEMM_OP_T))
@@ -310,6 +344,9 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   const DtypeInfo dt = dtype_info(dtype);
   if (!dt.valid) return GEMM_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+  // block-scaled types only through gemm_run_block_scaled, which passes the scales
+  if ((dt.sc != 0) != (bs != nullptr)) return GEMM_ERR_INVALID_ARG;
+  if (dt.sc != 0 && (batch != 1 || groups != 0)) return GEMM_ERR_UNSUPPORTED;
   pl.eb = dt.eb;
   pl.in_dtype = static_cast<int32_t>(dt.map_type);
   pl.c_type = dt.c_type;
@@ -347,6 +384,11 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   if (A == nullptr || B == nullptr) return GEMM_ERR_INVALID_ARG;
   if (lda < (transA == GEMM_OP_T ? M : K) || ldb < (transB == GEMM_OP_T ? K : N))
     return GEMM_ERR_INVALID_ARG;
+  if (dt.sc != 0) {  // A M x K and B N x K codes, a scale code per block of k
+    const int64_t nblk = cdiv(K, dt.block);
+    if (!bs->sfa || !bs->sfb || bs->ld_sfa < nblk || bs->ld_sfb < nblk) return GEMM_ERR_INVALID_ARG;
+    if (dt.sc == 2 && (lda % 2 != 0 || ldb % 2 != 0)) return GEMM_ERR_INVALID_ARG;  // rows start on a byte
+  }
   // 8-bit operands: K-major only (A stored M x K, B stored N x K).
   if (dt.eb == 1 && (transA != GEMM_OP_N || transB != GEMM_OP_T)) return GEMM_ERR_UNSUPPORTED;
 
@@ -356,6 +398,14 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   a.rows = a.kmajor ? M : K; a.cols = a.kmajor ? K : M;
   b.ptr = B; b.ld = ldb; b.kmajor = transB == GEMM_OP_T;
   b.rows = b.kmajor ? N : K; b.cols = b.kmajor ? K : N;
+  if (dt.sc != 0) {  // both are written as bf16 into the workspace first
+    a.dq = dt.src_a + 1;
+    a.sf = bs->sfa;
+    a.ld_sf = bs->ld_sfa;
+    b.dq = dt.src_b + 1;
+    b.sf = bs->sfb;
+    b.ld_sf = bs->ld_sfb;
+  }
   a.nb = (batch > 1 && strideA > 0) ? batch : 1;  // a stride of 0 shares one matrix
   b.nb = (batch > 1 && strideB > 0) ? batch : 1;
   if (groups > 1 && strideB > 0) b.nb = groups;  // one weight matrix per group
@@ -485,7 +535,7 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   // Workspace: repacked operands, then partial tiles of split tiles.
   size_t ws = 0;
   for (Operand* op : {&pl.p, &pl.q}) {
-    if (op->split_parts > 0 || !tma_aligned(op->ptr, op->ld, dt.eb, op->bstride, op->nb)) {
+    if (op->split_parts > 0 || op->dq > 0 || !tma_aligned(op->ptr, op->ld, dt.eb, op->bstride, op->nb)) {
       op->repack = true;  // rows padded to whole 16-byte pieces, batches packed
       op->packed_ld = static_cast<int64_t>(round_up(static_cast<size_t>(op->cols), 16 / dt.eb));
       op->ws_offset = ws;
@@ -792,7 +842,10 @@ static cudaError_t prepare_operands(const Plan& pl, uint8_t* ws, int sm_count, c
     if (!op.repack) continue;
     void* dst = ws + op.ws_offset;
     cudaError_t e;
-    if (op.split_parts > 0)
+    if (op.dq > 0)
+      e = dequant_launch(op.ptr, op.ld, op.sf, op.ld_sf, op.dq - 1, op.dq - 1 != 2 /* MXFP8: E8M0 */,
+                         op.dq - 1 == 2 ? 16 : 32, dst, op.packed_ld, op.rows, op.cols, sm_count, st);
+    else if (op.split_parts > 0)
       e = split_tf32_launch(static_cast<const float*>(op.ptr), op.ld, op.bstride, op.split_trans,
                             static_cast<float*>(dst), op.packed_ld, op.rows * op.packed_ld, op.rows, op.src_k,
                             op.nb, op.split_parts, op.split_pattern, sm_count, st);
@@ -811,11 +864,12 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
                               const void* B, int64_t ldb, float beta, void* C, int64_t ldc,
                               gemm_dtype_t dtype, EpiOps ops, void* stream, int64_t batch = 1,
                               int64_t strideA = 0, int64_t strideB = 0, int64_t strideC = 0,
-                              int64_t groups = 0, const int64_t* m_sizes = nullptr) {
+                              int64_t groups = 0, const int64_t* m_sizes = nullptr,
+                              const BlockScale* bs = nullptr) {
   if (!h) return GEMM_ERR_INVALID_ARG;
   Plan pl;
   gemm_status_t s = make_plan(h->opt, h->slots, transA, transB, M, N, K, A, lda, B, ldb, beta,
-                              C, ldc, dtype, &pl, batch, strideA, strideB, strideC, groups, m_sizes);
+                              C, ldc, dtype, &pl, batch, strideA, strideB, strideC, groups, m_sizes, bs);
   if (s == GEMM_OK && groups > 0) M = pl.I;  // the stacked rows
   if (s != GEMM_OK) return s;
   const gemm_plan_t& P = pl.pub;
@@ -964,6 +1018,44 @@ gemm_status_t gemm_run_grouped(gemm_handle_t h, gemm_op_t transB, int64_t groups
   if (groups == 0) return GEMM_OK;
   return run_gemm(h, GEMM_OP_N, transB, 0, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtype, ops, stream, 1, 0,
                   strideB, 0, groups, m_sizes);
+}
+
+gemm_status_t gemm_run_block_scaled(gemm_handle_t h, int64_t M, int64_t N, int64_t K, float alpha, const void* A,
+                                    int64_t lda, const void* SFA, int64_t ld_sfa, const void* B, int64_t ldb,
+                                    const void* SFB, int64_t ld_sfb, float beta, void* C, int64_t ldc,
+                                    gemm_dtype_t dtype, const gemm_epilogue_t* epi, void* stream) {
+  EpiOps ops;
+  gemm_status_t s = epi_ops(epi, &ops);
+  if (s != GEMM_OK) return s;
+  if (dtype_info(dtype).sc == 0) return GEMM_ERR_INVALID_ARG;
+  BlockScale bs;
+  bs.sfa = SFA;
+  bs.ld_sfa = ld_sfa;
+  bs.sfb = SFB;
+  bs.ld_sfb = ld_sfb;
+  return run_gemm(h, GEMM_OP_N, GEMM_OP_T, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtype, ops, stream, 1, 0,
+                  0, 0, 0, nullptr, &bs);
+}
+
+gemm_status_t gemm_plan_block_scaled(gemm_handle_t h, int sm_count, int64_t M, int64_t N, int64_t K, const void* A,
+                                     int64_t lda, const void* SFA, int64_t ld_sfa, const void* B, int64_t ldb,
+                                     const void* SFB, int64_t ld_sfb, float beta, const void* C, int64_t ldc,
+                                     gemm_dtype_t dtype, gemm_plan_t* plan) {
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  if (!h && sm_count <= 0) return GEMM_ERR_INVALID_ARG;
+  if (dtype_info(dtype).sc == 0) return GEMM_ERR_INVALID_ARG;
+  Options o = h ? h->opt : Options();
+  const SlotTable slots = h ? h->slots : SlotTable::even(sm_count);
+  BlockScale bs;
+  bs.sfa = SFA;
+  bs.ld_sfa = ld_sfa;
+  bs.sfb = SFB;
+  bs.ld_sfb = ld_sfb;
+  Plan pl;
+  gemm_status_t s = make_plan(o, slots, GEMM_OP_N, GEMM_OP_T, M, N, K, A, lda, B, ldb, beta, C, ldc, dtype, &pl, 1,
+                              0, 0, 0, 0, nullptr, &bs);
+  if (s == GEMM_OK) *plan = pl.pub;
+  return s;
 }
 
 gemm_status_t gemm_plan_grouped(gemm_handle_t h, int sm_count, gemm_op_t transB, int64_t groups,

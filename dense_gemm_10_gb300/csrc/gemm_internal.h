@@ -111,6 +111,15 @@ cudaError_t split_tf32_launch(const float* src, int64_t lds, int64_t sbs, bool t
                               int64_t ldd, int64_t dbs, int64_t rows, int64_t K, int64_t nb, int parts,
                               int pattern, int sm_count, cudaStream_t stream);
 
+// Block-scaled operand -> bf16, K-major: dst[r * ldd + k] = code(r, k) *
+// scale(r, k / block) for k < K, 0 for K <= k < ldd (ldd a multiple of 8, dst
+// 16-byte aligned).  fmt: 0 E4M3, 1 E5M2, 2 E2M1 packed two a byte (even k
+// low); lds counts values; scale codes E8M0 (e8m0) or unsigned E4M3, rows of
+// ld_sf codes.  block: 16 or 32.
+cudaError_t dequant_launch(const void* src, int64_t lds, const void* sf, int64_t ld_sf, int fmt, bool e8m0,
+                           int block, void* dst, int64_t ldd, int64_t rows, int64_t K, int sm_count,
+                           cudaStream_t stream);
+
 // The whole GEMM when K == 0: C = ops(beta * C) over `batch` M x N matrices
 // with leading dimension ldc, sbc elements apart (beta * C = 0 when beta == 0;
 // C is then not read).

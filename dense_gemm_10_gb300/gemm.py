@@ -14,6 +14,13 @@ LIB_PATH = os.path.join(HERE, "libgemm_gb300.so")
 OP_N, OP_T = 0, 1
 BF16_F32, BF16_BF16, F16_F32, F16_F16, BF16_E4M3, F16_E4M3 = 0, 1, 2, 3, 4, 5
 F32_F32, TF32_F32 = 6, 7   # fp32 inputs: three TF32 products per product, or one
+NVFP4_F32, NVFP4_BF16, NVFP4_F16 = 48, 49, 50   # block-scaled E2M1 (gemm_run_block_scaled)
+
+
+def mxfp8_dtype(a="e4m3", b=None, c="f32"):
+    """gemm_dtype_t of a block-scaled MXFP8 pair (E8M0 scales per 32 values of k)."""
+    b = a if b is None else b
+    return 32 + (a == "e5m2") + 2 * (b == "e5m2") + 4 * {"f32": 0, "bf16": 1, "f16": 2}[c]
 _FP8_FORMATS = ("e4m3", "e5m2")
 _C_TYPES = ("f32", "bf16", "f16", "e4m3")
 ACT_NONE, ACT_RELU, ACT_GELU = 0, 1, 2
@@ -82,6 +89,10 @@ SIGNATURES = {
                                 _i32, ctypes.POINTER(Epilogue), _vp]),
     "gemm_plan_grouped": (_i32, [_vp, ctypes.c_int, _i32, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _f32, _vp,
                                  _i64, _i32, ctypes.POINTER(Plan)]),
+    "gemm_run_block_scaled": (_i32, [_vp, _i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _f32,
+                                     _vp, _i64, _i32, ctypes.POINTER(Epilogue), _vp]),
+    "gemm_plan_block_scaled": (_i32, [_vp, ctypes.c_int, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
+                                      _f32, _vp, _i64, _i32, ctypes.POINTER(Plan)]),
 }
 
 _lib = None
@@ -185,6 +196,13 @@ class Handle:
         return lib().gemm_run_grouped(self.ptr, transB, len(m_sizes), ctypes.cast(sizes, _vp), N, K, alpha, A, lda, B,
                                       ldb, strideB, beta, C, ldc, dtype, ctypes.byref(epi), stream)
 
+    def run_block_scaled_raw(self, M, N, K, alpha, A, lda, SFA, ld_sfa, B, ldb, SFB, ld_sfb, beta, C, ldc, dtype,
+                             stream, bias=0, act=ACT_NONE, out_scale=1.0):
+        """gemm_run_block_scaled on raw device pointers; returns the status."""
+        epi = Epilogue(bias or None, int(act), float(out_scale))
+        return lib().gemm_run_block_scaled(self.ptr, M, N, K, alpha, A, lda, SFA, ld_sfa, B, ldb, SFB, ld_sfb, beta, C,
+                                           ldc, dtype, ctypes.byref(epi), stream)
+
     def run_ex_raw(self, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dtype, stream,
                    bias=0, act=ACT_NONE, out_scale=1.0):
         """gemm_run_ex on raw device pointers (bias: device pointer or 0); returns the status code."""
@@ -220,6 +238,25 @@ def plan_batched(M, N, K, batch, transA=0, transB=0, dtype=BF16_F32, lda=None, l
     st = lib().gemm_plan_strided_batched(h, sm_count, transA, transB, M, N, K, A, lda, strideA, B, ldb, strideB,
                                          beta, C, ldc, strideC, batch, dtype, ctypes.byref(p))
     _check(st, "gemm_plan_strided_batched")
+    return p
+
+
+def plan_block_scaled(M, N, K, dtype, lda=None, ldb=None, ld_sfa=None, ld_sfb=None, ldc=None, sm_count=152,
+                      A=0x1000, B=0x1000, SFA=0x1000, SFB=0x1000, C=0x1000, beta=0.0, handle=None):
+    """Host-only planner query for a block-scaled call (default pitches: K values,
+    scale rows padded to 16 bytes)."""
+    block = 16 if dtype >= NVFP4_F32 else 32
+    nblk = -(-K // block)
+    lda = K if lda is None else lda
+    ldb = K if ldb is None else ldb
+    ld_sfa = -(-max(nblk, 1) // 16) * 16 if ld_sfa is None else ld_sfa
+    ld_sfb = ld_sfa if ld_sfb is None else ld_sfb
+    ldc = N if ldc is None else ldc
+    p = Plan()
+    h = handle.ptr if handle is not None else None
+    st = lib().gemm_plan_block_scaled(h, sm_count, M, N, K, A, lda, SFA, ld_sfa, B, ldb, SFB, ld_sfb, beta, C, ldc,
+                                      dtype, ctypes.byref(p))
+    _check(st, "gemm_plan_block_scaled")
     return p
 
 

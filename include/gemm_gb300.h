@@ -102,7 +102,14 @@ typedef enum {
   GEMM_E4M3_E4M3OUT = 28,      /* ... and with E4M3 C (quantised output) */
   GEMM_E5M2_E4M3_E4M3OUT = 29,
   GEMM_E4M3_E5M2_E4M3OUT = 30,
-  GEMM_E5M2_E4M3OUT = 31
+  GEMM_E5M2_E4M3OUT = 31,
+  /* Block-scaled inputs, gemm_run_block_scaled only (see there):
+     MXFP8: 32 + (A is E5M2) + 2 * (B is E5M2) + 4 * (0 fp32, 1 bf16, 2 fp16 C) */
+  GEMM_MXFP8_F32 = 32,         /* A, B E4M3 with E8M0 scales per 32; C fp32 */
+  GEMM_MXFP8_E5M2_F16 = 43,    /* the last MXFP8 code: A, B E5M2; C fp16 */
+  GEMM_NVFP4_F32 = 48,         /* A, B E2M1 (packed) with unsigned E4M3 scales per 16; C fp32 */
+  GEMM_NVFP4_BF16 = 49,
+  GEMM_NVFP4_F16 = 50
 } gemm_dtype_t;
 
 typedef enum {
@@ -333,6 +340,43 @@ gemm_status_t gemm_plan_grouped(gemm_handle_t h, int sm_count, gemm_op_t transB,
                                 const int64_t* m_sizes, int64_t N, int64_t K, const void* A, int64_t lda,
                                 const void* B, int64_t ldb, int64_t strideB, float beta, const void* C,
                                 int64_t ldc, gemm_dtype_t dtype, gemm_plan_t* plan);
+
+/*
+ * gemm_run_block_scaled: C = alpha * A' * B'^T + beta * C for block-scaled
+ * operands, as the Blackwell section of "CUDA GEMM 矩阵乘法优化指南" (13.2)
+ * describes them: narrow codes sharing one scale factor per block of k:
+ *   a'(i, k) = code(A, i, k) * scale(SFA[i * ld_sfa + k / block])
+ *   b'(j, k) = code(B, j, k) * scale(SFB[j * ld_sfb + k / block])
+ * MXFP8 (GEMM_MXFP8_*): E4M3 / E5M2 codes, block 32, E8M0 scales (2^(s - 127)).
+ * NVFP4 (GEMM_NVFP4_*): E2M1 codes (sign, 2-bit exponent with bias 1, 1-bit
+ *   fraction), two a byte with the even k in the low four bits; block 16;
+ *   unsigned E4M3 scales (sign bit ignored).  A per-tensor scale folds into alpha.
+ * A is stored M x K and B N x K, K contiguous; lda / ldb count values (even
+ * for NVFP4).  SFA is M rows and SFB N rows of at least ceil(K / block) scale
+ * codes, row pitches ld_sfa / ld_sfb in bytes.  Codes past K in a row and scale
+ * codes past ceil(K / block) are never read.  C is M x N (ldc) in fp32, bf16
+ * or fp16.  The fused epilogue `epi` (may be NULL) applies as in gemm_run_ex.
+ * All pointers are device pointers owned by the caller.
+ * How it runs: one launch per operand writes a'(., k) as bf16 into the handle's
+ * workspace (exact: a code times a scale has at most 6 significant bits, so
+ * every value inside bf16's exponent range is held exactly; values below
+ * 2^-133 flush), then the bf16 tensor-core GEMM computes the product, so the
+ * result is the block-scaled product with fp32 accumulation at bf16 speed.
+ * (The tensor core's own block-scaled kinds are not used.)
+ * Returns GEMM_ERR_INVALID_ARG for a non-block-scaled dtype, null scales,
+ * scale pitches below ceil(K / block), odd NVFP4 pitches, or the argument
+ * errors of gemm_run.
+ */
+gemm_status_t gemm_run_block_scaled(gemm_handle_t h, int64_t M, int64_t N, int64_t K, float alpha, const void* A,
+                                    int64_t lda, const void* SFA, int64_t ld_sfa, const void* B, int64_t ldb,
+                                    const void* SFB, int64_t ld_sfb, float beta, void* C, int64_t ldc,
+                                    gemm_dtype_t dtype, const gemm_epilogue_t* epi, void* stream);
+
+/* gemm_plan for a block-scaled call (arguments as gemm_run_block_scaled). */
+gemm_status_t gemm_plan_block_scaled(gemm_handle_t h, int sm_count, int64_t M, int64_t N, int64_t K, const void* A,
+                                     int64_t lda, const void* SFA, int64_t ld_sfa, const void* B, int64_t ldb,
+                                     const void* SFB, int64_t ld_sfb, float beta, const void* C, int64_t ldc,
+                                     gemm_dtype_t dtype, gemm_plan_t* plan);
 
 /* gemm_plan for a strided batched call (arguments as gemm_run_strided_batched). */
 gemm_status_t gemm_plan_strided_batched(gemm_handle_t h, int sm_count, gemm_op_t transA, gemm_op_t transB,

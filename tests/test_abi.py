@@ -159,6 +159,27 @@ def test_plan_fp8():
             for a in ("e4m3", "e5m2")] == list(range(16, 32))
 
 
+def test_plan_block_scaled():
+    """Block-scaled operands are written as bf16 first (two more launches), then
+    the bf16 GEMM plans as usual; block-scaled types need their entry point."""
+    p = G.plan_block_scaled(4096, 4096, 4096, G.mxfp8_dtype())
+    assert p.repack_a == 1 and p.repack_b == 1 and p.launches == 3 and p.bk == 64 and p.bn == 256
+    assert p.workspace_bytes >= 2 * 4096 * 4096 * 2
+    q = G.plan_block_scaled(64, 32000, 4096, G.NVFP4_BF16)
+    assert q.swap_ab == 1 and q.launches == 3
+    r = G.plan_block_scaled(300, 264, 37, G.NVFP4_F32, lda=38, ldb=38)
+    assert r.workspace_bytes >= (300 + 264) * 40 * 2          # 37 values padded to 40 bf16
+    for kw in (dict(ld_sfa=1), dict(lda=39)):                  # scale rows too short; odd FP4 pitch
+        with pytest.raises(G.GemmError) as e:
+            G.plan_block_scaled(64, 64, 64, G.NVFP4_F32, **kw)
+        assert e.value.status == G.ERR_INVALID_ARG
+    with pytest.raises(G.GemmError) as e:
+        G.plan(64, 64, 64, 0, 1, G.NVFP4_F32)
+    assert e.value.status == G.ERR_INVALID_ARG
+    assert [G.mxfp8_dtype(a, b, c) for c in ("f32", "bf16", "f16") for b in ("e4m3", "e5m2")
+            for a in ("e4m3", "e5m2")] == list(range(32, 44))
+
+
 def test_plan_fp32():
     """fp32 inputs: 32-element (128-byte) k-slices of the TF32 kind, K-major only.
     The fp32 GEMM writes both operands as TF32 parts (3K values a row, padded to
