@@ -142,48 +142,79 @@ __device__ __forceinline__ float scale_value(uint8_t s, bool e8m0) {
   return s == 0 ? __int_as_float(0x00400000) /* 2^-127, a subnormal */ : __int_as_float(static_cast<int>(s) << 23);
 }
 
-// One thread per 8 consecutive values of a row: dst[r * ldd + k] for k0 <= k < k0 + 8
-// (values past K written as 0).  fmt: 0 E4M3, 1 E5M2, 2 E2M1 (two a byte, even k
-// in the low four bits); lds in values.  8 divides the block, so one scale code
-// covers the 8 values.
-__global__ void dequant_kernel(const uint8_t* __restrict__ src, int64_t lds, const uint8_t* __restrict__ sf,
-                               int64_t ld_sf, int fmt, int e8m0, int block, __nv_bfloat16* __restrict__ dst,
-                               int64_t ldd, int64_t rows, int64_t K) {
-  const int64_t vecs = ldd / 8;
-  const int64_t total = rows * vecs;
-  for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < total;
-       v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t r = v / vecs;
-    const int64_t k0 = (v - r * vecs) * 8;
-    uint32_t packed[4] = {0u, 0u, 0u, 0u};
-    if (k0 < K) {
-      const float scale = scale_value(sf[r * ld_sf + k0 / block], e8m0 != 0);
-      float x[8];
-      if (fmt == 2) {
-        const uint8_t* row = src + r * (lds / 2);
-#pragma unroll
-        for (int t = 0; t < 8; t += 2) {
-          const uint32_t byte = (k0 + t < K) ? row[(k0 + t) / 2] : 0u;
-          x[t] = e2m1_value(byte & 0xFu);
-          x[t + 1] = e2m1_value(byte >> 4);
-        }
-      } else {
-        const uint8_t* row = src + r * lds;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) x[t] = (k0 + t < K) ? fp8_value(row[k0 + t], fmt == 1) : 0.0f;
-      }
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        if (k0 + t >= K) x[t] = 0.0f;  // (the high half of a last, half-used FP4 byte too)
-      }
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const uint16_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(x[2 * t] * scale));
-        const uint16_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(x[2 * t + 1] * scale));
-        packed[t] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-      }
+// One thread per 16 consecutive values of a row: dst[r * ldd + k] for k0 <= k <
+// k0 + 16 (values past K written as 0; ldd a multiple of 16).  fmt: 0 E4M3, 1
+// E5M2, 2 E2M1 (two a byte, even k in the low four bits); lds in values.  16
+// divides the block, so one scale code covers the 16 values.  `vec`: rows
+// start 16-byte (FP8) / 8-byte (FP4) aligned, so whole pieces load as one
+// vector; the tail of a row (k0 + 16 > K) is read byte by byte.
+// Raw code words of one 16-value piece: FP8 w[0..3] (byte t of the piece at bits
+// 8 (t % 4) of w[t / 4]), FP4 w[0..1] (value t at bits 4 (t % 8) of w[t / 8]).
+__device__ __forceinline__ void load_piece(const uint8_t* __restrict__ src, int64_t lds, int fmt, int vec, int64_t r,
+                                           int64_t k0, int64_t K, uint32_t (&w)[4]) {
+  w[0] = w[1] = w[2] = w[3] = 0u;
+  if (k0 >= K) return;
+  const bool whole = vec != 0 && k0 + 16 <= K;
+  if (fmt == 2) {
+    const uint8_t* row = src + r * (lds / 2);
+    if (whole) {
+      const uint2 q = *reinterpret_cast<const uint2*>(row + k0 / 2);
+      w[0] = q.x;
+      w[1] = q.y;
+    } else {
+      for (int t = 0; t < 16 && k0 + t < K; t += 2)
+        w[t >> 3] |= static_cast<uint32_t>(row[(k0 + t) / 2]) << (4 * (t & 7));
     }
-    *reinterpret_cast<uint4*>(dst + r * ldd + k0) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  } else {
+    const uint8_t* row = src + r * lds;
+    if (whole) {
+      const uint4 q = *reinterpret_cast<const uint4*>(row + k0);
+      w[0] = q.x;
+      w[1] = q.y;
+      w[2] = q.z;
+      w[3] = q.w;
+    } else {
+      for (int t = 0; t < 16 && k0 + t < K; ++t) w[t >> 2] |= static_cast<uint32_t>(row[k0 + t]) << (8 * (t & 3));
+    }
+  }
+}
+
+// Thread x of the grid's x dimension takes the 16-value piece k0 = 16 x of rows
+// blockIdx.y, blockIdx.y + gridDim.y, ... and writes dst[r * ldd + k] for its
+// 16 values (values past K written as 0; ldd a multiple of 16).  fmt: 0 E4M3,
+// 1 E5M2, 2 E2M1 (two a byte, even k in the low four bits); lds in values.  16
+// divides the block, so one scale code covers a piece.  `vec`: rows start
+// 16-byte (FP8) / 8-byte (FP4) aligned, so whole pieces load as one vector; the
+// tail of a row (k0 + 16 > K) is read byte by byte.
+__global__ void dequant_kernel(const uint8_t* __restrict__ src, int64_t lds, const uint8_t* __restrict__ sf,
+                               int64_t ld_sf, int fmt, int e8m0, int block, int vec, __nv_bfloat16* __restrict__ dst,
+                               int64_t ldd, int64_t rows, int64_t K) {
+  const int64_t k0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 16;
+  if (k0 >= ldd) return;
+  for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+    uint32_t w[4];
+    load_piece(src, lds, fmt, vec, r, k0, K, w);
+    const float scale = k0 < K ? scale_value(sf[r * ld_sf + k0 / block], e8m0 != 0) : 0.0f;
+    uint32_t packed[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      float x0, x1;
+      if (fmt == 2) {
+        x0 = e2m1_value((w[(2 * t) >> 3] >> (4 * ((2 * t) & 7))) & 0xFu);
+        x1 = e2m1_value((w[(2 * t + 1) >> 3] >> (4 * ((2 * t + 1) & 7))) & 0xFu);
+      } else {
+        x0 = fp8_value(static_cast<uint8_t>(w[(2 * t) >> 2] >> (8 * ((2 * t) & 3))), fmt == 1);
+        x1 = fp8_value(static_cast<uint8_t>(w[(2 * t + 1) >> 2] >> (8 * ((2 * t + 1) & 3))), fmt == 1);
+      }
+      // values past K (the high half of a last, half-used FP4 byte too) are 0
+      if (k0 + 2 * t >= K) x0 = 0.0f;
+      if (k0 + 2 * t + 1 >= K) x1 = 0.0f;
+      const __nv_bfloat162 pr = __floats2bfloat162_rn(x0 * scale, x1 * scale);
+      packed[t] = *reinterpret_cast<const uint32_t*>(&pr);
+    }
+    uint4* out = reinterpret_cast<uint4*>(dst + r * ldd + k0);
+    out[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    out[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
   }
 }
 
@@ -231,13 +262,18 @@ cudaError_t split_tf32_launch(const float* src, int64_t lds, int64_t sbs, bool t
 cudaError_t dequant_launch(const void* src, int64_t lds, const void* sf, int64_t ld_sf, int fmt, bool e8m0,
                            int block, void* dst, int64_t ldd, int64_t rows, int64_t K, int sm_count,
                            cudaStream_t stream) {
-  const int64_t total = rows * (ldd / 8);
-  int64_t blocks = (total + 255) / 256;
-  const int64_t cap = static_cast<int64_t>(sm_count) * 8;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  dequant_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      static_cast<const uint8_t*>(src), lds, static_cast<const uint8_t*>(sf), ld_sf, fmt, e8m0 ? 1 : 0, block,
+  if (ldd % 16 != 0) return cudaErrorInvalidValue;
+  const int64_t pieces = ldd / 16;  // per row
+  const unsigned gx = static_cast<unsigned>((pieces + 127) / 128);
+  // rows per pass: about 16 blocks of 128 threads per SM in all
+  int64_t gy = static_cast<int64_t>(sm_count) * 16 / gx;
+  if (gy > rows) gy = rows;
+  if (gy > 65535) gy = 65535;
+  if (gy < 1) gy = 1;
+  const uintptr_t base = reinterpret_cast<uintptr_t>(src);
+  const int vec = fmt == 2 ? (base % 8 == 0 && (lds / 2) % 8 == 0) : (base % 16 == 0 && lds % 16 == 0);
+  dequant_kernel<<<dim3(gx, static_cast<unsigned>(gy), 1), 128, 0, stream>>>(
+      static_cast<const uint8_t*>(src), lds, static_cast<const uint8_t*>(sf), ld_sf, fmt, e8m0 ? 1 : 0, block, vec,
       static_cast<__nv_bfloat16*>(dst), ldd, rows, K);
   return cudaGetLastError();
 }

@@ -537,7 +537,8 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   for (Operand* op : {&pl.p, &pl.q}) {
     if (op->split_parts > 0 || op->dq > 0 || !tma_aligned(op->ptr, op->ld, dt.eb, op->bstride, op->nb)) {
       op->repack = true;  // rows padded to whole 16-byte pieces, batches packed
-      op->packed_ld = static_cast<int64_t>(round_up(static_cast<size_t>(op->cols), 16 / dt.eb));
+      // (dequantised rows: whole 16-value pieces, one per thread of dequant_launch)
+      op->packed_ld = static_cast<int64_t>(round_up(static_cast<size_t>(op->cols), op->dq > 0 ? 16 : 16 / dt.eb));
       op->ws_offset = ws;
       ws = round_up(ws + static_cast<size_t>(op->rows) * op->packed_ld * dt.eb * op->nb, 256);
     }

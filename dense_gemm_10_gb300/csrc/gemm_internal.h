@@ -112,7 +112,7 @@ cudaError_t split_tf32_launch(const float* src, int64_t lds, int64_t sbs, bool t
                               int pattern, int sm_count, cudaStream_t stream);
 
 // Block-scaled operand -> bf16, K-major: dst[r * ldd + k] = code(r, k) *
-// scale(r, k / block) for k < K, 0 for K <= k < ldd (ldd a multiple of 8, dst
+// scale(r, k / block) for k < K, 0 for K <= k < ldd (ldd a multiple of 16, dst
 // 16-byte aligned).  fmt: 0 E4M3, 1 E5M2, 2 E2M1 packed two a byte (even k
 // low); lds counts values; scale codes E8M0 (e8m0) or unsigned E4M3, rows of
 // ld_sf codes.  block: 16 or 32.
