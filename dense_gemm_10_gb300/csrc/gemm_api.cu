@@ -43,6 +43,7 @@ struct Options {
   int stages = 0;    // 0: the configuration's maximum ring depth
   int tma_store = 0; // GEMM_OPT_EPILOGUE: 0 auto, 1 bulk stores when possible, 2 direct stores
   int kdepth = 0;    // GEMM_OPT_KDEPTH: 0 auto, else 64-wide k-slices per ring stage
+  int pdl = 1;       // GEMM_OPT_PDL: programmatic dependent launch of the main kernel
 };
 
 // One stored operand, as the tensor-memory-accelerator copy engine will see it.
@@ -794,6 +795,10 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
       if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
       h->opt.kdepth = static_cast<int>(value);
       return GEMM_OK;
+    case GEMM_OPT_PDL:
+      if (value < 0 || value > 1) return GEMM_ERR_INVALID_ARG;
+      h->opt.pdl = static_cast<int>(value);
+      return GEMM_OK;
   }
   return GEMM_ERR_INVALID_ARG;
 }
@@ -968,6 +973,7 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
     a.group_row = d_row;
   }
   a.drop_load = h->opt.drop_load;
+  a.pdl = pl.sched.groups > 0 ? 0 : h->opt.pdl;  // (grouped: the group tables are copied just before)
   ops.bias_on_i = P.swap_ab;  // a swapped problem computes C^T: C's columns are the kernel's rows
   a.ops = ops;
   e = tc_launch(pl.cfg, map_p, map_q, map_c, a, P.grid, st);
@@ -1267,6 +1273,7 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   a.status = d->status;
   a.wait_limit_ns = static_cast<uint64_t>(o.wait_limit_ns);
   a.drop_load = 0;
+  a.pdl = 0;  // (the no-allocation entry point clears its arrays first, with ordinary stream order)
   a.ops = EpiOps();  // no fused operations (the memset above zeroed out_scale)
   e = tc_launch(pl.cfg, map_p, map_q, map_c, a, P.grid, st);
   return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;

@@ -62,6 +62,7 @@ struct TcArgs {
   int32_t* status;       // device status word
   uint64_t wait_limit_ns;
   int32_t drop_load;     // tests only: CTA 0 skips its drop_load-th k-block load (1-based)
+  int32_t pdl;           // launch as a programmatic dependent of the stream's previous kernel
   EpiOps ops;            // fused elementwise operations of the epilogue
   int64_t c_sb;          // batch stride of C in elements (strided batches; tile batch in Unit::tb)
   int32_t p_bcast;       // P is one matrix shared by every batch (its tensor map has one batch)

@@ -805,6 +805,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the global stores and "memory"-clobbering asm of the loops, instead of
   // reloading them from the parameter space after each one.
   const TcArgs a = args;
+  // The next kernel of the stream may be scheduled now: its CTAs take SMs as
+  // this grid's leave and run their set-up while this grid finishes.
+  grid_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   // 128-byte swizzle atoms need 1024-byte aligned tiles.
   const uint32_t raw = smem_u32(smem_raw);
@@ -850,6 +853,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (kCl > 1) cluster_sync();  // every CTA's barriers exist before any remote arrive
   tc_fence_after_sync();
   const uint32_t tmem_base = ctrl->tmem_base;
+  // Set-up done (barriers, tensor memory, tensor maps); no global memory has
+  // been touched.  From here on operands, C, partials and counters may be those
+  // of the previous kernel of the stream: wait until it has finished.
+  grid_dependency_wait();
 
   if (warp == 0) {
     // k-slices per stage are a template argument of the issuing roles, so that

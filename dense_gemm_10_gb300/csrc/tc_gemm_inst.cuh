@@ -35,22 +35,27 @@ cudaError_t TC_NAME(tc_launch_bn, TC_BN, _cg, TC_CG, _mc, TC_MC, _eb, TC_EB)(
     int grid, cudaStream_t stream) {
   using Cfg = TcConfig<TC_BN, TC_CG, TC_MC>;
   const size_t smem = args.tma_store ? Cfg::kSmemBytes : Cfg::kSmemNoStaging;
-  if (TC_CG * TC_MC == 1) {
-    TC_KERNEL<<<grid, kThreads, smem, stream>>>(map_p, map_q, map_c, args);
-    return cudaGetLastError();
-  }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = TC_CG * TC_MC;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (TC_CG * TC_MC > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = TC_CG * TC_MC;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (args.pdl) {  // may start while the previous kernel of the stream finishes (griddepcontrol)
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, TC_KERNEL, map_p, map_q, map_c, args);
 }
 

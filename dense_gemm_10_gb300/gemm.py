@@ -41,6 +41,7 @@ PATH_NOOP, PATH_SCALE_C, PATH_TC_1CTA, PATH_TC_2CTA, PATH_TC_2CTA_MULTICAST = 0,
  OPT_STREAM_K, OPT_STAGES) = range(9)
 OPT_EPILOGUE = 10
 OPT_KDEPTH = 11
+OPT_PDL = 12
 BULK_NONE, BULK_ROWS, BULK_TRANSPOSED = 0, 1, 2   # gemm_plan_t.bulk_store
 SCHED_TILES, SCHED_STREAM_K = 0, 1
 

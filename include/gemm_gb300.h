@@ -402,9 +402,13 @@ typedef enum {
                                   tensor stores when rows start 16-byte aligned, N is a whole
                                   number of 16-byte pieces and beta == 0;
                                   2: always direct stores from registers */
-  GEMM_OPT_KDEPTH = 11         /* 0 auto, else 1 or 2 64-wide k-slices per ring stage (2 halves
+  GEMM_OPT_KDEPTH = 11,        /* 0 auto, else 1 or 2 128-byte k-slices per ring stage (2 halves
                                   the barrier round trips per byte; falls back to 1 where the
                                   ring would hold fewer than two stages) */
+  GEMM_OPT_PDL = 12            /* 1 (default): the main kernel is launched as a programmatic
+                                  dependent of the stream's previous kernel, so its launch and
+                                  set-up overlap that kernel's end; it reads and writes memory only
+                                  after the previous kernel has finished.  0: ordinary launch */
 } gemm_option_t;
 
 /* Set an option on a handle.  Errors: GEMM_ERR_INVALID_ARG for an unknown
