@@ -73,6 +73,24 @@ def dist_env():
     return ws, rank, local
 
 
+def slowest_over_ranks(ms, device="cpu"):
+    """The largest of every rank's timed-region milliseconds (the job takes as
+    long as its slowest replica); ms itself when running alone."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank_step, ws, steps, ms_slowest):
+    """Whole-job throughput: every rank's units over the slowest rank's time,
+    in units per second / 1e12 (TFLOP/s for FLOPs)."""
+    return ws * units_per_rank_step * steps / (ms_slowest / 1e3) / 1e12
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -290,12 +308,8 @@ def run_ours(args):
     st, word = h.status(sptr)
     if st != G.OK:
         raise RuntimeError("timed kernel status %s (0x%x)" % (G.STATUS.get(st), word))
-    ms = ev[0].elapsed_time(ev[1])
-    if ws > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = ws * flops * K / (ms / 1e3) / 1e12
+    ms = slowest_over_ranks(ev[0].elapsed_time(ev[1]), dev)
+    value = job_value(flops, ws, K, ms)
     kernel_ms = ms / K   # one kernel launch per step, back to back on one stream
 
     # End to end through the public API: pinned host buffers, H2D + GEMM + D2H per step.
