@@ -663,6 +663,20 @@ struct DeviceGuard {
 
 }  // namespace
 
+// gemm_run_host: device copies of A, B and C, and the two copy streams (one
+// per direction) whose transfers overlap the GEMMs of neighbouring row chunks.
+constexpr int kHostChunks = 4;
+struct HostStage {
+  void* a = nullptr;
+  void* b = nullptr;
+  void* c = nullptr;
+  size_t a_bytes = 0, b_bytes = 0, c_bytes = 0;
+  cudaStream_t up = nullptr, down = nullptr;  // host -> device, device -> host
+  cudaEvent_t start = nullptr, end = nullptr;
+  cudaEvent_t loaded[kHostChunks] = {};       // a chunk's operands are on the device
+  cudaEvent_t computed[kHostChunks] = {};     // a chunk's C is ready to copy back
+};
+
 struct gemm_handle_s {
   int device = -1;
   int sm_count = 0;
@@ -674,6 +688,7 @@ struct gemm_handle_s {
   int last_cuda_error = 0;
   SlotTable slots;  // resident slots (CTAs, pairs, clusters) per kernel configuration
   Options opt;
+  HostStage host;
 };
 
 static gemm_status_t cuda_fail(gemm_handle_t h, cudaError_t e) {
@@ -725,6 +740,18 @@ gemm_status_t gemm_destroy(gemm_handle_t h) {
     cudaFree(h->d_ws);
     cudaFree(h->d_counters);
     cudaFree(h->d_status);
+    HostStage& hs = h->host;
+    cudaFree(hs.a);
+    cudaFree(hs.b);
+    cudaFree(hs.c);
+    if (hs.up) cudaStreamDestroy(hs.up);
+    if (hs.down) cudaStreamDestroy(hs.down);
+    if (hs.start) cudaEventDestroy(hs.start);
+    if (hs.end) cudaEventDestroy(hs.end);
+    for (int i = 0; i < kHostChunks; ++i) {
+      if (hs.loaded[i]) cudaEventDestroy(hs.loaded[i]);
+      if (hs.computed[i]) cudaEventDestroy(hs.computed[i]);
+    }
   }
   delete h;
   return GEMM_OK;
@@ -871,7 +898,7 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
                               gemm_dtype_t dtype, EpiOps ops, void* stream, int64_t batch = 1,
                               int64_t strideA = 0, int64_t strideB = 0, int64_t strideC = 0,
                               int64_t groups = 0, const int64_t* m_sizes = nullptr,
-                              const BlockScale* bs = nullptr) {
+                              const BlockScale* bs = nullptr, bool allow_pdl = true) {
   if (!h) return GEMM_ERR_INVALID_ARG;
   Plan pl;
   gemm_status_t s = make_plan(h->opt, h->slots, transA, transB, M, N, K, A, lda, B, ldb, beta,
@@ -973,7 +1000,8 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
     a.group_row = d_row;
   }
   a.drop_load = h->opt.drop_load;
-  a.pdl = pl.sched.groups > 0 ? 0 : h->opt.pdl;  // (grouped: the group tables are copied just before)
+  // (grouped: the group tables are copied just before; host calls: an event wait comes just before)
+  a.pdl = (pl.sched.groups > 0 || !allow_pdl) ? 0 : h->opt.pdl;
   ops.bias_on_i = P.swap_ab;  // a swapped problem computes C^T: C's columns are the kernel's rows
   a.ops = ops;
   e = tc_launch(pl.cfg, map_p, map_q, map_c, a, P.grid, st);
@@ -1063,6 +1091,114 @@ gemm_status_t gemm_plan_block_scaled(gemm_handle_t h, int sm_count, int64_t M, i
                               0, 0, 0, 0, nullptr, &bs);
   if (s == GEMM_OK) *plan = pl.pub;
   return s;
+}
+
+// Grow one device staging buffer (synchronous: the old one may still be in use).
+static cudaError_t host_stage_buffer(void** buf, size_t* have, size_t need) {
+  if (need <= *have) return cudaSuccess;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return e;
+  cudaFree(*buf);
+  *buf = nullptr;
+  *have = 0;
+  const size_t want = round_up(need, size_t{1} << 20);
+  e = cudaMalloc(buf, want);
+  if (e == cudaSuccess) *have = want;
+  return e;
+}
+
+gemm_status_t gemm_run_host(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int64_t M, int64_t N, int64_t K,
+                            float alpha, const void* A, int64_t lda, const void* B, int64_t ldb, float beta, void* C,
+                            int64_t ldc, gemm_dtype_t dtype, void* stream) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  const DtypeInfo dt = dtype_info(dtype);
+  if (!dt.valid) return GEMM_ERR_INVALID_ARG;
+  if (dt.sc != 0) return GEMM_ERR_UNSUPPORTED;  // block-scaled inputs: device buffers only
+  {  // the argument checks of gemm_run (host pointers stand in for the device copies)
+    Plan pl;
+    gemm_status_t s = make_plan(h->opt, h->slots, transA, transB, M, N, K, A, lda, B, ldb, beta, C, ldc, dtype, &pl);
+    if (s != GEMM_OK) return s;
+    if (pl.pub.path == GEMM_PATH_NOOP) return GEMM_OK;
+  }
+  const int64_t ea = dt.eb;
+  const int64_t ec = dt.c_type == kCF32 ? 4 : dt.c_type == kCE4M3 ? 1 : 2;
+  const int64_t a_rows = transA == GEMM_OP_N ? M : K, a_cols = transA == GEMM_OP_N ? K : M;
+  const int64_t b_rows = transB == GEMM_OP_T ? N : K, b_cols = transB == GEMM_OP_T ? K : N;
+  const size_t a_bytes = K > 0 ? static_cast<size_t>(((a_rows - 1) * lda + a_cols) * ea) : 0;
+  const size_t b_bytes = K > 0 ? static_cast<size_t>(((b_rows - 1) * ldb + b_cols) * ea) : 0;
+  const size_t c_bytes = static_cast<size_t>(((M - 1) * ldc + N) * ec);
+  DeviceGuard g(h->device);
+  HostStage& hs = h->host;
+  cudaError_t e = cudaSuccess;
+  if (!hs.up) {
+    e = cudaStreamCreateWithFlags(&hs.up, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hs.down, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hs.start, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hs.end, cudaEventDisableTiming);
+    for (int i = 0; i < kHostChunks && e == cudaSuccess; ++i) {
+      e = cudaEventCreateWithFlags(&hs.loaded[i], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hs.computed[i], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) return cuda_fail(h, e);
+  }
+  if ((e = host_stage_buffer(&hs.a, &hs.a_bytes, a_bytes)) != cudaSuccess ||
+      (e = host_stage_buffer(&hs.b, &hs.b_bytes, b_bytes)) != cudaSuccess ||
+      (e = host_stage_buffer(&hs.c, &hs.c_bytes, c_bytes)) != cudaSuccess) {
+    cudaGetLastError();
+    h->last_cuda_error = static_cast<int>(e);
+    return GEMM_ERR_WORKSPACE;
+  }
+  // Row chunks of A (stored M x K) and C: the copy of chunk c + 1 in and of
+  // chunk c - 1 out run while chunk c is multiplied.  One chunk for a
+  // transposed A or a short M.
+  const int64_t chunk = (transA == GEMM_OP_N && M >= 1024 && K > 0)
+                            ? static_cast<int64_t>(round_up(static_cast<size_t>(cdiv(M, kHostChunks)), 256))
+                            : M;
+  const int nch = static_cast<int>(cdiv(M, chunk));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ad = static_cast<char*>(hs.a);
+  char* bd = static_cast<char*>(hs.b);
+  char* cd = static_cast<char*>(hs.c);
+  const char* ah = static_cast<const char*>(A);
+  const char* bh = static_cast<const char*>(B);
+  char* ch = static_cast<char*>(C);
+  // the copy streams start after everything already queued on the caller's stream
+  e = cudaEventRecord(hs.start, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hs.up, hs.start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hs.down, hs.start, 0);
+  if (e == cudaSuccess && b_bytes > 0)
+    e = cudaMemcpy2DAsync(bd, ldb * ea, bh, ldb * ea, b_cols * ea, b_rows, cudaMemcpyHostToDevice, hs.up);
+  for (int c = 0; c < nch && e == cudaSuccess; ++c) {
+    const int64_t r0 = c * chunk;
+    const int64_t rows = std::min(chunk, M - r0);
+    const int64_t a_off = transA == GEMM_OP_N ? r0 * lda * ea : 0;
+    if (a_bytes > 0) {
+      if (transA == GEMM_OP_N)
+        e = cudaMemcpy2DAsync(ad + a_off, lda * ea, ah + a_off, lda * ea, K * ea, rows, cudaMemcpyHostToDevice, hs.up);
+      else
+        e = cudaMemcpy2DAsync(ad, lda * ea, ah, lda * ea, a_cols * ea, a_rows, cudaMemcpyHostToDevice, hs.up);
+    }
+    if (e == cudaSuccess && beta != 0.0f)
+      e = cudaMemcpy2DAsync(cd + r0 * ldc * ec, ldc * ec, ch + r0 * ldc * ec, ldc * ec, N * ec, rows,
+                            cudaMemcpyHostToDevice, hs.up);
+    if (e == cudaSuccess) e = cudaEventRecord(hs.loaded[c], hs.up);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, hs.loaded[c], 0);
+    if (e != cudaSuccess) break;
+    const gemm_status_t s = run_gemm(h, transA, transB, rows, N, K, alpha, ad + a_off, lda, bd, ldb, beta,
+                                     cd + r0 * ldc * ec, ldc, dtype, EpiOps(), st, 1, 0, 0, 0, 0, nullptr, nullptr,
+                                     false);
+    if (s != GEMM_OK) return s;
+    e = cudaEventRecord(hs.computed[c], st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hs.down, hs.computed[c], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpy2DAsync(ch + r0 * ldc * ec, ldc * ec, cd + r0 * ldc * ec, ldc * ec, N * ec, rows,
+                            cudaMemcpyDeviceToHost, hs.down);
+  }
+  // the caller's stream continues once C is back on the host
+  if (e == cudaSuccess) e = cudaEventRecord(hs.end, hs.down);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, hs.end, 0);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  return GEMM_OK;
 }
 
 gemm_status_t gemm_plan_grouped(gemm_handle_t h, int sm_count, gemm_op_t transB, int64_t groups,

@@ -90,6 +90,8 @@ SIGNATURES = {
                                 _i32, ctypes.POINTER(Epilogue), _vp]),
     "gemm_plan_grouped": (_i32, [_vp, ctypes.c_int, _i32, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _f32, _vp,
                                  _i64, _i32, ctypes.POINTER(Plan)]),
+    "gemm_run_host": (_i32, [_vp, _i32, _i32, _i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _i32,
+                             _vp]),
     "gemm_run_block_scaled": (_i32, [_vp, _i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _f32,
                                      _vp, _i64, _i32, ctypes.POINTER(Epilogue), _vp]),
     "gemm_plan_block_scaled": (_i32, [_vp, ctypes.c_int, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
@@ -337,18 +339,26 @@ def gemm(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0, handle=None, 
     return C
 
 
-def gemm_host(A_host, B_host, C_host, A_dev, B_dev, C_dev, transA=False, transB=False, alpha=1.0,
-              beta=0.0, handle=None, stream=None):
-    """End-to-end call on host buffers: copy A, B (and C when beta != 0) from
-    pinned host memory to the device, run the GEMM, copy C back, all enqueued
-    on one stream.  The device tensors are caller-provided staging buffers."""
+def gemm_host(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0, handle=None, stream=None):
+    """End-to-end call on CPU tensors (gemm_run_host): A, B (and C when beta
+    != 0) go to the device, the GEMM runs, C comes back, overlapped in row
+    chunks; use page-locked tensors (``pin_memory()``) for the overlap.  The
+    call is asynchronous on `stream` (default: torch's current stream):
+    synchronise it before reading C."""
     import torch
-    s = stream if stream is not None else torch.cuda.current_stream(C_dev.device)
-    with torch.cuda.stream(s):
-        A_dev.copy_(A_host, non_blocking=True)
-        B_dev.copy_(B_host, non_blocking=True)
-        if beta != 0.0:
-            C_dev.copy_(C_host, non_blocking=True)
-        gemm(A_dev, B_dev, C_dev, transA, transB, alpha, beta, handle=handle, stream=s.cuda_stream)
-        C_host.copy_(C_dev, non_blocking=True)
-    return C_host
+    for t, n in ((A, "A"), (B, "B"), (C, "C")):
+        if t.is_cuda:
+            raise ValueError("%s must be a host tensor" % n)
+    ta, tb = int(bool(transA)), int(bool(transB))
+    M = A.shape[1] if ta else A.shape[0]
+    K = A.shape[0] if ta else A.shape[1]
+    N = B.shape[0] if tb else B.shape[1]
+    code = dtype_code(A.dtype, C.dtype, B.dtype)
+    h = handle if handle is not None else default_handle(0)
+    if stream is None:
+        stream = torch.cuda.current_stream(h.device)
+    sptr = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+    st = lib().gemm_run_host(h.ptr, ta, tb, M, N, K, alpha, A.data_ptr(), _ld(A, "A"), B.data_ptr(), _ld(B, "B"),
+                             beta, C.data_ptr(), _ld(C, "C"), code, sptr)
+    _check(st, "gemm_run_host")
+    return C

@@ -378,6 +378,24 @@ gemm_status_t gemm_plan_block_scaled(gemm_handle_t h, int sm_count, int64_t M, i
                                      const void* SFB, int64_t ld_sfb, float beta, const void* C, int64_t ldc,
                                      gemm_dtype_t dtype, gemm_plan_t* plan);
 
+/*
+ * gemm_run_host: gemm_run on HOST buffers.  A, B and C are host pointers
+ * (page-locked memory lets the copies overlap the GEMM; pageable memory works
+ * but serialises them); sizes, leading dimensions, dtypes and errors as
+ * gemm_run (block-scaled types: GEMM_ERR_UNSUPPORTED).  The handle keeps device
+ * copies of A, B and C (grown as needed: a larger call synchronises the device
+ * once) and two copy streams, one per direction.  A non-transposed A with
+ * M >= 1024 is processed in four row chunks: chunk c + 1's rows of A (and of
+ * C when beta != 0) travel to the device and chunk c - 1's rows of C back to
+ * the host while chunk c is multiplied; B goes over once, first.  Everything
+ * is ordered after the work already queued on `stream`, and `stream` waits
+ * for the last copy back: C on the host is complete once `stream` is
+ * synchronised.  The host buffers must stay valid and unchanged until then.
+ */
+gemm_status_t gemm_run_host(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int64_t M, int64_t N, int64_t K,
+                            float alpha, const void* A, int64_t lda, const void* B, int64_t ldb, float beta, void* C,
+                            int64_t ldc, gemm_dtype_t dtype, void* stream);
+
 /* gemm_plan for a strided batched call (arguments as gemm_run_strided_batched). */
 gemm_status_t gemm_plan_strided_batched(gemm_handle_t h, int sm_count, gemm_op_t transA, gemm_op_t transB,
                                         int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,

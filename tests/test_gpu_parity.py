@@ -306,6 +306,46 @@ def test_bad_arguments_return_errors(h):
         == G.ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("pdl", [1, 0])
+def test_chained_gemms_read_each_others_output(h, pdl):
+    """C1 = A B, then C2 = C1 D and C3 = C2 E back to back on one stream: each
+    kernel starts its set-up while the previous one runs (programmatic
+    dependent launch) but must read the finished C of the one before.  The
+    middle GEMM's operand needs a repack (odd pitch), so a copy kernel sits
+    between two of them.  Checked against the oracle applied step by step."""
+    import oracle
+    g = torch.Generator().manual_seed(3)
+    A = torch.randn(520, 384, generator=g).to(torch.bfloat16)
+    B = torch.randn(384, 776, generator=g).to(torch.bfloat16)
+    D = (torch.randn(776, 264, generator=g) / 16).to(torch.bfloat16)
+    E = (torch.randn(264, 300, generator=g) / 8).to(torch.bfloat16)
+    h.set_option(G.OPT_PDL, pdl)
+    try:
+        Ad, Bd, Dd, Ed = A.cuda(), B.cuda(), D.cuda(), E.cuda()
+        C1 = torch.full((520, 777), float("nan"), dtype=torch.bfloat16, device="cuda")  # ldc 777: C2's A repacked
+        C2 = torch.full((520, 264), float("nan"), dtype=torch.bfloat16, device="cuda")
+        C3 = torch.full((520, 300), float("nan"), dtype=torch.float32, device="cuda")
+        for _ in range(3):
+            assert h.run_raw(0, 0, 520, 776, 384, 1.0, Ad.data_ptr(), 384, Bd.data_ptr(), 776, 0.0, C1.data_ptr(),
+                             777, G.BF16_BF16, None) == G.OK
+            assert h.run_raw(0, 0, 520, 264, 776, 1.0, C1.data_ptr(), 777, Dd.data_ptr(), 264, 0.0, C2.data_ptr(),
+                             264, G.BF16_BF16, None) == G.OK
+            assert h.run_raw(0, 0, 520, 300, 264, 1.0, C2.data_ptr(), 264, Ed.data_ptr(), 300, 0.0, C3.data_ptr(),
+                             300, G.BF16_F32, None) == G.OK
+        assert h.status()[0] == G.OK
+    finally:
+        h.set_option(G.OPT_PDL, 1)
+    bits = lambda t: t.contiguous().view(torch.uint16).numpy()
+    c1 = C1.cpu()
+    R1, M1 = oracle.gemm(0, 0, 520, 776, 384, 1.0, bits(A), 384, bits(B), 776, 0.0, None, 776, oracle.IN_BF16)
+    assert_close(c1[:, :776].double().numpy(), R1, M1, False, "C1")
+    c2 = C2.cpu()
+    R2, M2 = oracle.gemm(0, 0, 520, 264, 776, 1.0, bits(c1), 777, bits(D), 264, 0.0, None, 264, oracle.IN_BF16)
+    assert_close(c2.double().numpy(), R2, M2, False, "C2 from the C1 the GPU wrote")
+    R3, M3 = oracle.gemm(0, 0, 520, 300, 264, 1.0, bits(c2), 264, bits(E), 300, 0.0, None, 300, oracle.IN_BF16)
+    assert_close(C3.cpu().double().numpy(), R3, M3, True, "C3 from the C2 the GPU wrote")
+
+
 def test_run_to_run_determinism(h):
     """Same inputs, same bits, including the split-K fix-up (fixed summation order)."""
     for (M, N, K) in [(512, 768, 640), (64, 4000, 4096)]:
