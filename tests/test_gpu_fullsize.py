@@ -67,3 +67,23 @@ def test_lm_head_64(h):
     rows = np.full(p.N, 17, dtype=np.int64)
     r, m = _at(p, rows, cols)
     assert_close(Cd[17, :p.N].double().cpu().numpy(), r, m, True, "lm_head row 17")
+
+
+@pytest.mark.parametrize("M,N,K,transA,transB", [
+    (1, 4096, 4096, 0, 1),        # one row of C (swapped: the 4096 columns on the MMA's rows)
+    (4096, 1, 4096, 0, 0),        # one column of C
+    (128, 136, 131072, 0, 1),     # very long K: every k-block of one tile row, split across the grid
+    (262144, 64, 128, 0, 0),      # 2048 tile rows, one tile column
+    (3, 5, 7, 1, 1),              # smaller than every tile in all three dimensions
+])
+def test_extreme_shapes(h, M, N, K, transA, transB):
+    p = inputs.make_problem("extreme_%dx%dx%d" % (M, N, K), M, N, K, transA, transB, "bf16", "f32",
+                            ("normal", 0.0, 1.0), ("normal", 0.0, 1.0), seed=M % 97 + K % 89)
+    _sampled(p, h, count=2000)
+
+
+def test_largest_extent_is_refused_not_run(h):
+    """Extents past the kernels' 32-bit index range are refused at planning time."""
+    with pytest.raises(G.GemmError) as e:
+        G.plan(1 << 31, 64, 64, 0, 1, handle=h)
+    assert e.value.status == G.ERR_UNSUPPORTED
