@@ -7,8 +7,8 @@
 //    value cut to TF32 (sign, 8-bit exponent, top 10 fraction bits), as the
 //    tensor core reads an fp32 operand.  Several parts (the fp32 GEMM from
 //    three TF32 products): hi = TF32(x) and lo = TF32(x - hi), both rounded to
-//    nearest, laid out in segments of K chosen by a bit pattern, so that one
-//    TF32 GEMM over parts x K sums the chosen products;
+//    nearest, laid out in segments chosen by a bit pattern; the GEMM reads
+//    the segments in the order that sums the chosen products;
 //  * dequant_block_scaled: writes a block-scaled operand (MXFP8 or NVFP4 codes
 //    with one scale code per block of k, "CUDA GEMM 矩阵乘法优化指南", 13.2) as
 //    bf16 values code x scale, K-major, for the bf16 tensor-core GEMM.  Each
@@ -79,17 +79,18 @@ __device__ __forceinline__ float cut_tf32(float x) {
 }
 
 // Element (r, k) of one source matrix: src[k * lds + r] (kTrans) or src[r * lds + k].
-// Output row r: parts * K values at dst[r * ldd]; parts == 1: the cut value;
-// else segment s holds the low part when bit s of pattern is set, the high part
-// otherwise.  Transposed sources go through a 32 x 32 shared-memory tile so
-// that reads and writes are both coalesced.
+// Output row r: parts segments of seg (>= K) values at dst[r * ldd], values
+// K .. seg - 1 zero; parts == 1: the cut value; else segment s holds the low
+// part when bit s of pattern is set, the high part otherwise.  Transposed
+// sources go through a 32 x 32 shared-memory tile so that reads and writes are
+// both coalesced.
 template <bool kTrans>
 __global__ void split_tf32_kernel(const float* __restrict__ src, int64_t lds, int64_t sbs, float* __restrict__ dst,
-                                  int64_t ldd, int64_t dbs, int64_t rows, int64_t K, int64_t nb, int parts,
-                                  int pattern) {
+                                  int64_t ldd, int64_t dbs, int64_t rows, int64_t K, int64_t seg, int64_t nb,
+                                  int parts, int pattern) {
   __shared__ float tile[32][33];
   const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8 threads
-  const int64_t tiles_r = (rows + 31) / 32, tiles_k = (K + 31) / 32;
+  const int64_t tiles_r = (rows + 31) / 32, tiles_k = (seg + 31) / 32;
   for (int64_t b = blockIdx.z; b < nb; b += gridDim.z) {
     const float* S = src + b * sbs;
     float* D = dst + b * dbs;
@@ -108,8 +109,8 @@ __global__ void split_tf32_kernel(const float* __restrict__ src, int64_t lds, in
       __syncthreads();
       for (int i = ty; i < 32; i += 8) {
         const int64_t r = r0 + i, k = k0 + tx;
-        if (r >= rows || k >= K) continue;
-        const float x = tile[tx][i];
+        if (r >= rows || k >= seg) continue;
+        const float x = tile[tx][i];  // (0 past K)
         float* row = D + r * ldd;
         if (parts == 1) {
           row[k] = cut_tf32(x);
@@ -118,7 +119,7 @@ __global__ void split_tf32_kernel(const float* __restrict__ src, int64_t lds, in
         float hi = to_tf32(x);
         if (isinf(hi) && !isinf(x)) hi = cut_tf32(x);  // rounded past the largest value
         const float lo = isfinite(x) ? to_tf32(x - hi) : 0.0f;
-        for (int s = 0; s < parts; ++s) row[s * K + k] = ((pattern >> s) & 1) ? lo : hi;
+        for (int s = 0; s < parts; ++s) row[s * seg + k] = ((pattern >> s) & 1) ? lo : hi;
       }
     }
   }
@@ -243,19 +244,20 @@ cudaError_t repack_launch(const void* src, int64_t lds, int64_t sbs, void* dst, 
 }
 
 cudaError_t split_tf32_launch(const float* src, int64_t lds, int64_t sbs, bool transposed, float* dst,
-                              int64_t ldd, int64_t dbs, int64_t rows, int64_t K, int64_t nb, int parts,
+                              int64_t ldd, int64_t dbs, int64_t rows, int64_t K, int64_t seg, int64_t nb, int parts,
                               int pattern, int sm_count, cudaStream_t stream) {
-  const int64_t tiles = ((rows + 31) / 32) * ((K + 31) / 32);
+  if (seg < K || ldd < parts * seg) return cudaErrorInvalidValue;
+  const int64_t tiles = ((rows + 31) / 32) * ((seg + 31) / 32);
   int64_t gx = static_cast<int64_t>(sm_count) * 8;
   if (gx > tiles) gx = tiles;
   int64_t gz = nb < 65535 ? nb : 65535;
   const dim3 grid(static_cast<unsigned>(gx > 0 ? gx : 1), 1, static_cast<unsigned>(gz > 0 ? gz : 1));
   if (transposed)
-    split_tf32_kernel<true><<<grid, dim3(32, 8), 0, stream>>>(src, lds, sbs, dst, ldd, dbs, rows, K, nb, parts,
-                                                              pattern);
+    split_tf32_kernel<true><<<grid, dim3(32, 8), 0, stream>>>(src, lds, sbs, dst, ldd, dbs, rows, K, seg, nb,
+                                                              parts, pattern);
   else
-    split_tf32_kernel<false><<<grid, dim3(32, 8), 0, stream>>>(src, lds, sbs, dst, ldd, dbs, rows, K, nb, parts,
-                                                               pattern);
+    split_tf32_kernel<false><<<grid, dim3(32, 8), 0, stream>>>(src, lds, sbs, dst, ldd, dbs, rows, K, seg, nb,
+                                                               parts, pattern);
   return cudaGetLastError();
 }
 

@@ -59,11 +59,15 @@ struct Operand {
   int64_t nb = 1;             // distinct matrices: 1 when shared by every batch
   // fp32 operands written as TF32 parts (split_tf32_launch) instead of repacked:
   // the source is ptr/ld/bstride, `src_k` values of k per row, read transposed
-  // when `split_trans`; the copy is rows x cols (= parts * src_k) K-major.
+  // when `split_trans`; the copy is rows x cols (= split_parts segments of
+  // split_seg values) K-major.  seg_map: bit s = the stored segment that
+  // logical segment s of the GEMM's k reads (three-product fp32 GEMM).
   int split_parts = 0;
   int split_pattern = 0;
   bool split_trans = false;
   int64_t src_k = 0;
+  int64_t split_seg = 0;
+  int seg_map = 0;
   // block-scaled operands written as bf16 (dequant_launch) instead: source
   // codes of format dq - 1 at ptr (ld values a row), scale codes sf (ld_sf a row)
   int dq = 0;
@@ -418,19 +422,25 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   // other is written K-major with its values cut to TF32 the same way.  The
   // fp32 GEMM (GEMM_F32_F32) splits every value x into hi = TF32(x) and lo =
   // TF32(x - hi) and sums lo_a hi_b + hi_a lo_b + hi_a hi_b (the small
-  // products first) as one GEMM over 3K: A's rows become [lo | hi | hi] and
-  // B's [hi | lo | hi].
+  // products first) as one GEMM over three segments of k: A is stored as
+  // [lo | hi] and read as [lo | hi | hi], B stored as [hi | lo] and read as
+  // [hi | lo | hi], each segment K rounded up to a whole 32-value k-slice
+  // (zeros past K) so that no k-slice straddles two segments.
   int64_t Kg = K;  // k extent of the GEMM the kernel runs
+  int64_t seg = K;
   if (dt.parts > 0) {
-    Kg = K * dt.parts;
+    seg = dt.parts > 1 ? static_cast<int64_t>(round_up(static_cast<size_t>(K), slice_k(dt.eb))) : K;
+    Kg = seg * dt.parts;
     for (Operand* op : {&a, &b}) {
       if (dt.parts == 1 && op->kmajor && tma_aligned(op->ptr, op->ld, dt.eb, op->bstride, op->nb)) continue;
-      op->split_parts = dt.parts;
+      op->split_parts = dt.parts > 1 ? 2 : 1;
       op->split_pattern = dt.parts == 1 ? 0 : op == &a ? 0x1 : 0x2;
+      op->seg_map = dt.parts == 1 ? 0 : op == &a ? 0x6 : 0x2;
+      op->split_seg = seg;
       op->split_trans = !op->kmajor;
       op->src_k = K;
       op->rows = op->kmajor ? op->rows : op->cols;
-      op->cols = Kg;
+      op->cols = op->split_parts * seg;
       op->kmajor = true;
     }
   }
@@ -881,7 +891,7 @@ static cudaError_t prepare_operands(const Plan& pl, uint8_t* ws, int sm_count, c
     else if (op.split_parts > 0)
       e = split_tf32_launch(static_cast<const float*>(op.ptr), op.ld, op.bstride, op.split_trans,
                             static_cast<float*>(dst), op.packed_ld, op.rows * op.packed_ld, op.rows, op.src_k,
-                            op.nb, op.split_parts, op.split_pattern, sm_count, st);
+                            op.split_seg, op.nb, op.split_parts, op.split_pattern, sm_count, st);
     else
       e = repack_launch(op.ptr, op.ld, op.bstride, dst, op.packed_ld, op.rows * op.packed_ld, op.rows, op.cols,
                         op.nb, pl.eb, sm_count, st);
@@ -1002,6 +1012,10 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
   a.drop_load = h->opt.drop_load;
   // (grouped: the group tables are copied just before; host calls: an event wait comes just before)
   a.pdl = (pl.sched.groups > 0 || !allow_pdl) ? 0 : h->opt.pdl;
+  // three-product fp32 GEMM: the logical k runs over three stored segments
+  a.seg_slices = pl.p.seg_map != 0 ? static_cast<int32_t>(pl.p.split_seg / slice_k(pl.eb)) : 0;
+  a.p_seg = pl.p.seg_map;
+  a.q_seg = pl.q.seg_map;
   ops.bias_on_i = P.swap_ab;  // a swapped problem computes C^T: C's columns are the kernel's rows
   a.ops = ops;
   e = tc_launch(pl.cfg, map_p, map_q, map_c, a, P.grid, st);
@@ -1410,6 +1424,9 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   a.wait_limit_ns = static_cast<uint64_t>(o.wait_limit_ns);
   a.drop_load = 0;
   a.pdl = 0;  // (the no-allocation entry point clears its arrays first, with ordinary stream order)
+  a.seg_slices = pl.p.seg_map != 0 ? static_cast<int32_t>(pl.p.split_seg / slice_k(pl.eb)) : 0;
+  a.p_seg = pl.p.seg_map;
+  a.q_seg = pl.q.seg_map;
   a.ops = EpiOps();  // no fused operations (the memset above zeroed out_scale)
   e = tc_launch(pl.cfg, map_p, map_q, map_c, a, P.grid, st);
   return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;

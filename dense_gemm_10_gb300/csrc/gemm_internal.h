@@ -63,6 +63,11 @@ struct TcArgs {
   uint64_t wait_limit_ns;
   int32_t drop_load;     // tests only: CTA 0 skips its drop_load-th k-block load (1-based)
   int32_t pdl;           // launch as a programmatic dependent of the stream's previous kernel
+  // TF32 operands stored as two segments of seg_slices 128-byte k-slices
+  // (0: no segments): logical segment s of K reads stored segment bit s of
+  // p_seg (P) / q_seg (Q)
+  int32_t seg_slices;
+  int32_t p_seg, q_seg;
   EpiOps ops;            // fused elementwise operations of the epilogue
   int64_t c_sb;          // batch stride of C in elements (strided batches; tile batch in Unit::tb)
   int32_t p_bcast;       // P is one matrix shared by every batch (its tensor map has one batch)
@@ -103,13 +108,13 @@ cudaError_t repack_launch(const void* src, int64_t lds, int64_t sbs, void* dst, 
                           cudaStream_t stream);
 
 // TF32 values of fp32 operands, written K-major: row r of dst (b-th matrix at
-// dbs elements) receives parts x K values.  parts == 1: each value with its 13
-// low fraction bits dropped.  parts > 1: segment s holds lo = TF32(x - hi)
-// when bit s of pattern is set, else hi = TF32(x) (both rounded to nearest).
-// Source element (r, k) is src[k * lds + r] when transposed, else
-// src[r * lds + k].
+// dbs elements) receives parts segments of seg values (seg >= K; values K ..
+// seg - 1 of a segment are 0).  parts == 1: each value with its 13 low fraction
+// bits dropped.  parts > 1: segment s holds lo = TF32(x - hi) when bit s of
+// pattern is set, else hi = TF32(x) (both rounded to nearest).  Source element
+// (r, k) is src[k * lds + r] when transposed, else src[r * lds + k].
 cudaError_t split_tf32_launch(const float* src, int64_t lds, int64_t sbs, bool transposed, float* dst,
-                              int64_t ldd, int64_t dbs, int64_t rows, int64_t K, int64_t nb, int parts,
+                              int64_t ldd, int64_t dbs, int64_t rows, int64_t K, int64_t seg, int64_t nb, int parts,
                               int pattern, int sm_count, cudaStream_t stream);
 
 // Block-scaled operand -> bf16, K-major: dst[r * ldd + k] = code(r, k) *

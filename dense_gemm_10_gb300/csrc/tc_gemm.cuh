@@ -445,6 +445,14 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
     const int j0 = (w.tj * MC + pair) * BN + q * Cfg::kQRows;
     const int zp = a.p_bcast ? 0 : w.tb;  // batch coordinate (0 for an operand shared by all batches)
     const int zq = a.q_bcast ? 0 : w.tb;
+    // (three-product fp32 GEMM: segment and k-slice within it of the unit's first k-slice)
+    int seg_s = 0, seg_in = 0;
+    if constexpr (EB == 4) {
+      if (a.seg_slices > 0) {
+        seg_s = (w.kb0 * KD) / a.seg_slices;
+        seg_in = w.kb0 * KD - seg_s * a.seg_slices;
+      }
+    }
     for (int kb = w.kb0; kb < w.kb1; ++kb) {  // one stage: k-slices kb * kdepth .. + kdepth - 1
       if (!warp_wait(smem_u32(&ctrl->empty[stage]), phase ^ 1u, ctrl, a, kRoleProducer, kBarEmpty,
                      true)) {
@@ -478,7 +486,21 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
             const int slot = stage * KD + t;  // ring slot of one k-slice
             const uint32_t sa = smem_u32(ring_a + slot * Cfg::kABytes);
             const uint32_t sb = smem_u32(ring_b + slot * Cfg::kBBytes);
-            const int k0 = (ks0 + t) * kSliceK;
+            int k0 = (ks0 + t) * kSliceK;
+            int kq = k0;
+            if constexpr (EB == 4) {
+              // fp32 from three TF32 products: each operand is stored as two
+              // segments of seg_slices k-slices, and logical segment s of the
+              // GEMM over 3 segments reads stored segment bit s of p_seg / q_seg
+              if (a.seg_slices > 0) {
+                k0 = (((a.p_seg >> seg_s) & 1) * a.seg_slices + seg_in) * kSliceK;
+                kq = (((a.q_seg >> seg_s) & 1) * a.seg_slices + seg_in) * kSliceK;
+                if (++seg_in == a.seg_slices) {
+                  seg_in = 0;
+                  ++seg_s;
+                }
+              }
+            }
             if constexpr (MC == 2) {
               // this pair's half of the P tile: 64 rows (K-major) or one 64-wide atom (M-major)
               if (p_kmajor)
@@ -492,11 +514,11 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
               load(sa + kMnAtomBytes, map_p, i0 + 64, k0, zp);
             }
             if (q_kmajor) {
-              load(sb, map_q, k0, j0, zq);
+              load(sb, map_q, kq, j0, zq);
             } else {
 #pragma unroll
               for (int c = 0; c < Cfg::kQRows / 64; ++c)
-                load(sb + c * kMnAtomBytes, map_q, j0 + 64 * c, k0, zq);
+                load(sb + c * kMnAtomBytes, map_q, j0 + 64 * c, kq, zq);
             }
           }
         }
