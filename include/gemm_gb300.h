@@ -63,9 +63,9 @@ typedef enum { GEMM_OP_N = 0, GEMM_OP_T = 1 } gemm_op_t;
  *                  lo = TF32(x - hi) (rounded to nearest) and every product is
  *                  lo_a hi_b + hi_a lo_b + hi_a hi_b, which misses a * b by
  *                  about 2^-21 of |a b|.  Both operands are first written
- *                  K-major as TF32 parts into the workspace (3 x K values a
- *                  row: two more launches, 3x the operand bytes), then one
- *                  TF32 GEMM over 3K sums the three products.
+ *                  K-major into the workspace as two TF32 segments (two more
+ *                  launches, twice the operand bytes), then one TF32 GEMM
+ *                  over three segments of k sums the three products.
  *   GEMM_TF32_F32  one TF32 product per product: the 13 low fraction bits of
  *                  every input are dropped (about 2^-10 of each value).  A
  *                  K-major operand (A with transA == GEMM_OP_N, B with transB
