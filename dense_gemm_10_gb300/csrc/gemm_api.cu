@@ -302,9 +302,13 @@ Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64
   // Stream-K tail: the tiles of the incomplete last wave shared by g slots.
   const int64_t full_waves = tiles / slots;
   const int64_t sk_tiles = tiles - full_waves * slots;
-  // An HBM-bound GEMM with at least one full wave already streams from every
-  // SM: evening out the waves only adds the partial-sum traffic.
-  const bool sk_allowed = o.stream_k == 2 || (o.stream_k == 0 && !(hbm_bound && tiles >= slots));
+  // An HBM-bound GEMM whose whole tiles keep (nearly) every slot streaming
+  // gains nothing from evening out the waves but the partial-sum traffic; one
+  // that leaves a tenth of the slots idle gains their share of the bandwidth
+  // (64 x 32000 x 4096: 250 tiles on 125 of 152 SMs, 49.0 us; stream-K on all
+  // of them, 47.4 us).
+  const bool hbm_busy = hbm_bound && tiles >= slots && 10 * ch.slots >= 9 * slots;
+  const bool sk_allowed = o.stream_k == 2 || (o.stream_k == 0 && !hbm_busy);
   if (sk_allowed && sk_tiles > 0 && sk_tiles * cl <= kCounterCap) {
     const int64_t iters = sk_tiles * num_kb;
     int64_t best_g = 0;
@@ -313,8 +317,9 @@ Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64
       // After full waves, a tail whose share per slot exceeds half a tile is
       // mostly whole-tile work already; its partial sums and the tail tiles'
       // out-of-raster operand reads cost more than the quantisation saves
-      // (measured at 8192 x 4096 x 16384).
-      if (o.stream_k != 2 && full_waves > 0 && 2 * cdiv(iters, g) > num_kb) continue;
+      // (measured at 8192 x 4096 x 16384).  An HBM-bound GEMM gains the idle
+      // slots' bandwidth instead.
+      if (o.stream_k != 2 && !hbm_bound && full_waves > 0 && 2 * cdiv(iters, g) > num_kb) continue;
       const double t = sk_tail_cost(sk_tiles, num_kb, g, r);
       if (t < best_tail - 1e-9) {
         best_tail = t;

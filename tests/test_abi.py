@@ -105,15 +105,22 @@ def test_plan_major_modes(ta, tb, ak, bk):
 
 def test_plan_lm_head_swaps():
     """M = 64: the vocabulary rides on the MMA's M (swap-AB), 128 vocabulary rows
-    against the 64 activation rows per tile.  The GEMM is bound by HBM, so there
-    is no stream-K tail (more than a full wave of tiles already streams from
-    every SM), and the 250 tiles go out as two equal waves of 125 CTAs
-    rather than 152 + 98."""
+    against the 64 activation rows per tile.  The GEMM is bound by HBM: whole
+    tiles would stream from only 125 of the 152 SMs (two waves), so the 98
+    tiles past the first full wave are shared out by stream-K and every SM
+    streams."""
     p = G.plan(64, 32000, 4096, 0, 1)
     assert p.swap_ab == 1 and p.path == G.PATH_TC_1CTA and p.cluster == 1
     assert p.a_kmajor == 1 and p.b_kmajor == 1   # MMA A = weights (N x K), MMA B = activations (M x K)
     assert p.bm == 128 and p.bn == 64 and p.tiles == 250
-    assert p.schedule == G.SCHED_TILES and p.grid == 125
+    assert p.schedule == G.SCHED_STREAM_K and p.grid == 152 and p.dp_tiles == 152
+
+
+def test_plan_hbm_bound_full_waves_keep_whole_tiles():
+    """An HBM-bound GEMM whose whole tiles keep at least nine tenths of the
+    slots busy gets no stream-K tail (it would add only partial-sum traffic)."""
+    p = G.plan(64, 38912, 4096, 0, 1)   # 304 tiles of 128 rows: two full waves on 152 SMs
+    assert p.swap_ab == 1 and p.schedule == G.SCHED_TILES and p.grid == 152
 
 
 def test_plan_compute_bound_keeps_stream_k():
@@ -262,7 +269,7 @@ def test_plan_half_atom_pairs_need_k_major_q():
     which only the K-major layout allows."""
     p = G.plan(64, 32000, 4096, 1, 1)     # A stored K x M: the activations are M-major
     assert not (p.cluster == 2 and p.bn == 64)
-    assert p.vector_store == 0 and p.grid == 125   # two equal waves of 250 whole tiles
+    assert p.vector_store == 0 and p.grid == 152   # (HBM-bound: stream-K keeps every SM streaming)
 
 
 def test_plan_few_tiles_stream_k():
