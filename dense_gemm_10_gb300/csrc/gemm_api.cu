@@ -44,6 +44,7 @@ struct Options {
   int tma_store = 0; // GEMM_OPT_EPILOGUE: 0 auto, 1 bulk stores when possible, 2 direct stores
   int kdepth = 0;    // GEMM_OPT_KDEPTH: 0 auto, else 64-wide k-slices per ring stage
   int pdl = 1;       // GEMM_OPT_PDL: programmatic dependent launch of the main kernel
+  int plan_cache = 1;  // GEMM_OPT_PLAN_CACHE: reuse the plans of recent calls
 };
 
 // One stored operand, as the tensor-memory-accelerator copy engine will see it.
@@ -678,6 +679,26 @@ struct DeviceGuard {
 
 }  // namespace
 
+// Plans of recent plain and strided-batched calls, so that a repeated call
+// skips the planner (its schedule search costs several microseconds on the
+// host).  A plan depends on the pointers only through their 16-byte alignment;
+// a hit gets the call's own pointers back.
+struct PlanKey {
+  int32_t transA, transB, dtype;
+  uint32_t align_a, align_b, align_c;
+  int64_t M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC;
+  float beta;
+  Options opt;
+};
+constexpr int kPlanCache = 32;
+struct PlanCache {
+  PlanKey key[kPlanCache];
+  Plan plan[kPlanCache];
+  uint64_t used[kPlanCache] = {};  // 0: empty; else the tick of the last use
+  uint64_t tick = 0;
+  uint64_t hits = 0, misses = 0;
+};
+
 // gemm_run_host: device copies of A, B and C, and the two copy streams (one
 // per direction) whose transfers overlap the GEMMs of neighbouring row chunks.
 constexpr int kHostChunks = 4;
@@ -704,6 +725,7 @@ struct gemm_handle_s {
   SlotTable slots;  // resident slots (CTAs, pairs, clusters) per kernel configuration
   Options opt;
   HostStage host;
+  PlanCache plans;
 };
 
 static gemm_status_t cuda_fail(gemm_handle_t h, cudaError_t e) {
@@ -841,8 +863,19 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
       if (value < 0 || value > 1) return GEMM_ERR_INVALID_ARG;
       h->opt.pdl = static_cast<int>(value);
       return GEMM_OK;
+    case GEMM_OPT_PLAN_CACHE:
+      if (value < 0 || value > 1) return GEMM_ERR_INVALID_ARG;
+      h->opt.plan_cache = static_cast<int>(value);
+      return GEMM_OK;
   }
   return GEMM_ERR_INVALID_ARG;
+}
+
+gemm_status_t gemm_plan_cache_stats(gemm_handle_t h, uint64_t* hits, uint64_t* misses) {
+  if (!h || !hits || !misses) return GEMM_ERR_INVALID_ARG;
+  *hits = h->plans.hits;
+  *misses = h->plans.misses;
+  return GEMM_OK;
 }
 
 gemm_status_t gemm_launch_count(gemm_handle_t h, uint64_t* count) {
@@ -907,6 +940,52 @@ static cudaError_t prepare_operands(const Plan& pl, uint8_t* ws, int sm_count, c
   return cudaSuccess;
 }
 
+// make_plan through the handle's cache (plain and strided-batched calls).
+static gemm_status_t cached_plan(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int64_t M, int64_t N,
+                                 int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, float beta,
+                                 const void* C, int64_t ldc, gemm_dtype_t dtype, Plan* pl, int64_t batch,
+                                 int64_t strideA, int64_t strideB, int64_t strideC) {
+  if (!h->opt.plan_cache)
+    return make_plan(h->opt, h->slots, transA, transB, M, N, K, A, lda, B, ldb, beta, C, ldc, dtype, pl, batch,
+                     strideA, strideB, strideC);
+  PlanKey k;
+  std::memset(&k, 0, sizeof(k));  // (padding too: keys compare bytewise)
+  k.transA = transA;
+  k.transB = transB;
+  k.dtype = dtype;
+  k.align_a = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(A) % 16) | (A ? 0u : 0x100u);
+  k.align_b = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(B) % 16) | (B ? 0u : 0x100u);
+  k.align_c = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(C) % 16) | (C ? 0u : 0x100u);
+  k.M = M; k.N = N; k.K = K; k.lda = lda; k.ldb = ldb; k.ldc = ldc;
+  k.batch = batch; k.strideA = strideA; k.strideB = strideB; k.strideC = strideC;
+  k.beta = beta;
+  k.opt = h->opt;
+  PlanCache& pc = h->plans;
+  ++pc.tick;
+  int victim = 0;
+  for (int e = 0; e < kPlanCache; ++e) {
+    if (pc.used[e] != 0 && std::memcmp(&pc.key[e], &k, sizeof(k)) == 0) {
+      pc.used[e] = pc.tick;
+      ++pc.hits;
+      *pl = pc.plan[e];
+      // this call's operands (a swapped problem has B on the MMA's rows)
+      pl->p.ptr = pl->pub.swap_ab ? B : A;
+      pl->q.ptr = pl->pub.swap_ab ? A : B;
+      return GEMM_OK;
+    }
+    if (pc.used[e] < pc.used[victim]) victim = e;
+  }
+  ++pc.misses;
+  const gemm_status_t s = make_plan(h->opt, h->slots, transA, transB, M, N, K, A, lda, B, ldb, beta, C, ldc, dtype,
+                                    pl, batch, strideA, strideB, strideC);
+  if (s == GEMM_OK) {
+    pc.key[victim] = k;
+    pc.plan[victim] = *pl;
+    pc.used[victim] = pc.tick;
+  }
+  return s;
+}
+
 static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB, int64_t M,
                               int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
                               const void* B, int64_t ldb, float beta, void* C, int64_t ldc,
@@ -916,8 +995,12 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
                               const BlockScale* bs = nullptr, bool allow_pdl = true) {
   if (!h) return GEMM_ERR_INVALID_ARG;
   Plan pl;
-  gemm_status_t s = make_plan(h->opt, h->slots, transA, transB, M, N, K, A, lda, B, ldb, beta,
-                              C, ldc, dtype, &pl, batch, strideA, strideB, strideC, groups, m_sizes, bs);
+  gemm_status_t s =
+      (groups == 0 && bs == nullptr)
+          ? cached_plan(h, transA, transB, M, N, K, A, lda, B, ldb, beta, C, ldc, dtype, &pl, batch, strideA,
+                        strideB, strideC)
+          : make_plan(h->opt, h->slots, transA, transB, M, N, K, A, lda, B, ldb, beta, C, ldc, dtype, &pl, batch,
+                      strideA, strideB, strideC, groups, m_sizes, bs);
   if (s == GEMM_OK && groups > 0) M = pl.I;  // the stacked rows
   if (s != GEMM_OK) return s;
   const gemm_plan_t& P = pl.pub;

@@ -42,6 +42,7 @@ PATH_NOOP, PATH_SCALE_C, PATH_TC_1CTA, PATH_TC_2CTA, PATH_TC_2CTA_MULTICAST = 0,
 OPT_EPILOGUE = 10
 OPT_KDEPTH = 11
 OPT_PDL = 12
+OPT_PLAN_CACHE = 13
 BULK_NONE, BULK_ROWS, BULK_TRANSPOSED = 0, 1, 2   # gemm_plan_t.bulk_store
 SCHED_TILES, SCHED_STREAM_K = 0, 1
 
@@ -90,6 +91,7 @@ SIGNATURES = {
                                 _i32, ctypes.POINTER(Epilogue), _vp]),
     "gemm_plan_grouped": (_i32, [_vp, ctypes.c_int, _i32, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _f32, _vp,
                                  _i64, _i32, ctypes.POINTER(Plan)]),
+    "gemm_plan_cache_stats": (_i32, [_vp, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]),
     "gemm_run_host": (_i32, [_vp, _i32, _i32, _i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _i32,
                              _vp]),
     "gemm_run_block_scaled": (_i32, [_vp, _i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _f32,
@@ -198,6 +200,13 @@ class Handle:
         epi = Epilogue(bias or None, int(act), float(out_scale))
         return lib().gemm_run_grouped(self.ptr, transB, len(m_sizes), ctypes.cast(sizes, _vp), N, K, alpha, A, lda, B,
                                       ldb, strideB, beta, C, ldc, dtype, ctypes.byref(epi), stream)
+
+    def plan_cache_stats(self):
+        """(hits, misses) of the handle's plan cache."""
+        hits, misses = ctypes.c_uint64(), ctypes.c_uint64()
+        _check(lib().gemm_plan_cache_stats(self.ptr, ctypes.byref(hits), ctypes.byref(misses)),
+               "gemm_plan_cache_stats")
+        return hits.value, misses.value
 
     def run_block_scaled_raw(self, M, N, K, alpha, A, lda, SFA, ld_sfa, B, ldb, SFB, ld_sfb, beta, C, ldc, dtype,
                              stream, bias=0, act=ACT_NONE, out_scale=1.0):

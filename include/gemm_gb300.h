@@ -423,10 +423,15 @@ typedef enum {
   GEMM_OPT_KDEPTH = 11,        /* 0 auto, else 1 or 2 128-byte k-slices per ring stage (2 halves
                                   the barrier round trips per byte; falls back to 1 where the
                                   ring would hold fewer than two stages) */
-  GEMM_OPT_PDL = 12            /* 1 (default): the main kernel is launched as a programmatic
+  GEMM_OPT_PDL = 12,           /* 1 (default): the main kernel is launched as a programmatic
                                   dependent of the stream's previous kernel, so its launch and
                                   set-up overlap that kernel's end; it reads and writes memory only
                                   after the previous kernel has finished.  0: ordinary launch */
+  GEMM_OPT_PLAN_CACHE = 13     /* 1 (default): plain and strided-batched calls reuse the plan of
+                                  an earlier call with the same sizes, leading dimensions,
+                                  strides, dtype, beta, options and pointer alignments (32
+                                  plans per handle, least recently used replaced); 0: plan
+                                  every call */
 } gemm_option_t;
 
 /* Set an option on a handle.  Errors: GEMM_ERR_INVALID_ARG for an unknown
@@ -435,6 +440,10 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
 
 /* Kernels launched by gemm_run on this handle since it was created. */
 gemm_status_t gemm_launch_count(gemm_handle_t h, uint64_t* count);
+
+/* Plan-cache counters of the handle since its creation: calls whose plan was
+   reused (*hits) and calls that planned anew (*misses). */
+gemm_status_t gemm_plan_cache_stats(gemm_handle_t h, uint64_t* hits, uint64_t* misses);
 
 /* ---------------------------------------------------------------------------
  * gemm_run_noalloc: the GEMM of gemm_run for callers that must not allocate

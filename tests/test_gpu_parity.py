@@ -374,3 +374,46 @@ def test_launch_count_and_plan_agree(h):
     launch(p, h, Ad, Bd, Cd, ldc)
     assert h.status()[0] == G.OK
     assert h.launch_count() - before == plan.launches == 3
+
+
+@pytest.mark.parametrize("shape,code", [((300, 264, 200), G.BF16_F32), ((40, 1000, 512), G.BF16_BF16),
+                                        ((260, 200, 96), G.F32_F32)])
+def test_plan_cache_hits_use_the_calls_own_pointers(h, shape, code):
+    """Repeated calls of one shape on different buffers reuse the cached plan
+    (a swapped problem and the split fp32 operands included) and each writes
+    its own product; a differently aligned pointer plans anew."""
+    import oracle
+    M, N, K = shape
+    dt = torch.float32 if code == G.F32_F32 else torch.bfloat16
+    ct = torch.bfloat16 if code == G.BF16_BF16 else torch.float32
+    g = torch.Generator().manual_seed(sum(shape))
+    pairs = [(torch.randn(M, K, generator=g).to(dt), torch.randn(N, K, generator=g).to(dt)) for _ in range(3)]
+    hits0, misses0 = h.plan_cache_stats()
+    outs = []
+    for A, B in pairs:
+        Ad, Bd = A.cuda(), B.cuda()
+        C = torch.full((M, N), float("nan"), dtype=ct, device="cuda")
+        assert h.run_raw(0, 1, M, N, K, 1.0, Ad.data_ptr(), K, Bd.data_ptr(), K, 0.0, C.data_ptr(), N, code,
+                         None) == G.OK
+        torch.cuda.synchronize()
+        outs.append(C.cpu().double().numpy())
+    hits, misses = h.plan_cache_stats()
+    assert hits - hits0 >= 2 and misses - misses0 <= 1
+    # a C 4 bytes off a 16-byte boundary is a different plan (direct stores)
+    Cbig = torch.full((M * N + 4,), float("nan"), dtype=torch.float32, device="cuda")
+    Ad, Bd = pairs[0][0].cuda(), pairs[0][1].cuda()
+    if ct == torch.float32:
+        assert h.run_raw(0, 1, M, N, K, 1.0, Ad.data_ptr(), K, Bd.data_ptr(), K, 0.0, Cbig.data_ptr() + 4, N, code,
+                         None) == G.OK
+        torch.cuda.synchronize()
+        assert h.plan_cache_stats()[1] == misses + 1
+        outs_shift = Cbig[1:1 + M * N].view(M, N).cpu().double().numpy()
+        assert np.array_equal(outs_shift, outs[0])
+    for (A, B), out in zip(pairs, outs):
+        if dt == torch.float32:
+            R, Mag = oracle.gemm(0, 1, M, N, K, 1.0, A.numpy(), K, B.numpy(), K, 0.0, None, N, oracle.IN_F32)
+            assert oracle.within_tolerance(out, R, Mag, True, tf32x3_k=K).all()
+        else:
+            bits = lambda t: t.contiguous().view(torch.uint16).numpy()
+            R, Mag = oracle.gemm(0, 1, M, N, K, 1.0, bits(A), K, bits(B), K, 0.0, None, N, oracle.IN_BF16)
+            assert_close(out, R, Mag, ct == torch.float32, "plan cache")
