@@ -12,6 +12,8 @@ Also reported, in the same line:
                 host<->device copies inside the timed region
   cpu_baseline  the CPU oracle (plain fp64 triple loop) on a bounded sample
   skinny        the LM-head GEMM (M = 64, K = 4096, N = 32000) in GB/s
+  bf16_out      the same 4096^3 GEMM writing bf16 C (the other output type
+                of the square workload) in TFLOP/s
   fp8           the 4096^3 GEMM with 8-bit E4M3 inputs in TFLOP/s
   fp32          the 4096^3 fp32 GEMM from three TF32 products (and with one
                 TF32 product) in TFLOP/s of fp32 work
@@ -51,6 +53,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-skinny", action="store_true")
+    ap.add_argument("--bf16-out-steps", type=int, default=20000)
+    ap.add_argument("--no-bf16-out", action="store_true")
     ap.add_argument("--fp8-steps", type=int, default=4000)
     ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--fp32-steps", type=int, default=300)
@@ -348,13 +352,16 @@ def run_ours(args):
                 "traffic": recorded_traffic(kernel_key),
                 "peak_source": "%s %s (cuBLAS bf16; %s)" % (
                     pk_src, "bf16_tflops_sustained" if sustained else "bf16_tflops",
-                    "this run is back to back for %.1f s" % wall),
+                    "this run is back to back for %.3f s" % wall),
                 "frac_of_burst": achieved / peak_b, "frac_of_sustained": achieved / peak_s,
                 "frac_of_nominal_2250": achieved / 2250.0,
                 "kernel": "tc_gemm_kernel<BN=%d, CTA group %d>" % (plan.bn, cg), "kernel_ms": kernel_ms,
                 "algorithmic_flops_per_launch": flops,
                 "traffic_note": "DRAM bytes per launch from the committed ncu summary, if taken on these sources"}
 
+    bf16_out = None
+    if not args.no_bf16_out:
+        bf16_out = run_bf16_out(args, G, h, inputs, metrics, dev, stream, pk, pk_src)
     skinny = None
     if not args.no_skinny:
         skinny = run_skinny(args, G, h, inputs, metrics, dev, stream, pk, pk_src)
@@ -383,13 +390,62 @@ def run_ours(args):
                        "plan": plan.as_dict(), "parallelism": "replicas" if ws > 1 else "single GPU",
                        "wall_s_timed_region": wall},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clk, "skinny": skinny, "fp8": fp8, "fp32": fp32,
+            "clocks": clk, "bf16_out": bf16_out, "skinny": skinny, "fp8": fp8, "fp32": fp32,
         }
         print(json.dumps(line), flush=True)
     h.close()
     if ws > 1:
         dist.destroy_process_group()
     return 0
+
+
+def run_bf16_out(args, G, h, inputs, metrics, dev, stream, pk, pk_src):
+    """The square 4096^3 bf16 NT GEMM writing bf16 C (RNE), against the measured
+    bf16 peak: the sustained figure when the timed region lasts a second or
+    more (back to back under the power cap), else the burst figure."""
+    import torch
+    p = inputs.square_4096_bf16_nt("bf16", SIZE)
+    set_bytes = p.A.numel() * 2 + p.B.numel() * 2 + p.M * p.N * 2
+    n_sets = max(2, math.ceil(2 * L2_BYTES / set_bytes) + 1)
+    sets = [(p.A.to(dev), p.B.to(dev), torch.empty(p.M, p.N, dtype=torch.bfloat16, device=dev))
+            for _ in range(n_sets)]
+    plan = G.plan(p.M, p.N, p.K, p.transA, p.transB, G.BF16_BF16)
+    sptr = stream.cuda_stream
+
+    def step(i):
+        A, B, C = sets[i % n_sets]
+        st = h.run_raw(p.transA, p.transB, p.M, p.N, p.K, 1.0, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, 0.0,
+                       C.data_ptr(), p.N, G.BF16_BF16, sptr)
+        if st != G.OK:
+            raise G.GemmError(st, "gemm_run")
+
+    with torch.cuda.stream(stream):
+        for i in range(20):
+            step(i)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        wall0 = time.perf_counter()
+        e0.record(stream)
+        for i in range(args.bf16_out_steps):
+            step(i)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    st, word = h.status(sptr)
+    if st != G.OK:
+        raise RuntimeError("bf16-output kernel status %s (0x%x)" % (G.STATUS.get(st), word))
+    ms = e0.elapsed_time(e1) / args.bf16_out_steps
+    tflops = metrics.flops(p.M, p.N, p.K) / (ms / 1e3) / 1e12
+    sustained = wall >= 1.0
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    peak = float(pk.get(key, FALLBACK_PEAKS[key]))
+    return {"workload": "square_4096_bf16_nt_bf16", "value": tflops, "unit": "TFLOP/s", "us_per_call": ms * 1e3,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tflops / peak, "frac_of_nominal_2250": tflops / 2250.0,
+                         "peak_source": "%s %s (this leg is back to back for %.3f s)" % (pk_src, key, wall),
+                         "traffic": None},
+            "plan": plan.as_dict(), "l2": "%d rotating input sets (%.0f MB total)" % (
+                n_sets, n_sets * set_bytes / 2 ** 20)}
 
 
 def run_fp8(args, G, h, inputs, metrics, dev, stream, pk, pk_src):
