@@ -64,7 +64,8 @@ struct TcConfig {
   static constexpr int kBBytes = kQRows * kSliceBytes;
   static constexpr int kStageBytes = kABytes + kBBytes;
   // as many stages as fit in 227 KB beside the control block and alignment slack (at most 8)
-  // epilogue staging: per epilogue warp two 32-row x 128-byte buffers for bulk stores of C
+  // epilogue staging: per epilogue warp two 32-row x 128-byte buffers for C (bulk stores
+  // alternate between them; direct stores use the first)
   static constexpr int kStagingBytes = 4 * 2 * 32 * 128;
   static constexpr int kCtrlBytes = 256;
   static constexpr int kRingMax = 232448 - 1024 - kStagingBytes - 1024;  // 227 KB less the rest
@@ -73,11 +74,8 @@ struct TcConfig {
   // the last tile's epilogue stages C in the idle ring: eight 4 KB buffers per epilogue warp
   static_assert(kRingBytes >= 4 * 8 * 32 * 128, "ring too small to stage a tile of C");
   static constexpr int kTmemCols = 2 * BN;       // two fp32 accumulators of BN columns
-  // layout: [alignment slack][ring][control block, padded to 1 KB][staging]; a
-  // launch without the bulk-store epilogue requests shared memory only up to the
-  // control block, leaving the rest to L1.
-  static constexpr size_t kSmemNoStaging = 1024 + kRingBytes + 1024;
-  static constexpr size_t kSmemBytes = kSmemNoStaging + kStagingBytes;
+  // layout: [alignment slack][ring][control block, padded to 1 KB][staging]
+  static constexpr size_t kSmemBytes = 1024 + kRingBytes + 1024 + kStagingBytes;
 };
 
 struct TcCtrl {
@@ -354,9 +352,163 @@ struct EpiOut {
     ++nstore;
   }
 
+  // Stage the warp's 32 x 32 block, row `lane` from this thread, in `buf`:
+  // fp32, 128-byte rows whose 16-byte pieces are swizzled by row (piece k of
+  // row r at k ^ (r & 7)), so that neither these row writes nor the reads of
+  // one piece from 8 consecutive rows meet bank conflicts.
+  __device__ __forceinline__ void stage(uint32_t buf, const float (&v)[32]) {
+    const uint32_t row = buf + static_cast<uint32_t>(lane * 128);
+    const uint32_t sw = static_cast<uint32_t>(lane & 7);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      st_shared_v4(row + ((k ^ sw) << 4), __float_as_uint(v[4 * k]), __float_as_uint(v[4 * k + 1]),
+                   __float_as_uint(v[4 * k + 2]), __float_as_uint(v[4 * k + 3]));
+    __syncwarp();
+  }
+
+  // Direct stores when the rows of C are contiguous (unswapped problems): the
+  // warp's block goes through its staging buffer and comes back out along the
+  // rows of C, so that each global access of the warp covers whole row pieces:
+  // 16 bytes per lane where rows are 16-byte aligned and the block is whole in
+  // J, else one element per lane (32 consecutive elements of one row).  The
+  // old values for beta * C are read the same way, all of a block's loads
+  // issued (after the block is staged) before its first store.  (Written from each thread's own row, a
+  // warp's accesses fell into 32 rows and every load of C waited for the store
+  // before it: 4096^3 took 1.6 times as long with beta != 0.)
+  __device__ __forceinline__ void put_rows(int j, const float (&v)[32]) {
+    const uint32_t buf = staging;
+    const int ncols = c.J - j < 32 ? c.J - j : 32;
+    const bool whole = ncols == 32 && c.vec;
+    const bool blend = c.beta != 0.0f;
+    if (whole && c.type == kCF32) {
+      const int g = lane & 7;  // columns 4g .. 4g + 3 of rows 4p + lane / 8
+      stage(buf, v);
+      float4 x[8];
+#pragma unroll
+      for (int p = 0; p < 8; ++p) {
+        const int i = y0 + 4 * p + (lane >> 3);
+        x[p] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (blend && i < c.I)
+          x[p] = *reinterpret_cast<const float4*>(static_cast<const float*>(c.C) + static_cast<int64_t>(i) * c.si +
+                                                  j + 4 * g);
+      }
+#pragma unroll
+      for (int p = 0; p < 8; ++p) {
+        const int r = 4 * p + (lane >> 3);
+        const int i = y0 + r;
+        if (i < c.I) {
+          float4 o = ld_shared_v4_f32(buf + static_cast<uint32_t>(r * 128 + ((g ^ (r & 7)) << 4)));
+          if (blend) {
+            o.x += c.beta * x[p].x; o.y += c.beta * x[p].y; o.z += c.beta * x[p].z; o.w += c.beta * x[p].w;
+          }
+          if (c.has_ops) {
+            const int jj = j + 4 * g;
+            o.x = apply_ops(c.ops, o.x, i, jj);
+            o.y = apply_ops(c.ops, o.y, i, jj + 1);
+            o.z = apply_ops(c.ops, o.z, i, jj + 2);
+            o.w = apply_ops(c.ops, o.w, i, jj + 3);
+          }
+          *reinterpret_cast<float4*>(static_cast<float*>(c.C) + static_cast<int64_t>(i) * c.si + j + 4 * g) = o;
+        }
+      }
+    } else if (whole && c.type != kCE4M3) {  // 16-bit C
+      const int g = lane & 3;  // columns 8g .. 8g + 7 (staged pieces 2g, 2g + 1) of rows 8p + lane / 4
+      stage(buf, v);
+      uint4 x[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const int i = y0 + 8 * p + (lane >> 2);
+        x[p] = make_uint4(0u, 0u, 0u, 0u);
+        if (blend && i < c.I)
+          x[p] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(c.C) + static_cast<int64_t>(i) * c.si +
+                                                 j + 8 * g);
+      }
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const int r = 8 * p + (lane >> 2);
+        const int i = y0 + r;
+        if (i < c.I) {
+          const float4 a0 = ld_shared_v4_f32(buf + static_cast<uint32_t>(r * 128 + (((2 * g) ^ (r & 7)) << 4)));
+          const float4 a1 = ld_shared_v4_f32(buf + static_cast<uint32_t>(r * 128 + (((2 * g + 1) ^ (r & 7)) << 4)));
+          float o[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+          if (blend) {
+            const uint32_t xw[4] = {x[p].x, x[p].y, x[p].z, x[p].w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const float2 f = unpack2(c.type, xw[t]);
+              o[2 * t] += c.beta * f.x;
+              o[2 * t + 1] += c.beta * f.y;
+            }
+          }
+          if (c.has_ops) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t) o[t] = apply_ops(c.ops, o[t], i, j + 8 * g + t);
+          }
+          *reinterpret_cast<uint4*>(static_cast<uint16_t*>(c.C) + static_cast<int64_t>(i) * c.si + j + 8 * g) =
+              make_uint4(pack2(c.type, o[0], o[1]), pack2(c.type, o[2], o[3]), pack2(c.type, o[4], o[5]),
+                         pack2(c.type, o[6], o[7]));
+        }
+      }
+    } else if (whole) {  // 8-bit C (written only: beta == 0)
+      const int g = lane & 1;  // columns 16g .. 16g + 15 (staged pieces 4g .. 4g + 3) of rows 16p + lane / 2
+      stage(buf, v);
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        const int r = 16 * p + (lane >> 1);
+        const int i = y0 + r;
+        if (i < c.I) {
+          uint32_t w[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float4 f = ld_shared_v4_f32(buf + static_cast<uint32_t>(r * 128 + (((4 * g + k) ^ (r & 7)) << 4)));
+            float o[4] = {f.x, f.y, f.z, f.w};
+            uint32_t b = 0;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const float z = c.has_ops ? apply_ops(c.ops, o[t], i, j + 16 * g + 4 * k + t) : o[t];
+              b |= static_cast<uint32_t>(to_e4m3(z)) << (8 * t);
+            }
+            w[k] = b;
+          }
+          *reinterpret_cast<uint4*>(static_cast<uint8_t*>(c.C) + static_cast<int64_t>(i) * c.si + j + 16 * g) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    } else {  // misaligned rows, or the block's last columns lie past J
+      // (eight rows at a time: the old values of eight rows in flight together)
+      stage(buf, v);
+#pragma unroll 1
+      for (int r0 = 0; r0 < 32; r0 += 8) {
+        float x[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const int i = y0 + r0 + t;
+          x[t] = 0.0f;
+          if (blend && i < c.I && lane < ncols) x[t] = load_c(c, static_cast<int64_t>(i) * c.si + j + lane);
+        }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const int r = r0 + t;
+          const int i = y0 + r;
+          if (i < c.I && lane < ncols) {
+            float o = ld_shared_f32(buf + static_cast<uint32_t>(r * 128 + ((((lane >> 2) ^ (r & 7)) << 4) |
+                                                                            ((lane & 3) << 2))));
+            if (blend) o += c.beta * x[t];
+            if (c.has_ops) o = apply_ops(c.ops, o, i, j + lane);
+            store_c(c, static_cast<int64_t>(i) * c.si + j + lane, o);
+          }
+        }
+      }
+    }
+    __syncwarp();  // every lane has read the block before the next one is staged
+  }
+
   __device__ __forceinline__ void put(int i, int j, const float (&vin)[32], int half) {
     if (c.tma == kBulkNone) {
-      store_chunk(c, i, j, vin);
+      if (c.sj == 1)
+        put_rows(j, vin);
+      else  // swapped problems: consecutive lanes already hold consecutive elements of C
+        store_chunk(c, i, j, vin);
       return;
     }
     // bulk paths run with beta == 0: the fused operations apply to alpha * D,
@@ -656,6 +808,7 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
   out.lane = lane;
   out.nstore = 0;
   out.ring = false;
+  const int64_t esize = a.c_type == kCF32 ? 4 : a.c_type == kCE4M3 ? 1 : 2;
   int it = 0;
   WorkIter work(a.sched, first, stride);
   Unit w;
@@ -689,7 +842,6 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
     out.y0 = w.ti * Cfg::kTileM + q * kBM + quarter * 32;
     out.z = w.tb;
     {
-      const int64_t esize = a.c_type == kCF32 ? 4 : a.c_type == kCE4M3 ? 1 : 2;
       if (a.sched.groups > 0) {  // the group's rows of C; rows past its count are not stored
         out.c.C = static_cast<char*>(out.c0) + a.group_row[w.tb] * a.c_si * esize;
         out.c.I = a.group_m[w.tb];
@@ -837,7 +989,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* ring_a = smem;
   uint8_t* ring_b = smem + Cfg::kStages * Cfg::kABytes;
   TcCtrl* ctrl = reinterpret_cast<TcCtrl*>(smem + Cfg::kRingBytes);
-  uint8_t* staging = smem + Cfg::kRingBytes + 1024;  // 1024-byte aligned; requested only with tma_store
+  uint8_t* staging = smem + Cfg::kRingBytes + 1024;  // 1024-byte aligned
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;

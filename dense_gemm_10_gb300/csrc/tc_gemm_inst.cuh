@@ -34,7 +34,7 @@ cudaError_t TC_NAME(tc_launch_bn, TC_BN, _cg, TC_CG, _mc, TC_MC, _eb, TC_EB)(
     const CUtensorMap& map_p, const CUtensorMap& map_q, const CUtensorMap& map_c, const TcArgs& args,
     int grid, cudaStream_t stream) {
   using Cfg = TcConfig<TC_BN, TC_CG, TC_MC>;
-  const size_t smem = args.tma_store ? Cfg::kSmemBytes : Cfg::kSmemNoStaging;
+  const size_t smem = Cfg::kSmemBytes;  // every epilogue stages C (bulk or direct stores)
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   unsigned n = 0;
