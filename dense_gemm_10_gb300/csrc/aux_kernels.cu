@@ -2,6 +2,8 @@
 //  * repack: copies an operand whose rows are not 16-byte aligned into
 //    an aligned buffer, because the tensor-memory-accelerator copy engine only
 //    reads rows whose pitch is a multiple of 16 bytes;
+//  * unstage_c: the other way for C: the aligned copy that bulk stores wrote
+//    goes into C's own rows;
 //  * split_tf32: writes an fp32 operand K-major as TF32 values for the TF32
 //    tensor-core kind ("GPU GEMM 优化完全拆解（三）", 数值精度).  One part: the
 //    value cut to TF32 (sign, 8-bit exponent, top 10 fraction bits), as the
@@ -240,6 +242,60 @@ cudaError_t repack_launch(const void* src, int64_t lds, int64_t sbs, void* dst, 
   else
     repack_kernel<uint16_t><<<g, 256, 0, stream>>>(static_cast<const uint16_t*>(src), lds, sbs,
                                                    static_cast<uint16_t*>(dst), ldd, dbs, rows, cols, nb);
+  return cudaGetLastError();
+}
+
+// The aligned copy of C (rows of lds elements, 16-byte aligned) into C: one
+// thread per 16-byte piece of four rows, the four pieces loaded before any
+// element is stored (a thread that moved one element at a time kept one load
+// in flight and ran at a third of the HBM bandwidth); the elements go out one
+// by one, since C's rows may start anywhere.  Pieces past `cols` are read (the
+// aligned rows hold them) but not written.
+template <typename T>
+__global__ void __launch_bounds__(256) unstage_c_kernel(const T* __restrict__ src, int64_t lds, T* __restrict__ dst,
+                                                        int64_t ldd, int64_t rows, int64_t cols) {
+  constexpr int kV = 16 / sizeof(T);
+  constexpr int kRows = 4;
+  const int64_t c = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * kV;
+  if (c >= cols) return;
+  const int nv = cols - c < kV ? static_cast<int>(cols - c) : kV;
+  for (int64_t r0 = static_cast<int64_t>(blockIdx.y) * kRows; r0 < rows; r0 += static_cast<int64_t>(gridDim.y) * kRows) {
+    const int nr = rows - r0 < kRows ? static_cast<int>(rows - r0) : kRows;
+    uint4 x[kRows];
+#pragma unroll
+    for (int u = 0; u < kRows; ++u)
+      if (u < nr) x[u] = *reinterpret_cast<const uint4*>(src + (r0 + u) * lds + c);
+#pragma unroll
+    for (int u = 0; u < kRows; ++u) {
+      if (u < nr) {
+        const T* e = reinterpret_cast<const T*>(&x[u]);
+        T* d = dst + (r0 + u) * ldd + c;
+#pragma unroll
+        for (int t = 0; t < kV; ++t)
+          if (t < nv) d[t] = e[t];
+      }
+    }
+  }
+}
+
+cudaError_t unstage_c_launch(const void* src, int64_t lds, void* dst, int64_t ldd, int64_t rows, int64_t cols,
+                             int esize, cudaStream_t stream) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  if ((reinterpret_cast<uintptr_t>(src) % 16) != 0 || (lds * esize) % 16 != 0) return cudaErrorInvalidValue;
+  const int64_t pieces = (cols * esize + 15) / 16;
+  const int64_t gx = (pieces + 255) / 256;
+  int64_t gy = (rows + 3) / 4;
+  if (gy > 65535) gy = 65535;
+  if (gx > 0x7fffffff) return cudaErrorInvalidValue;
+  const dim3 g(static_cast<unsigned>(gx), static_cast<unsigned>(gy), 1);
+  if (esize == 4)
+    unstage_c_kernel<uint32_t><<<g, 256, 0, stream>>>(static_cast<const uint32_t*>(src), lds,
+                                                      static_cast<uint32_t*>(dst), ldd, rows, cols);
+  else if (esize == 2)
+    unstage_c_kernel<uint16_t><<<g, 256, 0, stream>>>(static_cast<const uint16_t*>(src), lds,
+                                                      static_cast<uint16_t*>(dst), ldd, rows, cols);
+  else
+    return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 

@@ -45,6 +45,7 @@ struct Options {
   int kdepth = 0;    // GEMM_OPT_KDEPTH: 0 auto, else 64-wide k-slices per ring stage
   int pdl = 1;       // GEMM_OPT_PDL: programmatic dependent launch of the main kernel
   int plan_cache = 1;  // GEMM_OPT_PLAN_CACHE: reuse the plans of recent calls
+  bool stage_c = true; // C that bulk stores cannot write may go through an aligned copy
 };
 
 // One stored operand, as the tensor-memory-accelerator copy engine will see it.
@@ -94,6 +95,12 @@ struct Plan {
   int32_t in_dtype = 0;            // CU_TENSOR_MAP data type of A and B
   int cfg = 0;                     // index into kTileConfigs
   size_t partial_offset = 0;
+  // C staged in the workspace (bulk_store == GEMM_BULK_STAGED): the kernel's
+  // bulk stores write an aligned copy, rows of c_ws_ld elements, which a copy
+  // kernel then writes into C
+  bool c_staged = false;
+  int64_t c_ws_ld = 0;
+  size_t c_ws_offset = 0;
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -571,7 +578,6 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
     pl.partial_offset = ws;
     ws = round_up(ws + static_cast<size_t>(partial_slots(pl.sched)) * cl * best.bn * kBM * 4, 256);
   }
-  P.workspace_bytes = static_cast<int64_t>(ws);
   const bool c_rows_aligned = reinterpret_cast<uintptr_t>(C) % 16 == 0 && (ldc * c_elem) % 16 == 0 &&
                               (pl.c_sb * c_elem) % 16 == 0;
   P.vector_store = (!swap && c_rows_aligned) ? 1 : 0;
@@ -586,6 +592,23 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   pl.tma_store = !bulk ? kBulkNone : swap ? kBulkTransposed : kBulkRows;
   P.bulk_store = pl.tma_store;
   P.launches = 1 + P.repack_a + P.repack_b;
+  // A large C whose rows bulk stores cannot write (misaligned rows, or a width
+  // that ends inside a 16-byte piece, which a bulk store would write whole):
+  // the kernel writes an aligned copy in the workspace with bulk stores, and a
+  // copy kernel moves it into C.  Direct stores cost more than that second pass
+  // (4096 x 4097 x 1000: 80 us with direct stores, 40 us with bulk stores).
+  if (!bulk && o.stage_c && o.tma_store != 2 && beta == 0.0f && !swap && groups == 0 && pl.batch == 1 &&
+      pl.c_type != kCE4M3 && M * N >= (int64_t{1} << 20)) {
+    pl.c_staged = true;
+    pl.c_ws_ld = static_cast<int64_t>(round_up(static_cast<size_t>(N), static_cast<size_t>(16 / c_elem)));
+    pl.c_ws_offset = ws;
+    ws = round_up(ws + static_cast<size_t>(M) * pl.c_ws_ld * c_elem, 256);
+    pl.tma_store = kBulkRows;
+    P.bulk_store = GEMM_BULK_STAGED;
+    P.vector_store = 1;
+    P.launches += 1;
+  }
+  P.workspace_bytes = static_cast<int64_t>(ws);
   *out = pl;
   if (out->sched.groups > 0) out->sched.group_tile_start = out->group_tiles.data();  // the copy's own table
   return GEMM_OK;
@@ -1050,10 +1073,14 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
   if (s != GEMM_OK) return s;
   CUtensorMap map_c;
   std::memset(&map_c, 0, sizeof(map_c));
+  // (staged C: the kernel writes the aligned copy, whole rows of c_ws_ld elements)
+  void* c_out = pl.c_staged ? static_cast<void*>(ws + pl.c_ws_offset) : C;
+  const int64_t c_ld = pl.c_staged ? pl.c_ws_ld : ldc;
   if (pl.tma_store != kBulkNone) {
     // C as stored: I x J, or J x I for a swapped problem
-    s = pl.tma_store == kBulkRows ? encode_c(&map_c, C, pl.I, pl.J, ldc, pl.c_type, false, pl.batch, pl.c_sb)
-                                  : encode_c(&map_c, C, pl.J, pl.I, ldc, pl.c_type, true, pl.batch, pl.c_sb);
+    s = pl.tma_store == kBulkRows
+            ? encode_c(&map_c, c_out, pl.I, pl.c_staged ? pl.c_ws_ld : pl.J, c_ld, pl.c_type, false, pl.batch, pl.c_sb)
+            : encode_c(&map_c, C, pl.J, pl.I, ldc, pl.c_type, true, pl.batch, pl.c_sb);
     if (s != GEMM_OK) return s;
   }
 
@@ -1070,8 +1097,8 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
   a.idesc = make_idesc(pl.a_fmt, pl.b_fmt, !pl.p.kmajor, !pl.q.kmajor, kBM * cg, P.bn);
   a.alpha = alpha;
   a.beta = beta;
-  a.C = C;
-  a.c_si = pl.c_si;
+  a.C = c_out;
+  a.c_si = pl.c_staged ? pl.c_ws_ld : pl.c_si;
   a.c_sj = pl.c_sj;
   a.c_sb = pl.c_sb;
   a.p_bcast = pl.p.nb == 1 ? 1 : 0;
@@ -1109,6 +1136,12 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
   e = tc_launch(pl.cfg, map_p, map_q, map_c, a, P.grid, st);
   if (e != cudaSuccess) return cuda_fail(h, e);
   h->launches += 1;
+  if (pl.c_staged) {  // the aligned copy's M x N elements into C
+    const int c_elem = pl.c_type == kCF32 ? 4 : 2;
+    e = unstage_c_launch(c_out, pl.c_ws_ld, C, ldc, pl.I, pl.J, c_elem, st);
+    if (e != cudaSuccess) return cuda_fail(h, e);
+    h->launches += 1;
+  }
   return GEMM_OK;
 }
 
@@ -1435,6 +1468,7 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   gemm_status_t s = noalloc_setup(device, &d);
   if (s != GEMM_OK) return s;
   Options o;
+  o.stage_c = false;  // no room for a copy of C in the fixed scratch
   Plan pl;
   s = make_plan(o, d->slots, transA, transB, M, N, K, A, lda, B, ldb, beta, C, ldc, dtype, &pl);
   if (s != GEMM_OK) return s;

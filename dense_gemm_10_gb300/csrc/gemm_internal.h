@@ -107,6 +107,13 @@ cudaError_t repack_launch(const void* src, int64_t lds, int64_t sbs, void* dst, 
                           int64_t rows, int64_t cols, int64_t nb, int esize, int sm_count,
                           cudaStream_t stream);
 
+// dst[r * ldd + c] = src[r * lds + c] for r < rows, c < cols, elements of
+// esize (2 or 4) bytes; src 16-byte aligned with 16-byte rows (lds * esize a
+// multiple of 16) that hold whole 16-byte pieces past cols.  Nothing outside
+// dst's rows x cols elements is written.
+cudaError_t unstage_c_launch(const void* src, int64_t lds, void* dst, int64_t ldd, int64_t rows, int64_t cols,
+                             int esize, cudaStream_t stream);
+
 // TF32 values of fp32 operands, written K-major: row r of dst (b-th matrix at
 // dbs elements) receives parts segments of seg values (seg >= K; values K ..
 // seg - 1 of a segment are 0).  parts == 1: each value with its 13 low fraction

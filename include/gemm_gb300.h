@@ -265,6 +265,18 @@ typedef enum {
                                      neighbouring tiles sharing the A-side tile by TMA multicast */
 } gemm_path_t;
 
+/* How C leaves the epilogue (gemm_plan_t.bulk_store). */
+typedef enum {
+  GEMM_BULK_NONE = 0,       /* direct stores by the epilogue warps (beta != 0, 8-bit C, grouped GEMMs,
+                               small C that bulk stores cannot write) */
+  GEMM_BULK_ROWS = 1,       /* bulk tensor stores of rows of C */
+  GEMM_BULK_TRANSPOSED = 2, /* bulk tensor stores of transposed blocks (swapped problems) */
+  GEMM_BULK_STAGED = 3      /* C's rows are misaligned, or end inside a 16-byte piece: bulk tensor
+                               stores write an aligned copy of C in the handle's workspace and a copy
+                               kernel then writes C's M x N elements (one more launch; beta == 0,
+                               unswapped, one GEMM, M * N >= 2^20) */
+} gemm_bulk_store_t;
+
 typedef struct {
   int32_t path;            /* gemm_path_t */
   int32_t swap_ab;         /* 1: the kernel computes C^T = op(B)^T * op(A)^T */
@@ -294,8 +306,7 @@ typedef struct {
   int32_t cluster;         /* CTAs per schedule slot: 1, 2 (a pair) or 4 (two pairs, multicast) */
   int32_t kdepth;          /* 128-byte k-slices per ring stage (1 or 2): each stage's copies
                               complete one barrier */
-  int32_t bulk_store;      /* how C leaves: 0 direct stores, 1 bulk tensor stores of rows,
-                              2 bulk tensor stores of transposed blocks (swapped problems) */
+  int32_t bulk_store;      /* how C leaves: gemm_bulk_store_t */
   int32_t batch;           /* GEMMs in the call (1 unless strided batched); tiles counts all */
 } gemm_plan_t;
 

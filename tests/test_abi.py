@@ -144,6 +144,25 @@ def test_plan_bulk_store_paths():
     assert G.plan(40, 1001, 256, 0, 1, G.BF16_BF16, ldc=1008).bulk_store == G.BULK_NONE
 
 
+def test_plan_staged_c():
+    """A large C that bulk stores cannot write (misaligned rows, or rows ending
+    inside a 16-byte piece) goes through an aligned copy in the workspace: one
+    more launch and M x round_up(N, 16 bytes) elements of workspace.  beta != 0,
+    8-bit C, swapped problems and C under 2^20 elements keep direct stores."""
+    p = G.plan(4095, 4097, 1000, 0, 0, ldb=4097, ldc=4097)       # the ragged 4095 x 4097 x 1000 workload
+    assert p.bulk_store == G.BULK_STAGED and p.launches == 3 and p.repack_b == 1
+    assert p.workspace_bytes >= 4095 * 4100 * 4
+    p = G.plan(2048, 1001, 512, 0, 1, ldc=1008)                 # aligned rows ending inside a piece
+    assert p.bulk_store == G.BULK_STAGED and p.launches == 2
+    p = G.plan(2048, 1024, 512, 0, 1, G.BF16_BF16, C=0x1002)    # misaligned base
+    assert p.bulk_store == G.BULK_STAGED
+    assert G.plan(2048, 1001, 512, 0, 1, ldc=1008, beta=0.5).bulk_store == G.BULK_NONE
+    assert G.plan(2048, 1001, 512, 0, 1, G.fp8_dtype("e4m3", "e4m3", "e4m3"), ldc=1008).bulk_store == G.BULK_NONE
+    assert G.plan(1000, 1001, 512, 0, 1, ldc=1008).bulk_store == G.BULK_NONE   # under 2^20 elements
+    assert G.plan(64, 32001, 4096, 0, 1, ldc=32008).swap_ab == 1
+    assert G.plan(64, 32001, 4096, 0, 1, ldc=32008).bulk_store == G.BULK_NONE  # swapped
+
+
 def test_plan_fp8():
     """8-bit inputs: 128-element k-slices (one 128-byte swizzle row), the 8-bit
     tile configurations, rows aligned to 16 elements, and K-major operands only."""
@@ -287,9 +306,11 @@ def test_plan_full_waves_need_no_stream_k():
 def test_plan_ragged_repacks_misaligned_b():
     p = G.plan(4095, 4097, 1000, 0, 0, lda=1000, ldb=4097, ldc=4097)
     assert p.repack_a == 0 and p.repack_b == 1
-    assert p.launches == 2
-    assert p.vector_store == 0          # 4097 fp32 = 16388-byte rows
-    assert p.workspace_bytes >= 1000 * 4104 * 2
+    # 4097 fp32 = 16388-byte rows: C goes through an aligned copy (repack, GEMM, copy into C)
+    assert p.launches == 3 and p.bulk_store == G.BULK_STAGED
+    assert p.workspace_bytes >= 1000 * 4104 * 2 + 4095 * 4100 * 4
+    with_direct = G.plan(4095, 4097, 1000, 0, 0, lda=1000, ldb=4097, ldc=4097, beta=1.0)
+    assert with_direct.launches == 2 and with_direct.vector_store == 0 and with_direct.bulk_store == G.BULK_NONE
 
 
 def test_plan_misaligned_pointer_repacks():

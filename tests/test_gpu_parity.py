@@ -198,6 +198,46 @@ OUT_TYPES = [("bf16", "f32"), ("bf16", "bf16"), ("f16", "f16")]
 
 
 @pytest.mark.parametrize("in_dtype,out_dtype", OUT_TYPES)
+@pytest.mark.parametrize("M,N,K,transB,guard_cols", [
+    (1100, 1001, 300, 1, 5),    # misaligned rows (ldc = 1006), ragged N
+    (1030, 1024, 200, 0, 3),    # misaligned rows, N whole pieces
+    (1500, 1003, 96, 1, 13),    # rows aligned for 16-bit C only (ldc = 1016), N ends inside a piece
+])
+def test_staged_c(h, M, N, K, transB, guard_cols, in_dtype, out_dtype):
+    """C that bulk stores cannot write goes through an aligned copy in the
+    workspace, then a copy kernel: exact values where they belong, and nothing
+    written in C's padding columns or the guard rows below it."""
+    p = inputs.make_problem("staged", M, N, K, 0, transB, in_dtype, out_dtype, ("normal", 0, 1), ("normal", 0, 1),
+                            alpha=0.5, seed=M + N + guard_cols)
+    plan = G.plan(p.M, p.N, p.K, p.transA, p.transB, dtype_code(p), handle=h, ldc=p.ldc + guard_cols)
+    aligned = ((p.ldc + guard_cols) * (4 if out_dtype == "f32" else 2)) % 16 == 0
+    whole = (N * (4 if out_dtype == "f32" else 2)) % 16 == 0
+    assert plan.bulk_store == (G.BULK_ROWS if aligned and whole else G.BULK_STAGED), plan.as_dict()
+    out, full = run(p, h, guard_rows=3, guard_cols=guard_cols)
+    R, Mag = oracle_full(p)
+    assert_close(out, R, Mag, p.out_dtype == "f32", p.name)
+    pad = full.clone().to(torch.float64)
+    pad[:p.M, :p.N] = SENTINEL
+    assert torch.all(pad == SENTINEL), "C written outside the M x N block"
+
+
+def test_staged_c_in_sequence(h):
+    """Staged calls of different sizes in a row on one stream share the
+    workspace copy of C; each one's C is complete when the stream is."""
+    outs = []
+    for i, (M, N, K) in enumerate([(1200, 1001, 128), (2100, 999, 64), (1100, 1001, 256)]):
+        p = inputs.make_problem("staged_seq%d" % i, M, N, K, 0, 1, "bf16", "f32", ("normal", 0, 1),
+                                ("normal", 0, 1), seed=40 + i)
+        Ad, Bd, Cd, ldc = device_problem(p, guard_rows=1, guard_cols=1)
+        launch(p, h, Ad, Bd, Cd, ldc)
+        outs.append((p, Cd))
+    assert h.status()[0] == G.OK
+    for p, Cd in outs:
+        R, Mag = oracle_full(p)
+        assert_close(Cd[:p.M, :p.N].double().cpu().numpy(), R, Mag, True, p.name)
+
+
+@pytest.mark.parametrize("in_dtype,out_dtype", OUT_TYPES)
 @pytest.mark.parametrize("grid", [0, 6])
 @pytest.mark.parametrize("cg,bn", CONFIGS)
 def test_bulk_store_rows(h, cg, bn, grid, in_dtype, out_dtype):
