@@ -118,6 +118,17 @@ def test_direct_store_with_blend(h, act, transA, transB):
     check(p, h, bias_for(p.N, 3), act, 2.0, guard_cols=5, expect_bulk=G.BULK_NONE)
 
 
+@pytest.mark.parametrize("act", ACTS)
+@pytest.mark.parametrize("out,guard", [("f32", 5), ("bf16", 3), ("f32", 7)])
+def test_staged_c(h, act, out, guard):
+    """Large C whose rows bulk stores cannot write (misaligned, or ending inside
+    a 16-byte piece): the operations ride on the bulk stores into the aligned
+    copy, which the copy kernel then writes into C, M x N elements only."""
+    p = inputs.make_problem("epi_staged", 1100, 1001, 300, 0, 1, "bf16", out, ("normal", 0, 1), ("normal", 0, 1),
+                            alpha=0.5, seed=40 + act + guard)
+    check(p, h, bias_for(p.N, 5), act, 0.75, guard_cols=guard, expect_bulk=G.BULK_STAGED)
+
+
 @pytest.mark.parametrize("sched", ["split", "stream_k"])
 def test_fix_up_paths(h, sched):
     """Split tiles: the operations apply once, to the summed tile, never to partials."""
