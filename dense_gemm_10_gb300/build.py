@@ -24,7 +24,7 @@ SOURCES = ["gemm_api.cu", "tc_dispatch.cu", "tc_gemm_bn64_cg1_mc1.cu", "tc_gemm_
            "tc_gemm_bn256_cg2_mc1_f8.cu", "tc_gemm_bn64_cg1_mc1_tf32.cu", "tc_gemm_bn128_cg1_mc1_tf32.cu",
            "tc_gemm_bn256_cg2_mc1_tf32.cu",
            "tc_gemm_bn256_cg1_mc1.cu", "tc_gemm_bn128_cg2_mc1.cu", "tc_gemm_bn256_cg2_mc1.cu",
-           "tc_gemm_bn256_cg2_mc2.cu", "tc_gemm_bn64_cg2_mc1.cu", "aux_kernels.cu"]
+           "tc_gemm_bn256_cg2_mc2.cu", "tc_gemm_bn64_cg2_mc1.cu", "aux_kernels.cu", "probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-I" + os.path.join(ROOT, "include")]

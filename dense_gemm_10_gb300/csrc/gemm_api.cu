@@ -1368,6 +1368,30 @@ gemm_status_t gemm_run_strided_batched(gemm_handle_t h, gemm_op_t transA, gemm_o
                   strideA, strideB, strideC);
 }
 
+gemm_status_t gemm_probe_tma_tile(gemm_handle_t h, const void* src, int64_t ld, int64_t cols, int64_t rows, void* dst,
+                                  void* stream) {
+  if (!h || !src || !dst || rows < 1 || rows > 256 || cols < 1 || ld < cols) return GEMM_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(src) % 16 != 0 || (ld * 2) % 16 != 0) return GEMM_ERR_INVALID_ARG;
+  auto fn = encode_fn();
+  if (!fn) return GEMM_ERR_TENSORMAP;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), 1};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2),
+                           static_cast<cuuint64_t>(round_up(static_cast<size_t>(rows * ld * 2), 16))};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUtensorMap map;
+  CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(src), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return GEMM_ERR_TENSORMAP;
+  DeviceGuard g(h->device);
+  cudaError_t e = tma_tile_probe_launch(map, static_cast<int>(rows), static_cast<uint16_t*>(dst), h->d_status,
+                                        static_cast<uint64_t>(h->opt.wait_limit_ns), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  h->launches += 1;
+  return GEMM_OK;
+}
+
 gemm_status_t gemm_get_status(gemm_handle_t h, void* stream, int32_t* detail) {
   if (!h) return GEMM_ERR_INVALID_ARG;
   DeviceGuard g(h->device);

@@ -107,6 +107,11 @@ cudaError_t repack_launch(const void* src, int64_t lds, int64_t sbs, void* dst, 
                           int64_t rows, int64_t cols, int64_t nb, int esize, int sm_count,
                           cudaStream_t stream);
 
+// One 128-byte-swizzled tile load (box 64 x rows of 16-bit elements) into
+// shared memory, written back out in shared-memory order (probe.cu).
+cudaError_t tma_tile_probe_launch(const CUtensorMap& map, int rows, uint16_t* dst, int32_t* status,
+                                  uint64_t wait_limit_ns, cudaStream_t stream);
+
 // dst[r * ldd + c] = src[r * lds + c] for r < rows, c < cols, elements of
 // esize (2 or 4) bytes; src 16-byte aligned with 16-byte rows (lds * esize a
 // multiple of 16) that hold whole 16-byte pieces past cols.  Nothing outside

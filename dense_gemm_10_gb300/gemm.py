@@ -92,6 +92,7 @@ SIGNATURES = {
     "gemm_plan_grouped": (_i32, [_vp, ctypes.c_int, _i32, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _f32, _vp,
                                  _i64, _i32, ctypes.POINTER(Plan)]),
     "gemm_plan_cache_stats": (_i32, [_vp, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]),
+    "gemm_probe_tma_tile": (_i32, [_vp, _vp, _i64, _i64, _i64, _vp, _vp]),
     "gemm_run_host": (_i32, [_vp, _i32, _i32, _i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _i32,
                              _vp]),
     "gemm_run_block_scaled": (_i32, [_vp, _i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _f32,

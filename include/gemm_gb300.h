@@ -456,6 +456,27 @@ gemm_status_t gemm_launch_count(gemm_handle_t h, uint64_t* count);
    reused (*hits) and calls that planned anew (*misses). */
 gemm_status_t gemm_plan_cache_stats(gemm_handle_t h, uint64_t* hits, uint64_t* misses);
 
+/*
+ * gemm_probe_tma_tile (test support): load one tile of a row-major 16-bit
+ * matrix into shared memory exactly as the GEMM loads a K-major operand tile
+ * (a tensor-memory-accelerator copy with the 128-byte swizzle; box of 64
+ * elements = 128 bytes by `rows` rows, starting at element (0, 0)), then copy
+ * the tile's shared-memory bytes unchanged to `dst`: rows * 64 16-bit values
+ * in shared-memory order, so that dst[p] is the element the copy engine put at
+ * 16-bit position p.  Elements past `cols` arrive as zeros.  The layout the
+ * MMA descriptors assume is element (r, c) at r * 64 + (c ^ ((r & 7) << 3))
+ * ("[CUDA 优化实战] hgemm sm120 - 100KB SMEM 中的“微雕”战争", section 4).
+ *   src: device pointer, 16-byte aligned; ld (elements, >= cols) with ld * 2 a
+ *        multiple of 16; 1 <= rows <= 256; cols >= 1.
+ *   dst: device pointer to rows * 64 uint16 values (caller-owned).
+ * Asynchronous on `stream`.  GEMM_ERR_INVALID_ARG for a bad argument (checked
+ * before any CUDA call), GEMM_ERR_TENSORMAP if the tile cannot be described,
+ * GEMM_ERR_CUDA on a launch failure; a copy that never lands is reported by
+ * gemm_get_status as GEMM_ERR_TIMEOUT.
+ */
+gemm_status_t gemm_probe_tma_tile(gemm_handle_t h, const void* src, int64_t ld, int64_t cols, int64_t rows, void* dst,
+                                  void* stream);
+
 /* ---------------------------------------------------------------------------
  * gemm_run_noalloc: the GEMM of gemm_run for callers that must not allocate
  * device memory -- for example a caller whose device memory is fully reserved

@@ -363,3 +363,16 @@ def test_plan_invariants(shape):
             assert p.grid == min(p.units, slots) * p.cluster
         assert 1 <= p.split_k <= max(1, p.num_kb)
         assert 1 <= p.raster_group <= max(1, -(-I // p.bm))
+
+
+def test_probe_tma_tile_rejects_bad_arguments():
+    """The swizzle probe checks its arguments before any CUDA call."""
+    L = G.lib()
+    fake = ctypes.c_void_p(0x1000)   # never dereferenced: every call below fails its checks
+    assert L.gemm_probe_tma_tile(None, 0x1000, 64, 64, 8, 0x2000, None) == G.ERR_INVALID_ARG
+    assert L.gemm_probe_tma_tile(fake, 0x1000, 64, 64, 0, 0x2000, None) == G.ERR_INVALID_ARG    # rows < 1
+    assert L.gemm_probe_tma_tile(fake, 0x1000, 64, 64, 257, 0x2000, None) == G.ERR_INVALID_ARG  # rows > 256
+    assert L.gemm_probe_tma_tile(fake, 0x1002, 64, 64, 8, 0x2000, None) == G.ERR_INVALID_ARG   # misaligned
+    assert L.gemm_probe_tma_tile(fake, 0x1000, 60, 60, 8, 0x2000, None) == G.ERR_INVALID_ARG    # 120-byte rows
+    assert L.gemm_probe_tma_tile(fake, 0x1000, 32, 64, 8, 0x2000, None) == G.ERR_INVALID_ARG    # ld < cols
+    assert L.gemm_probe_tma_tile(fake, 0x1000, 64, 64, 8, None, None) == G.ERR_INVALID_ARG
