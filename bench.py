@@ -225,12 +225,12 @@ class ClockSampler:
 
 def kernel_source_hash():
     """Hash of the sources that decide what the tensor-core kernel does: its
-    code, its instantiations and the planner (aux_kernels.cu, the copy and
-    conversion kernels beside it, is left out)."""
+    code, its instantiations and the planner (the copy and conversion kernels
+    of aux_kernels.cu and the swizzle probe of probe.cu are left out)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_gemm_10_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")) and f != "aux_kernels.cu":
+        if f.endswith((".cu", ".cuh", ".h")) and f not in ("aux_kernels.cu", "probe.cu"):
             h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
