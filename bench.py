@@ -6,18 +6,19 @@ entries N(0, 1)/sqrt(K), fp32 output, alpha 1, beta 0.  The metric is TFLOP/s
 (2*M*N*K per step).  Steps rotate over several input sets whose total exceeds
 the L2 cache, so no step starts with its operands in L2.
 
-Also reported, in the same line:
+Also reported, in the same line (kept under 2 KB; --detail FILE writes every
+leg's plan, timings and notes to a file):
   roofline      the GEMM kernel's achieved TFLOP/s against the measured bf16 peak
   e2e           the same metric through the public API with host buffers, the
                 host<->device copies inside the timed region
   cpu_baseline  the CPU oracle (plain fp64 triple loop) on a bounded sample
-  skinny        the LM-head GEMM (M = 64, K = 4096, N = 32000) in GB/s
-  bf16_out      the same 4096^3 GEMM writing bf16 C (the other output type
-                of the square workload) in TFLOP/s
-  fp8           the 4096^3 GEMM with 8-bit E4M3 inputs in TFLOP/s
-  fp32          the 4096^3 fp32 GEMM from three TF32 products (and with one
-                TF32 product) in TFLOP/s of fp32 work
   clocks        SM clocks and throttle reasons sampled during the timed region
+  legs          the other workloads, each [value, fraction of its roofline]:
+                c1 256^3 (device and host microseconds per call), c2 the
+                4096^3 workload with bf16 C, c3 4096^3 fp16 alpha 1.5 beta 0.5
+                in four layouts, c4 the LLM projections (QKV, FFN-up,
+                FFN-down, NN) and the ragged 4095 x 4097 x 1000, c5 the LM head
+                64 x 32000 x 4096 in GB/s, and the FP8 and fp32 GEMMs at 4096^3
 
 `--impl reference` times the CPU oracle instead (the reference arm).
 Under torchrun every rank runs its own replica (the GEMM does not exchange
@@ -49,17 +50,20 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=40)
-    ap.add_argument("--skinny-steps", type=int, default=4000)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-skinny", action="store_true")
+    ap.add_argument("--tiny-steps", type=int, default=2000)
     ap.add_argument("--bf16-out-steps", type=int, default=20000)
-    ap.add_argument("--no-bf16-out", action="store_true")
+    ap.add_argument("--llm-steps", type=int, default=200)
+    ap.add_argument("--skinny-steps", type=int, default=4000)
     ap.add_argument("--fp8-steps", type=int, default=4000)
-    ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--fp32-steps", type=int, default=300)
-    ap.add_argument("--no-fp32", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--skip", default="", help="comma-separated legs to leave out: " + ",".join(
+        n for n, _ in LEGS))
+    ap.add_argument("--detail", default="", help="write per-leg plans and timings to this JSON file")
+    a = ap.parse_args()
+    a.skip = set(x for x in a.skip.split(",") if x)
+    return a
 
 
 def peaks():
@@ -136,8 +140,7 @@ def oracle_sample(seconds, problem=None):
         if el >= seconds:
             break
     flops = 2.0 * rows_done * p.N * p.K
-    desc = "%d full rows of C (%d of %d outputs, K=%d) of the %s workload, fp64, all cores" % (
-        rows_done, rows_done * p.N, p.M * p.N, p.K, WORKLOAD)
+    desc = "%d of %d rows of C, fp64, all cores" % (rows_done, p.M)
     return flops / el / 1e12, desc, el
 
 
@@ -250,6 +253,84 @@ def recorded_traffic(kernel_key):
     return d.get("dram_bytes_per_launch")
 
 
+def _sig(x, digits=4):
+    """x rounded to `digits` significant figures (keeps the JSON line short)."""
+    if x is None or x == 0 or not math.isfinite(x):
+        return x
+    return round(x, digits - 1 - int(math.floor(math.log10(abs(x)))))
+
+
+def n_rotating_sets(set_bytes):
+    """Input sets to rotate over so that every step's operands and C miss L2:
+    together at least twice the L2 size (one set when a set alone exceeds it)."""
+    if set_bytes > 2 * L2_BYTES:
+        return 1
+    return max(2, math.ceil(2 * L2_BYTES / set_bytes) + 1)
+
+
+def time_steps(step, n, stream, dev, warm=10):
+    """Average device milliseconds of `step(i)` over n back-to-back calls on
+    `stream` (CUDA events on that stream, synchronised on both sides), and the
+    wall seconds of the timed region."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(warm):
+            step(i)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        wall0 = time.perf_counter()
+        e0.record(stream)
+        for i in range(n):
+            step(i)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / n, time.perf_counter() - wall0
+
+
+def device_operands(p, dev):
+    """Device copies of a problem's A and B, and its C: the initial C0 when
+    beta != 0 (read and updated in place by every step), else an empty buffer
+    of C's type and leading dimension."""
+    import torch
+    out = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[p.out_dtype]
+    C = p.C0.to(dev) if p.C0 is not None else torch.empty(p.M, p.ldc, dtype=out, device=dev)
+    return p.A.to(dev), p.B.to(dev), C
+
+
+class GemmLeg:
+    """One workload timed through gemm_run on device buffers: rotating input
+    sets larger than L2, back-to-back calls, status checked afterwards."""
+
+    def __init__(self, G, h, p, code, dev, stream):
+        self.G, self.h, self.p, self.code, self.stream = G, h, p, code, stream
+        A, B, C = device_operands(p, dev)
+        set_bytes = A.numel() * A.element_size() + B.numel() * B.element_size() + C.numel() * C.element_size()
+        self.n_sets = n_rotating_sets(set_bytes)
+        self.sets = [(A, B, C)] + [(A.clone(), B.clone(), C.clone()) for _ in range(self.n_sets - 1)]
+        self.set_mb = set_bytes / 2 ** 20
+        self.sptr = stream.cuda_stream
+        self.plan = G.plan(p.M, p.N, p.K, p.transA, p.transB, code, lda=p.lda, ldb=p.ldb, ldc=p.ldc,
+                           beta=p.beta, handle=h)
+
+    def step(self, i):
+        p = self.p
+        A, B, C = self.sets[i % self.n_sets]
+        st = self.h.run_raw(p.transA, p.transB, p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(),
+                            p.ldb, p.beta, C.data_ptr(), p.ldc, self.code, self.sptr)
+        if st != self.G.OK:
+            raise self.G.GemmError(st, "gemm_run " + p.name)
+
+    def time(self, n, dev, warm=10):
+        ms, wall = time_steps(self.step, n, self.stream, dev, warm)
+        st, word = self.h.status(self.sptr)
+        if st != self.G.OK:
+            raise RuntimeError("%s: kernel status %s (0x%x)" % (self.p.name, self.G.STATUS.get(st), word))
+        return ms, wall
+
+    def free(self):
+        self.sets = None
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -266,27 +347,16 @@ def run_ours(args):
     gbuild.build()
 
     h = G.Handle(local)
-    p = inputs.square_4096_bf16_nt("f32", SIZE)
-    flops = metrics.flops(p.M, p.N, p.K)
-    set_bytes = p.A.numel() * 2 + p.B.numel() * 2 + p.M * p.N * 4
-    n_sets = max(2, math.ceil(2 * L2_BYTES / set_bytes) + 1)
-    A0, B0 = p.A.to(dev), p.B.to(dev)
-    sets = [(A0.clone(), B0.clone(), torch.empty(p.M, p.N, dtype=torch.float32, device=dev)) for _ in range(n_sets)]
-    del A0, B0
     stream = torch.cuda.Stream(dev)
     sptr = stream.cuda_stream
-    plan = G.plan(p.M, p.N, p.K, p.transA, p.transB, G.BF16_F32, sm_count=torch.cuda.get_device_properties(dev).multi_processor_count)
-
-    def step(i):
-        A, B, C = sets[i % n_sets]
-        st = h.run_raw(p.transA, p.transB, p.M, p.N, p.K, 1.0, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, 0.0,
-                       C.data_ptr(), p.N, G.BF16_F32, sptr)
-        if st != G.OK:
-            raise G.GemmError(st, "gemm_run")
+    p = inputs.square_4096_bf16_nt("f32", SIZE)
+    flops = metrics.flops(p.M, p.N, p.K)
+    main = GemmLeg(G, h, p, G.BF16_F32, dev, stream)
+    plan = main.plan
 
     with torch.cuda.stream(stream):
         for i in range(max(3, args.warmup)):
-            step(i)
+            main.step(i)
     st, word = h.status(sptr)
     if st != G.OK:
         raise RuntimeError("warm-up kernel status %s (0x%x)" % (G.STATUS.get(st), word))
@@ -304,7 +374,7 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         ev[0].record(stream)
         for i in range(K):
-            step(i)
+            main.step(i)
         ev[1].record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
@@ -318,6 +388,8 @@ def run_ours(args):
     ms = slowest_over_ranks(ev[0].elapsed_time(ev[1]), dev)
     value = job_value(flops, ws, K, ms)
     kernel_ms = ms / K   # one kernel launch per step, back to back on one stream
+    main_l2 = "%d rotating sets of %.0f MB" % (main.n_sets, main.set_mb)
+    main.free()
 
     # End to end through the public API on host buffers (gemm_run_host): every
     # step copies A and B from page-locked host memory, runs the GEMM and copies
@@ -336,263 +408,170 @@ def run_ours(args):
         e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    e2e = {"value": flops / (e2e_ms / 1e3) / 1e12 * ws, "unit": "TFLOP/s",
-           "h2d_bytes_per_step": A_h.numel() * 2 + B_h.numel() * 2, "d2h_bytes_per_step": C_h.numel() * 4,
-           "ms_per_step": e2e_ms, "steps": args.e2e_steps}
+    e2e = {"value": _sig(flops / (e2e_ms / 1e3) / 1e12 * ws), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": A_h.numel() * 2 + B_h.numel() * 2, "d2h_bytes_per_step": C_h.numel() * 4}
+    del A_h, B_h, C_h
 
     pk, pk_src = peaks()
     peak_b = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     peak_s = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     achieved = flops / (kernel_ms / 1e3) / 1e12
     cg = 2 if plan.path == G.PATH_TC_2CTA else 1
-    kernel_key = "tc_gemm_kernel<%d,%d>:%s" % (plan.bn, cg, WORKLOAD)
     # The timed region runs the kernel back to back for seconds under the power
     # cap, as the sustained cuBLAS figure was measured; a short region compares
     # against the burst figure.
     sustained = wall >= 1.0
     peak = peak_s if sustained else peak_b
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": recorded_traffic(kernel_key),
-                "peak_source": "%s %s (cuBLAS bf16; %s)" % (
-                    pk_src, "bf16_tflops_sustained" if sustained else "bf16_tflops",
-                    "this run is back to back for %.3f s" % wall),
-                "frac_of_burst": achieved / peak_b, "frac_of_sustained": achieved / peak_s,
-                "frac_of_nominal_2250": achieved / 2250.0,
-                "kernel": "tc_gemm_kernel<BN=%d, CTA group %d>" % (plan.bn, cg), "kernel_ms": kernel_ms,
-                "algorithmic_flops_per_launch": flops,
-                "traffic_note": "DRAM bytes per launch from the committed ncu summary, if taken on these sources"}
+    roofline = {"bound": "tensor", "achieved": _sig(achieved), "peak": peak, "unit": "TFLOP/s",
+                "frac": _sig(achieved / peak),
+                "traffic": recorded_traffic("tc_gemm_kernel<%d,%d>:%s" % (plan.bn, cg, WORKLOAD)),
+                "peak_key": "%s %s" % (pk_src, "bf16_tflops_sustained" if sustained else "bf16_tflops"),
+                "frac_nominal_2250": _sig(achieved / 2250.0)}
+    detail = {"main": {"plan": plan.as_dict(), "kernel_ms": kernel_ms, "wall_s": wall, "l2": main_l2,
+                       "peak_source": "%s (cuBLAS bf16); timed region back to back for %.3f s" % (
+                           roofline["peak_key"], wall)},
+              "e2e": {"ms_per_step": e2e_ms, "steps": args.e2e_steps}}
 
-    bf16_out = None
-    if not args.no_bf16_out:
-        bf16_out = run_bf16_out(args, G, h, inputs, metrics, dev, stream, pk, pk_src)
-    skinny = None
-    if not args.no_skinny:
-        skinny = run_skinny(args, G, h, inputs, metrics, dev, stream, pk, pk_src)
-    fp8 = None
-    if not args.no_fp8:
-        fp8 = run_fp8(args, G, h, inputs, metrics, dev, stream, pk, pk_src)
-    fp32 = None
-    if not args.no_fp32:
-        fp32 = run_fp32(args, G, h, inputs, metrics, dev, stream, pk, pk_src)
+    legs = {}
+    ctx = dict(args=args, G=G, h=h, inputs=inputs, metrics=metrics, dev=dev, stream=stream, pk=pk,
+               peak_b=peak_b, peak_s=peak_s, legs=legs, detail=detail)
+    for name, fn in LEGS:
+        if name not in args.skip:
+            fn(ctx)
+            torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         v, desc, el = oracle_sample(args.cpu_seconds, p)
-        cpu = {"value": v, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle", "sample": desc,
-               "seconds": el, "cpu": cpu_model()}
+        cpu = {"value": _sig(v), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle", "sample": desc}
+        detail["cpu_baseline"] = {"seconds": el, "cpu": cpu_model()}
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
-            "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "M": p.M, "N": p.N, "K": p.K, "layout": "NT", "in": "bf16",
-                       "out": "f32", "alpha": 1.0, "beta": 0.0, "dist": "N(0,1)/sqrt(K), seeds 0/1",
-                       "l2": "%d rotating input sets of %.0f MB (%.0f MB total > %d MB L2)" % (
-                           n_sets, set_bytes / 2 ** 20, n_sets * set_bytes / 2 ** 20, L2_BYTES // 2 ** 20),
-                       "plan": plan.as_dict(), "parallelism": "replicas" if ws > 1 else "single GPU",
-                       "wall_s_timed_region": wall},
+            "metric": METRIC, "value": _sig(value, 5), "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
+            "warmup": args.warmup, "ms_per_step": _sig(ms / K, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": p.M, "N": p.N, "K": p.K, "layout": "NT", "out": "f32",
+                       "l2": main_l2 + " > L2", "parallelism": "replicas" if ws > 1 else "1 GPU"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clk, "bf16_out": bf16_out, "skinny": skinny, "fp8": fp8, "fp32": fp32,
+            "clocks": {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+            "legs": legs,
+            "legs_key": LEGS_KEY,
         }
-        print(json.dumps(line), flush=True)
+        if args.detail:
+            detail["clocks"] = clk
+            with open(args.detail, "w") as f:
+                json.dump(detail, f, indent=1)
+        print(json.dumps(line, separators=(",", ":"), ensure_ascii=False), flush=True)
     h.close()
     if ws > 1:
         dist.destroy_process_group()
     return 0
 
 
-def run_bf16_out(args, G, h, inputs, metrics, dev, stream, pk, pk_src):
-    """The square 4096^3 bf16 NT GEMM writing bf16 C (RNE), against the measured
-    bf16 peak: the sustained figure when the timed region lasts a second or
-    more (back to back under the power cap), else the burst figure."""
-    import torch
-    p = inputs.square_4096_bf16_nt("bf16", SIZE)
-    set_bytes = p.A.numel() * 2 + p.B.numel() * 2 + p.M * p.N * 2
-    n_sets = max(2, math.ceil(2 * L2_BYTES / set_bytes) + 1)
-    sets = [(p.A.to(dev), p.B.to(dev), torch.empty(p.M, p.N, dtype=torch.bfloat16, device=dev))
-            for _ in range(n_sets)]
-    plan = G.plan(p.M, p.N, p.K, p.transA, p.transB, G.BF16_BF16)
-    sptr = stream.cuda_stream
+LEGS_KEY = ("[v, frac]: _tf TFLOP/s vs bf16 peak (fp8 x2; fp32: 3 TF32 products vs x1.1/2.25), "
+            "_gbs GB/s vs copy; c1: [device, host] us per call")
 
-    def step(i):
-        A, B, C = sets[i % n_sets]
-        st = h.run_raw(p.transA, p.transB, p.M, p.N, p.K, 1.0, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, 0.0,
-                       C.data_ptr(), p.N, G.BF16_BF16, sptr)
-        if st != G.OK:
-            raise G.GemmError(st, "gemm_run")
 
-    with torch.cuda.stream(stream):
-        for i in range(20):
-            step(i)
-        torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        wall0 = time.perf_counter()
-        e0.record(stream)
-        for i in range(args.bf16_out_steps):
-            step(i)
-        e1.record(stream)
-    torch.cuda.synchronize(dev)
-    wall = time.perf_counter() - wall0
-    st, word = h.status(sptr)
-    if st != G.OK:
-        raise RuntimeError("bf16-output kernel status %s (0x%x)" % (G.STATUS.get(st), word))
-    ms = e0.elapsed_time(e1) / args.bf16_out_steps
-    tflops = metrics.flops(p.M, p.N, p.K) / (ms / 1e3) / 1e12
+def _tensor_leg(ctx, key, p, code, steps, peak_scale=1.0, work_scale=1.0):
+    """Time one GEMM workload; record [TFLOP/s, frac of the bf16 peak x peak_scale]."""
+    leg = GemmLeg(ctx["G"], ctx["h"], p, code, ctx["dev"], ctx["stream"])
+    ms, wall = leg.time(steps, ctx["dev"])
+    tflops = ctx["metrics"].flops(p.M, p.N, p.K) / (ms / 1e3) / 1e12
     sustained = wall >= 1.0
-    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
-    peak = float(pk.get(key, FALLBACK_PEAKS[key]))
-    return {"workload": "square_4096_bf16_nt_bf16", "value": tflops, "unit": "TFLOP/s", "us_per_call": ms * 1e3,
-            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
-                         "frac": tflops / peak, "frac_of_nominal_2250": tflops / 2250.0,
-                         "peak_source": "%s %s (this leg is back to back for %.3f s)" % (pk_src, key, wall),
-                         "traffic": None},
-            "plan": plan.as_dict(), "l2": "%d rotating input sets (%.0f MB total)" % (
-                n_sets, n_sets * set_bytes / 2 ** 20)}
+    peak = (ctx["peak_s"] if sustained else ctx["peak_b"]) * peak_scale
+    ctx["legs"][key] = [_sig(tflops), _sig(work_scale * tflops / peak, 3)]
+    ctx["detail"][key] = {"workload": p.name, "us_per_call": ms * 1e3, "tflops": tflops, "peak": peak,
+                          "sustained": sustained, "wall_s": wall, "plan": leg.plan.as_dict(),
+                          "l2": "%d rotating sets of %.0f MB" % (leg.n_sets, leg.set_mb)}
+    leg.free()
+    return ms
 
 
-def run_fp8(args, G, h, inputs, metrics, dev, stream, pk, pk_src):
-    """4096^3 with 8-bit E4M3 inputs (A M x K, B N x K), fp32 C: TFLOP/s against
-    the measured bf16 burst peak scaled by the nominal FP8 / bf16 ratio (2)."""
+def leg_tiny(ctx):
+    """256^3 NN bf16 -> fp32 (latency-bound): device microseconds per call over
+    back-to-back calls, and host microseconds per gemm_run call."""
+    G, h, stream, dev = ctx["G"], ctx["h"], ctx["stream"], ctx["dev"]
+    p = ctx["inputs"].tiny_256()
+    leg = GemmLeg(G, h, p, G.BF16_F32, dev, stream)
+    ms, _ = leg.time(ctx["args"].tiny_steps, dev)
+    # host time of the call alone (the launch is asynchronous), repeated on
+    # one set of buffers as a decode loop calls it: plan and tensor maps come
+    # from the handle's caches
     import torch
-    p = inputs.square_4096_fp8_nt("e4m3", "f32", SIZE)
-    code = G.fp8_dtype("e4m3", "e4m3", "f32")
-    set_bytes = p.A.numel() + p.B.numel() + p.M * p.N * 4
-    n_sets = max(2, math.ceil(2 * L2_BYTES / set_bytes) + 1)
-    sets = [(p.A.to(dev), p.B.to(dev), torch.empty(p.M, p.N, dtype=torch.float32, device=dev))
-            for _ in range(n_sets)]
-    plan = G.plan(p.M, p.N, p.K, p.transA, p.transB, code)
-    sptr = stream.cuda_stream
-
-    def step(i):
-        A, B, C = sets[i % n_sets]
-        st = h.run_raw(p.transA, p.transB, p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb,
-                       0.0, C.data_ptr(), p.N, code, sptr)
-        if st != G.OK:
-            raise G.GemmError(st, "gemm_run")
-
+    n = ctx["args"].tiny_steps
     with torch.cuda.stream(stream):
-        for i in range(20):
-            step(i)
-        torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(args.fp8_steps):
-            step(i)
-        e1.record(stream)
+        t0 = time.perf_counter()
+        for _ in range(n):
+            leg.step(0)
+        host_us = (time.perf_counter() - t0) / n * 1e6
     torch.cuda.synchronize(dev)
-    st, word = h.status(sptr)
-    if st != G.OK:
-        raise RuntimeError("fp8 kernel status %s (0x%x)" % (G.STATUS.get(st), word))
-    ms = e0.elapsed_time(e1) / args.fp8_steps
-    tflops = metrics.flops(p.M, p.N, p.K) / (ms / 1e3) / 1e12
-    peak = 2.0 * float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    cg = plan.bm // 128
-    return {"workload": "square_4096_e4m3_nt_f32", "value": tflops, "unit": "TFLOP/s", "us_per_call": ms * 1e3,
-            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
-                         "frac": tflops / peak, "frac_of_nominal_4500": tflops / 4500.0,
-                         "peak_source": "%s bf16_tflops x 2 (nominal FP8 / bf16 dense ratio 4.5 / 2.25)" % pk_src,
-                         "traffic": recorded_traffic("tc_gemm_kernel<%d,%d,e4m3>:square_4096_e4m3_nt_f32"
-                                                     % (plan.bn, cg))},
-            "plan": plan.as_dict(), "l2": "%d rotating input sets (%.0f MB total)" % (
-                n_sets, n_sets * set_bytes / 2 ** 20)}
+    ctx["legs"]["c1_256_us"] = [_sig(ms * 1e3, 3), _sig(host_us, 3)]
+    ctx["detail"]["c1_256_us"] = {"workload": p.name, "device_us_per_call": ms * 1e3, "host_us_per_call": host_us,
+                                  "plan": leg.plan.as_dict(),
+                                  "l2": "%d rotating sets of %.2f MB" % (leg.n_sets, leg.set_mb)}
+    leg.free()
 
 
-def run_fp32(args, G, h, inputs, metrics, dev, stream, pk, pk_src):
-    """4096^3 with fp32 inputs and C (A M x K, B N x K): the fp32 GEMM from
-    three TF32 products per product (two split launches and one GEMM over 3K)
-    and, for comparison, one TF32 product per product (one launch).  Values are
-    TFLOP/s of fp32 work (2 M N K per call); the roofline counts the TF32
-    products the tensor cores execute against the measured bf16 burst peak
-    scaled by the nominal TF32 / bf16 dense ratio (1.1 / 2.25)."""
-    import torch
-    p = inputs.square_4096_f32_nt(SIZE)
-    set_bytes = (p.A.numel() + p.B.numel() + p.M * p.N) * 4
-    n_sets = max(2, math.ceil(2 * L2_BYTES / set_bytes) + 1)
-    sets = [(p.A.to(dev), p.B.to(dev), torch.empty(p.M, p.N, dtype=torch.float32, device=dev))
-            for _ in range(n_sets)]
-    sptr = stream.cuda_stream
-    peak = 1.1 / 2.25 * float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    out = {"workload": "square_4096_f32_nt_f32", "unit": "TFLOP/s",
-           "l2": "%d rotating input sets (%.0f MB total)" % (n_sets, n_sets * set_bytes / 2 ** 20)}
-    for name, code, parts in (("f32_3xtf32", G.F32_F32, 3), ("tf32", G.TF32_F32, 1)):
-        def step(i):
-            A, B, C = sets[i % n_sets]
-            st = h.run_raw(0, 1, p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, 0.0,
-                           C.data_ptr(), p.N, code, sptr)
-            if st != G.OK:
-                raise G.GemmError(st, "gemm_run")
-
-        steps = args.fp32_steps * (3 if parts == 1 else 1)
-        with torch.cuda.stream(stream):
-            for i in range(5):
-                step(i)
-            torch.cuda.synchronize(dev)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for i in range(steps):
-                step(i)
-            e1.record(stream)
-        torch.cuda.synchronize(dev)
-        st, word = h.status(sptr)
-        if st != G.OK:
-            raise RuntimeError("fp32 kernel status %s (0x%x)" % (G.STATUS.get(st), word))
-        ms = e0.elapsed_time(e1) / steps
-        tflops = metrics.flops(p.M, p.N, p.K) / (ms / 1e3) / 1e12
-        plan = G.plan(p.M, p.N, p.K, 0, 1, code)
-        out[name] = {"value": tflops, "us_per_call": ms * 1e3, "launches_per_call": plan.launches,
-                     "roofline": {"bound": "tensor", "achieved": parts * tflops, "peak": peak, "unit": "TFLOP/s",
-                                  "frac": parts * tflops / peak,
-                                  "peak_source": "%s bf16_tflops x 1.1 / 2.25 (nominal TF32 / bf16 dense ratio)"
-                                                 % pk_src,
-                                  "achieved_counts": "%d TF32 products per product, whole call" % parts},
-                     "plan": plan.as_dict()}
-    out["value"] = out["f32_3xtf32"]["value"]
-    return out
+def leg_bf16_out(ctx):
+    """The 4096^3 bf16 NT workload with bf16 C (its other output type)."""
+    _tensor_leg(ctx, "c2_bf16c_tf", ctx["inputs"].square_4096_bf16_nt("bf16", SIZE), ctx["G"].BF16_BF16,
+                ctx["args"].bf16_out_steps)
 
 
-def run_skinny(args, G, h, inputs, metrics, dev, stream, pk, pk_src):
-    """LM-head GEMM, M = 64 x K = 4096 x N = 32000, weights N x K (NT), fp32 out:
-    HBM GB/s of algorithmic bytes against the measured copy bandwidth."""
-    import torch
-    p = inputs.lm_head_64()
-    A = p.A.to(dev)
-    Bs = [p.B.to(dev) for _ in range(2)]   # 2 x 262 MB of weights > L2
-    C = torch.empty(p.M, p.N, dtype=torch.float32, device=dev)
-    plan = G.plan(p.M, p.N, p.K, p.transA, p.transB, G.BF16_F32)
-    sptr = stream.cuda_stream
+def leg_blend(ctx):
+    """4096^3 fp16, alpha 1.5, beta 0.5 (C read and written), four layouts."""
+    for ta, tb in ((0, 0), (0, 1), (1, 0), (1, 1)):
+        lay = ("t" if ta else "n") + ("t" if tb else "n")
+        _tensor_leg(ctx, "c3_%s_tf" % lay, ctx["inputs"].square_4096_f16_blend(ta, tb, SIZE), ctx["G"].F16_F32,
+                    ctx["args"].llm_steps)
 
-    def step(i):
-        st = h.run_raw(p.transA, p.transB, p.M, p.N, p.K, 1.0, A.data_ptr(), p.lda, Bs[i % 2].data_ptr(), p.ldb,
-                       0.0, C.data_ptr(), p.N, G.BF16_F32, sptr)
-        if st != G.OK:
-            raise G.GemmError(st, "gemm_run")
 
-    with torch.cuda.stream(stream):
-        for i in range(20):
-            step(i)
-        torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(args.skinny_steps):
-            step(i)
-        e1.record(stream)
-    torch.cuda.synchronize(dev)
-    st, word = h.status(sptr)
-    if st != G.OK:
-        raise RuntimeError("skinny kernel status %s (0x%x)" % (G.STATUS.get(st), word))
-    ms = e0.elapsed_time(e1) / args.skinny_steps
+def leg_llm(ctx):
+    """LLM projections NN (weights K x N) and the ragged 4095 x 4097 x 1000 NN."""
+    inp = ctx["inputs"]
+    for name, key in (("qkv_proj", "c4_qkv_tf"), ("ffn_up", "c4_up_tf"), ("ffn_down", "c4_down_tf")):
+        _tensor_leg(ctx, key, inp.llm_projection(name, 0), ctx["G"].BF16_F32, ctx["args"].llm_steps)
+    _tensor_leg(ctx, "c4_ragged_tf", inp.ragged_4095_4097_1000(), ctx["G"].BF16_F32, ctx["args"].llm_steps)
+
+
+def leg_skinny(ctx):
+    """LM head M = 64 x K = 4096 x N = 32000, weights N x K (NT), fp32 C: GB/s of
+    algorithmic bytes against the measured copy bandwidth."""
+    G, metrics = ctx["G"], ctx["metrics"]
+    p = ctx["inputs"].lm_head_64()
+    leg = GemmLeg(G, ctx["h"], p, G.BF16_F32, ctx["dev"], ctx["stream"])
+    ms, wall = leg.time(ctx["args"].skinny_steps, ctx["dev"], warm=20)
     nbytes = metrics.algorithmic_bytes(p.M, p.N, p.K, "bf16", "f32")
     gbs = nbytes / (ms / 1e3) / 1e9
-    hbm = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    return {"workload": "lm_head_64x32000x4096_nt_f32", "value": gbs, "unit": "GB/s", "us_per_call": ms * 1e3,
-            "tflops": metrics.flops(p.M, p.N, p.K) / (ms / 1e3) / 1e12,
-            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
-                         "frac_of_8000": gbs / 8000.0, "peak_source": "%s hbm_gbs (copy)" % pk_src,
-                         "algorithmic_bytes_per_launch": nbytes,
-                         "traffic": recorded_traffic("tc_gemm_kernel<%d,%d>:lm_head_64x32000x4096_nt_f32"
-                                                     % (plan.bn, plan.bm // 128))},
-            "plan": plan.as_dict(), "l2": "2 weight copies of 262 MB alternate"}
+    hbm = float(ctx["pk"].get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    ctx["legs"]["c5_lmhead_gbs"] = [_sig(gbs), _sig(gbs / hbm, 3)]
+    ctx["detail"]["c5_lmhead_gbs"] = {
+        "workload": p.name, "us_per_call": ms * 1e3, "gbs": gbs, "frac_of_8000": gbs / 8000.0,
+        "algorithmic_bytes_per_launch": nbytes, "plan": leg.plan.as_dict(),
+        "traffic": recorded_traffic("tc_gemm_kernel<%d,%d>:lm_head_64x32000x4096_nt_f32"
+                                    % (leg.plan.bn, leg.plan.bm // 128)),
+        "l2": "%d rotating sets of %.0f MB" % (leg.n_sets, leg.set_mb)}
+    leg.free()
+
+
+def leg_fp8(ctx):
+    """4096^3 E4M3 NT -> fp32 against 2 x the measured bf16 burst peak."""
+    G = ctx["G"]
+    p = ctx["inputs"].square_4096_fp8_nt("e4m3", "f32", SIZE)
+    _tensor_leg(ctx, "fp8_tf", p, G.fp8_dtype("e4m3", "e4m3", "f32"), ctx["args"].fp8_steps, peak_scale=2.0)
+
+
+def leg_fp32(ctx):
+    """4096^3 fp32 NT -> fp32 from three TF32 products: TFLOP/s of fp32 work; the
+    frac counts the three TF32 products against bf16 x 1.1 / 2.25."""
+    G = ctx["G"]
+    p = ctx["inputs"].square_4096_f32_nt(SIZE)
+    _tensor_leg(ctx, "fp32_tf", p, G.F32_F32, ctx["args"].fp32_steps, peak_scale=1.1 / 2.25, work_scale=3.0)
+
+
+LEGS = [("tiny", leg_tiny), ("bf16_out", leg_bf16_out), ("blend", leg_blend), ("llm", leg_llm),
+        ("skinny", leg_skinny), ("fp8", leg_fp8), ("fp32", leg_fp32)]
 
 
 def main():

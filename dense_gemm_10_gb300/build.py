@@ -19,12 +19,12 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libgemm_gb300.so")
 HEADER = os.path.join(ROOT, "include", "gemm_gb300.h")
 
-SOURCES = ["gemm_api.cu", "tc_dispatch.cu", "tc_gemm_bn64_cg1_mc1.cu", "tc_gemm_bn128_cg1_mc1.cu",
-           "tc_gemm_bn64_cg1_mc1_f8.cu", "tc_gemm_bn128_cg1_mc1_f8.cu", "tc_gemm_bn128_cg2_mc1_f8.cu",
-           "tc_gemm_bn256_cg2_mc1_f8.cu", "tc_gemm_bn64_cg1_mc1_tf32.cu", "tc_gemm_bn128_cg1_mc1_tf32.cu",
-           "tc_gemm_bn256_cg2_mc1_tf32.cu",
-           "tc_gemm_bn256_cg1_mc1.cu", "tc_gemm_bn128_cg2_mc1.cu", "tc_gemm_bn256_cg2_mc1.cu",
-           "tc_gemm_bn256_cg2_mc2.cu", "tc_gemm_bn64_cg2_mc1.cu", "aux_kernels.cu", "probe.cu"]
+SOURCES = ["gemm_api.cu", "tc_dispatch.cu", "aux_kernels.cu", "probe.cu",
+           # one translation unit per kernel configuration: tile width, CTA group, input kind
+           "tc_gemm_bn64_cg1.cu", "tc_gemm_bn128_cg1.cu", "tc_gemm_bn256_cg1.cu", "tc_gemm_bn64_cg2.cu",
+           "tc_gemm_bn128_cg2.cu", "tc_gemm_bn256_cg2.cu",
+           "tc_gemm_bn64_cg1_f8.cu", "tc_gemm_bn128_cg1_f8.cu", "tc_gemm_bn128_cg2_f8.cu", "tc_gemm_bn256_cg2_f8.cu",
+           "tc_gemm_bn64_cg1_tf32.cu", "tc_gemm_bn128_cg1_tf32.cu", "tc_gemm_bn256_cg2_tf32.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-I" + os.path.join(ROOT, "include")]

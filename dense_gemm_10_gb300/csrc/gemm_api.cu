@@ -22,6 +22,7 @@
 #include "../../include/gemm_gb300.h"
 #include "gemm_internal.h"
 #include "ptx.cuh"
+#include "tmap_cache.h"
 
 using namespace g10;
 
@@ -189,10 +190,8 @@ int default_kdepth(const TileConfig& c) { return c.bn == 64 ? 2 : 1; }
 
 // Relative time of one 64-wide k-slice of one schedule tile for each tile
 // configuration, in units of the CTA-pair 256 x 256 tile, from GB300
-// measurements of the 4096^3 and 8192 x 12288 x 4096 bf16 GEMMs.  (A multicast
-// cluster's schedule tile is two 256 x 256 tiles worked side by side.)
+// measurements of the 4096^3 and 8192 x 12288 x 4096 bf16 GEMMs.
 double tile_kb_cost(const TileConfig& c) {
-  if (c.mc == 2) return 1.05;  // measured slightly slower than a lone pair: used only on request
   if (c.cg == 2) return c.bn == 256 ? 1.0 : c.bn == 128 ? 0.62 : 0.65;
   return c.bn == 256 ? 1.15 : c.bn == 128 ? 0.85 : 0.6;
 }
@@ -207,7 +206,7 @@ struct SlotTable {
   static SlotTable even(int sm_count) {
     SlotTable t;
     for (int i = 0; i < kNumTileConfigs; ++i)
-      t.n[i] = std::max(1, sm_count / (kTileConfigs[i].cg * kTileConfigs[i].mc));
+      t.n[i] = std::max(1, sm_count / kTileConfigs[i].cg);
     return t;
   }
 };
@@ -221,14 +220,14 @@ cudaError_t measure_slots(int sm_count, SlotTable* t) {
     int clusters = 0;
     cudaError_t e = tc_prepare(i, &clusters);
     if (e != cudaSuccess) return e;
-    if (c.cg * c.mc > 1 && clusters > 0) t->n[i] = std::min(clusters, sm_count / (c.cg * c.mc));
+    if (c.cg > 1 && clusters > 0) t->n[i] = std::min(clusters, sm_count / c.cg);
   }
   return cudaSuccess;
 }
 
 struct Choice {
   bool valid = false;
-  int cfg = 0, cg = 1, bn = 64, mc = 1, slots = 1, kdepth = 1;
+  int cfg = 0, cg = 1, bn = 64, slots = 1, kdepth = 1;
   double cost = 1e300;
   Sched sched{};
 };
@@ -273,11 +272,10 @@ Choice choose_schedule(const Options& o, int64_t tiles_i, int64_t tiles_j, int64
   Choice ch;
   ch.kdepth = kdepth;
   const TileConfig& tc = kTileConfigs[cfg];
-  const int cl = tc.cg * tc.mc;  // CTAs per slot
+  const int cl = tc.cg;  // CTAs per slot
   ch.cfg = cfg;
   ch.cg = tc.cg;
   ch.bn = tc.bn;
-  ch.mc = tc.mc;
   ch.slots = slots;
   const int64_t tiles = tiles_i * tiles_j * batch;
   // a CTA's fp32 partial tile (bn x 128) in stages of its operand bytes
@@ -486,21 +484,19 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
 
   // Tile configuration and schedule: the configuration with the lowest
   // estimated time, est_time() below.
-  static const int kPreference[kNumTileConfigs] = {5, 4, 3, 2, 1, 6, 0, 10, 9, 8, 7, 13, 12, 11};  // ties go first
+  static const int kPreference[kNumTileConfigs] = {4, 3, 2, 1, 5, 0, 9, 8, 7, 6, 12, 11, 10};  // ties go first
   Choice best;
   for (int cfg : kPreference) {
     const TileConfig& c = kTileConfigs[cfg];
     if (c.eb != dt.eb) continue;
-    if (groups > 0 && c.mc == 2) continue;  // groups share no A tile between neighbouring tiles
-    const int path = c.mc == 2 ? GEMM_PATH_TC_2CTA_MULTICAST : c.cg == 2 ? GEMM_PATH_TC_2CTA : GEMM_PATH_TC_1CTA;
+    const int path = c.cg == 2 ? GEMM_PATH_TC_2CTA : GEMM_PATH_TC_1CTA;
     if (o.force_path && o.force_path != path) continue;
     if (o.force_bn && c.bn != o.force_bn) continue;
     if (!o.force_bn && c.bn > 64 && pl.J <= c.bn / 2) continue;       // too wide for J
     if (!o.force_path && c.cg == 2 && pl.I <= kBM) continue;          // one row of tiles
-    if (!o.force_path && c.mc == 2 && cdiv(pl.J, c.bn) < 2) continue;  // nothing to share
     if (c.bn / c.cg < 64 && !pl.q.kmajor) continue;  // half-atom Q halves: K-major only
     int nslots = slots.of(cfg);
-    if (o.max_grid) nslots = std::min(nslots, std::max(1, o.max_grid / (c.cg * c.mc)));
+    if (o.max_grid) nslots = std::min(nslots, std::max(1, o.max_grid / c.cg));
     // Two k-slices per stage where the ring still holds at least two such stages.
     int kdepth = o.kdepth ? o.kdepth : default_kdepth(c);
     if (kdepth > 1 && tc_stages(cfg) / kdepth < 2) kdepth = 1;
@@ -511,13 +507,13 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
       for (int64_t g = 0; g < groups; ++g) tile_rows += cdiv(m_sizes[g], kBM * c.cg);
       if (tile_rows == 0) tile_rows = 1;
     }
-    Choice ch = choose_schedule(o, tile_rows, cdiv(cdiv(pl.J, c.bn), c.mc), batch,
+    Choice ch = choose_schedule(o, tile_rows, cdiv(pl.J, c.bn), batch,
                                 cdiv(num_kslices, kdepth), kdepth, cfg, nslots, hbm_bound);
     if (ch.valid && ch.cost < best.cost - 1e-9) best = ch;
   }
   if (!best.valid) return GEMM_ERR_INVALID_ARG;  // forced options admit no configuration
   const int cg = best.cg;
-  const int cl = best.cg * best.mc;
+  const int cl = best.cg;
   pl.sched = best.sched;
   pl.cfg = best.cfg;
   if (groups > 0) {
@@ -536,7 +532,7 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   }
   pl.sched.raster_group = o.raster_group ? o.raster_group : 8;
   if (pl.sched.raster_group > pl.sched.tiles_i) pl.sched.raster_group = pl.sched.tiles_i;
-  P.path = best.mc == 2 ? GEMM_PATH_TC_2CTA_MULTICAST : cg == 2 ? GEMM_PATH_TC_2CTA : GEMM_PATH_TC_1CTA;
+  P.path = cg == 2 ? GEMM_PATH_TC_2CTA : GEMM_PATH_TC_1CTA;
   P.cluster = cl;
   P.bm = kBM * cg;
   P.bn = best.bn;
@@ -583,11 +579,13 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   P.vector_store = (!swap && c_rows_aligned) ? 1 : 0;
   // Bulk tensor stores need 16-byte aligned rows and a row width that is a
   // whole number of 16-byte pieces (a partial piece at the right edge would be
-  // written whole, past column N); the blend with the old C (beta != 0) keeps
-  // the direct path, which reads C as it writes it.  A swapped problem stores
+  // written whole, past column N).  With beta != 0 the old C of each block is
+  // loaded by the copy engine into the staging buffer the block then leaves
+  // from (not for swapped problems, whose blocks leave transposed: they keep
+  // the direct path, which reads C as it writes it).  A swapped problem stores
   // transposed blocks (C's rows run along the kernel's J).
   // (a group's rows end inside C: a bulk store could not stop at the group's edge)
-  const bool bulk = c_rows_aligned && (N * c_elem) % 16 == 0 && beta == 0.0f && o.tma_store != 2 &&
+  const bool bulk = c_rows_aligned && (N * c_elem) % 16 == 0 && (beta == 0.0f || !swap) && o.tma_store != 2 &&
                     pl.c_type != kCE4M3 && groups == 0;  // 8-bit C leaves through direct stores
   pl.tma_store = !bulk ? kBulkNone : swap ? kBulkTransposed : kBulkRows;
   P.bulk_store = pl.tma_store;
@@ -630,63 +628,68 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// Encode the rank-3 tiled map that `d` describes, or copy it out of `cache`
+// (when one is given) if the same description was encoded before.
+gemm_status_t encode_tiled(TmapCache* cache, const TmapDesc& d, CUtensorMap* map) {
+  auto fn = encode_fn();
+  if (!fn) return GEMM_ERR_TENSORMAP;
+  auto encode = [fn](const TmapDesc& k, CUtensorMap* m) {
+    cuuint64_t dims[3] = {k.dims[0], k.dims[1], k.dims[2]};
+    cuuint64_t strides[2] = {k.strides[0], k.strides[1]};
+    cuuint32_t box[3] = {k.box[0], k.box[1], k.box[2]};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, static_cast<CUtensorMapDataType>(k.dtype), 3, reinterpret_cast<void*>(k.base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, static_cast<CUtensorMapSwizzle>(k.swizzle),
+              static_cast<CUtensorMapL2promotion>(k.promotion), CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  const bool ok = cache ? cache->get(d, map, encode) : encode(d, map);
+  return ok ? GEMM_OK : GEMM_ERR_TENSORMAP;
+}
+
 // Describe operand `op` (possibly its repacked copy at `base`/`ld`) for 2-D tiled
 // loads with the 128-byte swizzle: K-major tiles are {one 128-byte k-slice} x
 // {box_rows rows} (64 16-bit or 128 8-bit elements of k); MN-major tiles
 // (16-bit only) are {64 rows of M/N} x {64 k}, loaded one 64-wide atom at a time.
 gemm_status_t encode_operand(CUtensorMap* map, const Operand& op, const void* base, int64_t ld,
-                             int64_t bstride, int eb, int32_t map_type, int box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return GEMM_ERR_TENSORMAP;
+                             int64_t bstride, int eb, int32_t map_type, int box_rows, TmapCache* cache) {
   // third dimension: the batch (one matrix when shared; its stride is then any valid value)
-  cuuint64_t dims[3];
-  dims[2] = static_cast<cuuint64_t>(op.nb);
+  uint64_t dims[3];
+  dims[2] = static_cast<uint64_t>(op.nb);
   const int64_t one = round_up(static_cast<size_t>(op.rows * ld * eb), 16);
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * eb,
-                           static_cast<cuuint64_t>(op.nb > 1 ? bstride * eb : one)};
-  cuuint32_t box[3];
+  const uint64_t strides[2] = {static_cast<uint64_t>(ld) * eb, static_cast<uint64_t>(op.nb > 1 ? bstride * eb : one)};
+  uint32_t box[3];
   box[2] = 1;
-  cuuint32_t estr[3] = {1, 1, 1};
   if (op.kmajor) {
-    dims[0] = static_cast<cuuint64_t>(op.cols);  // K
-    dims[1] = static_cast<cuuint64_t>(op.rows);  // M or N
-    box[0] = static_cast<cuuint32_t>(slice_k(eb));
-    box[1] = static_cast<cuuint32_t>(box_rows);
+    dims[0] = static_cast<uint64_t>(op.cols);  // K
+    dims[1] = static_cast<uint64_t>(op.rows);  // M or N
+    box[0] = static_cast<uint32_t>(slice_k(eb));
+    box[1] = static_cast<uint32_t>(box_rows);
   } else {
-    dims[0] = static_cast<cuuint64_t>(op.cols);  // M or N
-    dims[1] = static_cast<cuuint64_t>(op.rows);  // K
+    dims[0] = static_cast<uint64_t>(op.cols);  // M or N
+    dims[1] = static_cast<uint64_t>(op.rows);  // K
     box[0] = 64;
     box[1] = kBK;
   }
-  CUresult r = fn(map, static_cast<CUtensorMapDataType>(map_type), 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_TENSORMAP;
+  return encode_tiled(cache, tmap_desc(base, dims, strides, box, map_type, CU_TENSOR_MAP_SWIZZLE_128B,
+                                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B), map);
 }
 
 // Describe C as stored (rows x cols, row pitch ldc) for bulk stores.  Rows:
 // boxes of 32 rows x 128 bytes with the 128-byte swizzle.  Transposed: boxes
 // of 32 rows x 32 elements, 128-byte swizzled for fp32, plain for 16 bits.
 gemm_status_t encode_c(CUtensorMap* map, void* C, int64_t rows, int64_t cols, int64_t ldc,
-                       int32_t c_type, bool transposed, int64_t batch, int64_t strideC) {
-  auto fn = encode_fn();
-  if (!fn) return GEMM_ERR_TENSORMAP;
+                       int32_t c_type, bool transposed, int64_t batch, int64_t strideC, TmapCache* cache) {
   const int64_t esize = c_type == kCF32 ? 4 : 2;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
-                        static_cast<cuuint64_t>(batch)};
+  const uint64_t dims[3] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows), static_cast<uint64_t>(batch)};
   const int64_t one = round_up(static_cast<size_t>(rows * ldc * esize), 16);
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ldc * esize),
-                           static_cast<cuuint64_t>(batch > 1 ? strideC * esize : one)};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(transposed ? 32 : 128 / esize), 32, 1};
-  const CUtensorMapSwizzle swz =
-      transposed && esize == 2 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUtensorMapDataType dt = c_type == kCF32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                           : c_type == kCBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUresult r = fn(map, dt, 3, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_TENSORMAP;
+  const uint64_t strides[2] = {static_cast<uint64_t>(ldc * esize),
+                               static_cast<uint64_t>(batch > 1 ? strideC * esize : one)};
+  const uint32_t box[3] = {static_cast<uint32_t>(transposed ? 32 : 128 / esize), 32, 1};
+  const int swz = transposed && esize == 2 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+  const int dt = c_type == kCF32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                 : c_type == kCBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return encode_tiled(cache, tmap_desc(C, dims, strides, box, dt, swz, CU_TENSOR_MAP_L2_PROMOTION_NONE), map);
 }
 
 struct DeviceGuard {
@@ -749,6 +752,7 @@ struct gemm_handle_s {
   Options opt;
   HostStage host;
   PlanCache plans;
+  TmapCache tmaps;  // encoded tensor maps of recent calls
 };
 
 static gemm_status_t cuda_fail(gemm_handle_t h, cudaError_t e) {
@@ -841,9 +845,7 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
       h->opt.wait_limit_ns = value;
       return GEMM_OK;
     case GEMM_OPT_FORCE_PATH:
-      if (value != 0 && value != GEMM_PATH_TC_1CTA && value != GEMM_PATH_TC_2CTA &&
-          value != GEMM_PATH_TC_2CTA_MULTICAST)
-        return GEMM_ERR_INVALID_ARG;
+      if (value != 0 && value != GEMM_PATH_TC_1CTA && value != GEMM_PATH_TC_2CTA) return GEMM_ERR_INVALID_ARG;
       h->opt.force_path = static_cast<int>(value);
       return GEMM_OK;
     case GEMM_OPT_SPLIT_K:
@@ -898,6 +900,13 @@ gemm_status_t gemm_plan_cache_stats(gemm_handle_t h, uint64_t* hits, uint64_t* m
   if (!h || !hits || !misses) return GEMM_ERR_INVALID_ARG;
   *hits = h->plans.hits;
   *misses = h->plans.misses;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_tensor_map_cache_stats(gemm_handle_t h, uint64_t* hits, uint64_t* misses) {
+  if (!h || !hits || !misses) return GEMM_ERR_INVALID_ARG;
+  *hits = h->tmaps.hits;
+  *misses = h->tmaps.misses;
   return GEMM_OK;
 }
 
@@ -1054,7 +1063,6 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
     h->ws_bytes = want;
   }
   const int cg = P.bm / kBM;
-  const int mc = P.cluster / cg;
 
   // Operands that the copy engine cannot read directly are repacked (or split) first.
   const void* pbase;
@@ -1065,11 +1073,12 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
   if (e != cudaSuccess) return cuda_fail(h, e);
 
   CUtensorMap map_p, map_q;
+  TmapCache* tc = &h->tmaps;
   s = encode_operand(&map_p, pl.p, pbase, pld, pl.p.repack ? pl.p.rows * pld : pl.p.bstride, pl.eb,
-                     pl.in_dtype, kBM / mc);
+                     pl.in_dtype, kBM, tc);
   if (s != GEMM_OK) return s;
   s = encode_operand(&map_q, pl.q, qbase, qld, pl.q.repack ? pl.q.rows * qld : pl.q.bstride, pl.eb,
-                     pl.in_dtype, P.bn / cg);
+                     pl.in_dtype, P.bn / cg, tc);
   if (s != GEMM_OK) return s;
   CUtensorMap map_c;
   std::memset(&map_c, 0, sizeof(map_c));
@@ -1079,8 +1088,9 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
   if (pl.tma_store != kBulkNone) {
     // C as stored: I x J, or J x I for a swapped problem
     s = pl.tma_store == kBulkRows
-            ? encode_c(&map_c, c_out, pl.I, pl.c_staged ? pl.c_ws_ld : pl.J, c_ld, pl.c_type, false, pl.batch, pl.c_sb)
-            : encode_c(&map_c, C, pl.J, pl.I, ldc, pl.c_type, true, pl.batch, pl.c_sb);
+            ? encode_c(&map_c, c_out, pl.I, pl.c_staged ? pl.c_ws_ld : pl.J, c_ld, pl.c_type, false, pl.batch, pl.c_sb,
+                       tc)
+            : encode_c(&map_c, C, pl.J, pl.I, ldc, pl.c_type, true, pl.batch, pl.c_sb, tc);
     if (s != GEMM_OK) return s;
   }
 
@@ -1435,6 +1445,10 @@ struct NoAllocDevice {
 
 NoAllocDevice g_noalloc_devices[kNoAllocMaxDevices];
 std::mutex g_noalloc_mutex;
+// Process-wide settings of the no-allocation path (gemm_noalloc_set_option):
+// the barrier wait limit and the test hook that drops one load.
+int64_t g_noalloc_wait_ns = kDefaultWaitNs;
+int g_noalloc_drop_load = 0;
 
 }  // namespace
 
@@ -1493,6 +1507,11 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   if (s != GEMM_OK) return s;
   Options o;
   o.stage_c = false;  // no room for a copy of C in the fixed scratch
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    o.wait_limit_ns = g_noalloc_wait_ns;
+    o.drop_load = g_noalloc_drop_load;
+  }
   Plan pl;
   s = make_plan(o, d->slots, transA, transB, M, N, K, A, lda, B, ldb, beta, C, ldc, dtype, &pl);
   if (s != GEMM_OK) return s;
@@ -1507,7 +1526,6 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
       return GEMM_ERR_WORKSPACE;  // needs more scratch than the fixed 16 MiB array holds
   }
   const int cg = pl.pub.path >= GEMM_PATH_TC_1CTA ? pl.pub.bm / kBM : 1;
-  const int mc = pl.pub.path >= GEMM_PATH_TC_1CTA ? pl.pub.cluster / cg : 1;
   const gemm_plan_t& P = pl.pub;
   if (P.path == GEMM_PATH_NOOP) return GEMM_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1529,17 +1547,17 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   if (e != cudaSuccess) return GEMM_ERR_CUDA;
   CUtensorMap map_p, map_q;
   s = encode_operand(&map_p, pl.p, pbase, pld, pl.p.repack ? pl.p.rows * pld : pl.p.bstride, pl.eb,
-                     pl.in_dtype, kBM / mc);
+                     pl.in_dtype, kBM, nullptr);
   if (s != GEMM_OK) return s;
   s = encode_operand(&map_q, pl.q, qbase, qld, pl.q.repack ? pl.q.rows * qld : pl.q.bstride, pl.eb,
-                     pl.in_dtype, P.bn / cg);
+                     pl.in_dtype, P.bn / cg, nullptr);
   if (s != GEMM_OK) return s;
   CUtensorMap map_c;
   std::memset(&map_c, 0, sizeof(map_c));
   if (pl.tma_store != kBulkNone) {
     // C as stored: I x J, or J x I for a swapped problem
-    s = pl.tma_store == kBulkRows ? encode_c(&map_c, C, pl.I, pl.J, ldc, pl.c_type, false, pl.batch, pl.c_sb)
-                                  : encode_c(&map_c, C, pl.J, pl.I, ldc, pl.c_type, true, pl.batch, pl.c_sb);
+    s = pl.tma_store == kBulkRows ? encode_c(&map_c, C, pl.I, pl.J, ldc, pl.c_type, false, pl.batch, pl.c_sb, nullptr)
+                                  : encode_c(&map_c, C, pl.J, pl.I, ldc, pl.c_type, true, pl.batch, pl.c_sb, nullptr);
     if (s != GEMM_OK) return s;
   }
   TcArgs a;
@@ -1568,7 +1586,7 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   a.counters = d->counters;
   a.status = d->status;
   a.wait_limit_ns = static_cast<uint64_t>(o.wait_limit_ns);
-  a.drop_load = 0;
+  a.drop_load = o.drop_load;
   a.pdl = 0;  // (the no-allocation entry point clears its arrays first, with ordinary stream order)
   a.seg_slices = pl.p.seg_map != 0 ? static_cast<int32_t>(pl.p.split_seg / slice_k(pl.eb)) : 0;
   a.p_seg = pl.p.seg_map;
@@ -1576,4 +1594,45 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   a.ops = EpiOps();  // no fused operations (the memset above zeroed out_scale)
   e = tc_launch(pl.cfg, map_p, map_q, map_c, a, P.grid, st);
   return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// The status word of the no-allocation path: synchronise `stream`, then read
+// the word of the current device's arrays and clear it.  Allocates nothing.
+extern "C" gemm_status_t gemm_noalloc_get_status(void* stream, int32_t* detail) {
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_NO_DEVICE;
+  }
+  NoAllocDevice* d = nullptr;
+  gemm_status_t s = noalloc_setup(device, &d);
+  if (s != GEMM_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, d->status, sizeof(word), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return GEMM_ERR_CUDA;
+  if (detail) *detail = word;
+  if (word == 0) return GEMM_OK;
+  // A kernel gave up part-way: clear the word (each call clears the counters it uses).
+  e = cudaMemsetAsync(d->status, 0, sizeof(int32_t), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return GEMM_ERR_CUDA;
+  return GEMM_ERR_TIMEOUT;
+}
+
+extern "C" gemm_status_t gemm_noalloc_set_option(gemm_option_t opt, int64_t value) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  switch (opt) {
+    case GEMM_OPT_WAIT_LIMIT_NS:
+      if (value < 1000000) return GEMM_ERR_INVALID_ARG;
+      g_noalloc_wait_ns = value;
+      return GEMM_OK;
+    case GEMM_OPT_TEST_DROP_LOAD:
+      if (value < 0 || value > (int64_t{1} << 30)) return GEMM_ERR_INVALID_ARG;
+      g_noalloc_drop_load = static_cast<int>(value);
+      return GEMM_OK;
+    default:
+      return GEMM_ERR_INVALID_ARG;
+  }
 }

@@ -37,7 +37,7 @@ struct EpiOps {
 enum : int32_t { kStatusTimeout = 6 };
 enum WaitRole : int32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3 };
 enum WaitBarrier : int32_t {
-  kBarEmpty = 1, kBarFull = 2, kBarAccEmpty = 3, kBarAccFull = 4, kBarDrain = 5
+  kBarEmpty = 1, kBarFull = 2, kBarAccEmpty = 3, kBarAccFull = 4, kBarDrain = 5, kBarCLoad = 6
 };
 
 // Arguments of the persistent tcgen05 GEMM kernel, in the kernel's own terms:
@@ -83,20 +83,19 @@ struct TcArgs {
 enum BulkStore : int32_t { kBulkNone = 0, kBulkRows = 1, kBulkTransposed = 2 };
 
 // Tile configurations: a tile of (128 * cg) x bn per CTA (cg == 1) or CTA
-// pair (cg == 2); mc == 2 clusters two pairs on neighbouring tiles of one tile
-// row, which share the P tile by multicast.  eb is the input element size in
-// bytes: 2 for bf16 / fp16 (tcgen05.mma kind::f16), 1 for the 8-bit formats
-// (kind::f8f6f4), 4 for TF32 (kind::tf32).
+// pair (cg == 2).  eb is the input element size in bytes: 2 for bf16 / fp16
+// (tcgen05.mma kind::f16), 1 for the 8-bit formats (kind::f8f6f4), 4 for TF32
+// (kind::tf32).
 struct TileConfig {
-  int bn, cg, mc, eb;
+  int bn, cg, eb;
 };
-constexpr int kNumTileConfigs = 14;
+constexpr int kNumTileConfigs = 13;
 extern const TileConfig kTileConfigs[kNumTileConfigs];
 int tc_stages(int cfg);  // ring depth in k-slices
 // One-time per device: opt in to the kernel's shared memory; for clusters also
 // report how many can be resident at once.
 cudaError_t tc_prepare(int cfg, int* max_clusters);
-// grid = CTAs (a multiple of cg * mc).
+// grid = CTAs (a multiple of cg).
 // map_c describes C for the bulk-store epilogue (ignored unless args.tma_store).
 cudaError_t tc_launch(int cfg, const CUtensorMap& map_p, const CUtensorMap& map_q,
                       const CUtensorMap& map_c, const TcArgs& args, int grid, cudaStream_t stream);

@@ -83,19 +83,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-// CTA-pair form with cluster multicast: the tile is written at the same
-// shared-memory offset in every CTA of `mask`, and each destination's bytes
-// are credited to the mbarrier at offset `bar` in the leader of its pair.
-__device__ __forceinline__ void tma_load_3d_pair_multicast(uint32_t dst, const CUtensorMap* map,
-                                                           uint32_t bar, int32_t x, int32_t y,
-                                                           int32_t z, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.cta_group::2 [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(mask)
-      : "memory");
-}
-
 // 3-D tiled tensor store shared -> global, tracked by this thread's bulk groups.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t x,
                                              int32_t y, int32_t z) {
@@ -336,7 +323,8 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
         : "memory");
 }
 
-// As mma_commit, arriving on the mbarrier at the same offset in every CTA of `mask`.
+// As mma_commit, arriving on the mbarrier at the same offset in every CTA of
+// `mask` (the two CTAs of a pair).  This signals a barrier; it moves no data.
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"

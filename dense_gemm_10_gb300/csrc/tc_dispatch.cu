@@ -8,29 +8,26 @@ using PrepareFn = cudaError_t (*)(int*);
 using LaunchFn = cudaError_t (*)(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                  const TcArgs&, int, cudaStream_t);
 
-#define TC_DECLARE(BN, CG, MC, EB)                                                                 \
-  cudaError_t tc_prepare_bn##BN##_cg##CG##_mc##MC##_eb##EB(int* max_clusters);                     \
-  cudaError_t tc_launch_bn##BN##_cg##CG##_mc##MC##_eb##EB(const CUtensorMap&, const CUtensorMap&,    \
-                                                         const CUtensorMap&, const TcArgs&, int,    \
-                                                         cudaStream_t);
-#define TC_ENTRY(BN, CG, MC, EB)                                                                   \
-  {{BN, CG, MC, EB}, TcConfig<BN, CG, MC>::kStages, tc_prepare_bn##BN##_cg##CG##_mc##MC##_eb##EB,  \
-   tc_launch_bn##BN##_cg##CG##_mc##MC##_eb##EB}
+#define TC_DECLARE(BN, CG, EB)                                                                  \
+  cudaError_t tc_prepare_bn##BN##_cg##CG##_eb##EB(int* max_clusters);                           \
+  cudaError_t tc_launch_bn##BN##_cg##CG##_eb##EB(const CUtensorMap&, const CUtensorMap&,          \
+                                                 const CUtensorMap&, const TcArgs&, int, cudaStream_t);
+#define TC_ENTRY(BN, CG, EB) \
+  {{BN, CG, EB}, TcConfig<BN, CG>::kStages, tc_prepare_bn##BN##_cg##CG##_eb##EB, tc_launch_bn##BN##_cg##CG##_eb##EB}
 
-TC_DECLARE(64, 1, 1, 2)
-TC_DECLARE(128, 1, 1, 2)
-TC_DECLARE(256, 1, 1, 2)
-TC_DECLARE(128, 2, 1, 2)
-TC_DECLARE(256, 2, 1, 2)
-TC_DECLARE(256, 2, 2, 2)
-TC_DECLARE(64, 2, 1, 2)
-TC_DECLARE(64, 1, 1, 1)
-TC_DECLARE(128, 1, 1, 1)
-TC_DECLARE(128, 2, 1, 1)
-TC_DECLARE(256, 2, 1, 1)
-TC_DECLARE(64, 1, 1, 4)
-TC_DECLARE(128, 1, 1, 4)
-TC_DECLARE(256, 2, 1, 4)
+TC_DECLARE(64, 1, 2)
+TC_DECLARE(128, 1, 2)
+TC_DECLARE(256, 1, 2)
+TC_DECLARE(128, 2, 2)
+TC_DECLARE(256, 2, 2)
+TC_DECLARE(64, 2, 2)
+TC_DECLARE(64, 1, 1)
+TC_DECLARE(128, 1, 1)
+TC_DECLARE(128, 2, 1)
+TC_DECLARE(256, 2, 1)
+TC_DECLARE(64, 1, 4)
+TC_DECLARE(128, 1, 4)
+TC_DECLARE(256, 2, 4)
 
 namespace {
 struct Entry {
@@ -40,16 +37,14 @@ struct Entry {
   LaunchFn launch;
 };
 const Entry kEntries[kNumTileConfigs] = {
-    TC_ENTRY(64, 1, 1, 2),  TC_ENTRY(128, 1, 1, 2), TC_ENTRY(256, 1, 1, 2), TC_ENTRY(128, 2, 1, 2),
-    TC_ENTRY(256, 2, 1, 2), TC_ENTRY(256, 2, 2, 2), TC_ENTRY(64, 2, 1, 2),  TC_ENTRY(64, 1, 1, 1),
-    TC_ENTRY(128, 1, 1, 1), TC_ENTRY(128, 2, 1, 1), TC_ENTRY(256, 2, 1, 1), TC_ENTRY(64, 1, 1, 4),
-    TC_ENTRY(128, 1, 1, 4), TC_ENTRY(256, 2, 1, 4)};
+    TC_ENTRY(64, 1, 2),  TC_ENTRY(128, 1, 2), TC_ENTRY(256, 1, 2), TC_ENTRY(128, 2, 2), TC_ENTRY(256, 2, 2),
+    TC_ENTRY(64, 2, 2),  TC_ENTRY(64, 1, 1),  TC_ENTRY(128, 1, 1), TC_ENTRY(128, 2, 1), TC_ENTRY(256, 2, 1),
+    TC_ENTRY(64, 1, 4),  TC_ENTRY(128, 1, 4), TC_ENTRY(256, 2, 4)};
 }  // namespace
 
 const TileConfig kTileConfigs[kNumTileConfigs] = {
-    {64, 1, 1, 2},  {128, 1, 1, 2}, {256, 1, 1, 2}, {128, 2, 1, 2}, {256, 2, 1, 2}, {256, 2, 2, 2},
-    {64, 2, 1, 2},  {64, 1, 1, 1},  {128, 1, 1, 1}, {128, 2, 1, 1}, {256, 2, 1, 1}, {64, 1, 1, 4},
-    {128, 1, 1, 4}, {256, 2, 1, 4}};
+    {64, 1, 2},  {128, 1, 2}, {256, 1, 2}, {128, 2, 2}, {256, 2, 2}, {64, 2, 2}, {64, 1, 1},
+    {128, 1, 1}, {128, 2, 1}, {256, 2, 1}, {64, 1, 4},  {128, 1, 4}, {256, 2, 4}};
 
 int tc_stages(int cfg) { return cfg >= 0 && cfg < kNumTileConfigs ? kEntries[cfg].stages : 0; }
 

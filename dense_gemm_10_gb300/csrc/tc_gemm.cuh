@@ -19,12 +19,6 @@
 //    and half of the tile's Q columns, and the leader CTA issues
 //    tcgen05.mma.cta_group::2 with M = 256, which reads both CTAs' shared memory.
 //    Per SM this halves the Q traffic from L2 for the same tile width.
-//  * MC == 2 puts two CTA pairs in one cluster of four on neighbouring tiles of
-//    the same tile row: they need the same P rows, so each pair loads half of
-//    them and the tensor-memory-accelerator multicast writes that half into
-//    both pairs ("CUDA GEMM 矩阵乘法优化指南" 13.3: one read, several CTAs).  A
-//    stage is reused only after both pairs' MMAs have released it.  L2 reads
-//    per k-block fall from 128 KB to 96 KB per four SMs.
 //  * The fp32 accumulator lives in Tensor Memory, double-buffered so that the
 //    epilogue of one tile overlaps the main loop of the next (the ping-pong idea
 //    of "GPU GEMM 优化完全拆解（三）", Hopper 时代的三种 kernel 设计).
@@ -49,15 +43,14 @@
 
 namespace g10 {
 
-template <int BN, int CG, int MC>
+template <int BN, int CG>
 struct TcConfig {
   static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
   static_assert(CG == 1 || CG == 2, "CTA group");
   // a CTA pair with BN == 64 loads 32-row halves of Q: K-major Q only (an
   // M/N-major swizzle atom is 64 elements wide); the planner enforces it
   static_assert(CG == 1 || BN >= 64, "a CTA pair needs at least 32-row halves of Q");
-  static_assert(MC == 1 || (MC == 2 && CG == 2), "multicast runs on CTA pairs");
-  static constexpr int kCluster = CG * MC;       // CTAs per cluster
+  static constexpr int kCluster = CG;           // CTAs per cluster
   static constexpr int kTileM = kBM * CG;        // rows of D per tile
   static constexpr int kQRows = BN / CG;         // rows of Q this CTA loads per k-block
   static constexpr int kABytes = kBM * kSliceBytes;  // this CTA's P tile: 128 rows x 128 bytes
@@ -84,6 +77,7 @@ struct TcCtrl {
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t mma_done;
+  uint64_t c_full[4][2];  // per epilogue warp and staging buffer: a block of old C has landed
   uint32_t tmem_base;
   uint32_t abort;
   uint32_t last;
@@ -94,21 +88,26 @@ static_assert(sizeof(TcCtrl) <= 256, "control block");
 // by 64 k-rows; atoms follow each other along M / N.
 constexpr uint32_t kMnAtomBytes = 64 * 128;
 
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, TcCtrl* ctrl,
-                                             const TcArgs& a, int role, int which,
-                                             bool honor_abort) {
+__device__ __forceinline__ bool wait_bounded_raw(uint32_t bar, uint32_t parity, TcCtrl* ctrl, int32_t* status,
+                                                 uint64_t limit_ns, int role, int which, bool honor_abort) {
   if (mbar_try_wait(bar, parity)) return true;
   volatile uint32_t* abort_flag = &ctrl->abort;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (honor_abort && *abort_flag) return false;
-    if (global_timer_ns() - t0 > a.wait_limit_ns) {
+    if (global_timer_ns() - t0 > limit_ns) {
       *abort_flag = 1u;
-      atomicCAS(a.status, 0, kStatusTimeout | (role << 8) | (which << 12));
+      atomicCAS(status, 0, kStatusTimeout | (role << 8) | (which << 12));
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, TcCtrl* ctrl,
+                                             const TcArgs& a, int role, int which,
+                                             bool honor_abort) {
+  return wait_bounded_raw(bar, parity, ctrl, a.status, a.wait_limit_ns, role, which, honor_abort);
 }
 
 // Lane 0 of a converged warp waits; the whole warp gets the outcome, so the
@@ -136,6 +135,7 @@ struct COut {
   bool vec;          // c_sj == 1 and rows 16-byte aligned: 16-byte stores
   int32_t tma;       // kBulkNone, kBulkRows or kBulkTransposed
   bool has_ops;      // any fused bias / activation / output scale
+  bool blend_load;   // beta != 0 with bulk row stores: old C arrives by tensor loads
   EpiOps ops;
 };
 
@@ -152,6 +152,7 @@ __device__ __forceinline__ COut make_cout(const TcArgs& a) {
   o.tma = a.tma_store;
   o.ops = a.ops;
   o.has_ops = a.ops.any();
+  o.blend_load = a.beta != 0.0f && a.tma_store == kBulkRows;
   return o;
 }
 
@@ -325,6 +326,15 @@ struct EpiOut {
   void* c0;          // C of batch 0; c.C points at the current tile's batch
   int nstore;        // bulk stores issued from the current buffers
   bool ring;         // buffers in the operand ring: no reuse, no waits
+  // beta != 0 with bulk stores: the old C of each 32-row block is loaded by the
+  // copy engine into the staging buffer it will leave from, one block ahead
+  uint32_t cbar;     // this warp's two mbarriers (buffer 0, buffer 1: 8 bytes apart)
+  uint32_t cphase;   // bit b: parity of buffer b's next load
+  uint32_t pending;  // bit b: a load into buffer b not yet waited for
+  int jend;          // first column past the current tile
+  TcCtrl* ctrl;
+  int32_t* status;
+  uint64_t wait_ns;
 
   __device__ __forceinline__ void use_ring(uint32_t base) {
     staging = base;
@@ -364,6 +374,105 @@ struct EpiOut {
       st_shared_v4(row + ((k ^ sw) << 4), __float_as_uint(v[4 * k]), __float_as_uint(v[4 * k + 1]),
                    __float_as_uint(v[4 * k + 2]), __float_as_uint(v[4 * k + 3]));
     __syncwarp();
+  }
+
+  // Old C for the blend: the copy engine loads the block at column x of the
+  // warp's 32 rows into staging buffer `slot` (the block's own bulk store will
+  // leave from it), once the store that last read that buffer is done.
+  __device__ __forceinline__ void load_block(int slot, int x) {
+    if (lane == 0) {
+      bulk_wait_group_read<0>();
+      const uint32_t bar = cbar + static_cast<uint32_t>(slot * 8);
+      mbar_arrive_expect_tx(bar, kStagingBuf);
+      tma_load_3d(staging + static_cast<uint32_t>(slot * kStagingBuf), map_c, bar, x, y0, z);
+    }
+    pending |= 1u << slot;
+    __syncwarp();
+  }
+
+  // Wait (bounded) until buffer `slot`'s load has landed.
+  __device__ __forceinline__ void wait_block(int slot, bool honor_abort) {
+    int ok = 1;
+    if (lane == 0)
+      ok = wait_bounded_raw(cbar + static_cast<uint32_t>(slot * 8), (cphase >> slot) & 1u, ctrl, status, wait_ns,
+                            kRoleEpilogue, kBarCLoad, honor_abort) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) {  // a load that gave up may still land: its phase is not consumed
+      cphase ^= 1u << slot;
+      pending &= ~(1u << slot);
+    }
+  }
+
+  // The first block of a tile whose columns run from jt to jend (exclusive).
+  __device__ __forceinline__ void begin_tile(int jt, int jend_) {
+    if (!c.blend_load) return;
+    jend = jend_;
+    load_block(nstore & 1, jt);
+  }
+
+  // No load may still be writing shared memory when the warp leaves.
+  __device__ __forceinline__ void drain_loads() {
+    for (int b = 0; b < 2; ++b)
+      if (pending & (1u << b)) wait_block(b, false);
+  }
+
+  // Bulk row stores with beta != 0: this block's old C is in its staging
+  // buffer (loaded one block ahead); each thread reads its row's values, adds
+  // beta times them to its own, applies the fused operations and writes the
+  // row back in place, and the block leaves through one bulk tensor store.
+  // Every byte of C crosses the shared-memory port four times (load, read,
+  // write, store), against two plus a global load and store through L1 when
+  // the blend read and wrote C directly.
+  __device__ __forceinline__ void put_blend(int i, int j, const float (&vin)[32], int half) {
+    const bool wide = c.type == kCF32;
+    const int slot = nstore & 1;
+    const uint32_t buf = staging + static_cast<uint32_t>(slot * kStagingBuf);
+    if (wide || half == 0) {
+      const int jn = j + (wide ? 32 : 64);
+      if (jn < jend) load_block(slot ^ 1, jn);
+      wait_block(slot, false);
+    }
+    float v[32];
+    const uint32_t row = buf + static_cast<uint32_t>(lane * 128);
+    const uint32_t sw = static_cast<uint32_t>(lane & 7);  // 128-byte swizzle of 16-byte pieces
+    if (wide) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float4 o = ld_shared_v4_f32(row + ((k ^ sw) << 4));
+        v[4 * k] = vin[4 * k] + c.beta * o.x;
+        v[4 * k + 1] = vin[4 * k + 1] + c.beta * o.y;
+        v[4 * k + 2] = vin[4 * k + 2] + c.beta * o.z;
+        v[4 * k + 3] = vin[4 * k + 3] + c.beta * o.w;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4 o = ld_shared_v4_f32(row + (((4 * half + k) ^ sw) << 4));
+        const uint32_t w[4] = {__float_as_uint(o.x), __float_as_uint(o.y), __float_as_uint(o.z), __float_as_uint(o.w)};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float2 f = unpack2(c.type, w[t]);
+          v[8 * k + 2 * t] = vin[8 * k + 2 * t] + c.beta * f.x;
+          v[8 * k + 2 * t + 1] = vin[8 * k + 2 * t + 1] + c.beta * f.y;
+        }
+      }
+    }
+    // (the whole warp: the bias shuffle needs every lane; rows past I compute
+    // values the clipped store drops)
+    if (c.has_ops) apply_ops32(c.ops, v, lane, i < c.I ? i : c.I - 1, j, c.J - j < 32 ? c.J - j : 32);
+    if (wide) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        st_shared_v4(row + ((k ^ sw) << 4), __float_as_uint(v[4 * k]), __float_as_uint(v[4 * k + 1]),
+                     __float_as_uint(v[4 * k + 2]), __float_as_uint(v[4 * k + 3]));
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        st_shared_v4(row + (((4 * half + k) ^ sw) << 4), pack2(c.type, v[8 * k], v[8 * k + 1]),
+                     pack2(c.type, v[8 * k + 2], v[8 * k + 3]), pack2(c.type, v[8 * k + 4], v[8 * k + 5]),
+                     pack2(c.type, v[8 * k + 6], v[8 * k + 7]));
+    }
+    if (wide || half == 1) issue(buf, wide ? j : j - 32, y0);
   }
 
   // Direct stores when the rows of C are contiguous (unswapped problems): the
@@ -511,8 +620,12 @@ struct EpiOut {
         store_chunk(c, i, j, vin);
       return;
     }
-    // bulk paths run with beta == 0: the fused operations apply to alpha * D,
-    // inside C only (the bias holds no value for the clipped edge of a tile)
+    if (c.blend_load) {
+      put_blend(i, j, vin, half);
+      return;
+    }
+    // the other bulk paths run with beta == 0: the fused operations apply to
+    // alpha * D, inside C only (the bias holds no value for the clipped edge of a tile)
     float v[32];
 #pragma unroll
     for (int t = 0; t < 32; ++t) v[t] = vin[t];
@@ -560,6 +673,7 @@ struct EpiOut {
   // Before the CTA exits, every bulk store must have read its staging buffer;
   // the global writes complete with the grid, like any other store.
   __device__ __forceinline__ void finish() {
+    drain_loads();
     if (c.tma != kBulkNone) {
       if (lane == 0) bulk_wait_group_read<0>();
       __syncwarp();
@@ -569,16 +683,12 @@ struct EpiOut {
 
 // ----------------------------------------------------------------- the roles --
 
-template <int BN, int CG, int MC, int EB, int KD>
+template <int BN, int CG, int EB, int KD>
 __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CUtensorMap* map_q,
                                               const TcArgs& a, uint8_t* ring_a, uint8_t* ring_b,
                                               TcCtrl* ctrl, uint32_t rank, int first, int stride) {
-  using Cfg = TcConfig<BN, CG, MC>;
-  const int q = static_cast<int>(rank) % CG;      // rank inside the CTA pair
-  const int pair = static_cast<int>(rank) / CG;   // which pair of the cluster
-  const uint32_t leader = static_cast<uint32_t>(pair * CG);
-  // multicast of P: this CTA and the CTA of the other pair with the same rank inside its pair
-  const uint16_t p_mask = static_cast<uint16_t>((1u << q) | (1u << (q + CG)));
+  using Cfg = TcConfig<BN, CG>;
+  const int q = static_cast<int>(rank);  // rank inside the CTA pair (0: the leader)
   constexpr int kSliceK = slice_k(EB);  // k elements of one 128-byte slice
   // 8- and 32-bit operands are always K-major (the planner admits no other layout)
   const bool p_kmajor = EB != 2 || a.p_kmajor != 0;
@@ -594,7 +704,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
   while (ok && work.next(w)) {
     // (grouped GEMMs: the group's rows start further down P)
     const int i0 = (a.sched.groups > 0 ? static_cast<int>(a.group_row[w.tb]) : 0) + w.ti * Cfg::kTileM + q * kBM;
-    const int j0 = (w.tj * MC + pair) * BN + q * Cfg::kQRows;
+    const int j0 = w.tj * BN + q * Cfg::kQRows;
     const int zp = a.p_bcast ? 0 : w.tb;  // batch coordinate (0 for an operand shared by all batches)
     const int zq = a.q_bcast ? 0 : w.tb;
     // (three-product fp32 GEMM: segment and k-slice within it of the unit's first k-slice)
@@ -614,7 +724,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
       ++nload;
       const uint32_t full_local = smem_u32(&ctrl->full[stage]);
       // A pair credits both CTAs' bytes to the leader's barrier, which the MMA waits on.
-      const uint32_t full = CG == 2 ? mapa_shared(full_local, leader) : full_local;
+      const uint32_t full = CG == 2 ? mapa_shared(full_local, 0) : full_local;
       if (a.drop_load != 0 && blockIdx.x == 0 && nload == a.drop_load) {
         pending &= ~(1u << stage);  // test hook: this stage's barrier is never completed
       } else {
@@ -628,9 +738,6 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
               tma_load_3d_pair(dst, map, full, x, y, z);
             else
               tma_load_3d(dst, map, full, x, y, z);
-          };
-          auto load_mc = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z) {
-            tma_load_3d_pair_multicast(dst, map, full, x, y, z, p_mask);
           };
 #pragma unroll
           for (int t = 0; t < KD; ++t) {
@@ -653,13 +760,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
                 }
               }
             }
-            if constexpr (MC == 2) {
-              // this pair's half of the P tile: 64 rows (K-major) or one 64-wide atom (M-major)
-              if (p_kmajor)
-                load_mc(sa + pair * 64 * 128, map_p, k0, i0 + 64 * pair, zp);
-              else
-                load_mc(sa + pair * kMnAtomBytes, map_p, i0 + 64 * pair, k0, zp);
-            } else if (p_kmajor) {
+            if (p_kmajor) {
               load(sa, map_p, k0, i0, zp);
             } else {
               load(sa, map_p, i0, k0, zp);
@@ -696,11 +797,11 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
   __syncwarp();
 }
 
-template <int BN, int CG, int MC, int EB, int KD>
+template <int BN, int CG, int EB, int KD>
 __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8_t* ring_b,
                                          TcCtrl* ctrl, uint32_t tmem_base, uint32_t rank, int first,
                                          int stride) {
-  using Cfg = TcConfig<BN, CG, MC>;
+  using Cfg = TcConfig<BN, CG>;
   constexpr int kSliceK = slice_k(EB);  // k elements of one 128-byte slice
   // 8- and 32-bit operands are always K-major (the planner admits no other layout)
   const bool p_kmajor = EB != 2 || a.p_kmajor != 0;
@@ -710,19 +811,12 @@ __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8
   uint32_t phase = 0;
   int it = 0;
   bool ok = true;
-  // A stage is freed in every CTA of the cluster (with multicast the other pair
-  // writes into it too); the accumulator is handed to the pair's two epilogues.
-  const uint16_t all_mask = static_cast<uint16_t>((1u << Cfg::kCluster) - 1u);
-  const uint16_t pair_mask = static_cast<uint16_t>(((1u << CG) - 1u) << rank);
-  auto commit_stage = [&](uint32_t bar) {
+  // A stage is freed, and the accumulator handed to the epilogues, in both
+  // CTAs of a pair (each CTA's copies land in its own shared memory and each
+  // CTA's epilogue reads its own rows of the accumulator).
+  auto commit_both = [&](uint32_t bar) {
     if constexpr (CG == 2)
-      mma_commit_pair(bar, all_mask);
-    else
-      mma_commit<1>(bar);
-  };
-  auto commit_acc = [&](uint32_t bar) {
-    if constexpr (CG == 2)
-      mma_commit_pair(bar, pair_mask);
+      mma_commit_pair(bar, 0x3);
     else
       mma_commit<1>(bar);
   };
@@ -764,7 +858,7 @@ __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8
             mma_ss<CG, EB>(d_tmem, ad0 + ((a_step * k) >> 4), bd0 + ((b_step * k) >> 4), a.idesc,
                            (kb > w.kb0 || t > 0 || k > 0) ? 1u : 0u);
         }
-        commit_stage(smem_u32(&ctrl->empty[stage]));  // frees the stage once these MMAs have read it
+        commit_both(smem_u32(&ctrl->empty[stage]));  // frees the stage once these MMAs have read it
       }
       __syncwarp();
       if (++stage == a.stages) {
@@ -773,7 +867,7 @@ __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8
       }
     }
     if (!ok) break;
-    if (elect_one()) commit_acc(smem_u32(&ctrl->acc_full[buf]));  // accumulator ready for the epilogues
+    if (elect_one()) commit_both(smem_u32(&ctrl->acc_full[buf]));  // accumulator ready for the epilogues
     __syncwarp();
   }
   // Tensor Memory is freed only after every MMA issued here has finished.  The
@@ -785,16 +879,14 @@ __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8
   __syncwarp();
 }
 
-template <int BN, int CG, int MC, int EB>
+template <int BN, int CG, int EB>
 __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap* map_c,
                                               uint8_t* staging, uint8_t* ring, TcCtrl* ctrl,
                                               uint32_t tmem_base,
                                               int warp, int lane, uint32_t rank, int first,
                                               int stride) {
-  using Cfg = TcConfig<BN, CG, MC>;
-  const int q = static_cast<int>(rank) % CG;
-  const int pair = static_cast<int>(rank) / CG;
-  const uint32_t leader = static_cast<uint32_t>(pair * CG);
+  using Cfg = TcConfig<BN, CG>;
+  const int q = static_cast<int>(rank);  // rank inside the CTA pair (0: the leader)
   const int quarter = warp & 3;  // a warp may only read TMEM lanes 32*(warp%4) .. +31
   const int row = quarter * 32 + lane;
   const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -808,6 +900,13 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
   out.lane = lane;
   out.nstore = 0;
   out.ring = false;
+  out.cbar = smem_u32(&ctrl->c_full[warp - 2][0]);
+  out.cphase = 0;
+  out.pending = 0;
+  out.jend = 0;
+  out.ctrl = ctrl;
+  out.status = a.status;
+  out.wait_ns = a.wait_limit_ns;
   const int64_t esize = a.c_type == kCF32 ? 4 : a.c_type == kCE4M3 ? 1 : 2;
   int it = 0;
   WorkIter work(a.sched, first, stride);
@@ -815,11 +914,18 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
   for (; work.next(w); ++it) {
     const int buf = it & 1;
     const uint32_t acc_parity = (it >> 1) & 1;
+    const int i = w.ti * Cfg::kTileM + q * kBM + row;
+    const int jt = w.tj * BN;  // first column of the tile
+    out.y0 = w.ti * Cfg::kTileM + q * kBM + quarter * 32;
+    out.z = w.tb;
+    // beta != 0 with bulk stores: the tile's first block of old C loads while
+    // the accumulator is still being computed
+    if (!w.partial) out.begin_tile(jt, jt + BN);
     const bool ok = wait_bounded(smem_u32(&ctrl->acc_full[buf]), acc_parity, ctrl, a,
                                  kRoleEpilogue, kBarAccFull, true);
     if (bar_any(1, 128, !ok)) break;  // all four epilogue warps leave together
     tc_fence_after_sync();
-    if (out.c.tma != kBulkNone && !out.ring) {
+    if (out.c.tma != kBulkNone && !out.ring && !out.c.blend_load) {
       WorkIter peek = work;
       Unit next_unit;
       // This CTA's last unit: its copies have landed and its MMAs (the pair's)
@@ -829,7 +935,7 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
     const uint32_t taddr = lane_base + static_cast<uint32_t>(buf * BN);
     // the MMA (leader CTA) waits until every epilogue thread of the pair has read the buffer
     const uint32_t acc_empty_local = smem_u32(&ctrl->acc_empty[buf]);
-    const uint32_t acc_empty = CG == 2 ? mapa_shared(acc_empty_local, leader) : acc_empty_local;
+    const uint32_t acc_empty = CG == 2 ? mapa_shared(acc_empty_local, 0) : acc_empty_local;
     auto release = [&]() {
       tc_fence_before_sync();
       if constexpr (CG == 2)
@@ -837,10 +943,6 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
       else
         mbar_arrive(acc_empty);
     };
-    const int i = w.ti * Cfg::kTileM + q * kBM + row;
-    const int jt = (w.tj * MC + pair) * BN;  // first column of this pair's tile
-    out.y0 = w.ti * Cfg::kTileM + q * kBM + quarter * 32;
-    out.z = w.tb;
     {
       if (a.sched.groups > 0) {  // the group's rows of C; rows past its count are not stored
         out.c.C = static_cast<char*>(out.c0) + a.group_row[w.tb] * a.c_si * esize;
@@ -927,6 +1029,7 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
       }
       bar_sync(1, 128);
       if (*reinterpret_cast<volatile uint32_t*>(&ctrl->last)) {
+        out.begin_tile(jt, jt + BN);
         // 64 columns per round: 16 independent 16-byte loads per contribution in
         // flight (the sum is latency-bound, one L2 round trip per round).
 #pragma unroll 1
@@ -968,12 +1071,12 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
   out.finish();  // every bulk store has read its staging buffer before the CTA can exit
 }
 
-template <int BN, int CG, int MC, int EB>
+template <int BN, int CG, int EB>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p,
                    const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_c, const TcArgs args) {
-  using Cfg = TcConfig<BN, CG, MC>;
+  using Cfg = TcConfig<BN, CG>;
   // The roles take the arguments by reference; a local copy whose address never
   // leaves this kernel lets the compiler keep the fields in registers across
   // the global stores and "memory"-clobbering asm of the loops, instead of
@@ -993,8 +1096,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // A CTA pair shares each tile; its even rank is the leader that issues the MMAs.
-  // A cluster (one or two pairs, or one CTA) walks the schedule as one slot.
+  // A CTA pair shares each tile; its rank-0 CTA is the leader that issues the MMAs.
+  // A cluster (a pair, or one CTA) walks the schedule as one slot.
   constexpr int kCl = Cfg::kCluster;
   const uint32_t rank = kCl > 1 ? cluster_ctarank() : 0u;
   const int first = static_cast<int>(blockIdx.x) / kCl;
@@ -1003,13 +1106,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::kStages; ++s) {
       mbar_init(smem_u32(&ctrl->full[s]), 1);
-      mbar_init(smem_u32(&ctrl->empty[s]), MC);  // one release per pair using the stage
+      mbar_init(smem_u32(&ctrl->empty[s]), 1);  // released by the pair's MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctrl->acc_full[b]), 1);
       mbar_init(smem_u32(&ctrl->acc_empty[b]), 128 * CG);
     }
     mbar_init(smem_u32(&ctrl->mma_done), 1);
+    for (int w = 0; w < 4; ++w)
+      for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&ctrl->c_full[w][b]), 1);
     ctrl->abort = 0;
     ctrl->last = 0;
     fence_barrier_init();
@@ -1037,18 +1142,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the one-slice loop compiles to the same straight-line issue code as
     // before two-slice stages existed (a runtime trip count cost ~12% at 4096^3)
     if (a.kdepth == 2)
-      producer_role<BN, CG, MC, EB, 2>(&map_p, &map_q, a, ring_a, ring_b, ctrl, rank, first, stride);
+      producer_role<BN, CG, EB, 2>(&map_p, &map_q, a, ring_a, ring_b, ctrl, rank, first, stride);
     else
-      producer_role<BN, CG, MC, EB, 1>(&map_p, &map_q, a, ring_a, ring_b, ctrl, rank, first, stride);
+      producer_role<BN, CG, EB, 1>(&map_p, &map_q, a, ring_a, ring_b, ctrl, rank, first, stride);
   } else if (warp == 1) {
     if (rank % CG == 0) {
       if (a.kdepth == 2)
-        mma_role<BN, CG, MC, EB, 2>(a, ring_a, ring_b, ctrl, tmem_base, rank, first, stride);
+        mma_role<BN, CG, EB, 2>(a, ring_a, ring_b, ctrl, tmem_base, rank, first, stride);
       else
-        mma_role<BN, CG, MC, EB, 1>(a, ring_a, ring_b, ctrl, tmem_base, rank, first, stride);
+        mma_role<BN, CG, EB, 1>(a, ring_a, ring_b, ctrl, tmem_base, rank, first, stride);
     }
   } else {
-    epilogue_role<BN, CG, MC, EB>(a, &map_c, staging, ring_a, ctrl, tmem_base, warp, lane, rank, first,
+    epilogue_role<BN, CG, EB>(a, &map_c, staging, ring_a, ctrl, tmem_base, warp, lane, rank, first,
                               stride);
   }
 

@@ -1,0 +1,5 @@
+// Tile width 64, one CTA per tile; 8-bit float inputs (tcgen05.mma kind::f8f6f4).
+#define TC_BN 64
+#define TC_CG 1
+#define TC_EB 1
+#include "tc_gemm_inst.cuh"

@@ -1,28 +1,28 @@
 // tc_gemm_inst.cuh -- one instantiation of the tcgen05 GEMM kernel per
-// translation unit (TC_BN, TC_CG, TC_MC and TC_EB set by the including file),
-// so the tile configurations compile in parallel.
+// translation unit (TC_BN, TC_CG and TC_EB set by the including file), so the
+// tile configurations compile in parallel.
 #include "tc_gemm.cuh"
 
-#define TC_CAT8(a, b, c, d, e, f, g, h) a##b##c##d##e##f##g##h
-#define TC_NAME(a, b, c, d, e, f, g, h) TC_CAT8(a, b, c, d, e, f, g, h)
-#define TC_KERNEL tc_gemm_kernel<TC_BN, TC_CG, TC_MC, TC_EB>
+#define TC_CAT6(a, b, c, d, e, f) a##b##c##d##e##f
+#define TC_NAME(a, b, c, d, e, f) TC_CAT6(a, b, c, d, e, f)
+#define TC_KERNEL tc_gemm_kernel<TC_BN, TC_CG, TC_EB>
 
 namespace g10 {
 
-cudaError_t TC_NAME(tc_prepare_bn, TC_BN, _cg, TC_CG, _mc, TC_MC, _eb, TC_EB)(int* max_clusters) {
-  using Cfg = TcConfig<TC_BN, TC_CG, TC_MC>;
+cudaError_t TC_NAME(tc_prepare_bn, TC_BN, _cg, TC_CG, _eb, TC_EB)(int* max_clusters) {
+  using Cfg = TcConfig<TC_BN, TC_CG>;
   cudaError_t e = cudaFuncSetAttribute(TC_KERNEL,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(Cfg::kSmemBytes));
-  if (e != cudaSuccess || TC_CG * TC_MC == 1) return e;
-  // How many clusters can be resident at once (a cluster must sit inside one GPC).
+  if (e != cudaSuccess || TC_CG == 1) return e;
+  // How many CTA pairs can be resident at once (a cluster must sit inside one GPC).
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = TC_CG * TC_MC;
+  attr[0].val.clusterDim.x = TC_CG;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(TC_CG * TC_MC, 1, 1);
+  cfg.gridDim = dim3(TC_CG, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = Cfg::kSmemBytes;
   cfg.attrs = attr;
@@ -30,17 +30,17 @@ cudaError_t TC_NAME(tc_prepare_bn, TC_BN, _cg, TC_CG, _mc, TC_MC, _eb, TC_EB)(in
   return cudaOccupancyMaxActiveClusters(max_clusters, TC_KERNEL, &cfg);
 }
 
-cudaError_t TC_NAME(tc_launch_bn, TC_BN, _cg, TC_CG, _mc, TC_MC, _eb, TC_EB)(
+cudaError_t TC_NAME(tc_launch_bn, TC_BN, _cg, TC_CG, _eb, TC_EB)(
     const CUtensorMap& map_p, const CUtensorMap& map_q, const CUtensorMap& map_c, const TcArgs& args,
     int grid, cudaStream_t stream) {
-  using Cfg = TcConfig<TC_BN, TC_CG, TC_MC>;
+  using Cfg = TcConfig<TC_BN, TC_CG>;
   const size_t smem = Cfg::kSmemBytes;  // every epilogue stages C (bulk or direct stores)
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   unsigned n = 0;
-  if (TC_CG * TC_MC > 1) {
+  if (TC_CG > 1) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = TC_CG * TC_MC;
+    attr[n].val.clusterDim.x = TC_CG;
     attr[n].val.clusterDim.y = 1;
     attr[n].val.clusterDim.z = 1;
     ++n;

@@ -36,7 +36,7 @@ E4M3_F32, E5M2_F32, E4M3_BF16, E5M2_BF16 = fp8_dtype(), fp8_dtype("e5m2", "e5m2"
 STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED", 3: "GEMM_ERR_NO_DEVICE",
           4: "GEMM_ERR_CUDA", 5: "GEMM_ERR_TENSORMAP", 6: "GEMM_ERR_TIMEOUT", 7: "GEMM_ERR_WORKSPACE"}
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NO_DEVICE, ERR_CUDA, ERR_TENSORMAP, ERR_TIMEOUT, ERR_WORKSPACE = range(8)
-PATH_NOOP, PATH_SCALE_C, PATH_TC_1CTA, PATH_TC_2CTA, PATH_TC_2CTA_MULTICAST = 0, 1, 2, 3, 4
+PATH_NOOP, PATH_SCALE_C, PATH_TC_1CTA, PATH_TC_2CTA = 0, 1, 2, 3
 (OPT_WAIT_LIMIT_NS, OPT_FORCE_PATH, OPT_SPLIT_K, OPT_RASTER_GROUP, OPT_FORCE_BN, OPT_TEST_DROP_LOAD, OPT_MAX_GRID,
  OPT_STREAM_K, OPT_STAGES) = range(9)
 OPT_EPILOGUE = 10
@@ -81,6 +81,8 @@ SIGNATURES = {
     "gemm_launch_count": (_i32, [_vp, ctypes.POINTER(_u64)]),
     "gemm_run_noalloc": (_i32, [_i32, _i32, _i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _i32,
                                 _vp]),
+    "gemm_noalloc_get_status": (_i32, [_vp, ctypes.POINTER(_i32)]),
+    "gemm_noalloc_set_option": (_i32, [_i32, _i64]),
     "gemm_run_ex": (_i32, [_vp, _i32, _i32, _i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64,
                            _i32, ctypes.POINTER(Epilogue), _vp]),
     "gemm_run_strided_batched": (_i32, [_vp, _i32, _i32, _i64, _i64, _i64, _f32, _vp, _i64, _i64, _vp, _i64,
@@ -92,6 +94,7 @@ SIGNATURES = {
     "gemm_plan_grouped": (_i32, [_vp, ctypes.c_int, _i32, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _f32, _vp,
                                  _i64, _i32, ctypes.POINTER(Plan)]),
     "gemm_plan_cache_stats": (_i32, [_vp, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]),
+    "gemm_tensor_map_cache_stats": (_i32, [_vp, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]),
     "gemm_probe_tma_tile": (_i32, [_vp, _vp, _i64, _i64, _i64, _vp, _vp]),
     "gemm_run_host": (_i32, [_vp, _i32, _i32, _i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _i32,
                              _vp]),
@@ -207,6 +210,13 @@ class Handle:
         hits, misses = ctypes.c_uint64(), ctypes.c_uint64()
         _check(lib().gemm_plan_cache_stats(self.ptr, ctypes.byref(hits), ctypes.byref(misses)),
                "gemm_plan_cache_stats")
+        return hits.value, misses.value
+
+    def tensor_map_cache_stats(self):
+        """(hits, misses) of the handle's tensor-map cache."""
+        hits, misses = ctypes.c_uint64(), ctypes.c_uint64()
+        _check(lib().gemm_tensor_map_cache_stats(self.ptr, ctypes.byref(hits), ctypes.byref(misses)),
+               "gemm_tensor_map_cache_stats")
         return hits.value, misses.value
 
     def run_block_scaled_raw(self, M, N, K, alpha, A, lda, SFA, ld_sfa, B, ldb, SFB, ld_sfb, beta, C, ldc, dtype,

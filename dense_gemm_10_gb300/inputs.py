@@ -13,6 +13,10 @@ Recipe (one rule for every workload):
     stay inside the 8-bit formats' ranges);
   * a matrix is drawn directly in its stored shape (row-major storage, see
     ``Problem``), so the "op" flags change the layout, not the distribution;
+    the one exception is a problem made with ``logical=True`` (the fp16
+    blend workload): there op(A) (M x K) and op(B) (K x N) are drawn in their
+    logical shapes and stored transposed where the layout says, so that every
+    layout of the workload multiplies the same two matrices;
   * padding columns beyond a leading dimension hold a NaN bit pattern, so a
     kernel that reads past the logical width shows up as NaN in its output.
 """
@@ -110,7 +114,8 @@ class Problem:
 
 def make_problem(name, M, N, K, transA=0, transB=0, in_dtype="bf16", out_dtype="f32",
                  dist_a=("uniform", -1.0, 1.0), dist_b=("uniform", -1.0, 1.0), alpha=1.0,
-                 beta=0.0, dist_c=("normal", 0.0, 1.0), seed=0, lda=None, ldb=None, ldc=None, b_dtype=None):
+                 beta=0.0, dist_c=("normal", 0.0, 1.0), seed=0, lda=None, ldb=None, ldc=None, b_dtype=None,
+                 logical=False):
     b_dtype = in_dtype if b_dtype is None else b_dtype
     a_shape = (K, M) if transA else (M, K)
     b_shape = (N, K) if transB else (K, N)
@@ -119,13 +124,21 @@ def make_problem(name, M, N, K, transA=0, transB=0, in_dtype="bf16", out_dtype="
     ldc = N if ldc is None else ldc
     if lda < a_shape[1] or ldb < b_shape[1] or ldc < N:
         raise ValueError("leading dimension smaller than the stored width")
-    A = _pad_columns(draw(a_shape, dist_a, seed, in_dtype), lda, in_dtype)
-    B = _pad_columns(draw(b_shape, dist_b, seed + 1, b_dtype), ldb, b_dtype)
+    if logical:   # op(A) and op(B) drawn as M x K and K x N, stored per the layout
+        a = draw((M, K), dist_a, seed, in_dtype)
+        b = draw((K, N), dist_b, seed + 1, b_dtype)
+        a = a.t().contiguous() if transA else a
+        b = b.t().contiguous() if transB else b
+    else:
+        a = draw(a_shape, dist_a, seed, in_dtype)
+        b = draw(b_shape, dist_b, seed + 1, b_dtype)
+    A = _pad_columns(a, lda, in_dtype)
+    B = _pad_columns(b, ldb, b_dtype)
     C0 = None
     if beta != 0.0:
         C0 = _pad_columns(draw((M, N), dist_c, seed + 2, out_dtype), ldc, out_dtype)
     recipe = {"dist_a": list(dist_a), "dist_b": list(dist_b), "dist_c": list(dist_c) if beta else None,
-              "seeds": [seed, seed + 1, seed + 2]}
+              "seeds": [seed, seed + 1, seed + 2], "drawn": "logical" if logical else "stored"}
     return Problem(name, M, N, K, transA, transB, in_dtype, out_dtype, float(alpha), float(beta),
                    A, lda, B, ldb, C0, ldc, seed, recipe, b_dtype)
 
@@ -292,10 +305,11 @@ def square_4096_bf16_nt(out_dtype="f32", size=4096):
 
 
 def square_4096_f16_blend(transA, transB, size=4096):
-    """M = N = K = 4096, fp16 U[-1, 1], alpha 1.5, beta 0.5, fp32 C0 ~ N(0, 1)."""
+    """M = N = K = 4096, fp16 U[-1, 1], alpha 1.5, beta 0.5, fp32 C0 ~ N(0, 1).
+    The four layouts store the same logical A and B (drawn as M x K and K x N)."""
     lay = ("T" if transA else "N") + ("T" if transB else "N")
     return make_problem("square_%d_f16_blend_%s" % (size, lay.lower()), size, size, size, transA,
-                        transB, "f16", "f32", alpha=1.5, beta=0.5, dist_c=("normal", 0.0, 1.0))
+                        transB, "f16", "f32", alpha=1.5, beta=0.5, dist_c=("normal", 0.0, 1.0), logical=True)
 
 
 LLM_SHAPES = {

@@ -260,9 +260,7 @@ typedef enum {
   GEMM_PATH_NOOP = 0,      /* M == 0 or N == 0 */
   GEMM_PATH_SCALE_C = 1,   /* K == 0: C = beta * C */
   GEMM_PATH_TC_1CTA = 2,   /* persistent tcgen05 kernel, one CTA per output tile (cta_group::1) */
-  GEMM_PATH_TC_2CTA = 3,   /* persistent tcgen05 kernel, CTA pairs share a 256-row tile (cta_group::2) */
-  GEMM_PATH_TC_2CTA_MULTICAST = 4 /* as GEMM_PATH_TC_2CTA, two pairs per cluster of four on
-                                     neighbouring tiles sharing the A-side tile by TMA multicast */
+  GEMM_PATH_TC_2CTA = 3    /* persistent tcgen05 kernel, CTA pairs share a 256-row tile (cta_group::2) */
 } gemm_path_t;
 
 /* How C leaves the epilogue (gemm_plan_t.bulk_store). */
@@ -298,12 +296,11 @@ typedef struct {
   int64_t units;           /* work units over all CTAs (tiles, split pieces or stream-K pieces) */
   int64_t workspace_bytes; /* handle workspace this call needs */
   int32_t tiles_i;         /* schedule tiles along the MMA rows (M, or N when swapped) */
-  int32_t tiles_j;         /* schedule tiles along the MMA columns (with multicast a schedule
-                              tile is two neighbouring output tiles) */
+  int32_t tiles_j;         /* schedule tiles along the MMA columns (N, or M when swapped) */
   int32_t num_kb;          /* k-blocks of bk per tile (GEMM_F32_F32: over 3K) */
   int32_t dp_tiles;        /* tiles run whole (stream-K: the complete waves) */
   int32_t sk_slots;        /* stream-K: clusters sharing the remaining tiles' k-blocks */
-  int32_t cluster;         /* CTAs per schedule slot: 1, 2 (a pair) or 4 (two pairs, multicast) */
+  int32_t cluster;         /* CTAs per schedule slot: 1, or 2 (a CTA pair) */
   int32_t kdepth;          /* 128-byte k-slices per ring stage (1 or 2): each stage's copies
                               complete one barrier */
   int32_t bulk_store;      /* how C leaves: gemm_bulk_store_t */
@@ -416,7 +413,7 @@ gemm_status_t gemm_plan_strided_batched(gemm_handle_t h, int sm_count, gemm_op_t
 
 typedef enum {
   GEMM_OPT_WAIT_LIMIT_NS = 0, /* barrier wait limit in ns (default 2e9; >= 1e6) */
-  GEMM_OPT_FORCE_PATH = 1,    /* 0 auto, or GEMM_PATH_TC_1CTA / _2CTA / _2CTA_MULTICAST */
+  GEMM_OPT_FORCE_PATH = 1,    /* 0 auto, or GEMM_PATH_TC_1CTA / GEMM_PATH_TC_2CTA */
   GEMM_OPT_SPLIT_K = 2,       /* 0 auto, else the k-split to use (clamped to the k-blocks) */
   GEMM_OPT_RASTER_GROUP = 3,  /* 0 auto, else tile rows per raster group */
   GEMM_OPT_FORCE_BN = 4,      /* 0 auto, else 64, 128 or 256 */
@@ -455,6 +452,14 @@ gemm_status_t gemm_launch_count(gemm_handle_t h, uint64_t* count);
 /* Plan-cache counters of the handle since its creation: calls whose plan was
    reused (*hits) and calls that planned anew (*misses). */
 gemm_status_t gemm_plan_cache_stats(gemm_handle_t h, uint64_t* hits, uint64_t* misses);
+
+/* Tensor-map cache counters of the handle since its creation.  Each launch
+   needs two or three tensor maps (A, B and, for bulk stores, C); a map whose
+   description (base address, extents, strides, box, type, swizzle) matches
+   one encoded by a recent call is copied from the handle's cache (*hits)
+   instead of being encoded again (*misses).  256 maps are kept (64 sets of 4,
+   least recently used replaced). */
+gemm_status_t gemm_tensor_map_cache_stats(gemm_handle_t h, uint64_t* hits, uint64_t* misses);
 
 /*
  * gemm_probe_tma_tile (test support): load one tile of a row-major 16-bit
@@ -501,14 +506,34 @@ gemm_status_t gemm_probe_tma_tile(gemm_handle_t h, const void* src, int64_t ld, 
  * first call before any stream capture.  Every call shares the same arrays
  * and each call clears the counters and status word it uses, so calls that
  * overlap on the GPU (two streams, or two host threads) race on them: order
- * them on one stream.  A kernel that gives up on a barrier records it only in
- * the internal status word, which this entry point does not report.
+ * them on one stream.  A kernel that gives up on a barrier records it in the
+ * path's own status word; gemm_noalloc_get_status reads it.
  * Returns GEMM_OK, the argument errors of gemm_run, GEMM_ERR_NO_DEVICE,
  * GEMM_ERR_WORKSPACE or GEMM_ERR_CUDA.
  * ------------------------------------------------------------------------- */
 gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, int64_t M, int64_t N, int64_t K,
                                float alpha, const void* A, int64_t lda, const void* B, int64_t ldb,
                                float beta, void* C, int64_t ldc, gemm_dtype_t dtype, void* stream);
+
+/*
+ * gemm_noalloc_get_status: the status of the no-allocation path on the
+ * current device, like gemm_get_status for a handle.  Synchronises `stream`,
+ * reads the path's device status word and clears it.  Returns GEMM_OK,
+ * GEMM_ERR_TIMEOUT (a kernel of an earlier gemm_run_noalloc gave up waiting on
+ * a barrier and returned early; its C is incomplete) or GEMM_ERR_CUDA;
+ * *detail (may be NULL) receives the raw word (layout as gemm_get_status).
+ * Allocates nothing.  The word is shared by every no-allocation call on the
+ * device, so read it after the calls it should cover, on their stream.
+ */
+gemm_status_t gemm_noalloc_get_status(void* stream, int32_t* detail);
+
+/*
+ * gemm_noalloc_set_option: process-wide options of the no-allocation path.
+ * Only GEMM_OPT_WAIT_LIMIT_NS (>= 1e6) and GEMM_OPT_TEST_DROP_LOAD (tests:
+ * make CTA 0 skip its n-th k-block load, 0 off) are accepted; any other option
+ * returns GEMM_ERR_INVALID_ARG.  Takes effect from the next gemm_run_noalloc.
+ */
+gemm_status_t gemm_noalloc_set_option(gemm_option_t opt, int64_t value);
 
 #ifdef __cplusplus
 }

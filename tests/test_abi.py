@@ -55,6 +55,24 @@ def test_create_without_gpu_reports_no_device():
     assert G.lib().gemm_create(None, 0) == G.ERR_INVALID_ARG
 
 
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour")
+def test_noalloc_status_without_gpu_reports_no_device():
+    word = ctypes.c_int32(-1)
+    assert G.lib().gemm_noalloc_get_status(None, ctypes.byref(word)) == G.ERR_NO_DEVICE
+
+
+def test_noalloc_options_are_checked():
+    """Only the wait limit and the test hook are options of the no-allocation
+    path; out-of-range values and other options are refused on the host."""
+    L = G.lib()
+    assert L.gemm_noalloc_set_option(G.OPT_WAIT_LIMIT_NS, 999_999) == G.ERR_INVALID_ARG
+    assert L.gemm_noalloc_set_option(G.OPT_TEST_DROP_LOAD, -1) == G.ERR_INVALID_ARG
+    for opt in (G.OPT_FORCE_PATH, G.OPT_SPLIT_K, G.OPT_PDL, 99):
+        assert L.gemm_noalloc_set_option(opt, 0) == G.ERR_INVALID_ARG
+    assert L.gemm_noalloc_set_option(G.OPT_WAIT_LIMIT_NS, 2_000_000_000) == G.OK
+    assert L.gemm_noalloc_set_option(G.OPT_TEST_DROP_LOAD, 0) == G.OK
+
+
 def test_null_handle_is_rejected():
     assert G.lib().gemm_run(None, 0, 0, 4, 4, 4, 1.0, 0x1000, 4, 0x1000, 4, 0.0, 0x1000, 4, 0, None) \
         == G.ERR_INVALID_ARG
@@ -82,14 +100,14 @@ def test_product_code_never_touches_the_oracle():
 # ----------------------------------------------------------------- planner --
 
 def test_plan_square_nt():
-    """4096^3: 256 x 256 tiles on CTA pairs (two pairs per cluster when the A tile
-    is multicast); the tiles of an incomplete last wave are shared by stream-K."""
+    """4096^3: 256 x 256 tiles on CTA pairs; the tiles of an incomplete last
+    wave are shared by stream-K."""
     p = G.plan(4096, 4096, 4096, 0, 1)
-    assert p.path in (G.PATH_TC_2CTA, G.PATH_TC_2CTA_MULTICAST) and p.swap_ab == 0
-    assert p.cluster == (4 if p.path == G.PATH_TC_2CTA_MULTICAST else 2)
+    assert p.path == G.PATH_TC_2CTA and p.swap_ab == 0
+    assert p.cluster == 2
     assert p.a_kmajor == 1 and p.b_kmajor == 1
     assert p.bm == 256 and p.bk == 64 and p.bn == 256 and p.num_kb == 64
-    assert p.tiles_i == 16 and p.tiles_j == 16 // (p.cluster // 2) and p.tiles == p.tiles_i * p.tiles_j
+    assert p.tiles_i == 16 and p.tiles_j == 16 and p.tiles == p.tiles_i * p.tiles_j
     slots = 152 // p.cluster
     assert p.schedule == G.SCHED_STREAM_K and p.dp_tiles == (p.tiles // slots) * slots and 0 < p.sk_slots <= slots
     assert p.grid == 152 and p.repack_a == 0 and p.repack_b == 0
@@ -130,13 +148,16 @@ def test_plan_compute_bound_keeps_stream_k():
 
 
 def test_plan_bulk_store_paths():
-    """C leaves through bulk tensor stores of rows, of transposed blocks for a
-    swapped problem, or directly (misaligned rows, a partial 16-byte piece at
-    the right edge, or beta != 0, which reads C)."""
+    """C leaves through bulk tensor stores of rows (beta != 0 too: the old C
+    arrives by tensor loads into the same staging), of transposed blocks for a
+    swapped problem with beta == 0, or directly (misaligned rows, a partial
+    16-byte piece at the right edge, or a swapped problem with beta != 0)."""
     assert G.plan(4096, 4096, 4096, 0, 1).bulk_store == G.BULK_ROWS
     assert G.plan(64, 32000, 4096, 0, 1).bulk_store == G.BULK_TRANSPOSED
     assert G.plan(64, 32000, 4096, 0, 1, G.BF16_BF16).bulk_store == G.BULK_TRANSPOSED
-    assert G.plan(4096, 4096, 4096, 0, 1, beta=0.5).bulk_store == G.BULK_NONE
+    for ta, tb in ((0, 0), (0, 1), (1, 0), (1, 1)):
+        assert G.plan(4096, 4096, 4096, ta, tb, G.F16_F32, beta=0.5).bulk_store == G.BULK_ROWS
+    assert G.plan(4096, 4096, 4096, 0, 1, G.BF16_BF16, beta=0.5).bulk_store == G.BULK_ROWS
     assert G.plan(64, 32000, 4096, 0, 1, beta=1.0).bulk_store == G.BULK_NONE
     assert G.plan(512, 1002, 256, 0, 1).bulk_store == G.BULK_NONE          # 4008-byte rows
     assert G.plan(512, 1004, 256, 0, 1, ldc=1008).bulk_store == G.BULK_ROWS
@@ -265,13 +286,13 @@ def test_plan_strided_batched():
 
 
 def test_plan_grouped():
-    """Grouped calls: tiles counted per group (padded to whole tiles), no
-    multicast, direct stores; sizes must be non-negative."""
+    """Grouped calls: tiles counted per group (padded to whole tiles), direct
+    stores; sizes must be non-negative."""
     sizes = [5, 0, 130, 1, 257, 64]
     p = G.plan_grouped(sizes, 300, 200, 1)
     cg = p.bm // 128
     rows = sum(-(-m // (128 * cg)) for m in sizes)
-    assert p.tiles == rows * p.tiles_j and p.path != G.PATH_TC_2CTA_MULTICAST and p.bulk_store == G.BULK_NONE
+    assert p.tiles == rows * p.tiles_j and p.bulk_store == G.BULK_NONE
     assert p.swap_ab == 0 and p.workspace_bytes >= (len(sizes) + 1) * 4
     assert G.plan_grouped([], 8, 8).path == G.PATH_NOOP
     assert G.plan_grouped([4, 0], 8, 0).path == G.PATH_SCALE_C
@@ -348,9 +369,8 @@ def test_plan_invariants(shape):
         p = G.plan(M, N, K, 0, 0, sm_count=sm)
         I, J = (N, M) if p.swap_ab else (M, N)
         cg = p.bm // 128
-        mc = p.cluster // cg
-        assert (cg, mc) == {G.PATH_TC_1CTA: (1, 1), G.PATH_TC_2CTA: (2, 1), G.PATH_TC_2CTA_MULTICAST: (2, 2)}[p.path]
-        assert p.tiles == -(-I // p.bm) * -(-(-(-J // p.bn)) // mc) == p.tiles_i * p.tiles_j
+        assert cg == p.cluster == {G.PATH_TC_1CTA: 1, G.PATH_TC_2CTA: 2}[p.path]
+        assert p.tiles == -(-I // p.bm) * -(-J // p.bn) == p.tiles_i * p.tiles_j
         assert p.kdepth in (1, 2) and p.bk == 64 * p.kdepth and 2 <= p.stages and p.stages * p.kdepth <= 8
         assert p.num_kb == -(-K // p.bk)
         slots = sm // p.cluster

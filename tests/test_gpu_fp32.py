@@ -116,6 +116,24 @@ def test_three_products_beat_one(h):
     assert np.median(e1) > 256 * np.median(e3)
 
 
+def test_three_products_statistical_bound_at_k4096(h):
+    """A statistical check beside the worst-case rule: at K = 4096, on N(0, 1)
+    inputs, the three-product result stays within 2^-16 of the magnitude m at
+    every element (observed about 2^-21), a bound one TF32 product (about
+    2^-12 of m) fails.  The worst-case rule alone, (3K 2^-23 + 2^-20) m = 2^-9.4
+    m at this K, cannot tell the two apart."""
+    p = inputs.make_problem("f32_k4096", 1024, 1024, 4096, 0, 1, "f32", "f32", NORMAL, NORMAL, seed=12)
+    R, Mag = oracle_full(p)
+    out3, _ = run(p, h, code=G.F32_F32)
+    out1, _ = run(p, h, code=G.TF32_F32)
+    e3 = float((np.abs(out3 - R) / Mag).max())
+    e1 = float((np.abs(out1 - R) / Mag).max())
+    print("K = 4096, max err / mag: 3xTF32 2^%.1f, TF32 2^%.1f" % (np.log2(e3), np.log2(e1)))
+    check_close(out3, R, Mag, p.K, G.F32_F32, "3xTF32 K=4096")
+    assert e3 <= 2.0 ** -16, "three TF32 products: max err / mag 2^%.1f" % np.log2(e3)
+    assert e1 > 2.0 ** -16, "one TF32 product should not meet the three-product bound"
+
+
 @pytest.mark.parametrize("sched", ["split", "stream_k"])
 def test_split_tiles(h, sched):
     p = inputs.make_problem("f32_sk", 700, 904, 1500, 0, 1, "f32", "f32", NORMAL, NORMAL, beta=0.25, seed=8)

@@ -1,6 +1,18 @@
 """GPU parity at the full workload sizes, in the launch configuration the
-benchmark times, on sampled outputs the oracle computes one by one (random
-entries, corners, first / last rows and columns, the ragged last tiles)."""
+benchmark times.
+
+Full matrix: every element of C is compared with the oracle for the square
+4096^3 bf16 NT workload (fp32 and bf16 C), the fp16 blend workload in its four
+layouts, the QKV projection (NN), the ragged 4095 x 4097 x 1000 workload, the
+LM head and the extreme shapes.  The oracle runs once per distinct logical
+product: the fp32- and bf16-output runs of the square workload share one, and
+so do the four blend layouts, which store the same logical A and B four ways.
+The oracle's share of the suite's time is about 5 minutes on 16 host cores
+(3.6 GFLOP/s: 137 GFLOP for each square product, 825 GFLOP for QKV).
+
+Sampled (random entries, corners, first / last rows and columns, the ragged
+last tiles): the FFN-up and FFN-down projections and the NT layouts of the
+projections, 1.1 TFLOP each, which would add about 5 minutes apiece."""
 import numpy as np
 import pytest
 import torch
@@ -8,7 +20,7 @@ import torch
 from dense_gemm_10_gb300 import gemm as G
 from dense_gemm_10_gb300 import inputs
 
-from gpu_util import assert_close, device_problem, launch, oracle_at, sample_indices
+from gpu_util import assert_close, device_problem, launch, oracle_at, oracle_full, sample_indices
 
 pytestmark = pytest.mark.gpu
 
@@ -20,11 +32,36 @@ def h():
     gh.close()
 
 
-def _sampled(p, h, count=3000):
+_ORACLE = {}
+
+
+def _oracle_once(key, p):
+    """The oracle's full result for logical product `key`, computed once and kept
+    while consecutive tests use it (one at a time: QKV's alone is 1.6 GB)."""
+    if key not in _ORACLE:
+        _ORACLE.clear()
+        _ORACLE[key] = oracle_full(p)
+    return _ORACLE[key]
+
+
+def _run(p, h):
     Ad, Bd, Cd, ldc = device_problem(p)
     launch(p, h, Ad, Bd, Cd, ldc)
     st, word = h.status()
     assert st == G.OK, "status %s word 0x%x" % (G.STATUS.get(st), word)
+    return Cd
+
+
+def _full(p, h, key):
+    Cd = _run(p, h)
+    out = Cd[:p.M, :p.N].double().cpu().numpy()
+    del Cd
+    R, Mag = _oracle_once(key, p)
+    assert_close(out, R, Mag, p.out_dtype == "f32", p.name)
+
+
+def _sampled(p, h, count=3000):
+    Cd = _run(p, h)
     rows, cols = sample_indices(p.M, p.N, count, seed=p.M * 7 + p.N)
     ri = torch.from_numpy(rows).cuda()
     ci = torch.from_numpy(cols).cuda()
@@ -33,40 +70,37 @@ def _sampled(p, h, count=3000):
     assert_close(out, r, m, p.out_dtype == "f32", p.name)
     # every output is finite (beta == 0 runs start from a NaN-filled C)
     assert bool(torch.isfinite(Cd[:p.M, :p.N]).all())
-    return Cd
 
 
 @pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
 def test_square_4096_bf16_nt(h, out_dtype):
-    _sampled(inputs.square_4096_bf16_nt(out_dtype), h)
+    _full(inputs.square_4096_bf16_nt(out_dtype), h, "square_4096_bf16_nt")
 
 
 @pytest.mark.parametrize("transA,transB", [(0, 0), (0, 1), (1, 0), (1, 1)])
 def test_square_4096_f16_blend(h, transA, transB):
-    _sampled(inputs.square_4096_f16_blend(transA, transB), h, count=2000)
+    _full(inputs.square_4096_f16_blend(transA, transB), h, "square_4096_f16_blend")
 
 
-@pytest.mark.parametrize("name", ["qkv_proj", "ffn_up", "ffn_down"])
-@pytest.mark.parametrize("transB", [0, 1])
-def test_llm_projections(h, name, transB):
+def test_qkv_projection_nn_full(h):
+    _full(inputs.llm_projection("qkv_proj", 0), h, "qkv_proj_nn")
+
+
+@pytest.mark.parametrize("name,transB", [("qkv_proj", 1), ("ffn_up", 0), ("ffn_up", 1), ("ffn_down", 0),
+                                         ("ffn_down", 1)])
+def test_llm_projections_sampled(h, name, transB):
     _sampled(inputs.llm_projection(name, transB), h, count=1500)
 
 
 def test_ragged_4095_4097_1000(h):
-    _sampled(inputs.ragged_4095_4097_1000(), h, count=4000)
+    _full(inputs.ragged_4095_4097_1000(), h, "ragged")
 
 
 def test_lm_head_64(h):
     p = inputs.lm_head_64()
     plan = G.plan(p.M, p.N, p.K, p.transA, p.transB)
     assert plan.swap_ab == 1
-    Cd = _sampled(p, h, count=6000)
-    # M = 64 is small enough to check one full row of the vocabulary as well
-    from gpu_util import oracle_at as _at
-    cols = np.arange(p.N, dtype=np.int64)
-    rows = np.full(p.N, 17, dtype=np.int64)
-    r, m = _at(p, rows, cols)
-    assert_close(Cd[17, :p.N].double().cpu().numpy(), r, m, True, "lm_head row 17")
+    _full(p, h, "lm_head")
 
 
 @pytest.mark.parametrize("M,N,K,transA,transB", [
@@ -79,7 +113,7 @@ def test_lm_head_64(h):
 def test_extreme_shapes(h, M, N, K, transA, transB):
     p = inputs.make_problem("extreme_%dx%dx%d" % (M, N, K), M, N, K, transA, transB, "bf16", "f32",
                             ("normal", 0.0, 1.0), ("normal", 0.0, 1.0), seed=M % 97 + K % 89)
-    _sampled(p, h, count=2000)
+    _full(p, h, p.name)
 
 
 def test_largest_extent_is_refused_not_run(h):

@@ -23,9 +23,9 @@ def h():
     gh.close()
 
 
-# (CTAs per schedule slot, tile width): one CTA, a CTA pair, or two pairs sharing A by multicast
-CONFIGS = [(1, 64), (1, 128), (1, 256), (2, 64), (2, 128), (2, 256), (4, 256)]
-PATHS = {1: G.PATH_TC_1CTA, 2: G.PATH_TC_2CTA, 4: G.PATH_TC_2CTA_MULTICAST}
+# (CTAs per schedule slot, tile width): one CTA or a CTA pair
+CONFIGS = [(1, 64), (1, 128), (1, 256), (2, 64), (2, 128), (2, 256)]
+PATHS = {1: G.PATH_TC_1CTA, 2: G.PATH_TC_2CTA}
 
 
 def skip_half_atom(cg, bn, q_kmajor):
@@ -65,7 +65,7 @@ def test_tiny_256(h):
     _check(inputs.tiny_256(), h)
 
 
-@pytest.mark.parametrize("cg", [1, 2, 4])
+@pytest.mark.parametrize("cg", [1, 2])
 @pytest.mark.parametrize("transA,transB", [(0, 0), (0, 1), (1, 0), (1, 1)])
 @pytest.mark.parametrize("in_dtype,out_dtype", [("bf16", "f32"), ("f16", "f32"), ("bf16", "bf16"), ("f16", "f16")])
 def test_layouts_and_types(h, transA, transB, in_dtype, out_dtype, cg):
@@ -85,7 +85,7 @@ def test_ragged_shapes(h, shape):
     _check(p, h)
 
 
-@pytest.mark.parametrize("cg", [1, 2, 4])
+@pytest.mark.parametrize("cg", [1, 2])
 @pytest.mark.parametrize("transA,transB", [(0, 0), (0, 1), (1, 0), (1, 1)])
 @pytest.mark.parametrize("kdepth", [1, 2])
 def test_small_integers_bit_exact(h, transA, transB, cg, kdepth):
@@ -457,3 +457,26 @@ def test_plan_cache_hits_use_the_calls_own_pointers(h, shape, code):
             bits = lambda t: t.contiguous().view(torch.uint16).numpy()
             R, Mag = oracle.gemm(0, 1, M, N, K, 1.0, bits(A), K, bits(B), K, 0.0, None, N, oracle.IN_BF16)
             assert_close(out, R, Mag, ct == torch.float32, "plan cache")
+
+
+def test_tensor_map_cache_reuses_maps_of_the_same_buffers(h):
+    """A repeated call on the same buffers copies its tensor maps from the
+    handle's cache instead of encoding them; a call on another buffer encodes
+    that buffer's map anew, and every result is the oracle's."""
+    # (a shape no other test uses, so no earlier call left maps of these extents)
+    p = inputs.make_problem("tmap", 296, 328, 200, 0, 1, "bf16", "f32", ("normal", 0, 1), ("normal", 0, 1), seed=61)
+    R, Mag = oracle_full(p)
+    Ad, Bd = p.A.cuda(), p.B.cuda()
+    C1 = torch.full((p.M, p.N), float("nan"), device="cuda")
+    C2 = torch.full((p.M, p.N), float("nan"), device="cuda")
+    hits0, misses0 = h.tensor_map_cache_stats()
+    for _ in range(4):
+        launch(p, h, Ad, Bd, C1, p.N)
+    hits1, misses1 = h.tensor_map_cache_stats()
+    assert misses1 - misses0 <= 3 and hits1 - hits0 >= 9      # 3 maps a call (A, B, C), encoded once
+    launch(p, h, Ad, Bd, C2, p.N)                             # only C's map is new
+    hits2, misses2 = h.tensor_map_cache_stats()
+    assert misses2 - misses1 == 1 and hits2 - hits1 == 2
+    assert h.status()[0] == G.OK
+    for C in (C1, C2):
+        assert_close(C.double().cpu().numpy(), R, Mag, True, "tensor-map cache")
