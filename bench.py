@@ -262,8 +262,9 @@ def _sig(x, digits=4):
 
 def n_rotating_sets(set_bytes):
     """Input sets to rotate over so that every step's operands and C miss L2:
-    together at least twice the L2 size (one set when a set alone exceeds it)."""
-    if set_bytes > 2 * L2_BYTES:
+    together at least twice the L2 size, and at least two sets unless one set
+    alone is four times the L2 size."""
+    if set_bytes > 4 * L2_BYTES:
         return 1
     return max(2, math.ceil(2 * L2_BYTES / set_bytes) + 1)
 

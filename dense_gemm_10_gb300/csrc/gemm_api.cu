@@ -102,6 +102,8 @@ struct Plan {
   bool c_staged = false;
   int64_t c_ws_ld = 0;
   size_t c_ws_offset = 0;
+  // fp32 C off 16-byte boundaries written by tensor stores per row class (CMaps)
+  int32_t c_classes = 0;
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -595,8 +597,35 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   // the kernel writes an aligned copy in the workspace with bulk stores, and a
   // copy kernel moves it into C.  Direct stores cost more than that second pass
   // (4096 x 4097 x 1000: 80 us with direct stores, 40 us with bulk stores).
-  if (!bulk && o.stage_c && o.tma_store != 2 && beta == 0.0f && !swap && groups == 0 && pl.batch == 1 &&
-      pl.c_type != kCE4M3 && M * N >= (int64_t{1} << 20)) {
+  // Otherwise, with beta == 0, either each epilogue thread writes its row's
+  // whole 16-byte pieces with 1-D bulk copies (the partial pieces at a tile's
+  // edges by plain stores), with no second pass over C, or (a large C, one
+  // GEMM) the kernel's bulk tensor stores write an aligned copy of C in the
+  // workspace that a copy kernel then moves into C.  The row copies cost one
+  // copy per row of each 32-column block, which keeps the copy engine busy;
+  // with a short K the epilogue is exposed and the second pass is cheaper
+  // (4095 x 4097 x 1000 fp32: 86.8 us with row copies, 72.5 us through the
+  // copy), with a long K it is hidden (4096 x 4097 x 4096: 102 against 116 us).
+  // GEMM_OPT_EPILOGUE = 3 / 4 asks for the copy / the row copies.
+  // fp32 C (one GEMM, at least P rows) has a better way: its rows fall into
+  // P <= 4 classes of one misalignment each whose rows lie a multiple of 16
+  // bytes apart, so each class is a tensor of its own and a block leaves
+  // through P tensor stores (GEMM_BULK_ROW_CLASSES; 4095 x 4097 x 1000: see
+  // DESIGN's measurements).
+  const bool misaligned_ok = !bulk && o.tma_store != 2 && beta == 0.0f && !swap && groups == 0 && pl.c_type != kCE4M3;
+  int classes = 0;
+  if (misaligned_ok && pl.c_type == kCF32 && pl.batch == 1 && o.tma_store != 3 && o.tma_store != 4) {
+    const int64_t g = (ldc * 4) % 16;  // 0, 4, 8 or 12
+    const int n = g == 0 ? 1 : g == 8 ? 2 : 4;
+    if (M >= n && N >= 8) classes = n;
+  }
+  const bool staged_ok = misaligned_ok && o.stage_c && pl.batch == 1 && M * N >= (int64_t{1} << 20);
+  const bool use_staged = staged_ok && classes == 0 && (o.tma_store == 3 || (o.tma_store != 4 && K < 2048));
+  if (misaligned_ok && !use_staged) {
+    pl.tma_store = kBulkRowCopies;
+    pl.c_classes = classes;
+    P.bulk_store = classes > 0 ? GEMM_BULK_ROW_CLASSES : GEMM_BULK_ROW_COPIES;
+  } else if (use_staged) {
     pl.c_staged = true;
     pl.c_ws_ld = static_cast<int64_t>(round_up(static_cast<size_t>(N), static_cast<size_t>(16 / c_elem)));
     pl.c_ws_offset = ws;
@@ -690,6 +719,37 @@ gemm_status_t encode_c(CUtensorMap* map, void* C, int64_t rows, int64_t cols, in
                  : c_type == kCBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   return encode_tiled(cache, tmap_desc(C, dims, strides, box, dt, swz, CU_TENSOR_MAP_L2_PROMOTION_NONE), map);
+}
+
+// The row-class tensor maps of fp32 C (rows x cols, row pitch ldc elements,
+// rows off 16-byte boundaries; see CMaps): class r holds rows r, r + P, ...,
+// its base rounded down to 16 bytes and its columns shifted by the rounding,
+// its width cut to whole 16-byte pieces.
+gemm_status_t encode_c_classes(CMaps* cm, void* C, int64_t rows, int64_t cols, int64_t ldc, int P, TmapCache* cache) {
+  std::memset(cm, 0, sizeof(*cm));
+  for (int r = 0; r < P; ++r) {
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(C) + static_cast<uintptr_t>(r * ldc * 4);
+    const int64_t sh = static_cast<int64_t>((addr & 15u) / 4);
+    const uint64_t nrows = static_cast<uint64_t>((rows - r + P - 1) / P);
+    // whole 16-byte pieces only: a tensor store writes the whole last piece of
+    // a row that ends inside one, so the values past the last whole piece go
+    // out by plain stores
+    const uint64_t dims[3] = {static_cast<uint64_t>((cols + sh) & ~int64_t{3}), nrows, 1};
+    const uint64_t strides[2] = {static_cast<uint64_t>(P * ldc * 4), round_up(nrows * P * ldc * 4, 16)};
+    const void* base = reinterpret_cast<const void*>(addr - static_cast<uintptr_t>(sh * 4));
+    const uint32_t rows_box = static_cast<uint32_t>(32 / P);
+    const uint32_t box[3] = {32, rows_box, 1};
+    const uint32_t box_first[3] = {28, rows_box, 1};
+    gemm_status_t s = encode_tiled(cache, tmap_desc(base, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                                                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE),
+                                   &cm->m[r]);
+    if (s != GEMM_OK) return s;
+    s = encode_tiled(cache, tmap_desc(base, dims, strides, box_first, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE),
+                     &cm->m[4 + r]);
+    if (s != GEMM_OK) return s;
+  }
+  return GEMM_OK;
 }
 
 struct DeviceGuard {
@@ -877,7 +937,7 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
       h->opt.stages = static_cast<int>(value);
       return GEMM_OK;
     case GEMM_OPT_EPILOGUE:
-      if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+      if (value < 0 || value > 4) return GEMM_ERR_INVALID_ARG;
       h->opt.tma_store = static_cast<int>(value);
       return GEMM_OK;
     case GEMM_OPT_KDEPTH:
@@ -1085,12 +1145,19 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
   // (staged C: the kernel writes the aligned copy, whole rows of c_ws_ld elements)
   void* c_out = pl.c_staged ? static_cast<void*>(ws + pl.c_ws_offset) : C;
   const int64_t c_ld = pl.c_staged ? pl.c_ws_ld : ldc;
-  if (pl.tma_store != kBulkNone) {
+  if (pl.tma_store == kBulkRows || pl.tma_store == kBulkTransposed) {
     // C as stored: I x J, or J x I for a swapped problem
     s = pl.tma_store == kBulkRows
             ? encode_c(&map_c, c_out, pl.I, pl.c_staged ? pl.c_ws_ld : pl.J, c_ld, pl.c_type, false, pl.batch, pl.c_sb,
                        tc)
             : encode_c(&map_c, C, pl.J, pl.I, ldc, pl.c_type, true, pl.batch, pl.c_sb, tc);
+    if (s != GEMM_OK) return s;
+  }
+
+  CMaps cmaps;
+  std::memset(&cmaps, 0, sizeof(cmaps));
+  if (pl.c_classes > 0) {
+    s = encode_c_classes(&cmaps, C, pl.I, pl.J, ldc, pl.c_classes, tc);
     if (s != GEMM_OK) return s;
   }
 
@@ -1107,6 +1174,7 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
   a.idesc = make_idesc(pl.a_fmt, pl.b_fmt, !pl.p.kmajor, !pl.q.kmajor, kBM * cg, P.bn);
   a.alpha = alpha;
   a.beta = beta;
+  a.c_classes = pl.c_classes;
   a.C = c_out;
   a.c_si = pl.c_staged ? pl.c_ws_ld : pl.c_si;
   a.c_sj = pl.c_sj;
@@ -1143,7 +1211,7 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
   a.q_seg = pl.q.seg_map;
   ops.bias_on_i = P.swap_ab;  // a swapped problem computes C^T: C's columns are the kernel's rows
   a.ops = ops;
-  e = tc_launch(pl.cfg, map_p, map_q, map_c, a, P.grid, st);
+  e = tc_launch(pl.cfg, map_p, map_q, map_c, cmaps, a, P.grid, st);
   if (e != cudaSuccess) return cuda_fail(h, e);
   h->launches += 1;
   if (pl.c_staged) {  // the aligned copy's M x N elements into C
@@ -1554,10 +1622,16 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   if (s != GEMM_OK) return s;
   CUtensorMap map_c;
   std::memset(&map_c, 0, sizeof(map_c));
-  if (pl.tma_store != kBulkNone) {
+  if (pl.tma_store == kBulkRows || pl.tma_store == kBulkTransposed) {
     // C as stored: I x J, or J x I for a swapped problem
     s = pl.tma_store == kBulkRows ? encode_c(&map_c, C, pl.I, pl.J, ldc, pl.c_type, false, pl.batch, pl.c_sb, nullptr)
                                   : encode_c(&map_c, C, pl.J, pl.I, ldc, pl.c_type, true, pl.batch, pl.c_sb, nullptr);
+    if (s != GEMM_OK) return s;
+  }
+  CMaps cmaps;
+  std::memset(&cmaps, 0, sizeof(cmaps));
+  if (pl.c_classes > 0) {
+    s = encode_c_classes(&cmaps, C, pl.I, pl.J, ldc, pl.c_classes, nullptr);
     if (s != GEMM_OK) return s;
   }
   TcArgs a;
@@ -1573,6 +1647,7 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   a.idesc = make_idesc(pl.a_fmt, pl.b_fmt, !pl.p.kmajor, !pl.q.kmajor, kBM * cg, P.bn);
   a.alpha = alpha;
   a.beta = beta;
+  a.c_classes = pl.c_classes;
   a.C = C;
   a.c_si = pl.c_si;
   a.c_sj = pl.c_sj;
@@ -1592,7 +1667,7 @@ extern "C" gemm_status_t gemm_run_noalloc(gemm_op_t transA, gemm_op_t transB, in
   a.p_seg = pl.p.seg_map;
   a.q_seg = pl.q.seg_map;
   a.ops = EpiOps();  // no fused operations (the memset above zeroed out_scale)
-  e = tc_launch(pl.cfg, map_p, map_q, map_c, a, P.grid, st);
+  e = tc_launch(pl.cfg, map_p, map_q, map_c, cmaps, a, P.grid, st);
   return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 

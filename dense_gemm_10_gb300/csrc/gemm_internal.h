@@ -76,11 +76,26 @@ struct TcArgs {
   // group_row[g] and number group_m[g]; the tile's group is Unit::tb
   const int64_t* group_row;
   const int32_t* group_m;
+  int32_t c_classes;     // kBulkRowCopies with fp32 C: P row classes with tensor maps in CMaps (0: per-row copies)
 };
 
 // Epilogue store paths: direct stores, or staged bulk tensor stores of rows of
-// C, or (for swapped problems, whose C is stored J x I) of transposed blocks.
-enum BulkStore : int32_t { kBulkNone = 0, kBulkRows = 1, kBulkTransposed = 2 };
+// C, or (for swapped problems, whose C is stored J x I) of transposed blocks,
+// or, for rows of C that bulk tensor stores cannot write (not 16-byte aligned,
+// or ending inside a 16-byte piece), one 1-D bulk copy per row of a block.
+enum BulkStore : int32_t { kBulkNone = 0, kBulkRows = 1, kBulkTransposed = 2, kBulkRowCopies = 3 };
+
+// Tensor maps of fp32 C whose rows start off 16-byte boundaries (c_classes
+// P > 0 in TcArgs): the rows i = r, r + P, r + 2P, ... (class r) all start the
+// same s_r values past a 16-byte boundary and lie P * ldc * 4 bytes apart, a
+// multiple of 16, so each class is a tensor of its own whose columns are C's
+// shifted by s_r.  m[r]: class r, boxes of 32 columns by 32 / P rows, 128-byte
+// swizzle; m[4 + r]: the same class, boxes of 28 columns (unswizzled 112-byte
+// rows) for a tile's first block, whose first 16-byte piece holds values of
+// the tile to its left.
+struct CMaps {
+  CUtensorMap m[8];
+};
 
 // Tile configurations: a tile of (128 * cg) x bn per CTA (cg == 1) or CTA
 // pair (cg == 2).  eb is the input element size in bytes: 2 for bf16 / fp16
@@ -98,7 +113,8 @@ cudaError_t tc_prepare(int cfg, int* max_clusters);
 // grid = CTAs (a multiple of cg).
 // map_c describes C for the bulk-store epilogue (ignored unless args.tma_store).
 cudaError_t tc_launch(int cfg, const CUtensorMap& map_p, const CUtensorMap& map_q,
-                      const CUtensorMap& map_c, const TcArgs& args, int grid, cudaStream_t stream);
+                      const CUtensorMap& map_c, const CMaps& cmaps, const TcArgs& args, int grid,
+                      cudaStream_t stream);
 
 // dst[b * dbs + r * ldd + c] = src[b * sbs + r * lds + c] for elements of
 // esize (1 or 2) bytes, b < nb, r < rows, c < cols; strides in elements.

@@ -5,13 +5,14 @@
 namespace g10 {
 
 using PrepareFn = cudaError_t (*)(int*);
-using LaunchFn = cudaError_t (*)(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+using LaunchFn = cudaError_t (*)(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CMaps&,
                                  const TcArgs&, int, cudaStream_t);
 
 #define TC_DECLARE(BN, CG, EB)                                                                  \
   cudaError_t tc_prepare_bn##BN##_cg##CG##_eb##EB(int* max_clusters);                           \
   cudaError_t tc_launch_bn##BN##_cg##CG##_eb##EB(const CUtensorMap&, const CUtensorMap&,          \
-                                                 const CUtensorMap&, const TcArgs&, int, cudaStream_t);
+                                                 const CUtensorMap&, const CMaps&, const TcArgs&, int,    \
+                                                 cudaStream_t);
 #define TC_ENTRY(BN, CG, EB) \
   {{BN, CG, EB}, TcConfig<BN, CG>::kStages, tc_prepare_bn##BN##_cg##CG##_eb##EB, tc_launch_bn##BN##_cg##CG##_eb##EB}
 
@@ -55,9 +56,10 @@ cudaError_t tc_prepare(int cfg, int* max_clusters) {
 }
 
 cudaError_t tc_launch(int cfg, const CUtensorMap& map_p, const CUtensorMap& map_q,
-                      const CUtensorMap& map_c, const TcArgs& args, int grid, cudaStream_t stream) {
+                      const CUtensorMap& map_c, const CMaps& cmaps, const TcArgs& args, int grid,
+                      cudaStream_t stream) {
   if (cfg < 0 || cfg >= kNumTileConfigs) return cudaErrorInvalidValue;
-  return kEntries[cfg].launch(map_p, map_q, map_c, args, grid, stream);
+  return kEntries[cfg].launch(map_p, map_q, map_c, cmaps, args, grid, stream);
 }
 
 }  // namespace g10

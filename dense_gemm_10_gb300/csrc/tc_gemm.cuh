@@ -331,10 +331,15 @@ struct EpiOut {
   uint32_t cbar;     // this warp's two mbarriers (buffer 0, buffer 1: 8 bytes apart)
   uint32_t cphase;   // bit b: parity of buffer b's next load
   uint32_t pending;  // bit b: a load into buffer b not yet waited for
+  int jstart;        // first column of the current tile
   int jend;          // first column past the current tile
   TcCtrl* ctrl;
   int32_t* status;
   uint64_t wait_ns;
+  // fp32 C whose rows start off 16-byte boundaries, in row classes
+  const CMaps* cmaps;
+  int classes;       // P (0: per-row copies instead)
+  float cy[4];       // this thread's row: the previous block's last four values
 
   __device__ __forceinline__ void use_ring(uint32_t base) {
     staging = base;
@@ -403,11 +408,182 @@ struct EpiOut {
     }
   }
 
-  // The first block of a tile whose columns run from jt to jend (exclusive).
+  // A tile whose columns run from jt to jend (exclusive) begins: with beta !=
+  // 0 and bulk stores, its first block of old C starts loading.
   __device__ __forceinline__ void begin_tile(int jt, int jend_) {
-    if (!c.blend_load) return;
+    jstart = jt;
     jend = jend_;
-    load_block(nstore & 1, jt);
+    if (c.blend_load) load_block(nstore & 1, jt);
+  }
+
+  // fp32 C whose rows start off 16-byte boundaries, in P row classes (CMaps):
+  // the rows of class r start s_r values past a boundary, so the block's 32
+  // columns j .. j + 31 of such a row, shifted right by s_r behind the s_r last
+  // values of the previous block, fill whole 16-byte pieces from column j -
+  // s_r.  Each thread writes that shifted row into its class's part of a
+  // 128-byte-swizzled staging buffer, and one tensor store per class writes
+  // the block (P stores where per-row copies took 32).  A tile's first block
+  // cannot write the piece it shares with the tile to its left: its store
+  // starts one piece later (28-column boxes, unswizzled 112-byte rows) and the
+  // first 4 - s_r values go out by plain stores, as do the values after a
+  // tile's last block.  The classes' tensors end at their last whole 16-byte
+  // piece before column N (a store would write a partial last piece whole);
+  // the few values past it go out by plain stores too.
+  __device__ __forceinline__ void put_row_class(int i, int j, const float (&v)[32]) {
+    const int jv = c.J < jend ? c.J : jend;  // first column past the tile's columns inside C
+    if (j >= jv) return;                     // (the same for the whole warp)
+    const int ncols = jv - j < 32 ? jv - j : 32;
+    const bool first = j == jstart;
+    const bool last = j + 32 >= jv;
+    const int P = classes;
+    const int rows = 32 / P;                 // a class's rows in the warp's 32
+    const int cls = lane % P;
+    const int br = lane / P;                 // this thread's row in its class's part of the buffer
+    char* rowp = static_cast<char*>(c.C) + (static_cast<int64_t>(i) * c.si + j) * 4;
+    const int sh = static_cast<int>((reinterpret_cast<uintptr_t>(rowp) & 15u) >> 2);
+    const uint32_t buf = buffer(true);
+    const uint32_t sub = buf + static_cast<uint32_t>(cls * rows * 128);  // 1024-byte aligned (P <= 4)
+    if (first) {
+      // v[4 - sh .. 31 - sh]: columns j + 4 - sh .. j + 31 - sh, from the block's second piece on
+      const uint32_t row = sub + static_cast<uint32_t>(br * 112);
+#pragma unroll
+      for (int k = 0; k < 7; ++k) {
+        float o[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = 4 * k + u;
+          float x = v[e + 4];
+#pragma unroll
+          for (int t = 1; t < 4; ++t)
+            if (t == sh) x = v[e + 4 - t];
+          o[u] = x;
+        }
+        st_shared_v4(row + static_cast<uint32_t>(k * 16), __float_as_uint(o[0]), __float_as_uint(o[1]),
+                     __float_as_uint(o[2]), __float_as_uint(o[3]));
+      }
+    } else {
+      // [the previous block's last sh values | v[0 .. 31 - sh]]: columns j - sh .. j + 31 - sh
+      const uint32_t row = sub + static_cast<uint32_t>(br * 128);
+      const uint32_t sw = static_cast<uint32_t>(br & 7);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float o[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = 4 * k + u;
+          float x = v[e];
+#pragma unroll
+          for (int t = 1; t < 4; ++t)
+            if (t == sh) x = e < t ? cy[4 - t + (e < t ? e : 0)] : v[e - t < 0 ? 0 : e - t];
+          o[u] = x;
+        }
+        st_shared_v4(row + ((static_cast<uint32_t>(k) ^ sw) << 4), __float_as_uint(o[0]), __float_as_uint(o[1]),
+                     __float_as_uint(o[2]), __float_as_uint(o[3]));
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) cy[t] = v[28 + t];
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      for (int r = 0; r < P; ++r)
+        tma_store_3d(&cmaps->m[first ? 4 + r : r], buf + static_cast<uint32_t>(r * rows * 128), first ? j + 4 : j,
+                     y0 / P, 0);
+      bulk_commit_group();
+    }
+    __syncwarp();
+    ++nstore;
+    // plain stores: the first block's values before its box, after the tile's
+    // last block the values past its box, and the values past the class
+    // tensor's last whole 16-byte piece (columns jcut and on)
+    if (i < c.I) {
+      const int jcut = ((c.J + sh) & ~3) - sh;
+      const int64_t off = static_cast<int64_t>(i) * c.si + j;
+#pragma unroll
+      for (int t = 0; t < 32; ++t)
+        if (t < ncols && ((first && t < 4 - sh) || j + t >= jcut || (last && t >= 32 - sh)))
+          static_cast<float*>(c.C)[off + t] = v[t];
+    }
+  }
+
+  // Rows of C that bulk tensor stores cannot write (not 16-byte aligned, or
+  // ending inside a 16-byte piece): each thread writes its own row of the
+  // block.  Its 32 values go into a slot of shared memory shifted by the row's
+  // misalignment (sh elements), so that the slot's first byte stands for the
+  // 16-byte boundary at or before the row's first value; one 1-D bulk copy
+  // then writes the row's whole 16-byte pieces.  The piece that the block's
+  // last values share with the next block of the same row stays in the slot's
+  // last piece and leaves with the next block's copy.  At the tile's first and
+  // last columns, whose neighbouring values belong to other tiles, the values
+  // of the partial pieces are written by plain stores.  Slots of 144 (fp32)
+  // or 80 (16-bit) bytes put the 16-byte stores of eight consecutive threads
+  // on distinct banks.  Nothing outside the tile's columns inside C is written.
+  template <int ESZ>
+  __device__ __forceinline__ void put_row_copy(int i, int j, const float (&v)[32]) {
+    constexpr int kPer = 16 / ESZ;              // values per 16-byte piece
+    constexpr int kPieces = 32 / kPer + 1;      // the block's pieces and the one it may share
+    constexpr uint32_t kSlot = kPieces * 16;
+    const int jv = c.J < jend ? c.J : jend;     // first column past the tile's columns inside C
+    if (j >= jv || i >= c.I) return;
+    const int ncols = jv - j < 32 ? jv - j : 32;
+    char* rowp = static_cast<char*>(c.C) + (static_cast<int64_t>(i) * c.si + j) * ESZ;
+    const int mbytes = static_cast<int>(reinterpret_cast<uintptr_t>(rowp) & 15u);
+    const int sh = mbytes / ESZ;
+    const bool first = j == jstart;
+    const bool last = j + 32 >= jv;
+    const uint32_t slot = staging + static_cast<uint32_t>(lane) * kSlot;
+    bulk_wait_group_read<0>();  // this thread's previous copy has read the slot
+    float carry[kPer];          // the values the previous block left in the shared piece
+    {
+      const float4 q = ld_shared_v4_f32(slot + (kPieces - 1) * 16);
+      if constexpr (ESZ == 4) {
+        carry[0] = q.x; carry[1] = q.y; carry[2] = q.z; carry[3] = q.w;
+      } else {
+        const uint32_t w[4] = {__float_as_uint(q.x), __float_as_uint(q.y), __float_as_uint(q.z), __float_as_uint(q.w)};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float2 f = unpack2(c.type, w[t]);
+          carry[2 * t] = f.x;
+          carry[2 * t + 1] = f.y;
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kPieces; ++k) {
+      float o[kPer];
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int e = k * kPer + u;  // slot position: carry[e] before the shift, v[e - sh] after it
+        float x = 0.0f;
+#pragma unroll
+        for (int t = 0; t < kPer; ++t)
+          if (t == sh) x = e < t ? carry[e < kPer ? e : 0] : (e - t < 32 ? v[e - t < 32 ? e - t : 0] : 0.0f);
+        o[u] = x;
+      }
+      if constexpr (ESZ == 4)
+        st_shared_v4(slot + k * 16, __float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]),
+                     __float_as_uint(o[3]));
+      else
+        st_shared_v4(slot + k * 16, pack2(c.type, o[0], o[1]), pack2(c.type, o[2], o[3]), pack2(c.type, o[4], o[5]),
+                     pack2(c.type, o[6], o[7]));
+    }
+    fence_proxy_async_smem();
+    char* base = rowp - mbytes;  // the slot's first byte stands here
+    char* lo = base + ((first && sh > 0) ? 16 : 0);
+    char* hi = reinterpret_cast<char*>(reinterpret_cast<uintptr_t>(rowp + ncols * ESZ) & ~uintptr_t{15});
+    if (hi > lo) {
+      bulk_copy_s2g(lo, slot + static_cast<uint32_t>(lo - base), static_cast<uint32_t>(hi - lo));
+      bulk_commit_group();
+    }
+    // plain stores: the values before the copy in the tile's first block, and
+    // after the tile's last block the values past the copy
+    const int head = (first && sh > 0) ? (kPer - sh < ncols ? kPer - sh : ncols) : 0;
+    const int past = static_cast<int>((hi - rowp) / ESZ);
+    const int tail = past > head ? past : head;
+    const int64_t off = static_cast<int64_t>(i) * c.si + j;
+#pragma unroll
+    for (int t = 0; t < 32; ++t)
+      if (t < head || (last && t >= tail && t < ncols)) store_c(c, off + t, v[t]);
   }
 
   // No load may still be writing shared memory when the warp leaves.
@@ -632,6 +808,15 @@ struct EpiOut {
     // (the whole warp enters: the bias shuffle needs every lane; rows past I
     // compute values the clipped store drops)
     if (c.has_ops) apply_ops32(c.ops, v, lane, i < c.I ? i : c.I - 1, j, c.J - j < 32 ? c.J - j : 32);
+    if (c.tma == kBulkRowCopies) {
+      if (classes > 0)
+        put_row_class(i, j, v);
+      else if (c.type == kCF32)
+        put_row_copy<4>(i, j, v);
+      else
+        put_row_copy<2>(i, j, v);
+      return;
+    }
     if (c.tma == kBulkTransposed) {
       const uint32_t buf = buffer(true);
       if (c.type == kCF32) {
@@ -674,10 +859,12 @@ struct EpiOut {
   // the global writes complete with the grid, like any other store.
   __device__ __forceinline__ void finish() {
     drain_loads();
-    if (c.tma != kBulkNone) {
+    if (c.tma == kBulkRowCopies && classes == 0) {
+      bulk_wait_group_read<0>();  // every thread issued copies of its own row
+    } else if (c.tma != kBulkNone) {
       if (lane == 0) bulk_wait_group_read<0>();
-      __syncwarp();
     }
+    __syncwarp();
   }
 };
 
@@ -880,7 +1067,7 @@ __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8
 }
 
 template <int BN, int CG, int EB>
-__device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap* map_c,
+__device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap* map_c, const CMaps* cmaps,
                                               uint8_t* staging, uint8_t* ring, TcCtrl* ctrl,
                                               uint32_t tmem_base,
                                               int warp, int lane, uint32_t rank, int first,
@@ -903,10 +1090,15 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
   out.cbar = smem_u32(&ctrl->c_full[warp - 2][0]);
   out.cphase = 0;
   out.pending = 0;
+  out.jstart = 0;
   out.jend = 0;
   out.ctrl = ctrl;
   out.status = a.status;
   out.wait_ns = a.wait_limit_ns;
+  out.cmaps = cmaps;
+  out.classes = a.c_classes;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) out.cy[t] = 0.0f;
   const int64_t esize = a.c_type == kCF32 ? 4 : a.c_type == kCE4M3 ? 1 : 2;
   int it = 0;
   WorkIter work(a.sched, first, stride);
@@ -925,7 +1117,7 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
                                  kRoleEpilogue, kBarAccFull, true);
     if (bar_any(1, 128, !ok)) break;  // all four epilogue warps leave together
     tc_fence_after_sync();
-    if (out.c.tma != kBulkNone && !out.ring && !out.c.blend_load) {
+    if ((out.c.tma == kBulkRows || out.c.tma == kBulkTransposed) && !out.ring && !out.c.blend_load) {
       WorkIter peek = work;
       Unit next_unit;
       // This CTA's last unit: its copies have landed and its MMAs (the pair's)
@@ -1075,7 +1267,8 @@ template <int BN, int CG, int EB>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p,
                    const __grid_constant__ CUtensorMap map_q,
-                   const __grid_constant__ CUtensorMap map_c, const TcArgs args) {
+                   const __grid_constant__ CUtensorMap map_c, const __grid_constant__ CMaps cmaps,
+                   const TcArgs args) {
   using Cfg = TcConfig<BN, CG>;
   // The roles take the arguments by reference; a local copy whose address never
   // leaves this kernel lets the compiler keep the fields in registers across
@@ -1153,7 +1346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_role<BN, CG, EB, 1>(a, ring_a, ring_b, ctrl, tmem_base, rank, first, stride);
     }
   } else {
-    epilogue_role<BN, CG, EB>(a, &map_c, staging, ring_a, ctrl, tmem_base, warp, lane, rank, first,
+    epilogue_role<BN, CG, EB>(a, &map_c, &cmaps, staging, ring_a, ctrl, tmem_base, warp, lane, rank, first,
                               stride);
   }
 

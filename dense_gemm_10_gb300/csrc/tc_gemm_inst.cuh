@@ -31,8 +31,8 @@ cudaError_t TC_NAME(tc_prepare_bn, TC_BN, _cg, TC_CG, _eb, TC_EB)(int* max_clust
 }
 
 cudaError_t TC_NAME(tc_launch_bn, TC_BN, _cg, TC_CG, _eb, TC_EB)(
-    const CUtensorMap& map_p, const CUtensorMap& map_q, const CUtensorMap& map_c, const TcArgs& args,
-    int grid, cudaStream_t stream) {
+    const CUtensorMap& map_p, const CUtensorMap& map_q, const CUtensorMap& map_c, const CMaps& cmaps,
+    const TcArgs& args, int grid, cudaStream_t stream) {
   using Cfg = TcConfig<TC_BN, TC_CG>;
   const size_t smem = Cfg::kSmemBytes;  // every epilogue stages C (bulk or direct stores)
   cudaLaunchConfig_t cfg = {};
@@ -56,7 +56,7 @@ cudaError_t TC_NAME(tc_launch_bn, TC_BN, _cg, TC_CG, _eb, TC_EB)(
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, TC_KERNEL, map_p, map_q, map_c, args);
+  return cudaLaunchKernelEx(&cfg, TC_KERNEL, map_p, map_q, map_c, cmaps, args);
 }
 
 }  // namespace g10

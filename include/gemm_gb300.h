@@ -269,10 +269,22 @@ typedef enum {
                                small C that bulk stores cannot write) */
   GEMM_BULK_ROWS = 1,       /* bulk tensor stores of rows of C */
   GEMM_BULK_TRANSPOSED = 2, /* bulk tensor stores of transposed blocks (swapped problems) */
-  GEMM_BULK_STAGED = 3      /* C's rows are misaligned, or end inside a 16-byte piece: bulk tensor
-                               stores write an aligned copy of C in the handle's workspace and a copy
-                               kernel then writes C's M x N elements (one more launch; beta == 0,
-                               unswapped, one GEMM, M * N >= 2^20) */
+  GEMM_BULK_STAGED = 3,     /* C's rows are misaligned, or end inside a 16-byte piece, K < 2048 and
+                               GEMM_BULK_ROW_CLASSES does not apply:
+                               bulk tensor stores write an aligned copy of C in the handle's workspace
+                               and a copy kernel then writes C's M x N elements (one more launch;
+                               beta == 0, unswapped, one GEMM, M * N >= 2^20) */
+  GEMM_BULK_ROW_COPIES = 4, /* C's rows are misaligned, or end inside a 16-byte piece (beta == 0,
+                               unswapped, not grouped; where GEMM_BULK_STAGED is not chosen): each
+                               row of a block leaves through one 1-D bulk copy of its whole 16-byte
+                               pieces; the partial pieces at a tile's first and last columns are
+                               written by plain stores.  No workspace for C, no second launch */
+  GEMM_BULK_ROW_CLASSES = 5 /* fp32 C whose rows are misaligned (beta == 0, unswapped, one GEMM, at
+                               least 4 rows): the rows fall into 1, 2 or 4 classes of one misalignment
+                               each, whose rows lie a multiple of 16 bytes apart; each class is
+                               described as a tensor of its own and a block of C leaves through one
+                               bulk tensor store per class; the partial pieces at a tile's first and
+                               last columns are written by plain stores */
 } gemm_bulk_store_t;
 
 typedef struct {
@@ -425,9 +437,15 @@ typedef enum {
   GEMM_OPT_STREAM_K = 7,       /* 0 auto, 1 never, 2 always when the last wave is incomplete */
   GEMM_OPT_STAGES = 8,         /* 0 auto (deepest ring that fits), else at most this many stages */
   GEMM_OPT_EPILOGUE = 10,      /* 0 auto: C tiles leave through shared-memory staging and bulk
-                                  tensor stores when rows start 16-byte aligned, N is a whole
-                                  number of 16-byte pieces and beta == 0;
-                                  2: always direct stores from registers */
+                                  tensor stores when rows start 16-byte aligned and N is a whole
+                                  number of 16-byte pieces (beta != 0: old C arrives by tensor
+                                  loads); else, with beta == 0 and unswapped, through an aligned
+                                  copy in the workspace and a second kernel (GEMM_BULK_STAGED;
+                                  one GEMM, M * N >= 2^20, K < 2048) or by per-row bulk copies
+                                  (GEMM_BULK_ROW_COPIES); 2: always direct stores from
+                                  registers; 3: prefer GEMM_BULK_STAGED where allowed;
+                                  4: prefer GEMM_BULK_ROW_COPIES.  In auto mode fp32 C of one
+                                  GEMM takes GEMM_BULK_ROW_CLASSES before either */
   GEMM_OPT_KDEPTH = 11,        /* 0 auto, else 1 or 2 128-byte k-slices per ring stage (2 halves
                                   the barrier round trips per byte; falls back to 1 where the
                                   ring would hold fewer than two stages) */

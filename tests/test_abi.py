@@ -150,8 +150,9 @@ def test_plan_compute_bound_keeps_stream_k():
 def test_plan_bulk_store_paths():
     """C leaves through bulk tensor stores of rows (beta != 0 too: the old C
     arrives by tensor loads into the same staging), of transposed blocks for a
-    swapped problem with beta == 0, or directly (misaligned rows, a partial
-    16-byte piece at the right edge, or a swapped problem with beta != 0)."""
+    swapped problem with beta == 0, by per-row bulk copies (misaligned rows or
+    a partial 16-byte piece at the right edge, beta == 0), or directly (the
+    same with beta != 0, or a swapped problem with beta != 0)."""
     assert G.plan(4096, 4096, 4096, 0, 1).bulk_store == G.BULK_ROWS
     assert G.plan(64, 32000, 4096, 0, 1).bulk_store == G.BULK_TRANSPOSED
     assert G.plan(64, 32000, 4096, 0, 1, G.BF16_BF16).bulk_store == G.BULK_TRANSPOSED
@@ -159,29 +160,40 @@ def test_plan_bulk_store_paths():
         assert G.plan(4096, 4096, 4096, ta, tb, G.F16_F32, beta=0.5).bulk_store == G.BULK_ROWS
     assert G.plan(4096, 4096, 4096, 0, 1, G.BF16_BF16, beta=0.5).bulk_store == G.BULK_ROWS
     assert G.plan(64, 32000, 4096, 0, 1, beta=1.0).bulk_store == G.BULK_NONE
-    assert G.plan(512, 1002, 256, 0, 1).bulk_store == G.BULK_NONE          # 4008-byte rows
+    assert G.plan(512, 1002, 256, 0, 1).bulk_store == G.BULK_ROW_CLASSES   # 4008-byte rows
+    assert G.plan(512, 1002, 256, 0, 1, G.BF16_BF16).bulk_store == G.BULK_ROW_COPIES
+    assert G.plan(512, 1002, 256, 0, 1, beta=0.5).bulk_store == G.BULK_NONE
     assert G.plan(512, 1004, 256, 0, 1, ldc=1008).bulk_store == G.BULK_ROWS
-    assert G.plan(512, 1004, 256, 0, 1, C=0x1004, ldc=1008).bulk_store == G.BULK_NONE
+    assert G.plan(512, 1004, 256, 0, 1, C=0x1004, ldc=1008).bulk_store == G.BULK_ROW_CLASSES
     assert G.plan(40, 1001, 256, 0, 1, G.BF16_BF16, ldc=1008).bulk_store == G.BULK_NONE
 
 
-def test_plan_staged_c():
-    """A large C that bulk stores cannot write (misaligned rows, or rows ending
-    inside a 16-byte piece) goes through an aligned copy in the workspace: one
-    more launch and M x round_up(N, 16 bytes) elements of workspace.  beta != 0,
-    8-bit C, swapped problems and C under 2^20 elements keep direct stores."""
+def test_plan_misaligned_c():
+    """C that bulk tensor stores cannot write (misaligned rows, or rows ending
+    inside a 16-byte piece), beta == 0, unswapped.  fp32 C of one GEMM: the
+    rows fall into 1, 2 or 4 classes of one misalignment each, one tensor store
+    per class and block.  Otherwise a large C of one GEMM with a short K
+    (epilogue-bound) goes through an aligned copy in the workspace and a copy
+    kernel (one more launch), and the rest leaves through per-row bulk copies.
+    beta != 0, 8-bit C and swapped problems keep direct stores."""
     p = G.plan(4095, 4097, 1000, 0, 0, ldb=4097, ldc=4097)       # the ragged 4095 x 4097 x 1000 workload
-    assert p.bulk_store == G.BULK_STAGED and p.launches == 3 and p.repack_b == 1
-    assert p.workspace_bytes >= 4095 * 4100 * 4
-    p = G.plan(2048, 1001, 512, 0, 1, ldc=1008)                 # aligned rows ending inside a piece
+    assert p.bulk_store == G.BULK_ROW_CLASSES and p.launches == 2 and p.repack_b == 1
+    assert p.workspace_bytes < 1000 * 4104 * 2 + (1 << 20)        # the repacked B only
+    assert G.plan(4096, 4097, 4096, 0, 1, ldc=4097).bulk_store == G.BULK_ROW_CLASSES
+    p = G.plan(2048, 1001, 512, 0, 1, ldc=1008)                 # aligned rows ending inside a piece: one class
+    assert p.bulk_store == G.BULK_ROW_CLASSES and p.launches == 1
+    p = G.plan(2048, 1001, 512, 0, 1, G.BF16_BF16, ldc=1008)    # 16-bit C, short K: the workspace copy
     assert p.bulk_store == G.BULK_STAGED and p.launches == 2
-    p = G.plan(2048, 1024, 512, 0, 1, G.BF16_BF16, C=0x1002)    # misaligned base
-    assert p.bulk_store == G.BULK_STAGED
+    p = G.plan(2048, 1024, 2048, 0, 1, G.BF16_BF16, C=0x1002)   # 16-bit C, misaligned base, K = 2048
+    assert p.bulk_store == G.BULK_ROW_COPIES
+    assert G.plan(1000, 1001, 512, 0, 1, G.BF16_BF16, ldc=1008).bulk_store == G.BULK_ROW_COPIES   # small C
+    assert G.plan(3, 2, 512, 0, 1, ldc=3).bulk_store == G.BULK_ROW_COPIES   # fewer rows than classes
     assert G.plan(2048, 1001, 512, 0, 1, ldc=1008, beta=0.5).bulk_store == G.BULK_NONE
     assert G.plan(2048, 1001, 512, 0, 1, G.fp8_dtype("e4m3", "e4m3", "e4m3"), ldc=1008).bulk_store == G.BULK_NONE
-    assert G.plan(1000, 1001, 512, 0, 1, ldc=1008).bulk_store == G.BULK_NONE   # under 2^20 elements
     assert G.plan(64, 32001, 4096, 0, 1, ldc=32008).swap_ab == 1
     assert G.plan(64, 32001, 4096, 0, 1, ldc=32008).bulk_store == G.BULK_NONE  # swapped
+    pb = G.plan_batched(1000, 1001, 256, 3, ldc=1001)           # strided batches: per-row copies
+    assert pb.bulk_store == G.BULK_ROW_COPIES
 
 
 def test_plan_fp8():
@@ -327,9 +339,9 @@ def test_plan_full_waves_need_no_stream_k():
 def test_plan_ragged_repacks_misaligned_b():
     p = G.plan(4095, 4097, 1000, 0, 0, lda=1000, ldb=4097, ldc=4097)
     assert p.repack_a == 0 and p.repack_b == 1
-    # 4097 fp32 = 16388-byte rows: C goes through an aligned copy (repack, GEMM, copy into C)
-    assert p.launches == 3 and p.bulk_store == G.BULK_STAGED
-    assert p.workspace_bytes >= 1000 * 4104 * 2 + 4095 * 4100 * 4
+    # 4097 fp32 = 16388-byte rows: four row classes, one tensor store each per block (repack, GEMM)
+    assert p.launches == 2 and p.bulk_store == G.BULK_ROW_CLASSES
+    assert p.workspace_bytes >= 1000 * 4104 * 2
     with_direct = G.plan(4095, 4097, 1000, 0, 0, lda=1000, ldb=4097, ldc=4097, beta=1.0)
     assert with_direct.launches == 2 and with_direct.vector_store == 0 and with_direct.bulk_store == G.BULK_NONE
 

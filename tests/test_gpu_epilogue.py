@@ -120,13 +120,33 @@ def test_direct_store_with_blend(h, act, transA, transB):
 
 @pytest.mark.parametrize("act", ACTS)
 @pytest.mark.parametrize("out,guard", [("f32", 5), ("bf16", 3), ("f32", 7)])
-def test_staged_c(h, act, out, guard):
-    """Large C whose rows bulk stores cannot write (misaligned, or ending inside
-    a 16-byte piece): the operations ride on the bulk stores into the aligned
-    copy, which the copy kernel then writes into C, M x N elements only."""
-    p = inputs.make_problem("epi_staged", 1100, 1001, 300, 0, 1, "bf16", out, ("normal", 0, 1), ("normal", 0, 1),
-                            alpha=0.5, seed=40 + act + guard)
-    check(p, h, bias_for(p.N, 5), act, 0.75, guard_cols=guard, expect_bulk=G.BULK_STAGED)
+@pytest.mark.parametrize("mode", [0, 3, 4])
+def test_misaligned_c(h, act, out, guard, mode):
+    """C whose rows bulk tensor stores cannot write (misaligned, or ending
+    inside a 16-byte piece): the operations ride on the row-class stores (fp32
+    C, auto), on the per-row bulk copies (GEMM_OPT_EPILOGUE = 4) or on the bulk
+    stores into the aligned workspace copy that the copy kernel then writes
+    into C (3), M x N elements only."""
+    if mode == 0 and out != "f32":
+        pytest.skip("row classes are planned for fp32 C")
+    p = inputs.make_problem("epi_misaligned", 1100, 1001, 300, 0, 1, "bf16", out, ("normal", 0, 1),
+                            ("normal", 0, 1), alpha=0.5, seed=40 + act + guard)
+    h.set_option(G.OPT_EPILOGUE, mode)
+    try:
+        expect = {0: G.BULK_ROW_CLASSES, 3: G.BULK_STAGED, 4: G.BULK_ROW_COPIES}[mode]
+        check(p, h, bias_for(p.N, 5), act, 0.75, guard_cols=guard, expect_bulk=expect)
+    finally:
+        h.set_option(G.OPT_EPILOGUE, 0)
+
+
+@pytest.mark.parametrize("act", ACTS)
+@pytest.mark.parametrize("transA,transB", [(0, 0), (1, 1)])
+def test_bulk_store_with_blend(h, act, transA, transB):
+    """beta != 0 with rows bulk stores can write: the old C arrives by tensor
+    loads into the staging buffer; the blend comes before the bias and activation."""
+    p = inputs.make_problem("epi_blend_bulk", 300, 520, 200, transA, transB, "f16", "f16", ("uniform", -1, 1),
+                            ("uniform", -1, 1), alpha=1.5, beta=-0.5, seed=30 + act)
+    check(p, h, bias_for(p.N, 4), act, 2.0, guard_cols=8, expect_bulk=G.BULK_ROWS)
 
 
 @pytest.mark.parametrize("sched", ["split", "stream_k"])

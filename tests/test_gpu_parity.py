@@ -197,23 +197,49 @@ def _check_bulk(p, h, expect_bulk):
 OUT_TYPES = [("bf16", "f32"), ("bf16", "bf16"), ("f16", "f16")]
 
 
+def _expected_misaligned_path(M, N, K, mode, out_dtype):
+    """The planner's choice for C that bulk tensor stores cannot write (beta == 0,
+    one unswapped GEMM): fp32 C in row classes (auto mode, at least 4 rows and
+    8 columns); else the workspace copy for a large C with K < 2048, else
+    per-row copies.  GEMM_OPT_EPILOGUE = 3 asks for the copy where allowed, 4
+    for per-row copies."""
+    staged_ok = M * N >= 1 << 20
+    if mode == 3:
+        return G.BULK_STAGED if staged_ok else G.BULK_ROW_COPIES
+    if mode == 4:
+        return G.BULK_ROW_COPIES
+    if out_dtype == "f32" and M >= 4 and N >= 8:
+        return G.BULK_ROW_CLASSES
+    return G.BULK_STAGED if staged_ok and K < 2048 else G.BULK_ROW_COPIES
+
+
+@pytest.mark.parametrize("mode", [0, 3, 4])
 @pytest.mark.parametrize("in_dtype,out_dtype", OUT_TYPES)
 @pytest.mark.parametrize("M,N,K,transB,guard_cols", [
     (1100, 1001, 300, 1, 5),    # misaligned rows (ldc = 1006), ragged N
     (1030, 1024, 200, 0, 3),    # misaligned rows, N whole pieces
     (1500, 1003, 96, 1, 13),    # rows aligned for 16-bit C only (ldc = 1016), N ends inside a piece
+    (300, 77, 130, 1, 1),       # small C, a single partial tile column (ldc = 78)
+    (600, 2003, 2100, 1, 2),    # long K
 ])
-def test_staged_c(h, M, N, K, transB, guard_cols, in_dtype, out_dtype):
-    """C that bulk stores cannot write goes through an aligned copy in the
-    workspace, then a copy kernel: exact values where they belong, and nothing
-    written in C's padding columns or the guard rows below it."""
-    p = inputs.make_problem("staged", M, N, K, 0, transB, in_dtype, out_dtype, ("normal", 0, 1), ("normal", 0, 1),
-                            alpha=0.5, seed=M + N + guard_cols)
-    plan = G.plan(p.M, p.N, p.K, p.transA, p.transB, dtype_code(p), handle=h, ldc=p.ldc + guard_cols)
+def test_misaligned_c(h, M, N, K, transB, guard_cols, in_dtype, out_dtype, mode):
+    """C that bulk tensor stores cannot write: each row of a block leaves
+    through one 1-D bulk copy of its whole 16-byte pieces (plain stores for the
+    partial pieces at a tile's edges), or bulk stores write an aligned copy in
+    the workspace that a copy kernel moves into C.  Exact values where they
+    belong, nothing written in C's padding columns or the guard rows below it."""
+    p = inputs.make_problem("misaligned", M, N, K, 0, transB, in_dtype, out_dtype, ("normal", 0, 1),
+                            ("normal", 0, 1), alpha=0.5, seed=M + N + guard_cols)
     aligned = ((p.ldc + guard_cols) * (4 if out_dtype == "f32" else 2)) % 16 == 0
     whole = (N * (4 if out_dtype == "f32" else 2)) % 16 == 0
-    assert plan.bulk_store == (G.BULK_ROWS if aligned and whole else G.BULK_STAGED), plan.as_dict()
-    out, full = run(p, h, guard_rows=3, guard_cols=guard_cols)
+    h.set_option(G.OPT_EPILOGUE, mode)
+    try:
+        plan = G.plan(p.M, p.N, p.K, p.transA, p.transB, dtype_code(p), handle=h, ldc=p.ldc + guard_cols)
+        expect = G.BULK_ROWS if aligned and whole else _expected_misaligned_path(M, N, K, mode, out_dtype)
+        assert plan.bulk_store == expect, plan.as_dict()
+        out, full = run(p, h, guard_rows=3, guard_cols=guard_cols)
+    finally:
+        h.set_option(G.OPT_EPILOGUE, 0)
     R, Mag = oracle_full(p)
     assert_close(out, R, Mag, p.out_dtype == "f32", p.name)
     pad = full.clone().to(torch.float64)
@@ -221,20 +247,72 @@ def test_staged_c(h, M, N, K, transB, guard_cols, in_dtype, out_dtype):
     assert torch.all(pad == SENTINEL), "C written outside the M x N block"
 
 
-def test_staged_c_in_sequence(h):
-    """Staged calls of different sizes in a row on one stream share the
-    workspace copy of C; each one's C is complete when the stream is."""
-    outs = []
-    for i, (M, N, K) in enumerate([(1200, 1001, 128), (2100, 999, 64), (1100, 1001, 256)]):
-        p = inputs.make_problem("staged_seq%d" % i, M, N, K, 0, 1, "bf16", "f32", ("normal", 0, 1),
-                                ("normal", 0, 1), seed=40 + i)
-        Ad, Bd, Cd, ldc = device_problem(p, guard_rows=1, guard_cols=1)
-        launch(p, h, Ad, Bd, Cd, ldc)
-        outs.append((p, Cd))
+@pytest.mark.parametrize("mode", [0, 4])
+@pytest.mark.parametrize("cg,bn", CONFIGS)
+@pytest.mark.parametrize("ldc_extra", [0, 1, 2])
+def test_misaligned_fp32_every_tile_config(h, cg, bn, ldc_extra, mode):
+    """Row classes (mode 0) and per-row bulk copies (mode 4) in every tile
+    configuration, several tiles per CTA (grid 6) and every misalignment a row
+    of fp32 C can have: with the 5 guard columns, ldc = 909, 910, 911 makes
+    consecutive rows start 4, 8 or 12 bytes further off a 16-byte boundary
+    (four, two and four row classes)."""
+    p = inputs.make_problem("rowcopy", 700, 904, 2100, 0, 1, "bf16", "f32", ("normal", 0, 1), ("normal", 0, 1),
+                            alpha=0.75, seed=bn + cg + ldc_extra, ldc=904 + ldc_extra)
+    h.set_option(G.OPT_EPILOGUE, mode)
+    try:
+        with options(h, path=PATHS[cg], bn=bn, grid=6, stream_k=1):
+            plan = G.plan(p.M, p.N, p.K, p.transA, p.transB, handle=h, ldc=p.ldc + 5)   # _check adds 5 guard columns
+            assert plan.bulk_store == (G.BULK_ROW_CLASSES if mode == 0 else G.BULK_ROW_COPIES), plan.as_dict()
+            _check(p, h)
+    finally:
+        h.set_option(G.OPT_EPILOGUE, 0)
+
+
+@pytest.mark.parametrize("M,N,K,ldc", [(4095, 4097, 1000, 4097), (300, 77, 130, 78), (129, 1001, 64, 1001),
+                                       (70, 8, 16, 9), (1000, 1003, 300, 1006), (260, 36, 70, 39)])
+def test_row_classes_shapes(h, M, N, K, ldc):
+    """fp32 C in row classes at ragged sizes: tiles narrower than a block, a
+    right edge inside a 16-byte piece (the values past the class tensor's last
+    whole piece go out by plain stores), a single tile column, fewer rows than
+    a tile, and C's rows packed end to end (ldc = N), where any write past
+    column N would land in the next row."""
+    p = inputs.make_problem("rowclass", M, N, K, 0, 0, "bf16", "f32", ("normal", 0, 1), ("normal", 0, 1),
+                            alpha=1.25, seed=M + N + K, ldc=ldc)
+    plan = G.plan(p.M, p.N, p.K, p.transA, p.transB, handle=h, ldc=ldc)
+    assert plan.bulk_store == G.BULK_ROW_CLASSES, plan.as_dict()
+    Ad, Bd = p.A.cuda(), p.B.cuda()
+    C = torch.full((p.M + 2, ldc), SENTINEL, dtype=torch.float32, device="cuda")
+    C[:p.M, :p.N] = float("nan")
+    launch(p, h, Ad, Bd, C, ldc)
     assert h.status()[0] == G.OK
-    for p, Cd in outs:
-        R, Mag = oracle_full(p)
-        assert_close(Cd[:p.M, :p.N].double().cpu().numpy(), R, Mag, True, p.name)
+    full = C.cpu()
+    R, Mag = oracle_full(p)
+    assert_close(full[:p.M, :p.N].double().numpy(), R, Mag, True, p.name)
+    pad = full.clone().to(torch.float64)
+    pad[:p.M, :p.N] = SENTINEL
+    assert torch.all(pad == SENTINEL), "C written outside the M x N block"
+
+
+def test_misaligned_c_in_sequence(h):
+    """Misaligned calls of different sizes in a row on one stream, with per-row
+    copies and with the workspace copy of C: each one's C is complete when the
+    stream is."""
+    for mode in (3, 4):
+        h.set_option(G.OPT_EPILOGUE, mode)
+        outs = []
+        try:
+            for i, (M, N, K) in enumerate([(1200, 1001, 128), (2100, 999, 64), (1100, 1001, 256)]):
+                p = inputs.make_problem("misaligned_seq%d" % i, M, N, K, 0, 1, "bf16", "f32", ("normal", 0, 1),
+                                        ("normal", 0, 1), seed=40 + i)
+                Ad, Bd, Cd, ldc = device_problem(p, guard_rows=1, guard_cols=1)
+                launch(p, h, Ad, Bd, Cd, ldc)
+                outs.append((p, Cd))
+            assert h.status()[0] == G.OK
+        finally:
+            h.set_option(G.OPT_EPILOGUE, 0)
+        for p, Cd in outs:
+            R, Mag = oracle_full(p)
+            assert_close(Cd[:p.M, :p.N].double().cpu().numpy(), R, Mag, True, p.name)
 
 
 @pytest.mark.parametrize("in_dtype,out_dtype", OUT_TYPES)
