@@ -571,8 +571,48 @@ def leg_fp32(ctx):
     _tensor_leg(ctx, "fp32_tf", p, G.F32_F32, ctx["args"].fp32_steps, peak_scale=1.1 / 2.25, work_scale=3.0)
 
 
+def leg_nvfp4_lm_head(ctx):
+    """The LM head with NVFP4 operands (E2M1 codes, an unsigned E4M3 scale per 16
+    values), bf16 C: GB/s of algorithmic bytes (codes, scale codes, C) against
+    the measured copy bandwidth.  The weights stay in their codes; the GEMM
+    converts them as they arrive."""
+    import torch
+    G, dev = ctx["G"], ctx["dev"]
+    inp = ctx["inputs"]
+    p = inp.make_block_scaled_problem("lm_head_64x32000x4096_nvfp4", 64, 32000, 4096, "nvfp4", "bf16", seed=0,
+                                      alpha=1.0 / 64)
+    ops = [p.A.to(dev), p.SFA.to(dev), p.B.to(dev), p.SFB.to(dev)]
+    set_bytes = sum(t.numel() for t in ops) + p.M * p.ldc * 2
+    n = n_rotating_sets(set_bytes)
+    sets = [ops] + [[t.clone() for t in ops] for _ in range(n - 1)]
+    C = torch.empty(p.M, p.ldc, dtype=torch.bfloat16, device=dev)
+    h, sptr = ctx["h"], ctx["stream"].cuda_stream
+
+    def step(i):
+        A, SA, B, SB = sets[i % n]
+        st = h.run_block_scaled_raw(p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, SA.data_ptr(), p.ld_sfa,
+                                    B.data_ptr(), p.ldb, SB.data_ptr(), p.ld_sfb, 0.0, C.data_ptr(), p.ldc,
+                                    G.NVFP4_BF16, sptr)
+        if st != G.OK:
+            raise G.GemmError(st, "gemm_run_block_scaled")
+
+    ms, wall = time_steps(step, ctx["args"].skinny_steps, ctx["stream"], dev, warm=20)
+    st, word = h.status(sptr)
+    if st != G.OK:
+        raise RuntimeError("nvfp4 kernel status %s (0x%x)" % (G.STATUS.get(st), word))
+    nbytes = sum(t.numel() for t in ops) + p.M * p.N * 2
+    gbs = nbytes / (ms / 1e3) / 1e9
+    hbm = float(ctx["pk"].get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    plan = G.plan_block_scaled(p.M, p.N, p.K, G.NVFP4_BF16, lda=p.lda, ldb=p.ldb, ld_sfa=p.ld_sfa,
+                               ld_sfb=p.ld_sfb, ldc=p.ldc, handle=h)
+    ctx["legs"]["f1_nvfp4_lm_gbs"] = [_sig(gbs), _sig(gbs / hbm, 3)]
+    ctx["detail"]["f1_nvfp4_lm_gbs"] = {"workload": p.name, "us_per_call": ms * 1e3, "gbs": gbs,
+                                        "algorithmic_bytes_per_call": nbytes, "plan": plan.as_dict(),
+                                        "l2": "%d rotating sets of %.0f MB" % (n, set_bytes / 2 ** 20)}
+
+
 LEGS = [("tiny", leg_tiny), ("bf16_out", leg_bf16_out), ("blend", leg_blend), ("llm", leg_llm),
-        ("skinny", leg_skinny), ("fp8", leg_fp8), ("fp32", leg_fp32)]
+        ("skinny", leg_skinny), ("nvfp4", leg_nvfp4_lm_head), ("fp8", leg_fp8), ("fp32", leg_fp32)]
 
 
 def main():

@@ -213,8 +213,9 @@ __device__ __forceinline__ void load_piece(const uint8_t* __restrict__ src, int6
 // divides the block, so one scale code covers a piece.  `vec`: rows start
 // 16-byte (FP8) / 8-byte (FP4) aligned, so whole pieces load as one vector; the
 // tail of a row (k0 + 16 > K) is read byte by byte.
+template <bool kF16>
 __global__ void dequant_kernel(const uint8_t* __restrict__ src, int64_t lds, const uint8_t* __restrict__ sf,
-                               int64_t ld_sf, int fmt, int e8m0, int block, int vec, __nv_bfloat16* __restrict__ dst,
+                               int64_t ld_sf, int fmt, int e8m0, int block, int vec, uint16_t* __restrict__ dst,
                                int64_t ldd, int64_t rows, int64_t K) {
   const int64_t k0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 16;
   if (k0 >= ldd) return;
@@ -236,8 +237,13 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ src, int64_t lds, con
       // values past K (the high half of a last, half-used FP4 byte too) are 0
       if (k0 + 2 * t >= K) x0 = 0.0f;
       if (k0 + 2 * t + 1 >= K) x1 = 0.0f;
-      const __nv_bfloat162 pr = __floats2bfloat162_rn(x0 * scale, x1 * scale);
-      packed[t] = *reinterpret_cast<const uint32_t*>(&pr);
+      if constexpr (kF16) {  // (NVFP4 values: at most 6 significant bits, inside fp16's range)
+        const __half2 pr = __floats2half2_rn(x0 * scale, x1 * scale);
+        packed[t] = *reinterpret_cast<const uint32_t*>(&pr);
+      } else {
+        const __nv_bfloat162 pr = __floats2bfloat162_rn(x0 * scale, x1 * scale);
+        packed[t] = *reinterpret_cast<const uint32_t*>(&pr);
+      }
     }
     uint4* out = reinterpret_cast<uint4*>(dst + r * ldd + k0);
     out[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
@@ -352,7 +358,7 @@ cudaError_t split_tf32_launch(const float* src, int64_t lds, int64_t sbs, bool t
 }
 
 cudaError_t dequant_launch(const void* src, int64_t lds, const void* sf, int64_t ld_sf, int fmt, bool e8m0,
-                           int block, void* dst, int64_t ldd, int64_t rows, int64_t K, int sm_count,
+                           int block, void* dst, int64_t ldd, int64_t rows, int64_t K, bool f16_out, int sm_count,
                            cudaStream_t stream) {
   if (ldd % 16 != 0) return cudaErrorInvalidValue;
   const int64_t pieces = ldd / 16;  // per row
@@ -364,9 +370,15 @@ cudaError_t dequant_launch(const void* src, int64_t lds, const void* sf, int64_t
   if (gy < 1) gy = 1;
   const uintptr_t base = reinterpret_cast<uintptr_t>(src);
   const int vec = fmt == 2 ? (base % 8 == 0 && (lds / 2) % 8 == 0) : (base % 16 == 0 && lds % 16 == 0);
-  dequant_kernel<<<dim3(gx, static_cast<unsigned>(gy), 1), 128, 0, stream>>>(
-      static_cast<const uint8_t*>(src), lds, static_cast<const uint8_t*>(sf), ld_sf, fmt, e8m0 ? 1 : 0, block, vec,
-      static_cast<__nv_bfloat16*>(dst), ldd, rows, K);
+  const dim3 grid(gx, static_cast<unsigned>(gy), 1);
+  if (f16_out)
+    dequant_kernel<true><<<grid, 128, 0, stream>>>(static_cast<const uint8_t*>(src), lds,
+                                                   static_cast<const uint8_t*>(sf), ld_sf, fmt, e8m0 ? 1 : 0, block,
+                                                   vec, static_cast<uint16_t*>(dst), ldd, rows, K);
+  else
+    dequant_kernel<false><<<grid, 128, 0, stream>>>(static_cast<const uint8_t*>(src), lds,
+                                                    static_cast<const uint8_t*>(sf), ld_sf, fmt, e8m0 ? 1 : 0, block,
+                                                    vec, static_cast<uint16_t*>(dst), ldd, rows, K);
   return cudaGetLastError();
 }
 

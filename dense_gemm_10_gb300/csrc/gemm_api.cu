@@ -47,6 +47,7 @@ struct Options {
   int pdl = 1;       // GEMM_OPT_PDL: programmatic dependent launch of the main kernel
   int plan_cache = 1;  // GEMM_OPT_PLAN_CACHE: reuse the plans of recent calls
   bool stage_c = true; // C that bulk stores cannot write may go through an aligned copy
+  int dq_kernel = 0;   // GEMM_OPT_DEQUANT_IN_KERNEL: 0 auto, 1 never (the dequantising pass for both operands)
 };
 
 // One stored operand, as the tensor-memory-accelerator copy engine will see it.
@@ -76,6 +77,9 @@ struct Operand {
   int dq = 0;
   const void* sf = nullptr;
   int64_t ld_sf = 0;
+  // block-scaled codes read by a DQ kernel as they are (converted in the kernel)
+  bool codes = false;
+  bool dq_f16 = false;  // dequant_launch writes fp16 (NVFP4 operands of a DQ kernel) instead of bf16
 };
 
 struct Plan {
@@ -104,6 +108,9 @@ struct Plan {
   size_t c_ws_offset = 0;
   // fp32 C off 16-byte boundaries written by tensor stores per row class (CMaps)
   int32_t c_classes = 0;
+  // a DQ kernel: P's block-scaled codes converted in the kernel
+  int32_t dq_fmt = 0, code_bytes = 0, spk = 0;
+  int64_t code_cols = 0, scale_cols = 0;  // bytes of codes and scale codes in a row of P
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -460,6 +467,31 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
 
   // A short M rides on the MMA's N dimension: compute C^T = op(B)^T op(A)^T.
   const bool swap = groups == 0 && M <= 64 && N > M;
+  // Block-scaled operands of such a swapped (HBM-bound) GEMM: the weights B,
+  // streamed once, stay in their codes and the DQ kernel's converter warps
+  // write their 16-bit values into the ring as they arrive (fp16 for NVFP4,
+  // whose code x scale products fp16 holds exactly; bf16 for MXFP8), instead
+  // of a pass that writes two to four times the bytes it reads.  The copy
+  // engine needs 16-byte aligned rows of codes and of scale codes.
+  bool dq_kernel = false;
+  if (dt.sc != 0 && swap && o.dq_kernel == 0) {
+    const int64_t row_bytes = dt.sc == 2 ? ldb / 2 : ldb;
+    dq_kernel = reinterpret_cast<uintptr_t>(B) % 16 == 0 && row_bytes % 16 == 0 &&
+                reinterpret_cast<uintptr_t>(bs->sfb) % 16 == 0 && bs->ld_sfb % 16 == 0;
+  }
+  if (dq_kernel) {
+    b.dq = 0;
+    b.codes = true;
+    a.dq_f16 = dt.sc == 2;
+    pl.dq_fmt = dt.sc == 2 ? 1 : (dt.src_b == 1 ? 3 : 2);
+    pl.code_bytes = dt.sc == 2 ? 32 : 64;
+    pl.spk = dt.sc == 2 ? 4 : 2;
+    pl.code_cols = dt.sc == 2 ? (K + 1) / 2 : K;
+    pl.scale_cols = cdiv(K, dt.block);
+    if (dt.sc == 2) {  // fp16 operands
+      pl.in_dtype = static_cast<int32_t>(CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+    }
+  }
   P.swap_ab = swap ? 1 : 0;
   pl.I = swap ? N : M;
   pl.J = swap ? M : N;
@@ -470,6 +502,7 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   if (cdiv(pl.I, kBM) * cdiv(pl.J, 64) * batch > (int64_t{1} << 30)) return GEMM_ERR_UNSUPPORTED;
   pl.a_fmt = swap ? dt.b_fmt : dt.a_fmt;  // formats of the MMA's A (P) and B (Q) operands
   pl.b_fmt = swap ? dt.a_fmt : dt.b_fmt;
+  if (dq_kernel && dt.sc == 2) pl.a_fmt = pl.b_fmt = 0;  // fp16
   pl.c_si = swap ? 1 : ldc;
   pl.c_sj = swap ? ldc : 1;
   P.a_kmajor = pl.p.kmajor ? 1 : 0;
@@ -486,11 +519,12 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
 
   // Tile configuration and schedule: the configuration with the lowest
   // estimated time, est_time() below.
-  static const int kPreference[kNumTileConfigs] = {4, 3, 2, 1, 5, 0, 9, 8, 7, 6, 12, 11, 10};  // ties go first
+  static const int kPreference[kNumTileConfigs] = {4, 3, 2, 1, 5, 0, 9, 8, 7, 6, 12, 11, 10, 13};  // ties go first
   Choice best;
   for (int cfg : kPreference) {
     const TileConfig& c = kTileConfigs[cfg];
     if (c.eb != dt.eb) continue;
+    if ((c.dq != 0) != dq_kernel) continue;
     const int path = c.cg == 2 ? GEMM_PATH_TC_2CTA : GEMM_PATH_TC_1CTA;
     if (o.force_path && o.force_path != path) continue;
     if (o.force_bn && c.bn != o.force_bn) continue;
@@ -499,8 +533,9 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
     if (c.bn / c.cg < 64 && !pl.q.kmajor) continue;  // half-atom Q halves: K-major only
     int nslots = slots.of(cfg);
     if (o.max_grid) nslots = std::min(nslots, std::max(1, o.max_grid / c.cg));
-    // Two k-slices per stage where the ring still holds at least two such stages.
-    int kdepth = o.kdepth ? o.kdepth : default_kdepth(c);
+    // Two k-slices per stage where the ring still holds at least two such stages
+    // (a DQ kernel converts one k-slice a stage).
+    int kdepth = c.dq ? 1 : o.kdepth ? o.kdepth : default_kdepth(c);
     if (kdepth > 1 && tc_stages(cfg) / kdepth < 2) kdepth = 1;
     // grouped: each group's rows padded to whole tiles
     int64_t tile_rows = cdiv(pl.I, kBM * c.cg);
@@ -557,6 +592,7 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
   // Workspace: repacked operands, then partial tiles of split tiles.
   size_t ws = 0;
   for (Operand* op : {&pl.p, &pl.q}) {
+    if (op->codes) continue;  // read as codes by the DQ kernel
     if (op->split_parts > 0 || op->dq > 0 || !tma_aligned(op->ptr, op->ld, dt.eb, op->bstride, op->nb)) {
       op->repack = true;  // rows padded to whole 16-byte pieces, batches packed
       // (dequantised rows: whole 16-value pieces, one per thread of dequant_launch)
@@ -719,6 +755,29 @@ gemm_status_t encode_c(CUtensorMap* map, void* C, int64_t rows, int64_t cols, in
                  : c_type == kCBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   return encode_tiled(cache, tmap_desc(C, dims, strides, box, dt, swz, CU_TENSOR_MAP_L2_PROMOTION_NONE), map);
+}
+
+// A DQ kernel's P operand as it is stored: rows of block-scaled codes
+// (code_cols bytes a row, ld_bytes apart; boxes of code_bytes x 128 rows,
+// one k-slice) and their scale codes (scale_cols bytes a row, ld_sf apart;
+// boxes of 16 x 128 rows, four or eight k-slices' worth).  Bytes past a row's
+// codes or scale codes arrive as zeros.
+gemm_status_t encode_codes(CUtensorMap* codes, CUtensorMap* scales, const void* ptr, int64_t rows, int64_t code_cols,
+                           int64_t ld_bytes, int code_bytes, const void* sf, int64_t scale_cols, int64_t ld_sf,
+                           TmapCache* cache) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(code_cols), static_cast<uint64_t>(rows), 1};
+  const uint64_t strides[2] = {static_cast<uint64_t>(ld_bytes), round_up(static_cast<size_t>(rows * ld_bytes), 16)};
+  const uint32_t box[3] = {static_cast<uint32_t>(code_bytes), static_cast<uint32_t>(kBM), 1};
+  gemm_status_t s = encode_tiled(cache, tmap_desc(ptr, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                                                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B),
+                                 codes);
+  if (s != GEMM_OK) return s;
+  const uint64_t sdims[3] = {static_cast<uint64_t>(scale_cols), static_cast<uint64_t>(rows), 1};
+  const uint64_t sstrides[2] = {static_cast<uint64_t>(ld_sf), round_up(static_cast<size_t>(rows * ld_sf), 16)};
+  const uint32_t sbox[3] = {16, static_cast<uint32_t>(kBM), 1};
+  return encode_tiled(cache, tmap_desc(sf, sdims, sstrides, sbox, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                                       CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B),
+                      scales);
 }
 
 // The row-class tensor maps of fp32 C (rows x cols, row pitch ldc elements,
@@ -952,6 +1011,10 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
       if (value < 0 || value > 1) return GEMM_ERR_INVALID_ARG;
       h->opt.plan_cache = static_cast<int>(value);
       return GEMM_OK;
+    case GEMM_OPT_DEQUANT_IN_KERNEL:
+      if (value < 0 || value > 1) return GEMM_ERR_INVALID_ARG;
+      h->opt.dq_kernel = static_cast<int>(value);
+      return GEMM_OK;
   }
   return GEMM_ERR_INVALID_ARG;
 }
@@ -1017,7 +1080,7 @@ static cudaError_t prepare_operands(const Plan& pl, uint8_t* ws, int sm_count, c
     cudaError_t e;
     if (op.dq > 0)
       e = dequant_launch(op.ptr, op.ld, op.sf, op.ld_sf, op.dq - 1, op.dq - 1 != 2 /* MXFP8: E8M0 */,
-                         op.dq - 1 == 2 ? 16 : 32, dst, op.packed_ld, op.rows, op.cols, sm_count, st);
+                         op.dq - 1 == 2 ? 16 : 32, dst, op.packed_ld, op.rows, op.cols, op.dq_f16, sm_count, st);
     else if (op.split_parts > 0)
       e = split_tf32_launch(static_cast<const float*>(op.ptr), op.ld, op.bstride, op.split_trans,
                             static_cast<float*>(dst), op.packed_ld, op.rows * op.packed_ld, op.rows, op.src_k,
@@ -1134,8 +1197,14 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
 
   CUtensorMap map_p, map_q;
   TmapCache* tc = &h->tmaps;
-  s = encode_operand(&map_p, pl.p, pbase, pld, pl.p.repack ? pl.p.rows * pld : pl.p.bstride, pl.eb,
-                     pl.in_dtype, kBM, tc);
+  CMaps cmaps;
+  std::memset(&cmaps, 0, sizeof(cmaps));
+  if (pl.p.codes)  // (a DQ kernel: P's codes, and their scale codes in cmaps.m[0])
+    s = encode_codes(&map_p, &cmaps.m[0], pl.p.ptr, pl.p.rows, pl.code_cols, pl.dq_fmt == 1 ? pl.p.ld / 2 : pl.p.ld,
+                     pl.code_bytes, pl.p.sf, pl.scale_cols, pl.p.ld_sf, tc);
+  else
+    s = encode_operand(&map_p, pl.p, pbase, pld, pl.p.repack ? pl.p.rows * pld : pl.p.bstride, pl.eb,
+                       pl.in_dtype, kBM, tc);
   if (s != GEMM_OK) return s;
   s = encode_operand(&map_q, pl.q, qbase, qld, pl.q.repack ? pl.q.rows * qld : pl.q.bstride, pl.eb,
                      pl.in_dtype, P.bn / cg, tc);
@@ -1154,8 +1223,6 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
     if (s != GEMM_OK) return s;
   }
 
-  CMaps cmaps;
-  std::memset(&cmaps, 0, sizeof(cmaps));
   if (pl.c_classes > 0) {
     s = encode_c_classes(&cmaps, C, pl.I, pl.J, ldc, pl.c_classes, tc);
     if (s != GEMM_OK) return s;
@@ -1175,6 +1242,13 @@ static gemm_status_t run_gemm(gemm_handle_t h, gemm_op_t transA, gemm_op_t trans
   a.alpha = alpha;
   a.beta = beta;
   a.c_classes = pl.c_classes;
+  a.dq_fmt = pl.dq_fmt;
+  a.code_bytes = pl.code_bytes;
+  a.spk = pl.spk;
+  if (pl.dq_fmt != 0) {  // the code ring: Q's 16-bit tile, 128 rows of codes, 128 x 16 bytes of scale codes
+    a.code_stage_bytes = P.bn / cg * kSliceBytes + kBM * pl.code_bytes + kBM * 16;
+    a.code_stages = std::min(16, tc_code_ring_bytes(pl.cfg) / a.code_stage_bytes);
+  }
   a.C = c_out;
   a.c_si = pl.c_staged ? pl.c_ws_ld : pl.c_si;
   a.c_sj = pl.c_sj;

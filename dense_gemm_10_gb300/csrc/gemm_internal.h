@@ -14,6 +14,8 @@ constexpr int kBM = 128;          // MMA M (rows of the output tile held in TMEM
 constexpr int kSliceBytes = 128;  // a k-slice: one 128-byte swizzle row of every tile row
 constexpr int kBK = 64;           // k-slice of 16-bit elements (64 x 2 bytes)
 constexpr int kThreads = 192;     // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue
+constexpr int kThreadsDq = 320;   // the same, and warps 6-9 converting block-scaled codes (DQ kernels)
+__host__ __device__ constexpr int threads_of(bool dq) { return dq ? kThreadsDq : kThreads; }
 
 // k elements of one k-slice for an element of eb bytes (2: bf16 / fp16, 1: FP8).
 __host__ __device__ constexpr int slice_k(int eb) { return kSliceBytes / eb; }
@@ -35,9 +37,9 @@ struct EpiOps {
 // Status-word layout written by a kernel that gives up on a barrier:
 //   bits 0-7 = 6 (GEMM_ERR_TIMEOUT), bits 8-11 = role, bits 12-15 = barrier.
 enum : int32_t { kStatusTimeout = 6 };
-enum WaitRole : int32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3 };
+enum WaitRole : int32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleConvert = 4 };
 enum WaitBarrier : int32_t {
-  kBarEmpty = 1, kBarFull = 2, kBarAccEmpty = 3, kBarAccFull = 4, kBarDrain = 5, kBarCLoad = 6
+  kBarEmpty = 1, kBarFull = 2, kBarAccEmpty = 3, kBarAccFull = 4, kBarDrain = 5, kBarCLoad = 6, kBarCodeFull = 7
 };
 
 // Arguments of the persistent tcgen05 GEMM kernel, in the kernel's own terms:
@@ -77,6 +79,15 @@ struct TcArgs {
   const int64_t* group_row;
   const int32_t* group_m;
   int32_t c_classes;     // kBulkRowCopies with fp32 C: P row classes with tensor maps in CMaps (0: per-row copies)
+  // DQ kernels: P arrives as block-scaled codes (map_p: the codes, CMaps m[0]:
+  // their scale codes) and converter warps write its 16-bit values into the
+  // ring.  dq_fmt: 1 E2M1 codes with unsigned E4M3 scales per 16 values (to
+  // fp16), 2 / 3 E4M3 / E5M2 codes with E8M0 scales per 32 values (to bf16).
+  int32_t dq_fmt;
+  int32_t code_bytes;    // code bytes of one row of a k-slice (32 for E2M1, 64 for the 8-bit codes)
+  int32_t spk;           // scale codes of one row of a k-slice (4 or 2)
+  int32_t code_stages;       // stages of the code ring (<= 16)
+  int32_t code_stage_bytes;  // Q's tile, 128 rows of codes, 128 x 16 bytes of scale codes (a multiple of 1024)
 };
 
 // Epilogue store paths: direct stores, or staged bulk tensor stores of rows of
@@ -103,10 +114,12 @@ struct CMaps {
 // (kind::tf32).
 struct TileConfig {
   int bn, cg, eb;
+  int dq;  // 1: P arrives as block-scaled codes, converted in the kernel (kThreadsDq threads)
 };
-constexpr int kNumTileConfigs = 13;
+constexpr int kNumTileConfigs = 14;
 extern const TileConfig kTileConfigs[kNumTileConfigs];
 int tc_stages(int cfg);  // ring depth in k-slices
+int tc_code_ring_bytes(int cfg);  // DQ kernels: shared memory of the code ring (0 for the others)
 // One-time per device: opt in to the kernel's shared memory; for clusters also
 // report how many can be resident at once.
 cudaError_t tc_prepare(int cfg, int* max_clusters);
@@ -144,13 +157,13 @@ cudaError_t split_tf32_launch(const float* src, int64_t lds, int64_t sbs, bool t
                               int64_t ldd, int64_t dbs, int64_t rows, int64_t K, int64_t seg, int64_t nb, int parts,
                               int pattern, int sm_count, cudaStream_t stream);
 
-// Block-scaled operand -> bf16, K-major: dst[r * ldd + k] = code(r, k) *
+// Block-scaled operand -> bf16 (fp16 when f16_out), K-major: dst[r * ldd + k] = code(r, k) *
 // scale(r, k / block) for k < K, 0 for K <= k < ldd (ldd a multiple of 16, dst
 // 16-byte aligned).  fmt: 0 E4M3, 1 E5M2, 2 E2M1 packed two a byte (even k
 // low); lds counts values; scale codes E8M0 (e8m0) or unsigned E4M3, rows of
 // ld_sf codes.  block: 16 or 32.
 cudaError_t dequant_launch(const void* src, int64_t lds, const void* sf, int64_t ld_sf, int fmt, bool e8m0,
-                           int block, void* dst, int64_t ldd, int64_t rows, int64_t K, int sm_count,
+                           int block, void* dst, int64_t ldd, int64_t rows, int64_t K, bool f16_out, int sm_count,
                            cudaStream_t stream);
 
 // The whole GEMM when K == 0: C = ops(beta * C) over `batch` M x N matrices

@@ -137,6 +137,38 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.b16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Two E2M1 codes (byte bits 0-3 and 4-7) -> two fp16 values (low and high
+// half of the result), one hardware conversion.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(r) : "r"(byte));
+  return r;
+}
+
+// Two E4M3 (or E5M2) codes (bits 0-7 and 8-15) -> two fp16 values, one hardware conversion.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 h;\n\tcvt.u16.u32 h, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, h;\n\t}" : "=r"(r) : "r"(pair));
+  return r;
+}
+__device__ __forceinline__ uint32_t e5m2x2_to_f16x2(uint32_t pair) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 h;\n\tcvt.u16.u32 h, %1;\n\tcvt.rn.f16x2.e5m2x2 %0, h;\n\t}" : "=r"(r) : "r"(pair));
+  return r;
+}
+
 __device__ __forceinline__ float4 ld_shared_v4_f32(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)

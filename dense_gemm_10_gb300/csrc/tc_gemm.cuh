@@ -36,6 +36,8 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
 
 #include "epi_ops.cuh"
 #include "gemm_internal.h"
@@ -43,7 +45,7 @@
 
 namespace g10 {
 
-template <int BN, int CG>
+template <int BN, int CG, bool DQ = false>
 struct TcConfig {
   static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
   static_assert(CG == 1 || CG == 2, "CTA group");
@@ -62,13 +64,21 @@ struct TcConfig {
   static constexpr int kStagingBytes = 4 * 2 * 32 * 128;
   static constexpr int kCtrlBytes = 256;
   static constexpr int kRingMax = 232448 - 1024 - kStagingBytes - 1024;  // 227 KB less the rest
-  static constexpr int kStages = kRingMax / kStageBytes > 8 ? 8 : kRingMax / kStageBytes;
-  static constexpr int kRingBytes = kStages * kStageBytes;
+  // DQ: the ring holds only P's converted 16-bit tiles (three stages); Q's
+  // tile, P's block-scaled codes and a 16-byte box of their scale codes per
+  // row arrive in a deeper code ring filling the rest (its stage size and
+  // count depend on the code format: TcArgs::code_stage_bytes, code_stages),
+  // which the MMA reads Q from in place
+  static constexpr int kStages = DQ ? 3 : kRingMax / kStageBytes > 8 ? 8 : kRingMax / kStageBytes;
+  static constexpr int kRingBytes = DQ ? kStages * kABytes : kStages * kStageBytes;
+  static constexpr int kCodeRingBytes = DQ ? kRingMax - kRingBytes : 0;
+  static_assert(kCodeRingBytes % 1024 == 0, "code stages start on 1024-byte boundaries");
   // the last tile's epilogue stages C in the idle ring: eight 4 KB buffers per epilogue warp
-  static_assert(kRingBytes >= 4 * 8 * 32 * 128, "ring too small to stage a tile of C");
+  static constexpr bool kRingStagesC = kRingBytes >= 4 * 8 * 32 * 128;
+  static_assert(DQ || kRingStagesC, "ring too small to stage a tile of C");
   static constexpr int kTmemCols = 2 * BN;       // two fp32 accumulators of BN columns
-  // layout: [alignment slack][ring][control block, padded to 1 KB][staging]
-  static constexpr size_t kSmemBytes = 1024 + kRingBytes + 1024 + kStagingBytes;
+  // layout: [alignment slack][ring][code ring][control block, padded to 1 KB][staging]
+  static constexpr size_t kSmemBytes = 1024 + kRingBytes + kCodeRingBytes + 1024 + kStagingBytes;
 };
 
 struct TcCtrl {
@@ -78,11 +88,13 @@ struct TcCtrl {
   uint64_t acc_empty[2];
   uint64_t mma_done;
   uint64_t c_full[4][2];  // per epilogue warp and staging buffer: a block of old C has landed
+  uint64_t code_full[16];   // DQ: a code stage's Q tile, codes and scale codes have landed
+  uint64_t code_empty[16];  // DQ: the MMA has read a code stage's Q tile (the converters its codes before)
   uint32_t tmem_base;
   uint32_t abort;
   uint32_t last;
 };
-static_assert(sizeof(TcCtrl) <= 256, "control block");
+static_assert(sizeof(TcCtrl) <= 1024, "control block");
 
 // Swizzle atoms of an MN-major operand: 64 elements along M or N (128 bytes)
 // by 64 k-rows; atoms follow each other along M / N.
@@ -443,12 +455,15 @@ struct EpiOut {
     const int sh = static_cast<int>((reinterpret_cast<uintptr_t>(rowp) & 15u) >> 2);
     const uint32_t buf = buffer(true);
     const uint32_t sub = buf + static_cast<uint32_t>(cls * rows * 128);  // 1024-byte aligned (P <= 4)
+    // The P threads of one 8-thread store phase that share a buffer row index
+    // (one per class) write their pieces in an order rotated by their class,
+    // so that they reach different banks: piece (k + cls) mod n at step k.
     if (first) {
       // v[4 - sh .. 31 - sh]: columns j + 4 - sh .. j + 31 - sh, from the block's second piece on
       const uint32_t row = sub + static_cast<uint32_t>(br * 112);
+      float o[7][4];
 #pragma unroll
-      for (int k = 0; k < 7; ++k) {
-        float o[4];
+      for (int k = 0; k < 7; ++k)
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int e = 4 * k + u;
@@ -456,18 +471,30 @@ struct EpiOut {
 #pragma unroll
           for (int t = 1; t < 4; ++t)
             if (t == sh) x = v[e + 4 - t];
-          o[u] = x;
+          o[k][u] = x;
         }
-        st_shared_v4(row + static_cast<uint32_t>(k * 16), __float_as_uint(o[0]), __float_as_uint(o[1]),
-                     __float_as_uint(o[2]), __float_as_uint(o[3]));
+      float t1[7][4], t2[7][4];  // rotated left by cls (mod 7): by 1, then by 2
+#pragma unroll
+      for (int k = 0; k < 7; ++k)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) t1[k][u] = (cls & 1) ? o[(k + 1) % 7][u] : o[k][u];
+#pragma unroll
+      for (int k = 0; k < 7; ++k)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) t2[k][u] = (cls & 2) ? t1[(k + 2) % 7][u] : t1[k][u];
+#pragma unroll
+      for (int k = 0; k < 7; ++k) {
+        const int q = (k + cls) % 7;
+        st_shared_v4(row + static_cast<uint32_t>(q * 16), __float_as_uint(t2[k][0]), __float_as_uint(t2[k][1]),
+                     __float_as_uint(t2[k][2]), __float_as_uint(t2[k][3]));
       }
     } else {
       // [the previous block's last sh values | v[0 .. 31 - sh]]: columns j - sh .. j + 31 - sh
       const uint32_t row = sub + static_cast<uint32_t>(br * 128);
       const uint32_t sw = static_cast<uint32_t>(br & 7);
+      float o[8][4];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        float o[4];
+      for (int k = 0; k < 8; ++k)
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int e = 4 * k + u;
@@ -475,10 +502,22 @@ struct EpiOut {
 #pragma unroll
           for (int t = 1; t < 4; ++t)
             if (t == sh) x = e < t ? cy[4 - t + (e < t ? e : 0)] : v[e - t < 0 ? 0 : e - t];
-          o[u] = x;
+          o[k][u] = x;
         }
-        st_shared_v4(row + ((static_cast<uint32_t>(k) ^ sw) << 4), __float_as_uint(o[0]), __float_as_uint(o[1]),
-                     __float_as_uint(o[2]), __float_as_uint(o[3]));
+      float t1[8][4], t2[8][4];  // rotated left by cls (mod 8): by 1, then by 2
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) t1[k][u] = (cls & 1) ? o[(k + 1) & 7][u] : o[k][u];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) t2[k][u] = (cls & 2) ? t1[(k + 2) & 7][u] : t1[k][u];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t q = static_cast<uint32_t>((k + cls) & 7);
+        st_shared_v4(row + ((q ^ sw) << 4), __float_as_uint(t2[k][0]), __float_as_uint(t2[k][1]),
+                     __float_as_uint(t2[k][2]), __float_as_uint(t2[k][3]));
       }
     }
 #pragma unroll
@@ -496,7 +535,8 @@ struct EpiOut {
     // plain stores: the first block's values before its box, after the tile's
     // last block the values past its box, and the values past the class
     // tensor's last whole 16-byte piece (columns jcut and on)
-    if (i < c.I) {
+    // (jcut >= J - 3: an interior block with no values from column J - 3 on stores nothing)
+    if ((first || last || j + 32 > c.J - 3) && i < c.I) {
       const int jcut = ((c.J + sh) & ~3) - sh;
       const int64_t off = static_cast<int64_t>(i) * c.si + j;
 #pragma unroll
@@ -870,11 +910,12 @@ struct EpiOut {
 
 // ----------------------------------------------------------------- the roles --
 
-template <int BN, int CG, int EB, int KD>
+template <int BN, int CG, int EB, int KD, bool DQ>
 __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CUtensorMap* map_q,
-                                              const TcArgs& a, uint8_t* ring_a, uint8_t* ring_b,
-                                              TcCtrl* ctrl, uint32_t rank, int first, int stride) {
-  using Cfg = TcConfig<BN, CG>;
+                                              const CUtensorMap* map_sf, const TcArgs& a, uint8_t* ring_a,
+                                              uint8_t* ring_b, uint8_t* code_ring, TcCtrl* ctrl, uint32_t rank,
+                                              int first, int stride) {
+  using Cfg = TcConfig<BN, CG, DQ>;
   const int q = static_cast<int>(rank);  // rank inside the CTA pair (0: the leader)
   constexpr int kSliceK = slice_k(EB);  // k elements of one 128-byte slice
   // 8- and 32-bit operands are always K-major (the planner admits no other layout)
@@ -903,6 +944,37 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
       }
     }
     for (int kb = w.kb0; kb < w.kb1; ++kb) {  // one stage: k-slices kb * kdepth .. + kdepth - 1
+      if constexpr (DQ) {
+        // The code ring, one k-slice a stage: Q's 16-bit tile (which the MMA
+        // reads in place), P's codes and a 16-byte box of their scale codes
+        // per row, all counted on code_full; the converter warps fill the ring
+        // with P's values.
+        if (!warp_wait(smem_u32(&ctrl->code_empty[stage]), phase ^ 1u, ctrl, a, kRoleProducer, kBarEmpty, true)) {
+          ok = false;
+          break;
+        }
+        ++nload;
+        if (a.drop_load != 0 && blockIdx.x == 0 && nload == a.drop_load) {
+          pending &= ~(1u << stage);  // test hook: this stage's barrier is never completed
+        } else {
+          const uint32_t cbar = smem_u32(&ctrl->code_full[stage]);
+          if (elect_one()) {
+            mbar_arrive_expect_tx(cbar, Cfg::kBBytes + kBM * a.code_bytes + kBM * 16);
+            const uint32_t cs = smem_u32(code_ring + stage * a.code_stage_bytes);
+            tma_load_3d(cs, map_q, cbar, kb * slice_k(EB), j0, zq);
+            tma_load_3d(cs + Cfg::kBBytes, map_p, cbar, kb * a.code_bytes, i0, 0);
+            tma_load_3d(cs + Cfg::kBBytes + kBM * a.code_bytes, map_sf, cbar, (kb * a.spk) & ~15, i0, 0);
+          }
+          __syncwarp();
+          pending |= 1u << stage;
+          pending_parity = (pending_parity & ~(1u << stage)) | (phase << stage);
+        }
+        if (++stage == a.code_stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        continue;
+      }
       if (!warp_wait(smem_u32(&ctrl->empty[stage]), phase ^ 1u, ctrl, a, kRoleProducer, kBarEmpty,
                      true)) {
         ok = false;
@@ -976,19 +1048,125 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
   // barrier counts both CTAs' bytes, so the leader's wait covers the pair; a
   // peer CTA is held at the final cluster barrier until the leader has waited.
   if (q == 0 && (threadIdx.x & 31) == 0) {
-    for (int s = 0; s < Cfg::kStages; ++s)
+    const int nstages = DQ ? a.code_stages : Cfg::kStages;
+    for (int s = 0; s < nstages; ++s)
       if (pending & (1u << s))
-        wait_bounded(smem_u32(&ctrl->full[s]), (pending_parity >> s) & 1u, ctrl, a, kRoleProducer,
-                     kBarDrain, false);
+        wait_bounded(smem_u32(DQ ? &ctrl->code_full[s] : &ctrl->full[s]), (pending_parity >> s) & 1u, ctrl, a,
+                     kRoleProducer, kBarDrain, false);
   }
   __syncwarp();
 }
 
-template <int BN, int CG, int EB, int KD>
-__device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8_t* ring_b,
+// DQ kernels: four converter warps turn P's block-scaled codes into the 16-bit
+// values the MMA reads, stage by stage (the producer's order: the same work
+// units and k-blocks, one k-slice a stage).  Warp cw converts rows 32 cw ..
+// 32 cw + 31 of the 128-row P tile, one row per thread, into the ring's
+// 128-byte-swizzled K-major layout (16-byte piece p of row r at p ^ (r & 7)),
+// then completes the stage's full barrier with one arrival per warp.
+//  * E2M1 codes (two a byte, the even k in the low four bits) with unsigned
+//    E4M3 scales per 16 values -> fp16: code and scale as fp16, one fp16
+//    product, exact (at most 6 significant bits, inside fp16's range).
+//  * E4M3 / E5M2 codes with E8M0 scales (2^(s - 127)) per 32 values -> bf16:
+//    code as fp16, then fp32 times the scale, rounded to bf16 (exact inside
+//    bf16's range; the dequantising copy kernel rounds the same way).
+// Products past K, or past P's rows, come from zero codes the copy engine
+// filled in, so they are 0.
+template <int BN, int CG>
+__device__ __forceinline__ void converter_role(const TcArgs& a, uint8_t* ring_a, uint8_t* code_ring, TcCtrl* ctrl,
+                                               int cw, int lane, int first, int stride) {
+  using Cfg = TcConfig<BN, CG, true>;
+  const int r = cw * 32 + lane;
+  const uint32_t sw = static_cast<uint32_t>(r & 7);
+  int stage = 0, cstage = 0;  // the P ring and the code ring
+  uint32_t phase = 0, cphase = 0;
+  bool ok = true;
+  WorkIter work(a.sched, first, stride);
+  Unit w;
+  while (ok && work.next(w)) {
+    for (int kb = w.kb0; kb < w.kb1; ++kb) {
+      if (!warp_wait(smem_u32(&ctrl->code_full[cstage]), cphase, ctrl, a, kRoleConvert, kBarCodeFull, true) ||
+          !warp_wait(smem_u32(&ctrl->empty[stage]), phase ^ 1u, ctrl, a, kRoleConvert, kBarEmpty, true)) {
+        ok = false;
+        break;
+      }
+      const uint8_t* cst = code_ring + cstage * a.code_stage_bytes + Cfg::kBBytes;  // past the Q tile
+      const uint32_t codes = smem_u32(cst) + static_cast<uint32_t>(r * a.code_bytes);
+      const uint32_t scales =
+          smem_u32(cst + kBM * a.code_bytes) + static_cast<uint32_t>(r * 16 + ((kb * a.spk) & 15));
+      const uint32_t dst = smem_u32(ring_a + stage * Cfg::kABytes) + static_cast<uint32_t>(r * 128);
+      if (a.dq_fmt == 1) {
+        uint32_t wd[8];
+        {
+          const float4 c0 = ld_shared_v4_f32(codes), c1 = ld_shared_v4_f32(codes + 16);
+          wd[0] = __float_as_uint(c0.x); wd[1] = __float_as_uint(c0.y); wd[2] = __float_as_uint(c0.z);
+          wd[3] = __float_as_uint(c0.w); wd[4] = __float_as_uint(c1.x); wd[5] = __float_as_uint(c1.y);
+          wd[6] = __float_as_uint(c1.z); wd[7] = __float_as_uint(c1.w);
+        }
+        // the four unsigned E4M3 scales as fp16 pairs (sign bits cleared)
+        const uint32_t sc = ld_shared_u32(scales) & 0x7F7F7F7Fu;
+        const uint32_t s01 = e4m3x2_to_f16x2(sc & 0xFFFFu), s23 = e4m3x2_to_f16x2(sc >> 16);
+        const uint32_t sf[4] = {__byte_perm(s01, 0, 0x1010), __byte_perm(s01, 0, 0x3232), __byte_perm(s23, 0, 0x1010),
+                                __byte_perm(s23, 0, 0x3232)};
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {  // values 8p .. 8p + 7, scale p / 2
+          const __half2 s2 = *reinterpret_cast<const __half2*>(&sf[p >> 1]);
+          uint32_t o[4];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const uint32_t hv = e2m1x2_to_f16x2((wd[p] >> (8 * b)) & 0xFFu);
+            const __half2 prod = __hmul2(*reinterpret_cast<const __half2*>(&hv), s2);
+            o[b] = *reinterpret_cast<const uint32_t*>(&prod);
+          }
+          st_shared_v4(dst + ((static_cast<uint32_t>(p) ^ sw) << 4), o[0], o[1], o[2], o[3]);
+        }
+      } else {
+        const bool e5m2 = a.dq_fmt == 3;
+        const uint32_t sc = ld_shared_u16(scales);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // 32 values under one scale
+          const uint32_t s = (sc >> (8 * h)) & 0xFFu;
+          const float f = s == 255u ? __int_as_float(0x7FC00000)
+                                    : s == 0u ? __int_as_float(0x00400000) : __int_as_float(static_cast<int>(s << 23));
+          const float4 c0 = ld_shared_v4_f32(codes + 32 * h), c1 = ld_shared_v4_f32(codes + 32 * h + 16);
+          const uint32_t wd[8] = {__float_as_uint(c0.x), __float_as_uint(c0.y), __float_as_uint(c0.z),
+                                  __float_as_uint(c0.w), __float_as_uint(c1.x), __float_as_uint(c1.y),
+                                  __float_as_uint(c1.z), __float_as_uint(c1.w)};
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {  // piece 4h + p: words 2p, 2p + 1
+            uint32_t o[4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              const uint32_t pair = (wd[2 * p + (b >> 1)] >> (16 * (b & 1))) & 0xFFFFu;
+              const uint32_t hv = e5m2 ? e5m2x2_to_f16x2(pair) : e4m3x2_to_f16x2(pair);
+              const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&hv));
+              const __nv_bfloat162 y = __floats2bfloat162_rn(x.x * f, x.y * f);
+              o[b] = *reinterpret_cast<const uint32_t*>(&y);
+            }
+            st_shared_v4(dst + ((static_cast<uint32_t>(4 * h + p) ^ sw) << 4), o[0], o[1], o[2], o[3]);
+          }
+        }
+      }
+      fence_proxy_async_smem();  // the MMA reads these values through the async proxy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctrl->full[stage]));
+      if (++stage == a.stages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      if (++cstage == a.code_stages) {
+        cstage = 0;
+        cphase ^= 1u;
+      }
+    }
+  }
+}
+
+template <int BN, int CG, int EB, int KD, bool DQ>
+__device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8_t* ring_b, uint8_t* code_ring,
                                          TcCtrl* ctrl, uint32_t tmem_base, uint32_t rank, int first,
                                          int stride) {
-  using Cfg = TcConfig<BN, CG>;
+  using Cfg = TcConfig<BN, CG, DQ>;
+  int cstage = 0;  // DQ: the code ring stage holding the k-slice's Q tile
   constexpr int kSliceK = slice_k(EB);  // k elements of one 128-byte slice
   // 8- and 32-bit operands are always K-major (the planner admits no other layout)
   const bool p_kmajor = EB != 2 || a.p_kmajor != 0;
@@ -1038,19 +1216,23 @@ __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8
           const int slot = stage * KD + t;
           const uint64_t ad0 =
               smem_desc_sw128(smem_u32(ring_a + slot * Cfg::kABytes), p_kmajor ? 16u : kMnAtomBytes, 1024);
-          const uint64_t bd0 =
-              smem_desc_sw128(smem_u32(ring_b + slot * Cfg::kBBytes), q_kmajor ? 16u : kMnAtomBytes, 1024);
+          const uint8_t* qtile = DQ ? code_ring + cstage * a.code_stage_bytes : ring_b + slot * Cfg::kBBytes;
+          const uint64_t bd0 = smem_desc_sw128(smem_u32(qtile), q_kmajor ? 16u : kMnAtomBytes, 1024);
 #pragma unroll
           for (int k = 0; k < kSliceBytes / 32; ++k)  // the start address sits in the descriptor's low bits
             mma_ss<CG, EB>(d_tmem, ad0 + ((a_step * k) >> 4), bd0 + ((b_step * k) >> 4), a.idesc,
                            (kb > w.kb0 || t > 0 || k > 0) ? 1u : 0u);
         }
         commit_both(smem_u32(&ctrl->empty[stage]));  // frees the stage once these MMAs have read it
+        if constexpr (DQ) mma_commit<1>(smem_u32(&ctrl->code_empty[cstage]));  // and the code stage's Q tile
       }
       __syncwarp();
       if (++stage == a.stages) {
         stage = 0;
         phase ^= 1u;
+      }
+      if constexpr (DQ) {
+        if (++cstage == a.code_stages) cstage = 0;
       }
     }
     if (!ok) break;
@@ -1066,13 +1248,13 @@ __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8
   __syncwarp();
 }
 
-template <int BN, int CG, int EB>
+template <int BN, int CG, int EB, bool DQ>
 __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap* map_c, const CMaps* cmaps,
                                               uint8_t* staging, uint8_t* ring, TcCtrl* ctrl,
                                               uint32_t tmem_base,
                                               int warp, int lane, uint32_t rank, int first,
                                               int stride) {
-  using Cfg = TcConfig<BN, CG>;
+  using Cfg = TcConfig<BN, CG, DQ>;
   const int q = static_cast<int>(rank);  // rank inside the CTA pair (0: the leader)
   const int quarter = warp & 3;  // a warp may only read TMEM lanes 32*(warp%4) .. +31
   const int row = quarter * 32 + lane;
@@ -1117,7 +1299,8 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
                                  kRoleEpilogue, kBarAccFull, true);
     if (bar_any(1, 128, !ok)) break;  // all four epilogue warps leave together
     tc_fence_after_sync();
-    if ((out.c.tma == kBulkRows || out.c.tma == kBulkTransposed) && !out.ring && !out.c.blend_load) {
+    if (Cfg::kRingStagesC && (out.c.tma == kBulkRows || out.c.tma == kBulkTransposed) && !out.ring &&
+        !out.c.blend_load) {
       WorkIter peek = work;
       Unit next_unit;
       // This CTA's last unit: its copies have landed and its MMAs (the pair's)
@@ -1263,13 +1446,13 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
   out.finish();  // every bulk store has read its staging buffer before the CTA can exit
 }
 
-template <int BN, int CG, int EB>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, int CG, int EB, bool DQ>
+__global__ void __launch_bounds__(threads_of(DQ), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p,
                    const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_c, const __grid_constant__ CMaps cmaps,
                    const TcArgs args) {
-  using Cfg = TcConfig<BN, CG>;
+  using Cfg = TcConfig<BN, CG, DQ>;
   // The roles take the arguments by reference; a local copy whose address never
   // leaves this kernel lets the compiler keep the fields in registers across
   // the global stores and "memory"-clobbering asm of the loops, instead of
@@ -1284,8 +1467,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   uint8_t* ring_a = smem;
   uint8_t* ring_b = smem + Cfg::kStages * Cfg::kABytes;
-  TcCtrl* ctrl = reinterpret_cast<TcCtrl*>(smem + Cfg::kRingBytes);
-  uint8_t* staging = smem + Cfg::kRingBytes + 1024;  // 1024-byte aligned
+  uint8_t* code_ring = smem + Cfg::kRingBytes;  // (DQ kernels)
+  TcCtrl* ctrl = reinterpret_cast<TcCtrl*>(smem + Cfg::kRingBytes + Cfg::kCodeRingBytes);
+  uint8_t* staging = smem + Cfg::kRingBytes + Cfg::kCodeRingBytes + 1024;  // 1024-byte aligned
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -1298,9 +1482,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::kStages; ++s) {
-      mbar_init(smem_u32(&ctrl->full[s]), 1);
+      mbar_init(smem_u32(&ctrl->full[s]), DQ ? 4 : 1);  // (DQ: one arrival per converter warp)
       mbar_init(smem_u32(&ctrl->empty[s]), 1);  // released by the pair's MMA commit
     }
+    if (DQ)
+      for (int s = 0; s < a.code_stages; ++s) {
+        mbar_init(smem_u32(&ctrl->code_full[s]), 1);
+        mbar_init(smem_u32(&ctrl->code_empty[s]), 1);
+      }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctrl->acc_full[b]), 1);
       mbar_init(smem_u32(&ctrl->acc_empty[b]), 128 * CG);
@@ -1315,6 +1504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&map_p);
     prefetch_tensormap(&map_q);
+    if (DQ) prefetch_tensormap(&cmaps.m[0]);
   }
   if (warp == 1) {
     tmem_alloc<CG>(smem_u32(&ctrl->tmem_base), Cfg::kTmemCols);
@@ -1334,20 +1524,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     // k-slices per stage are a template argument of the issuing roles, so that
     // the one-slice loop compiles to the same straight-line issue code as
     // before two-slice stages existed (a runtime trip count cost ~12% at 4096^3)
-    if (a.kdepth == 2)
-      producer_role<BN, CG, EB, 2>(&map_p, &map_q, a, ring_a, ring_b, ctrl, rank, first, stride);
+    // (DQ kernels: one k-slice a stage, the planner's choice)
+    if (!DQ && a.kdepth == 2)
+      producer_role<BN, CG, EB, 2, DQ>(&map_p, &map_q, &cmaps.m[0], a, ring_a, ring_b, code_ring, ctrl, rank, first,
+                                       stride);
     else
-      producer_role<BN, CG, EB, 1>(&map_p, &map_q, a, ring_a, ring_b, ctrl, rank, first, stride);
+      producer_role<BN, CG, EB, 1, DQ>(&map_p, &map_q, &cmaps.m[0], a, ring_a, ring_b, code_ring, ctrl, rank, first,
+                                       stride);
   } else if (warp == 1) {
     if (rank % CG == 0) {
-      if (a.kdepth == 2)
-        mma_role<BN, CG, EB, 2>(a, ring_a, ring_b, ctrl, tmem_base, rank, first, stride);
+      if (!DQ && a.kdepth == 2)
+        mma_role<BN, CG, EB, 2, DQ>(a, ring_a, ring_b, code_ring, ctrl, tmem_base, rank, first, stride);
       else
-        mma_role<BN, CG, EB, 1>(a, ring_a, ring_b, ctrl, tmem_base, rank, first, stride);
+        mma_role<BN, CG, EB, 1, DQ>(a, ring_a, ring_b, code_ring, ctrl, tmem_base, rank, first, stride);
     }
-  } else {
-    epilogue_role<BN, CG, EB>(a, &map_c, &cmaps, staging, ring_a, ctrl, tmem_base, warp, lane, rank, first,
-                              stride);
+  } else if (warp < 6) {
+    epilogue_role<BN, CG, EB, DQ>(a, &map_c, &cmaps, staging, ring_a, ctrl, tmem_base, warp, lane, rank, first,
+                                  stride);
+  } else if constexpr (DQ) {
+    converter_role<BN, CG>(a, ring_a, code_ring, ctrl, warp - 6, lane, first, stride);
   }
 
   tc_fence_before_sync();

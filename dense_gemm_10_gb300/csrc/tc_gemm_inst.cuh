@@ -1,16 +1,20 @@
 // tc_gemm_inst.cuh -- one instantiation of the tcgen05 GEMM kernel per
-// translation unit (TC_BN, TC_CG and TC_EB set by the including file), so the
-// tile configurations compile in parallel.
+// translation unit (TC_BN, TC_CG, TC_EB and, for kernels that convert
+// block-scaled codes, TC_DQ set by the including file), so the tile
+// configurations compile in parallel.
 #include "tc_gemm.cuh"
 
-#define TC_CAT6(a, b, c, d, e, f) a##b##c##d##e##f
-#define TC_NAME(a, b, c, d, e, f) TC_CAT6(a, b, c, d, e, f)
-#define TC_KERNEL tc_gemm_kernel<TC_BN, TC_CG, TC_EB>
+#ifndef TC_DQ
+#define TC_DQ 0
+#endif
+#define TC_CAT8(a, b, c, d, e, f, g, h) a##b##c##d##e##f##g##h
+#define TC_NAME(a, b, c, d, e, f, g, h) TC_CAT8(a, b, c, d, e, f, g, h)
+#define TC_KERNEL tc_gemm_kernel<TC_BN, TC_CG, TC_EB, TC_DQ != 0>
 
 namespace g10 {
 
-cudaError_t TC_NAME(tc_prepare_bn, TC_BN, _cg, TC_CG, _eb, TC_EB)(int* max_clusters) {
-  using Cfg = TcConfig<TC_BN, TC_CG>;
+cudaError_t TC_NAME(tc_prepare_bn, TC_BN, _cg, TC_CG, _eb, TC_EB, _dq, TC_DQ)(int* max_clusters) {
+  using Cfg = TcConfig<TC_BN, TC_CG, TC_DQ != 0>;
   cudaError_t e = cudaFuncSetAttribute(TC_KERNEL,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(Cfg::kSmemBytes));
@@ -23,17 +27,17 @@ cudaError_t TC_NAME(tc_prepare_bn, TC_BN, _cg, TC_CG, _eb, TC_EB)(int* max_clust
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(TC_CG, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(threads_of(TC_DQ != 0), 1, 1);
   cfg.dynamicSmemBytes = Cfg::kSmemBytes;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaOccupancyMaxActiveClusters(max_clusters, TC_KERNEL, &cfg);
 }
 
-cudaError_t TC_NAME(tc_launch_bn, TC_BN, _cg, TC_CG, _eb, TC_EB)(
+cudaError_t TC_NAME(tc_launch_bn, TC_BN, _cg, TC_CG, _eb, TC_EB, _dq, TC_DQ)(
     const CUtensorMap& map_p, const CUtensorMap& map_q, const CUtensorMap& map_c, const CMaps& cmaps,
     const TcArgs& args, int grid, cudaStream_t stream) {
-  using Cfg = TcConfig<TC_BN, TC_CG>;
+  using Cfg = TcConfig<TC_BN, TC_CG, TC_DQ != 0>;
   const size_t smem = Cfg::kSmemBytes;  // every epilogue stages C (bulk or direct stores)
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
@@ -51,7 +55,7 @@ cudaError_t TC_NAME(tc_launch_bn, TC_BN, _cg, TC_CG, _eb, TC_EB)(
     ++n;
   }
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(threads_of(TC_DQ != 0), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;

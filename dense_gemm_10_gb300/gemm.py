@@ -43,6 +43,7 @@ OPT_EPILOGUE = 10
 OPT_KDEPTH = 11
 OPT_PDL = 12
 OPT_PLAN_CACHE = 13
+OPT_DEQUANT_IN_KERNEL = 15
 BULK_NONE, BULK_ROWS, BULK_TRANSPOSED, BULK_STAGED, BULK_ROW_COPIES, BULK_ROW_CLASSES = 0, 1, 2, 3, 4, 5  # bulk_store
 SCHED_TILES, SCHED_STREAM_K = 0, 1
 

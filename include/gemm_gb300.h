@@ -382,6 +382,14 @@ gemm_status_t gemm_plan_grouped(gemm_handle_t h, int sm_count, gemm_op_t transB,
  * every value inside bf16's exponent range is held exactly; values below
  * 2^-133 flush), then the bf16 tensor-core GEMM computes the product, so the
  * result is the block-scaled product with fp32 accumulation at bf16 speed.
+ * With M <= 64 < N (a decode-batch GEMM against a weight matrix, bound by
+ * reading B), B instead stays in its codes: only A goes through the pass, and
+ * four more warps of the GEMM convert B's codes and scales into the tensor
+ * core's operand tiles as they arrive (NVFP4 as fp16, exact; MXFP8 as bf16),
+ * so B's bytes are read once, at their code size.  This needs B and SFB
+ * 16-byte aligned with rows of a multiple of 16 bytes (ldb / 2 bytes for
+ * NVFP4, ldb for MXFP8; ld_sfb); otherwise, or with the option
+ * GEMM_OPT_DEQUANT_IN_KERNEL = 1, both operands take the pass.
  * (The tensor core's own block-scaled kinds are not used.)
  * Returns GEMM_ERR_INVALID_ARG for a non-block-scaled dtype, null scales,
  * scale pitches below ceil(K / block), odd NVFP4 pitches, or the argument
@@ -453,11 +461,15 @@ typedef enum {
                                   dependent of the stream's previous kernel, so its launch and
                                   set-up overlap that kernel's end; it reads and writes memory only
                                   after the previous kernel has finished.  0: ordinary launch */
-  GEMM_OPT_PLAN_CACHE = 13     /* 1 (default): plain and strided-batched calls reuse the plan of
+  GEMM_OPT_PLAN_CACHE = 13,    /* 1 (default): plain and strided-batched calls reuse the plan of
                                   an earlier call with the same sizes, leading dimensions,
                                   strides, dtype, beta, options and pointer alignments (32
                                   plans per handle, least recently used replaced); 0: plan
                                   every call */
+  GEMM_OPT_DEQUANT_IN_KERNEL = 15 /* block-scaled GEMMs with M <= 64 < N: 0 (default) the weights
+                                  B stay in their codes and the GEMM converts them as they
+                                  arrive (see gemm_run_block_scaled); 1: a pass writes both
+                                  operands as 16-bit values first */
 } gemm_option_t;
 
 /* Set an option on a handle.  Errors: GEMM_ERR_INVALID_ARG for an unknown

@@ -224,8 +224,18 @@ def test_plan_block_scaled():
     p = G.plan_block_scaled(4096, 4096, 4096, G.mxfp8_dtype())
     assert p.repack_a == 1 and p.repack_b == 1 and p.launches == 3 and p.bk == 64 and p.bn == 256
     assert p.workspace_bytes >= 2 * 4096 * 4096 * 2
+    # M <= 64: the weights B stay in their codes and the GEMM converts them (the
+    # pass only for A); misaligned code or scale rows keep the pass for both
     q = G.plan_block_scaled(64, 32000, 4096, G.NVFP4_BF16)
-    assert q.swap_ab == 1 and q.launches == 3
+    assert q.swap_ab == 1 and q.launches == 2 and q.repack_b == 0 and q.repack_a == 1
+    assert q.bn == 64 and q.bm == 128 and q.kdepth == 1 and q.path == G.PATH_TC_1CTA
+    assert q.workspace_bytes < 32000 * 4096                       # no 16-bit copy of B (2 x 131 MB)
+    assert G.plan_block_scaled(64, 32000, 4096, G.mxfp8_dtype()).launches == 2
+    assert G.plan_block_scaled(64, 32000, 4096, G.NVFP4_BF16, ldb=4128).launches == 2    # 2064-byte code rows
+    assert G.plan_block_scaled(64, 32000, 4096, G.NVFP4_BF16, ldb=4104).launches == 3   # 2052-byte code rows
+    assert G.plan_block_scaled(64, 32000, 4096, G.NVFP4_BF16, ld_sfb=264).launches == 3  # scale rows
+    assert G.plan_block_scaled(64, 32000, 4096, G.NVFP4_BF16, SFB=0x1008).launches == 3
+    assert G.plan_block_scaled(64, 32000, 4096, G.mxfp8_dtype(), ldb=4100).launches == 3
     r = G.plan_block_scaled(300, 264, 37, G.NVFP4_F32, lda=38, ldb=38)
     assert r.workspace_bytes >= (300 + 264) * 48 * 2          # 37 values padded to 48 bf16
     for kw in (dict(ld_sfa=1), dict(lda=39)):                  # scale rows too short; odd FP4 pitch

@@ -148,3 +148,78 @@ def test_bad_arguments(h):
                                   16, 0.0, C.data_ptr(), 64, G.mxfp8_dtype(), None) == G.ERR_INVALID_ARG
     assert h.run_block_scaled_raw(64, 64, 64, 1.0, A.data_ptr(), 65, A.data_ptr(), 16, A.data_ptr(), 64,
                                   A.data_ptr(), 16, 0.0, C.data_ptr(), 64, G.NVFP4_F32, None) == G.ERR_INVALID_ARG
+
+
+# ---------------------------------------------------- codes converted in the GEMM --
+
+def _dq_plan(p, h):
+    return G.plan_block_scaled(p.M, p.N, p.K, code_of(p), lda=p.lda, ldb=p.ldb, ld_sfa=p.ld_sfa, ld_sfb=p.ld_sfb,
+                               ldc=p.ldc + 2, handle=h)
+
+
+@pytest.mark.parametrize("fmt,a,b", PAIRS)
+@pytest.mark.parametrize("M,N,K", [(40, 1000, 200), (1, 257, 64), (64, 520, 1000)])
+def test_dq_kernel_formats(h, fmt, a, b, M, N, K):
+    """M <= 64: the weights B stay in their codes and the GEMM's converter warps
+    write their 16-bit values into the ring (A alone goes through the pass).
+    Ragged N, K with partial k-slices and blocks; the same result as the pass
+    for both operands (GEMM_OPT_DEQUANT_IN_KERNEL = 1), within the tolerance."""
+    p = inputs.make_block_scaled_problem("bs_dq_%s_%s_%s" % (fmt, a, b), M, N, K, fmt, "f32", a, b, alpha=0.5,
+                                         seed=M + N + K + len(a) + 3 * len(b))
+    plan = _dq_plan(p, h)
+    assert plan.swap_ab == 1 and plan.launches == 2 and plan.repack_b == 0, plan.as_dict()
+    R, Mag = reference(p)
+    out = run(p, h)
+    assert_close(out, R, Mag, True, p.name)
+    h.set_option(G.OPT_DEQUANT_IN_KERNEL, 1)
+    try:
+        assert _dq_plan(p, h).launches == 3
+        assert_close(run(p, h), R, Mag, True, p.name + " (pass)")
+    finally:
+        h.set_option(G.OPT_DEQUANT_IN_KERNEL, 0)
+
+
+def test_dq_kernel_fp4_odd_k(h):
+    """K = 37 on the converting path: the last code byte of each weight row holds
+    one value, its high four bits set to -6 here; the product past K is zero
+    because A's 16-bit copy is zero there."""
+    p = inputs.make_block_scaled_problem("bs_dq_odd", 40, 300, 37, "nvfp4", seed=18, lda=64, ldb=64)
+    for X in (p.A, p.B):
+        X[:, 18] |= 0xF0
+    assert _dq_plan(p, h).launches == 2
+    R, Mag = reference(p)
+    assert_close(run(p, h), R, Mag, True, p.name)
+
+
+@pytest.mark.parametrize("fmt,out", [("nvfp4", "bf16"), ("mxfp8", "f32")])
+def test_dq_kernel_lm_head_full(h, fmt, out):
+    """The LM head, 64 x 32000 x 4096, every element against the oracle
+    (stream-K over all SMs, transposed bulk stores of C)."""
+    p = inputs.make_block_scaled_problem("bs_dq_lmhead", 64, 32000, 4096, fmt, out, seed=19, alpha=1.0 / 64)
+    plan = _dq_plan(p, h)
+    assert plan.launches == 2 and plan.schedule == G.SCHED_STREAM_K
+    R, Mag = reference(p)
+    assert_close(run(p, h), R, Mag, out == "f32", p.name)
+
+
+def test_dq_kernel_timeout_then_clean(h):
+    """A dropped load on the converting path: the converter warps' and the MMA's
+    bounded waits run out, the status reports a timeout, and the next call on
+    the same handle is correct."""
+    p = inputs.make_block_scaled_problem("bs_dq_drop", 40, 1000, 512, "nvfp4", "f32", seed=20)
+    assert _dq_plan(p, h).launches == 2
+    Cd = torch.zeros(p.M, p.ldc, device="cuda")
+    A, B, SA, SB = p.A.cuda(), p.B.cuda(), p.SFA.cuda(), p.SFB.cuda()
+    h.set_option(G.OPT_WAIT_LIMIT_NS, 50_000_000)
+    h.set_option(G.OPT_TEST_DROP_LOAD, 3)
+    try:
+        st = h.run_block_scaled_raw(p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, SA.data_ptr(), p.ld_sfa, B.data_ptr(),
+                                    p.ldb, SB.data_ptr(), p.ld_sfb, 0.0, Cd.data_ptr(), p.ldc, code_of(p), None)
+        assert st == G.OK
+        st, word = h.status()
+        assert st == G.ERR_TIMEOUT and word & 0xFF == 6
+    finally:
+        h.set_option(G.OPT_TEST_DROP_LOAD, 0)
+        h.set_option(G.OPT_WAIT_LIMIT_NS, 2_000_000_000)
+    R, Mag = reference(p)
+    assert_close(run(p, h), R, Mag, True, p.name)
