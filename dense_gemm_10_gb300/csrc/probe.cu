@@ -36,7 +36,11 @@ __global__ void __launch_bounds__(128) tma_tile_probe_kernel(const __grid_consta
     while (!done && global_timer_ns() - t0 <= wait_limit_ns) done = mbar_try_wait(b, 0);
     if (!done) {
       atomicCAS(status, 0, kStatusTimeout);
-      // the copy may still land: wait once more (bounded) before the CTA may exit
+      // The copy may still land: wait once more (bounded) before the CTA may
+      // exit.  If that wait runs out too, the copy can land after the CTA has
+      // left, in shared memory it no longer owns; so a timed-out probe ends its
+      // caller's use of probes: the caller reads the status (a stream
+      // synchronise) and launches no further probe in the process.
       const uint64_t t1 = global_timer_ns();
       while (!mbar_try_wait(b, 0) && global_timer_ns() - t1 <= wait_limit_ns) {
       }

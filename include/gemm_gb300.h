@@ -507,7 +507,9 @@ gemm_status_t gemm_tensor_map_cache_stats(gemm_handle_t h, uint64_t* hits, uint6
  * Asynchronous on `stream`.  GEMM_ERR_INVALID_ARG for a bad argument (checked
  * before any CUDA call), GEMM_ERR_TENSORMAP if the tile cannot be described,
  * GEMM_ERR_CUDA on a launch failure; a copy that never lands is reported by
- * gemm_get_status as GEMM_ERR_TIMEOUT.
+ * gemm_get_status as GEMM_ERR_TIMEOUT.  After that report the caller launches
+ * no further probe in the process: the timed-out copy may still land in the
+ * shared memory of an exited block.
  */
 gemm_status_t gemm_probe_tma_tile(gemm_handle_t h, const void* src, int64_t ld, int64_t cols, int64_t rows, void* dst,
                                   void* stream);
