@@ -25,7 +25,7 @@ SOURCES = ["gemm_api.cu", "tc_dispatch.cu", "aux_kernels.cu", "probe.cu",
            "tc_gemm_bn128_cg2.cu", "tc_gemm_bn256_cg2.cu",
            "tc_gemm_bn64_cg1_f8.cu", "tc_gemm_bn128_cg1_f8.cu", "tc_gemm_bn128_cg2_f8.cu", "tc_gemm_bn256_cg2_f8.cu",
            "tc_gemm_bn64_cg1_tf32.cu", "tc_gemm_bn128_cg1_tf32.cu", "tc_gemm_bn256_cg2_tf32.cu",
-           "tc_gemm_bn64_cg1_dq.cu"]
+           "tc_gemm_bn64_cg1_dq.cu", "tc_gemm_bn256_cg2_ew8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-I" + os.path.join(ROOT, "include")]

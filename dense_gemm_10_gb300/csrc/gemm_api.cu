@@ -48,6 +48,7 @@ struct Options {
   int plan_cache = 1;  // GEMM_OPT_PLAN_CACHE: reuse the plans of recent calls
   bool stage_c = true; // C that bulk stores cannot write may go through an aligned copy
   int dq_kernel = 0;   // GEMM_OPT_DEQUANT_IN_KERNEL: 0 auto, 1 never (the dequantising pass for both operands)
+  int epi_warps = 0;   // GEMM_OPT_EPILOGUE_WARPS: 0 auto, else 4 or 8 where the tile has both kernels
 };
 
 // One stored operand, as the tensor-memory-accelerator copy engine will see it.
@@ -519,10 +520,13 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
 
   // Tile configuration and schedule: the configuration with the lowest
   // estimated time, est_time() below.
-  static const int kPreference[kNumTileConfigs] = {4, 3, 2, 1, 5, 0, 9, 8, 7, 6, 12, 11, 10, 13};  // ties go first
+  // (ties go first; the eight-epilogue-warp kernel of a tile is chosen below,
+  // once the store path is known)
+  static const int kPreference[kNumTileConfigs] = {4, 3, 2, 1, 5, 0, 9, 8, 7, 6, 12, 11, 10, 13, 14};
   Choice best;
   for (int cfg : kPreference) {
     const TileConfig& c = kTileConfigs[cfg];
+    if (c.ew != 4) continue;
     if (c.eb != dt.eb) continue;
     if ((c.dq != 0) != dq_kernel) continue;
     const int path = c.cg == 2 ? GEMM_PATH_TC_2CTA : GEMM_PATH_TC_1CTA;
@@ -671,6 +675,30 @@ gemm_status_t make_plan(const Options& o, const SlotTable& slots, gemm_op_t tran
     P.vector_store = 1;
     P.launches += 1;
   }
+  // Eight epilogue warps (two per tensor-memory lane quarter, each storing half
+  // of a tile's columns) where C leaves through direct stores, row classes or
+  // per-row copies: there a block's own work (shifting rows across pieces,
+  // plain stores at the edges) outweighs the tensor-memory reads, and two warps
+  // a quarter share it (4095 x 4097 x 1000 fp32 with ldc = 4097: 69.8 -> 57.9
+  // us; ldc = 4100: 56.0 -> 47.8 us).  With bulk tensor stores the tensor-memory
+  // reads and shared-memory writes bound the epilogue and the smaller ring of
+  // the wider kernel costs more than the warps gain (4096^3 88.3 -> 92.7 us), so
+  // the four-warp kernel stays.
+  const bool wide_epilogue = pl.tma_store == kBulkNone || pl.tma_store == kBulkRowCopies;
+  if (o.epi_warps == 8 || (o.epi_warps == 0 && wide_epilogue)) {
+    const TileConfig& c = kTileConfigs[pl.cfg];
+    for (int i = 0; i < kNumTileConfigs; ++i) {
+      const TileConfig& e = kTileConfigs[i];
+      if (e.ew == 8 && e.bn == c.bn && e.cg == c.cg && e.eb == c.eb && e.dq == c.dq &&
+          slots.of(i) >= slots.of(pl.cfg) && tc_stages(i) / P.kdepth >= 2) {
+        pl.cfg = i;
+        P.stages = tc_stages(i) / P.kdepth;
+        if (o.stages > 0 && o.stages < P.stages) P.stages = o.stages;
+        break;
+      }
+    }
+  }
+  P.epilogue_warps = kTileConfigs[pl.cfg].ew;
   P.workspace_bytes = static_cast<int64_t>(ws);
   *out = pl;
   if (out->sched.groups > 0) out->sched.group_tile_start = out->group_tiles.data();  // the copy's own table
@@ -1014,6 +1042,10 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
     case GEMM_OPT_DEQUANT_IN_KERNEL:
       if (value < 0 || value > 1) return GEMM_ERR_INVALID_ARG;
       h->opt.dq_kernel = static_cast<int>(value);
+      return GEMM_OK;
+    case GEMM_OPT_EPILOGUE_WARPS:
+      if (value != 0 && value != 4 && value != 8) return GEMM_ERR_INVALID_ARG;
+      h->opt.epi_warps = static_cast<int>(value);
       return GEMM_OK;
   }
   return GEMM_ERR_INVALID_ARG;

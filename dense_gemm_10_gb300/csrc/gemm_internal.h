@@ -13,9 +13,11 @@ namespace g10 {
 constexpr int kBM = 128;          // MMA M (rows of the output tile held in TMEM lanes)
 constexpr int kSliceBytes = 128;  // a k-slice: one 128-byte swizzle row of every tile row
 constexpr int kBK = 64;           // k-slice of 16-bit elements (64 x 2 bytes)
-constexpr int kThreads = 192;     // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue
-constexpr int kThreadsDq = 320;   // the same, and warps 6-9 converting block-scaled codes (DQ kernels)
-__host__ __device__ constexpr int threads_of(bool dq) { return dq ? kThreadsDq : kThreads; }
+// Warps of a GEMM CTA: warp 0 TMA producer, warp 1 MMA issuer, then `ew`
+// epilogue warps (four, one per 32-lane quarter of tensor memory; or eight,
+// two per quarter, each of a pair storing half of the tile's columns), then in
+// DQ kernels four warps converting block-scaled codes.
+__host__ __device__ constexpr int threads_of(int ew, bool dq) { return 64 + 32 * (ew + (dq ? 4 : 0)); }
 
 // k elements of one k-slice for an element of eb bytes (2: bf16 / fp16, 1: FP8).
 __host__ __device__ constexpr int slice_k(int eb) { return kSliceBytes / eb; }
@@ -114,9 +116,10 @@ struct CMaps {
 // (kind::tf32).
 struct TileConfig {
   int bn, cg, eb;
-  int dq;  // 1: P arrives as block-scaled codes, converted in the kernel (kThreadsDq threads)
+  int dq;  // 1: P arrives as block-scaled codes, converted in the kernel (four more warps)
+  int ew;  // epilogue warps: 4, or 8 (two per tensor-memory lane quarter)
 };
-constexpr int kNumTileConfigs = 14;
+constexpr int kNumTileConfigs = 15;
 extern const TileConfig kTileConfigs[kNumTileConfigs];
 int tc_stages(int cfg);  // ring depth in k-slices
 int tc_code_ring_bytes(int cfg);  // DQ kernels: shared memory of the code ring (0 for the others)

@@ -45,7 +45,7 @@
 
 namespace g10 {
 
-template <int BN, int CG, bool DQ = false>
+template <int BN, int CG, bool DQ = false, int EW = 4>
 struct TcConfig {
   static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
   static_assert(CG == 1 || CG == 2, "CTA group");
@@ -61,7 +61,10 @@ struct TcConfig {
   // as many stages as fit in 227 KB beside the control block and alignment slack (at most 8)
   // epilogue staging: per epilogue warp two 32-row x 128-byte buffers for C (bulk stores
   // alternate between them; direct stores use the first)
-  static constexpr int kStagingBytes = 4 * 2 * 32 * 128;
+  static_assert(EW == 4 || (EW == 8 && !DQ && BN >= 128), "epilogue warps");
+  static constexpr int kEpiWarps = EW;
+  static constexpr int kEpiCols = BN / (kEpiWarps / 4);  // columns of a tile one epilogue warp stores
+  static constexpr int kStagingBytes = kEpiWarps * 2 * 32 * 128;
   static constexpr int kCtrlBytes = 256;
   static constexpr int kRingMax = 232448 - 1024 - kStagingBytes - 1024;  // 227 KB less the rest
   // DQ: the ring holds only P's converted 16-bit tiles (three stages); Q's
@@ -73,7 +76,10 @@ struct TcConfig {
   static constexpr int kRingBytes = DQ ? kStages * kABytes : kStages * kStageBytes;
   static constexpr int kCodeRingBytes = DQ ? kRingMax - kRingBytes : 0;
   static_assert(kCodeRingBytes % 1024 == 0, "code stages start on 1024-byte boundaries");
-  // the last tile's epilogue stages C in the idle ring: eight 4 KB buffers per epilogue warp
+  // the last tile's epilogue stages C in the idle ring: 32 KB per epilogue warp
+  // quarter (eight 4 KB buffers a warp, or four for each of two), one per
+  // 32-column block of the tile
+  static constexpr int kRingBufs = 32 / kEpiWarps;
   static constexpr bool kRingStagesC = kRingBytes >= 4 * 8 * 32 * 128;
   static_assert(DQ || kRingStagesC, "ring too small to stage a tile of C");
   static constexpr int kTmemCols = 2 * BN;       // two fp32 accumulators of BN columns
@@ -87,7 +93,7 @@ struct TcCtrl {
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t mma_done;
-  uint64_t c_full[4][2];  // per epilogue warp and staging buffer: a block of old C has landed
+  uint64_t c_full[8][2];  // per epilogue warp and staging buffer: a block of old C has landed
   uint64_t code_full[16];   // DQ: a code stage's Q tile, codes and scale codes have landed
   uint64_t code_empty[16];  // DQ: the MMA has read a code stage's Q tile (the converters its codes before)
   uint32_t tmem_base;
@@ -910,12 +916,12 @@ struct EpiOut {
 
 // ----------------------------------------------------------------- the roles --
 
-template <int BN, int CG, int EB, int KD, bool DQ>
+template <int BN, int CG, int EB, int KD, bool DQ, int EW>
 __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CUtensorMap* map_q,
                                               const CUtensorMap* map_sf, const TcArgs& a, uint8_t* ring_a,
                                               uint8_t* ring_b, uint8_t* code_ring, TcCtrl* ctrl, uint32_t rank,
                                               int first, int stride) {
-  using Cfg = TcConfig<BN, CG, DQ>;
+  using Cfg = TcConfig<BN, CG, DQ, EW>;
   const int q = static_cast<int>(rank);  // rank inside the CTA pair (0: the leader)
   constexpr int kSliceK = slice_k(EB);  // k elements of one 128-byte slice
   // 8- and 32-bit operands are always K-major (the planner admits no other layout)
@@ -1161,11 +1167,11 @@ __device__ __forceinline__ void converter_role(const TcArgs& a, uint8_t* ring_a,
   }
 }
 
-template <int BN, int CG, int EB, int KD, bool DQ>
+template <int BN, int CG, int EB, int KD, bool DQ, int EW>
 __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8_t* ring_b, uint8_t* code_ring,
                                          TcCtrl* ctrl, uint32_t tmem_base, uint32_t rank, int first,
                                          int stride) {
-  using Cfg = TcConfig<BN, CG, DQ>;
+  using Cfg = TcConfig<BN, CG, DQ, EW>;
   int cstage = 0;  // DQ: the code ring stage holding the k-slice's Q tile
   constexpr int kSliceK = slice_k(EB);  // k elements of one 128-byte slice
   // 8- and 32-bit operands are always K-major (the planner admits no other layout)
@@ -1248,16 +1254,22 @@ __device__ __forceinline__ void mma_role(const TcArgs& a, uint8_t* ring_a, uint8
   __syncwarp();
 }
 
-template <int BN, int CG, int EB, bool DQ>
+template <int BN, int CG, int EB, bool DQ, int EW>
 __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap* map_c, const CMaps* cmaps,
                                               uint8_t* staging, uint8_t* ring, TcCtrl* ctrl,
                                               uint32_t tmem_base,
                                               int warp, int lane, uint32_t rank, int first,
                                               int stride) {
-  using Cfg = TcConfig<BN, CG, DQ>;
+  using Cfg = TcConfig<BN, CG, DQ, EW>;
+  constexpr int kEpiThreads = 32 * Cfg::kEpiWarps;
   const int q = static_cast<int>(rank);  // rank inside the CTA pair (0: the leader)
+  const int ew = warp - 2;       // epilogue warp
   const int quarter = warp & 3;  // a warp may only read TMEM lanes 32*(warp%4) .. +31
   const int row = quarter * 32 + lane;
+  // the tile's columns cb .. cb + kEpiCols - 1 are this warp's (with eight
+  // epilogue warps, two to a quarter of the rows, each takes half)
+  const int cb = (ew / 4) * Cfg::kEpiCols;
+  constexpr int kCols = Cfg::kEpiCols;
   const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
   const float alpha = a.alpha;
   EpiOut out;
@@ -1265,11 +1277,11 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
   out.c0 = a.C;
   out.z = 0;
   out.map_c = map_c;
-  out.staging = smem_u32(staging + (warp - 2) * 2 * kStagingBuf);
+  out.staging = smem_u32(staging + ew * 2 * kStagingBuf);
   out.lane = lane;
   out.nstore = 0;
   out.ring = false;
-  out.cbar = smem_u32(&ctrl->c_full[warp - 2][0]);
+  out.cbar = smem_u32(&ctrl->c_full[ew][0]);
   out.cphase = 0;
   out.pending = 0;
   out.jstart = 0;
@@ -1294,10 +1306,10 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
     out.z = w.tb;
     // beta != 0 with bulk stores: the tile's first block of old C loads while
     // the accumulator is still being computed
-    if (!w.partial) out.begin_tile(jt, jt + BN);
+    if (!w.partial) out.begin_tile(jt + cb, jt + cb + kCols);
     const bool ok = wait_bounded(smem_u32(&ctrl->acc_full[buf]), acc_parity, ctrl, a,
                                  kRoleEpilogue, kBarAccFull, true);
-    if (bar_any(1, 128, !ok)) break;  // all four epilogue warps leave together
+    if (bar_any(1, kEpiThreads, !ok)) break;  // all epilogue warps leave together
     tc_fence_after_sync();
     if (Cfg::kRingStagesC && (out.c.tma == kBulkRows || out.c.tma == kBulkTransposed) && !out.ring &&
         !out.c.blend_load) {
@@ -1305,7 +1317,7 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
       Unit next_unit;
       // This CTA's last unit: its copies have landed and its MMAs (the pair's)
       // have read the ring for the last time, so the ring can stage C.
-      if (!peek.next(next_unit)) out.use_ring(smem_u32(ring + (warp - 2) * 8 * kStagingBuf));
+      if (!peek.next(next_unit)) out.use_ring(smem_u32(ring + ew * Cfg::kRingBufs * kStagingBuf));
     }
     const uint32_t taddr = lane_base + static_cast<uint32_t>(buf * BN);
     // the MMA (leader CTA) waits until every epilogue thread of the pair has read the buffer
@@ -1330,11 +1342,11 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
       // 8-bit inputs: one 32-column read at a time (reading ahead, below,
       // measured 2% slower on the 4096^3 E4M3 GEMM, whose tiles are half as long)
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
+      for (int c = cb; c < cb + kCols; c += 32) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(taddr + c, r);
         tmem_ld_wait(r);
-        if (c + 32 == BN) release();  // last read of this accumulator: hand it back
+        if (c + 32 == cb + kCols) release();  // last read of this accumulator: hand it back
         float v[32];
 #pragma unroll
         for (int t = 0; t < 32; ++t) v[t] = alpha * __uint_as_float(r[t]);
@@ -1345,9 +1357,9 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
       // current ones are converted and stored (5% faster at K = 1024, where the
       // epilogue of one tile outlasts the next tile's main loop).
       uint32_t ra[32], rb[32];
-      tmem_ld_32x32b_x32(taddr, ra);
+      tmem_ld_32x32b_x32(taddr + cb, ra);
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 64) {
+      for (int c = cb; c < cb + kCols; c += 64) {
         tmem_ld_wait(ra);
         tmem_ld_32x32b_x32(taddr + c + 32, rb);
         {
@@ -1357,7 +1369,7 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
           out.put(i, jt + c, v, 0);
         }
         tmem_ld_wait(rb);
-        if (c + 64 < BN)
+        if (c + 64 < cb + kCols)
           tmem_ld_32x32b_x32(taddr + c + 64, ra);
         else
           release();  // last read of this accumulator: hand it back
@@ -1376,11 +1388,11 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
       const int ctr = w.ctr * Cfg::kCluster + static_cast<int>(rank);
       float4* part = reinterpret_cast<float4*>(a.partials + static_cast<size_t>(slot) * BN * kBM);
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
+      for (int c = cb; c < cb + kCols; c += 32) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(taddr + c, r);
         tmem_ld_wait(r);
-        if (c + 32 == BN) release();
+        if (c + 32 == cb + kCols) release();
 #pragma unroll
         for (int g = 0; g < 8; ++g)
           __stcg(part + static_cast<size_t>((c >> 2) + g) * kBM + row,
@@ -1389,9 +1401,9 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
       }
       // One GPU-scope fence by the arriving thread, after the barrier that orders
       // every epilogue thread's partial stores before it, publishes the whole
-      // partial (fences are cumulative); a fence in each of the 128 threads
-      // would stall every one of them on its own stores.
-      bar_sync(1, 128);
+      // partial (fences are cumulative); a fence in each epilogue thread would
+      // stall every one of them on its own stores.
+      bar_sync(1, kEpiThreads);
       if (threadIdx.x == 64) {
         __threadfence();
         const int old = atomicAdd(&a.counters[ctr], 1);
@@ -1402,13 +1414,13 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
         }
         *reinterpret_cast<volatile uint32_t*>(&ctrl->last) = last;
       }
-      bar_sync(1, 128);
+      bar_sync(1, kEpiThreads);
       if (*reinterpret_cast<volatile uint32_t*>(&ctrl->last)) {
-        out.begin_tile(jt, jt + BN);
+        out.begin_tile(jt + cb, jt + cb + kCols);
         // 64 columns per round: 16 independent 16-byte loads per contribution in
         // flight (the sum is latency-bound, one L2 round trip per round).
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 64) {
+        for (int c = cb; c < cb + kCols; c += 64) {
           float4 acc[16];
 #pragma unroll
           for (int g = 0; g < 16; ++g) acc[g] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -1446,13 +1458,13 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
   out.finish();  // every bulk store has read its staging buffer before the CTA can exit
 }
 
-template <int BN, int CG, int EB, bool DQ>
-__global__ void __launch_bounds__(threads_of(DQ), 1)
+template <int BN, int CG, int EB, bool DQ, int EW>
+__global__ void __launch_bounds__(threads_of(EW, DQ), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p,
                    const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_c, const __grid_constant__ CMaps cmaps,
                    const TcArgs args) {
-  using Cfg = TcConfig<BN, CG, DQ>;
+  using Cfg = TcConfig<BN, CG, DQ, EW>;
   // The roles take the arguments by reference; a local copy whose address never
   // leaves this kernel lets the compiler keep the fields in registers across
   // the global stores and "memory"-clobbering asm of the loops, instead of
@@ -1492,10 +1504,10 @@ __global__ void __launch_bounds__(threads_of(DQ), 1)
       }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctrl->acc_full[b]), 1);
-      mbar_init(smem_u32(&ctrl->acc_empty[b]), 128 * CG);
+      mbar_init(smem_u32(&ctrl->acc_empty[b]), 32 * Cfg::kEpiWarps * CG);
     }
     mbar_init(smem_u32(&ctrl->mma_done), 1);
-    for (int w = 0; w < 4; ++w)
+    for (int w = 0; w < Cfg::kEpiWarps; ++w)
       for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&ctrl->c_full[w][b]), 1);
     ctrl->abort = 0;
     ctrl->last = 0;
@@ -1526,20 +1538,20 @@ __global__ void __launch_bounds__(threads_of(DQ), 1)
     // before two-slice stages existed (a runtime trip count cost ~12% at 4096^3)
     // (DQ kernels: one k-slice a stage, the planner's choice)
     if (!DQ && a.kdepth == 2)
-      producer_role<BN, CG, EB, 2, DQ>(&map_p, &map_q, &cmaps.m[0], a, ring_a, ring_b, code_ring, ctrl, rank, first,
+      producer_role<BN, CG, EB, 2, DQ, EW>(&map_p, &map_q, &cmaps.m[0], a, ring_a, ring_b, code_ring, ctrl, rank, first,
                                        stride);
     else
-      producer_role<BN, CG, EB, 1, DQ>(&map_p, &map_q, &cmaps.m[0], a, ring_a, ring_b, code_ring, ctrl, rank, first,
+      producer_role<BN, CG, EB, 1, DQ, EW>(&map_p, &map_q, &cmaps.m[0], a, ring_a, ring_b, code_ring, ctrl, rank, first,
                                        stride);
   } else if (warp == 1) {
     if (rank % CG == 0) {
       if (!DQ && a.kdepth == 2)
-        mma_role<BN, CG, EB, 2, DQ>(a, ring_a, ring_b, code_ring, ctrl, tmem_base, rank, first, stride);
+        mma_role<BN, CG, EB, 2, DQ, EW>(a, ring_a, ring_b, code_ring, ctrl, tmem_base, rank, first, stride);
       else
-        mma_role<BN, CG, EB, 1, DQ>(a, ring_a, ring_b, code_ring, ctrl, tmem_base, rank, first, stride);
+        mma_role<BN, CG, EB, 1, DQ, EW>(a, ring_a, ring_b, code_ring, ctrl, tmem_base, rank, first, stride);
     }
-  } else if (warp < 6) {
-    epilogue_role<BN, CG, EB, DQ>(a, &map_c, &cmaps, staging, ring_a, ctrl, tmem_base, warp, lane, rank, first,
+  } else if (warp < 2 + Cfg::kEpiWarps) {
+    epilogue_role<BN, CG, EB, DQ, EW>(a, &map_c, &cmaps, staging, ring_a, ctrl, tmem_base, warp, lane, rank, first,
                                   stride);
   } else if constexpr (DQ) {
     converter_role<BN, CG>(a, ring_a, code_ring, ctrl, warp - 6, lane, first, stride);

@@ -44,6 +44,7 @@ OPT_KDEPTH = 11
 OPT_PDL = 12
 OPT_PLAN_CACHE = 13
 OPT_DEQUANT_IN_KERNEL = 15
+OPT_EPILOGUE_WARPS = 16
 BULK_NONE, BULK_ROWS, BULK_TRANSPOSED, BULK_STAGED, BULK_ROW_COPIES, BULK_ROW_CLASSES = 0, 1, 2, 3, 4, 5  # bulk_store
 SCHED_TILES, SCHED_STREAM_K = 0, 1
 
@@ -62,7 +63,7 @@ class Plan(ctypes.Structure):
                                     "grid", "launches", "schedule")] + \
                [(n, _i64) for n in ("tiles", "units", "workspace_bytes")] + \
                [(n, _i32) for n in ("tiles_i", "tiles_j", "num_kb", "dp_tiles", "sk_slots", "cluster", "kdepth",
-                                    "bulk_store", "batch")]
+                                    "bulk_store", "batch", "epilogue_warps")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

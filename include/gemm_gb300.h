@@ -317,6 +317,10 @@ typedef struct {
                               complete one barrier */
   int32_t bulk_store;      /* how C leaves: gemm_bulk_store_t */
   int32_t batch;           /* GEMMs in the call (1 unless strided batched); tiles counts all */
+  int32_t epilogue_warps;  /* warps storing C: 4 (one per 32-lane quarter of the accumulator), or
+                              8 (two per quarter, each storing half of a tile's columns; for
+                              256-wide CTA-pair 16-bit tiles whose C leaves through direct
+                              stores, row classes or per-row copies) */
 } gemm_plan_t;
 
 /*
@@ -466,10 +470,14 @@ typedef enum {
                                   strides, dtype, beta, options and pointer alignments (32
                                   plans per handle, least recently used replaced); 0: plan
                                   every call */
-  GEMM_OPT_DEQUANT_IN_KERNEL = 15 /* block-scaled GEMMs with M <= 64 < N: 0 (default) the weights
+  GEMM_OPT_DEQUANT_IN_KERNEL = 15, /* block-scaled GEMMs with M <= 64 < N: 0 (default) the weights
                                   B stay in their codes and the GEMM converts them as they
                                   arrive (see gemm_run_block_scaled); 1: a pass writes both
                                   operands as 16-bit values first */
+  GEMM_OPT_EPILOGUE_WARPS = 16  /* 0 auto (eight where C leaves through direct stores, row
+                                  classes or per-row copies and the tile has such a kernel),
+                                  else 4 or 8: the kernel with that many epilogue warps where
+                                  the tile has one (gemm_plan_t.epilogue_warps) */
 } gemm_option_t;
 
 /* Set an option on a handle.  Errors: GEMM_ERR_INVALID_ARG for an unknown

@@ -196,6 +196,26 @@ def test_plan_misaligned_c():
     assert pb.bulk_store == G.BULK_ROW_COPIES
 
 
+def test_plan_epilogue_warps():
+    """The 256-wide CTA-pair tile has a kernel with eight epilogue warps, taken
+    where C leaves through row classes, per-row copies or direct stores; with
+    bulk tensor stores (and for other tiles) the four-warp kernel stays."""
+    p = G.plan(4095, 4097, 1000, 0, 0, ldb=4097, ldc=4097)       # row classes
+    assert p.bulk_store == G.BULK_ROW_CLASSES and p.bm == 256 and p.bn == 256 and p.epilogue_warps == 8
+    p = G.plan(4095, 4097, 1000, 0, 0, ldb=4104, ldc=4100)       # aligned rows ending inside a piece
+    assert p.bulk_store == G.BULK_ROW_CLASSES and p.epilogue_warps == 8
+    p = G.plan(4096, 4096, 4096, 0, 0, G.F16_F16, ldc=4100, beta=0.5)   # beta != 0, 16-bit C: direct stores
+    assert p.bulk_store == G.BULK_NONE and p.epilogue_warps == 8
+    for args, kw in (((4096, 4096, 4096, 0, 1), {}),                       # bulk rows
+                     ((4096, 4096, 4096, 1, 0, G.F16_F16), {"beta": 0.5}),  # bulk rows with the blend
+                     ((64, 32000, 4096, 0, 1), {}),                        # swapped, 64-wide tiles
+                     ((2048, 1001, 512, 0, 1, G.BF16_BF16), {"ldc": 1008})):  # the aligned workspace copy
+        q = G.plan(*args, **kw)
+        assert q.epilogue_warps == 4, (args, q.as_dict())
+    # a 256-wide CTA-pair tile with eight warps keeps at least two ring stages
+    assert 2 <= p.stages < G.plan(4096, 4096, 4096, 0, 1).stages
+
+
 def test_plan_fp8():
     """8-bit inputs: 128-element k-slices (one 128-byte swizzle row), the 8-bit
     tile configurations, rows aligned to 16 elements, and K-major operands only."""

@@ -223,3 +223,44 @@ def test_dq_kernel_timeout_then_clean(h):
         h.set_option(G.OPT_WAIT_LIMIT_NS, 2_000_000_000)
     R, Mag = reference(p)
     assert_close(run(p, h), R, Mag, True, p.name)
+
+
+@pytest.mark.parametrize("elem", ["e4m3", "e5m2", "e2m1"])
+def test_dq_kernel_every_code_exact(h, elem):
+    """Every code of the weights' format through the converting path, one
+    product per output: token i is 1.0 at k = i and 0 elsewhere, so C[i, j] is
+    weight (j, i) times its row's scale, exactly (the E8M0 scales keep every
+    product inside bf16's normal range; E2M1 x E4M3 products are exact in
+    fp16).  Rows 0 .. 255 hold every finite code at every position of a
+    k-slice; rows 256 .. 511 hold the special codes too (E4M3 NaN, E5M2
+    infinities and NaNs), whose columns come out NaN as in the oracle."""
+    fmt = "nvfp4" if elem == "e2m1" else "mxfp8"
+    M, N, K = 64, 512, 64
+    p = inputs.make_block_scaled_problem("bs_dq_codes_" + elem, M, N, K, fmt, "f32", elem, elem, seed=21)
+    A, B, SA, SB = p.A.numpy(), p.B.numpy(), p.SFA.numpy(), p.SFB.numpy()
+    nblk = K // p.block
+    A[:, :] = 0
+    j = np.arange(N)[:, None]
+    k = np.arange(K)[None, :]
+    if fmt == "nvfp4":
+        A[np.arange(M), np.arange(M) // 2] = np.where(np.arange(M) % 2 == 0, 0x02, 0x20)  # E2M1 1.0
+        SA[:, :nblk] = 0x38                                                                # UE4M3 1.0
+        nib = (j + k) % 16
+        B[:, :K // 2] = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+        SB[:, :nblk] = np.array([0x38, 0x01, 0x7E, 0x08, 0x40, 0x20, 0x30, 0x50], np.uint8)[np.arange(N) % 8, None]
+    else:
+        A[np.arange(M), np.arange(M)] = 0x38 if elem == "e4m3" else 0x3C                # 1.0
+        SA[:, :nblk] = 127
+        codes = (j * 64 + k) % 256
+        special = (codes & 0x7F) == 0x7F if elem == "e4m3" else (codes & 0x7C) == 0x7C
+        codes = np.where(special & (j < N // 2), 0, codes)
+        B[:, :K] = codes.astype(np.uint8)
+        top = 240 if elem == "e4m3" else 225   # largest code x 2^(top - 127) finite in bf16
+        SB[:, :nblk] = np.array([17, 60, 100, 127, 150, 200, top, 127], np.uint8)[np.arange(N) % 8, None]
+    assert _dq_plan(p, h).launches == 2
+    R, _ = reference(p)
+    out = run(p, h)
+    np.testing.assert_array_equal(out.astype(np.float32), R.astype(np.float32))
+    assert np.isfinite(out[:, :N // 2]).all()
+    if fmt == "mxfp8":
+        assert np.isnan(out[:, N // 2:]).any()

@@ -217,3 +217,51 @@ def test_tensor_binding_bias_gelu(h):
     R, Mag = oracle_full(p)
     R, Mag = oracle.epilogue(R, Mag, bias=b.numpy(), act=G.ACT_GELU, scale=0.5)
     assert oracle.within_tolerance(C.double().cpu().numpy(), R, Mag, False).all()
+
+
+EW_CASES = [  # name, M, N, K, transA, transB, inputs, C, beta, guard columns, GEMM_OPT_EPILOGUE, store path
+    ("rows", 600, 904, 300, 0, 1, "bf16", "f32", 0.0, 8, 0, G.BULK_ROWS),
+    ("rows_bf16", 600, 904, 300, 0, 1, "bf16", "bf16", 0.0, 8, 0, G.BULK_ROWS),
+    ("blend", 300, 520, 200, 1, 1, "f16", "f16", -0.5, 8, 0, G.BULK_ROWS),
+    ("direct_blend", 300, 520, 200, 0, 0, "f16", "f16", -0.5, 5, 0, G.BULK_NONE),
+    ("classes", 1100, 1001, 300, 0, 1, "bf16", "f32", 0.0, 5, 0, G.BULK_ROW_CLASSES),
+    ("row_copies", 1100, 1001, 300, 0, 1, "bf16", "bf16", 0.0, 3, 4, G.BULK_ROW_COPIES),
+    ("staged", 1100, 1001, 300, 0, 1, "bf16", "f32", 0.0, 7, 3, G.BULK_STAGED),
+]
+
+
+@pytest.mark.parametrize("ew", [4, 8])
+@pytest.mark.parametrize("case", EW_CASES, ids=lambda c: c[0])
+def test_epilogue_warps(h, case, ew):
+    """The 256-wide CTA-pair tile with four or with eight epilogue warps (two
+    per tensor-memory lane quarter, each storing half of a tile's columns) on
+    every store path, with the fused operations."""
+    name, M, N, K, ta, tb, fin, fout, beta, guard, mode, bulk = case
+    p = inputs.make_problem("epi_ew_" + name, M, N, K, ta, tb, fin, fout, ("normal", 0, 1), ("normal", 0, 1),
+                            alpha=0.5, beta=beta, seed=50 + ew + len(name))
+    h.set_option(G.OPT_EPILOGUE, mode)
+    h.set_option(G.OPT_EPILOGUE_WARPS, ew)
+    try:
+        with options(h, path=G.PATH_TC_2CTA, bn=256):
+            plan = G.plan(p.M, p.N, p.K, ta, tb, dtype_code(p), handle=h, ldc=p.ldc + guard, beta=p.beta)
+            assert plan.epilogue_warps == ew and plan.bn == 256 and plan.bm == 256
+            check(p, h, bias_for(p.N, 6), G.ACT_GELU, 0.75, guard_cols=guard, expect_bulk=bulk)
+    finally:
+        h.set_option(G.OPT_EPILOGUE, 0)
+        h.set_option(G.OPT_EPILOGUE_WARPS, 0)
+
+
+@pytest.mark.parametrize("sched", ["split", "stream_k"])
+def test_epilogue_warps_fix_up(h, sched):
+    """Eight epilogue warps on split tiles: each warp writes and sums its half
+    of the columns of every partial."""
+    p = inputs.make_problem("epi_ew_sk", 700, 904, 1500, 0, 1, "bf16", "f32", ("normal", 0, 1), ("normal", 0, 1),
+                            seed=57)
+    kw = dict(split=3) if sched == "split" else dict(grid=14, stream_k=2)
+    h.set_option(G.OPT_EPILOGUE_WARPS, 8)
+    try:
+        with options(h, path=G.PATH_TC_2CTA, bn=256, **kw):
+            assert G.plan(p.M, p.N, p.K, 0, 1, handle=h, ldc=p.ldc + 8).epilogue_warps == 8
+            check(p, h, bias_for(p.N, 7), G.ACT_RELU, 1.5)
+    finally:
+        h.set_option(G.OPT_EPILOGUE_WARPS, 0)
