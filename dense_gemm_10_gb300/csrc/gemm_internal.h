@@ -16,8 +16,9 @@ constexpr int kBK = 64;           // k-slice of 16-bit elements (64 x 2 bytes)
 // Warps of a GEMM CTA: warp 0 TMA producer, warp 1 MMA issuer, then `ew`
 // epilogue warps (four, one per 32-lane quarter of tensor memory; or eight,
 // two per quarter, each of a pair storing half of the tile's columns), then in
-// DQ kernels four warps converting block-scaled codes.
-__host__ __device__ constexpr int threads_of(int ew, bool dq) { return 64 + 32 * (ew + (dq ? 4 : 0)); }
+// DQ kernels kConvWarps warps converting block-scaled codes.
+constexpr int kConvWarps = 8;
+__host__ __device__ constexpr int threads_of(int ew, bool dq) { return 64 + 32 * (ew + (dq ? kConvWarps : 0)); }
 
 // k elements of one k-slice for an element of eb bytes (2: bf16 / fp16, 1: FP8).
 __host__ __device__ constexpr int slice_k(int eb) { return kSliceBytes / eb; }

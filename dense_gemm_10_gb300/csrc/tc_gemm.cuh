@@ -1063,12 +1063,16 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_p, const CU
   __syncwarp();
 }
 
-// DQ kernels: four converter warps turn P's block-scaled codes into the 16-bit
-// values the MMA reads, stage by stage (the producer's order: the same work
-// units and k-blocks, one k-slice a stage).  Warp cw converts rows 32 cw ..
-// 32 cw + 31 of the 128-row P tile, one row per thread, into the ring's
-// 128-byte-swizzled K-major layout (16-byte piece p of row r at p ^ (r & 7)),
-// then completes the stage's full barrier with one arrival per warp.
+// DQ kernels: kConvWarps converter warps turn P's block-scaled codes into the
+// 16-bit values the MMA reads, stage by stage (the producer's order: the same
+// work units and k-blocks, one k-slice a stage).  Warp cw converts rows
+// 16 cw .. 16 cw + 15 of the 128-row P tile, two threads a row, each half of
+// the row's 64 values, into the ring's 128-byte-swizzled K-major layout
+// (16-byte piece p of row r at p ^ (r & 7)), then completes the stage's full
+// barrier with one arrival per warp.  (Two warps on each of the SM's four
+// schedulers halve each warp's share of a stage: four warps with a whole row
+// per thread left the conversion on the critical path, about 20 us of the
+// LM head's 65.)
 //  * E2M1 codes (two a byte, the even k in the low four bits) with unsigned
 //    E4M3 scales per 16 values -> fp16: code and scale as fp16, one fp16
 //    product, exact (at most 6 significant bits, inside fp16's range).
@@ -1081,7 +1085,9 @@ template <int BN, int CG>
 __device__ __forceinline__ void converter_role(const TcArgs& a, uint8_t* ring_a, uint8_t* code_ring, TcCtrl* ctrl,
                                                int cw, int lane, int first, int stride) {
   using Cfg = TcConfig<BN, CG, true>;
-  const int r = cw * 32 + lane;
+  static_assert(kBM == 16 * kConvWarps, "two threads a row");
+  const int r = cw * 16 + (lane >> 1);
+  const int h = lane & 1;  // values 32 h .. 32 h + 31 of the row's 64
   const uint32_t sw = static_cast<uint32_t>(r & 7);
   int stage = 0, cstage = 0;  // the P ring and the code ring
   uint32_t phase = 0, cphase = 0;
@@ -1096,25 +1102,23 @@ __device__ __forceinline__ void converter_role(const TcArgs& a, uint8_t* ring_a,
         break;
       }
       const uint8_t* cst = code_ring + cstage * a.code_stage_bytes + Cfg::kBBytes;  // past the Q tile
-      const uint32_t codes = smem_u32(cst) + static_cast<uint32_t>(r * a.code_bytes);
+      const uint32_t codes = smem_u32(cst) + static_cast<uint32_t>(r * a.code_bytes + h * (a.code_bytes / 2));
       const uint32_t scales =
           smem_u32(cst + kBM * a.code_bytes) + static_cast<uint32_t>(r * 16 + ((kb * a.spk) & 15));
       const uint32_t dst = smem_u32(ring_a + stage * Cfg::kABytes) + static_cast<uint32_t>(r * 128);
       if (a.dq_fmt == 1) {
-        uint32_t wd[8];
+        uint32_t wd[4];
         {
-          const float4 c0 = ld_shared_v4_f32(codes), c1 = ld_shared_v4_f32(codes + 16);
+          const float4 c0 = ld_shared_v4_f32(codes);
           wd[0] = __float_as_uint(c0.x); wd[1] = __float_as_uint(c0.y); wd[2] = __float_as_uint(c0.z);
-          wd[3] = __float_as_uint(c0.w); wd[4] = __float_as_uint(c1.x); wd[5] = __float_as_uint(c1.y);
-          wd[6] = __float_as_uint(c1.z); wd[7] = __float_as_uint(c1.w);
+          wd[3] = __float_as_uint(c0.w);
         }
-        // the four unsigned E4M3 scales as fp16 pairs (sign bits cleared)
-        const uint32_t sc = ld_shared_u32(scales) & 0x7F7F7F7Fu;
-        const uint32_t s01 = e4m3x2_to_f16x2(sc & 0xFFFFu), s23 = e4m3x2_to_f16x2(sc >> 16);
-        const uint32_t sf[4] = {__byte_perm(s01, 0, 0x1010), __byte_perm(s01, 0, 0x3232), __byte_perm(s23, 0, 0x1010),
-                                __byte_perm(s23, 0, 0x3232)};
+        // this half's two unsigned E4M3 scales as fp16 pairs (sign bits cleared)
+        const uint32_t sc = ld_shared_u16(scales + 2 * h) & 0x7F7Fu;
+        const uint32_t s01 = e4m3x2_to_f16x2(sc);
+        const uint32_t sf[2] = {__byte_perm(s01, 0, 0x1010), __byte_perm(s01, 0, 0x3232)};
 #pragma unroll
-        for (int p = 0; p < 8; ++p) {  // values 8p .. 8p + 7, scale p / 2
+        for (int p = 0; p < 4; ++p) {  // values 32 h + 8p .. + 7, scale p / 2 of the half
           const __half2 s2 = *reinterpret_cast<const __half2*>(&sf[p >> 1]);
           uint32_t o[4];
 #pragma unroll
@@ -1123,33 +1127,29 @@ __device__ __forceinline__ void converter_role(const TcArgs& a, uint8_t* ring_a,
             const __half2 prod = __hmul2(*reinterpret_cast<const __half2*>(&hv), s2);
             o[b] = *reinterpret_cast<const uint32_t*>(&prod);
           }
-          st_shared_v4(dst + ((static_cast<uint32_t>(p) ^ sw) << 4), o[0], o[1], o[2], o[3]);
+          st_shared_v4(dst + ((static_cast<uint32_t>(4 * h + p) ^ sw) << 4), o[0], o[1], o[2], o[3]);
         }
       } else {
         const bool e5m2 = a.dq_fmt == 3;
-        const uint32_t sc = ld_shared_u16(scales);
+        const uint32_t s = (ld_shared_u16(scales) >> (8 * h)) & 0xFFu;  // the half's one scale
+        const float f = s == 255u ? __int_as_float(0x7FC00000)
+                                  : s == 0u ? __int_as_float(0x00400000) : __int_as_float(static_cast<int>(s << 23));
+        const float4 c0 = ld_shared_v4_f32(codes), c1 = ld_shared_v4_f32(codes + 16);
+        const uint32_t wd[8] = {__float_as_uint(c0.x), __float_as_uint(c0.y), __float_as_uint(c0.z),
+                                __float_as_uint(c0.w), __float_as_uint(c1.x), __float_as_uint(c1.y),
+                                __float_as_uint(c1.z), __float_as_uint(c1.w)};
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {  // 32 values under one scale
-          const uint32_t s = (sc >> (8 * h)) & 0xFFu;
-          const float f = s == 255u ? __int_as_float(0x7FC00000)
-                                    : s == 0u ? __int_as_float(0x00400000) : __int_as_float(static_cast<int>(s << 23));
-          const float4 c0 = ld_shared_v4_f32(codes + 32 * h), c1 = ld_shared_v4_f32(codes + 32 * h + 16);
-          const uint32_t wd[8] = {__float_as_uint(c0.x), __float_as_uint(c0.y), __float_as_uint(c0.z),
-                                  __float_as_uint(c0.w), __float_as_uint(c1.x), __float_as_uint(c1.y),
-                                  __float_as_uint(c1.z), __float_as_uint(c1.w)};
+        for (int p = 0; p < 4; ++p) {  // piece 4h + p: words 2p, 2p + 1
+          uint32_t o[4];
 #pragma unroll
-          for (int p = 0; p < 4; ++p) {  // piece 4h + p: words 2p, 2p + 1
-            uint32_t o[4];
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-              const uint32_t pair = (wd[2 * p + (b >> 1)] >> (16 * (b & 1))) & 0xFFFFu;
-              const uint32_t hv = e5m2 ? e5m2x2_to_f16x2(pair) : e4m3x2_to_f16x2(pair);
-              const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&hv));
-              const __nv_bfloat162 y = __floats2bfloat162_rn(x.x * f, x.y * f);
-              o[b] = *reinterpret_cast<const uint32_t*>(&y);
-            }
-            st_shared_v4(dst + ((static_cast<uint32_t>(4 * h + p) ^ sw) << 4), o[0], o[1], o[2], o[3]);
+          for (int b = 0; b < 4; ++b) {
+            const uint32_t pair = (wd[2 * p + (b >> 1)] >> (16 * (b & 1))) & 0xFFFFu;
+            const uint32_t hv = e5m2 ? e5m2x2_to_f16x2(pair) : e4m3x2_to_f16x2(pair);
+            const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&hv));
+            const __nv_bfloat162 y = __floats2bfloat162_rn(x.x * f, x.y * f);
+            o[b] = *reinterpret_cast<const uint32_t*>(&y);
           }
+          st_shared_v4(dst + ((static_cast<uint32_t>(4 * h + p) ^ sw) << 4), o[0], o[1], o[2], o[3]);
         }
       }
       fence_proxy_async_smem();  // the MMA reads these values through the async proxy
@@ -1418,21 +1418,24 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
       if (*reinterpret_cast<volatile uint32_t*>(&ctrl->last)) {
         out.begin_tile(jt + cb, jt + cb + kCols);
         // 64 columns per round: 16 independent 16-byte loads per contribution in
-        // flight (the sum is latency-bound, one L2 round trip per round).
+        // flight (the sum is latency-bound, one L2 round trip per round); 32 in
+        // kernels of more than 320 threads, whose threads hold fewer registers.
+        constexpr int kRound = threads_of(EW, DQ) > 320 ? 32 : 64;
+        constexpr int kG = kRound / 4;
 #pragma unroll 1
-        for (int c = cb; c < cb + kCols; c += 64) {
-          float4 acc[16];
+        for (int c = cb; c < cb + kCols; c += kRound) {
+          float4 acc[kG];
 #pragma unroll
-          for (int g = 0; g < 16; ++g) acc[g] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          for (int g = 0; g < kG; ++g) acc[g] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll 1
           for (int k = 0; k < w.ncontrib; ++k) {  // fixed k order: the sum does not depend on timing
             const int ks = contrib_slot(a.sched, w, k) * Cfg::kCluster + static_cast<int>(rank);
             const float4* ps = reinterpret_cast<const float4*>(a.partials + static_cast<size_t>(ks) * BN * kBM);
-            float4 x[16];
+            float4 x[kG];
 #pragma unroll
-            for (int g = 0; g < 16; ++g) x[g] = __ldcg(ps + static_cast<size_t>((c >> 2) + g) * kBM + row);
+            for (int g = 0; g < kG; ++g) x[g] = __ldcg(ps + static_cast<size_t>((c >> 2) + g) * kBM + row);
 #pragma unroll
-            for (int g = 0; g < 16; ++g) {
+            for (int g = 0; g < kG; ++g) {
               acc[g].x += x[g].x;
               acc[g].y += x[g].y;
               acc[g].z += x[g].z;
@@ -1440,7 +1443,7 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
             }
           }
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < kRound / 32; ++h) {
             float v[32];
 #pragma unroll
             for (int g = 0; g < 8; ++g) {
@@ -1449,7 +1452,7 @@ __device__ __forceinline__ void epilogue_role(const TcArgs& a, const CUtensorMap
               v[4 * g + 2] = alpha * acc[8 * h + g].z;
               v[4 * g + 3] = alpha * acc[8 * h + g].w;
             }
-            out.put(i, jt + c + 32 * h, v, h);
+            out.put(i, jt + c + 32 * h, v, ((c + 32 * h) >> 5) & 1);
           }
         }
       }
@@ -1494,7 +1497,7 @@ __global__ void __launch_bounds__(threads_of(EW, DQ), 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::kStages; ++s) {
-      mbar_init(smem_u32(&ctrl->full[s]), DQ ? 4 : 1);  // (DQ: one arrival per converter warp)
+      mbar_init(smem_u32(&ctrl->full[s]), DQ ? kConvWarps : 1);  // (DQ: one arrival per converter warp)
       mbar_init(smem_u32(&ctrl->empty[s]), 1);  // released by the pair's MMA commit
     }
     if (DQ)

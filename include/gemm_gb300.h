@@ -542,8 +542,8 @@ gemm_status_t gemm_probe_tma_tile(gemm_handle_t h, const void* src, int64_t ld, 
  * GEMM_ERR_WORKSPACE and launches nothing.
  *
  * The first call on a device sets that device up (looks up the arrays'
- * device addresses, opts the kernels in to their shared memory); make that
- * first call before any stream capture.  Every call shares the same arrays
+ * device addresses, opts the kernels in to their shared memory); later calls
+ * only plan and launch.  Every call shares the same arrays
  * and each call clears the counters and status word it uses, so calls that
  * overlap on the GPU (two streams, or two host threads) race on them: order
  * them on one stream.  A kernel that gives up on a barrier records it in the
