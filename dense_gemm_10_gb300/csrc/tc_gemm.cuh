@@ -9,8 +9,11 @@
 //    Kernel; "GPU GEMM 优化完全拆解（三）", rasterization).
 //  * Warp specialisation: warp 0 issues TMA copies into a multi-stage shared
 //    memory ring guarded by full / empty mbarriers, warp 1 issues tcgen05.mma
-//    from one thread, warps 2-5 run the epilogue ("GPU GEMM 优化完全拆解（三）",
-//    warp specialization; "CUDA GEMM 矩阵乘法优化指南", 12.4 and 13.2).
+//    from one thread, warps 2 .. 2 + EW - 1 run the epilogue (EW = 4, one per
+//    32-lane quarter of tensor memory, or 8, two per quarter each storing half
+//    of a tile's columns), and in DQ kernels kConvWarps more warps convert
+//    block-scaled codes ("GPU GEMM 优化完全拆解（三）", warp specialization;
+//    "CUDA GEMM 矩阵乘法优化指南", 12.4 and 13.2).
 //  * Tiles arrive 128-byte swizzled ("[CUDA 优化实战] hgemm sm120", section 4:
 //    the swizzle of 16-bit element (r, c) in a 64-wide row is c ^ ((r & 7) << 3)),
 //    which is the layout the tensor core's shared-memory descriptor expects.
