@@ -875,6 +875,7 @@ struct PlanCache {
 // gemm_run_host: device copies of A, B and C, and the two copy streams (one
 // per direction) whose transfers overlap the GEMMs of neighbouring row chunks.
 constexpr int kHostChunks = 4;
+constexpr int kHostBlocks = kHostChunks * kHostChunks;  // blocks of C: row chunks x column chunks
 struct HostStage {
   void* a = nullptr;
   void* b = nullptr;
@@ -882,8 +883,8 @@ struct HostStage {
   size_t a_bytes = 0, b_bytes = 0, c_bytes = 0;
   cudaStream_t up = nullptr, down = nullptr;  // host -> device, device -> host
   cudaEvent_t start = nullptr, end = nullptr;
-  cudaEvent_t loaded[kHostChunks] = {};       // a chunk's operands are on the device
-  cudaEvent_t computed[kHostChunks] = {};     // a chunk's C is ready to copy back
+  cudaEvent_t loaded[kHostBlocks] = {};       // a block's operands (and old C) are on the device
+  cudaEvent_t computed[kHostBlocks] = {};     // a block's C is ready to copy back
 };
 
 struct gemm_handle_s {
@@ -959,7 +960,7 @@ gemm_status_t gemm_destroy(gemm_handle_t h) {
     if (hs.down) cudaStreamDestroy(hs.down);
     if (hs.start) cudaEventDestroy(hs.start);
     if (hs.end) cudaEventDestroy(hs.end);
-    for (int i = 0; i < kHostChunks; ++i) {
+    for (int i = 0; i < kHostBlocks; ++i) {
       if (hs.loaded[i]) cudaEventDestroy(hs.loaded[i]);
       if (hs.computed[i]) cudaEventDestroy(hs.computed[i]);
     }
@@ -1454,7 +1455,7 @@ gemm_status_t gemm_run_host(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB,
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hs.down, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hs.start, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hs.end, cudaEventDisableTiming);
-    for (int i = 0; i < kHostChunks && e == cudaSuccess; ++i) {
+    for (int i = 0; i < kHostBlocks && e == cudaSuccess; ++i) {
       e = cudaEventCreateWithFlags(&hs.loaded[i], cudaEventDisableTiming);
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hs.computed[i], cudaEventDisableTiming);
     }
@@ -1467,13 +1468,17 @@ gemm_status_t gemm_run_host(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB,
     h->last_cuda_error = static_cast<int>(e);
     return GEMM_ERR_WORKSPACE;
   }
-  // Row chunks of A (stored M x K) and C: the copy of chunk c + 1 in and of
-  // chunk c - 1 out run while chunk c is multiplied.  One chunk for a
-  // transposed A or a short M.
-  const int64_t chunk = (transA == GEMM_OP_N && M >= 1024 && K > 0)
-                            ? static_cast<int64_t>(round_up(static_cast<size_t>(cdiv(M, kHostChunks)), 256))
-                            : M;
-  const int nch = static_cast<int>(cdiv(M, chunk));
+  // C in blocks of row chunks x column chunks (up to 4 x 4; one chunk along a
+  // dimension shorter than 1024).  A's row chunks and B's column chunks go over
+  // alternately (A0, B0, A1, B1, ...), and every block of C whose rows and
+  // columns have both arrived is multiplied and copied back at once, so that
+  // copies out start after an eighth of the inputs and overlap the rest of the
+  // copies in.  (Row chunks alone, after all of B: 4096^3 took 0.624 ms; the
+  // first row chunk in column blocks: 0.608 ms.)
+  const int64_t rch = (M >= 1024 && K > 0) ? static_cast<int64_t>(round_up(static_cast<size_t>(cdiv(M, kHostChunks)), 256)) : M;
+  const int64_t cch = (N >= 1024 && K > 0) ? static_cast<int64_t>(round_up(static_cast<size_t>(cdiv(N, kHostChunks)), 256)) : N;
+  const int nr = static_cast<int>(cdiv(M, rch));
+  const int nc = static_cast<int>(cdiv(N, cch));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ad = static_cast<char*>(hs.a);
   char* bd = static_cast<char*>(hs.b);
@@ -1481,37 +1486,74 @@ gemm_status_t gemm_run_host(gemm_handle_t h, gemm_op_t transA, gemm_op_t transB,
   const char* ah = static_cast<const char*>(A);
   const char* bh = static_cast<const char*>(B);
   char* ch = static_cast<char*>(C);
+  // A's rows of C r0 .. r0 + rows - 1 (rows of A stored M x K, else a column slice of each of its K rows)
+  auto copy_a = [&](int64_t r0, int64_t rows) {
+    if (a_bytes == 0) return cudaSuccess;
+    if (transA == GEMM_OP_N)
+      return cudaMemcpy2DAsync(ad + r0 * lda * ea, lda * ea, ah + r0 * lda * ea, lda * ea, K * ea, rows,
+                               cudaMemcpyHostToDevice, hs.up);
+    return cudaMemcpy2DAsync(ad + r0 * ea, lda * ea, ah + r0 * ea, lda * ea, rows * ea, K, cudaMemcpyHostToDevice,
+                             hs.up);
+  };
+  // B's columns of C j0 .. j0 + cols - 1 (rows of B stored N x K, else a column slice of each of its K rows)
+  auto copy_b = [&](int64_t j0, int64_t cols) {
+    if (b_bytes == 0) return cudaSuccess;
+    if (transB == GEMM_OP_T)
+      return cudaMemcpy2DAsync(bd + j0 * ldb * ea, ldb * ea, bh + j0 * ldb * ea, ldb * ea, K * ea, cols,
+                               cudaMemcpyHostToDevice, hs.up);
+    return cudaMemcpy2DAsync(bd + j0 * ea, ldb * ea, bh + j0 * ea, ldb * ea, cols * ea, K, cudaMemcpyHostToDevice,
+                             hs.up);
+  };
+  // block (i, j) of C: its old values in for the blend, the GEMM once everything
+  // queued on the copy-in stream so far has landed, its values out
+  int ev = 0;
+  auto block = [&](int i, int j) -> gemm_status_t {
+    const int64_t r0 = i * rch, rows = std::min(rch, M - r0);
+    const int64_t j0 = j * cch, cols = std::min(cch, N - j0);
+    char* cdb = cd + (r0 * ldc + j0) * ec;
+    char* chb = ch + (r0 * ldc + j0) * ec;
+    cudaError_t e2 = cudaSuccess;
+    if (beta != 0.0f)
+      e2 = cudaMemcpy2DAsync(cdb, ldc * ec, chb, ldc * ec, cols * ec, rows, cudaMemcpyHostToDevice, hs.up);
+    if (e2 == cudaSuccess) e2 = cudaEventRecord(hs.loaded[ev], hs.up);
+    if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(st, hs.loaded[ev], 0);
+    if (e2 != cudaSuccess) return cuda_fail(h, e2);
+    const char* a_blk = transA == GEMM_OP_N ? ad + r0 * lda * ea : ad + r0 * ea;
+    const char* b_blk = transB == GEMM_OP_T ? bd + j0 * ldb * ea : bd + j0 * ea;
+    const gemm_status_t s2 = run_gemm(h, transA, transB, rows, cols, K, alpha, a_blk, lda, b_blk, ldb, beta, cdb, ldc,
+                                      dtype, EpiOps(), st, 1, 0, 0, 0, 0, nullptr, nullptr, false);
+    if (s2 != GEMM_OK) return s2;
+    e2 = cudaEventRecord(hs.computed[ev], st);
+    if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(hs.down, hs.computed[ev], 0);
+    if (e2 == cudaSuccess)
+      e2 = cudaMemcpy2DAsync(chb, ldc * ec, cdb, ldc * ec, cols * ec, rows, cudaMemcpyDeviceToHost, hs.down);
+    ++ev;
+    return e2 == cudaSuccess ? GEMM_OK : cuda_fail(h, e2);
+  };
   // the copy streams start after everything already queued on the caller's stream
   e = cudaEventRecord(hs.start, st);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(hs.up, hs.start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(hs.down, hs.start, 0);
-  if (e == cudaSuccess && b_bytes > 0)
-    e = cudaMemcpy2DAsync(bd, ldb * ea, bh, ldb * ea, b_cols * ea, b_rows, cudaMemcpyHostToDevice, hs.up);
-  for (int c = 0; c < nch && e == cudaSuccess; ++c) {
-    const int64_t r0 = c * chunk;
-    const int64_t rows = std::min(chunk, M - r0);
-    const int64_t a_off = transA == GEMM_OP_N ? r0 * lda * ea : 0;
-    if (a_bytes > 0) {
-      if (transA == GEMM_OP_N)
-        e = cudaMemcpy2DAsync(ad + a_off, lda * ea, ah + a_off, lda * ea, K * ea, rows, cudaMemcpyHostToDevice, hs.up);
-      else
-        e = cudaMemcpy2DAsync(ad, lda * ea, ah, lda * ea, a_cols * ea, a_rows, cudaMemcpyHostToDevice, hs.up);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  int ia = 0, ib = 0;  // row chunks of A and column chunks of B sent so far
+  while (ia < nr || ib < nc) {
+    if (ia < nr && (ia <= ib || ib == nc)) {  // A's next row chunk, then its blocks with the columns already there
+      e = copy_a(ia * rch, std::min(rch, M - ia * rch));
+      if (e != cudaSuccess) return cuda_fail(h, e);
+      ++ia;
+      for (int j = 0; j < ib; ++j) {
+        const gemm_status_t s = block(ia - 1, j);
+        if (s != GEMM_OK) return s;
+      }
+    } else {  // B's next column chunk, then its blocks with the rows already there
+      e = copy_b(ib * cch, std::min(cch, N - ib * cch));
+      if (e != cudaSuccess) return cuda_fail(h, e);
+      ++ib;
+      for (int i = 0; i < ia; ++i) {
+        const gemm_status_t s = block(i, ib - 1);
+        if (s != GEMM_OK) return s;
+      }
     }
-    if (e == cudaSuccess && beta != 0.0f)
-      e = cudaMemcpy2DAsync(cd + r0 * ldc * ec, ldc * ec, ch + r0 * ldc * ec, ldc * ec, N * ec, rows,
-                            cudaMemcpyHostToDevice, hs.up);
-    if (e == cudaSuccess) e = cudaEventRecord(hs.loaded[c], hs.up);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, hs.loaded[c], 0);
-    if (e != cudaSuccess) break;
-    const gemm_status_t s = run_gemm(h, transA, transB, rows, N, K, alpha, ad + a_off, lda, bd, ldb, beta,
-                                     cd + r0 * ldc * ec, ldc, dtype, EpiOps(), st, 1, 0, 0, 0, 0, nullptr, nullptr,
-                                     false);
-    if (s != GEMM_OK) return s;
-    e = cudaEventRecord(hs.computed[c], st);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(hs.down, hs.computed[c], 0);
-    if (e == cudaSuccess)
-      e = cudaMemcpy2DAsync(ch + r0 * ldc * ec, ldc * ec, cd + r0 * ldc * ec, ldc * ec, N * ec, rows,
-                            cudaMemcpyDeviceToHost, hs.down);
   }
   // the caller's stream continues once C is back on the host
   if (e == cudaSuccess) e = cudaEventRecord(hs.end, hs.down);

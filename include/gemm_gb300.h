@@ -416,10 +416,12 @@ gemm_status_t gemm_plan_block_scaled(gemm_handle_t h, int sm_count, int64_t M, i
  * but serialises them); sizes, leading dimensions, dtypes and errors as
  * gemm_run (block-scaled types: GEMM_ERR_UNSUPPORTED).  The handle keeps device
  * copies of A, B and C (grown as needed: a larger call synchronises the device
- * once) and two copy streams, one per direction.  A non-transposed A with
- * M >= 1024 is processed in four row chunks: chunk c + 1's rows of A (and of
- * C when beta != 0) travel to the device and chunk c - 1's rows of C back to
- * the host while chunk c is multiplied; B goes over once, first.  Everything
+ * once) and two copy streams, one per direction.  C is processed in blocks of
+ * up to four row chunks by four column chunks (M or N of 1024 or more is cut
+ * in four): A's row chunks and B's column chunks travel to the device
+ * alternately, each block of C (its old values first when beta != 0) is
+ * multiplied as soon as its rows of A and columns of B are there, and goes
+ * back to the host while the next inputs travel.  Everything
  * is ordered after the work already queued on `stream`, and `stream` waits
  * for the last copy back: C on the host is complete once `stream` is
  * synchronised.  The host buffers must stay valid and unchanged until then.

@@ -1,6 +1,7 @@
 """GPU parity of gemm_run_host (host buffers in and out, copies overlapped with
-the GEMM in row chunks) against the oracle: every layout, chunked (M >= 1024,
-A not transposed) and single-chunk calls, a ragged last chunk, the blend with
+the GEMM in blocks of C) against the oracle: every layout, row chunks
+(M >= 1024), row and column chunks (M, N >= 1024) and single-block calls,
+ragged last chunks, the blend with
 C, 16-bit and fp32 C, page-locked and pageable host memory, K == 0, a growing
 sequence of calls that reuses and grows the handle's device copies, and the
 order with other work on the same stream.  Host C's padding columns must stay
@@ -54,11 +55,22 @@ def run_host(p, h, pinned=True, pad=3):
 @pytest.mark.parametrize("transA,transB", [(0, 0), (0, 1), (1, 0), (1, 1)])
 @pytest.mark.parametrize("out", ["f32", "bf16"])
 def test_layouts_chunked_and_blend(h, transA, transB, out):
-    """M = 1100: four-way chunks of 512 rows (the last 76) when A is not transposed."""
+    """M = 1100: three row chunks of 512 rows (the last 76)."""
     p = inputs.make_problem("host_%d%d" % (transA, transB), 1100, 300, 200, transA, transB, "bf16", out,
                             ("normal", 0, 1), ("normal", 0, 1), alpha=0.5, beta=-0.25, seed=transA + 2 * transB)
     R, Mag = oracle_full(p)
     assert_close(run_host(p, h), R, Mag, out == "f32", p.name)
+
+
+@pytest.mark.parametrize("transA,transB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("beta", [0.0, 0.5])
+def test_blocks_of_c(h, transA, transB, beta):
+    """M, N >= 1024: C in 3 x 3 blocks of 512 (the last 76) computed as A's row
+    chunks and B's column chunks arrive, every layout, with and without the blend."""
+    p = inputs.make_problem("host_2d_%d%d" % (transA, transB), 1100, 1100, 200, transA, transB, "bf16", "f32",
+                            ("normal", 0, 1), ("normal", 0, 1), alpha=0.75, beta=beta, seed=30 + transA + 2 * transB)
+    R, Mag = oracle_full(p)
+    assert_close(run_host(p, h), R, Mag, True, p.name)
 
 
 @pytest.mark.parametrize("pinned", [True, False])
