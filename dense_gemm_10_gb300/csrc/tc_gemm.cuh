@@ -70,12 +70,13 @@ struct TcConfig {
   static constexpr int kStagingBytes = kEpiWarps * 2 * 32 * 128;
   static constexpr int kCtrlBytes = 256;
   static constexpr int kRingMax = 232448 - 1024 - kStagingBytes - 1024;  // 227 KB less the rest
-  // DQ: the ring holds only P's converted 16-bit tiles (three stages); Q's
-  // tile, P's block-scaled codes and a 16-byte box of their scale codes per
-  // row arrive in a deeper code ring filling the rest (its stage size and
-  // count depend on the code format: TcArgs::code_stage_bytes, code_stages),
-  // which the MMA reads Q from in place
-  static constexpr int kStages = DQ ? 3 : kRingMax / kStageBytes > 8 ? 8 : kRingMax / kStageBytes;
+  // DQ: the ring holds only P's converted 16-bit tiles (five stages: the
+  // NVFP4 LM head took 63.7 us with three, 61.6 us with five); Q's tile, P's
+  // block-scaled codes and a 16-byte box of their scale codes per row arrive
+  // in a code ring filling the rest (its stage size and count depend on the
+  // code format: TcArgs::code_stage_bytes, code_stages), which the MMA reads
+  // Q from in place
+  static constexpr int kStages = DQ ? 5 : kRingMax / kStageBytes > 8 ? 8 : kRingMax / kStageBytes;
   static constexpr int kRingBytes = DQ ? kStages * kABytes : kStages * kStageBytes;
   static constexpr int kCodeRingBytes = DQ ? kRingMax - kRingBytes : 0;
   static_assert(kCodeRingBytes % 1024 == 0, "code stages start on 1024-byte boundaries");
