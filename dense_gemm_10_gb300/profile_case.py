@@ -1,12 +1,14 @@
 """Run one benchmark workload a few times through the library, for a profiler.
 
-    python -m dense_gemm_10_gb300.profile_case CASE [--launches N]
+    python -m dense_gemm_10_gb300.profile_case CASE [--launches N] [--raster-group G]
 
 Every case is one of the benchmark's workloads (seeded synthetic inputs of the
 benchmark's shapes), called N times back to back on one stream through the
 public entry points; the handle's status is checked at the end and the
-process exits non-zero on any error.  Under a profiler, skip the first calls
-(their set-up and cold caches) and capture one or two of the later ones:
+process exits non-zero on any error.  --raster-group sets the number of tile
+rows per raster group of the persistent schedule (0: the library's choice).
+Under a profiler, skip the first calls (their set-up and cold caches) and
+capture one or two of the later ones:
 
     ncu --set full --clock-control none -k regex:tc_gemm_kernel -s 2 -c 1 \\
         -o prof python -m dense_gemm_10_gb300.profile_case square_4096_nt_f32
@@ -36,9 +38,11 @@ CASES = {
 BLOCK_CASES = ("lm_head_64x32000x4096_nvfp4",)
 
 
-def run(case, launches):
+def run(case, launches, raster_group=0):
     h = G.Handle(0)
     try:
+        if raster_group:
+            h.set_option(G.OPT_RASTER_GROUP, raster_group)
         if case in BLOCK_CASES:
             p = inputs.make_block_scaled_problem(case, 64, 32000, 4096, "nvfp4", "bf16", seed=0, alpha=1.0 / 64)
             A, SA, B, SB = p.A.cuda(), p.SFA.cuda(), p.B.cuda(), p.SFB.cuda()
@@ -71,8 +75,11 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("case", choices=sorted(CASES) + list(BLOCK_CASES))
     ap.add_argument("--launches", type=int, default=4)
+    ap.add_argument("--raster-group", type=int, default=0)
     a = ap.parse_args(argv)
-    run(a.case, a.launches)
+    if a.raster_group < 0:
+        ap.error("--raster-group must be >= 0")
+    run(a.case, a.launches, a.raster_group)
     return 0
 
 
