@@ -1,12 +1,14 @@
 """Run one benchmark workload a few times through the library, for a profiler.
 
-    python -m dense_gemm_10_gb300.profile_case CASE [--launches N] [--raster-group G]
+    python -m dense_gemm_10_gb300.profile_case CASE [--launches N] [--raster-group G] [--option OPT_X=V ...]
 
 Every case is one of the benchmark's workloads (seeded synthetic inputs of the
 benchmark's shapes), called N times back to back on one stream through the
 public entry points; the handle's status is checked at the end and the
 process exits non-zero on any error.  --raster-group sets the number of tile
-rows per raster group of the persistent schedule (0: the library's choice).
+rows per raster group of the persistent schedule (0: the library's choice);
+--option sets any other handle option by its binding name (OPT_STREAM_K=1:
+no stream-K).
 Under a profiler, skip the first calls (their set-up and cold caches) and
 capture one or two of the later ones:
 
@@ -38,11 +40,13 @@ CASES = {
 BLOCK_CASES = ("lm_head_64x32000x4096_nvfp4",)
 
 
-def run(case, launches, raster_group=0):
+def run(case, launches, raster_group=0, options=()):
     h = G.Handle(0)
     try:
         if raster_group:
             h.set_option(G.OPT_RASTER_GROUP, raster_group)
+        for opt, value in options:
+            h.set_option(opt, value)
         if case in BLOCK_CASES:
             p = inputs.make_block_scaled_problem(case, 64, 32000, 4096, "nvfp4", "bf16", seed=0, alpha=1.0 / 64)
             A, SA, B, SB = p.A.cuda(), p.SFA.cuda(), p.B.cuda(), p.SFB.cuda()
@@ -76,10 +80,17 @@ def main(argv=None):
     ap.add_argument("case", choices=sorted(CASES) + list(BLOCK_CASES))
     ap.add_argument("--launches", type=int, default=4)
     ap.add_argument("--raster-group", type=int, default=0)
+    ap.add_argument("--option", action="append", default=[], metavar="OPT_NAME=V")
     a = ap.parse_args(argv)
     if a.raster_group < 0:
         ap.error("--raster-group must be >= 0")
-    run(a.case, a.launches, a.raster_group)
+    options = []
+    for item in a.option:
+        name, _, value = item.partition("=")
+        if not name.startswith("OPT_") or not hasattr(G, name) or not value.lstrip("-").isdigit():
+            ap.error("--option wants OPT_NAME=INTEGER, got %r" % item)
+        options.append((getattr(G, name), int(value)))
+    run(a.case, a.launches, a.raster_group, options)
     return 0
 
 
