@@ -438,3 +438,18 @@ def test_probe_tma_tile_rejects_bad_arguments():
     assert L.gemm_probe_tma_tile(fake, 0x1000, 60, 60, 8, 0x2000, None) == G.ERR_INVALID_ARG    # 120-byte rows
     assert L.gemm_probe_tma_tile(fake, 0x1000, 32, 64, 8, 0x2000, None) == G.ERR_INVALID_ARG    # ld < cols
     assert L.gemm_probe_tma_tile(fake, 0x1000, 64, 64, 8, None, None) == G.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("argv", [
+    ["square_4096_nt_f32", "--option", "OPT_BOGUS=1"],       # no such option
+    ["square_4096_nt_f32", "--option", "OPT_STREAM_K=x"],    # not an integer
+    ["square_4096_nt_f32", "--option", "STREAM_K=1"],        # not a binding option name
+    ["square_4096_nt_f32", "--raster-group", "-1"],
+    ["no_such_case"],
+])
+def test_profile_case_rejects_bad_arguments(argv, capsys):
+    """The profiling entry point checks its arguments before any GPU call."""
+    from dense_gemm_10_gb300 import profile_case
+    with pytest.raises(SystemExit) as e:
+        profile_case.main(argv)
+    assert e.value.code == 2
